@@ -1,0 +1,617 @@
+/*
+ * gq_oracle.c -- plain, slow, obviously-correct CPU reference for the
+ * block-quantized matrix-vector / matrix-matrix product.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file: only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark do.  It shares no code, header, table or constant with
+ * the CUDA library; its only inputs are the seeded arrays produced by the
+ * synthetic-input module.
+ *
+ * Compile: gcc -O2 -ffp-contract=off -fno-fast-math -fopenmp -shared -fPIC.
+ * Every floating-point step below is a single IEEE fp32 (or fp64) operation
+ * written out in source order; there is no FMA contraction and no division
+ * replaced by a reciprocal multiply.
+ *
+ * Sources followed (page title, then section):
+ *   [P2] "llama.cpp 推理引擎" (runguoli.com/llm-libs/14-llama-cpp)
+ *        §5.1 symmetric quantization, §5.2 asymmetric quantization,
+ *        §5.3 Q4_0, §5.4 Q8_0, §5.5 K-quant (Q4_K super-block and its
+ *        two-level dequantization), §6.4 the Q4_0 vec_dot pseudocode
+ *        (nibble order: low nibble of byte j is element 2j, high nibble is
+ *        element 2j+1).
+ *   [P4] "llama.cpp：一个人、一个周末、一个改变 AI 推理格局的 C++ 文件"
+ *        (tech-blog-56a.pages.dev), 第二层：量化引擎 -- the block
+ *        quantization figure and the 256 = 8 x 32 K-quant hierarchy.
+ *   The library's format definition fixes what the pages leave open or
+ *   print inconsistently: Q8_0 carries an fp16 scale (34 B, where [P2] §5.4
+ *   prints fp32), Q4_K carries 6-bit sub-block scales and mins (144 B, where
+ *   [P2] §5.5 prints 4-bit fields) and dequantizes as d*sc*q - dmin*m, codes
+ *   are rounded half away from zero.  Q8_K (the 256-element activation
+ *   block) is not described by any page; its layout is this library's own.
+ *
+ * Readings taken where the pages are silent (each also listed in the design
+ * notes of the repository):
+ *   - Q4_0 scale d = max|x| / 7 ([P2] §5.1 worked example); codes c = q + 8
+ *     with q = round(x/d) clamped to [-8, 7].
+ *   - fp16 scales of Q8_0 / Q4_0 are rounded to nearest-even; the fp16 d and
+ *     dmin of Q4_K are rounded toward +infinity so that the 6-bit ceilings
+ *     below always cover the sub-block's range.
+ *   - Q4_K: non-iterative min/max fit (the asymmetric formula of [P2] §5.2
+ *     with the minimum clamped to <= 0 because the min term is subtracted).
+ *   - A zero scale yields zero codes (Q4_0 code 8).
+ *   - Non-finite inputs are rejected (return -2).
+ *
+ * parity pins: every function here is pinned by tests under tests/ that do
+ * not call back into this file for their expected values.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Type codes, in the order of the public type enumeration. */
+enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q8_K = 3 };
+
+/* ------------------------------------------------------------------ */
+/* Bit-level helpers                                                    */
+/* ------------------------------------------------------------------ */
+
+static uint32_t f32_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float bits_f32(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* fp16 -> fp32, exact (every fp16 value is an fp32 value). */
+float or_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    uint32_t e = (h >> 10) & 0x1fu;
+    uint32_t m = h & 0x3ffu;
+    if (e == 0x1f) /* inf / nan */
+        return bits_f32(sign | 0x7f800000u | (m << 13));
+    if (e == 0) {
+        /* zero or subnormal: value = m * 2^-24, exact in fp32 */
+        float v = (float)m * bits_f32(0x33800000u); /* 2^-24 */
+        return sign ? -v : v;
+    }
+    return bits_f32(sign | ((e + 112u) << 23) | (m << 13));
+}
+
+/*
+ * fp32 -> fp16 with a selectable rounding rule.
+ *   up == 0 : round to nearest, ties to even (IEEE default)
+ *   up == 1 : round toward +infinity
+ * Works on the magnitude: the fp32 significand (with its hidden bit) is
+ * shifted right to the fp16 grid of the target exponent; the bits shifted out
+ * decide the rounding.
+ */
+static uint16_t f32_to_f16(float f, int up)
+{
+    uint32_t x = f32_bits(f);
+    uint32_t sign = (x >> 16) & 0x8000u;
+    uint32_t a = x & 0x7fffffffu;
+    int neg = sign != 0;
+
+    if (a > 0x7f800000u) /* nan: keep it a quiet nan */
+        return (uint16_t)(sign | 0x7e00u);
+    if (a == 0x7f800000u)
+        return (uint16_t)(sign | 0x7c00u);
+
+    int32_t exp = (int32_t)(a >> 23);           /* biased fp32 exponent */
+    uint32_t sig = (a & 0x7fffffu) | (exp ? 0x800000u : 0); /* 24-bit */
+    if (exp == 0) exp = 1;                      /* fp32 subnormal */
+
+    /* The fp16 grid unit at this magnitude: normal fp16 numbers with
+     * unbiased exponent E >= -14 keep 10 fraction bits, i.e. a unit of
+     * 2^(E-10); below 2^-14 the unit is fixed at 2^-24. */
+    int32_t e_unb = exp - 127;
+    int32_t unit_exp = (e_unb >= -14) ? e_unb - 10 : -24;
+    /* sig * 2^(exp-150) expressed in units of 2^unit_exp: shift right by
+     * (unit_exp - (exp - 150)). */
+    int32_t shift = unit_exp - (exp - 150);
+    uint64_t q, rem, half;
+    if (shift >= 40) {
+        q = 0; rem = sig; half = (uint64_t)1 << 39; /* rem < half always */
+    } else {
+        q = (uint64_t)sig >> shift;
+        rem = (uint64_t)sig & (((uint64_t)1 << shift) - 1);
+        half = (uint64_t)1 << (shift - 1);
+    }
+    /* shift is >= 13 for every finite fp32 input, so half is well defined */
+    int round_up;
+    if (up)
+        round_up = (!neg) && rem != 0; /* toward +inf: magnitudes of
+                                          positives grow, of negatives drop */
+    else
+        round_up = rem > half || (rem == half && (q & 1));
+    q += (uint64_t)round_up;
+
+    /* q counts units of 2^unit_exp; rebuild the fp16 encoding. */
+    uint32_t h;
+    if (unit_exp == -24) {
+        /* subnormal range: q < 2^10 is a subnormal, q == 2^10 is the
+         * smallest normal 2^-14 -- both encode as the plain value of q. */
+        h = (uint32_t)q;
+    } else {
+        /* normal: q in [2^10, 2^11]; q == 2^11 carries into the exponent */
+        int32_t E = e_unb;
+        if (q == 2048) { q = 1024; E += 1; }
+        if (E > 15) {
+            /* overflow: nearest rounds to inf, toward +inf keeps the
+             * largest finite negative */
+            h = (up && neg) ? 0x7bffu : 0x7c00u;
+        } else {
+            h = ((uint32_t)(E + 15) << 10) | ((uint32_t)q & 0x3ffu);
+        }
+    }
+    return (uint16_t)(sign | h);
+}
+
+uint16_t or_f16_rn(float f) { return f32_to_f16(f, 0); }
+uint16_t or_f16_ru(float f) { return f32_to_f16(f, 1); }
+
+void or_f16_rn_array(const float *x, uint16_t *h, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) h[i] = f32_to_f16(x[i], 0);
+}
+void or_f16_ru_array(const float *x, uint16_t *h, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) h[i] = f32_to_f16(x[i], 1);
+}
+
+static void put_u16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
+static uint16_t get_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static void put_f32(uint8_t *p, float f)
+{
+    uint32_t u = f32_bits(f);
+    p[0] = (uint8_t)u; p[1] = (uint8_t)(u >> 8); p[2] = (uint8_t)(u >> 16); p[3] = (uint8_t)(u >> 24);
+}
+static float get_f32(const uint8_t *p)
+{
+    return bits_f32((uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24));
+}
+
+/* round half away from zero: the code rounding rule of every format */
+static float rha(float v) { return roundf(v); }
+
+static float clampf(float v, float lo, float hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+/* ------------------------------------------------------------------ */
+/* Block geometry                                                       */
+/* ------------------------------------------------------------------ */
+
+int64_t or_block_elems(int type)
+{
+    switch (type) {
+    case OR_Q4_0: case OR_Q8_0: return 32;
+    case OR_Q4_K: case OR_Q8_K: return 256;
+    }
+    return -1;
+}
+
+/* Q4_0: fp16 d + 16 bytes of nibbles ([P2] §5.3: 144 bits).
+ * Q8_0: fp16 d + 32 int8.
+ * Q4_K: fp16 d, fp16 dmin, 12 bytes of 6-bit scales/mins, 128 bytes of
+ *       nibbles.
+ * Q8_K: fp32 d, 256 int8, eight int16 sub-block sums. */
+int64_t or_block_bytes(int type)
+{
+    switch (type) {
+    case OR_Q4_0: return 2 + 16;
+    case OR_Q8_0: return 2 + 32;
+    case OR_Q4_K: return 2 + 2 + 12 + 128;
+    case OR_Q8_K: return 4 + 256 + 2 * 8;
+    }
+    return -1;
+}
+
+static int all_finite(const float *x, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++)
+        if (!isfinite(x[i])) return 0;
+    return 1;
+}
+
+/* ------------------------------------------------------------------ */
+/* Encoders                                                             */
+/* ------------------------------------------------------------------ */
+
+/* Q8_0 ([P2] §5.1 with b = 8, §5.4): symmetric, scale = max|x| / 127. */
+static void quantize_q8_0_block(const float *x, uint8_t *blk)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    uint16_t dh = or_f16_rn(amax / 127.0f);
+    float d = or_f16_to_f32(dh);
+    put_u16(blk, dh);
+    for (int i = 0; i < 32; i++) {
+        float q = (d == 0.0f) ? 0.0f : clampf(rha(x[i] / d), -127.0f, 127.0f);
+        blk[2 + i] = (uint8_t)(int8_t)q;
+    }
+}
+
+/* Q4_0 ([P2] §5.1 with b = 4 -- scale = max|x| / 7 -- and §5.3; the code
+ * stored is q + 8, and byte j holds element 2j in its low nibble and 2j+1 in
+ * its high nibble as in the §6.4 pseudocode). */
+static void quantize_q4_0_block(const float *x, uint8_t *blk)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 32; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    uint16_t dh = or_f16_rn(amax / 7.0f);
+    float d = or_f16_to_f32(dh);
+    put_u16(blk, dh);
+    uint8_t c[32];
+    for (int i = 0; i < 32; i++) {
+        float q = (d == 0.0f) ? 0.0f : clampf(rha(x[i] / d), -8.0f, 7.0f);
+        c[i] = (uint8_t)((int)q + 8);
+    }
+    for (int j = 0; j < 16; j++)
+        blk[2 + j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
+}
+
+/* Pack sixteen 6-bit fields LSB-first into 12 bytes (a 96-bit little-endian
+ * integer): fields 0..7 are the sub-block scales, 8..15 the mins. */
+static void pack6(const uint8_t f[16], uint8_t out[12])
+{
+    memset(out, 0, 12);
+    for (int k = 0; k < 16; k++) {
+        for (int b = 0; b < 6; b++) {
+            int bit = 6 * k + b;
+            if ((f[k] >> b) & 1) out[bit / 8] |= (uint8_t)(1u << (bit % 8));
+        }
+    }
+}
+static void unpack6(const uint8_t in[12], uint8_t f[16])
+{
+    for (int k = 0; k < 16; k++) {
+        uint8_t v = 0;
+        for (int b = 0; b < 6; b++) {
+            int bit = 6 * k + b;
+            v |= (uint8_t)(((in[bit / 8] >> (bit % 8)) & 1) << b);
+        }
+        f[k] = v;
+    }
+}
+
+/* Q4_K ([P2] §5.2 asymmetric fit per 32-element sub-block, §5.5 two-level
+ * scales; [P4] 256 = 8 x 32 super-block).  For sub-block j:
+ *   lo_j = min(0, min x), hi_j = max x
+ *   dmin = f16_ru(max_j(-lo_j) / 63),  m_j = min(63, ceil(-lo_j / dmin))
+ *   base_j = -(dmin * m_j)                      (exact in fp32)
+ *   r_j = hi_j - base_j
+ *   d = f16_ru(max_j r_j / 945),  sc_j = min(63, ceil(r_j / (15 d)))
+ *   step_j = d * sc_j                           (exact in fp32)
+ *   q_i = clamp(round((x_i - base_j) / step_j), 0, 15)
+ * and the element is reconstructed as d*sc_j*q_i - dmin*m_j. */
+static void quantize_q4_k_block(const float *x, uint8_t *blk)
+{
+    float lo[8], hi[8];
+    for (int j = 0; j < 8; j++) {
+        float mn = x[32 * j], mx = x[32 * j];
+        for (int i = 1; i < 32; i++) {
+            float v = x[32 * j + i];
+            if (v < mn) mn = v;
+            if (v > mx) mx = v;
+        }
+        lo[j] = mn < 0.0f ? mn : 0.0f;
+        hi[j] = mx;
+    }
+    float neg_lo_max = 0.0f;
+    for (int j = 0; j < 8; j++)
+        if (-lo[j] > neg_lo_max) neg_lo_max = -lo[j];
+    uint16_t dminh = or_f16_ru(neg_lo_max / 63.0f);
+    float dmin = or_f16_to_f32(dminh);
+
+    uint8_t m[8], sc[8];
+    float base[8], r[8];
+    float r_max = 0.0f;
+    for (int j = 0; j < 8; j++) {
+        float mj = (dmin == 0.0f) ? 0.0f : ceilf(-lo[j] / dmin);
+        if (mj > 63.0f) mj = 63.0f;
+        m[j] = (uint8_t)mj;
+        base[j] = -(dmin * mj);
+        r[j] = hi[j] - base[j];
+        if (r[j] > r_max) r_max = r[j];
+    }
+    uint16_t dh = or_f16_ru(r_max / 945.0f);
+    float d = or_f16_to_f32(dh);
+    for (int j = 0; j < 8; j++) {
+        float s = (d == 0.0f) ? 0.0f : ceilf(r[j] / (15.0f * d));
+        if (s > 63.0f) s = 63.0f;
+        sc[j] = (uint8_t)s;
+    }
+
+    put_u16(blk + 0, dh);
+    put_u16(blk + 2, dminh);
+    uint8_t fields[16];
+    for (int j = 0; j < 8; j++) { fields[j] = sc[j]; fields[8 + j] = m[j]; }
+    pack6(fields, blk + 4);
+
+    uint8_t q[256];
+    for (int j = 0; j < 8; j++) {
+        float step = d * (float)sc[j];
+        for (int i = 0; i < 32; i++) {
+            float v = (step == 0.0f) ? 0.0f
+                      : clampf(rha((x[32 * j + i] - base[j]) / step), 0.0f, 15.0f);
+            q[32 * j + i] = (uint8_t)v;
+        }
+    }
+    for (int l = 0; l < 128; l++)
+        blk[16 + l] = (uint8_t)(q[2 * l] | (q[2 * l + 1] << 4));
+}
+
+/* Q8_K: the 256-element activation block.  Same symmetric rule as Q8_0 but
+ * the scale stays fp32, and the eight 32-element sums of the codes are
+ * stored so that the Q4_K min term needs no second pass over the codes. */
+static void quantize_q8_k_block(const float *x, uint8_t *blk)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 256; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float d = amax / 127.0f;
+    put_f32(blk, d);
+    int8_t q[256];
+    for (int i = 0; i < 256; i++) {
+        float v = (d == 0.0f) ? 0.0f : clampf(rha(x[i] / d), -127.0f, 127.0f);
+        q[i] = (int8_t)v;
+        blk[4 + i] = (uint8_t)q[i];
+    }
+    for (int j = 0; j < 8; j++) {
+        int s = 0;
+        for (int i = 0; i < 32; i++) s += q[32 * j + i];
+        put_u16(blk + 260 + 2 * j, (uint16_t)(int16_t)s);
+    }
+}
+
+int or_quantize(int type, const float *x, uint8_t *dst, int64_t n)
+{
+    int64_t be = or_block_elems(type), bb = or_block_bytes(type);
+    if (be <= 0 || n < 0 || n % be) return -1;
+    if (!all_finite(x, n)) return -2;
+    for (int64_t b = 0; b < n / be; b++) {
+        const float *xb = x + b * be;
+        uint8_t *ob = dst + b * bb;
+        switch (type) {
+        case OR_Q4_0: quantize_q4_0_block(xb, ob); break;
+        case OR_Q8_0: quantize_q8_0_block(xb, ob); break;
+        case OR_Q4_K: quantize_q4_k_block(xb, ob); break;
+        case OR_Q8_K: quantize_q8_k_block(xb, ob); break;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Decoders                                                             */
+/* ------------------------------------------------------------------ */
+
+/* Per-element reconstruction of one block, exact in double:
+ *   Q4_0: d * (c - 8)      Q8_0, Q8_K: d * q      Q4_K: d*sc_j*q - dmin*m_j
+ * Every product of an fp16 (or fp32) scale with these small integers, and
+ * the Q4_K difference, fits in the 53-bit double significand. */
+static void decode_block_f64(int type, const uint8_t *blk, double *out)
+{
+    switch (type) {
+    case OR_Q4_0: {
+        double d = or_f16_to_f32(get_u16(blk));
+        for (int j = 0; j < 16; j++) {
+            out[2 * j] = d * (double)((blk[2 + j] & 0x0f) - 8);
+            out[2 * j + 1] = d * (double)((blk[2 + j] >> 4) - 8);
+        }
+        break;
+    }
+    case OR_Q8_0: {
+        double d = or_f16_to_f32(get_u16(blk));
+        for (int i = 0; i < 32; i++) out[i] = d * (double)(int8_t)blk[2 + i];
+        break;
+    }
+    case OR_Q4_K: {
+        double d = or_f16_to_f32(get_u16(blk + 0));
+        double dmin = or_f16_to_f32(get_u16(blk + 2));
+        uint8_t f[16];
+        unpack6(blk + 4, f);
+        for (int e = 0; e < 256; e++) {
+            int j = e / 32;
+            int byte = blk[16 + e / 2];
+            int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);
+            out[e] = d * (double)f[j] * (double)q - dmin * (double)f[8 + j];
+        }
+        break;
+    }
+    case OR_Q8_K: {
+        double d = get_f32(blk);
+        for (int i = 0; i < 256; i++) out[i] = d * (double)(int8_t)blk[4 + i];
+        break;
+    }
+    }
+}
+
+/* The fp32 reconstruction is the exact value rounded once to fp32 (for
+ * Q4_0, Q8_0 and Q8_K the exact value is already an fp32 number). */
+static void decode_block(int type, const uint8_t *blk, float *out)
+{
+    double tmp[256];
+    decode_block_f64(type, blk, tmp);
+    for (int i = 0; i < or_block_elems(type); i++) out[i] = (float)tmp[i];
+}
+
+int or_dequantize_f64(int type, const uint8_t *src, double *dst, int64_t n)
+{
+    int64_t be = or_block_elems(type), bb = or_block_bytes(type);
+    if (be <= 0 || n < 0 || n % be) return -1;
+    for (int64_t b = 0; b < n / be; b++) decode_block_f64(type, src + b * bb, dst + b * be);
+    return 0;
+}
+
+int or_dequantize(int type, const uint8_t *src, float *dst, int64_t n)
+{
+    int64_t be = or_block_elems(type), bb = or_block_bytes(type);
+    if (be <= 0 || n < 0 || n % be) return -1;
+    for (int64_t b = 0; b < n / be; b++) decode_block(type, src + b * bb, dst + b * be);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* The product                                                          */
+/* ------------------------------------------------------------------ */
+
+static int pairing_ok(int wtype, int *atype)
+{
+    switch (wtype) {
+    case OR_Q4_0: case OR_Q8_0: *atype = OR_Q8_0; return 1;
+    case OR_Q4_K: *atype = OR_Q8_K; return 1;
+    }
+    return 0;
+}
+
+/* Integer dot of one weight block against one activation block.
+ *   Q4_0 x Q8_0: s = sum_i (c_i - 8) * a_i          ([P2] §6.4)
+ *   Q8_0 x Q8_0: s = sum_i w_i * a_i
+ *   Q4_K x Q8_K: s_j = sum_{i in j} q_i * a_i per sub-block,
+ *                S1 = sum_j sc_j * s_j,  S2 = sum_j m_j * t_j
+ *                with t_j the activation sub-block sum (stored bsums).
+ * out[0] (and out[1] for Q4_K) receive the sums; returns the number written. */
+static int block_int_dot(int wtype, const uint8_t *w, const uint8_t *a, int32_t *out)
+{
+    if (wtype == OR_Q4_0) {
+        int32_t s = 0;
+        for (int j = 0; j < 16; j++) {
+            int v0 = (w[2 + j] & 0x0f) - 8;
+            int v1 = (w[2 + j] >> 4) - 8;
+            s += v0 * (int8_t)a[2 + 2 * j] + v1 * (int8_t)a[2 + 2 * j + 1];
+        }
+        out[0] = s;
+        return 1;
+    }
+    if (wtype == OR_Q8_0) {
+        int32_t s = 0;
+        for (int i = 0; i < 32; i++) s += (int8_t)w[2 + i] * (int8_t)a[2 + i];
+        out[0] = s;
+        return 1;
+    }
+    /* Q4_K x Q8_K */
+    uint8_t f[16];
+    unpack6(w + 4, f);
+    int32_t S1 = 0, S2 = 0;
+    for (int j = 0; j < 8; j++) {
+        int32_t s = 0;
+        for (int i = 0; i < 32; i++) {
+            int e = 32 * j + i;
+            int byte = w[16 + e / 2];
+            int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);
+            s += q * (int8_t)a[4 + e];
+        }
+        int16_t t = (int16_t)get_u16(a + 260 + 2 * j);
+        S1 += (int32_t)f[j] * s;
+        S2 += (int32_t)f[8 + j] * (int32_t)t;
+    }
+    out[0] = S1;
+    out[1] = S2;
+    return 2;
+}
+
+/* Per-block integer sums of the whole product.
+ * Layout: out[b][r][k][c] with k over the weight blocks of a row and
+ * c = 1 (Q4_0, Q8_0) or 2 (Q4_K: S1, S2). */
+int or_block_sums(int wtype, const uint8_t *W, const uint8_t *xq, int64_t rows,
+                  int64_t cols, int64_t batch, int32_t *out)
+{
+    int atype;
+    if (!pairing_ok(wtype, &atype)) return -1;
+    int64_t be = or_block_elems(wtype);
+    if (rows < 0 || batch < 0 || cols < 0 || cols % be) return -1;
+    int64_t nb = cols / be, wbb = or_block_bytes(wtype), abb = or_block_bytes(atype);
+    int c = (wtype == OR_Q4_K) ? 2 : 1;
+    for (int64_t b = 0; b < batch; b++)
+        for (int64_t r = 0; r < rows; r++)
+            for (int64_t k = 0; k < nb; k++)
+                block_int_dot(wtype, W + (r * nb + k) * wbb, xq + (b * nb + k) * abb,
+                              out + ((b * rows + r) * nb + k) * c);
+    return 0;
+}
+
+/* Scale terms of one block pair in double:
+ *   Q4_0 / Q8_0: d_w * d_x * s
+ *   Q4_K:        d_x * d * S1   and   -(d_x * dmin * S2)
+ * y accumulates the terms, T their absolute values. */
+static void block_terms(int wtype, const uint8_t *w, const uint8_t *a, double *y, double *T)
+{
+    int32_t s[2];
+    block_int_dot(wtype, w, a, s);
+    if (wtype == OR_Q4_K) {
+        double dx = get_f32(a);
+        double d = or_f16_to_f32(get_u16(w + 0));
+        double dmin = or_f16_to_f32(get_u16(w + 2));
+        double t1 = dx * d * (double)s[0];
+        double t2 = -(dx * dmin * (double)s[1]);
+        *y += t1 + t2;
+        *T += fabs(t1) + fabs(t2);
+    } else {
+        double dw = or_f16_to_f32(get_u16(w));
+        double dx = or_f16_to_f32(get_u16(a));
+        double t = dw * dx * (double)s[0];
+        *y += t;
+        *T += fabs(t);
+    }
+}
+
+/* y[b][r] = sum over the row's blocks of the scaled block terms, in double;
+ * T[b][r] = sum of their magnitudes (the tolerance scale).  nthreads > 0
+ * splits the rows across that many OpenMP threads (0 = one thread). */
+int or_matmul_ref(int wtype, const uint8_t *W, const uint8_t *xq, int64_t rows,
+                  int64_t cols, int64_t batch, double *y, double *T, int nthreads)
+{
+    int atype;
+    if (!pairing_ok(wtype, &atype)) return -1;
+    int64_t be = or_block_elems(wtype);
+    if (rows < 0 || batch < 0 || cols < 0 || cols % be) return -1;
+    int64_t nb = cols / be, wbb = or_block_bytes(wtype), abb = or_block_bytes(atype);
+    int nt = nthreads > 0 ? nthreads : 1;
+    (void)nt;
+#pragma omp parallel for num_threads(nt) schedule(static)
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < batch; b++) {
+            double acc = 0.0, tol = 0.0;
+            for (int64_t k = 0; k < nb; k++)
+                block_terms(wtype, W + (r * nb + k) * wbb, xq + (b * nb + k) * abb, &acc, &tol);
+            y[b * rows + r] = acc;
+            if (T) T[b * rows + r] = tol;
+        }
+    }
+    return 0;
+}
+
+/* Whole-row quantization across OpenMP threads, for timing the CPU baseline
+ * on larger inputs (rows of `cols` elements each). */
+int or_quantize_rows_mt(int type, const float *x, uint8_t *dst, int64_t rows, int64_t cols,
+                        int nthreads)
+{
+    int64_t be = or_block_elems(type), bb = or_block_bytes(type);
+    if (be <= 0 || rows < 0 || cols % be) return -1;
+    int nt = nthreads > 0 ? nthreads : 1;
+    int err = 0;
+    (void)nt;
+#pragma omp parallel for num_threads(nt) schedule(static) reduction(| : err)
+    for (int64_t r = 0; r < rows; r++)
+        err |= or_quantize(type, x + r * cols, dst + r * (cols / be) * bb, cols) != 0;
+    return err ? -1 : 0;
+}
+
+int or_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

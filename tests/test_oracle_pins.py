@@ -1,0 +1,388 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants,
+special cases that reduce to a library routine, and brute force on tiny inputs.
+
+None of the expected values here comes from the oracle itself or from the CUDA
+path: they are the pages' numbers (tests/golden, each with its citation),
+numpy's own fp16 conversion and float64/int64 matmul, or properties that hold
+by the definition of the formats.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+from block_quantized_gb300 import inputs
+from conftest import read_golden
+
+Q4_0, Q8_0, Q4_K, Q8_K = orc.Q4_0, orc.Q8_0, orc.Q4_K, orc.Q8_K
+
+
+def hexbytes(tokens):
+    return np.array([int(t, 16) for t in tokens], dtype=np.uint8)
+
+
+# --------------------------------------------------------------------------
+# Block sizes ("llama.cpp 推理引擎" §5.3: 144 bits per 32 weights = 4.5 bpw;
+# the format definition: 18 / 34 / 144 bytes; Q8_K 276 bytes by construction)
+# --------------------------------------------------------------------------
+
+def test_block_sizes():
+    assert [orc.block_elems(t) for t in (Q4_0, Q8_0, Q4_K, Q8_K)] == [32, 32, 256, 256]
+    assert [orc.block_bytes(t) for t in (Q4_0, Q8_0, Q4_K, Q8_K)] == [18, 34, 144, 276]
+    assert orc.block_bytes(Q4_0) * 8 / 32 == 4.5
+    assert orc.block_bytes(Q4_0) * 8 == 144
+    assert orc.block_bytes(Q4_K) * 8 / 256 == 4.5
+    for t in (Q4_0, Q8_0, Q4_K, Q8_K):
+        x = np.zeros(orc.block_elems(t) * 3, np.float32)
+        assert orc.quantize(t, x).shape == (3, orc.block_bytes(t))
+
+
+# --------------------------------------------------------------------------
+# Printed examples
+# --------------------------------------------------------------------------
+
+def test_q4_0_worked_example():
+    g = read_golden("q4_0_worked_example.txt")
+    x = np.zeros(32, np.float32)
+    x[:5] = np.array(g["x"], dtype=np.float32)
+    blk = orc.quantize(Q4_0, x)[0]
+    assert blk.tobytes() == hexbytes(g["bytes"]).tobytes()
+    # the scale printed is 0.5
+    assert blk[:2].view(np.float16)[0] == np.float16(0.5)
+    # codes: stored nibble minus 8, element 2j in the low nibble of byte j
+    nib = np.empty(32, np.int32)
+    nib[0::2] = blk[2:] & 0x0F
+    nib[1::2] = blk[2:] >> 4
+    assert list(nib[:5] - 8) == [int(v) for v in g["codes"]]
+    xh = orc.dequantize(Q4_0, blk, 32)
+    np.testing.assert_array_equal(xh[:5], np.array(g["dequant"], np.float32))
+    np.testing.assert_allclose(np.abs(x[:5] - xh[:5]), np.array(g["abs_err"], np.float32),
+                               atol=1e-6)
+    assert np.all(xh[5:] == 0)
+
+
+def test_rounding_illustration():
+    g = read_golden("rounding_illustration.txt")
+    x = np.zeros(256, np.float32)
+    x[:4] = np.array(g["x"], dtype=np.float32)
+    x[4] = np.float32(g["amax_pad"][0])
+    blk = orc.quantize(Q8_K, x)[0]
+    d = blk[:4].view(np.float32)[0]
+    assert abs(d - 0.08) < 1e-7
+    codes = blk[4:260].view(np.int8)
+    assert list(codes[:4]) == [int(v) for v in g["codes"]]
+    assert codes[4] == 127
+    xh = orc.dequantize(Q8_K, blk, 256)
+    np.testing.assert_allclose(xh[:4], np.array(g["dequant"], np.float32), atol=2e-7)
+
+
+def test_q8_0_ties_round_half_away():
+    g = read_golden("q8_0_ties.txt")
+    x = np.zeros(32, np.float32)
+    x[:5] = np.array(g["x"], dtype=np.float32)
+    blk = orc.quantize(Q8_0, x)[0]
+    assert blk.tobytes() == hexbytes(g["bytes"]).tobytes()
+    assert list(blk[2:7].view(np.int8)) == [int(v) for v in g["codes"]]
+    # the same ties through the fp32-scale block
+    x8 = np.zeros(256, np.float32)
+    x8[:5] = x[:5]
+    b8 = orc.quantize(Q8_K, x8)[0]
+    assert b8[:4].view(np.float32)[0] == np.float32(0.5)
+    assert list(b8[4:9].view(np.int8)) == [127, 3, -3, 1, -1]
+
+
+def test_q4_k_handmade_block():
+    g = read_golden("q4_k_handmade.txt")
+    k0 = np.array(g["sub0_k"], np.int64)
+    k1 = np.array(g["sub1_k"], np.int64)
+    k2 = np.array(g["sub2_k"], np.int64)
+    x = np.zeros(256, np.float32)
+    x[0:32] = (63 * k0 - 252) / 256.0
+    x[32:64] = 5 * k1 / 256.0
+    x[64:96] = -0.5 + k2 / 128.0
+    blk = orc.quantize(Q4_K, x)[0]
+    expect = np.concatenate([hexbytes(g["header"]), hexbytes(g["scales"]), hexbytes(g["qs0"]),
+                             hexbytes(g["qs1"]), hexbytes(g["qs2"]), np.zeros(80, np.uint8)])
+    assert blk.tobytes() == expect.tobytes()
+    # every element lies on its grid, so the reconstruction is exact
+    np.testing.assert_array_equal(orc.dequantize(Q4_K, blk, 256), x)
+
+
+# --------------------------------------------------------------------------
+# fp16 converters: numpy's float16 cast is IEEE round-to-nearest-even
+# --------------------------------------------------------------------------
+
+def _f16_sweep():
+    """fp32 inputs for the fp16 converters: every positive fp32 whose exponent
+    lies in the window where fp16 rounding is non-trivial (2^-26 <= x < 2^16,
+    all 2^23 mantissas of each of those 42 binades), plus seeded samples of
+    the negatives, of the underflow region (incl. fp32 subnormals) and of the
+    overflow region."""
+    n = 1 << 23
+    for e in range(101, 143):
+        u = np.arange(e << 23, (e << 23) + n, dtype=np.uint32)
+        yield u.view(np.float32)
+    g = np.random.Generator(np.random.PCG64(1234))
+    yield (g.integers(0, 1 << 32, size=1 << 22, dtype=np.uint64).astype(np.uint32)
+           | np.uint32(0x80000000)).view(np.float32)
+    yield g.integers(0, 101 << 23, size=1 << 20, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    yield g.integers(143 << 23, 0x7F800001, size=1 << 20, dtype=np.uint64).astype(np.uint32).view(np.float32)
+
+
+def test_f16_rn_sweep_vs_numpy():
+    for x in _f16_sweep():
+        got = orc.f16_rn(x)
+        ref = x.astype(np.float16).view(np.uint16)
+        nan = np.isnan(x)
+        assert np.array_equal(got[~nan], ref[~nan])
+        assert np.all((got[nan] & 0x7C00) == 0x7C00) and np.all((got[nan] & 0x3FF) != 0)
+
+
+def test_f16_rn_special_values():
+    x = np.array([0.0, -0.0, 1.0, 65504.0, 65519.99, 65520.0, 2.0 ** -24, 2.0 ** -25,
+                  2.0 ** -25 * 1.0000001, 2.0 ** -14, 1e-30, -np.inf, 3.5 / 7], np.float32)
+    np.testing.assert_array_equal(orc.f16_rn(x), x.astype(np.float16).view(np.uint16))
+
+
+def test_f16_ru_sweep_properties():
+    """Round toward +inf: the result is >= v, and the next fp16 value below the
+    result is < v (so it is the least fp16 value >= v)."""
+    for x in _f16_sweep():
+        x = x[np.isfinite(x)]
+        h = orc.f16_ru(x)
+        r = h.view(np.float16).astype(np.float32)
+        assert np.all((r >= x) | (np.isinf(r) & (r > 0)))
+        pos = (h & 0x8000) == 0
+        pred = np.where(pos & (h != 0), h - 1, np.where(pos, 0x8001, h + 1)).astype(np.uint16)
+        below = pred.view(np.float16).astype(np.float32)
+        assert np.all(below < x)
+
+
+def test_f16_ru_spot_values():
+    assert orc.f16_ru(np.array([1.0], np.float32))[0] == 0x3C00
+    assert orc.f16_ru(np.array([1.0000001], np.float32))[0] == 0x3C01
+    assert orc.f16_ru(np.array([-1.0000001], np.float32))[0] == 0xBC00
+    assert orc.f16_ru(np.array([1e-30], np.float32))[0] == 0x0001
+    assert orc.f16_ru(np.array([70000.0], np.float32))[0] == 0x7C00
+    assert orc.f16_ru(np.array([-70000.0], np.float32))[0] == 0xFBFF
+
+
+# --------------------------------------------------------------------------
+# Round-trip bounds (|x - x_hat| <= half the step) on the workload
+# distributions and the degenerate blocks
+# --------------------------------------------------------------------------
+
+def _blocks_zoo(be, seed=1):
+    g = inputs.rng(seed)
+    rows = [
+        inputs.normal(g, (64, 8 * be), 0.02),               # N(0, 0.02^2) weights
+        inputs.outlier_weights(g, 16, 8 * be, frac=0.01),   # row spread + outliers
+        inputs.normal(g, (16, 8 * be)),                     # N(0, 1) activations
+        np.abs(inputs.normal(g, (4, 8 * be))),              # all positive
+        -np.abs(inputs.normal(g, (4, 8 * be))),             # all negative
+        np.full((2, 8 * be), 0.37, np.float32),             # all equal
+        np.full((2, 8 * be), -2.5, np.float32),
+        np.zeros((2, 8 * be), np.float32),                  # all zero
+        inputs.normal(g, (4, 8 * be), 1e-6),                # tiny sigma: subnormal fp16 scales
+        inputs.normal(g, (4, 8 * be), 1e-9),
+    ]
+    x = np.concatenate([r.reshape(-1, be) for r in rows])
+    # a block with one huge outlier
+    x[3, 5] = 40.0
+    return np.ascontiguousarray(x.reshape(-1))
+
+
+@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q8_K])
+def test_roundtrip_symmetric(t):
+    be, bb = orc.block_elems(t), orc.block_bytes(t)
+    x = _blocks_zoo(be)
+    q = orc.quantize(t, x)
+    xh = orc.dequantize(t, q, x.size).reshape(-1, be)
+    xb = x.reshape(-1, be)
+    if t == Q8_K:
+        d = q[:, :4].copy().view(np.float32)[:, 0].astype(np.float64)
+    else:
+        d = q[:, :2].copy().view(np.float16)[:, 0].astype(np.float64)
+    x64 = xb.astype(np.float64)
+    err = np.abs(x64 - xh)
+    amax = np.abs(xb).max(axis=1).astype(np.float64)
+    # Within the code range the nearest code is at most d/2 away; a value
+    # beyond the extreme code (possible when the fp16 scale rounded down, or
+    # underflowed to 0 for a tiny block) is clipped, adding its excess.
+    top_pos = (7.0 if t == Q4_0 else 127.0) * d
+    top_neg = (8.0 if t == Q4_0 else 127.0) * d
+    top = np.where(x64 >= 0, top_pos[:, None], top_neg[:, None])
+    excess = np.maximum(0.0, np.abs(x64) - top)
+    assert np.all(err <= d[:, None] / 2 * (1 + 1e-6) + excess + 1e-7 * amax[:, None])
+    # with a normal fp16 scale the clipped excess is only the scale's rounding
+    normal = d >= 2.0 ** -14
+    assert np.all(excess[normal] <= amax[normal, None] * 2.0 ** -10)
+    # max|x| maps to the extreme code for the 8-bit formats
+    if t in (Q8_0, Q8_K):
+        off = 2 if t == Q8_0 else 4
+        codes = q[:, off:off + be].view(np.int8)
+        nz = d >= (2.0 ** -14 if t == Q8_0 else 1e-30)   # normal scales only
+        i = np.abs(xb).argmax(axis=1)
+        assert np.all(np.abs(codes[np.arange(len(i)), i][nz]) == 127)
+    if t == Q8_K:
+        codes = q[:, 4:260].view(np.int8).astype(np.int32)
+        bs = q[:, 260:276].copy().view(np.int16).astype(np.int32)
+        np.testing.assert_array_equal(bs, codes.reshape(-1, 8, 32).sum(axis=2))
+
+
+def _q4k_fields(q):
+    """Decode d, dmin and the 6-bit fields of Q4_K blocks straight from the bytes."""
+    d = q[:, 0:2].copy().view(np.float16)[:, 0].astype(np.float64)
+    dmin = q[:, 2:4].copy().view(np.float16)[:, 0].astype(np.float64)
+    v = np.zeros(len(q), dtype=object)
+    for i in range(12):
+        v = v + (q[:, 4 + i].astype(object) << (8 * i))
+    f = np.array([[(int(vv) >> (6 * k)) & 63 for k in range(16)] for vv in v], np.int64)
+    return d, dmin, f[:, :8], f[:, 8:]
+
+
+def test_roundtrip_q4_k():
+    x = _blocks_zoo(256)
+    q = orc.quantize(Q4_K, x)
+    xh = orc.dequantize(Q4_K, q, x.size).reshape(-1, 8, 32).astype(np.float64)
+    xb = x.reshape(-1, 8, 32).astype(np.float64)
+    d, dmin, sc, m = _q4k_fields(q)
+    step = d[:, None] * sc
+    err = np.abs(xb - xh)
+    scale = np.abs(xb).max(axis=(1, 2))
+    bound = step / 2 * (1 + 1e-6) + 1e-6 * scale[:, None] + 1e-30
+    assert np.all(err <= bound[:, :, None])
+    # the reconstruction is d*sc*q - dmin*m: recover q and check it is an integer in [0, 15]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        qq = (xh + (dmin[:, None] * m)[:, :, None]) / step[:, :, None]
+    ok = step > 0
+    assert np.all(np.abs(qq[ok] - np.round(qq[ok])) < 1e-3)
+    assert np.all((np.round(qq[ok]) >= 0) & (np.round(qq[ok]) <= 15))
+
+
+def test_nonfinite_rejected():
+    x = np.zeros(32, np.float32)
+    x[3] = np.nan
+    with pytest.raises(ValueError):
+        orc.quantize(Q8_0, x)
+
+
+# --------------------------------------------------------------------------
+# The product: brute force in float64 on tiny inputs, and exact integer cases
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
+@pytest.mark.parametrize("rows,cols,batch", [(1, 256, 1), (5, 512, 3), (7, 1024, 2)])
+def test_matmul_ref_vs_bruteforce(wtype, rows, cols, batch):
+    atype = orc.ACT_TYPE[wtype]
+    g = inputs.rng(100 + rows)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.01)
+    X = inputs.normal(g, (batch, cols))
+    Wq = orc.quantize(wtype, W)
+    Xq = orc.quantize(atype, X)
+    Wd = orc.dequantize_f64(wtype, Wq, W.size).reshape(rows, cols)
+    Xd = orc.dequantize_f64(atype, Xq, X.size).reshape(batch, cols)
+    # the fp32 reconstruction is the exact one rounded once
+    np.testing.assert_array_equal(orc.dequantize(wtype, Wq, W.size).reshape(rows, cols),
+                                  Wd.astype(np.float32))
+    # the brute-force double dot of dequantized values, by a naive loop ...
+    naive = np.zeros((batch, rows))
+    for b in range(batch):
+        for r in range(rows):
+            s = 0.0
+            for i in range(cols):
+                s += Wd[r, i] * Xd[b, i]
+            naive[b, r] = s
+    # ... and by numpy's float64 matmul
+    lib = Xd @ Wd.T
+    y, T = orc.matmul_ref(wtype, Wq, Xq, rows, cols, batch)
+    assert np.all(T > 0)
+    np.testing.assert_allclose(y, naive, rtol=0, atol=1e-12 * T.max())
+    np.testing.assert_allclose(y, lib, rtol=0, atol=1e-12 * T.max())
+
+
+def _q8_0_blocks_d1(codes):
+    """Q8_0 blocks with fp16 scale 1.0 (0x3C00) holding the given int8 codes."""
+    nb = codes.size // 32
+    q = np.zeros((nb, 34), np.uint8)
+    q[:, 0] = 0x00
+    q[:, 1] = 0x3C
+    q[:, 2:] = codes.reshape(nb, 32).astype(np.int8).view(np.uint8)
+    return q
+
+
+def test_integer_special_case_q8_0():
+    """With every scale 1, the product is a pure integer matvec: numpy int64."""
+    g = inputs.rng(7)
+    rows, cols, batch = 9, 512, 4
+    Wc = g.integers(-127, 128, size=(rows, cols))
+    Xc = g.integers(-127, 128, size=(batch, cols))
+    y, _ = orc.matmul_ref(Q8_0, _q8_0_blocks_d1(Wc), _q8_0_blocks_d1(Xc), rows, cols, batch)
+    np.testing.assert_array_equal(y, (Xc @ Wc.T).astype(np.float64))
+    s = orc.block_sums(Q8_0, _q8_0_blocks_d1(Wc), _q8_0_blocks_d1(Xc), rows, cols, batch)
+    ref = (Xc.reshape(batch, 1, cols // 32, 32) * Wc.reshape(1, rows, cols // 32, 32)).sum(-1)
+    np.testing.assert_array_equal(s, ref)
+
+
+def test_integer_special_case_q4_0():
+    """Q4_0 with scale 1: codes c in [0, 15] stand for c - 8."""
+    g = inputs.rng(8)
+    rows, cols, batch = 6, 256, 3
+    C = g.integers(0, 16, size=(rows, cols))
+    Xc = g.integers(-127, 128, size=(batch, cols))
+    nb = cols // 32
+    Wq = np.zeros((rows * nb, 18), np.uint8)
+    Wq[:, 1] = 0x3C
+    Cb = C.reshape(rows * nb, 32)
+    Wq[:, 2:] = (Cb[:, 0::2] | (Cb[:, 1::2] << 4)).astype(np.uint8)
+    y, _ = orc.matmul_ref(Q4_0, Wq, _q8_0_blocks_d1(Xc), rows, cols, batch)
+    np.testing.assert_array_equal(y, (Xc @ (C - 8).T).astype(np.float64))
+
+
+def test_integer_special_case_q4_k():
+    """Q4_K with d = dmin = 1 and a Q8_K scale of 1: y = sum sc*q*a - m*a exactly."""
+    g = inputs.rng(9)
+    rows, cols, batch = 4, 512, 2
+    nsb = cols // 256
+    Q = g.integers(0, 16, size=(rows, cols))
+    SC = g.integers(0, 64, size=(rows, nsb, 8))
+    M = g.integers(0, 64, size=(rows, nsb, 8))
+    A = g.integers(-127, 128, size=(batch, cols))
+    Wq = np.zeros((rows, nsb, 144), np.uint8)
+    Wq[:, :, 1] = 0x3C
+    Wq[:, :, 3] = 0x3C
+    for r in range(rows):
+        for s in range(nsb):
+            v = 0
+            for k in range(8):
+                v |= int(SC[r, s, k]) << (6 * k)
+                v |= int(M[r, s, k]) << (6 * (k + 8))
+            Wq[r, s, 4:16] = np.frombuffer(v.to_bytes(12, "little"), np.uint8)
+            qb = Q[r, 256 * s:256 * (s + 1)]
+            Wq[r, s, 16:] = (qb[0::2] | (qb[1::2] << 4)).astype(np.uint8)
+    Xq = np.zeros((batch, nsb, 276), np.uint8)
+    Xq[:, :, 0:4] = np.frombuffer(np.float32(1.0).tobytes(), np.uint8)
+    Ab = A.reshape(batch, nsb, 256)
+    Xq[:, :, 4:260] = Ab.astype(np.int8).view(np.uint8)
+    Xq[:, :, 260:276] = Ab.reshape(batch, nsb, 8, 32).sum(-1).astype(np.int16).view(np.uint8)
+    # dense reconstruction in integers: w = sc*q - m
+    Wint = (SC.repeat(32, axis=2).reshape(rows, cols) * Q - M.repeat(32, axis=2).reshape(rows, cols))
+    y, _ = orc.matmul_ref(Q4_K, Wq.reshape(rows, -1), Xq.reshape(batch, -1), rows, cols, batch)
+    np.testing.assert_array_equal(y, (A @ Wint.T).astype(np.float64))
+    s = orc.block_sums(Q4_K, Wq.reshape(rows, -1), Xq.reshape(batch, -1), rows, cols, batch)
+    S1 = np.einsum("rsk,brski->brs", SC, Q.reshape(1, rows, nsb, 8, 32) * Ab.reshape(batch, 1, nsb, 8, 32))
+    S2 = np.einsum("rsk,bsk->brs", M, Ab.reshape(batch, nsb, 8, 32).sum(-1))
+    np.testing.assert_array_equal(s[..., 0], S1)
+    np.testing.assert_array_equal(s[..., 1], S2)
+
+
+def test_tolerance_scale_is_sum_of_magnitudes():
+    """T is at least |y| (triangle inequality) and equals |y| when every term
+    has the same sign (all-positive weights and activations, Q8_0 x Q8_0)."""
+    g = inputs.rng(11)
+    W = np.abs(inputs.normal(g, (3, 256)))
+    X = np.abs(inputs.normal(g, (2, 256)))
+    y, T = orc.matmul_ref(Q8_0, orc.quantize(Q8_0, W), orc.quantize(Q8_0, X), 3, 256, 2)
+    np.testing.assert_allclose(T, np.abs(y), rtol=1e-15)
+    W2 = inputs.normal(g, (3, 256))
+    y2, T2 = orc.matmul_ref(Q8_0, orc.quantize(Q8_0, W2), orc.quantize(Q8_0, X), 3, 256, 2)
+    assert np.all(T2 >= np.abs(y2))
