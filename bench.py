@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the block-quantized GEMV/GEMM library on GB300.
+
+Headline (one JSON line on stdout, rank 0):
+  metric  Q4_K GEMV weight GB/s (and % of HBM peak); 7B-shape decode tok/s
+  step    one pass of the hot path over 64 distinct Q4_K 4096x4096 weight
+          matrices at batch 1 (outlier-weighted weights): per matrix, the
+          activation quantize (fp32 -> Q8_K) and the GEMV.  64 x 9.44 MB of
+          weights per step is larger than L2, so no step is served from L2.
+  value   weight bytes streamed per second over the timed steps (device
+          resident inputs; CUDA-event timing of a CUDA graph of the step).
+Also in the line: roofline of the GEMV kernel, the 7B-shape decode sweep
+(tok/s), the batch sweep on 14336x4096, the 512-column prefill GEMM, the
+end-to-end figure with host buffers, the CPU oracle baseline, and the SM
+clocks sampled during the timed region.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+GEMV_ROWS = GEMV_COLS = 4096
+COPIES = 64
+Q4K_ROW_BYTES = GEMV_COLS // 256 * 144
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="gq", choices=["gq", "reference"])
+    p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if
+    the kernel source has not changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+        src = os.path.join(ROOT, d["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        return d["bytes_per_launch"] if h == d["sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        # samples taken under load: clocks near their maximum or power well above idle
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args)
+        return
+    run_gpu(args, world, rank)
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_gemv_sample():
+    import oracle as orc
+    from block_quantized_gb300 import inputs
+    W, x = inputs.gemv_q4_k(0)
+    Wq = orc.quantize(orc.Q4_K, W)
+    return orc, Wq, x
+
+
+def run_cpu_baseline(seconds=10.0):
+    """The oracle, as it stands, on the host cores: act-quantize + GEMV of the
+    4096x4096 Q4_K matrix, repeated for about `seconds`."""
+    orc, Wq, x = oracle_gemv_sample()
+    nt = orc.max_threads()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        xq = orc.quantize(orc.Q8_K, x)
+        orc.matmul_ref(orc.Q4_K, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, nt)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": n * Wq.nbytes / dt / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
+            "sample": f"{n} x (Q8_K act-quant + Q4_K GEMV 4096x4096, batch 1) in {dt:.1f} s"}
+
+
+def run_reference(args):
+    orc, Wq, x = oracle_gemv_sample()
+    nt = orc.max_threads()
+
+    def step():
+        xq = orc.quantize(orc.Q8_K, x)
+        orc.matmul_ref(orc.Q4_K, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, nt)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = args.steps * Wq.nbytes / dt / 1e9
+    sample = "per step: Q8_K act-quant + Q4_K GEMV 4096x4096 batch 1 (one of the 64 matrices of a GPU step)"
+    print(json.dumps({
+        "impl": "reference", "metric": "Q4_K GEMV weight GB/s", "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "Q4_K x Q8_K GEMV 4096x4096 batch 1 (CPU oracle sample)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": nt, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------------- GPU
+
+def run_gpu(args, world, rank):
+    import numpy as np
+    import torch
+
+    from block_quantized_gb300 import gq, inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    gq.load(build_if_missing=True)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v: float) -> float:
+        if dist is None:
+            return v
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline workload: 64 distinct Q4_K 4096x4096 matrices per step
+    W, x0 = inputs.gemv_q4_k(0)
+    Wq1 = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
+    del W
+    Wall = Wq1.reshape(1, -1).repeat(COPIES, 1)          # [64, 4096 * 2304] distinct copies
+    g = inputs.rng(1)
+    X = torch.from_numpy(np.concatenate([x0[None], inputs.normal(g, (COPIES - 1, GEMV_COLS))])).to(dev)
+    XQ = torch.empty(COPIES, GEMV_COLS // 256 * 276, dtype=torch.uint8, device=dev)
+    Y = torch.empty(COPIES, GEMV_ROWS, dtype=torch.float32, device=dev)
+    w_bytes = GEMV_ROWS * Q4K_ROW_BYTES
+    s = torch.cuda.Stream(device=dev)
+
+    def step_body():
+        for i in range(COPIES):
+            gq.gq_quantize_rows_async(gq.Q8_K, X[i], XQ[i], GEMV_COLS)
+            gq.gq_matmul(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
+
+    def gemv_only():
+        for i in range(COPIES):
+            gq.gq_matmul(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
+
+    def capture(fn):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            fn()  # warm (module load, attribute cache) outside capture
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=s):
+                fn()
+        torch.cuda.synchronize()
+        return graph
+
+    def time_graph(graph, steps, warmup, clocks=None):
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                graph.replay()
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if clocks:
+                clocks.start()
+            e0.record(s)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(s)
+            torch.cuda.synchronize()
+            clk = clocks.stop() if clocks else None
+            barrier()
+        return max_over_ranks(e0.elapsed_time(e1) / 1e3), clk
+
+    step_graph = capture(step_body)
+    sampler = ClockSampler(local)
+    t_total, clk = time_graph(step_graph, args.steps, max(3, args.warmup), sampler)
+    ms_step = t_total / args.steps * 1e3
+    value = world * args.steps * COPIES * w_bytes / t_total / 1e9
+
+    # correctness sentinel on the timed buffers (no oracle here): finite outputs
+    if not torch.isfinite(Y).all():
+        raise RuntimeError("non-finite GEMV output")
+
+    # ---- roofline of the GEMV kernel: GEMV-only graph, per-launch duration
+    gemv_graph = capture(gemv_only)
+    k_steps = max(50, args.steps // 4)
+    t_g, _ = time_graph(gemv_graph, k_steps, 5)
+    per_launch = t_g / (k_steps * COPIES)
+    alg_bytes = w_bytes + GEMV_COLS // 256 * 276 + GEMV_ROWS * 4
+    achieved = alg_bytes / per_launch / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": kernel_traffic("gemv_q4_k_kernel"),
+                "kernel": "gemv_q4_k_kernel<1>", "peak_source": peak_src,
+                "launch_us": per_launch * 1e6, "alg_bytes_per_launch": alg_bytes}
+
+    # ---- end to end with host buffers: pinned H2D of each x, D2H of each y
+    Xh = X.cpu().pin_memory()
+    Yh = torch.empty(COPIES, GEMV_ROWS, dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(X)
+
+    def e2e_body():
+        for i in range(COPIES):
+            Xd[i].copy_(Xh[i], non_blocking=True)
+            gq.gq_quantize_rows_async(gq.Q8_K, Xd[i], XQ[i], GEMV_COLS)
+            gq.gq_matmul(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
+            Yh[i].copy_(Y[i], non_blocking=True)
+
+    e2e_graph = capture(e2e_body)
+    e2e_steps = max(20, args.steps // 4)
+    t_e2e, _ = time_graph(e2e_graph, e2e_steps, 3)
+    e2e = {"value": world * e2e_steps * COPIES * w_bytes / t_e2e / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": COPIES * GEMV_COLS * 4, "d2h_bytes_per_step": COPIES * GEMV_ROWS * 4,
+           "how": "CUDA graph of the public calls: pinned H2D x, gq_quantize_rows_async, gq_matmul, D2H y"}
+    del Wall, Xh, Yh
+
+    extras = {}
+    if not args.quick:
+        extras["decode"] = bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world)
+        extras["batch_sweep"] = bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph)
+        extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = run_cpu_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": "Q4_K GEMV weight GB/s (% of HBM peak); 7B-shape decode tok/s",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8xint4->int32,fp32",
+            "data": "synthetic",
+            "config": {"workload": "Q4_K x Q8_K GEMV 4096x4096 batch 1, row-std spread + 0.1% "
+                                   "outliers; step = 64 distinct weight matrices, each with its "
+                                   "activation quantize",
+                       "rows": GEMV_ROWS, "cols": GEMV_COLS, "batch": 1,
+                       "matrices_per_step": COPIES, "weight_bytes_per_step": COPIES * w_bytes,
+                       "l2": "inputs larger than L2 (604 MB of weights per step)",
+                       "parallelism": f"replicas x{world}", "timing": "CUDA graph, CUDA events"},
+            "pct_of_hbm_peak": value / hbm_peak * 100.0,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * COPIES * 2,
+            "clocks": clk,
+        }
+        line.update(extras)
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
+    """7B-shape decode: 32 layers x (wq, wk, wv, wo, w1, w3, w2) Q4_K GEMVs
+    with their activation quantizes, then the Q8_0 output head; one token =
+    one pass.  Layer weights are 32 device copies of one generated layer."""
+    ws, _ = inputs.decode_weights(0)
+    layer = {}
+    for name, r, c in inputs.DECODE_LAYER:
+        layer[name] = gq.quantize(gq.Q4_K, torch.from_numpy(ws[name]).to(dev))
+    hname, hr, hc = inputs.DECODE_HEAD
+    head = gq.quantize(gq.Q8_0, torch.from_numpy(ws[hname]).to(dev))
+    del ws
+    L = inputs.DECODE_LAYERS
+    layers = [{k: v.clone() for k, v in layer.items()} for _ in range(L)]
+    del layer
+    g = inputs.rng(2)
+    xin = {k: torch.from_numpy(inputs.normal(g, (c,))).to(dev)
+           for k, c in (("attn", 4096), ("o", 4096), ("ffn", 4096), ("down", 11008), ("head", 4096))}
+    xq = {k: torch.empty(v.numel() // 256 * 276, dtype=torch.uint8, device=dev) for k, v in xin.items()}
+    xq["head"] = torch.empty(4096 // 32 * 34, dtype=torch.uint8, device=dev)
+    outs = {name: torch.empty(r, dtype=torch.float32, device=dev) for name, r, c in inputs.DECODE_LAYER}
+    yh = torch.empty(hr, dtype=torch.float32, device=dev)
+    launches = [0]
+
+    def token(count=False):
+        n = 0
+        for lw in layers:
+            gq.gq_quantize_rows_async(gq.Q8_K, xin["attn"], xq["attn"], 4096)
+            for nm in ("wq", "wk", "wv"):
+                gq.gq_matmul(gq.Q4_K, lw[nm], xq["attn"], outs[nm], 4096, 4096, 1)
+            gq.gq_quantize_rows_async(gq.Q8_K, xin["o"], xq["o"], 4096)
+            gq.gq_matmul(gq.Q4_K, lw["wo"], xq["o"], outs["wo"], 4096, 4096, 1)
+            gq.gq_quantize_rows_async(gq.Q8_K, xin["ffn"], xq["ffn"], 4096)
+            gq.gq_matmul(gq.Q4_K, lw["w1"], xq["ffn"], outs["w1"], 11008, 4096, 1)
+            gq.gq_matmul(gq.Q4_K, lw["w3"], xq["ffn"], outs["w3"], 11008, 4096, 1)
+            gq.gq_quantize_rows_async(gq.Q8_K, xin["down"], xq["down"], 11008)
+            gq.gq_matmul(gq.Q4_K, lw["w2"], xq["down"], outs["w2"], 4096, 11008, 1)
+            n += 11
+        gq.gq_quantize_rows_async(gq.Q8_0, xin["head"], xq["head"], 4096)
+        gq.gq_matmul(gq.Q8_0, head, xq["head"], yh, hr, hc, 1)
+        launches[0] = n + 2
+
+    graph = capture(token)
+    steps = 40
+    t, _ = time_graph(graph, steps, 3)
+    per_tok = t / steps
+    bytes_tok = sum(v.numel() for v in layers[0].values()) * L + head.numel()
+    del layers, head
+    torch.cuda.empty_cache()
+    return {"tok_s": world / per_tok, "ms_per_token": per_tok * 1e3,
+            "weight_bytes_per_token": bytes_tok, "weight_gbps": bytes_tok / per_tok / 1e9,
+            "launches_per_token": launches[0], "tokens_timed": steps,
+            "workload": "7B shapes: 32 x (4 x 4096x4096, 2 x 11008x4096, 4096x11008) Q4_K + "
+                        "32000x4096 Q8_0 head, batch 1, act-quant per input vector"}
+
+
+def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
+    """GEMV path on Q4_K 14336x4096 at batch 1..64 (weights rotated over 8
+    copies, 264 MB > L2)."""
+    rows, cols, copies = 14336, 4096, 8
+    W, X = inputs.gemm_q4_k(0, rows, cols, 64)
+    Wq = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
+    del W
+    Wc = Wq.reshape(1, -1).repeat(copies, 1)
+    Xq = gq.quantize(gq.Q8_K, torch.from_numpy(X).to(dev))
+    Y = torch.empty(64, rows, dtype=torch.float32, device=dev)
+    wbytes = Wq.numel()
+    out = {}
+    for b in (1, 2, 4, 8, 16, 32, 64):
+        res = {}
+        for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
+            def body():
+                for i in range(copies):
+                    gq.gq_matmul_path(gq.Q4_K, Wc[i], Xq, Y, rows, cols, b, path)
+            try:
+                graph = capture(body)
+            except gq.GQError:
+                continue
+            steps = 20
+            t, _ = time_graph(graph, steps, 3)
+            per = t / (steps * copies)
+            res[pname] = {"us": per * 1e6, "weight_gbps": wbytes / per / 1e9,
+                          "tops": 2.0 * rows * cols * b / per / 1e12}
+        out[str(b)] = res
+    del Wc, Wq, Xq, Y
+    torch.cuda.empty_cache()
+    return {"rows": rows, "cols": cols, "results": out}
+
+
+def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph):
+    """Q4_K 28672x8192 weights x 512 Q8_K columns (70B FFN shape)."""
+    rows, cols, batch = 28672, 8192, 512
+    W, X = inputs.gemm_q4_k(0, rows, cols, batch)
+    Wq = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
+    del W
+    Xq = gq.quantize(gq.Q8_K, torch.from_numpy(X).to(dev))
+    Y = torch.empty(batch, rows, dtype=torch.float32, device=dev)
+    res = {}
+    for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
+        def body():
+            gq.gq_matmul_path(gq.Q4_K, Wq, Xq, Y, rows, cols, batch, path)
+        try:
+            graph = capture(body)
+        except gq.GQError:
+            continue
+        steps = 5
+        t, _ = time_graph(graph, steps, 2)
+        per = t / steps
+        res[pname] = {"ms": per * 1e3, "tops": 2.0 * rows * cols * batch / per / 1e12}
+    del Wq, Xq, Y
+    torch.cuda.empty_cache()
+    return {"rows": rows, "cols": cols, "batch": batch, "results": res}
+
+
+if __name__ == "__main__":
+    main()

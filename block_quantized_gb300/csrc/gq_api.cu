@@ -1,0 +1,248 @@
+// gq_api.cu -- the C ABI declared in include/gq.h: argument validation,
+// per-device launch context, kernel-family dispatch and error reporting.
+// Nothing here allocates device memory ("llama.cpp：一个人、一个周末…",
+// 内存管理：推理时零分配: all buffers exist before the inference loop).
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+// Device status word (bit mask of the kernel families whose bounded waits
+// ran out).  One per device: module-scope device memory, no allocation.
+__device__ uint32_t g_status_word;
+
+constexpr int MAX_DEVICES = 64;
+
+struct DevInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *status = nullptr;
+};
+
+DevInfo g_dev[MAX_DEVICES];
+thread_local int t_last_cuda_error = 0;
+
+gq_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return GQ_ERR_CUDA;
+}
+
+gq_status make_ctx(gq_stream_t stream, LaunchCtx *ctx) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= MAX_DEVICES) return cuda_fail(cudaErrorInvalidDevice);
+    DevInfo &d = g_dev[dev];
+    std::call_once(d.once, [&d, dev]() {
+        cudaError_t r = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r == cudaSuccess)
+            r = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (r == cudaSuccess)
+            r = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (r == cudaSuccess && d.cc_major == 10 && d.cc_minor == 3)
+            r = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word);
+        d.err = r;
+    });
+    if (d.err != cudaSuccess) return cuda_fail(d.err);
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return GQ_ERR_ARCH;
+    ctx->stream = reinterpret_cast<cudaStream_t>(stream);
+    ctx->device = dev;
+    ctx->num_sms = d.num_sms;
+    ctx->status = d.status;
+    return GQ_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_type(int t) { return t >= GQ_Q4_0 && t <= GQ_Q8_K; }
+
+int64_t block_elems(int t) {
+    switch (t) {
+    case GQ_Q4_0: case GQ_Q8_0: return 32;
+    case GQ_Q4_K: case GQ_Q8_K: return 256;
+    }
+    return -1;
+}
+
+int64_t block_bytes(int t) {
+    switch (t) {
+    case GQ_Q4_0: return Q4_0_BYTES;
+    case GQ_Q8_0: return Q8_0_BYTES;
+    case GQ_Q4_K: return Q4_K_BYTES;
+    case GQ_Q8_K: return Q8_K_BYTES;
+    }
+    return -1;
+}
+
+// Largest element count accepted by the codecs (keeps every byte offset
+// well inside int64 and the grid-stride loops exact).
+constexpr int64_t MAX_ELEMS = (int64_t)1 << 46;
+// Largest reduction length of the product; bounded by the shared memory the
+// GEMV kernels stage one activation vector in.
+constexpr int64_t MAX_COLS = 131072;
+constexpr int64_t MAX_DIM = 0x7fffffff;
+
+gq_status check_codec(gq_type type, const void *x, const void *q, int64_t n, bool quant) {
+    if (!valid_type(type)) return GQ_ERR_TYPE;
+    if (n < 0 || n > MAX_ELEMS || n % block_elems(type) != 0) return GQ_ERR_SHAPE;
+    if (n == 0) return GQ_OK;
+    if (!x || !q) return GQ_ERR_NULL;
+    if (!aligned(x, 4)) return GQ_ERR_ALIGN;
+    const uintptr_t qa = (type == GQ_Q4_K || type == GQ_Q8_K) ? 4 : 2;
+    if (!aligned(q, qa)) return GQ_ERR_ALIGN;
+    (void)quant;
+    return GQ_OK;
+}
+
+gq_status check_matmul(gq_type wtype, const void *W, const void *xq, const void *out,
+                       int64_t rows, int64_t cols, int64_t batch, uintptr_t out_align) {
+    if (wtype != GQ_Q4_0 && wtype != GQ_Q8_0 && wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+    if (rows < 0 || cols < 0 || batch < 0) return GQ_ERR_SHAPE;
+    if (cols % block_elems(wtype) != 0) return GQ_ERR_SHAPE;
+    if (rows > MAX_DIM || batch > MAX_DIM || cols > MAX_COLS) return GQ_ERR_SHAPE;
+    const int64_t nblk = cols / block_elems(wtype);
+    if (rows * nblk > ((int64_t)1 << 40) || batch * nblk > MAX_DIM || batch * rows > ((int64_t)1 << 40))
+        return GQ_ERR_SHAPE;
+    if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
+    if (!W || !xq || !out) return GQ_ERR_NULL;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(out, out_align)) return GQ_ERR_ALIGN;
+    return GQ_OK;
+}
+
+int64_t tc_min_batch_value() {
+    static int64_t v = []() -> int64_t {
+        const char *s = std::getenv("GQ_TC_MIN_BATCH");
+        if (s && *s) {
+            char *end = nullptr;
+            long long x = std::strtoll(s, &end, 10);
+            if (end && *end == '\0' && x > 0) return (int64_t)x;
+        }
+        return 16;
+    }();
+    return v;
+}
+
+gq_status run_matmul(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums,
+                     int64_t rows, int64_t cols, int64_t batch, gq_path path, gq_stream_t stream) {
+    if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_MMA) return GQ_ERR_TYPE;
+    gq_status st = sums ? check_matmul(wtype, W, xq, sums, rows, cols, batch, 4)
+                        : check_matmul(wtype, W, xq, y, rows, cols, batch, 4);
+    if (st != GQ_OK) return st;
+    if (path == GQ_PATH_MMA) {
+        if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+        if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+    }
+    if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    bool use_mma = path == GQ_PATH_MMA;
+    if (path == GQ_PATH_AUTO)
+        use_mma = wtype == GQ_Q4_K && batch >= tc_min_batch_value() && mma_supported(rows, cols, batch);
+    cudaError_t e = use_mma ? launch_mma_q4k(W, xq, y, sums, rows, cols, batch, ctx)
+                            : launch_gemv(wtype, W, xq, y, sums, rows, cols, batch, ctx);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return GQ_OK;
+}
+
+}  // namespace
+}  // namespace gq
+
+using namespace gq;
+
+extern "C" {
+
+int64_t gq_block_elems(gq_type type) { return block_elems(type); }
+int64_t gq_block_bytes(gq_type type) { return block_bytes(type); }
+
+const char *gq_status_string(gq_status status) {
+    switch (status) {
+    case GQ_OK: return "ok";
+    case GQ_ERR_NULL: return "null pointer";
+    case GQ_ERR_TYPE: return "unsupported type, pairing or path";
+    case GQ_ERR_SHAPE: return "invalid size (negative, not a block multiple, or too large)";
+    case GQ_ERR_ALIGN: return "misaligned pointer";
+    case GQ_ERR_CUDA: return "CUDA error (see gq_last_cuda_error)";
+    case GQ_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case GQ_ERR_ARCH: return "current device is not an sm_103 GPU";
+    }
+    return "unknown status";
+}
+
+int gq_last_cuda_error(void) { return t_last_cuda_error; }
+
+gq_status gq_quantize_rows_async(gq_type type, const float *src, void *dst, int64_t n,
+                                 gq_stream_t stream) {
+    gq_status st = check_codec(type, src, dst, n, true);
+    if (st != GQ_OK || n == 0) return st;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    cudaError_t e = launch_quantize(type, src, dst, n, ctx);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e);
+}
+
+gq_status gq_quantize_rows(gq_type type, const float *src, void *dst, int64_t n) {
+    return gq_quantize_rows_async(type, src, dst, n, nullptr);
+}
+
+gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, int64_t n,
+                                   gq_stream_t stream) {
+    gq_status st = check_codec(type, dst, src, n, false);
+    if (st != GQ_OK || n == 0) return st;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    cudaError_t e = launch_dequantize(type, src, dst, n, ctx);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e);
+}
+
+gq_status gq_dequantize_rows(gq_type type, const void *src, float *dst, int64_t n) {
+    return gq_dequantize_rows_async(type, src, dst, n, nullptr);
+}
+
+gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
+                    int64_t cols, int64_t batch, gq_stream_t stream) {
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, GQ_PATH_AUTO, stream);
+}
+
+gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
+                         int64_t cols, int64_t batch, gq_path path, gq_stream_t stream) {
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, stream);
+}
+
+gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,
+                        int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                        gq_stream_t stream) {
+    if (!sums && rows > 0 && cols > 0 && batch > 0) return GQ_ERR_NULL;
+    return run_matmul(wtype, W, xq, nullptr, sums, rows, cols, batch, path, stream);
+}
+
+int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }
+
+gq_status gq_device_status(uint32_t *word, int reset) {
+    LaunchCtx ctx;
+    gq_status st = make_ctx(nullptr, &ctx);
+    if (st != GQ_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, ctx.status, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (reset && v) {
+        const uint32_t zero = 0;
+        e = cudaMemcpy(ctx.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (word) *word = v;
+    return v ? GQ_ERR_TIMEOUT : GQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,288 @@
+// gq_codec.cu -- block codecs: quantize (fp32 -> blocks) and dequantize
+// (blocks -> fp32) for Q4_0, Q8_0, Q4_K and Q8_K.
+//
+// Every step is the IEEE fp32 operation the format definition names, written
+// with explicit round-to-nearest intrinsics (and this file is compiled with
+// -fmad=false), so the bytes produced are identical to the reference
+// definition:
+//   "llama.cpp 推理引擎" (runguoli.com), §5.1 symmetric quantization
+//   (scale = max|x| / (2^(b-1) - 1), Q = round(x / scale)) for Q8_0 (b = 8),
+//   Q4_0 (b = 4, the §5.1 worked example) and the activation block Q8_K;
+//   §5.2 asymmetric quantization (scale and zero point from the min/max) and
+//   §5.5 (super-block scale d and min dmin over 6-bit per-sub-block factors)
+//   for Q4_K; §6.4 for the nibble order (element 2j in the low nibble of
+//   byte j).  Codes round half away from zero (roundf).
+//
+// Work split: one warp per block.  Q8_0 / Q4_0: lane i owns element i.
+// Q4_K / Q8_K: lane l owns elements 8l..8l+7, so the four lanes 4j..4j+3 own
+// sub-block j and sub-block statistics are 2-step shuffle reductions.
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float clampf(float v, float lo, float hi) {
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+// Symmetric block of 32 (Q8_0 when QMAX = 127, Q4_0 when QMAX = 7).
+template <int QMAX>
+__global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict__ x,
+                                                         uint8_t *__restrict__ dst,
+                                                         int64_t nblocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_wait();
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += warps) {
+        const float v = x[b * 32 + lane];
+        // max|x| (fabsf never yields -0, so the max of the block is well defined)
+        const float amax = warp_max(fabsf(v));
+        const __half dh = __float2half_rn(__fdiv_rn(amax, (float)QMAX));
+        const float d = __half2float(dh);
+        if (QMAX == 127) {
+            const float q = (d == 0.0f) ? 0.0f : clampf(roundf(__fdiv_rn(v, d)), -127.0f, 127.0f);
+            const int qi = (int)q & 0xff;
+            const int nxt = __shfl_down_sync(FULL, qi, 1);
+            uint8_t *blk = dst + b * Q8_0_BYTES;
+            if ((lane & 1) == 0)
+                *reinterpret_cast<uint16_t *>(blk + 2 + lane) = (uint16_t)(qi | (nxt << 8));
+            if (lane == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(dh);
+        } else {
+            const float q = (d == 0.0f) ? 0.0f : clampf(roundf(__fdiv_rn(v, d)), -8.0f, 7.0f);
+            const int c = (int)q + 8;  // stored code 0..15
+            const int hi = __shfl_down_sync(FULL, c, 1);
+            const int byte = c | (hi << 4);  // valid on even lanes: element 2j low, 2j+1 high
+            const int byte2 = __shfl_down_sync(FULL, byte, 2);
+            uint8_t *blk = dst + b * Q4_0_BYTES;
+            if ((lane & 3) == 0)
+                *reinterpret_cast<uint16_t *>(blk + 2 + (lane >> 1)) =
+                    (uint16_t)((byte & 0xff) | ((byte2 & 0xff) << 8));
+            if (lane == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(dh);
+        }
+    }
+    pdl_launch_dependents();
+}
+
+// Q8_K: 256 elements, fp32 scale d = max|x| / 127, eight int16 sub-block sums.
+__global__ void __launch_bounds__(256) quantize_q8_k_kernel(const float *__restrict__ x,
+                                                            uint8_t *__restrict__ dst,
+                                                            int64_t nblocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_wait();
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += warps) {
+        const float *xb = x + b * QK_K + 8 * lane;
+        float v[8];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = xb[i];
+            amax = fmaxf(amax, fabsf(v[i]));
+        }
+        amax = warp_max(amax);
+        const float d = __fdiv_rn(amax, 127.0f);
+        uint32_t w0 = 0, w1 = 0;
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q =
+                (d == 0.0f) ? 0.0f : clampf(roundf(__fdiv_rn(v[i], d)), -127.0f, 127.0f);
+            const int qi = (int)q;
+            sum += qi;
+            if (i < 4)
+                w0 |= (uint32_t)(qi & 0xff) << (8 * i);
+            else
+                w1 |= (uint32_t)(qi & 0xff) << (8 * (i - 4));
+        }
+        sum += __shfl_xor_sync(FULL, sum, 1);
+        sum += __shfl_xor_sync(FULL, sum, 2);
+        uint8_t *blk = dst + b * Q8_K_BYTES;
+        reinterpret_cast<uint32_t *>(blk + 4 + 8 * lane)[0] = w0;
+        reinterpret_cast<uint32_t *>(blk + 4 + 8 * lane)[1] = w1;
+        if ((lane & 3) == 0)
+            *reinterpret_cast<int16_t *>(blk + 260 + 2 * (lane >> 2)) = (int16_t)sum;
+        if (lane == 0) *reinterpret_cast<float *>(blk) = d;
+    }
+    pdl_launch_dependents();
+}
+
+// Q4_K: per 32-element sub-block j (lanes 4j..4j+3):
+//   lo_j = min(0, min x), hi_j = max x
+//   dmin = fp16_up(max_j(-lo_j) / 63), m_j = min(63, ceil(-lo_j / dmin))
+//   base_j = -(dmin * m_j), r_j = hi_j - base_j
+//   d = fp16_up(max_j r_j / 945), sc_j = min(63, ceil(r_j / (15 d)))
+//   q = clamp(round((x - base_j) / (d * sc_j)), 0, 15)
+__global__ void __launch_bounds__(256) quantize_q4_k_kernel(const float *__restrict__ x,
+                                                            uint8_t *__restrict__ dst,
+                                                            int64_t nblocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_wait();
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
+         b += warps) {
+        const float *xb = x + b * QK_K + 8 * lane;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = xb[i];
+        float mn = v[0], mx = v[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) {
+            mn = fminf(mn, v[i]);
+            mx = fmaxf(mx, v[i]);
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+        }
+        const float lo = mn < 0.0f ? mn : 0.0f;
+        const float hi = mx;
+        // max over sub-blocks of -lo_j, as a +0-initialised maximum
+        float nlo = mn < 0.0f ? -mn : 0.0f;
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) nlo = fmaxf(nlo, __shfl_xor_sync(FULL, nlo, o));
+        if (!(nlo > 0.0f)) nlo = 0.0f;
+        const __half dminh = __float2half_ru(__fdiv_rn(nlo, 63.0f));
+        const float dmin = __half2float(dminh);
+        float m = (dmin == 0.0f) ? 0.0f : ceilf(__fdiv_rn(-lo, dmin));
+        if (m > 63.0f) m = 63.0f;
+        const float base = -__fmul_rn(dmin, m);
+        const float r = __fsub_rn(hi, base);
+        float rmax = r;
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) rmax = fmaxf(rmax, __shfl_xor_sync(FULL, rmax, o));
+        if (!(rmax > 0.0f)) rmax = 0.0f;
+        const __half dh = __float2half_ru(__fdiv_rn(rmax, 945.0f));
+        const float d = __half2float(dh);
+        float sc = (d == 0.0f) ? 0.0f : ceilf(__fdiv_rn(r, __fmul_rn(15.0f, d)));
+        if (sc > 63.0f) sc = 63.0f;
+        const float step = __fmul_rn(d, sc);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q = (step == 0.0f)
+                                ? 0.0f
+                                : clampf(roundf(__fdiv_rn(__fsub_rn(v[i], base), step)), 0.0f,
+                                         15.0f);
+            packed |= (uint32_t)q << (4 * i);  // element 8l+i -> nibble i of the word
+        }
+        uint8_t *blk = dst + b * Q4_K_BYTES;
+        reinterpret_cast<uint32_t *>(blk + 16)[lane] = packed;
+        // gather the eight (sc_j, m_j) pairs and pack sixteen 6-bit fields
+        uint32_t w[3] = {0u, 0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t scj = (uint32_t)__shfl_sync(FULL, (int)sc, 4 * j);
+            const uint32_t mj = (uint32_t)__shfl_sync(FULL, (int)m, 4 * j);
+#pragma unroll
+            for (int f = 0; f < 2; ++f) {
+                const uint32_t val = f ? mj : scj;
+                const int bit = 6 * (j + 8 * f);
+                const int wi = bit >> 5, sh = bit & 31;
+                w[wi] |= val << sh;
+                if (sh > 26) w[wi + 1] |= val >> (32 - sh);
+            }
+        }
+        if (lane == 0) {
+            uint32_t *hdr = reinterpret_cast<uint32_t *>(blk);
+            hdr[0] = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(dminh) << 16);
+            hdr[1] = w[0];
+            hdr[2] = w[1];
+            hdr[3] = w[2];
+        }
+    }
+    pdl_launch_dependents();
+}
+
+// ------------------------------------------------------------------ decoders
+// One thread per element; each output is the exact reconstruction rounded
+// once to fp32 (products of the scales with the small integer codes are
+// exact in fp32, only the Q4_K difference and the fp32 Q8_K product round).
+
+__global__ void dequantize_kernel(int type, const uint8_t *__restrict__ src,
+                                  float *__restrict__ dst, int64_t n) {
+    pdl_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
+        float out;
+        if (type == GQ_Q4_0) {
+            const uint8_t *blk = src + (e >> 5) * Q4_0_BYTES;
+            const int i = (int)(e & 31);
+            const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+            const int byte = blk[2 + (i >> 1)];
+            const int c = (i & 1) ? (byte >> 4) : (byte & 15);
+            out = __fmul_rn(d, (float)(c - 8));
+        } else if (type == GQ_Q8_0) {
+            const uint8_t *blk = src + (e >> 5) * Q8_0_BYTES;
+            const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+            out = __fmul_rn(d, (float)(int8_t)blk[2 + (e & 31)]);
+        } else if (type == GQ_Q4_K) {
+            const uint8_t *blk = src + (e >> 8) * Q4_K_BYTES;
+            const int i = (int)(e & 255), j = i >> 5;
+            const uint32_t *hdr = reinterpret_cast<const uint32_t *>(blk);
+            const float d = half_bits_to_float(hdr[0]);
+            const float dmin = half_bits_to_float(hdr[0] >> 16);
+            const uint64_t lo64 = (uint64_t)hdr[1] | ((uint64_t)hdr[2] << 32);
+            const uint64_t hi64 = (uint64_t)hdr[2] | ((uint64_t)hdr[3] << 32);
+            const float sc = (float)((lo64 >> (6 * j)) & 63);
+            const float m = (float)((hi64 >> (6 * j + 16)) & 63);
+            const int byte = blk[16 + (i >> 1)];
+            const float q = (float)((i & 1) ? (byte >> 4) : (byte & 15));
+            out = __fsub_rn(__fmul_rn(__fmul_rn(d, sc), q), __fmul_rn(dmin, m));
+        } else {
+            const uint8_t *blk = src + (e >> 8) * Q8_K_BYTES;
+            const float d = *reinterpret_cast<const float *>(blk);
+            out = __fmul_rn(d, (float)(int8_t)blk[4 + (e & 255)]);
+        }
+        dst[e] = out;
+    }
+    pdl_launch_dependents();
+}
+
+int grid_for(int64_t work_items, int per_cta, int num_sms) {
+    int64_t g = (work_items + per_cta - 1) / per_cta;
+    const int64_t cap = (int64_t)num_sms * 16;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
+                            const LaunchCtx &ctx) {
+    const int64_t nb = n / (t == GQ_Q4_K || t == GQ_Q8_K ? QK_K : 32);
+    const int grid = grid_for(nb, 8, ctx.num_sms);
+    uint8_t *d8 = static_cast<uint8_t *>(dst);
+    switch (t) {
+    case GQ_Q8_0:
+        return launch_pdl(quantize32_kernel<127>, grid, 256, 0, ctx.stream, src, d8, nb);
+    case GQ_Q4_0:
+        return launch_pdl(quantize32_kernel<7>, grid, 256, 0, ctx.stream, src, d8, nb);
+    case GQ_Q4_K:
+        return launch_pdl(quantize_q4_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
+    case GQ_Q8_K:
+        return launch_pdl(quantize_q8_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dequantize(gq_type t, const void *src, float *dst, int64_t n,
+                              const LaunchCtx &ctx) {
+    const int grid = grid_for(n, 256, ctx.num_sms);
+    return launch_pdl(dequantize_kernel, grid, 256, 0, ctx.stream, (int)t,
+                      static_cast<const uint8_t *>(src), dst, n);
+}
+
+}  // namespace gq

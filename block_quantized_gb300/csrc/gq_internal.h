@@ -1,0 +1,51 @@
+// gq_internal.h -- host-side interface between the API translation unit and
+// the kernel translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "gq.h"
+
+namespace gq {
+
+struct LaunchCtx;
+
+// Launch with programmatic stream serialization allowed, so a kernel's
+// prologue (weight prefetch) may overlap the tail of the previous kernel in
+// the stream; every kernel calls griddepcontrol.wait before it touches data
+// another kernel may produce or consume.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
+                            const LaunchCtx &ctx);
+cudaError_t launch_dequantize(gq_type t, const void *src, float *dst, int64_t n,
+                              const LaunchCtx &ctx);
+
+// dp4a GEMV family.  sums != nullptr selects the block-sum diagnostic output
+// instead of y.
+cudaError_t launch_gemv(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums,
+                        int64_t rows, int64_t cols, int64_t batch, const LaunchCtx &ctx);
+
+// tcgen05 tensor-core family (Q4_K x Q8_K).
+cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
+                           int64_t cols, int64_t batch, const LaunchCtx &ctx);
+bool mma_supported(int64_t rows, int64_t cols, int64_t batch);
+
+}  // namespace gq

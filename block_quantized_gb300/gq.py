@@ -1,0 +1,206 @@
+"""Thin Python binding of the C ABI in include/gq.h (libgq.so).
+
+Argument marshalling only: every function forwards device pointers and sizes
+to the library, where all of the work runs in CUDA kernels.  Functions named
+``gq_*`` mirror the C entry points one to one and accept either torch CUDA
+tensors or raw integer device pointers; a stream argument of ``None`` means
+the current torch stream.  The convenience helpers below them only allocate
+outputs with torch and call the same entry points.
+
+There is no fallback: if the library cannot be loaded, or a call returns an
+error status, a GQError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+Q4_0, Q8_0, Q4_K, Q8_K = 0, 1, 2, 3
+PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q8_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q8_K: 276}
+
+STATUS = {0: "GQ_OK", 1: "GQ_ERR_NULL", 2: "GQ_ERR_TYPE", 3: "GQ_ERR_SHAPE",
+          4: "GQ_ERR_ALIGN", 5: "GQ_ERR_CUDA", 6: "GQ_ERR_TIMEOUT", 7: "GQ_ERR_ARCH"}
+
+# Every symbol the header declares, with its ctypes signature.
+_i64, _i32, _vp, _u32p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)
+SIGNATURES = {
+    "gq_block_elems": ([_i32], _i64),
+    "gq_block_bytes": ([_i32], _i64),
+    "gq_status_string": ([_i32], ctypes.c_char_p),
+    "gq_last_cuda_error": ([], _i32),
+    "gq_quantize_rows": ([_i32, _vp, _vp, _i64], _i32),
+    "gq_quantize_rows_async": ([_i32, _vp, _vp, _i64, _vp], _i32),
+    "gq_dequantize_rows": ([_i32, _vp, _vp, _i64], _i32),
+    "gq_dequantize_rows_async": ([_i32, _vp, _vp, _i64, _vp], _i32),
+    "gq_matmul": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
+    "gq_matmul_path": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp], _i32),
+    "gq_block_sums": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp], _i32),
+    "gq_tc_min_batch": ([], _i64),
+    "gq_device_status": ([_u32p, _i32], _i32),
+}
+
+
+class GQError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        detail = ""
+        if status == 5 and _lib is not None:
+            detail = f" (cudaError {_lib.gq_last_cuda_error()})"
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}{detail}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libgq.so (optionally compiling it first)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build_if_missing and _build.needs_build():
+                _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libgq.so not built ({path}); run __graft_entry__.build() first")
+            L = ctypes.CDLL(path)
+            for name, (args, res) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = L
+    return _lib
+
+
+def _p(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _s(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int) -> None:
+    if st != 0:
+        raise GQError(fn, st)
+
+
+# ----------------------------------------------------------- 1:1 entry points
+
+def gq_block_elems(t: int) -> int:
+    return int(load().gq_block_elems(t))
+
+
+def gq_block_bytes(t: int) -> int:
+    return int(load().gq_block_bytes(t))
+
+
+def gq_quantize_rows_async(t: int, src, dst, n: int, stream=None) -> None:
+    _check("gq_quantize_rows_async",
+           load().gq_quantize_rows_async(t, _p(src), _p(dst), n, _s(stream)))
+
+
+def gq_quantize_rows(t: int, src, dst, n: int) -> None:
+    _check("gq_quantize_rows", load().gq_quantize_rows(t, _p(src), _p(dst), n))
+
+
+def gq_dequantize_rows_async(t: int, src, dst, n: int, stream=None) -> None:
+    _check("gq_dequantize_rows_async",
+           load().gq_dequantize_rows_async(t, _p(src), _p(dst), n, _s(stream)))
+
+
+def gq_dequantize_rows(t: int, src, dst, n: int) -> None:
+    _check("gq_dequantize_rows", load().gq_dequantize_rows(t, _p(src), _p(dst), n))
+
+
+def gq_matmul(wtype: int, W, xq, y, rows: int, cols: int, batch: int, stream=None) -> None:
+    _check("gq_matmul", load().gq_matmul(wtype, _p(W), _p(xq), _p(y), rows, cols, batch,
+                                         _s(stream)))
+
+
+def gq_matmul_path(wtype: int, W, xq, y, rows: int, cols: int, batch: int, path: int,
+                   stream=None) -> None:
+    _check("gq_matmul_path", load().gq_matmul_path(wtype, _p(W), _p(xq), _p(y), rows, cols,
+                                                   batch, path, _s(stream)))
+
+
+def gq_block_sums(wtype: int, W, xq, sums, rows: int, cols: int, batch: int, path: int,
+                  stream=None) -> None:
+    _check("gq_block_sums", load().gq_block_sums(wtype, _p(W), _p(xq), _p(sums), rows, cols,
+                                                 batch, path, _s(stream)))
+
+
+def gq_tc_min_batch() -> int:
+    return int(load().gq_tc_min_batch())
+
+
+def gq_device_status(reset: bool = True) -> int:
+    """Returns the device status word (0 = no bounded wait ran out)."""
+    w = ctypes.c_uint32(0)
+    st = load().gq_device_status(ctypes.byref(w), 1 if reset else 0)
+    if st not in (0, 6):
+        raise GQError("gq_device_status", st)
+    return int(w.value)
+
+
+# ------------------------------------------------------ convenience (torch)
+
+def packed_bytes(t: int, n: int) -> int:
+    return n // BLOCK_ELEMS[t] * BLOCK_BYTES[t]
+
+
+def quantize(t: int, x, stream=None):
+    """Quantize a CUDA fp32 tensor [..., cols] into a uint8 tensor
+    [..., cols / block_elems * block_bytes]."""
+    import torch
+    assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
+    cols = x.shape[-1]
+    out = torch.empty(*x.shape[:-1], cols // BLOCK_ELEMS[t] * BLOCK_BYTES[t],
+                      dtype=torch.uint8, device=x.device)
+    gq_quantize_rows_async(t, x, out, x.numel(), stream)
+    return out
+
+
+def dequantize(t: int, q, n: int, stream=None):
+    import torch
+    out = torch.empty(n, dtype=torch.float32, device=q.device)
+    gq_dequantize_rows_async(t, q, out, n, stream)
+    return out
+
+
+def matmul(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH_AUTO,
+           out=None, stream=None):
+    import torch
+    y = out if out is not None else torch.empty(batch, rows, dtype=torch.float32, device=W.device)
+    gq_matmul_path(wtype, W, xq, y, rows, cols, batch, path, stream)
+    return y
+
+
+def block_sums(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH_GEMV,
+               stream=None):
+    import torch
+    nb = cols // BLOCK_ELEMS[wtype]
+    shape = (batch, rows, nb, 2) if wtype == Q4_K else (batch, rows, nb)
+    s = torch.empty(shape, dtype=torch.int32, device=W.device)
+    gq_block_sums(wtype, W, xq, s, rows, cols, batch, path, stream)
+    return s

@@ -1,0 +1,201 @@
+/*
+ * gq.h -- C ABI of the block-quantized GEMV/GEMM library for GB300 (sm_103a).
+ *
+ * The library multiplies weights stored as Q4_0 / Q8_0 / Q4_K blocks with
+ * activations quantized to int8 per 32-element (Q8_0) or 256-element (Q8_K)
+ * block, as per-block integer dot products scaled by the block factors and
+ * summed.  The method is the one the llama.cpp pages describe:
+ *   "llama.cpp 推理引擎" (runguoli.com/llm-libs/14-llama-cpp), §5.1-§5.5
+ *   (symmetric / asymmetric quantization, Q4_0, Q8_0, K-quants) and §6.4
+ *   (the Q4_0 vec_dot: per-block integer products scaled by the block
+ *   scale); "llama.cpp：一个人、一个周末、一个改变 AI 推理格局的 C++ 文件"
+ *   (tech-blog-56a.pages.dev), 第二层：量化引擎 (block quantization, the
+ *   256 = 8 x 32 K-quant super-block) and 内存管理：推理时零分配 (no
+ *   allocation during inference).
+ *
+ * Block formats (all multi-byte fields little-endian, blocks packed back to
+ * back, a row of a matrix is cols / block_elems consecutive blocks and rows
+ * are consecutive):
+ *   Q4_0  18 B / 32 elements : fp16 d @0, 16 bytes of 4-bit codes c @2;
+ *                              byte j holds element 2j (low nibble) and
+ *                              2j+1 (high nibble); w = d * (c - 8).
+ *   Q8_0  34 B / 32 elements : fp16 d @0, int8 q[32] @2; w = d * q.
+ *   Q4_K 144 B / 256 elements: fp16 d @0, fp16 dmin @2, twelve bytes @4
+ *                              holding sixteen 6-bit fields LSB-first
+ *                              (fields 0..7 = sub-block scales sc_j, 8..15 =
+ *                              sub-block mins m_j), 128 bytes of 4-bit codes
+ *                              q @16 in the Q4_0 nibble order;
+ *                              w = d * sc_j * q - dmin * m_j for element i
+ *                              of sub-block j = i / 32.
+ *   Q8_K 276 B / 256 elements: fp32 d @0, int8 q[256] @4, int16 bsums[8]
+ *                              @260 (bsums[j] = sum of q over sub-block j);
+ *                              w = d * q.
+ * Quantization rounds codes half away from zero.  Q8_0 and Q8_K use
+ * d = max|x| / 127, Q4_0 uses d = max|x| / 7 (fp16 scales rounded to
+ * nearest-even); Q4_K fits each 32-element sub-block by its min/max with fp16
+ * d and dmin rounded toward +infinity (so that the ceilinged 6-bit scale and
+ * min always cover the sub-block) -- see the quantize entry point below.
+ *
+ * Pairings for the product: Q4_0 and Q8_0 weights take Q8_0 activations;
+ * Q4_K weights take Q8_K activations.
+ *
+ * General rules for every entry point:
+ *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
+ *     memory) owned by the caller.  The library never allocates or frees
+ *     device memory and never copies between host and device on these calls.
+ *   - Calls are asynchronous on the given stream (NULL = the legacy default
+ *     stream); none of them synchronizes.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns an error status and launches nothing.  The
+ *     library never aborts, exits or prints.
+ *   - GQ_ERR_CUDA is returned when a launch fails; gq_last_cuda_error()
+ *     then gives the cudaError_t value (per calling thread).
+ *   - Device-side waits (on TMA transfer barriers) are bounded; a wait that
+ *     runs out sets a device status word instead of hanging, and
+ *     gq_device_status() reports it as GQ_ERR_TIMEOUT.
+ *   - Thread safety: every entry point may be called from several host
+ *     threads at once; the only shared state is a per-device attribute cache
+ *     and the device status word.
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *gq_stream_t;
+
+typedef enum {
+    GQ_Q4_0 = 0,
+    GQ_Q8_0 = 1,
+    GQ_Q4_K = 2,
+    GQ_Q8_K = 3
+} gq_type;
+
+typedef enum {
+    GQ_OK = 0,
+    GQ_ERR_NULL = 1,    /* a required pointer is NULL */
+    GQ_ERR_TYPE = 2,    /* unknown type, or an unsupported weight/activation pairing */
+    GQ_ERR_SHAPE = 3,   /* negative size, size not a block multiple, or size overflow */
+    GQ_ERR_ALIGN = 4,   /* a pointer is not aligned as the call requires */
+    GQ_ERR_CUDA = 5,    /* a CUDA launch or query failed (see gq_last_cuda_error) */
+    GQ_ERR_TIMEOUT = 6, /* a bounded device wait ran out (reported by gq_device_status) */
+    GQ_ERR_ARCH = 7     /* the current device is not an sm_103 GPU */
+} gq_status;
+
+/* Kernel family selection for gq_matmul_path / gq_block_sums. */
+typedef enum {
+    GQ_PATH_AUTO = 0,   /* GEMV below the tensor-core crossover batch, MMA at or above */
+    GQ_PATH_GEMV = 1,   /* dp4a GEMV kernels (any batch; batch is processed in chunks) */
+    GQ_PATH_MMA = 2     /* tcgen05 tensor-core kernel (Q4_K weights only) */
+} gq_path;
+
+/* Elements per block: 32, 32, 256, 256.  -1 for an unknown type. */
+int64_t gq_block_elems(gq_type type);
+/* Bytes per block: 18, 34, 144, 276.  -1 for an unknown type. */
+int64_t gq_block_bytes(gq_type type);
+/* Static text for a status code (never NULL). */
+const char *gq_status_string(gq_status status);
+/* cudaError_t of the last GQ_ERR_CUDA returned to this host thread (0 if none). */
+int gq_last_cuda_error(void);
+
+/*
+ * Quantize n fp32 values (n / block_elems(type) blocks) into packed blocks.
+ *   src : device, n floats, 4-byte aligned, finite values (non-finite input
+ *         gives unspecified codes; magnitudes must keep the fp16 scales in
+ *         range: |x| < 65504 * 127 for Q8_0, 65504 * 7 for Q4_0, 65504 * 945
+ *         for Q4_K).
+ *   dst : device, n / block_elems * block_bytes bytes; 4-byte aligned for
+ *         Q8_K, 16-byte aligned for Q4_K, 2-byte aligned for Q4_0 / Q8_0.
+ *   n   : element count, >= 0 and a multiple of block_elems(type).
+ * Results are bit-identical to the reference definition of each format
+ * ("llama.cpp 推理引擎" §5.1 symmetric rule for Q8_0 / Q4_0 / Q8_K, §5.2
+ * asymmetric min/max rule per sub-block and §5.5 two-level scales for Q4_K).
+ * Errors: GQ_ERR_NULL (n > 0 and a NULL pointer), GQ_ERR_TYPE, GQ_ERR_SHAPE,
+ * GQ_ERR_ALIGN, GQ_ERR_CUDA.  Enqueued on the legacy default stream.
+ */
+gq_status gq_quantize_rows(gq_type type, const float *src, void *dst, int64_t n);
+gq_status gq_quantize_rows_async(gq_type type, const float *src, void *dst, int64_t n,
+                                 gq_stream_t stream);
+
+/*
+ * Reconstruct n fp32 values from packed blocks ("llama.cpp 推理引擎" §5.3
+ * and §5.5 dequantization formulas, with the fp16 scale of Q8_0 and the
+ * subtracted Q4_K min of this library's formats).  Each output is the exact
+ * reconstruction rounded once to fp32.
+ *   src : device, packed blocks (alignment as for gq_quantize_rows' dst).
+ *   dst : device, n floats, 4-byte aligned.
+ * Errors as for gq_quantize_rows.
+ */
+gq_status gq_dequantize_rows(gq_type type, const void *src, float *dst, int64_t n);
+gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, int64_t n,
+                                   gq_stream_t stream);
+
+/*
+ * y[b][r] = sum over the blocks k of row r of the scaled integer block dots
+ * ("llama.cpp 推理引擎" §6.4 for the per-block dot; §5.5 for the Q4_K
+ * two-level scales):
+ *   Q4_0 x Q8_0 : d_w * d_x * sum_i (c_i - 8) * a_i
+ *   Q8_0 x Q8_0 : d_w * d_x * sum_i w_i * a_i
+ *   Q4_K x Q8_K : d_x * (d * sum_j sc_j * s_j - dmin * sum_j m_j * t_j),
+ *                 s_j = sum_{i in j} q_i * a_i, t_j = bsums[j]
+ *   wtype : GQ_Q4_0, GQ_Q8_0 or GQ_Q4_K.
+ *   W     : device, rows x (cols / block_elems) weight blocks, 16-byte aligned.
+ *   xq    : device, batch x (cols / block_elems) activation blocks (Q8_0 for
+ *           Q4_0 / Q8_0 weights, Q8_K for Q4_K), one vector after another;
+ *           16-byte aligned.
+ *   y     : device, float[batch][rows], 16-byte aligned; fully overwritten.
+ *   rows, cols, batch : > 0 (a zero size is a no-op returning GQ_OK);
+ *           cols a multiple of 256 for Q4_K and of 32 for Q4_0 / Q8_0 (the
+ *           fast kernels need cols % 256 == 0; other multiples of 32 run a
+ *           plain per-block kernel).
+ * The integer block sums are exact (int32); y matches the double-precision
+ * sum of the same terms within 1e-4 of the sum of their magnitudes.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
+                    int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
+
+/* gq_matmul with an explicit kernel family (crossover studies, tests).
+ * GQ_PATH_MMA is defined for Q4_K only (GQ_ERR_TYPE otherwise). */
+gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
+                         int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                         gq_stream_t stream);
+
+/*
+ * Diagnostic: the integer block sums of the product, as computed by the
+ * chosen kernel family, without the float scaling.
+ *   sums : device, int32, 4-byte aligned, laid out [batch][rows][nblk][c] with
+ *          nblk = cols / block_elems(wtype) and c = 1 (Q4_0, Q8_0: the block
+ *          dot) or c = 2 (Q4_K: S1 = sum_j sc_j * s_j, S2 = sum_j m_j * t_j).
+ * Other arguments and errors as gq_matmul_path.
+ */
+gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,
+                        int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                        gq_stream_t stream);
+
+/* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
+ * Q4_K (the measured crossover; the environment variable GQ_TC_MIN_BATCH,
+ * read once, overrides it). */
+int64_t gq_tc_min_batch(void);
+
+/*
+ * Reads (and with reset != 0 clears) the device status word of the current
+ * device.  Synchronizes the device.  Returns GQ_OK when no bounded wait ran
+ * out since the last reset, GQ_ERR_TIMEOUT otherwise (the raw word, a bit
+ * mask of the kernels that gave up, is stored to *word when word != NULL),
+ * GQ_ERR_CUDA if the query itself failed.  Not callable during stream
+ * capture.
+ */
+gq_status gq_device_status(uint32_t *word, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQ_H */

@@ -1,0 +1,110 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/gq.h declares, and rejects invalid
+arguments on the host with the documented status codes before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_quantized_gb300 import build as gqbuild
+from block_quantized_gb300 import gq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, NULL, TYPE, SHAPE, ALIGN, CUDA = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gqbuild.build()
+    return gq.load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "gq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(gq.SIGNATURES), "binding and header disagree"
+
+
+def test_block_geometry(lib):
+    assert [gq.gq_block_elems(t) for t in range(4)] == [32, 32, 256, 256]
+    assert [gq.gq_block_bytes(t) for t in range(4)] == [18, 34, 144, 276]
+    assert gq.gq_block_elems(9) == -1 and gq.gq_block_bytes(-1) == -1
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.gq_status_string(s)
+    assert lib.gq_status_string(123) == b"unknown status"
+
+
+# Fake, never-dereferenced device addresses: validation happens on the host
+# and returns before any CUDA call.
+A16 = 0x10000
+MIS = 0x10002
+
+
+def test_matmul_validation(lib):
+    f = lib.gq_matmul
+    assert f(3, A16, A16, A16, 8, 256, 1, None) == TYPE          # Q8_K is not a weight type
+    assert f(7, A16, A16, A16, 8, 256, 1, None) == TYPE
+    assert f(2, A16, A16, A16, 8, 100, 1, None) == SHAPE         # not a block multiple
+    assert f(0, A16, A16, A16, 8, 48, 1, None) == SHAPE
+    assert f(2, A16, A16, A16, -1, 256, 1, None) == SHAPE
+    assert f(2, A16, A16, A16, 8, 256, -3, None) == SHAPE
+    assert f(2, A16, A16, A16, 1 << 40, 256, 1, None) == SHAPE   # size overflow
+    assert f(2, A16, A16, A16, 8, 1 << 30, 1, None) == SHAPE     # cols above the maximum
+    assert f(2, 0, A16, A16, 8, 256, 1, None) == NULL
+    assert f(2, A16, 0, A16, 8, 256, 1, None) == NULL
+    assert f(2, A16, A16, 0, 8, 256, 1, None) == NULL
+    assert f(2, MIS, A16, A16, 8, 256, 1, None) == ALIGN
+    assert f(2, A16, MIS, A16, 8, 256, 1, None) == ALIGN
+    assert f(2, A16, A16, A16 + 1, 8, 256, 1, None) == ALIGN
+    # zero sizes are a no-op, even with NULL pointers
+    assert f(2, 0, 0, 0, 0, 256, 1, None) == OK
+    assert f(2, 0, 0, 0, 8, 256, 0, None) == OK
+    # path and pairing rules
+    g = lib.gq_matmul_path
+    assert g(2, A16, A16, A16, 8, 256, 1, 9, None) == TYPE
+    assert g(0, A16, A16, A16, 8, 256, 64, 2, None) == TYPE      # MMA is Q4_K only
+    assert lib.gq_block_sums(2, A16, A16, 0, 8, 256, 1, 1, None) == NULL
+
+
+def test_codec_validation(lib):
+    q = lib.gq_quantize_rows
+    assert q(5, A16, A16, 32) == TYPE
+    assert q(0, A16, A16, 33) == SHAPE
+    assert q(2, A16, A16, 32) == SHAPE                          # Q4_K needs 256-multiples
+    assert q(1, A16, A16, -32) == SHAPE
+    assert q(1, 0, A16, 32) == NULL
+    assert q(1, A16, 0, 32) == NULL
+    assert q(1, A16 + 2, A16, 32) == ALIGN                      # src must be 4-aligned
+    assert q(3, A16, A16 + 2, 256) == ALIGN                     # Q8_K dst 4-aligned
+    assert q(1, A16, A16 + 1, 32) == ALIGN                      # Q8_0 dst 2-aligned
+    assert q(1, 0, 0, 0) == OK
+    d = lib.gq_dequantize_rows
+    assert d(0, A16, A16, 31) == SHAPE
+    assert d(2, A16 + 2, A16, 256) == ALIGN
+    assert d(0, 0, 0, 0) == OK
+
+
+def test_valid_call_without_gpu_fails_loudly(lib):
+    """With arguments that pass validation, the library needs a CUDA device;
+    without one it reports GQ_ERR_CUDA (never a silent CPU result)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.gq_matmul(2, A16, A16, A16, 8, 256, 1, None) == CUDA
+    assert lib.gq_last_cuda_error() != 0
+    with pytest.raises(gq.GQError):
+        gq.gq_matmul(2, A16, A16, A16, 8, 256, 1, stream=0)
