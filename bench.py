@@ -43,6 +43,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return p.parse_args()
 
 
@@ -315,7 +316,7 @@ def run_gpu(args, world, rank):
         extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph)
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and not args.no_cpu:
         cpu = run_cpu_baseline()
 
     if rank == 0:

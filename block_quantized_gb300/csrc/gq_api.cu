@@ -129,25 +129,36 @@ int64_t tc_min_batch_value() {
     return v;
 }
 
-gq_status run_matmul(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums,
-                     int64_t rows, int64_t cols, int64_t batch, gq_path path, gq_stream_t stream) {
+// One product call.  act is xq (quantized blocks) or, with fused_f32, fp32
+// activations; exactly one of y / sums is non-null.
+gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
+                     int64_t rows, int64_t cols, int64_t batch, gq_path path, unsigned flags,
+                     bool fused_f32, gq_stream_t stream) {
     if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_MMA) return GQ_ERR_TYPE;
-    gq_status st = sums ? check_matmul(wtype, W, xq, sums, rows, cols, batch, 4)
-                        : check_matmul(wtype, W, xq, y, rows, cols, batch, 4);
+    if (flags & ~(unsigned)GQ_FLAG_W_STATIC) return GQ_ERR_TYPE;
+    gq_status st = sums ? check_matmul(wtype, W, act, sums, rows, cols, batch, 4)
+                        : check_matmul(wtype, W, act, y, rows, cols, batch, 4);
     if (st != GQ_OK) return st;
+    if (fused_f32) {
+        if (path == GQ_PATH_MMA) return GQ_ERR_TYPE;
+        if (cols % 256 != 0) return GQ_ERR_SHAPE;
+    }
     if (path == GQ_PATH_MMA) {
         if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
         if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
     }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
+    bool use_mma = path == GQ_PATH_MMA;
+    if (path == GQ_PATH_AUTO)
+        use_mma = !fused_f32 && wtype == GQ_Q4_K && batch >= tc_min_batch_value() &&
+                  mma_supported(rows, cols, batch);
+    if (!use_mma && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    bool use_mma = path == GQ_PATH_MMA;
-    if (path == GQ_PATH_AUTO)
-        use_mma = wtype == GQ_Q4_K && batch >= tc_min_batch_value() && mma_supported(rows, cols, batch);
-    cudaError_t e = use_mma ? launch_mma_q4k(W, xq, y, sums, rows, cols, batch, ctx)
-                            : launch_gemv(wtype, W, xq, y, sums, rows, cols, batch, ctx);
+    cudaError_t e = use_mma ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ctx)
+                            : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
+                                          (flags & GQ_FLAG_W_STATIC) != 0, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
     return GQ_OK;
 }
@@ -210,19 +221,38 @@ gq_status gq_dequantize_rows(gq_type type, const void *src, float *dst, int64_t 
 
 gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
                     int64_t cols, int64_t batch, gq_stream_t stream) {
-    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, GQ_PATH_AUTO, stream);
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, GQ_PATH_AUTO, 0, false, stream);
 }
 
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
                          int64_t cols, int64_t batch, gq_path path, gq_stream_t stream) {
-    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, stream);
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, 0, false, stream);
+}
+
+gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
+                       int64_t cols, int64_t batch, gq_path path, unsigned flags,
+                       gq_stream_t stream) {
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, flags, false, stream);
+}
+
+gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y, int64_t rows,
+                        int64_t cols, int64_t batch, unsigned flags, gq_stream_t stream) {
+    if (x && ((reinterpret_cast<uintptr_t>(x) & 15) != 0)) return GQ_ERR_ALIGN;
+    return run_matmul(wtype, W, x, y, nullptr, rows, cols, batch, GQ_PATH_GEMV, flags, true, stream);
 }
 
 gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,
                         int64_t rows, int64_t cols, int64_t batch, gq_path path,
                         gq_stream_t stream) {
     if (!sums && rows > 0 && cols > 0 && batch > 0) return GQ_ERR_NULL;
-    return run_matmul(wtype, W, xq, nullptr, sums, rows, cols, batch, path, stream);
+    return run_matmul(wtype, W, xq, nullptr, sums, rows, cols, batch, path, 0, false, stream);
+}
+
+gq_status gq_block_sums_f32(gq_type wtype, const void *W, const float *x, int32_t *sums,
+                            int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream) {
+    if (!sums && rows > 0 && cols > 0 && batch > 0) return GQ_ERR_NULL;
+    if (x && ((reinterpret_cast<uintptr_t>(x) & 15) != 0)) return GQ_ERR_ALIGN;
+    return run_matmul(wtype, W, x, nullptr, sums, rows, cols, batch, GQ_PATH_GEMV, 0, true, stream);
 }
 
 int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }

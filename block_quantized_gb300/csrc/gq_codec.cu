@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict
                                                          int64_t nblocks) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_launch_dependents();  // dependents still wait for this grid's completion
     pdl_wait();
     for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
          b += warps) {
@@ -70,7 +71,6 @@ __global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict
             if (lane == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(dh);
         }
     }
-    pdl_launch_dependents();
 }
 
 // Q8_K: 256 elements, fp32 scale d = max|x| / 127, eight int16 sub-block sums.
@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(256) quantize_q8_k_kernel(const float *__restr
                                                             int64_t nblocks) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_launch_dependents();  // dependents still wait for this grid's completion
     pdl_wait();
     for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
          b += warps) {
@@ -114,7 +115,6 @@ __global__ void __launch_bounds__(256) quantize_q8_k_kernel(const float *__restr
             *reinterpret_cast<int16_t *>(blk + 260 + 2 * (lane >> 2)) = (int16_t)sum;
         if (lane == 0) *reinterpret_cast<float *>(blk) = d;
     }
-    pdl_launch_dependents();
 }
 
 // Q4_K: per 32-element sub-block j (lanes 4j..4j+3):
@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(256) quantize_q4_k_kernel(const float *__restr
                                                             int64_t nblocks) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_launch_dependents();  // dependents still wait for this grid's completion
     pdl_wait();
     for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
          b += warps) {
@@ -202,7 +203,6 @@ __global__ void __launch_bounds__(256) quantize_q4_k_kernel(const float *__restr
             hdr[3] = w[2];
         }
     }
-    pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------ decoders
@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(256) quantize_q4_k_kernel(const float *__restr
 
 __global__ void dequantize_kernel(int type, const uint8_t *__restrict__ src,
                                   float *__restrict__ dst, int64_t n) {
+    pdl_launch_dependents();  // dependents still wait for this grid's completion
     pdl_wait();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
@@ -247,7 +248,6 @@ __global__ void dequantize_kernel(int type, const uint8_t *__restrict__ src,
         }
         dst[e] = out;
     }
-    pdl_launch_dependents();
 }
 
 int grid_for(int64_t work_items, int per_cta, int num_sms) {

@@ -4,25 +4,27 @@
 // The per-block integer dot of "llama.cpp 推理引擎" (runguoli.com) §6.4 --
 // low nibble of byte j pairs with activation 2j, high nibble with 2j+1, the
 // block offset of 8 is applied to the integer sum, and the block scales
-// multiply the integer result -- done with __dp4a on int8 activations, and
-// the two-level Q4_K scales of §5.5 applied per 32-element sub-block in
+// multiply the integer result -- done with __dp4a on int8 activations; the
+// two-level Q4_K scales of §5.5 are applied per 32-element sub-block in
 // integers (sc_j * s_j, m_j * t_j) before one float scaling per super-block.
-// Decode is bandwidth-bound ("llama.cpp 推理引擎" §7.3: token generation is
-// limited by memory bandwidth), so the design goal is streaming the weights
-// once at HBM speed:
-//   - one warp per weight row, eight rows per 256-thread CTA;
-//   - the CTA's activation vectors are staged once in shared memory, with
-//     each group of 8 int8 codes stored as (a0,a2,a4,a6 | a1,a3,a5,a7) so a
-//     packed nibble word w feeds dp4a directly as (w & 0x0F0F0F0F) and
-//     ((w >> 4) & 0x0F0F0F0F);
-//   - Q4_K rows (144-byte blocks, 16-byte aligned) are read with 128-bit
-//     non-allocating global loads, issued for the whole first part of the
-//     row before the activation staging so the two latencies overlap;
-//   - Q4_0 / Q8_0 rows (18 / 34-byte blocks, only 2-byte aligned) are moved
-//     into shared memory by the TMA engine (cp.async.bulk, 16-byte aligned
-//     chunks of 64 blocks, two stages per warp) and unaligned blocks are
-//     read from there with funnel shifts;
-//   - warp-shuffle reduction of the per-lane partial sums.
+// Token generation is bound by memory bandwidth ("llama.cpp 推理引擎" §7.3),
+// so the kernels are built to stream the weights once at HBM speed:
+//   - every warp owns whole rows (grid-stride over rows, a persistent grid
+//     of a few CTAs per SM for tall matrices) and streams each row through
+//     its own two-stage shared-memory ring, filled by the TMA engine
+//     (cp.async.bulk, ~2.3 KB chunks, completion on an mbarrier; every wait
+//     is bounded);
+//   - the CTA's activation vectors are staged once in shared memory, each
+//     group of 8 int8 codes stored as (a0,a2,a4,a6 | a1,a3,a5,a7) so a
+//     packed nibble word w feeds dp4a as (w & 0x0F0F0F0F) and
+//     ((w >> 4) & 0x0F0F0F0F); the fused variants quantize fp32
+//     activations straight into that layout (same arithmetic as the
+//     standalone quantizer, so the codes are identical);
+//   - Q4_0 / Q8_0 blocks (18 / 34 bytes, 2-byte aligned) are read from the
+//     ring with aligned 32-bit loads and funnel shifts;
+//   - per-lane fp32 partial sums, one warp-shuffle reduction per row.
+#include <algorithm>
+
 #include "gq_common.cuh"
 #include "gq_internal.h"
 
@@ -30,209 +32,154 @@ namespace gq {
 namespace {
 
 constexpr uint32_t NIB = 0x0F0F0F0Fu;
-constexpr int WARPS = 8;  // rows per CTA
+constexpr unsigned FULL = 0xffffffffu;
+// Launch-shape parameters (compile-time; the defaults are the measured best).
+#ifndef GQ_GEMV_NSTAGE
+#define GQ_GEMV_NSTAGE 2
+#endif
+#ifndef GQ_GEMV_ROWS_PER_WARP
+#define GQ_GEMV_ROWS_PER_WARP 2
+#endif
+#ifndef GQ_GEMV_CTAS_PER_SM
+#define GQ_GEMV_CTAS_PER_SM 4
+#endif
+#ifndef GQ_GEMV_Q4K_CHUNK
+#define GQ_GEMV_Q4K_CHUNK 16
+#endif
+#ifndef GQ_GEMV_EARLY_TRIGGER
+#define GQ_GEMV_EARLY_TRIGGER 0
+#endif
 
-// ---------------------------------------------------------------- Q4_K x Q8_K
+constexpr int WARPS = 8;                  // warps per CTA
+constexpr int NSTAGE = GQ_GEMV_NSTAGE;    // ring stages per warp
 
-// Activation staging for Q8_K: per vector and super-block, 256 code bytes in
-// the (even | odd) order, then the fp32 scale and the eight int32 sums.
-struct ActK {
-    uint8_t *codes;  // [nb][nsb][256]
-    float *dx;       // [nb][nsb]
-    int32_t *bsum;   // [nb][nsb][8]
+// Weight formats as seen by the streaming kernel: block bytes, elements per
+// block, and blocks per ring chunk (chunks are 16-byte multiples).
+template <int WT>
+struct Fmt;
+template <>
+struct Fmt<GQ_Q4_0> {
+    static constexpr int BB = Q4_0_BYTES, BE = 32, CH = 128;  // 2304-byte chunks
+};
+template <>
+struct Fmt<GQ_Q8_0> {
+    static constexpr int BB = Q8_0_BYTES, BE = 32, CH = 64;  // 2176-byte chunks
+};
+template <>
+struct Fmt<GQ_Q4_K> {
+    static constexpr int BB = Q4_K_BYTES, BE = 256, CH = GQ_GEMV_Q4K_CHUNK;  // 2304-byte chunks
 };
 
-__device__ __forceinline__ ActK act_k_layout(uint8_t *smem, int nb, int nsb) {
-    ActK a;
-    a.codes = smem;
-    a.dx = reinterpret_cast<float *>(smem + (size_t)nb * nsb * 256);
-    a.bsum = reinterpret_cast<int32_t *>(a.dx + (size_t)nb * nsb);
+template <int WT>
+struct Ring {
+    static constexpr int CHUNK = Fmt<WT>::CH * Fmt<WT>::BB;
+    static constexpr int BUF = ((CHUNK + 16 + 15) / 16) * 16;  // +16: over-read slack
+    // WARPS * NSTAGE mbarriers of 8 bytes come first, then the ring buffers
+    static constexpr int BARS_BYTES = WARPS * NSTAGE * 8;
+    static constexpr int BUFS_OFF = ((BARS_BYTES + 127) / 128) * 128;
+    static_assert(BUFS_OFF >= BARS_BYTES, "mbarriers must not overlap the ring");
+    static_assert(BUFS_OFF % 16 == 0 && BUF % 16 == 0, "bulk-copy destinations are 16-byte aligned");
+    static constexpr int ACT_OFF = BUFS_OFF + WARPS * NSTAGE * BUF;
+};
+
+// Staged activations.  Q8_K (for Q4_K weights): per vector and super-block
+// 256 code bytes, the fp32 scale and the eight sub-block sums.  Q8_0 (for
+// Q4_0 / Q8_0 weights): per vector and block 32 code bytes, the scale as
+// fp32 and the sum of the 32 codes (for the Q4_0 offset of 8).
+struct Act {
+    uint8_t *codes;
+    float *dx;
+    int32_t *isum;
+};
+
+template <int WT>
+__host__ __device__ constexpr int act_block_bytes() {
+    return WT == GQ_Q4_K ? 256 + 4 + 32 : 32 + 4 + 4;
+}
+
+template <int WT>
+__device__ __forceinline__ Act act_layout(uint8_t *base, int nb, int nblk) {
+    constexpr int CB = WT == GQ_Q4_K ? 256 : 32;
+    Act a;
+    a.codes = base;
+    a.dx = reinterpret_cast<float *>(base + (size_t)nb * nblk * CB);
+    a.isum = reinterpret_cast<int32_t *>(a.dx + (size_t)nb * nblk);
     return a;
 }
 
-__device__ __forceinline__ void stage_q8_k(const ActK &a, const uint8_t *__restrict__ xq,
-                                           int nvec, int nsb) {
-    const int groups = nvec * nsb * 32;
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
-        const int blk = g >> 5, k = g & 31;
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + (size_t)blk * Q8_K_BYTES + 4 + 8 * k);
-        const uint32_t a0 = __ldg(src), a1 = __ldg(src + 1);
-        uint2 v;
-        v.x = __byte_perm(a0, a1, 0x6420);
-        v.y = __byte_perm(a0, a1, 0x7531);
-        reinterpret_cast<uint2 *>(a.codes + (size_t)blk * 256)[k] = v;
-    }
-    for (int blk = threadIdx.x; blk < nvec * nsb; blk += blockDim.x) {
-        const uint8_t *src = xq + (size_t)blk * Q8_K_BYTES;
-        a.dx[blk] = __ldg(reinterpret_cast<const float *>(src));
-        const uint32_t *bs = reinterpret_cast<const uint32_t *>(src + 260);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w = __ldg(bs + i);
-            a.bsum[blk * 8 + 2 * i] = (int32_t)(int16_t)(w & 0xffffu);
-            a.bsum[blk * 8 + 2 * i + 1] = (int32_t)(int16_t)(w >> 16);
-        }
-    }
+__device__ __forceinline__ uint2 split8(uint32_t a0, uint32_t a1) {
+    return make_uint2(__byte_perm(a0, a1, 0x6420), __byte_perm(a0, a1, 0x7531));
 }
 
-// Sub-block factors of a Q4_K block header (bytes 0..15 as four words).
-__device__ __forceinline__ void q4k_factors(const uint4 &h, int j, int &sc, int &m) {
-    const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);  // header bits 32..95
-    const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);  // header bits 64..127
-    sc = (int)((lo64 >> (6 * j)) & 63);
-    m = (int)((hi64 >> (6 * j + 16)) & 63);
-}
+// ---- unfused staging: copy quantized activation blocks into the layout.
+// All loads of a pass are issued before any store, so a pass costs one
+// L2 round trip.
 
-// One lane = one 32-element sub-block j = lane & 7 of super-block
-// 4 * iteration + (lane >> 3); a warp covers four super-blocks (576
-// contiguous bytes) per iteration.  U iterations are kept in flight.
-template <int NB, bool SUMS>
-__global__ void __launch_bounds__(256) gemv_q4_k_kernel(const uint8_t *__restrict__ W,
-                                                        const uint8_t *__restrict__ xq,
-                                                        float *__restrict__ y,
-                                                        int32_t *__restrict__ sums, int rows,
-                                                        int nsb, int batch) {
-    constexpr int U = 4;
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * WARPS + warp;
-    const int b0 = blockIdx.y * NB;
-    const int nvec = min(NB, batch - b0);
-    const int j = lane & 7, sbl = lane >> 3;
-    const int iters = (nsb + 3) >> 2;
-    const bool active = row < rows;
-    const uint8_t *wrow = W + (size_t)(active ? row : 0) * nsb * Q4_K_BYTES;
-
-    uint4 hdr[U], qs[U];
+__device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nblocks) {
+    const int groups = nblocks * 32;
+    // pass p copies groups [4p*T, 4(p+1)*T) and block headers [p*T, (p+1)*T)
+    // (T = blockDim.x); there are at least as many group passes as header
+    // passes since every block has 32 groups.
+    int pass = 0;
+    for (int base = 0; base < groups; base += 4 * blockDim.x, ++pass) {
+        uint32_t w0[4], w1[4], hd[5];
+        const int hb = pass * blockDim.x + threadIdx.x;
+        const bool has_h = hb < nblocks;
+        if (has_h) {
+            const uint8_t *src = xq + (size_t)hb * Q8_K_BYTES;
+            hd[0] = __ldg(reinterpret_cast<const uint32_t *>(src));
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int sb = 4 * u + sbl;
-        if (active && u < iters && sb < nsb) {
-            hdr[u] = ldg_nc_v4(wrow + (size_t)sb * Q4_K_BYTES);
-            qs[u] = ldg_nc_v4(wrow + (size_t)sb * Q4_K_BYTES + 16 + 16 * j);
+            for (int i = 0; i < 4; ++i) hd[1 + i] = __ldg(reinterpret_cast<const uint32_t *>(src + 260) + i);
         }
-    }
-
-    const ActK act = act_k_layout(smem, NB, nsb);
-    pdl_wait();  // activations may come from the preceding kernel
-    stage_q8_k(act, xq + (size_t)b0 * nsb * Q8_K_BYTES, nvec, nsb);
-    __syncthreads();
-    pdl_launch_dependents();
-    if (!active) return;
-
-    float acc[NB];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
-
-    for (int it0 = 0; it0 < iters; it0 += U) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int it = it0 + u;
-            const int sb = 4 * it + sbl;
-            if (it < iters && sb < nsb) {
-                const uint32_t lo0 = qs[u].x & NIB, hi0 = (qs[u].x >> 4) & NIB;
-                const uint32_t lo1 = qs[u].y & NIB, hi1 = (qs[u].y >> 4) & NIB;
-                const uint32_t lo2 = qs[u].z & NIB, hi2 = (qs[u].z >> 4) & NIB;
-                const uint32_t lo3 = qs[u].w & NIB, hi3 = (qs[u].w >> 4) & NIB;
-                int sc, m;
-                q4k_factors(hdr[u], j, sc, m);
-                const float d = half_bits_to_float(hdr[u].x);
-                const float dmin = half_bits_to_float(hdr[u].x >> 16);
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (b < nvec) {
-                        const int blk = b * nsb + sb;
-                        const int4 *ap = reinterpret_cast<const int4 *>(act.codes + (size_t)blk * 256 + 32 * j);
-                        const int4 a0 = ap[0], a1 = ap[1];
-                        int s = 0;
-                        s = dp4a((int)lo0, a0.x, s);
-                        s = dp4a((int)hi0, a0.y, s);
-                        s = dp4a((int)lo1, a0.z, s);
-                        s = dp4a((int)hi1, a0.w, s);
-                        s = dp4a((int)lo2, a1.x, s);
-                        s = dp4a((int)hi2, a1.y, s);
-                        s = dp4a((int)lo3, a1.z, s);
-                        s = dp4a((int)hi3, a1.w, s);
-                        const int t = act.bsum[blk * 8 + j];
-                        int is1 = sc * s, is2 = m * t;
-                        if (SUMS) {
-                            // lanes of super-blocks that exist in this iteration
-                            const int cnt = min(4, nsb - 4 * it);
-                            const unsigned gmask = 0xffffffffu >> (32 - 8 * cnt);
-#pragma unroll
-                            for (int o = 1; o < 8; o <<= 1) {
-                                is1 += __shfl_xor_sync(gmask, is1, o);
-                                is2 += __shfl_xor_sync(gmask, is2, o);
-                            }
-                            if (j == 0) {
-                                int32_t *o = sums + (((size_t)(b0 + b) * rows + row) * nsb + sb) * 2;
-                                o[0] = is1;
-                                o[1] = is2;
-                            }
-                        } else {
-                            acc[b] += act.dx[blk] * (d * (float)is1 - dmin * (float)is2);
-                        }
-                    }
-                }
-                // refill this slot with the iteration U ahead
-                const int itn = it + U, sbn = 4 * itn + sbl;
-                if (itn < iters && sbn < nsb) {
-                    hdr[u] = ldg_nc_v4(wrow + (size_t)sbn * Q4_K_BYTES);
-                    qs[u] = ldg_nc_v4(wrow + (size_t)sbn * Q4_K_BYTES + 16 + 16 * j);
-                }
+        for (int u = 0; u < 4; ++u) {
+            const int g = base + u * blockDim.x + threadIdx.x;
+            if (g < groups) {
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(
+                    xq + (size_t)(g >> 5) * Q8_K_BYTES + 4 + 8 * (g & 31));
+                w0[u] = __ldg(src);
+                w1[u] = __ldg(src + 1);
             }
         }
-    }
-    if (!SUMS) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if (b < nvec) {
-                const float v = warp_sum(acc[b]);
-                if (lane == 0) y[(size_t)(b0 + b) * rows + row] = v;
+        for (int u = 0; u < 4; ++u) {
+            const int g = base + u * blockDim.x + threadIdx.x;
+            if (g < groups) reinterpret_cast<uint2 *>(a.codes)[g] = split8(w0[u], w1[u]);
+        }
+        if (has_h) {
+            a.dx[hb] = __uint_as_float(hd[0]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                a.isum[hb * 8 + 2 * i] = (int32_t)(int16_t)(hd[1 + i] & 0xffffu);
+                a.isum[hb * 8 + 2 * i + 1] = (int32_t)(int16_t)(hd[1 + i] >> 16);
             }
         }
     }
 }
 
-// ------------------------------------------------------- Q4_0 / Q8_0 x Q8_0
-
-constexpr int CH_BLOCKS = 64;  // blocks per TMA chunk
-
-struct Act0 {
-    uint8_t *codes;  // [nb][nblk][32]
-    float *dx;       // [nb][nblk]
-    int32_t *asum;   // [nb][nblk]  (sum of the 32 codes, for the Q4_0 offset)
-};
-
-__device__ __forceinline__ Act0 act_0_layout(uint8_t *smem, int nb, int nblk) {
-    Act0 a;
-    a.codes = smem;
-    a.dx = reinterpret_cast<float *>(smem + (size_t)nb * nblk * 32);
-    a.asum = reinterpret_cast<int32_t *>(a.dx + (size_t)nb * nblk);
-    return a;
-}
-
-// SPLIT: store each group of 8 codes as (even | odd) for nibble weights.
 template <bool SPLIT>
-__device__ __forceinline__ void stage_q8_0(const Act0 &a, const uint8_t *__restrict__ xq, int nvec,
-                                           int nblk) {
-    for (int blk = threadIdx.x; blk < nvec * nblk; blk += blockDim.x) {
+__device__ void stage_q8_0(const Act &a, const uint8_t *__restrict__ xq, int nblocks) {
+    for (int base = 0; base < nblocks; base += blockDim.x) {
+        const int blk = base + threadIdx.x;
+        if (blk >= nblocks) continue;
         const uint16_t *src = reinterpret_cast<const uint16_t *>(xq + (size_t)blk * Q8_0_BYTES);
-        a.dx[blk] = half_bits_to_float(__ldg(src));
+        uint32_t h[17];
+#pragma unroll
+        for (int i = 0; i < 17; ++i) h[i] = __ldg(src + i);
         uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = (uint32_t)__ldg(src + 1 + 2 * i) | ((uint32_t)__ldg(src + 2 + 2 * i) << 16);
+        for (int i = 0; i < 8; ++i) w[i] = h[1 + 2 * i] | (h[2 + 2 * i] << 16);
         int s = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) s = dp4a((int)w[i], 0x01010101, s);
-        a.asum[blk] = s;
+        a.isum[blk] = s;
+        a.dx[blk] = half_bits_to_float(h[0]);
         uint4 *dst = reinterpret_cast<uint4 *>(a.codes + (size_t)blk * 32);
         if (SPLIT) {
-            dst[0] = make_uint4(__byte_perm(w[0], w[1], 0x6420), __byte_perm(w[0], w[1], 0x7531),
-                                __byte_perm(w[2], w[3], 0x6420), __byte_perm(w[2], w[3], 0x7531));
-            dst[1] = make_uint4(__byte_perm(w[4], w[5], 0x6420), __byte_perm(w[4], w[5], 0x7531),
-                                __byte_perm(w[6], w[7], 0x6420), __byte_perm(w[6], w[7], 0x7531));
+            const uint2 p0 = split8(w[0], w[1]), p1 = split8(w[2], w[3]);
+            const uint2 p2 = split8(w[4], w[5]), p3 = split8(w[6], w[7]);
+            dst[0] = make_uint4(p0.x, p0.y, p1.x, p1.y);
+            dst[1] = make_uint4(p2.x, p2.y, p3.x, p3.y);
         } else {
             dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
             dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -240,148 +187,340 @@ __device__ __forceinline__ void stage_q8_0(const Act0 &a, const uint8_t *__restr
     }
 }
 
-// Integer dot of the weight block that starts `off` bytes into a 4-byte
-// aligned shared-memory chunk with the staged activation block `ap`.
-template <bool Q4>
-__device__ __forceinline__ int block_dot_smem(const uint8_t *chunk, int off, const int4 *ap,
-                                              int asum, float &dw) {
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(chunk + (off & ~3));
-    const uint32_t sh = (off & 2) ? 32u : 16u;  // code bytes start 2 or 4 bytes into w[0]
-    const int4 a0 = ap[0], a1 = ap[1];
-    if (Q4) {
-        uint32_t v[5];
+// ---- fused staging: quantize fp32 activations straight into the layout.
+// Same operations, in the same order, as the standalone Q8_K / Q8_0
+// quantizers (round-to-nearest division, roundf, fp16 round-to-nearest for
+// the Q8_0 scale), so the codes equal theirs bit for bit.
+
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-        for (int i = 0; i < 5; ++i) v[i] = w[i];
-        dw = half_bits_to_float((off & 2) ? (v[0] >> 16) : v[0]);
-        const uint32_t c0 = __funnelshift_rc(v[0], v[1], sh), c1 = __funnelshift_rc(v[1], v[2], sh);
-        const uint32_t c2 = __funnelshift_rc(v[2], v[3], sh), c3 = __funnelshift_rc(v[3], v[4], sh);
-        int s = 0;
-        s = dp4a((int)(c0 & NIB), a0.x, s);
-        s = dp4a((int)((c0 >> 4) & NIB), a0.y, s);
-        s = dp4a((int)(c1 & NIB), a0.z, s);
-        s = dp4a((int)((c1 >> 4) & NIB), a0.w, s);
-        s = dp4a((int)(c2 & NIB), a1.x, s);
-        s = dp4a((int)((c2 >> 4) & NIB), a1.y, s);
-        s = dp4a((int)(c3 & NIB), a1.z, s);
-        s = dp4a((int)((c3 >> 4) & NIB), a1.w, s);
-        return s - 8 * asum;
-    } else {
-        uint32_t v[9];
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float clamp127(float v) {
+    return v < -127.0f ? -127.0f : (v > 127.0f ? 127.0f : v);
+}
+
+// Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
+// (= code group l of the layout).
+__device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b0 = warp; b0 < nblocks; b0 += 2 * WARPS) {
+        float4 v[2][2];
 #pragma unroll
-        for (int i = 0; i < 9; ++i) v[i] = w[i];
-        dw = half_bits_to_float((off & 2) ? (v[0] >> 16) : v[0]);
-        int s = 0;
-        s = dp4a((int)__funnelshift_rc(v[0], v[1], sh), a0.x, s);
-        s = dp4a((int)__funnelshift_rc(v[1], v[2], sh), a0.y, s);
-        s = dp4a((int)__funnelshift_rc(v[2], v[3], sh), a0.z, s);
-        s = dp4a((int)__funnelshift_rc(v[3], v[4], sh), a0.w, s);
-        s = dp4a((int)__funnelshift_rc(v[4], v[5], sh), a1.x, s);
-        s = dp4a((int)__funnelshift_rc(v[5], v[6], sh), a1.y, s);
-        s = dp4a((int)__funnelshift_rc(v[6], v[7], sh), a1.z, s);
-        s = dp4a((int)__funnelshift_rc(v[7], v[8], sh), a1.w, s);
-        return s;
+        for (int u = 0; u < 2; ++u) {
+            const int blk = b0 + u * WARPS;
+            if (blk < nblocks) {
+                const float4 *p = reinterpret_cast<const float4 *>(x + (size_t)blk * QK_K + 8 * lane);
+                v[u][0] = __ldg(p);
+                v[u][1] = __ldg(p + 1);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int blk = b0 + u * WARPS;
+            if (blk >= nblocks) break;  // warp-uniform
+            const float e[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                                v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(e[i]));
+            amax = warp_max(amax);
+            const float d = __fdiv_rn(amax, 127.0f);
+            uint32_t w0 = 0, w1 = 0;
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float q = (d == 0.0f) ? 0.0f : clamp127(roundf(__fdiv_rn(e[i], d)));
+                const int qi = (int)q;
+                sum += qi;
+                if (i < 4)
+                    w0 |= (uint32_t)(qi & 0xff) << (8 * i);
+                else
+                    w1 |= (uint32_t)(qi & 0xff) << (8 * (i - 4));
+            }
+            reinterpret_cast<uint2 *>(a.codes)[(size_t)blk * 32 + lane] = split8(w0, w1);
+            sum += __shfl_xor_sync(FULL, sum, 1);
+            sum += __shfl_xor_sync(FULL, sum, 2);
+            if ((lane & 3) == 0) a.isum[blk * 8 + (lane >> 2)] = sum;
+            if (lane == 0) a.dx[blk] = d;
+        }
     }
 }
 
-// Shared memory of the Q4_0 / Q8_0 kernel: per warp two chunk buffers (plus
-// 16 bytes of slack for the last block's over-read) and two mbarriers, then
-// the staged activations.
-template <int BB>
-struct ChunkLayout {
-    static constexpr int CHUNK_BYTES = CH_BLOCKS * BB;
-    static constexpr int BUF = ((CHUNK_BYTES + 16 + 15) / 16) * 16;
-    static constexpr int PER_WARP = 2 * BUF;
-    static constexpr int BARS_OFF = WARPS * PER_WARP;
-    static constexpr int ACT_OFF = BARS_OFF + WARPS * 2 * 8;
-};
-
-template <bool Q4, int NB, bool SUMS>
-__global__ void __launch_bounds__(256) gemv_q_0_kernel(const uint8_t *__restrict__ W,
-                                                       const uint8_t *__restrict__ xq,
-                                                       float *__restrict__ y,
-                                                       int32_t *__restrict__ sums, int rows,
-                                                       int nblk, int batch,
-                                                       uint32_t *__restrict__ status) {
-    constexpr int BB = Q4 ? Q4_0_BYTES : Q8_0_BYTES;
-    using L = ChunkLayout<BB>;
-    extern __shared__ __align__(16) uint8_t smem[];
+// Q8_0: one warp per 32-element block, lane = element.
+template <bool SPLIT>
+__device__ void quant_stage_q8_0(const Act &a, const float *__restrict__ x, int nblocks) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * WARPS + warp;
+    // position of this lane's code in the staged block
+    const int e = lane & 7;
+    const int pos = SPLIT ? ((lane & ~7) | ((e & 1) ? 4 + (e >> 1) : (e >> 1))) : lane;
+    for (int b0 = warp; b0 < nblocks; b0 += 8 * WARPS) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int blk = b0 + u * WARPS;
+            v[u] = blk < nblocks ? __ldg(x + (size_t)blk * 32 + lane) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int blk = b0 + u * WARPS;
+            if (blk >= nblocks) break;  // warp-uniform
+            const float amax = warp_max(fabsf(v[u]));
+            const float d = __half2float(__float2half_rn(__fdiv_rn(amax, 127.0f)));
+            const float q = (d == 0.0f) ? 0.0f : clamp127(roundf(__fdiv_rn(v[u], d)));
+            int qi = (int)q;
+            a.codes[(size_t)blk * 32 + pos] = (uint8_t)(qi & 0xff);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) qi += __shfl_xor_sync(FULL, qi, o);
+            if (lane == 0) {
+                a.isum[blk] = qi;
+                a.dx[blk] = d;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------ chunk compute
+
+// Sub-block factors of a Q4_K block header (bytes 0..15 as four words): the
+// sixteen 6-bit fields sit LSB-first in header bits 32..127.
+__device__ __forceinline__ void q4k_factors(const uint4 &h, int j, int &sc, int &m) {
+    const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);  // header bits 32..95
+    const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);  // header bits 64..127
+    sc = (int)((lo64 >> (6 * j)) & 63);
+    m = (int)((hi64 >> (6 * j + 16)) & 63);
+}
+
+// Q4_K chunk of nb_c super-blocks starting at super-block sb0 of the row.
+// Lane = sub-block j = lane & 7 of super-block 4t + (lane >> 3).
+// sums (diagnostic) points at [b = 0][row][sb = 0][0] with stride bstride
+// between vectors.
+template <int NB, bool SUMS>
+__device__ __forceinline__ void chunk_q4_k(const uint8_t *ch, int nb_c, int sb0, int nsb,
+                                           const Act &a, int nvec, float (&acc)[NB],
+                                           int32_t *sums, size_t bstride, int lane) {
+    const int j = lane & 7, sbl = lane >> 3;
+#pragma unroll
+    for (int t = 0; t < Fmt<GQ_Q4_K>::CH / 4; ++t) {
+        if (4 * t >= nb_c) break;  // warp-uniform
+        const int sl = 4 * t + sbl;
+        if (sl < nb_c) {
+            const uint4 h = *reinterpret_cast<const uint4 *>(ch + sl * Q4_K_BYTES);
+            const uint4 q = *reinterpret_cast<const uint4 *>(ch + sl * Q4_K_BYTES + 16 + 16 * j);
+            const int lo0 = (int)(q.x & NIB), hi0 = (int)((q.x >> 4) & NIB);
+            const int lo1 = (int)(q.y & NIB), hi1 = (int)((q.y >> 4) & NIB);
+            const int lo2 = (int)(q.z & NIB), hi2 = (int)((q.z >> 4) & NIB);
+            const int lo3 = (int)(q.w & NIB), hi3 = (int)((q.w >> 4) & NIB);
+            int sc, m;
+            q4k_factors(h, j, sc, m);
+            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
+            const int sb = sb0 + sl;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (b >= nvec) break;
+                const int blk = b * nsb + sb;
+                const int4 *ap = reinterpret_cast<const int4 *>(a.codes + (size_t)blk * 256 + 32 * j);
+                const int4 a0 = ap[0], a1 = ap[1];
+                int s = dp4a(lo0, a0.x, 0);
+                s = dp4a(hi0, a0.y, s);
+                s = dp4a(lo1, a0.z, s);
+                s = dp4a(hi1, a0.w, s);
+                s = dp4a(lo2, a1.x, s);
+                s = dp4a(hi2, a1.y, s);
+                s = dp4a(lo3, a1.z, s);
+                s = dp4a(hi3, a1.w, s);
+                int is1 = sc * s, is2 = m * a.isum[blk * 8 + j];
+                if (SUMS) {
+                    const int cnt = min(4, nb_c - 4 * t);  // super-blocks present in this step
+                    const unsigned gmask = FULL >> (32 - 8 * cnt);
+#pragma unroll
+                    for (int o = 1; o < 8; o <<= 1) {
+                        is1 += __shfl_xor_sync(gmask, is1, o);
+                        is2 += __shfl_xor_sync(gmask, is2, o);
+                    }
+                    if (j == 0) {
+                        int32_t *o = sums + b * bstride + (size_t)sb * 2;
+                        o[0] = is1;
+                        o[1] = is2;
+                    }
+                } else {
+                    acc[b] += a.dx[blk] * (d * (float)is1 - dmin * (float)is2);
+                }
+            }
+        }
+    }
+}
+
+// Q4_0 / Q8_0 chunk of nb_c blocks starting at block blk0 of the row; lane k
+// takes blocks k, k + 32, ...  A block starting `off` bytes into the chunk is
+// read as aligned words from off & ~3; its code bytes begin 2 or 4 bytes into
+// the first word, so funnel shifts by 16 or 32 (clamped) realign them.
+template <int WT, int NB, bool SUMS>
+__device__ __forceinline__ void chunk_q_0(const uint8_t *ch, int nb_c, int blk0, int nblk,
+                                          const Act &a, int nvec, float (&acc)[NB],
+                                          int32_t *sums, size_t bstride, int lane) {
+    constexpr bool Q4 = WT == GQ_Q4_0;
+    constexpr int BB = Fmt<WT>::BB;
+    constexpr int PER = Fmt<WT>::CH / 32;
+#pragma unroll
+    for (int hh = 0; hh < PER; ++hh) {
+        const int k = lane + 32 * hh;
+        if (k >= nb_c) break;
+        const int off = k * BB;
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(ch + (off & ~3));
+        const uint32_t sh = (off & 2) ? 32u : 16u;
+        constexpr int NW = Q4 ? 5 : 9;
+        uint32_t v[NW];
+#pragma unroll
+        for (int i = 0; i < NW; ++i) v[i] = w[i];
+        const float dw = half_bits_to_float((off & 2) ? (v[0] >> 16) : v[0]);
+        int wl[8];  // dp4a operands in activation-layout order
+        if (Q4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t c = __funnelshift_rc(v[i], v[i + 1], sh);
+                wl[2 * i] = (int)(c & NIB);
+                wl[2 * i + 1] = (int)((c >> 4) & NIB);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) wl[i] = (int)__funnelshift_rc(v[i], v[i + 1], sh);
+        }
+        const int blk = blk0 + k;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (b >= nvec) break;
+            const int ab = b * nblk + blk;
+            const int4 *ap = reinterpret_cast<const int4 *>(a.codes + (size_t)ab * 32);
+            const int4 a0 = ap[0], a1 = ap[1];
+            int s = dp4a(wl[0], a0.x, 0);
+            s = dp4a(wl[1], a0.y, s);
+            s = dp4a(wl[2], a0.z, s);
+            s = dp4a(wl[3], a0.w, s);
+            s = dp4a(wl[4], a1.x, s);
+            s = dp4a(wl[5], a1.y, s);
+            s = dp4a(wl[6], a1.z, s);
+            s = dp4a(wl[7], a1.w, s);
+            if (Q4) s -= 8 * a.isum[ab];
+            if (SUMS)
+                sums[b * bstride + blk] = s;
+            else
+                acc[b] += dw * a.dx[ab] * (float)s;
+        }
+    }
+}
+
+// ------------------------------------------------------------- the kernel
+
+// One launch covers NB activation vectors (blockIdx.y selects the chunk of
+// vectors) and all rows.  FUSED: `act` is fp32 [batch][cols] and is
+// quantized in the CTA; otherwise `act` holds the quantized blocks.
+// w_static != 0 lets the first weight chunks be requested before the
+// dependency wait on the preceding kernel (the caller guarantees no kernel
+// still in flight writes W).
+template <int WT, int NB, bool SUMS, bool FUSED>
+__global__ void __launch_bounds__(256) gemv_kernel(const uint8_t *__restrict__ W,
+                                                   const void *__restrict__ act_in,
+                                                   float *__restrict__ y,
+                                                   int32_t *__restrict__ sums, int rows,
+                                                   int nblk, int batch, int w_static,
+                                                   uint32_t *__restrict__ status) {
+    using F = Fmt<WT>;
+    using R = Ring<WT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b0 = blockIdx.y * NB;
     const int nvec = min(NB, batch - b0);
-    const bool active = row < rows;
-    const int nchunks = (nblk + CH_BLOCKS - 1) / CH_BLOCKS;
-    uint8_t *buf = smem + warp * L::PER_WARP;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::BARS_OFF) + 2 * warp;
-    const uint8_t *wrow = W + (size_t)(active ? row : 0) * nblk * BB;
+    const int warps_total = gridDim.x * WARPS;
+    const int wg = blockIdx.x * WARPS + warp;
+    const int nrows_w = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
+    const int nchunk = (nblk + F::CH - 1) / F::CH;
+    const int total = nrows_w * nchunk;
+    const size_t row_bytes = (size_t)nblk * F::BB;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * NSTAGE;
+    uint8_t *ring = smem + R::BUFS_OFF + warp * NSTAGE * R::BUF;
 
-    auto issue = [&](int c) {
-        const int nb_c = min(CH_BLOCKS, nblk - c * CH_BLOCKS);
-        const uint32_t bytes = (uint32_t)(nb_c * BB);
-        uint64_t *b = bar + (c & 1);
-        mbar_arrive_expect_tx(b, bytes);
-        bulk_g2s(buf + (c & 1) * L::BUF, wrow + (size_t)c * CH_BLOCKS * BB, bytes, b);
+    // item i of this warp = chunk (i % nchunk) of its (i / nchunk)-th row
+    auto issue = [&](int i) {
+        const int row = wg + (i / nchunk) * warps_total;
+        const int c = i % nchunk;
+        const int nb_c = min(F::CH, nblk - c * F::CH);
+        const uint32_t bytes = (uint32_t)(nb_c * F::BB);
+        const int st = i % NSTAGE;
+        mbar_arrive_expect_tx(bar + st, bytes);
+        bulk_g2s(ring + st * R::BUF, W + row * row_bytes + (size_t)c * F::CH * F::BB, bytes, bar + st);
     };
 
-    if (active && lane == 0) {
-        mbar_init(bar, 1);
-        mbar_init(bar + 1, 1);
+    // With the early trigger the next kernel in the stream may launch right
+    // away (its CTAs wait on griddepcontrol.wait before touching anything this
+    // kernel produces); otherwise it launches once this kernel's activations
+    // are staged.
+    if (GQ_GEMV_EARLY_TRIGGER) pdl_launch_dependents();
+    if (lane == 0 && total > 0) {
+#pragma unroll
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(bar + s, 1);
         fence_mbar_init();
-        issue(0);
-        if (nchunks > 1) issue(1);
+        if (w_static)
+            for (int i = 0; i < NSTAGE && i < total; ++i) issue(i);
     }
+    pdl_wait();  // activations (and, unless static, W) may come from the preceding kernel
+    if (lane == 0 && !w_static)
+        for (int i = 0; i < NSTAGE && i < total; ++i) issue(i);
 
-    const Act0 act = act_0_layout(smem + L::ACT_OFF, NB, nblk);
-    pdl_wait();
-    stage_q8_0<Q4>(act, xq + (size_t)b0 * nblk * Q8_0_BYTES, nvec, nblk);
+    const Act a = act_layout<WT>(smem + R::ACT_OFF, NB, nblk);
+    const int nact = nvec * nblk;
+    if (FUSED) {
+        const float *x = static_cast<const float *>(act_in) + (size_t)b0 * nblk * F::BE;
+        if (WT == GQ_Q4_K)
+            quant_stage_q8_k(a, x, nact);
+        else
+            quant_stage_q8_0<WT == GQ_Q4_0>(a, x, nact);
+    } else {
+        const uint8_t *xq = static_cast<const uint8_t *>(act_in);
+        if (WT == GQ_Q4_K)
+            stage_q8_k(a, xq + (size_t)b0 * nblk * Q8_K_BYTES, nact);
+        else
+            stage_q8_0<WT == GQ_Q4_0>(a, xq + (size_t)b0 * nblk * Q8_0_BYTES, nact);
+    }
     __syncthreads();
-    pdl_launch_dependents();
-    if (!active) return;
+    if (!GQ_GEMV_EARLY_TRIGGER) pdl_launch_dependents();
 
     float acc[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
+    const size_t bstride = (size_t)rows * nblk * (WT == GQ_Q4_K ? 2 : 1);
 
-    for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait_bounded(bar + (c & 1), (uint32_t)(c >> 1) & 1u)) {
-            // A transfer never completed: flag it, let the other stage drain
-            // (bounded), and leave this row unwritten.
+    for (int i = 0; i < total; ++i) {
+        const int st = i % NSTAGE;
+        if (!mbar_wait_bounded(bar + st, (uint32_t)(i / NSTAGE) & 1u)) {
+            // A transfer never completed: flag it, let the other issued
+            // stages drain (bounded), and leave the remaining rows unwritten.
             if (lane == 0) atomicOr(status, STATUS_GEMV_TMA_TIMEOUT);
-            if (c + 1 < nchunks) mbar_wait_bounded(bar + ((c + 1) & 1), (uint32_t)((c + 1) >> 1) & 1u);
+            for (int k = i + 1; k < total && k < i + NSTAGE; ++k)
+                mbar_wait_bounded(bar + k % NSTAGE, (uint32_t)(k / NSTAGE) & 1u);
             return;
         }
-        const uint8_t *chunk = buf + (c & 1) * L::BUF;
-        const int nb_c = min(CH_BLOCKS, nblk - c * CH_BLOCKS);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int k = lane + 32 * h;
-            if (k < nb_c) {
-                const int blk = c * CH_BLOCKS + k;
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    if (b < nvec) {
-                        const int ab = b * nblk + blk;
-                        float dw;
-                        const int s = block_dot_smem<Q4>(
-                            chunk, k * BB, reinterpret_cast<const int4 *>(act.codes + (size_t)ab * 32),
-                            act.asum[ab], dw);
-                        if (SUMS)
-                            sums[((size_t)(b0 + b) * rows + row) * nblk + blk] = s;
-                        else
-                            acc[b] += dw * act.dx[ab] * (float)s;
-                    }
-                }
-            }
-        }
+        const int row = wg + (i / nchunk) * warps_total;
+        const int c = i % nchunk;
+        const int nb_c = min(F::CH, nblk - c * F::CH);
+        const uint8_t *ch = ring + st * R::BUF;
+        int32_t *srow = SUMS ? sums + ((size_t)b0 * rows + row) * nblk * (WT == GQ_Q4_K ? 2 : 1) : nullptr;
+        if (WT == GQ_Q4_K)
+            chunk_q4_k<NB, SUMS>(ch, nb_c, c * F::CH, nblk, a, nvec, acc, srow, bstride, lane);
+        else
+            chunk_q_0<WT, NB, SUMS>(ch, nb_c, c * F::CH, nblk, a, nvec, acc, srow, bstride, lane);
         __syncwarp();
-        if (lane == 0 && c + 2 < nchunks) issue(c + 2);
-    }
-    if (!SUMS) {
+        if (lane == 0 && i + NSTAGE < total) issue(i + NSTAGE);
+        if (!SUMS && c == nchunk - 1) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            if (b < nvec) {
-                const float v = warp_sum(acc[b]);
-                if (lane == 0) y[(size_t)(b0 + b) * rows + row] = v;
+            for (int b = 0; b < NB; ++b) {
+                if (b < nvec) {
+                    const float v = warp_sum(acc[b]);
+                    if (lane == 0) y[(size_t)(b0 + b) * rows + row] = v;
+                }
+                acc[b] = 0.0f;
             }
         }
     }
@@ -389,19 +528,19 @@ __global__ void __launch_bounds__(256) gemv_q_0_kernel(const uint8_t *__restrict
 
 // Plain per-block kernel for Q4_0 / Q8_0 rows whose byte length is not a
 // multiple of 16 (cols % 256 != 0): warp per row, lane per block, 16-bit
-// global loads.
+// global loads, activations read from global memory.
 template <bool Q4, bool SUMS>
-__global__ void __launch_bounds__(256) gemv_q_0_plain_kernel(const uint8_t *__restrict__ W,
-                                                             const uint8_t *__restrict__ xq,
-                                                             float *__restrict__ y,
-                                                             int32_t *__restrict__ sums, int rows,
-                                                             int nblk, int batch) {
+__global__ void __launch_bounds__(256) gemv_plain_kernel(const uint8_t *__restrict__ W,
+                                                         const uint8_t *__restrict__ xq,
+                                                         float *__restrict__ y,
+                                                         int32_t *__restrict__ sums, int rows,
+                                                         int nblk, int batch) {
     constexpr int BB = Q4 ? Q4_0_BYTES : Q8_0_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * WARPS + warp;
     const int b = blockIdx.y;
-    pdl_wait();
     pdl_launch_dependents();
+    pdl_wait();
     if (row >= rows || b >= batch) return;
     float acc = 0.0f;
     for (int blk = lane; blk < nblk; blk += 32) {
@@ -411,9 +550,9 @@ __global__ void __launch_bounds__(256) gemv_q_0_plain_kernel(const uint8_t *__re
         if (Q4) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const uint32_t w2 = __ldg(wb + 1 + i);        // code bytes 2i, 2i+1
-                const uint32_t a01 = __ldg(ab + 1 + 2 * i);   // activations 4i, 4i+1
-                const uint32_t a23 = __ldg(ab + 2 + 2 * i);   // activations 4i+2, 4i+3
+                const uint32_t w2 = __ldg(wb + 1 + i);       // code bytes 2i, 2i+1
+                const uint32_t a01 = __ldg(ab + 1 + 2 * i);  // activations 4i, 4i+1
+                const uint32_t a23 = __ldg(ab + 2 + 2 * i);  // activations 4i+2, 4i+3
                 const int c0 = (int)(w2 & 15) - 8, c1 = (int)((w2 >> 4) & 15) - 8;
                 const int c2 = (int)((w2 >> 8) & 15) - 8, c3 = (int)((w2 >> 12) & 15) - 8;
                 s += c0 * (int)(int8_t)(a01 & 0xff) + c1 * (int)(int8_t)(a01 >> 8) +
@@ -440,87 +579,95 @@ __global__ void __launch_bounds__(256) gemv_q_0_plain_kernel(const uint8_t *__re
     }
 }
 
-template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+// ------------------------------------------------------------------ launch
+
+constexpr int SMEM_MAX = 232448;  // opt-in shared memory per CTA on sm_103
+constexpr int ROWS_PER_WARP = GQ_GEMV_ROWS_PER_WARP;  // target rows per warp before the grid caps
+constexpr int CTAS_PER_SM = GQ_GEMV_CTAS_PER_SM;
+
+template <int WT>
+size_t smem_bytes(int nb, int nblk) {
+    return (size_t)Ring<WT>::ACT_OFF + (size_t)nb * nblk * act_block_bytes<WT>();
 }
 
-template <int NB, bool SUMS>
-cudaError_t launch_q4k(const void *W, const void *xq, float *y, int32_t *sums, int rows, int nsb,
-                       int batch, const LaunchCtx &ctx) {
-    const size_t smem = (size_t)NB * nsb * (256 + 4 + 32);
-    auto k = gemv_q4_k_kernel<NB, SUMS>;
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((rows + WARPS - 1) / WARPS, (batch + NB - 1) / NB);
-    return launch_pdl(k, grid, dim3(256), smem, ctx.stream, static_cast<const uint8_t *>(W),
-                      static_cast<const uint8_t *>(xq), y, sums, rows, nsb, batch);
-}
-
-template <bool Q4, int NB, bool SUMS>
-cudaError_t launch_q0(const void *W, const void *xq, float *y, int32_t *sums, int rows, int nblk,
-                      int batch, const LaunchCtx &ctx) {
-    using L = ChunkLayout<Q4 ? Q4_0_BYTES : Q8_0_BYTES>;
-    const size_t smem = L::ACT_OFF + (size_t)NB * nblk * (32 + 4 + 4);
-    auto k = gemv_q_0_kernel<Q4, NB, SUMS>;
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((rows + WARPS - 1) / WARPS, (batch + NB - 1) / NB);
-    return launch_pdl(k, grid, dim3(256), smem, ctx.stream, static_cast<const uint8_t *>(W),
-                      static_cast<const uint8_t *>(xq), y, sums, rows, nblk, batch, ctx.status);
-}
-
-// Batch chunk per launch: the largest NB in {1, 2, 4, 8} not above batch
-// (bigger batches run as several chunks of 8 vectors in blockIdx.y).
-template <bool SUMS>
-cudaError_t dispatch(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums,
-                     int rows, int cols, int batch, const LaunchCtx &ctx) {
-    const int nb = batch >= 8 ? 8 : batch >= 4 ? 4 : batch >= 2 ? 2 : 1;
-    if (wtype == GQ_Q4_K) {
-        const int nsb = cols / QK_K;
-        switch (nb) {
-        case 1: return launch_q4k<1, SUMS>(W, xq, y, sums, rows, nsb, batch, ctx);
-        case 2: return launch_q4k<2, SUMS>(W, xq, y, sums, rows, nsb, batch, ctx);
-        case 4: return launch_q4k<4, SUMS>(W, xq, y, sums, rows, nsb, batch, ctx);
-        default: return launch_q4k<8, SUMS>(W, xq, y, sums, rows, nsb, batch, ctx);
-        }
+template <int WT, int NB, bool SUMS, bool FUSED>
+cudaError_t launch_one(const void *W, const void *act, float *y, int32_t *sums, int rows,
+                       int nblk, int batch, int w_static, const LaunchCtx &ctx) {
+    auto k = gemv_kernel<WT, NB, SUMS, FUSED>;
+    const size_t smem = smem_bytes<WT>(NB, nblk);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+        if (e != cudaSuccess) return e;
     }
+    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(CTAS_PER_SM, SMEM_MAX / (smem + 1024)));
+    int grid = (rows + WARPS * ROWS_PER_WARP - 1) / (WARPS * ROWS_PER_WARP);
+    grid = std::max(1, std::min(grid, ctx.num_sms * per_sm));
+    dim3 g(grid, (batch + NB - 1) / NB);
+    return launch_pdl(k, g, dim3(256), smem, ctx.stream, static_cast<const uint8_t *>(W), act, y,
+                      sums, rows, nblk, batch, w_static, ctx.status);
+}
+
+// Largest batch chunk in {8, 4, 2, 1} not above `batch` whose staged
+// activations fit in shared memory; 0 if none fits.
+template <int WT>
+int pick_nb(int batch, int nblk) {
+    for (int nb = 8; nb >= 1; nb >>= 1)
+        if (nb <= std::max(batch, 1) && smem_bytes<WT>(nb, nblk) <= (size_t)SMEM_MAX) return nb;
+    return 0;
+}
+
+template <int WT, bool SUMS, bool FUSED>
+cudaError_t dispatch_wt(const void *W, const void *act, float *y, int32_t *sums, int rows,
+                        int nblk, int batch, int w_static, const LaunchCtx &ctx) {
+    switch (pick_nb<WT>(batch, nblk)) {
+    case 8: return launch_one<WT, 8, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    case 4: return launch_one<WT, 4, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    case 2: return launch_one<WT, 2, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    case 1: return launch_one<WT, 1, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <bool SUMS, bool FUSED>
+cudaError_t dispatch(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
+                     int rows, int cols, int batch, int w_static, const LaunchCtx &ctx) {
+    if (wtype == GQ_Q4_K)
+        return dispatch_wt<GQ_Q4_K, SUMS, FUSED>(W, act, y, sums, rows, cols / QK_K, batch, w_static, ctx);
     const int nblk = cols / 32;
-    const bool q4 = wtype == GQ_Q4_0;
     if (cols % 256 != 0) {
+        if (FUSED) return cudaErrorInvalidValue;
         dim3 grid((rows + WARPS - 1) / WARPS, batch);
-        if (q4)
-            return launch_pdl(gemv_q_0_plain_kernel<true, SUMS>, grid, dim3(256), 0, ctx.stream,
-                              static_cast<const uint8_t *>(W), static_cast<const uint8_t *>(xq), y,
-                              sums, rows, nblk, batch);
-        return launch_pdl(gemv_q_0_plain_kernel<false, SUMS>, grid, dim3(256), 0, ctx.stream,
-                          static_cast<const uint8_t *>(W), static_cast<const uint8_t *>(xq), y, sums,
-                          rows, nblk, batch);
+        const uint8_t *w8 = static_cast<const uint8_t *>(W);
+        const uint8_t *a8 = static_cast<const uint8_t *>(act);
+        if (wtype == GQ_Q4_0)
+            return launch_pdl(gemv_plain_kernel<true, SUMS>, grid, dim3(256), 0, ctx.stream, w8, a8,
+                              y, sums, rows, nblk, batch);
+        return launch_pdl(gemv_plain_kernel<false, SUMS>, grid, dim3(256), 0, ctx.stream, w8, a8, y,
+                          sums, rows, nblk, batch);
     }
-    if (q4) {
-        switch (nb) {
-        case 1: return launch_q0<true, 1, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-        case 2: return launch_q0<true, 2, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-        case 4: return launch_q0<true, 4, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-        default: return launch_q0<true, 8, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-        }
-    }
-    switch (nb) {
-    case 1: return launch_q0<false, 1, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-    case 2: return launch_q0<false, 2, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-    case 4: return launch_q0<false, 4, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-    default: return launch_q0<false, 8, SUMS>(W, xq, y, sums, rows, nblk, batch, ctx);
-    }
+    if (wtype == GQ_Q4_0)
+        return dispatch_wt<GQ_Q4_0, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    return dispatch_wt<GQ_Q8_0, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums,
-                        int64_t rows, int64_t cols, int64_t batch, const LaunchCtx &ctx) {
-    if (sums)
-        return dispatch<true>(wtype, W, xq, y, sums, (int)rows, (int)cols, (int)batch, ctx);
-    return dispatch<false>(wtype, W, xq, y, sums, (int)rows, (int)cols, (int)batch, ctx);
+bool gemv_fits(gq_type wtype, int64_t cols) {
+    if (wtype == GQ_Q4_K) return pick_nb<GQ_Q4_K>(1, (int)(cols / QK_K)) > 0;
+    if (cols % 256 != 0) return true;
+    if (wtype == GQ_Q4_0) return pick_nb<GQ_Q4_0>(1, (int)(cols / 32)) > 0;
+    return pick_nb<GQ_Q8_0>(1, (int)(cols / 32)) > 0;
+}
+
+cudaError_t launch_gemv(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
+                        int64_t rows, int64_t cols, int64_t batch, bool fused_f32, bool w_static,
+                        const LaunchCtx &ctx) {
+    const int ws = w_static ? 1 : 0;
+    if (fused_f32)
+        return sums ? dispatch<true, true>(wtype, W, act, y, sums, (int)rows, (int)cols, (int)batch, ws, ctx)
+                    : dispatch<false, true>(wtype, W, act, y, sums, (int)rows, (int)cols, (int)batch, ws, ctx);
+    return sums ? dispatch<true, false>(wtype, W, act, y, sums, (int)rows, (int)cols, (int)batch, ws, ctx)
+                : dispatch<false, false>(wtype, W, act, y, sums, (int)rows, (int)cols, (int)batch, ws, ctx);
 }
 
 }  // namespace gq

@@ -39,9 +39,15 @@ cudaError_t launch_dequantize(gq_type t, const void *src, float *dst, int64_t n,
                               const LaunchCtx &ctx);
 
 // dp4a GEMV family.  sums != nullptr selects the block-sum diagnostic output
-// instead of y.
-cudaError_t launch_gemv(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums,
-                        int64_t rows, int64_t cols, int64_t batch, const LaunchCtx &ctx);
+// instead of y.  fused_f32: `act` is fp32 activations quantized inside the
+// kernel (cols % 256 == 0 required); otherwise `act` holds quantized blocks.
+// w_static: W may be fetched before the dependency wait on the previous
+// kernel in the stream.
+cudaError_t launch_gemv(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
+                        int64_t rows, int64_t cols, int64_t batch, bool fused_f32, bool w_static,
+                        const LaunchCtx &ctx);
+// True when one activation vector of `cols` fits the GEMV's shared memory.
+bool gemv_fits(gq_type wtype, int64_t cols);
 
 // tcgen05 tensor-core family (Q4_K x Q8_K).
 cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,

@@ -20,6 +20,7 @@ from . import build as _build
 
 Q4_0, Q8_0, Q4_K, Q8_K = 0, 1, 2, 3
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+FLAG_W_STATIC = 1
 ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K}
 BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q8_K: 256}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q8_K: 276}
@@ -40,7 +41,10 @@ SIGNATURES = {
     "gq_dequantize_rows_async": ([_i32, _vp, _vp, _i64, _vp], _i32),
     "gq_matmul": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
     "gq_matmul_path": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp], _i32),
+    "gq_matmul_ex": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, ctypes.c_uint, _vp], _i32),
+    "gq_matmul_f32": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp], _i32),
     "gq_block_sums": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp], _i32),
+    "gq_block_sums_f32": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
     "gq_tc_min_batch": ([], _i64),
     "gq_device_status": ([_u32p, _i32], _i32),
 }
@@ -144,6 +148,24 @@ def gq_matmul_path(wtype: int, W, xq, y, rows: int, cols: int, batch: int, path:
                                                    batch, path, _s(stream)))
 
 
+def gq_matmul_ex(wtype: int, W, xq, y, rows: int, cols: int, batch: int, path: int = PATH_AUTO,
+                 flags: int = 0, stream=None) -> None:
+    _check("gq_matmul_ex", load().gq_matmul_ex(wtype, _p(W), _p(xq), _p(y), rows, cols, batch,
+                                               path, flags, _s(stream)))
+
+
+def gq_matmul_f32(wtype: int, W, x, y, rows: int, cols: int, batch: int, flags: int = 0,
+                  stream=None) -> None:
+    _check("gq_matmul_f32", load().gq_matmul_f32(wtype, _p(W), _p(x), _p(y), rows, cols, batch,
+                                                 flags, _s(stream)))
+
+
+def gq_block_sums_f32(wtype: int, W, x, sums, rows: int, cols: int, batch: int,
+                      stream=None) -> None:
+    _check("gq_block_sums_f32", load().gq_block_sums_f32(wtype, _p(W), _p(x), _p(sums), rows, cols,
+                                                         batch, _s(stream)))
+
+
 def gq_block_sums(wtype: int, W, xq, sums, rows: int, cols: int, batch: int, path: int,
                   stream=None) -> None:
     _check("gq_block_sums", load().gq_block_sums(wtype, _p(W), _p(xq), _p(sums), rows, cols,
@@ -196,11 +218,30 @@ def matmul(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH
     return y
 
 
-def block_sums(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH_GEMV,
+def matmul_f32(wtype: int, W, x, rows: int, cols: int, batch: int, flags: int = 0, out=None,
                stream=None):
+    """Fused activation quantize + product from fp32 activations [batch, cols]."""
+    import torch
+    y = out if out is not None else torch.empty(batch, rows, dtype=torch.float32, device=W.device)
+    gq_matmul_f32(wtype, W, x, y, rows, cols, batch, flags, stream)
+    return y
+
+
+def _sums_buffer(wtype, W, rows, cols, batch):
     import torch
     nb = cols // BLOCK_ELEMS[wtype]
     shape = (batch, rows, nb, 2) if wtype == Q4_K else (batch, rows, nb)
-    s = torch.empty(shape, dtype=torch.int32, device=W.device)
+    return torch.empty(shape, dtype=torch.int32, device=W.device)
+
+
+def block_sums(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH_GEMV,
+               stream=None):
+    s = _sums_buffer(wtype, W, rows, cols, batch)
     gq_block_sums(wtype, W, xq, s, rows, cols, batch, path, stream)
+    return s
+
+
+def block_sums_f32(wtype: int, W, x, rows: int, cols: int, batch: int, stream=None):
+    s = _sums_buffer(wtype, W, rows, cols, batch)
+    gq_block_sums_f32(wtype, W, x, s, rows, cols, batch, stream)
     return s

@@ -88,6 +88,17 @@ typedef enum {
     GQ_ERR_ARCH = 7     /* the current device is not an sm_103 GPU */
 } gq_status;
 
+/* Flags for gq_matmul_ex / gq_matmul_f32. */
+enum {
+    /* W is not written by any kernel that may still be running on the stream
+     * (model weights written once at load time).  The GEMV kernels then
+     * request their first weight chunks before waiting for the preceding
+     * kernel in the stream to finish, overlapping the weight fetch with that
+     * kernel's tail.  Without the flag every read of W happens after that
+     * wait. */
+    GQ_FLAG_W_STATIC = 1u
+};
+
 /* Kernel family selection for gq_matmul_path / gq_block_sums. */
 typedef enum {
     GQ_PATH_AUTO = 0,   /* GEMV below the tensor-core crossover batch, MMA at or above */
@@ -111,7 +122,8 @@ int gq_last_cuda_error(void);
  *         range: |x| < 65504 * 127 for Q8_0, 65504 * 7 for Q4_0, 65504 * 945
  *         for Q4_K).
  *   dst : device, n / block_elems * block_bytes bytes; 4-byte aligned for
- *         Q8_K, 16-byte aligned for Q4_K, 2-byte aligned for Q4_0 / Q8_0.
+ *         Q8_K and Q4_K, 2-byte aligned for Q4_0 / Q8_0 (the product needs
+ *         16-byte aligned weights, see gq_matmul).
  *   n   : element count, >= 0 and a multiple of block_elems(type).
  * Results are bit-identical to the reference definition of each format
  * ("llama.cpp 推理引擎" §5.1 symmetric rule for Q8_0 / Q4_0 / Q8_K, §5.2
@@ -149,11 +161,13 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *   xq    : device, batch x (cols / block_elems) activation blocks (Q8_0 for
  *           Q4_0 / Q8_0 weights, Q8_K for Q4_K), one vector after another;
  *           16-byte aligned.
- *   y     : device, float[batch][rows], 16-byte aligned; fully overwritten.
+ *   y     : device, float[batch][rows], 4-byte aligned; fully overwritten.
  *   rows, cols, batch : > 0 (a zero size is a no-op returning GQ_OK);
  *           cols a multiple of 256 for Q4_K and of 32 for Q4_0 / Q8_0 (the
  *           fast kernels need cols % 256 == 0; other multiples of 32 run a
- *           plain per-block kernel).
+ *           plain per-block kernel); cols at most 131072 (and small
+ *           enough for one activation vector to fit the kernels' shared
+ *           memory: every cols up to that bound does).
  * The integer block sums are exact (int32); y matches the double-precision
  * sum of the same terms within 1e-4 of the sum of their magnitudes.
  * Asynchronous on `stream`; allocates nothing.
@@ -168,6 +182,29 @@ gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
                          gq_stream_t stream);
 
 /*
+ * gq_matmul_path with flags (GQ_FLAG_W_STATIC).  Unknown flag bits give
+ * GQ_ERR_TYPE.
+ */
+gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y,
+                       int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                       unsigned flags, gq_stream_t stream);
+
+/*
+ * Fused activation quantize + product: x holds fp32 activations
+ * float[batch][cols] (device, 16-byte aligned); each CTA quantizes them to
+ * Q8_K (Q4_K weights) or Q8_0 (Q4_0 / Q8_0 weights) in shared memory with
+ * exactly the arithmetic of gq_quantize_rows, then runs the GEMV.  The result
+ * equals gq_quantize_rows followed by gq_matmul_path(..., GQ_PATH_GEMV), bit
+ * for bit, with one launch instead of two and no quantized activation buffer
+ * ("llama.cpp：一个人、一个周末…", 第一层：GGML 张量库: operators fused over
+ * the computation graph).  GEMV kernels only (any batch); cols must be a
+ * multiple of 256 (GQ_ERR_SHAPE otherwise).  Other arguments as gq_matmul.
+ */
+gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
+                        int64_t rows, int64_t cols, int64_t batch, unsigned flags,
+                        gq_stream_t stream);
+
+/*
  * Diagnostic: the integer block sums of the product, as computed by the
  * chosen kernel family, without the float scaling.
  *   sums : device, int32, 4-byte aligned, laid out [batch][rows][nblk][c] with
@@ -178,6 +215,10 @@ gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
 gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,
                         int64_t rows, int64_t cols, int64_t batch, gq_path path,
                         gq_stream_t stream);
+
+/* gq_block_sums for the fused path (fp32 activations, as gq_matmul_f32). */
+gq_status gq_block_sums_f32(gq_type wtype, const void *W, const float *x, int32_t *sums,
+                            int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
 
 /* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
  * Q4_K (the measured crossover; the environment variable GQ_TC_MIN_BATCH,

@@ -108,3 +108,16 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     assert lib.gq_last_cuda_error() != 0
     with pytest.raises(gq.GQError):
         gq.gq_matmul(2, A16, A16, A16, 8, 256, 1, stream=0)
+
+
+def test_fused_and_flag_validation(lib):
+    f = lib.gq_matmul_f32
+    assert f(2, A16, A16 + 4, A16, 8, 256, 1, 0, None) == ALIGN     # x must be 16-aligned
+    assert f(0, A16, A16, A16, 8, 96, 1, 0, None) == SHAPE          # fused needs cols % 256 == 0
+    assert f(2, A16, A16, A16, 8, 256, 1, 2, None) == TYPE          # unknown flag bit
+    assert f(3, A16, A16, A16, 8, 256, 1, 0, None) == TYPE
+    assert f(2, 0, 0, 0, 0, 256, 1, 0, None) == OK
+    e = lib.gq_matmul_ex
+    assert e(2, A16, A16, A16, 8, 256, 1, 1, 4, None) == TYPE
+    assert e(2, A16, A16, MIS + 1, 8, 256, 1, 1, 1, None) == ALIGN
+    assert lib.gq_block_sums_f32(2, A16, A16, 0, 8, 256, 1, None) == NULL

@@ -243,3 +243,65 @@ def test_config_decode_shapes(name):
 def test_config_batch_sweep_gemv(batch):
     W, X = inputs.gemm_q4_k(0, 14336, 4096, batch)
     check_full(Q4_K, W, X, 14336, 4096, batch, gq.PATH_GEMV, nsample=24)
+
+
+# ------------------------------------------- fused activation quantize path
+
+FUSED_SHAPES = [(1, 256, 1), (37, 1024, 1), (130, 4096, 1), (64, 11008, 1), (19, 2816, 3),
+                (33, 768, 5), (24, 1280, 8), (9, 4352, 16)]
+
+
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
+@pytest.mark.parametrize("rows,cols,batch", FUSED_SHAPES)
+def test_fused_f32_matches_unfused_and_oracle(wtype, rows, cols, batch):
+    W, X, Wq, Xq = make_case(wtype, rows, cols, batch, seed=3 * rows + cols + batch)
+    Wd, Xf = dev(Wq), dev(X)
+    Xd = gq.quantize(orc.ACT_TYPE[wtype], Xf)
+    # integer sums of the fused path equal the oracle's
+    s = host(gq.block_sums_f32(wtype, Wd, Xf, rows, cols, batch))
+    np.testing.assert_array_equal(s, orc.block_sums(wtype, Wq, Xq, rows, cols, batch))
+    # the fused result is the unfused result, bit for bit
+    y_f = host(gq.matmul_f32(wtype, Wd, Xf, rows, cols, batch))
+    y_u = host(gq.matmul(wtype, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    assert y_f.view(np.uint32).tobytes() == y_u.view(np.uint32).tobytes()
+    y_ref, T = orc.matmul_ref(wtype, Wq, Xq, rows, cols, batch)
+    assert_close(y_f, y_ref, T)
+
+
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
+def test_w_static_flag_same_result(wtype):
+    rows, cols, batch = 300, 4096, 2
+    W, X, Wq, Xq = make_case(wtype, rows, cols, batch, seed=11)
+    Wd, Xd = dev(Wq), dev(Xq)
+    torch.cuda.synchronize()
+    y0 = torch.empty(batch, rows, device="cuda")
+    y1 = torch.empty(batch, rows, device="cuda")
+    gq.gq_matmul_ex(wtype, Wd, Xd, y0, rows, cols, batch, gq.PATH_GEMV, 0)
+    gq.gq_matmul_ex(wtype, Wd, Xd, y1, rows, cols, batch, gq.PATH_GEMV, gq.FLAG_W_STATIC)
+    assert host(y0).view(np.uint32).tobytes() == host(y1).view(np.uint32).tobytes()
+    y_ref, T = orc.matmul_ref(wtype, Wq, Xq, rows, cols, batch)
+    assert_close(host(y1), y_ref, T)
+
+
+def test_weights_written_by_previous_kernel_are_read_after_it():
+    """Without GQ_FLAG_W_STATIC, a product issued right after the kernel that
+    writes W (its quantize) must see the new weights, repeatedly."""
+    rows, cols = 2048, 4096
+    g = inputs.rng(21)
+    Wa = inputs.normal(g, (rows, cols), 0.02)
+    Wb = inputs.normal(g, (rows, cols), 0.02)
+    x = inputs.normal(g, (1, cols))
+    Wd = torch.empty(rows, cols // 256 * 144, dtype=torch.uint8, device="cuda")
+    Xd = gq.quantize(Q8_K, dev(x))
+    Wa_d, Wb_d = dev(Wa), dev(Wb)
+    y = torch.empty(1, rows, device="cuda")
+    ref = {}
+    for name, Wf in (("a", Wa), ("b", Wb)):
+        Wq = orc.quantize(Q4_K, Wf)
+        ref[name] = orc.matmul_ref(Q4_K, Wq, orc.quantize(Q8_K, x), rows, cols, 1)
+    for it in range(6):
+        name, src = ("a", Wa_d) if it % 2 == 0 else ("b", Wb_d)
+        gq.gq_quantize_rows_async(Q4_K, src, Wd, rows * cols)
+        gq.gq_matmul(Q4_K, Wd, Xd, y, rows, cols, 1)
+        y_ref, T = ref[name]
+        assert_close(host(y), y_ref, T)
