@@ -70,16 +70,16 @@ struct Fmt<GQ_Q4_K> {
     static constexpr int BB = Q4_K_BYTES, BE = 256, CH = GQ_GEMV_Q4K_CHUNK;  // 2304-byte chunks
 };
 
-template <int WT>
+template <int WT, int NW>
 struct Ring {
     static constexpr int CHUNK = Fmt<WT>::CH * Fmt<WT>::BB;
     static constexpr int BUF = ((CHUNK + 16 + 15) / 16) * 16;  // +16: over-read slack
     // WARPS * NSTAGE mbarriers of 8 bytes come first, then the ring buffers
-    static constexpr int BARS_BYTES = WARPS * NSTAGE * 8;
+    static constexpr int BARS_BYTES = NW * NSTAGE * 8;
     static constexpr int BUFS_OFF = ((BARS_BYTES + 127) / 128) * 128;
     static_assert(BUFS_OFF >= BARS_BYTES, "mbarriers must not overlap the ring");
     static_assert(BUFS_OFF % 16 == 0 && BUF % 16 == 0, "bulk-copy destinations are 16-byte aligned");
-    static constexpr int ACT_OFF = BUFS_OFF + WARPS * NSTAGE * BUF;
+    static constexpr int ACT_OFF = BUFS_OFF + NW * NSTAGE * BUF;
 };
 
 // Staged activations.  Q8_K (for Q4_K weights): per vector and super-block
@@ -205,12 +205,12 @@ __device__ __forceinline__ float clamp127(float v) {
 // Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
 // (= code group l of the layout).
 __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int b0 = warp; b0 < nblocks; b0 += 2 * WARPS) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int b0 = warp; b0 < nblocks; b0 += 2 * nw) {
         float4 v[2][2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int blk = b0 + u * WARPS;
+            const int blk = b0 + u * nw;
             if (blk < nblocks) {
                 const float4 *p = reinterpret_cast<const float4 *>(x + (size_t)blk * QK_K + 8 * lane);
                 v[u][0] = __ldg(p);
@@ -219,7 +219,7 @@ __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int 
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int blk = b0 + u * WARPS;
+            const int blk = b0 + u * nw;
             if (blk >= nblocks) break;  // warp-uniform
             const float e[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
                                 v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
@@ -256,16 +256,17 @@ __device__ void quant_stage_q8_0(const Act &a, const float *__restrict__ x, int 
     // position of this lane's code in the staged block
     const int e = lane & 7;
     const int pos = SPLIT ? ((lane & ~7) | ((e & 1) ? 4 + (e >> 1) : (e >> 1))) : lane;
-    for (int b0 = warp; b0 < nblocks; b0 += 8 * WARPS) {
+    const int nw = blockDim.x >> 5;
+    for (int b0 = warp; b0 < nblocks; b0 += 8 * nw) {
         float v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int blk = b0 + u * WARPS;
+            const int blk = b0 + u * nw;
             v[u] = blk < nblocks ? __ldg(x + (size_t)blk * 32 + lane) : 0.0f;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int blk = b0 + u * WARPS;
+            const int blk = b0 + u * nw;
             if (blk >= nblocks) break;  // warp-uniform
             const float amax = warp_max(fabsf(v[u]));
             const float d = __half2float(__float2half_rn(__fdiv_rn(amax, 127.0f)));
@@ -284,17 +285,10 @@ __device__ void quant_stage_q8_0(const Act &a, const float *__restrict__ x, int 
 
 // ------------------------------------------------------------ chunk compute
 
-// Sub-block factors of a Q4_K block header (bytes 0..15 as four words): the
-// sixteen 6-bit fields sit LSB-first in header bits 32..127.
-__device__ __forceinline__ void q4k_factors(const uint4 &h, int j, int &sc, int &m) {
-    const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);  // header bits 32..95
-    const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);  // header bits 64..127
-    sc = (int)((lo64 >> (6 * j)) & 63);
-    m = (int)((hi64 >> (6 * j + 16)) & 63);
-}
-
 // Q4_K chunk of nb_c super-blocks starting at super-block sb0 of the row.
 // Lane = sub-block j = lane & 7 of super-block 4t + (lane >> 3).
+// The high nibbles are used in place (bytes 16 q, unsigned) and the second
+// dp4a chain's sum divided by 16 -- exact, every term is a multiple of 16.
 // sums (diagnostic) points at [b = 0][row][sb = 0][0] with stride bstride
 // between vectors.
 template <int NB, bool SUMS>
@@ -302,6 +296,9 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t *ch, int nb_c, int sb0,
                                            const Act &a, int nvec, float (&acc)[NB],
                                            int32_t *sums, size_t bstride, int lane) {
     const int j = lane & 7, sbl = lane >> 3;
+    // bit offsets of this lane's 6-bit scale / min inside header words 1..3
+    const int sh_sc = (6 * j) & 31, sh_m = (48 + 6 * j) & 31;
+    const bool sc_hi = j >= 6, m_hi = j >= 3;
 #pragma unroll
     for (int t = 0; t < Fmt<GQ_Q4_K>::CH / 4; ++t) {
         if (4 * t >= nb_c) break;  // warp-uniform
@@ -309,12 +306,10 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t *ch, int nb_c, int sb0,
         if (sl < nb_c) {
             const uint4 h = *reinterpret_cast<const uint4 *>(ch + sl * Q4_K_BYTES);
             const uint4 q = *reinterpret_cast<const uint4 *>(ch + sl * Q4_K_BYTES + 16 + 16 * j);
-            const int lo0 = (int)(q.x & NIB), hi0 = (int)((q.x >> 4) & NIB);
-            const int lo1 = (int)(q.y & NIB), hi1 = (int)((q.y >> 4) & NIB);
-            const int lo2 = (int)(q.z & NIB), hi2 = (int)((q.z >> 4) & NIB);
-            const int lo3 = (int)(q.w & NIB), hi3 = (int)((q.w >> 4) & NIB);
-            int sc, m;
-            q4k_factors(h, j, sc, m);
+            const uint32_t lo0 = q.x & NIB, hi0 = q.x & ~NIB, lo1 = q.y & NIB, hi1 = q.y & ~NIB;
+            const uint32_t lo2 = q.z & NIB, hi2 = q.z & ~NIB, lo3 = q.w & NIB, hi3 = q.w & ~NIB;
+            const int sc = (int)(__funnelshift_r(sc_hi ? h.z : h.y, sc_hi ? h.w : h.z, sh_sc) & 63u);
+            const int m = (int)(__funnelshift_r(m_hi ? h.w : h.z, m_hi ? 0u : h.w, sh_m) & 63u);
             const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
             const int sb = sb0 + sl;
 #pragma unroll
@@ -323,14 +318,14 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t *ch, int nb_c, int sb0,
                 const int blk = b * nsb + sb;
                 const int4 *ap = reinterpret_cast<const int4 *>(a.codes + (size_t)blk * 256 + 32 * j);
                 const int4 a0 = ap[0], a1 = ap[1];
-                int s = dp4a(lo0, a0.x, 0);
-                s = dp4a(hi0, a0.y, s);
-                s = dp4a(lo1, a0.z, s);
-                s = dp4a(hi1, a0.w, s);
-                s = dp4a(lo2, a1.x, s);
-                s = dp4a(hi2, a1.y, s);
-                s = dp4a(lo3, a1.z, s);
-                s = dp4a(hi3, a1.w, s);
+                int sl_ = dp4a_us(lo0, a0.x, 0), sh_ = dp4a_us(hi0, a0.y, 0);
+                sl_ = dp4a_us(lo1, a0.z, sl_);
+                sh_ = dp4a_us(hi1, a0.w, sh_);
+                sl_ = dp4a_us(lo2, a1.x, sl_);
+                sh_ = dp4a_us(hi2, a1.y, sh_);
+                sl_ = dp4a_us(lo3, a1.z, sl_);
+                sh_ = dp4a_us(hi3, a1.w, sh_);
+                const int s = sl_ + (sh_ >> 4);
                 int is1 = sc * s, is2 = m * a.isum[blk * 8 + j];
                 if (SUMS) {
                     const int cnt = min(4, nb_c - 4 * t);  // super-blocks present in this step
@@ -420,21 +415,21 @@ __device__ __forceinline__ void chunk_q_0(const uint8_t *ch, int nb_c, int blk0,
 // w_static != 0 lets the first weight chunks be requested before the
 // dependency wait on the preceding kernel (the caller guarantees no kernel
 // still in flight writes W).
-template <int WT, int NB, bool SUMS, bool FUSED>
-__global__ void __launch_bounds__(256) gemv_kernel(const uint8_t *__restrict__ W,
+template <int WT, int NB, bool SUMS, bool FUSED, int NW>
+__global__ void __launch_bounds__(NW * 32) gemv_kernel(const uint8_t *__restrict__ W,
                                                    const void *__restrict__ act_in,
                                                    float *__restrict__ y,
                                                    int32_t *__restrict__ sums, int rows,
                                                    int nblk, int batch, int w_static,
                                                    uint32_t *__restrict__ status) {
     using F = Fmt<WT>;
-    using R = Ring<WT>;
+    using R = Ring<WT, NW>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b0 = blockIdx.y * NB;
     const int nvec = min(NB, batch - b0);
-    const int warps_total = gridDim.x * WARPS;
-    const int wg = blockIdx.x * WARPS + warp;
+    const int warps_total = gridDim.x * NW;
+    const int wg = blockIdx.x * NW + warp;
     const int nrows_w = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
     const int nchunk = (nblk + F::CH - 1) / F::CH;
     const int total = nrows_w * nchunk;
@@ -585,26 +580,26 @@ constexpr int SMEM_MAX = 232448;  // opt-in shared memory per CTA on sm_103
 constexpr int ROWS_PER_WARP = GQ_GEMV_ROWS_PER_WARP;  // target rows per warp before the grid caps
 constexpr int CTAS_PER_SM = GQ_GEMV_CTAS_PER_SM;
 
-template <int WT>
+template <int WT, int NW = WARPS>
 size_t smem_bytes(int nb, int nblk) {
-    return (size_t)Ring<WT>::ACT_OFF + (size_t)nb * nblk * act_block_bytes<WT>();
+    return (size_t)Ring<WT, NW>::ACT_OFF + (size_t)nb * nblk * act_block_bytes<WT>();
 }
 
-template <int WT, int NB, bool SUMS, bool FUSED>
+template <int WT, int NB, bool SUMS, bool FUSED, int NW>
 cudaError_t launch_one(const void *W, const void *act, float *y, int32_t *sums, int rows,
-                       int nblk, int batch, int w_static, const LaunchCtx &ctx) {
-    auto k = gemv_kernel<WT, NB, SUMS, FUSED>;
-    const size_t smem = smem_bytes<WT>(NB, nblk);
+                       int nblk, int batch, int w_static, int rows_per_warp, const LaunchCtx &ctx) {
+    auto k = gemv_kernel<WT, NB, SUMS, FUSED, NW>;
+    const size_t smem = smem_bytes<WT, NW>(NB, nblk);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
         if (e != cudaSuccess) return e;
     }
     const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(CTAS_PER_SM, SMEM_MAX / (smem + 1024)));
-    int grid = (rows + WARPS * ROWS_PER_WARP - 1) / (WARPS * ROWS_PER_WARP);
+    int grid = (rows + NW * rows_per_warp - 1) / (NW * rows_per_warp);
     grid = std::max(1, std::min(grid, ctx.num_sms * per_sm));
     dim3 g(grid, (batch + NB - 1) / NB);
-    return launch_pdl(k, g, dim3(256), smem, ctx.stream, static_cast<const uint8_t *>(W), act, y,
-                      sums, rows, nblk, batch, w_static, ctx.status);
+    return launch_pdl(k, g, dim3(NW * 32), smem, ctx.stream, static_cast<const uint8_t *>(W), act,
+                      y, sums, rows, nblk, batch, w_static, ctx.status);
 }
 
 // Largest batch chunk in {8, 4, 2, 1} not above `batch` whose staged
@@ -619,11 +614,13 @@ int pick_nb(int batch, int nblk) {
 template <int WT, bool SUMS, bool FUSED>
 cudaError_t dispatch_wt(const void *W, const void *act, float *y, int32_t *sums, int rows,
                         int nblk, int batch, int w_static, const LaunchCtx &ctx) {
-    switch (pick_nb<WT>(batch, nblk)) {
-    case 8: return launch_one<WT, 8, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
-    case 4: return launch_one<WT, 4, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
-    case 2: return launch_one<WT, 2, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
-    case 1: return launch_one<WT, 1, SUMS, FUSED>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    const int nb = pick_nb<WT>(batch, nblk);
+    const int rpw = ROWS_PER_WARP;
+    switch (nb) {
+    case 8: return launch_one<WT, 8, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
+    case 4: return launch_one<WT, 4, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
+    case 2: return launch_one<WT, 2, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
+    case 1: return launch_one<WT, 1, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
     }
     return cudaErrorInvalidValue;
 }
