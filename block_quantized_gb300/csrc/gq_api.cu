@@ -133,7 +133,7 @@ int64_t tc_min_batch_value() {
 // activations; exactly one of y / sums is non-null.
 gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
                      int64_t rows, int64_t cols, int64_t batch, gq_path path, unsigned flags,
-                     bool fused_f32, gq_stream_t stream) {
+                     bool fused_f32, void *ws, size_t ws_bytes, gq_stream_t stream) {
     if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_MMA) return GQ_ERR_TYPE;
     if (flags & ~(unsigned)GQ_FLAG_W_STATIC) return GQ_ERR_TYPE;
     gq_status st = sums ? check_matmul(wtype, W, act, sums, rows, cols, batch, 4)
@@ -145,18 +145,23 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     }
     if (path == GQ_PATH_MMA) {
         if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+        if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
         if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+        if (!ws) return GQ_ERR_NULL;
+        if (ws_bytes < mma_workspace_bytes(rows, cols, batch)) return GQ_ERR_SHAPE;
+        if (!aligned(ws, 16)) return GQ_ERR_ALIGN;
     }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
     bool use_mma = path == GQ_PATH_MMA;
     if (path == GQ_PATH_AUTO)
         use_mma = !fused_f32 && wtype == GQ_Q4_K && batch >= tc_min_batch_value() &&
-                  mma_supported(rows, cols, batch);
+                  mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
+                  ws_bytes >= mma_workspace_bytes(rows, cols, batch);
     if (!use_mma && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = use_mma ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ctx)
+    cudaError_t e = use_mma ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
                             : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
                                           (flags & GQ_FLAG_W_STATIC) != 0, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -221,38 +226,59 @@ gq_status gq_dequantize_rows(gq_type type, const void *src, float *dst, int64_t 
 
 gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
                     int64_t cols, int64_t batch, gq_stream_t stream) {
-    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, GQ_PATH_AUTO, 0, false, stream);
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, GQ_PATH_AUTO, 0, false, nullptr, 0, stream);
 }
 
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
                          int64_t cols, int64_t batch, gq_path path, gq_stream_t stream) {
-    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, 0, false, stream);
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, 0, false, nullptr, 0, stream);
 }
 
 gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
                        int64_t cols, int64_t batch, gq_path path, unsigned flags,
                        gq_stream_t stream) {
-    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, flags, false, stream);
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, flags, false, nullptr, 0, stream);
 }
 
 gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y, int64_t rows,
                         int64_t cols, int64_t batch, unsigned flags, gq_stream_t stream) {
     if (x && ((reinterpret_cast<uintptr_t>(x) & 15) != 0)) return GQ_ERR_ALIGN;
-    return run_matmul(wtype, W, x, y, nullptr, rows, cols, batch, GQ_PATH_GEMV, flags, true, stream);
+    return run_matmul(wtype, W, x, y, nullptr, rows, cols, batch, GQ_PATH_GEMV, flags, true, nullptr, 0, stream);
 }
 
 gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,
                         int64_t rows, int64_t cols, int64_t batch, gq_path path,
                         gq_stream_t stream) {
     if (!sums && rows > 0 && cols > 0 && batch > 0) return GQ_ERR_NULL;
-    return run_matmul(wtype, W, xq, nullptr, sums, rows, cols, batch, path, 0, false, stream);
+    return run_matmul(wtype, W, xq, nullptr, sums, rows, cols, batch, path, 0, false, nullptr, 0, stream);
 }
 
 gq_status gq_block_sums_f32(gq_type wtype, const void *W, const float *x, int32_t *sums,
                             int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream) {
     if (!sums && rows > 0 && cols > 0 && batch > 0) return GQ_ERR_NULL;
     if (x && ((reinterpret_cast<uintptr_t>(x) & 15) != 0)) return GQ_ERR_ALIGN;
-    return run_matmul(wtype, W, x, nullptr, sums, rows, cols, batch, GQ_PATH_GEMV, 0, true, stream);
+    return run_matmul(wtype, W, x, nullptr, sums, rows, cols, batch, GQ_PATH_GEMV, 0, true, nullptr, 0, stream);
+}
+
+gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
+                       int64_t cols, int64_t batch, gq_path path, unsigned flags, void *workspace,
+                       size_t workspace_bytes, gq_stream_t stream) {
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, path, flags, false, workspace,
+                      workspace_bytes, stream);
+}
+
+gq_status gq_block_sums_ws(gq_type wtype, const void *W, const void *xq, int32_t *sums,
+                           int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                           void *workspace, size_t workspace_bytes, gq_stream_t stream) {
+    if (!sums && rows > 0 && cols > 0 && batch > 0) return GQ_ERR_NULL;
+    return run_matmul(wtype, W, xq, nullptr, sums, rows, cols, batch, path, 0, false, workspace,
+                      workspace_bytes, stream);
+}
+
+size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int64_t batch) {
+    if (wtype != GQ_Q4_K || rows < 1 || batch < 1 || cols > MAX_COLS || !mma_supported(rows, cols, batch))
+        return 0;
+    return mma_workspace_bytes(rows, cols, batch);
 }
 
 int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }

@@ -49,9 +49,11 @@ cudaError_t launch_gemv(gq_type wtype, const void *W, const void *act, float *y,
 // True when one activation vector of `cols` fits the GEMV's shared memory.
 bool gemv_fits(gq_type wtype, int64_t cols);
 
-// tcgen05 tensor-core family (Q4_K x Q8_K).
+// tcgen05 tensor-core family (Q4_K x Q8_K): a pack kernel writes the
+// activation operand into `workspace`, then the MMA kernel runs.
 cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
-                           int64_t cols, int64_t batch, const LaunchCtx &ctx);
+                           int64_t cols, int64_t batch, void *workspace, const LaunchCtx &ctx);
 bool mma_supported(int64_t rows, int64_t cols, int64_t batch);
+size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch);
 
 }  // namespace gq

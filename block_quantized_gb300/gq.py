@@ -45,6 +45,11 @@ SIGNATURES = {
     "gq_matmul_f32": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint, _vp], _i32),
     "gq_block_sums": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp], _i32),
     "gq_block_sums_f32": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
+    "gq_matmul_workspace_bytes": ([_i32, _i64, _i64, _i64], ctypes.c_size_t),
+    "gq_matmul_ws": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, ctypes.c_uint, _vp,
+                      ctypes.c_size_t, _vp], _i32),
+    "gq_block_sums_ws": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, ctypes.c_size_t,
+                          _vp], _i32),
     "gq_tc_min_batch": ([], _i64),
     "gq_device_status": ([_u32p, _i32], _i32),
 }
@@ -172,6 +177,23 @@ def gq_block_sums(wtype: int, W, xq, sums, rows: int, cols: int, batch: int, pat
                                                  batch, path, _s(stream)))
 
 
+def gq_matmul_workspace_bytes(wtype: int, rows: int, cols: int, batch: int) -> int:
+    return int(load().gq_matmul_workspace_bytes(wtype, rows, cols, batch))
+
+
+def gq_matmul_ws(wtype: int, W, xq, y, rows: int, cols: int, batch: int, path: int, flags: int,
+                 workspace, workspace_bytes: int, stream=None) -> None:
+    _check("gq_matmul_ws", load().gq_matmul_ws(wtype, _p(W), _p(xq), _p(y), rows, cols, batch, path,
+                                               flags, _p(workspace), workspace_bytes, _s(stream)))
+
+
+def gq_block_sums_ws(wtype: int, W, xq, sums, rows: int, cols: int, batch: int, path: int,
+                     workspace, workspace_bytes: int, stream=None) -> None:
+    _check("gq_block_sums_ws", load().gq_block_sums_ws(wtype, _p(W), _p(xq), _p(sums), rows, cols,
+                                                       batch, path, _p(workspace), workspace_bytes,
+                                                       _s(stream)))
+
+
 def gq_tc_min_batch() -> int:
     return int(load().gq_tc_min_batch())
 
@@ -234,10 +256,33 @@ def _sums_buffer(wtype, W, rows, cols, batch):
     return torch.empty(shape, dtype=torch.int32, device=W.device)
 
 
+def workspace(wtype: int, rows: int, cols: int, batch: int, device=None):
+    """A torch uint8 device buffer sized for the tensor-core path (or None)."""
+    import torch
+    n = gq_matmul_workspace_bytes(wtype, rows, cols, batch)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda") if n else None
+
+
+def matmul_ws(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH_AUTO,
+              flags: int = 0, ws=None, out=None, stream=None):
+    import torch
+    y = out if out is not None else torch.empty(batch, rows, dtype=torch.float32, device=W.device)
+    if ws is None:
+        ws = workspace(wtype, rows, cols, batch, W.device)
+    gq_matmul_ws(wtype, W, xq, y, rows, cols, batch, path, flags, ws,
+                 0 if ws is None else ws.numel(), stream)
+    return y
+
+
 def block_sums(wtype: int, W, xq, rows: int, cols: int, batch: int, path: int = PATH_GEMV,
                stream=None):
     s = _sums_buffer(wtype, W, rows, cols, batch)
-    gq_block_sums(wtype, W, xq, s, rows, cols, batch, path, stream)
+    if path == PATH_MMA:
+        ws = workspace(wtype, rows, cols, batch, W.device)
+        gq_block_sums_ws(wtype, W, xq, s, rows, cols, batch, path, ws,
+                         0 if ws is None else ws.numel(), stream)
+    else:
+        gq_block_sums(wtype, W, xq, s, rows, cols, batch, path, stream)
     return s
 
 

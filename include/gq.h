@@ -190,6 +190,31 @@ gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y,
                        unsigned flags, gq_stream_t stream);
 
 /*
+ * Bytes of workspace the tensor-core path needs for this product (0 when the
+ * shape or type has no tensor-core path).  The workspace holds the activation
+ * operand repacked once per call as fp16 tiles (plus per-block scales and
+ * the min-term operand): ceil(batch / 128) * (cols / 256) * 70144 bytes.
+ */
+size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int64_t batch);
+
+/*
+ * The product with a caller-provided device workspace (16-byte aligned, at
+ * least gq_matmul_workspace_bytes bytes, owned by the caller, contents
+ * overwritten; calls that share a workspace must not overlap on the GPU).
+ * GQ_PATH_AUTO runs the tcgen05 tensor-core kernel for Q4_K when batch >=
+ * gq_tc_min_batch() and the workspace suffices, the GEMV kernels otherwise.
+ * The tensor-core path computes the same y (within the tolerance above); its
+ * integer super-block sums S1 are exact while partial sums of one super-block
+ * stay below 2^24 in magnitude (always, unless codes and scales sit at their
+ * extremes together).  Errors as gq_matmul_path, plus GQ_ERR_NULL (MMA path
+ * without workspace), GQ_ERR_SHAPE (workspace too small), GQ_ERR_ALIGN.
+ */
+gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y,
+                       int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                       unsigned flags, void *workspace, size_t workspace_bytes,
+                       gq_stream_t stream);
+
+/*
  * Fused activation quantize + product: x holds fp32 activations
  * float[batch][cols] (device, 16-byte aligned); each CTA quantizes them to
  * Q8_K (Q4_K weights) or Q8_0 (Q4_0 / Q8_0 weights) in shared memory with
@@ -215,6 +240,11 @@ gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
 gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,
                         int64_t rows, int64_t cols, int64_t batch, gq_path path,
                         gq_stream_t stream);
+
+/* gq_block_sums with a workspace (required for GQ_PATH_MMA). */
+gq_status gq_block_sums_ws(gq_type wtype, const void *W, const void *xq, int32_t *sums,
+                           int64_t rows, int64_t cols, int64_t batch, gq_path path,
+                           void *workspace, size_t workspace_bytes, gq_stream_t stream);
 
 /* gq_block_sums for the fused path (fp32 activations, as gq_matmul_f32). */
 gq_status gq_block_sums_f32(gq_type wtype, const void *W, const float *x, int32_t *sums,

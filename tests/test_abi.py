@@ -121,3 +121,17 @@ def test_fused_and_flag_validation(lib):
     assert e(2, A16, A16, A16, 8, 256, 1, 1, 4, None) == TYPE
     assert e(2, A16, A16, MIS + 1, 8, 256, 1, 1, 1, None) == ALIGN
     assert lib.gq_block_sums_f32(2, A16, A16, 0, 8, 256, 1, None) == NULL
+
+
+def test_workspace_rules_on_host(lib):
+    wb = lib.gq_matmul_workspace_bytes
+    assert wb(2, 14336, 4096, 64) == 1 * 16 * 70144
+    assert wb(2, 28672, 8192, 512) == 4 * 32 * 70144
+    assert wb(0, 128, 256, 64) == 0 and wb(2, 128, 100, 64) == 0 and wb(2, 0, 256, 64) == 0
+    m = lib.gq_matmul_ws
+    need = wb(2, 128, 256, 64)
+    assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, 0, need, None) == NULL
+    assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, A16, need - 1, None) == SHAPE
+    assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, A16 + 8, need, None) == ALIGN
+    assert m(0, A16, A16, A16, 128, 256, 64, 2, 0, A16, need, None) == TYPE
+    assert lib.gq_matmul_path(2, A16, A16, A16, 128, 256, 64, 2, None) == NULL

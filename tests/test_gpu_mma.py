@@ -1,0 +1,124 @@
+"""GPU parity of the tcgen05 tensor-core path (Q4_K x Q8_K, batched) against
+the CPU oracle: integer super-block sums S1 / S2 bit-identical, y within
+1e-4 * sum|terms|, and the same y as the GEMV path within that tolerance."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as orc  # noqa: E402
+from block_quantized_gb300 import gq, inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+Q4_K, Q8_K = 2, 3
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gq.load(build_if_missing=True)
+    yield
+    torch.cuda.synchronize()
+    assert gq.gq_device_status(reset=True) == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_close(y, y_ref, T):
+    err = np.abs(y.astype(np.float64) - y_ref)
+    bad = err > TOL * T
+    assert not bad.any(), (
+        f"{bad.sum()} outputs out of tolerance; worst ratio {np.max(err / np.maximum(T, 1e-300)):.3g}")
+
+
+SHAPES = [(128, 256, 128), (128, 512, 16), (200, 768, 40), (256, 1024, 130), (77, 256, 1),
+          (384, 4096, 64)]
+
+
+@pytest.mark.parametrize("rows,cols,batch", SHAPES)
+def test_mma_sums_and_y(rows, cols, batch):
+    g = inputs.rng(rows + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q4_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = host(gq.block_sums(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA))
+    np.testing.assert_array_equal(s, orc.block_sums(Q4_K, Wq, Xq, rows, cols, batch))
+    y = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA))
+    y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+    # and the GEMV path agrees within the same bound
+    y_g = host(gq.matmul(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    assert_close(y_g, y_ref, T)
+
+
+def test_mma_auto_dispatch_and_workspace_rules():
+    rows, cols, batch = 256, 512, 48
+    g = inputs.rng(5)
+    Wq = orc.quantize(Q4_K, inputs.normal(g, (rows, cols), 0.02))
+    Xq = orc.quantize(Q8_K, inputs.normal(g, (batch, cols)))
+    need = gq.gq_matmul_workspace_bytes(Q4_K, rows, cols, batch)
+    assert need == 1 * 2 * 70144
+    assert gq.gq_matmul_workspace_bytes(0, rows, cols, batch) == 0
+    y = torch.empty(batch, rows, device="cuda")
+    with pytest.raises(gq.GQError):  # MMA without a workspace
+        gq.gq_matmul_path(Q4_K, dev(Wq), dev(Xq), y, rows, cols, batch, gq.PATH_MMA)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gq.GQError):  # workspace too small
+        gq.gq_matmul_ws(Q4_K, dev(Wq), dev(Xq), y, rows, cols, batch, gq.PATH_MMA, 0, ws, need - 16)
+    gq.gq_matmul_ws(Q4_K, dev(Wq), dev(Xq), y, rows, cols, batch, gq.PATH_AUTO, 0, ws, need)
+    y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
+    assert_close(host(y), y_ref, T)
+
+
+def test_mma_degenerate_blocks():
+    """Zero weights / activations, constant and all-negative rows."""
+    rows, cols, batch = 130, 512, 20
+    W = np.zeros((rows, cols), np.float32)
+    W[1] = 1.0
+    W[2] = -3.0
+    W[3, ::2] = 7.0
+    W[4] = np.linspace(-1, 1, cols, dtype=np.float32)
+    W[5:] = inputs.normal(inputs.rng(3), (rows - 5, cols), 0.02)
+    X = inputs.normal(inputs.rng(4), (batch, cols))
+    X[0] = 0.0
+    X[1] = 1000.0  # large activation scale: the min-term split keeps fp32 range
+    Wq, Xq = orc.quantize(Q4_K, W), orc.quantize(Q8_K, X)
+    s = host(gq.block_sums(Q4_K, dev(Wq), dev(Xq), rows, cols, batch, gq.PATH_MMA))
+    np.testing.assert_array_equal(s, orc.block_sums(Q4_K, Wq, Xq, rows, cols, batch))
+    y = host(gq.matmul_ws(Q4_K, dev(Wq), dev(Xq), rows, cols, batch, gq.PATH_MMA))
+    y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
+    assert np.all(y[0] == 0)
+    assert_close(y, y_ref, T)
+
+
+def sampled_rows(rows, k, seed):
+    g = np.random.Generator(np.random.PCG64(seed))
+    return np.unique(np.concatenate([[0, rows - 1], g.choice(rows, size=min(k, rows), replace=False)]))
+
+
+@pytest.mark.parametrize("rows,cols,batch", [(14336, 4096, 16), (14336, 4096, 64),
+                                             (28672, 8192, 512)])
+def test_mma_full_size(rows, cols, batch):
+    """The batch-sweep and prefill shapes at full size; the oracle recomputes
+    sampled rows from the same fp32 inputs."""
+    W, X = inputs.gemm_q4_k(0, rows, cols, batch)
+    Wd = gq.quantize(Q4_K, dev(W))
+    Xd = gq.quantize(Q8_K, dev(X))
+    y = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA))
+    idx = sampled_rows(rows, 32, rows + batch)
+    Wq_s = orc.quantize(Q4_K, W[idx])
+    assert host(Wd)[idx].tobytes() == Wq_s.tobytes()
+    Xq = orc.quantize(Q8_K, X)
+    y_ref, T = orc.matmul_ref(Q4_K, Wq_s, Xq, len(idx), cols, batch, nthreads=orc.max_threads())
+    assert_close(y[:, idx], y_ref, T)
