@@ -44,6 +44,8 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--only", choices=["prefill", "sweep", "decode"], default=None,
+                   help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
 
 
@@ -219,26 +221,7 @@ def run_gpu(args, world, rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    # ---- headline workload: 64 distinct Q4_K 4096x4096 matrices per step
-    W, x0 = inputs.gemv_q4_k(0)
-    Wq1 = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
-    del W
-    Wall = Wq1.reshape(1, -1).repeat(COPIES, 1)          # [64, 4096 * 2304] distinct copies
-    g = inputs.rng(1)
-    X = torch.from_numpy(np.concatenate([x0[None], inputs.normal(g, (COPIES - 1, GEMV_COLS))])).to(dev)
-    XQ = torch.empty(COPIES, GEMV_COLS // 256 * 276, dtype=torch.uint8, device=dev)
-    Y = torch.empty(COPIES, GEMV_ROWS, dtype=torch.float32, device=dev)
-    w_bytes = GEMV_ROWS * Q4K_ROW_BYTES
     s = torch.cuda.Stream(device=dev)
-
-    def step_body():
-        for i in range(COPIES):
-            gq.gq_quantize_rows_async(gq.Q8_K, X[i], XQ[i], GEMV_COLS)
-            gq.gq_matmul(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
-
-    def gemv_only():
-        for i in range(COPIES):
-            gq.gq_matmul(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
 
     def capture(fn):
         graph = torch.cuda.CUDAGraph()
@@ -267,27 +250,74 @@ def run_gpu(args, world, rank):
             barrier()
         return max_over_ranks(e0.elapsed_time(e1) / 1e3), clk
 
+    if args.only:
+        fn = {"prefill": lambda: bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak),
+              "sweep": lambda: bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph),
+              "decode": lambda: bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world)}
+        if rank == 0:
+            print(json.dumps({"only": args.only, "result": fn[args.only]()}))
+        else:
+            fn[args.only]()
+        return
+
+    # ---- headline workload: 64 distinct Q4_K 4096x4096 matrices per step
+    W, x0 = inputs.gemv_q4_k(0)
+    Wq1 = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
+    del W
+    Wall = Wq1.reshape(1, -1).repeat(COPIES, 1)          # [64, 4096 * 2304] distinct copies
+    g = inputs.rng(1)
+    X = torch.from_numpy(np.concatenate([x0[None], inputs.normal(g, (COPIES - 1, GEMV_COLS))])).to(dev)
+    XQ = torch.empty(COPIES, GEMV_COLS // 256 * 276, dtype=torch.uint8, device=dev)
+    Y = torch.empty(COPIES, GEMV_ROWS, dtype=torch.float32, device=dev)
+    w_bytes = GEMV_ROWS * Q4K_ROW_BYTES
+
+    FLAGS = gq.FLAG_W_STATIC  # model weights: written once, never by a kernel in flight
+
+    def step_body():
+        # the hot path per matrix: fp32 activations -> Q8_K (in-kernel) -> GEMV
+        for i in range(COPIES):
+            gq.gq_matmul_f32(gq.Q4_K, Wall[i], X[i], Y[i], GEMV_ROWS, GEMV_COLS, 1, FLAGS)
+
+    def step_unfused():
+        for i in range(COPIES):
+            gq.gq_quantize_rows_async(gq.Q8_K, X[i], XQ[i], GEMV_COLS)
+            gq.gq_matmul_ex(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1,
+                            gq.PATH_GEMV, FLAGS)
+
     step_graph = capture(step_body)
     sampler = ClockSampler(local)
     t_total, clk = time_graph(step_graph, args.steps, max(3, args.warmup), sampler)
     ms_step = t_total / args.steps * 1e3
     value = world * args.steps * COPIES * w_bytes / t_total / 1e9
-
-    # correctness sentinel on the timed buffers (no oracle here): finite outputs
     if not torch.isfinite(Y).all():
         raise RuntimeError("non-finite GEMV output")
 
-    # ---- roofline of the GEMV kernel: GEMV-only graph, per-launch duration
-    gemv_graph = capture(gemv_only)
-    k_steps = max(50, args.steps // 4)
-    t_g, _ = time_graph(gemv_graph, k_steps, 5)
-    per_launch = t_g / (k_steps * COPIES)
-    alg_bytes = w_bytes + GEMV_COLS // 256 * 276 + GEMV_ROWS * 4
+    # the step is nothing but launches of the fused GEMV kernel, so its
+    # per-launch duration is the step time over the launches in it
+    per_launch = t_total / (args.steps * COPIES)
+    alg_bytes = w_bytes + GEMV_COLS * 4 + GEMV_ROWS * 4
     achieved = alg_bytes / per_launch / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": kernel_traffic("gemv_q4_k_kernel"),
-                "kernel": "gemv_q4_k_kernel<1>", "peak_source": peak_src,
-                "launch_us": per_launch * 1e6, "alg_bytes_per_launch": alg_bytes}
+                "frac": achieved / hbm_peak, "traffic": kernel_traffic("gemv_q4k_fused"),
+                "kernel": "gemv_kernel<Q4_K, NB=1, fused fp32 activations>",
+                "peak_source": peak_src, "launch_us": per_launch * 1e6,
+                "alg_bytes_per_launch": alg_bytes,
+                "note": "dependent back-to-back launches of one 9.44 MB matrix each"}
+
+    # the unfused pair (standalone act-quant kernel + GEMV) for comparison
+    k_steps = max(50, args.steps // 4)
+    t_u, _ = time_graph(capture(step_unfused), k_steps, 5)
+    unfused = {"value": world * k_steps * COPIES * w_bytes / t_u / 1e9, "unit": "GB/s",
+               "us_per_matrix": t_u / (k_steps * COPIES) * 1e6}
+
+    # streaming capability: the same 64 matrices as one tall GEMV launch
+    def tall():
+        gq.gq_matmul_f32(gq.Q4_K, Wall, X[0], Yt, GEMV_ROWS * COPIES, GEMV_COLS, 1, FLAGS)
+    Yt = torch.empty(1, GEMV_ROWS * COPIES, dtype=torch.float32, device=dev)
+    t_t, _ = time_graph(capture(tall), k_steps, 5)
+    streaming = {"achieved": COPIES * w_bytes / (t_t / k_steps) / 1e9, "unit": "GB/s",
+                 "frac": COPIES * w_bytes / (t_t / k_steps) / 1e9 / hbm_peak,
+                 "workload": "one launch over 262144 x 4096 Q4_K rows (604 MB)"}
 
     # ---- end to end with host buffers: pinned H2D of each x, D2H of each y
     Xh = X.cpu().pin_memory()
@@ -295,25 +325,25 @@ def run_gpu(args, world, rank):
     Xd = torch.empty_like(X)
 
     def e2e_body():
+        Xd.copy_(Xh, non_blocking=True)
         for i in range(COPIES):
-            Xd[i].copy_(Xh[i], non_blocking=True)
-            gq.gq_quantize_rows_async(gq.Q8_K, Xd[i], XQ[i], GEMV_COLS)
-            gq.gq_matmul(gq.Q4_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
-            Yh[i].copy_(Y[i], non_blocking=True)
+            gq.gq_matmul_f32(gq.Q4_K, Wall[i], Xd[i], Y[i], GEMV_ROWS, GEMV_COLS, 1, FLAGS)
+        Yh.copy_(Y, non_blocking=True)
 
     e2e_graph = capture(e2e_body)
     e2e_steps = max(20, args.steps // 4)
     t_e2e, _ = time_graph(e2e_graph, e2e_steps, 3)
     e2e = {"value": world * e2e_steps * COPIES * w_bytes / t_e2e / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": COPIES * GEMV_COLS * 4, "d2h_bytes_per_step": COPIES * GEMV_ROWS * 4,
-           "how": "CUDA graph of the public calls: pinned H2D x, gq_quantize_rows_async, gq_matmul, D2H y"}
-    del Wall, Xh, Yh
+           "how": "CUDA graph of the public calls: one pinned H2D of the 64 activation vectors, "
+                  "64 x gq_matmul_f32, one D2H of the 64 outputs"}
+    del Wall, Xh, Yh, Yt
 
     extras = {}
     if not args.quick:
         extras["decode"] = bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world)
         extras["batch_sweep"] = bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph)
-        extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph)
+        extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -335,9 +365,11 @@ def run_gpu(args, world, rank):
                        "parallelism": f"replicas x{world}", "timing": "CUDA graph, CUDA events"},
             "pct_of_hbm_peak": value / hbm_peak * 100.0,
             "roofline": roofline,
+            "roofline_streaming": streaming,
+            "unfused_step": unfused,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * COPIES * 2,
+            "gpu_launches": args.steps * COPIES,
             "clocks": clk,
         }
         line.update(extras)
@@ -349,7 +381,9 @@ def run_gpu(args, world, rank):
 def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
     """7B-shape decode: 32 layers x (wq, wk, wv, wo, w1, w3, w2) Q4_K GEMVs
     with their activation quantizes, then the Q8_0 output head; one token =
-    one pass.  Layer weights are 32 device copies of one generated layer."""
+    one pass.  Layer weights are 32 device copies of one generated layer.
+    Timed twice: with the standalone act-quant kernel before each group of
+    products sharing an input, and with the act-quant fused into every GEMV."""
     ws, _ = inputs.decode_weights(0)
     layer = {}
     for name, r, c in inputs.DECODE_LAYER:
@@ -367,43 +401,51 @@ def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
     xq["head"] = torch.empty(4096 // 32 * 34, dtype=torch.uint8, device=dev)
     outs = {name: torch.empty(r, dtype=torch.float32, device=dev) for name, r, c in inputs.DECODE_LAYER}
     yh = torch.empty(hr, dtype=torch.float32, device=dev)
-    launches = [0]
+    F = gq.FLAG_W_STATIC
+    G = gq.PATH_GEMV
 
-    def token(count=False):
-        n = 0
+    def token_unfused():
         for lw in layers:
             gq.gq_quantize_rows_async(gq.Q8_K, xin["attn"], xq["attn"], 4096)
             for nm in ("wq", "wk", "wv"):
-                gq.gq_matmul(gq.Q4_K, lw[nm], xq["attn"], outs[nm], 4096, 4096, 1)
+                gq.gq_matmul_ex(gq.Q4_K, lw[nm], xq["attn"], outs[nm], 4096, 4096, 1, G, F)
             gq.gq_quantize_rows_async(gq.Q8_K, xin["o"], xq["o"], 4096)
-            gq.gq_matmul(gq.Q4_K, lw["wo"], xq["o"], outs["wo"], 4096, 4096, 1)
+            gq.gq_matmul_ex(gq.Q4_K, lw["wo"], xq["o"], outs["wo"], 4096, 4096, 1, G, F)
             gq.gq_quantize_rows_async(gq.Q8_K, xin["ffn"], xq["ffn"], 4096)
-            gq.gq_matmul(gq.Q4_K, lw["w1"], xq["ffn"], outs["w1"], 11008, 4096, 1)
-            gq.gq_matmul(gq.Q4_K, lw["w3"], xq["ffn"], outs["w3"], 11008, 4096, 1)
+            gq.gq_matmul_ex(gq.Q4_K, lw["w1"], xq["ffn"], outs["w1"], 11008, 4096, 1, G, F)
+            gq.gq_matmul_ex(gq.Q4_K, lw["w3"], xq["ffn"], outs["w3"], 11008, 4096, 1, G, F)
             gq.gq_quantize_rows_async(gq.Q8_K, xin["down"], xq["down"], 11008)
-            gq.gq_matmul(gq.Q4_K, lw["w2"], xq["down"], outs["w2"], 4096, 11008, 1)
-            n += 11
+            gq.gq_matmul_ex(gq.Q4_K, lw["w2"], xq["down"], outs["w2"], 4096, 11008, 1, G, F)
         gq.gq_quantize_rows_async(gq.Q8_0, xin["head"], xq["head"], 4096)
-        gq.gq_matmul(gq.Q8_0, head, xq["head"], yh, hr, hc, 1)
-        launches[0] = n + 2
+        gq.gq_matmul_ex(gq.Q8_0, head, xq["head"], yh, hr, hc, 1, G, F)
 
-    graph = capture(token)
-    steps = 40
-    t, _ = time_graph(graph, steps, 3)
-    per_tok = t / steps
+    def token_fused():
+        for lw in layers:
+            for nm, x in (("wq", "attn"), ("wk", "attn"), ("wv", "attn"), ("wo", "o"),
+                          ("w1", "ffn"), ("w3", "ffn"), ("w2", "down")):
+                r, c = lw[nm].shape[0], xin[x].numel()
+                gq.gq_matmul_f32(gq.Q4_K, lw[nm], xin[x], outs[nm], r, c, 1, F)
+        gq.gq_matmul_f32(gq.Q8_0, head, xin["head"], yh, hr, hc, 1, F)
+
     bytes_tok = sum(v.numel() for v in layers[0].values()) * L + head.numel()
+    res = {"weight_bytes_per_token": bytes_tok, "tokens_timed": 40,
+           "workload": "7B shapes: 32 x (4 x 4096x4096, 2 x 11008x4096, 4096x11008) Q4_K + "
+                       "32000x4096 Q8_0 head, batch 1"}
+    for name, fn, launches in (("unfused", token_unfused, 32 * 11 + 2), ("fused", token_fused, 32 * 7 + 1)):
+        t, _ = time_graph(capture(fn), 40, 3)
+        per_tok = t / 40
+        res[name] = {"tok_s": world / per_tok, "ms_per_token": per_tok * 1e3,
+                     "weight_gbps": bytes_tok / per_tok / 1e9, "launches_per_token": launches}
+    res["tok_s"] = max(res["unfused"]["tok_s"], res["fused"]["tok_s"])
     del layers, head
     torch.cuda.empty_cache()
-    return {"tok_s": world / per_tok, "ms_per_token": per_tok * 1e3,
-            "weight_bytes_per_token": bytes_tok, "weight_gbps": bytes_tok / per_tok / 1e9,
-            "launches_per_token": launches[0], "tokens_timed": steps,
-            "workload": "7B shapes: 32 x (4 x 4096x4096, 2 x 11008x4096, 4096x11008) Q4_K + "
-                        "32000x4096 Q8_0 head, batch 1, act-quant per input vector"}
+    return res
 
 
 def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
-    """GEMV path on Q4_K 14336x4096 at batch 1..64 (weights rotated over 8
-    copies, 264 MB > L2)."""
+    """Q4_K 14336x4096 at batch 1..64 through both kernel families (weights
+    rotated over 8 copies, 264 MB > L2); the tensor path includes its
+    activation pack kernel."""
     rows, cols, copies = 14336, 4096, 8
     W, X = inputs.gemm_q4_k(0, rows, cols, 64)
     Wq = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
@@ -411,6 +453,7 @@ def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
     Wc = Wq.reshape(1, -1).repeat(copies, 1)
     Xq = gq.quantize(gq.Q8_K, torch.from_numpy(X).to(dev))
     Y = torch.empty(64, rows, dtype=torch.float32, device=dev)
+    wsb = torch.empty(gq.gq_matmul_workspace_bytes(gq.Q4_K, rows, cols, 64), dtype=torch.uint8, device=dev)
     wbytes = Wq.numel()
     out = {}
     for b in (1, 2, 4, 8, 16, 32, 64):
@@ -418,23 +461,21 @@ def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
         for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
             def body():
                 for i in range(copies):
-                    gq.gq_matmul_path(gq.Q4_K, Wc[i], Xq, Y, rows, cols, b, path)
-            try:
-                graph = capture(body)
-            except gq.GQError:
-                continue
+                    gq.gq_matmul_ws(gq.Q4_K, Wc[i], Xq, Y, rows, cols, b, path, gq.FLAG_W_STATIC,
+                                    wsb, wsb.numel())
             steps = 20
-            t, _ = time_graph(graph, steps, 3)
+            t, _ = time_graph(capture(body), steps, 3)
             per = t / (steps * copies)
             res[pname] = {"us": per * 1e6, "weight_gbps": wbytes / per / 1e9,
                           "tops": 2.0 * rows * cols * b / per / 1e12}
+        res["faster"] = min(("gemv", "mma"), key=lambda k: res[k]["us"])
         out[str(b)] = res
-    del Wc, Wq, Xq, Y
+    del Wc, Wq, Xq, Y, wsb
     torch.cuda.empty_cache()
     return {"rows": rows, "cols": cols, "results": out}
 
 
-def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph):
+def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak):
     """Q4_K 28672x8192 weights x 512 Q8_K columns (70B FFN shape)."""
     rows, cols, batch = 28672, 8192, 512
     W, X = inputs.gemm_q4_k(0, rows, cols, batch)
@@ -442,19 +483,19 @@ def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph):
     del W
     Xq = gq.quantize(gq.Q8_K, torch.from_numpy(X).to(dev))
     Y = torch.empty(batch, rows, dtype=torch.float32, device=dev)
+    wsb = torch.empty(gq.gq_matmul_workspace_bytes(gq.Q4_K, rows, cols, batch), dtype=torch.uint8, device=dev)
     res = {}
-    for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
+    for pname, path, steps in (("mma", gq.PATH_MMA, 20), ("gemv", gq.PATH_GEMV, 3)):
         def body():
-            gq.gq_matmul_path(gq.Q4_K, Wq, Xq, Y, rows, cols, batch, path)
-        try:
-            graph = capture(body)
-        except gq.GQError:
-            continue
-        steps = 5
-        t, _ = time_graph(graph, steps, 2)
+            gq.gq_matmul_ws(gq.Q4_K, Wq, Xq, Y, rows, cols, batch, path, gq.FLAG_W_STATIC, wsb, wsb.numel())
+        t, _ = time_graph(capture(body), steps, 2)
         per = t / steps
-        res[pname] = {"ms": per * 1e3, "tops": 2.0 * rows * cols * batch / per / 1e12}
-    del Wq, Xq, Y
+        tops = 2.0 * rows * cols * batch / per / 1e12
+        res[pname] = {"ms": per * 1e3, "tops": tops}
+    res["mma"]["roofline"] = {"bound": "tensor", "achieved": res["mma"]["tops"], "peak": bf16_peak,
+                              "unit": "TFLOP/s", "frac": res["mma"]["tops"] / bf16_peak,
+                              "note": "int ops counted as 2 per multiply-add; fp16 tensor kind"}
+    del Wq, Xq, Y, wsb
     torch.cuda.empty_cache()
     return {"rows": rows, "cols": cols, "batch": batch, "results": res}
 

@@ -19,14 +19,18 @@
 //   y[b][r] += dx(b) * (d(r) * S1 - dmin(r) * S2)      (fp32, in registers)
 //
 // CTA tile: 128 weight rows x 128 batch columns, one super-block (K = 256) per
-// step, 16 warps:
-//   warp 0     producer: TMA bulk copies of raw Q4_K rows, the packed
-//              activation tiles, their min-term tiles and scales;
+// step, 28 warps:
+//   warp 0     activation producer: 1-D bulk copies of the packed B tiles
+//              into their own 6-slot ring (1.5 super-blocks ahead);
 //   warp 1     MMA issuer (one thread) and tensor-memory owner;
-//   warps 4-7  A builders: one thread per weight row turns the raw super-block
-//              into the fp16 A tile (128-byte swizzled K-major), the bf16
-//              min-term row and the row scale d;
-//   warps 8-15 epilogue: two threads per row, 64 columns each.
+//   warp 2     weight producer: one 2-D tiled TMA load per super-block of
+//              the raw Q4_K rows (box 144 bytes x 128 rows; rows past the
+//              matrix read as zeros), the min-term B tile and the scales;
+//   warps 4-11 A builders: two threads per weight row, each turning half of
+//              the raw super-block into two fp16 A stages (128-byte swizzled
+//              K-major); the first half also writes the min-term row and the
+//              row scales d, dmin;
+//   warps 12-27 epilogue: four threads per row, 32 columns each.
 // The activation operand is packed once per call by pack_kernel into a
 // caller-provided workspace, already in the swizzled shared-memory image, so
 // each operand tile is a single 1-D bulk copy.
@@ -34,7 +38,10 @@
 // Every mbarrier wait is bounded; a wait that gives up sets the device status
 // bit and an abort flag that stops all roles of the CTA, which then drains its
 // transfers and frees tensor memory before exiting.
-#include <cuda_bf16.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
@@ -45,14 +52,14 @@ namespace {
 constexpr int TM = 128;   // weight rows per tile (MMA M)
 constexpr int TN = 128;   // batch columns per tile (MMA N)
 constexpr int KS = 64;    // K per operand stage (one 128-byte swizzle atom)
-constexpr int NOP = 4;    // operand stages (= one super-block)
+constexpr int NOP = 4;    // A operand stages (= one super-block)
+constexpr int NBR = 6;    // B operand stages (1.5 super-blocks of lookahead)
 constexpr int NRAW = 2;   // raw weight stages
 constexpr int KMIN = 16;  // min-term K per super-block (8 mins, two halves of t)
 
 // Shared-memory layout (bytes from a 1024-aligned base).
 constexpr int OP_A = TM * KS * 2;                 // 16 KB
 constexpr int OP_B = TN * KS * 2;                 // 16 KB
-constexpr int OP_STAGE = OP_A + OP_B;             // 32 KB
 constexpr int MIN_A = TM * KMIN * 2;              // 4 KB
 constexpr int MIN_B = TN * KMIN * 2;              // 4 KB
 constexpr int MIN_STAGE = MIN_A + MIN_B;          // 8 KB
@@ -61,19 +68,22 @@ constexpr int RAW_STAGE = TM * Q4_K_BYTES;        // 18 KB
 constexpr int META_D = 0, META_DMIN = TM * 4, META_DX = 2 * TM * 4;
 constexpr int META_STAGE = 2 * TM * 4 + TN * 4;
 
-constexpr int OFF_OP = 0;
-constexpr int OFF_MIN = OFF_OP + NOP * OP_STAGE;          // 131072
+constexpr int OFF_A = 0;                                  // NOP x 16 KB
+constexpr int OFF_B = OFF_A + NOP * OP_A;                 // NBR x 16 KB
+constexpr int OFF_MIN = OFF_B + NBR * OP_B;
 constexpr int OFF_RAW = OFF_MIN + 2 * MIN_STAGE;          // 163840
 constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;      // 200704
 constexpr int OFF_BAR = OFF_META + 2 * META_STAGE;        // 202752
-// op: full (builders), full-tx (producer), empty; min: same three; raw: full,
-// empty; meta: full (builders), full-tx, empty; acc: full, empty; final.
-constexpr int NBARS = 3 * NOP + 3 * 2 + 2 * NRAW + 3 * 2 + 2 * 2 + 1;
+// A: full (builders), empty; B: full-tx (producer), empty; min: full
+// (builders), full-tx, empty; raw: full, empty; meta: full (builders),
+// full-tx, empty; acc: full, empty; final.
+constexpr int NBARS = 2 * NOP + 2 * NBR + 3 * 2 + 2 * NRAW + 3 * 2 + 2 * 2 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-static_assert(OFF_OP % 1024 == 0 && OP_STAGE % 1024 == 0 && OP_A % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+static_assert(OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && OP_A % 1024 == 0 && OP_B % 1024 == 0,
+              "SW128 tiles need 1024-byte alignment");
 
 // Workspace (packed activations) per (column tile, super-block).
 constexpr size_t WS_B = (size_t)NOP * OP_B;   // 64 KB, the four B stage images
@@ -87,7 +97,8 @@ constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t col_s1(int p) { return 128u * (uint32_t)p; }
 __host__ __device__ constexpr uint32_t col_s2(int p) { return 256u + 128u * (uint32_t)p; }
 
-constexpr int NTHREADS = 512;
+constexpr int NTHREADS = 896;
+constexpr int EPI_WARP0 = 12, EPI_WARPS = 16, BLD_WARP0 = 4, BLD_THREADS = 256;
 
 // ------------------------------------------------------------ tcgen05 helpers
 
@@ -175,10 +186,10 @@ __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volati
 }
 
 // Ring position: stage index and the parity of its current use.
-struct Ring {
+struct RingPos {
     int n, idx;
     uint32_t phase;
-    __device__ explicit Ring(int stages) : n(stages), idx(0), phase(0) {}
+    __device__ explicit RingPos(int stages) : n(stages), idx(0), phase(0) {}
     __device__ void next() {
         if (++idx == n) {
             idx = 0;
@@ -262,17 +273,18 @@ constexpr uint32_t IDESC_BF16 = idesc_f16(TM, TN, 1);
 // ones and raw_full) tell the producer that a copy has landed; the builders
 // arrive on the plain *_full ones.
 struct Bars {
-    uint64_t *op_full, *op_tx, *op_empty, *min_full, *min_tx, *min_empty, *raw_full, *raw_empty;
+    uint64_t *a_full, *a_empty, *b_tx, *b_empty, *min_full, *min_tx, *min_empty, *raw_full, *raw_empty;
     uint64_t *meta_full, *meta_tx, *meta_empty, *acc_full, *acc_empty, *fin;
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     Bars r;
-    r.op_full = b;
-    r.op_tx = b + NOP;
-    r.op_empty = b + 2 * NOP;
-    r.min_full = b + 3 * NOP;
+    r.a_full = b;
+    r.a_empty = r.a_full + NOP;
+    r.b_tx = r.a_empty + NOP;
+    r.b_empty = r.b_tx + NBR;
+    r.min_full = r.b_empty + NBR;
     r.min_tx = r.min_full + 2;
     r.min_empty = r.min_tx + 2;
     r.raw_full = r.min_empty + 2;
@@ -286,28 +298,58 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     return r;
 }
 
-// Producer (warp 0): raw weight rows one super-block ahead, then per
-// super-block the column scales, the four B stage images and the min-term B
-// tile.  On abort it waits (bounded) for every transfer it started.
-__device__ void role_producer(uint8_t *smem, const Bars &B, const uint8_t *__restrict__ W,
-                              const uint8_t *__restrict__ ws, int row0, int nvalid, int nsb, int ct,
-                              volatile uint32_t *abort) {
+// Producer of the activation operand (warp 0): the four B stage images of
+// every super-block, through a ring of NBR slots.  On abort it waits
+// (bounded) for every copy it started before the CTA may exit.
+__device__ void role_producer_b(uint8_t *smem, const Bars &B, const uint8_t *__restrict__ ws, int nsb,
+                                int ct, volatile uint32_t *abort) {
     const int lane = threadIdx.x & 31;
-    const size_t row_bytes = (size_t)nsb * Q4_K_BYTES;
-    int raw_last[NRAW], op_last[NOP], min_last[2], meta_last[2];
+    int last[NBR];
+    for (int i = 0; i < NBR; ++i) last[i] = -1;
+    RingPos br(NBR);
+    bool ok = true;
+    for (int sb = 0; ok && sb < nsb; ++sb) {
+        const uint8_t *unit = ws + ((size_t)ct * nsb + sb) * WS_UNIT;
+        for (int q = 0; q < NOP; ++q) {
+            if (!(ok = wait_warp(B.b_empty + br.idx, br.phase ^ 1u, abort))) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(B.b_tx + br.idx, OP_B);
+                bulk_g2s(smem + OFF_B + br.idx * OP_B, unit + (size_t)q * OP_B, OP_B, B.b_tx + br.idx);
+            }
+            last[br.idx] = (int)br.phase;
+            br.next();
+        }
+    }
+    if (!ok)
+        for (int i = 0; i < NBR; ++i)
+            if (last[i] >= 0) mbar_wait_bounded(B.b_tx + i, (uint32_t)last[i]);
+}
+
+// Producer of the weight side and the small per-super-block operands
+// (warp 2): the raw Q4_K rows one super-block ahead (one 2-D tiled TMA load,
+// box 144 bytes x 128 rows; rows past the matrix read as zeros), then the
+// min-term B tile and the column scales of the current super-block.
+__device__ void role_producer_w(uint8_t *smem, const Bars &B, const CUtensorMap *tmap_w,
+                                const uint8_t *__restrict__ ws, int row0, int nsb, int ct,
+                                volatile uint32_t *abort) {
+    const int lane = threadIdx.x & 31;
+    int raw_last[NRAW], min_last[2], meta_last[2];
     for (int i = 0; i < NRAW; ++i) raw_last[i] = -1;
-    for (int i = 0; i < NOP; ++i) op_last[i] = -1;
     for (int i = 0; i < 2; ++i) min_last[i] = meta_last[i] = -1;
-    Ring rr(NRAW), orr(NOP), mr(2);
+    RingPos rr(NRAW), mr(2);
 
     auto issue_raw = [&](int sb) -> bool {
         if (!wait_warp(B.raw_empty + rr.idx, rr.phase ^ 1u, abort)) return false;
-        if (lane == 0) mbar_arrive_expect_tx(B.raw_full + rr.idx, (uint32_t)(nvalid * Q4_K_BYTES));
+        if (lane == 0) {
+            mbar_arrive_expect_tx(B.raw_full + rr.idx, RAW_STAGE);
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + OFF_RAW + rr.idx * RAW_STAGE)),
+                "l"(reinterpret_cast<uint64_t>(tmap_w)), "r"(sb * Q4_K_BYTES), "r"(row0),
+                "r"(smem_u32(B.raw_full + rr.idx))
+                : "memory");
+        }
         __syncwarp();
-        uint8_t *dst = smem + OFF_RAW + rr.idx * RAW_STAGE;
-        for (int r = lane; r < nvalid; r += 32)
-            bulk_g2s(dst + r * Q4_K_BYTES, W + (size_t)(row0 + r) * row_bytes + (size_t)sb * Q4_K_BYTES,
-                     Q4_K_BYTES, B.raw_full + rr.idx);
         raw_last[rr.idx] = (int)rr.phase;
         rr.next();
         return true;
@@ -317,6 +359,13 @@ __device__ void role_producer(uint8_t *smem, const Bars &B, const uint8_t *__res
     for (int sb = 0; ok && sb < nsb; ++sb) {
         if (sb + 1 < nsb && !(ok = issue_raw(sb + 1))) break;
         const uint8_t *unit = ws + ((size_t)ct * nsb + sb) * WS_UNIT;
+        if (!(ok = wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort))) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(B.min_tx + mr.idx, MIN_B);
+            bulk_g2s(smem + OFF_MIN + mr.idx * MIN_STAGE + MIN_A, unit + WS_B, MIN_B, B.min_tx + mr.idx);
+        }
+        min_last[mr.idx] = (int)mr.phase;
+        mr.next();
         const int mp = sb & 1;
         const uint32_t mph = (uint32_t)(sb >> 1) & 1u;
         if (!(ok = wait_warp(B.meta_empty + mp, mph ^ 1u, abort))) break;
@@ -326,31 +375,10 @@ __device__ void role_producer(uint8_t *smem, const Bars &B, const uint8_t *__res
                      B.meta_tx + mp);
         }
         meta_last[mp] = (int)mph;
-        for (int q = 0; q < NOP; ++q) {
-            if (!(ok = wait_warp(B.op_empty + orr.idx, orr.phase ^ 1u, abort))) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(B.op_tx + orr.idx, OP_B);
-                bulk_g2s(smem + OFF_OP + orr.idx * OP_STAGE + OP_A, unit + (size_t)q * OP_B, OP_B,
-                         B.op_tx + orr.idx);
-            }
-            op_last[orr.idx] = (int)orr.phase;
-            orr.next();
-        }
-        if (!ok) break;
-        if (!(ok = wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort))) break;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(B.min_tx + mr.idx, MIN_B);
-            bulk_g2s(smem + OFF_MIN + mr.idx * MIN_STAGE + MIN_A, unit + WS_B, MIN_B, B.min_tx + mr.idx);
-        }
-        min_last[mr.idx] = (int)mr.phase;
-        mr.next();
     }
     if (!ok) {
-        // drain: every started transfer completes before the CTA may exit
         for (int i = 0; i < NRAW; ++i)
             if (raw_last[i] >= 0) mbar_wait_bounded(B.raw_full + i, (uint32_t)raw_last[i]);
-        for (int i = 0; i < NOP; ++i)
-            if (op_last[i] >= 0) mbar_wait_bounded(B.op_tx + i, (uint32_t)op_last[i]);
         for (int i = 0; i < 2; ++i) {
             if (min_last[i] >= 0) mbar_wait_bounded(B.min_tx + i, (uint32_t)min_last[i]);
             if (meta_last[i] >= 0) mbar_wait_bounded(B.meta_tx + i, (uint32_t)meta_last[i]);
@@ -378,49 +406,45 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
                       bits_h2(__hfma2(p2, s1, c1)), bits_h2(__hfma2(p3, s16, c16)));
 }
 
-// A builders (warps 4-7): thread t = tile row t.
-__device__ void role_builder(uint8_t *smem, const Bars &B, int t, int nvalid, int nsb,
+// A builders (warps 4-11): thread idx -> tile row t = idx % 128 and half
+// hh = idx / 128, which builds operand stages 2hh and 2hh + 1 (sub-blocks
+// 4hh .. 4hh + 3).  Stage q of every super-block uses ring slot q, so each
+// half owns its two slots; the ring parity is the super-block's.
+__device__ void role_builder(uint8_t *smem, const Bars &B, int idx, int nvalid, int nsb,
                              volatile uint32_t *abort) {
     const int lane = threadIdx.x & 31;
+    const int t = idx & (TM - 1), hh = idx >> 7;
     const bool valid = t < nvalid;
-    Ring rr(NRAW), orr(NOP), mr(2);
+    RingPos rr(NRAW), mr(2);
     for (int sb = 0; sb < nsb; ++sb) {
         const int mp = sb & 1;
+        const uint32_t par = (uint32_t)sb & 1u;
         const uint32_t mph = (uint32_t)(sb >> 1) & 1u;
         if (!wait_warp(B.raw_full + rr.idx, rr.phase, abort)) return;
         const uint8_t *raw = smem + OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
-        uint4 h = make_uint4(0, 0, 0, 0), q[8];
+        uint4 h = make_uint4(0, 0, 0, 0), q[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) q[j] = make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < 4; ++j) q[j] = make_uint4(0, 0, 0, 0);
         if (valid) {
             h = *reinterpret_cast<const uint4 *>(raw);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) q[j] = *reinterpret_cast<const uint4 *>(raw + 16 + 16 * j);
+            for (int j = 0; j < 4; ++j) q[j] = *reinterpret_cast<const uint4 *>(raw + 16 + 16 * (4 * hh + j));
         }
         mbar_arrive(B.raw_empty + rr.idx);
         rr.next();
 
-        // header: d, dmin, sixteen 6-bit fields LSB-first from byte 4
-        const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
-        const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);
-        int sc[8], mn[8];
+        if (hh == 0) {
+            // row scales and the min-term row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
+            const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);
+            int mn[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            sc[j] = (int)((lo64 >> (6 * j)) & 63);
-            mn[j] = (int)((hi64 >> (6 * j + 16)) & 63);
-        }
-        const float dmin = half_bits_to_float(h.x >> 16);
-
-        // row scales
-        if (!wait_warp(B.meta_empty + mp, mph ^ 1u, abort)) return;
-        uint8_t *meta = smem + OFF_META + mp * META_STAGE;
-        reinterpret_cast<float *>(meta + META_D)[t] = half_bits_to_float(h.x);
-        reinterpret_cast<float *>(meta + META_DMIN)[t] = dmin;
-        mbar_arrive(B.meta_full + mp);
-
-        // min-term row: [m_0..m_7 | 64 m_0..64 m_7] in fp16 (exact)
-        if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-        {
+            for (int j = 0; j < 8; ++j) mn[j] = (int)((hi64 >> (6 * j + 16)) & 63);
+            if (!wait_warp(B.meta_empty + mp, mph ^ 1u, abort)) return;
+            uint8_t *meta = smem + OFF_META + mp * META_STAGE;
+            reinterpret_cast<float *>(meta + META_D)[t] = half_bits_to_float(h.x);
+            reinterpret_cast<float *>(meta + META_DMIN)[t] = half_bits_to_float(h.x >> 16);
+            mbar_arrive(B.meta_full + mp);
+            if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
             uint8_t *ma = smem + OFF_MIN + mr.idx * MIN_STAGE;
             if (valid) {
                 uint32_t lo[4], hi[4];
@@ -438,18 +462,20 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, int t, int nvalid, in
             mr.next();
         }
 
-        // four operand stages of 64 K (two sub-blocks each)
+        // this half's two operand stages of 64 K (two sub-blocks each)
+        const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
 #pragma unroll
-        for (int qq = 0; qq < NOP; ++qq) {
-            if (!wait_warp(B.op_empty + orr.idx, orr.phase ^ 1u, abort)) return;
-            uint8_t *A = smem + OFF_OP + orr.idx * OP_STAGE;
+        for (int k = 0; k < 2; ++k) {
+            const int slot = 2 * hh + k;
+            if (!wait_warp(B.a_empty + slot, par ^ 1u, abort)) return;
+            uint8_t *A = smem + OFF_A + slot * OP_A;
             if (valid) {
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * qq + jj;
-                    const float s = (float)sc[j];
-                    const __half2 s1 = __float2half2_rn(s), c1 = __float2half2_rn(-1024.0f * s);
-                    const __half2 s16 = __float2half2_rn(s * 0.0625f), c16 = __float2half2_rn(-64.0f * s);
+                    const int j = 2 * k + jj;  // sub-block within this half
+                    const float sc = (float)(int)((lo64 >> (6 * (4 * hh + j))) & 63);
+                    const __half2 s1 = __float2half2_rn(sc), c1 = __float2half2_rn(-1024.0f * sc);
+                    const __half2 s16 = __float2half2_rn(sc * 0.0625f), c16 = __float2half2_rn(-64.0f * sc);
                     const uint32_t wd[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -459,8 +485,7 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, int t, int nvalid, in
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(B.op_full + orr.idx);
-            orr.next();
+            if (lane == 0) mbar_arrive(B.a_full + slot);
         }
     }
 }
@@ -471,7 +496,7 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, int t, int nvalid, in
 // accumulator.  Always ends with a commit to `fin` so the epilogue (and the
 // teardown) can wait for every MMA to finish.
 __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, volatile uint32_t *abort) {
-    Ring orr(NOP), mr(2);
+    RingPos orr(NOP), br(NBR), mr(2);
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
         const int p = sb & 1;
@@ -479,17 +504,19 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
         if (!(ok = wait_or_abort(B.acc_empty + p, ph ^ 1u, abort))) break;
         tc_fence_after();
         for (int qq = 0; qq < NOP; ++qq) {
-            if (!(ok = wait_or_abort(B.op_full + orr.idx, orr.phase, abort))) break;
-            if (!(ok = wait_or_abort(B.op_tx + orr.idx, orr.phase, abort))) break;
+            if (!(ok = wait_or_abort(B.a_full + orr.idx, orr.phase, abort))) break;
+            if (!(ok = wait_or_abort(B.b_tx + br.idx, br.phase, abort))) break;
             tc_fence_after();
-            const uint32_t a = smem_u32(smem + OFF_OP + orr.idx * OP_STAGE);
-            const uint32_t b = a + OP_A;
+            const uint32_t a = smem_u32(smem + OFF_A + orr.idx * OP_A);
+            const uint32_t b = smem_u32(smem + OFF_B + br.idx * OP_B);
 #pragma unroll
             for (int kk = 0; kk < KS / 16; ++kk)
                 mma_f16(tmem + col_s1(p), desc_sw128(a + 32 * kk), desc_sw128(b + 32 * kk), IDESC_F16,
                         (qq | kk) != 0);
-            mma_commit(B.op_empty + orr.idx);
+            mma_commit(B.a_empty + orr.idx);  // both slots free once these MMAs complete
+            mma_commit(B.b_empty + br.idx);
             orr.next();
+            br.next();
         }
         if (!ok) break;
         if (!(ok = wait_or_abort(B.min_full + mr.idx, mr.phase, abort))) break;
@@ -504,20 +531,20 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
     mma_commit(B.fin);
 }
 
-// Epilogue (warps 8-15): warp w reads tensor-memory lanes 32 (w % 4) .. + 31
-// (its 32 rows) and columns 64 h .. + 63, h = (w - 8) / 4.
+// Epilogue (warps 12-27): warp w reads tensor-memory lanes 32 (w % 4) .. + 31
+// (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4.
 template <bool SUMS>
 __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int row0, int rows, int ct,
                               int nsb, int batch, float *__restrict__ y, int32_t *__restrict__ sums,
                               const uint8_t *__restrict__ xq, volatile uint32_t *abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int lq = warp & 3, h = (warp - 8) >> 2;
+    const int lq = warp & 3, h = (warp - EPI_WARP0) >> 2;
     const int r = lq * 32 + lane;
     const int row = row0 + r;
-    const uint32_t lane_addr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(64 * h);
-    float yacc[64];
+    const uint32_t lane_addr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(32 * h);
+    float yacc[32];
 #pragma unroll
-    for (int c = 0; c < 64; ++c) yacc[c] = 0.0f;
+    for (int c = 0; c < 32; ++c) yacc[c] = 0.0f;
     bool ok = true;
     for (int sb = 0; sb < nsb; ++sb) {
         const int p = sb & 1;
@@ -529,16 +556,16 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
         const uint8_t *meta = smem + OFF_META + p * META_STAGE;
         const float d = reinterpret_cast<const float *>(meta + META_D)[r];
         const float dmin = reinterpret_cast<const float *>(meta + META_DMIN)[r];
-        const float *dx = reinterpret_cast<const float *>(meta + META_DX) + 64 * h;
+        const float *dx = reinterpret_cast<const float *>(meta + META_DX) + 32 * h;
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
+        for (int c0 = 0; c0 < 32; c0 += 16) {
             float s1[16], s2[16];
             tmem_ld16(lane_addr + col_s1(p) + c0, s1);
             tmem_ld16(lane_addr + col_s2(p) + c0, s2);
             if (SUMS) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int b = ct * TN + 64 * h + c0 + i;
+                    const int b = ct * TN + 32 * h + c0 + i;
                     if (row < rows && b < batch) {
                         int32_t *o = sums + (((size_t)b * rows + row) * nsb + sb) * 2;
                         o[0] = (int32_t)s1[i];
@@ -561,15 +588,15 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
     if (!ok || SUMS) return;
     if (row < rows) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const int b = ct * TN + 64 * h + c;
+        for (int c = 0; c < 32; ++c) {
+            const int b = ct * TN + 32 * h + c;
             if (b < batch) y[(size_t)b * rows + row] = yacc[c];
         }
     }
 }
 
 template <bool SUMS>
-__global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const uint8_t *__restrict__ W,
+__global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                                               const uint8_t *__restrict__ ws,
                                                               const uint8_t *__restrict__ xq,
                                                               float *__restrict__ y,
@@ -582,14 +609,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const uint8_t *__r
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = blockIdx.x * TM, ct = blockIdx.y;
+    // column tiles vary fastest, so the CTAs that read the same weight rows
+    // run together and share them through L2
+    const int row0 = blockIdx.y * TM, ct = blockIdx.x;
     const int nvalid = min(TM, rows - row0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NOP; ++i) {
-            mbar_init(B.op_full + i, 4);
-            mbar_init(B.op_tx + i, 1);
-            mbar_init(B.op_empty + i, 1);
+            mbar_init(B.a_full + i, 4);
+            mbar_init(B.a_empty + i, 1);
+        }
+        for (int i = 0; i < NBR; ++i) {
+            mbar_init(B.b_tx + i, 1);
+            mbar_init(B.b_empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(B.min_full + i, 4);
@@ -597,13 +629,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const uint8_t *__r
             mbar_init(B.min_empty + i, 1);
             mbar_init(B.meta_full + i, TM);
             mbar_init(B.meta_tx + i, 1);
-            mbar_init(B.meta_empty + i, 8);
+            mbar_init(B.meta_empty + i, EPI_WARPS);
             mbar_init(B.acc_full + i, 1);
-            mbar_init(B.acc_empty + i, 8);
+            mbar_init(B.acc_empty + i, EPI_WARPS);
         }
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
-            mbar_init(B.raw_empty + i, TM);
+            mbar_init(B.raw_empty + i, BLD_THREADS);
         }
         mbar_init(B.fin, 1);
         *abort = 0u;
@@ -622,13 +654,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const uint8_t *__r
     pdl_wait();  // the packed activations come from the preceding kernel
 
     if (warp == 0) {
-        role_producer(smem, B, W, ws, row0, nvalid, nsb, ct, abort);
+        role_producer_b(smem, B, ws, nsb, ct, abort);
+    } else if (warp == 2) {
+        role_producer_w(smem, B, &tmap_w, ws, row0, nsb, ct, abort);
     } else if (warp == 1) {
         if (lane == 0) role_mma(smem, B, tmem, nsb, abort);
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
-        role_builder(smem, B, threadIdx.x - 128, nvalid, nsb, abort);
-    } else if (warp >= 8) {
+    } else if (warp >= BLD_WARP0 && warp < EPI_WARP0) {
+        role_builder(smem, B, threadIdx.x - 32 * BLD_WARP0, nvalid, nsb, abort);
+    } else if (warp >= EPI_WARP0) {
         role_epilogue<SUMS>(smem, B, tmem, row0, rows, ct, nsb, batch, y, sums, xq, abort);
     }
     pdl_launch_dependents();
@@ -660,29 +694,59 @@ size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch) {
     return (size_t)((batch + TN - 1) / TN) * (size_t)(cols / QK_K) * WS_UNIT;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link
+// dependency on the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
                            int64_t cols, int64_t batch, void *workspace, const LaunchCtx &ctx) {
     const int nsb = (int)(cols / QK_K);
     const int ctiles = (int)((batch + TN - 1) / TN);
+    const int rtiles = (int)((rows + TM - 1) / TM);
+    if (rtiles > 65535) return cudaErrorInvalidConfiguration;
+    // W as a 2-D byte tensor: rows of nsb * 144 bytes; box = one super-block
+    // (144 bytes) of 128 rows
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    CUtensorMap tmap;
+    const cuuint64_t gdim[2] = {(cuuint64_t)nsb * Q4_K_BYTES, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)nsb * Q4_K_BYTES};
+    const cuuint32_t box[2] = {(cuuint32_t)Q4_K_BYTES, (cuuint32_t)TM};
+    const cuuint32_t estride[2] = {1, 1};
+    if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     cudaError_t e = launch_pdl(pack_kernel, dim3(nsb, ctiles), dim3(256), 0, ctx.stream,
                                static_cast<const uint8_t *>(xq), ws, nsb, (int)batch);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((rows + TM - 1) / TM), (unsigned)ctiles);
+    const dim3 grid((unsigned)ctiles, (unsigned)rtiles);
     if (sums) {
         auto k = mma_q4k_kernel<true>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, static_cast<const uint8_t *>(W),
-                          (const uint8_t *)ws, static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb,
-                          (int)batch, ctx.status);
+        return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
+                          static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb, (int)batch, ctx.status);
     }
     auto k = mma_q4k_kernel<false>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, static_cast<const uint8_t *>(W),
-                      (const uint8_t *)ws, static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb,
-                      (int)batch, ctx.status);
+    return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
+                      static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb, (int)batch, ctx.status);
 }
 
 }  // namespace gq
