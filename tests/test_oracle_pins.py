@@ -386,3 +386,11 @@ def test_tolerance_scale_is_sum_of_magnitudes():
     W2 = inputs.normal(g, (3, 256))
     y2, T2 = orc.matmul_ref(Q8_0, orc.quantize(Q8_0, W2), orc.quantize(Q8_0, X), 3, 256, 2)
     assert np.all(T2 >= np.abs(y2))
+
+
+@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q4_K, Q8_K])
+def test_multithreaded_quantize_equals_blockwise(t):
+    """The row-parallel quantizer used for timing is the pinned one, row by row."""
+    be = orc.block_elems(t)
+    x = inputs.outlier_weights(inputs.rng(17), 33, 4 * be, frac=0.01)
+    np.testing.assert_array_equal(orc.quantize_rows_mt(t, x, 4), orc.quantize(t, x))
