@@ -281,6 +281,24 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
     return mma_workspace_bytes(rows, cols, batch);
 }
 
+gq_status gq_matmul_noalloc(gq_type wtype, const void *W, const void *xq, float *y, int64_t rows,
+                            int64_t cols, int64_t batch, gq_stream_t stream) {
+    if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+    gq_status st = check_matmul(wtype, W, xq, y, rows, cols, batch, 4);
+    if (st != GQ_OK || rows == 0 || cols == 0 || batch == 0) return st;
+    if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+    const size_t need = mma_workspace_bytes(rows, cols, batch);
+    if (need > mma_noalloc_scratch_bytes()) return GQ_ERR_SHAPE;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    void *scratch = nullptr;
+    cudaError_t e = mma_noalloc_scratch(ctx.device, &scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_matmul(wtype, W, xq, y, nullptr, rows, cols, batch, GQ_PATH_MMA, 0, false, scratch,
+                      mma_noalloc_scratch_bytes(), stream);
+}
+
 int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }
 
 gq_status gq_device_status(uint32_t *word, int reset) {

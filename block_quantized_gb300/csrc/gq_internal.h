@@ -55,5 +55,10 @@ cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sum
                            int64_t cols, int64_t batch, void *workspace, const LaunchCtx &ctx);
 bool mma_supported(int64_t rows, int64_t cols, int64_t batch);
 size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch);
+// The library's static scratch (no allocation): its size, and its device
+// address on `device` (looked up on the first call for that device, which
+// must be the current device).
+size_t mma_noalloc_scratch_bytes();
+cudaError_t mma_noalloc_scratch(int device, void **ptr);
 
 }  // namespace gq

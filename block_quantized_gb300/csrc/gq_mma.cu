@@ -694,6 +694,22 @@ size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch) {
     return (size_t)((batch + TN - 1) / TN) * (size_t)(cols / QK_K) * WS_UNIT;
 }
 
+// Static scratch for callers that cannot allocate device memory (see
+// gq_matmul_noalloc in gq.h).  It is module-scope device memory: every GPU
+// that loads this library holds these bytes until the process exits.  Host
+// code must never hand the symbol itself to a kernel -- on the host it only
+// names the array; the device address comes from cudaGetSymbolAddress.
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)16 << 20;  // 16 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+struct ScratchSlot {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+ScratchSlot g_scratch_slot[NOALLOC_MAX_DEVICES];
+
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link
 // dependency on the driver library).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -747,6 +763,22 @@ cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sum
     if (e != cudaSuccess) return e;
     return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
                       static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb, (int)batch, ctx.status);
+}
+
+size_t mma_noalloc_scratch_bytes() { return NOALLOC_SCRATCH_BYTES; }
+
+// Device address of the static scratch on the current device, resolved once
+// per device (with that device current) on the first call there.
+cudaError_t mma_noalloc_scratch(int device, void **ptr) {
+    if (device < 0 || device >= NOALLOC_MAX_DEVICES) return cudaErrorInvalidDevice;
+    ScratchSlot &slot = g_scratch_slot[device];
+    std::call_once(slot.once, [&slot]() {
+        void *p = nullptr;
+        slot.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        slot.ptr = p;
+    });
+    *ptr = slot.ptr;
+    return slot.err;
 }
 
 }  // namespace gq

@@ -50,6 +50,7 @@ SIGNATURES = {
                       ctypes.c_size_t, _vp], _i32),
     "gq_block_sums_ws": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, ctypes.c_size_t,
                           _vp], _i32),
+    "gq_matmul_noalloc": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
     "gq_tc_min_batch": ([], _i64),
     "gq_device_status": ([_u32p, _i32], _i32),
 }
@@ -192,6 +193,14 @@ def gq_block_sums_ws(wtype: int, W, xq, sums, rows: int, cols: int, batch: int, 
     _check("gq_block_sums_ws", load().gq_block_sums_ws(wtype, _p(W), _p(xq), _p(sums), rows, cols,
                                                        batch, path, _p(workspace), workspace_bytes,
                                                        _s(stream)))
+
+
+def gq_matmul_noalloc(wtype: int, W, xq, y, rows: int, cols: int, batch: int,
+                      stream=None) -> None:
+    """Tensor-core product using the library's static scratch (no allocation
+    anywhere); see gq.h for the size limit and the sharing rules."""
+    _check("gq_matmul_noalloc", load().gq_matmul_noalloc(wtype, _p(W), _p(xq), _p(y), rows, cols,
+                                                         batch, _s(stream)))
 
 
 def gq_tc_min_batch() -> int:

@@ -250,6 +250,35 @@ gq_status gq_block_sums_ws(gq_type wtype, const void *W, const void *xq, int32_t
 gq_status gq_block_sums_f32(gq_type wtype, const void *W, const float *x, int32_t *sums,
                             int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
 
+/*
+ * The tensor-core product for callers that cannot allocate device memory.
+ * The pages describe no such call; it exists for users of this library who
+ * must not call cudaMalloc themselves: hosts that own the GPU's memory pool
+ * and forbid other allocators, services that plan every byte at start-up and
+ * may not allocate on the request path, and callers for whom cudaMalloc's
+ * implicit device synchronisation would stall a latency-sensitive pipeline.
+ * The call is gq_matmul_ws(wtype, W, xq, y, rows, cols, batch, GQ_PATH_MMA,
+ * 0, workspace, ...) except that the workspace is a fixed 16 MiB scratch
+ * array inside the library (module-scope device memory that every GPU
+ * loading the library holds until the process exits).  Nothing is
+ * allocated or freed.
+ *   - wtype must be GQ_Q4_K (GQ_ERR_TYPE otherwise); other arguments,
+ *     alignment and errors as gq_matmul.
+ *   - A product whose workspace (gq_matmul_workspace_bytes) exceeds
+ *     16 MiB = 16777216 bytes is rejected with GQ_ERR_SHAPE before anything
+ *     is launched; e.g. 8192 columns allow batches up to 896, 4096 columns
+ *     up to 1792.
+ *   - The first call on a device looks up the scratch's device address with
+ *     that device current (cudaGetSymbolAddress); make that first call
+ *     before any stream capture on the device.
+ *   - Every call shares the one scratch array, and it keeps the previous
+ *     call's contents: each call rewrites every scratch byte it reads, so no
+ *     clearing is needed, but calls that overlap on the GPU (different
+ *     streams, or different host threads) race on it and give wrong results.
+ */
+gq_status gq_matmul_noalloc(gq_type wtype, const void *W, const void *xq, float *y,
+                            int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
+
 /* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
  * Q4_K (the measured crossover; the environment variable GQ_TC_MIN_BATCH,
  * read once, overrides it). */
