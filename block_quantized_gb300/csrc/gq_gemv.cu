@@ -9,20 +9,28 @@
 // integers (sc_j * s_j, m_j * t_j) before one float scaling per super-block.
 // Token generation is bound by memory bandwidth ("llama.cpp 推理引擎" §7.3),
 // so the kernels are built to stream the weights once at HBM speed:
-//   - every warp owns whole rows (grid-stride over rows, a persistent grid
-//     of a few CTAs per SM for tall matrices) and streams each row through
-//     its own two-stage shared-memory ring, filled by the TMA engine
-//     (cp.async.bulk, ~2.3 KB chunks, completion on an mbarrier; every wait
-//     is bounded);
+//   - a persistent grid of one CTA per SM; every warp owns whole row groups
+//     (grid-stride) and streams them through its own shared-memory ring,
+//     filled by the TMA engine (cp.async.bulk, completion on an mbarrier,
+//     every wait bounded).  A ring item is up to four whole rows in one bulk
+//     copy (9 KB at 4096 columns) when a row fits in one 16-super-block
+//     chunk, else one chunk of one row; the ring depth per warp is chosen per
+//     launch so a small matrix is requested in full before the dependency
+//     wait and a tall one keeps ~150 KB per SM in flight;
 //   - the CTA's activation vectors are staged once in shared memory, each
 //     group of 8 int8 codes stored as (a0,a2,a4,a6 | a1,a3,a5,a7) so a
 //     packed nibble word w feeds dp4a as (w & 0x0F0F0F0F) and
-//     ((w >> 4) & 0x0F0F0F0F); the fused variants quantize fp32
-//     activations straight into that layout (same arithmetic as the
-//     standalone quantizer, so the codes are identical);
+//     (w & 0xF0F0F0F0) (high nibbles in place, sum divided by 16); the
+//     fused variants quantize fp32 activations straight into that layout
+//     (same arithmetic as the standalone quantizer, so the codes are
+//     identical);
+//   - Q4_K: a lane takes half a super-block (four sub-blocks), so one warp
+//     instruction covers a 16-super-block row chunk; at batch 1 the lane's
+//     activation slice stays in registers and the rows of an item are
+//     interleaved, with one transposed butterfly reducing all of them;
 //   - Q4_0 / Q8_0 blocks (18 / 34 bytes, 2-byte aligned) are read from the
 //     ring with aligned 32-bit loads and funnel shifts;
-//   - per-lane fp32 partial sums, one warp-shuffle reduction per row.
+//   - per-lane fp32 partial sums, warp-shuffle reductions per row.
 #include <algorithm>
 
 #include "gq_common.cuh"
@@ -34,24 +42,26 @@ namespace {
 constexpr uint32_t NIB = 0x0F0F0F0Fu;
 constexpr unsigned FULL = 0xffffffffu;
 // Launch-shape parameters (compile-time; the defaults are the measured best).
-#ifndef GQ_GEMV_NSTAGE
-#define GQ_GEMV_NSTAGE 2
-#endif
-#ifndef GQ_GEMV_ROWS_PER_WARP
-#define GQ_GEMV_ROWS_PER_WARP 2
-#endif
 #ifndef GQ_GEMV_CTAS_PER_SM
-#define GQ_GEMV_CTAS_PER_SM 4
+#define GQ_GEMV_CTAS_PER_SM 1
 #endif
-#ifndef GQ_GEMV_Q4K_CHUNK
-#define GQ_GEMV_Q4K_CHUNK 16
+#ifndef GQ_GEMV_RING_BUDGET
+#define GQ_GEMV_RING_BUDGET (150 * 1024)
 #endif
 #ifndef GQ_GEMV_EARLY_TRIGGER
 #define GQ_GEMV_EARLY_TRIGGER 0
 #endif
+#ifndef GQ_GEMV_WARPS
+#define GQ_GEMV_WARPS 8
+#endif
+#ifndef GQ_GEMV_MAX_R
+#define GQ_GEMV_MAX_R 4
+#endif
+#ifndef GQ_GEMV_MIN_BLOCKS
+#define GQ_GEMV_MIN_BLOCKS 1
+#endif
 
-constexpr int WARPS = 8;                  // warps per CTA
-constexpr int NSTAGE = GQ_GEMV_NSTAGE;    // ring stages per warp
+constexpr int WARPS = GQ_GEMV_WARPS;      // warps per CTA
 
 // Weight formats as seen by the streaming kernel: block bytes, elements per
 // block, and blocks per ring chunk (chunks are 16-byte multiples).
@@ -67,20 +77,10 @@ struct Fmt<GQ_Q8_0> {
 };
 template <>
 struct Fmt<GQ_Q4_K> {
-    static constexpr int BB = Q4_K_BYTES, BE = 256, CH = GQ_GEMV_Q4K_CHUNK;  // 2304-byte chunks
+    // 2304-byte chunks: one super-block per lane pair
+    static constexpr int BB = Q4_K_BYTES, BE = 256, CH = 16;
 };
 
-template <int WT, int NW>
-struct Ring {
-    static constexpr int CHUNK = Fmt<WT>::CH * Fmt<WT>::BB;
-    static constexpr int BUF = ((CHUNK + 16 + 15) / 16) * 16;  // +16: over-read slack
-    // WARPS * NSTAGE mbarriers of 8 bytes come first, then the ring buffers
-    static constexpr int BARS_BYTES = NW * NSTAGE * 8;
-    static constexpr int BUFS_OFF = ((BARS_BYTES + 127) / 128) * 128;
-    static_assert(BUFS_OFF >= BARS_BYTES, "mbarriers must not overlap the ring");
-    static_assert(BUFS_OFF % 16 == 0 && BUF % 16 == 0, "bulk-copy destinations are 16-byte aligned");
-    static constexpr int ACT_OFF = BUFS_OFF + NW * NSTAGE * BUF;
-};
 
 // Staged activations.  Q8_K (for Q4_K weights): per vector and super-block
 // 256 code bytes, the fp32 scale and the eight sub-block sums.  Q8_0 (for
@@ -97,14 +97,33 @@ __host__ __device__ constexpr int act_block_bytes() {
     return WT == GQ_Q4_K ? 256 + 4 + 32 : 32 + 4 + 4;
 }
 
+// Q8_K: codes, then the sub-block sums (16-byte aligned for vector loads),
+// then the scales.  Q8_0: codes, scales, sums.
 template <int WT>
 __device__ __forceinline__ Act act_layout(uint8_t *base, int nb, int nblk) {
-    constexpr int CB = WT == GQ_Q4_K ? 256 : 32;
     Act a;
     a.codes = base;
-    a.dx = reinterpret_cast<float *>(base + (size_t)nb * nblk * CB);
-    a.isum = reinterpret_cast<int32_t *>(a.dx + (size_t)nb * nblk);
+    if (WT == GQ_Q4_K) {
+        a.isum = reinterpret_cast<int32_t *>(base + (size_t)nb * nblk * 256);
+        a.dx = reinterpret_cast<float *>(a.isum + (size_t)nb * nblk * 8);
+    } else {
+        a.dx = reinterpret_cast<float *>(base + (size_t)nb * nblk * 32);
+        a.isum = reinterpret_cast<int32_t *>(a.dx + (size_t)nb * nblk);
+    }
     return a;
+}
+
+// Q8_K codes of one super-block are kept as 16 units of 16 bytes.  Half h
+// (sub-blocks 4h..4h+3) owns units 8h..8h+7; its logical unit k' holds code
+// groups 2k' and 2k'+1 of that half (each group = 8 codes in the split order
+// of split8), and is stored at unit 8h + (k' ^ ((2 sb + h) & 7)) so that the
+// eight lanes of a quarter-warp, which read the same k' of consecutive
+// half-super-blocks, hit eight different bank quads.  sb is the super-block's
+// index within its vector; g is the code group (0..31) within the super-block.
+__device__ __forceinline__ int q8k_group_off(int sb, int g) {
+    const int j = g >> 2, i = g & 3, h = j >> 2;
+    const int kp = 2 * (j & 3) + (i >> 1);
+    return 128 * h + 16 * (kp ^ ((2 * sb + h) & 7)) + 8 * (i & 1);
 }
 
 __device__ __forceinline__ uint2 split8(uint32_t a0, uint32_t a1) {
@@ -115,7 +134,7 @@ __device__ __forceinline__ uint2 split8(uint32_t a0, uint32_t a1) {
 // All loads of a pass are issued before any store, so a pass costs one
 // L2 round trip.
 
-__device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nblocks) {
+__device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nblocks, int nsb) {
     const int groups = nblocks * 32;
     // pass p copies groups [4p*T, 4(p+1)*T) and block headers [p*T, (p+1)*T)
     // (T = blockDim.x); there are at least as many group passes as header
@@ -144,7 +163,11 @@ __device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nbl
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int g = base + u * blockDim.x + threadIdx.x;
-            if (g < groups) reinterpret_cast<uint2 *>(a.codes)[g] = split8(w0[u], w1[u]);
+            if (g < groups) {
+                const int blk = g >> 5;
+                *reinterpret_cast<uint2 *>(a.codes + (size_t)blk * 256 + q8k_group_off(blk % nsb, g & 31)) =
+                    split8(w0[u], w1[u]);
+            }
         }
         if (has_h) {
             a.dx[hb] = __uint_as_float(hd[0]);
@@ -204,7 +227,7 @@ __device__ __forceinline__ float clamp127(float v) {
 
 // Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
 // (= code group l of the layout).
-__device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks) {
+__device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks, int nsb) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     for (int b0 = warp; b0 < nblocks; b0 += 2 * nw) {
         float4 v[2][2];
@@ -240,7 +263,8 @@ __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int 
                 else
                     w1 |= (uint32_t)(qi & 0xff) << (8 * (i - 4));
             }
-            reinterpret_cast<uint2 *>(a.codes)[(size_t)blk * 32 + lane] = split8(w0, w1);
+            *reinterpret_cast<uint2 *>(a.codes + (size_t)blk * 256 + q8k_group_off(blk % nsb, lane)) =
+                split8(w0, w1);
             sum += __shfl_xor_sync(FULL, sum, 1);
             sum += __shfl_xor_sync(FULL, sum, 2);
             if ((lane & 3) == 0) a.isum[blk * 8 + (lane >> 2)] = sum;
@@ -285,67 +309,152 @@ __device__ void quant_stage_q8_0(const Act &a, const float *__restrict__ x, int 
 
 // ------------------------------------------------------------ chunk compute
 
-// Q4_K chunk of nb_c super-blocks starting at super-block sb0 of the row.
-// Lane = sub-block j = lane & 7 of super-block 4t + (lane >> 3).
-// The high nibbles are used in place (bytes 16 q, unsigned) and the second
-// dp4a chain's sum divided by 16 -- exact, every term is a multiple of 16.
+// Q4_K chunk: nb_c (<= 16) super-blocks of one row, starting at super-block
+// sb0.  Lane l takes half h = l & 1 (sub-blocks 4h..4h+3) of super-block
+// l >> 1, so one warp instruction covers the whole chunk: per lane four
+// 16-byte nibble loads, one (pair-shared) header load, 32 dp4a, and one
+// float update for the pair of integer sums
+//   S1 = sum_j sc_j * s_j,   S2 = sum_j m_j * t_j   (j over the half)
+// with s_j the sub-block integer dot and t_j the Q8_K sub-block sum.  The
+// high nibbles are used in place (values 16 q, unsigned) and that dp4a
+// chain's sum is divided by 16 -- exact, every term is a multiple of 16.
+// The lane's activation slice (8 units of 16 codes, the four t_j and the
+// vector scale) lives in registers: loaded once per kernel when the row has
+// a single chunk and NB == 1, else reloaded per chunk and vector.
+struct Q4KAct {
+    uint4 u[8];
+    int4 t;
+    float dx;
+};
+
+__device__ __forceinline__ void load_q4k_act(Q4KAct &r, const Act &a, int blk, int h, int sw) {
+    const uint4 *u = reinterpret_cast<const uint4 *>(a.codes + (size_t)blk * 256 + 128 * h);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r.u[k] = u[k ^ sw];
+    r.t = reinterpret_cast<const int4 *>(a.isum + (size_t)blk * 8)[h];
+    r.dx = a.dx[blk];
+}
+
+__device__ __forceinline__ void dot_q4k_half(const uint4 (&q)[4], const Q4KAct &r, uint32_t sc24,
+                                             uint32_t m24, int &S1, int &S2) {
+    const int t[4] = {r.t.x, r.t.y, r.t.z, r.t.w};
+    S1 = 0;
+    S2 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint4 w = q[k], a0 = r.u[2 * k], a1 = r.u[2 * k + 1];
+        int sl = dp4a_us(w.x & NIB, (int)a0.x, 0), sh = dp4a_us(w.x & ~NIB, (int)a0.y, 0);
+        sl = dp4a_us(w.y & NIB, (int)a0.z, sl);
+        sh = dp4a_us(w.y & ~NIB, (int)a0.w, sh);
+        sl = dp4a_us(w.z & NIB, (int)a1.x, sl);
+        sh = dp4a_us(w.z & ~NIB, (int)a1.y, sh);
+        sl = dp4a_us(w.w & NIB, (int)a1.z, sl);
+        sh = dp4a_us(w.w & ~NIB, (int)a1.w, sh);
+        const int s = sl + (sh >> 4);
+        S1 += (int)((sc24 >> (6 * k)) & 63u) * s;
+        S2 += (int)((m24 >> (6 * k)) & 63u) * t[k];
+    }
+}
+
 // sums (diagnostic) points at [b = 0][row][sb = 0][0] with stride bstride
-// between vectors.
+// between vectors.  act_resident: `reg` already holds this lane's slice.
 template <int NB, bool SUMS>
 __device__ __forceinline__ void chunk_q4_k(const uint8_t *ch, int nb_c, int sb0, int nsb,
-                                           const Act &a, int nvec, float (&acc)[NB],
-                                           int32_t *sums, size_t bstride, int lane) {
-    const int j = lane & 7, sbl = lane >> 3;
-    // bit offsets of this lane's 6-bit scale / min inside header words 1..3
-    const int sh_sc = (6 * j) & 31, sh_m = (48 + 6 * j) & 31;
-    const bool sc_hi = j >= 6, m_hi = j >= 3;
+                                           const Act &a, int nvec, float (&acc)[NB], Q4KAct &reg,
+                                           bool act_resident, int32_t *sums, size_t bstride,
+                                           int lane) {
+    const int h = lane & 1, sbl = lane >> 1;
+    const bool active = sbl < nb_c;
+    const uint8_t *p = ch + sbl * Q4_K_BYTES;
+    uint4 hd = make_uint4(0, 0, 0, 0), q[4];
 #pragma unroll
-    for (int t = 0; t < Fmt<GQ_Q4_K>::CH / 4; ++t) {
-        if (4 * t >= nb_c) break;  // warp-uniform
-        const int sl = 4 * t + sbl;
-        if (sl < nb_c) {
-            const uint4 h = *reinterpret_cast<const uint4 *>(ch + sl * Q4_K_BYTES);
-            const uint4 q = *reinterpret_cast<const uint4 *>(ch + sl * Q4_K_BYTES + 16 + 16 * j);
-            const uint32_t lo0 = q.x & NIB, hi0 = q.x & ~NIB, lo1 = q.y & NIB, hi1 = q.y & ~NIB;
-            const uint32_t lo2 = q.z & NIB, hi2 = q.z & ~NIB, lo3 = q.w & NIB, hi3 = q.w & ~NIB;
-            const int sc = (int)(__funnelshift_r(sc_hi ? h.z : h.y, sc_hi ? h.w : h.z, sh_sc) & 63u);
-            const int m = (int)(__funnelshift_r(m_hi ? h.w : h.z, m_hi ? 0u : h.w, sh_m) & 63u);
-            const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
-            const int sb = sb0 + sl;
+    for (int k = 0; k < 4; ++k) q[k] = make_uint4(0, 0, 0, 0);
+    if (active) {
+        hd = *reinterpret_cast<const uint4 *>(p);
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (b >= nvec) break;
-                const int blk = b * nsb + sb;
-                const int4 *ap = reinterpret_cast<const int4 *>(a.codes + (size_t)blk * 256 + 32 * j);
-                const int4 a0 = ap[0], a1 = ap[1];
-                int sl_ = dp4a_us(lo0, a0.x, 0), sh_ = dp4a_us(hi0, a0.y, 0);
-                sl_ = dp4a_us(lo1, a0.z, sl_);
-                sh_ = dp4a_us(hi1, a0.w, sh_);
-                sl_ = dp4a_us(lo2, a1.x, sl_);
-                sh_ = dp4a_us(hi2, a1.y, sh_);
-                sl_ = dp4a_us(lo3, a1.z, sl_);
-                sh_ = dp4a_us(hi3, a1.w, sh_);
-                const int s = sl_ + (sh_ >> 4);
-                int is1 = sc * s, is2 = m * a.isum[blk * 8 + j];
-                if (SUMS) {
-                    const int cnt = min(4, nb_c - 4 * t);  // super-blocks present in this step
-                    const unsigned gmask = FULL >> (32 - 8 * cnt);
+        for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4 *>(p + 16 + 64 * h + 16 * k);
+    }
+    // header bytes 4..15 = words y, z, w: the 6-bit fields sc_0..sc_7 then
+    // m_0..m_7, LSB first.  This half's four sc (bits 24h..24h+23) and four m
+    // (bits 48+24h..71+24h) are three whole bytes each.
+    const uint32_t sc24 = __byte_perm(hd.y, hd.z, h ? 0x0543u : 0x0210u);
+    const uint32_t m24 = __byte_perm(hd.z, hd.w, h ? 0x0765u : 0x0432u);
+    const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+    const int sb = sb0 + sbl;
 #pragma unroll
-                    for (int o = 1; o < 8; o <<= 1) {
-                        is1 += __shfl_xor_sync(gmask, is1, o);
-                        is2 += __shfl_xor_sync(gmask, is2, o);
-                    }
-                    if (j == 0) {
-                        int32_t *o = sums + b * bstride + (size_t)sb * 2;
-                        o[0] = is1;
-                        o[1] = is2;
-                    }
-                } else {
-                    acc[b] += a.dx[blk] * (d * (float)is1 - dmin * (float)is2);
-                }
+    for (int b = 0; b < NB; ++b) {
+        if (b >= nvec) break;  // warp-uniform
+        const int blk = b * nsb + sb;
+        if (!act_resident && active) load_q4k_act(reg, a, blk, h, lane & 7);
+        int S1 = 0, S2 = 0;
+        if (active) dot_q4k_half(q, reg, sc24, m24, S1, S2);
+        if (SUMS) {
+            S1 += __shfl_xor_sync(FULL, S1, 1);
+            S2 += __shfl_xor_sync(FULL, S2, 1);
+            if (active && h == 0) {
+                int32_t *o = sums + b * bstride + (size_t)sb * 2;
+                o[0] = S1;
+                o[1] = S2;
             }
+        } else if (active) {
+            acc[b] += reg.dx * (d * (float)S1 - dmin * (float)S2);
         }
     }
+}
+
+// Batch-1 Q4_K fast path for an item of nr <= RR whole rows (row = one
+// chunk): the rows' loads and dp4a chains are interleaved, and the RR row
+// sums are reduced across the warp in a transposed butterfly -- each level
+// halves the rows a lane keeps -- so four rows cost six shuffles instead of
+// twenty.  Afterwards lane l holds the sum of row 2 * bit4(l) + bit3(l) (for
+// RR == 4; row bit4(l) for RR == 2; row 0 for RR == 1).
+template <int RR>
+__device__ __forceinline__ float rows_q4_k_nb1(const uint8_t *ch, size_t row_bytes, int nr, int nblk,
+                                               const Q4KAct &reg, int lane) {
+    const int h = lane & 1, sbl = lane >> 1;
+    const bool active = sbl < nblk;
+    const uint32_t sel_sc = h ? 0x0543u : 0x0210u, sel_m = h ? 0x0765u : 0x0432u;
+    uint4 hd[RR], q[RR][4];
+#pragma unroll
+    for (int r = 0; r < RR; ++r) {
+        hd[r] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) q[r][k] = make_uint4(0, 0, 0, 0);
+        if (active && r < nr) {
+            const uint8_t *p = ch + r * row_bytes + sbl * Q4_K_BYTES;
+            hd[r] = *reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q[r][k] = *reinterpret_cast<const uint4 *>(p + 16 + 64 * h + 16 * k);
+        }
+    }
+    float v[RR];
+#pragma unroll
+    for (int r = 0; r < RR; ++r) {
+        int S1, S2;
+        dot_q4k_half(q[r], reg, __byte_perm(hd[r].y, hd[r].z, sel_sc), __byte_perm(hd[r].z, hd[r].w, sel_m), S1,
+                     S2);
+        const float d = half_bits_to_float(hd[r].x), dmin = half_bits_to_float(hd[r].x >> 16);
+        v[r] = active ? reg.dx * (d * (float)S1 - dmin * (float)S2) : 0.0f;
+    }
+    float s;
+    if (RR == 4) {
+        const bool up = lane & 16;
+        const float x0 = __shfl_xor_sync(FULL, up ? v[0] : v[2], 16);
+        const float x1 = __shfl_xor_sync(FULL, up ? v[1] : v[3], 16);
+        const float k0 = (up ? v[2] : v[0]) + x0, k1 = (up ? v[3] : v[1]) + x1;
+        const bool up8 = lane & 8;
+        s = (up8 ? k1 : k0) + __shfl_xor_sync(FULL, up8 ? k0 : k1, 8);
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    } else if (RR == 2) {
+        const bool up = lane & 16;
+        s = (up ? v[1] : v[0]) + __shfl_xor_sync(FULL, up ? v[0] : v[1], 16);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    } else {
+        s = warp_sum(v[0]);
+    }
+    return s;
 }
 
 // Q4_0 / Q8_0 chunk of nb_c blocks starting at block blk0 of the row; lane k
@@ -409,43 +518,68 @@ __device__ __forceinline__ void chunk_q_0(const uint8_t *ch, int nb_c, int blk0,
 
 // ------------------------------------------------------------- the kernel
 
+// Ring geometry, chosen per launch.  A ring item is R whole rows (one bulk
+// copy of R * row_bytes contiguous bytes) when a row fits in one chunk, else
+// one chunk of one row (R = 1).  Each warp owns `ns` stages of `stage_bytes`.
+struct Geo {
+    int R;            // rows per item (1, 2 or 4)
+    int ns;           // stages per warp, 1..MAX_STAGE
+    int stage_bytes;  // bytes per stage: a 16-byte multiple with 16 bytes of over-read slack
+};
+constexpr int MAX_STAGE = 8;
+constexpr int MAX_R = GQ_GEMV_MAX_R;
+
+template <int NW>
+__host__ __device__ constexpr int bufs_off() {
+    return ((NW * MAX_STAGE * 8 + 127) / 128) * 128;  // the mbarriers come first
+}
+
 // One launch covers NB activation vectors (blockIdx.y selects the chunk of
 // vectors) and all rows.  FUSED: `act` is fp32 [batch][cols] and is
 // quantized in the CTA; otherwise `act` holds the quantized blocks.
-// w_static != 0 lets the first weight chunks be requested before the
+// w_static != 0 lets the first ring items be requested before the
 // dependency wait on the preceding kernel (the caller guarantees no kernel
 // still in flight writes W).
 template <int WT, int NB, bool SUMS, bool FUSED, int NW>
-__global__ void __launch_bounds__(NW * 32) gemv_kernel(const uint8_t *__restrict__ W,
+__global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const uint8_t *__restrict__ W,
                                                    const void *__restrict__ act_in,
                                                    float *__restrict__ y,
                                                    int32_t *__restrict__ sums, int rows,
-                                                   int nblk, int batch, int w_static,
+                                                   int nblk, int batch, int w_static, Geo geo,
                                                    uint32_t *__restrict__ status) {
     using F = Fmt<WT>;
-    using R = Ring<WT, NW>;
+    constexpr int SPB = WT == GQ_Q4_K ? 2 : 1;  // int32 sums per block (diagnostic output)
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b0 = blockIdx.y * NB;
     const int nvec = min(NB, batch - b0);
     const int warps_total = gridDim.x * NW;
     const int wg = blockIdx.x * NW + warp;
-    const int nrows_w = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
     const int nchunk = (nblk + F::CH - 1) / F::CH;
-    const int total = nrows_w * nchunk;
+    const int R = geo.R, ns = geo.ns;
+    const int ngroups = (rows + R - 1) / R;
+    const int mine = wg < ngroups ? (ngroups - 1 - wg) / warps_total + 1 : 0;
+    const int total = mine * nchunk;
     const size_t row_bytes = (size_t)nblk * F::BB;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * NSTAGE;
-    uint8_t *ring = smem + R::BUFS_OFF + warp * NSTAGE * R::BUF;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * MAX_STAGE;
+    uint8_t *ring = smem + bufs_off<NW>() + (size_t)warp * ns * geo.stage_bytes;
 
-    // item i of this warp = chunk (i % nchunk) of its (i / nchunk)-th row
-    auto issue = [&](int i) {
-        const int row = wg + (i / nchunk) * warps_total;
-        const int c = i % nchunk;
-        const int nb_c = min(F::CH, nblk - c * F::CH);
-        const uint32_t bytes = (uint32_t)(nb_c * F::BB);
-        const int st = i % NSTAGE;
+    // item i of this warp = chunk (i % nchunk) of row group wg + (i / nchunk) * warps_total
+    auto issue = [&](int i, int st) {
+        const int g = wg + (i / nchunk) * warps_total;
+        const uint8_t *src;
+        uint32_t bytes;
+        if (nchunk == 1) {
+            const int nr = min(R, rows - g * R);
+            src = W + (size_t)g * R * row_bytes;
+            bytes = (uint32_t)(nr * row_bytes);
+        } else {
+            const int c = i % nchunk;
+            src = W + (size_t)g * row_bytes + (size_t)c * F::CH * F::BB;
+            bytes = (uint32_t)(min(F::CH, nblk - c * F::CH) * F::BB);
+        }
         mbar_arrive_expect_tx(bar + st, bytes);
-        bulk_g2s(ring + st * R::BUF, W + row * row_bytes + (size_t)c * F::CH * F::BB, bytes, bar + st);
+        bulk_g2s(ring + (size_t)st * geo.stage_bytes, src, bytes, bar + st);
     };
 
     // With the early trigger the next kernel in the stream may launch right
@@ -454,28 +588,27 @@ __global__ void __launch_bounds__(NW * 32) gemv_kernel(const uint8_t *__restrict
     // are staged.
     if (GQ_GEMV_EARLY_TRIGGER) pdl_launch_dependents();
     if (lane == 0 && total > 0) {
-#pragma unroll
-        for (int s = 0; s < NSTAGE; ++s) mbar_init(bar + s, 1);
+        for (int s = 0; s < ns; ++s) mbar_init(bar + s, 1);
         fence_mbar_init();
         if (w_static)
-            for (int i = 0; i < NSTAGE && i < total; ++i) issue(i);
+            for (int i = 0; i < ns && i < total; ++i) issue(i, i);
     }
     pdl_wait();  // activations (and, unless static, W) may come from the preceding kernel
     if (lane == 0 && !w_static)
-        for (int i = 0; i < NSTAGE && i < total; ++i) issue(i);
+        for (int i = 0; i < ns && i < total; ++i) issue(i, i);
 
-    const Act a = act_layout<WT>(smem + R::ACT_OFF, NB, nblk);
+    const Act a = act_layout<WT>(smem + bufs_off<NW>() + (size_t)NW * ns * geo.stage_bytes, NB, nblk);
     const int nact = nvec * nblk;
     if (FUSED) {
         const float *x = static_cast<const float *>(act_in) + (size_t)b0 * nblk * F::BE;
         if (WT == GQ_Q4_K)
-            quant_stage_q8_k(a, x, nact);
+            quant_stage_q8_k(a, x, nact, nblk);
         else
             quant_stage_q8_0<WT == GQ_Q4_0>(a, x, nact);
     } else {
         const uint8_t *xq = static_cast<const uint8_t *>(act_in);
         if (WT == GQ_Q4_K)
-            stage_q8_k(a, xq + (size_t)b0 * nblk * Q8_K_BYTES, nact);
+            stage_q8_k(a, xq + (size_t)b0 * nblk * Q8_K_BYTES, nact, nblk);
         else
             stage_q8_0<WT == GQ_Q4_0>(a, xq + (size_t)b0 * nblk * Q8_0_BYTES, nact);
     }
@@ -485,30 +618,25 @@ __global__ void __launch_bounds__(NW * 32) gemv_kernel(const uint8_t *__restrict
     float acc[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
-    const size_t bstride = (size_t)rows * nblk * (WT == GQ_Q4_K ? 2 : 1);
+    const size_t bstride = (size_t)rows * nblk * SPB;
+    // Q4_K, one vector, rows of one chunk: every item this warp sees pairs
+    // with the same activation slice, so it stays in registers.
+    Q4KAct reg;
+    const bool act_resident = WT == GQ_Q4_K && NB == 1 && nchunk == 1;
+    if (act_resident && (lane >> 1) < nblk) load_q4k_act(reg, a, lane >> 1, lane & 1, lane & 7);
 
-    for (int i = 0; i < total; ++i) {
-        const int st = i % NSTAGE;
-        if (!mbar_wait_bounded(bar + st, (uint32_t)(i / NSTAGE) & 1u)) {
-            // A transfer never completed: flag it, let the other issued
-            // stages drain (bounded), and leave the remaining rows unwritten.
-            if (lane == 0) atomicOr(status, STATUS_GEMV_TMA_TIMEOUT);
-            for (int k = i + 1; k < total && k < i + NSTAGE; ++k)
-                mbar_wait_bounded(bar + k % NSTAGE, (uint32_t)(k / NSTAGE) & 1u);
-            return;
-        }
-        const int row = wg + (i / nchunk) * warps_total;
-        const int c = i % nchunk;
+    // one row segment: accumulate into acc (or write the diagnostic sums)
+    auto segment = [&](const uint8_t *ch, int row, int c) {
         const int nb_c = min(F::CH, nblk - c * F::CH);
-        const uint8_t *ch = ring + st * R::BUF;
-        int32_t *srow = SUMS ? sums + ((size_t)b0 * rows + row) * nblk * (WT == GQ_Q4_K ? 2 : 1) : nullptr;
+        int32_t *srow = SUMS ? sums + ((size_t)b0 * rows + row) * nblk * SPB : nullptr;
         if (WT == GQ_Q4_K)
-            chunk_q4_k<NB, SUMS>(ch, nb_c, c * F::CH, nblk, a, nvec, acc, srow, bstride, lane);
+            chunk_q4_k<NB, SUMS>(ch, nb_c, c * F::CH, nblk, a, nvec, acc, reg, act_resident, srow,
+                                 bstride, lane);
         else
             chunk_q_0<WT, NB, SUMS>(ch, nb_c, c * F::CH, nblk, a, nvec, acc, srow, bstride, lane);
-        __syncwarp();
-        if (lane == 0 && i + NSTAGE < total) issue(i + NSTAGE);
-        if (!SUMS && c == nchunk - 1) {
+    };
+    auto finish_row = [&](int row) {
+        if (!SUMS) {
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 if (b < nvec) {
@@ -518,21 +646,79 @@ __global__ void __launch_bounds__(NW * 32) gemv_kernel(const uint8_t *__restrict
                 acc[b] = 0.0f;
             }
         }
+    };
+
+    int st = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < total; ++i) {
+        if (!mbar_wait_bounded(bar + st, ph)) {
+            // A transfer never completed: flag it, let the other issued
+            // stages drain (bounded), and leave the remaining rows unwritten.
+            if (lane == 0) atomicOr(status, STATUS_GEMV_TMA_TIMEOUT);
+            int s2 = st;
+            uint32_t p2 = ph;
+            for (int k = i + 1; k < total && k < i + ns; ++k) {
+                if (++s2 == ns) {
+                    s2 = 0;
+                    p2 ^= 1u;
+                }
+                mbar_wait_bounded(bar + s2, p2);
+            }
+            return;
+        }
+        const int g = wg + (i / nchunk) * warps_total;
+        const uint8_t *ch = ring + (size_t)st * geo.stage_bytes;
+        if (WT == GQ_Q4_K && NB == 1 && !SUMS && nchunk == 1) {
+            // batch-1 hot path: the item's rows interleaved (act_resident holds)
+            const int nr = min(R, rows - g * R), r0 = g * R;
+            float v;
+            int rr;
+            if (MAX_R >= 4 && R == 4) {
+                v = rows_q4_k_nb1<4>(ch, row_bytes, nr, nblk, reg, lane);
+                rr = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            } else if (MAX_R >= 2 && R == 2) {
+                v = rows_q4_k_nb1<2>(ch, row_bytes, nr, nblk, reg, lane);
+                rr = (lane >> 4) & 1;
+            } else {
+                v = rows_q4_k_nb1<1>(ch, row_bytes, nr, nblk, reg, lane);
+                rr = 0;
+            }
+            if ((lane & 7) == 0 && rr < nr && (R == 4 || (lane & 8) == 0) && (R >= 2 || lane == 0))
+                y[(size_t)b0 * rows + r0 + rr] = v;
+        } else if (nchunk == 1) {
+            const int nr = min(R, rows - g * R);
+            for (int r = 0; r < nr; ++r) {
+                segment(ch + r * row_bytes, g * R + r, 0);
+                finish_row(g * R + r);
+            }
+        } else {
+            const int c = i % nchunk;
+            segment(ch, g, c);
+            if (c == nchunk - 1) finish_row(g);
+        }
+        __syncwarp();
+        if (lane == 0 && i + ns < total) issue(i + ns, st);
+        if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+        }
     }
 }
 
 // Plain per-block kernel for Q4_0 / Q8_0 rows whose byte length is not a
 // multiple of 16 (cols % 256 != 0): warp per row, lane per block, 16-bit
 // global loads, activations read from global memory.
+constexpr int PLAIN_WARPS = 8;
+
 template <bool Q4, bool SUMS>
-__global__ void __launch_bounds__(256) gemv_plain_kernel(const uint8_t *__restrict__ W,
+__global__ void __launch_bounds__(PLAIN_WARPS * 32) gemv_plain_kernel(const uint8_t *__restrict__ W,
                                                          const uint8_t *__restrict__ xq,
                                                          float *__restrict__ y,
                                                          int32_t *__restrict__ sums, int rows,
                                                          int nblk, int batch) {
     constexpr int BB = Q4 ? Q4_0_BYTES : Q8_0_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * WARPS + warp;
+    const int row = blockIdx.x * PLAIN_WARPS + warp;
     const int b = blockIdx.y;
     pdl_launch_dependents();
     pdl_wait();
@@ -577,37 +763,82 @@ __global__ void __launch_bounds__(256) gemv_plain_kernel(const uint8_t *__restri
 // ------------------------------------------------------------------ launch
 
 constexpr int SMEM_MAX = 232448;  // opt-in shared memory per CTA on sm_103
-constexpr int ROWS_PER_WARP = GQ_GEMV_ROWS_PER_WARP;  // target rows per warp before the grid caps
 constexpr int CTAS_PER_SM = GQ_GEMV_CTAS_PER_SM;
+constexpr int RING_BUDGET = GQ_GEMV_RING_BUDGET;
 
-template <int WT, int NW = WARPS>
-size_t smem_bytes(int nb, int nblk) {
-    return (size_t)Ring<WT, NW>::ACT_OFF + (size_t)nb * nblk * act_block_bytes<WT>();
+inline int round16(size_t v) { return (int)((v + 15) / 16 * 16); }
+
+template <int WT>
+size_t act_bytes(int nb, int nblk) {
+    return (size_t)nb * nblk * act_block_bytes<WT>();
+}
+
+template <int WT, int NW>
+size_t smem_bytes(const Geo &g, int nb, int nblk) {
+    return (size_t)bufs_off<NW>() + (size_t)NW * g.ns * g.stage_bytes + act_bytes<WT>(nb, nblk);
+}
+
+// Ring geometry for `rows` rows of `nblk` blocks streamed by `warps` warps:
+// the most rows per bulk copy (up to 4) that still gives every warp an item,
+// then as many stages as the warp has items, within the per-CTA budget.
+template <int WT, int NW>
+Geo pick_geo(int rows, int nblk, int warps) {
+    using F = Fmt<WT>;
+    const int nchunk = (nblk + F::CH - 1) / F::CH;
+    const size_t row_bytes = (size_t)nblk * F::BB;
+    Geo g;
+    g.R = 1;
+    if (nchunk == 1)
+        for (int r = MAX_R; r > 1; r >>= 1)
+            if ((rows + r - 1) / r >= warps) {
+                g.R = r;
+                break;
+            }
+    g.stage_bytes = round16((nchunk == 1 ? g.R * row_bytes : (size_t)F::CH * F::BB) + 16);
+    const int items = (rows + g.R - 1) / g.R * nchunk;
+    const int per_warp = (items + warps - 1) / warps;
+    const int ns_budget = std::max(1, RING_BUDGET / (NW * g.stage_bytes));
+    g.ns = std::max(1, std::min(std::min(per_warp, ns_budget), MAX_STAGE));
+    return g;
 }
 
 template <int WT, int NB, bool SUMS, bool FUSED, int NW>
 cudaError_t launch_one(const void *W, const void *act, float *y, int32_t *sums, int rows,
-                       int nblk, int batch, int w_static, int rows_per_warp, const LaunchCtx &ctx) {
+                       int nblk, int batch, int w_static, const LaunchCtx &ctx) {
     auto k = gemv_kernel<WT, NB, SUMS, FUSED, NW>;
-    const size_t smem = smem_bytes<WT, NW>(NB, nblk);
+    Geo geo = pick_geo<WT, NW>(rows, nblk, ctx.num_sms * CTAS_PER_SM * NW);
+    while (geo.ns > 1 && smem_bytes<WT, NW>(geo, NB, nblk) > (size_t)SMEM_MAX) --geo.ns;
+    const size_t smem = smem_bytes<WT, NW>(geo, NB, nblk);
+    if (smem > (size_t)SMEM_MAX) return cudaErrorInvalidValue;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
         if (e != cudaSuccess) return e;
     }
-    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(CTAS_PER_SM, SMEM_MAX / (smem + 1024)));
-    int grid = (rows + NW * rows_per_warp - 1) / (NW * rows_per_warp);
+    // resident CTAs per SM: the occupancy calculator covers registers and
+    // shared memory; the persistent grid never exceeds one wave.
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, NW * 32, smem);
+    if (e != cudaSuccess) return e;
+    const int per_sm = std::max(1, std::min(CTAS_PER_SM, occ));
+    const int groups = (rows + geo.R - 1) / geo.R;
+    int grid = (groups + NW - 1) / NW;
     grid = std::max(1, std::min(grid, ctx.num_sms * per_sm));
     dim3 g(grid, (batch + NB - 1) / NB);
     return launch_pdl(k, g, dim3(NW * 32), smem, ctx.stream, static_cast<const uint8_t *>(W), act,
-                      y, sums, rows, nblk, batch, w_static, ctx.status);
+                      y, sums, rows, nblk, batch, w_static, geo, ctx.status);
 }
 
 // Largest batch chunk in {8, 4, 2, 1} not above `batch` whose staged
-// activations fit in shared memory; 0 if none fits.
+// activations fit in shared memory next to a one-stage ring; 0 if none fits.
 template <int WT>
 int pick_nb(int batch, int nblk) {
+    using F = Fmt<WT>;
+    Geo g1;
+    g1.R = 1;
+    g1.ns = 1;
+    g1.stage_bytes = round16((size_t)F::CH * F::BB + 16);
     for (int nb = 8; nb >= 1; nb >>= 1)
-        if (nb <= std::max(batch, 1) && smem_bytes<WT>(nb, nblk) <= (size_t)SMEM_MAX) return nb;
+        if (nb <= std::max(batch, 1) && smem_bytes<WT, WARPS>(g1, nb, nblk) <= (size_t)SMEM_MAX) return nb;
     return 0;
 }
 
@@ -615,12 +846,11 @@ template <int WT, bool SUMS, bool FUSED>
 cudaError_t dispatch_wt(const void *W, const void *act, float *y, int32_t *sums, int rows,
                         int nblk, int batch, int w_static, const LaunchCtx &ctx) {
     const int nb = pick_nb<WT>(batch, nblk);
-    const int rpw = ROWS_PER_WARP;
     switch (nb) {
-    case 8: return launch_one<WT, 8, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
-    case 4: return launch_one<WT, 4, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
-    case 2: return launch_one<WT, 2, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
-    case 1: return launch_one<WT, 1, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, rpw, ctx);
+    case 8: return launch_one<WT, 8, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    case 4: return launch_one<WT, 4, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    case 2: return launch_one<WT, 2, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
+    case 1: return launch_one<WT, 1, SUMS, FUSED, WARPS>(W, act, y, sums, rows, nblk, batch, w_static, ctx);
     }
     return cudaErrorInvalidValue;
 }
@@ -633,13 +863,13 @@ cudaError_t dispatch(gq_type wtype, const void *W, const void *act, float *y, in
     const int nblk = cols / 32;
     if (cols % 256 != 0) {
         if (FUSED) return cudaErrorInvalidValue;
-        dim3 grid((rows + WARPS - 1) / WARPS, batch);
+        dim3 grid((rows + PLAIN_WARPS - 1) / PLAIN_WARPS, batch);
         const uint8_t *w8 = static_cast<const uint8_t *>(W);
         const uint8_t *a8 = static_cast<const uint8_t *>(act);
         if (wtype == GQ_Q4_0)
-            return launch_pdl(gemv_plain_kernel<true, SUMS>, grid, dim3(256), 0, ctx.stream, w8, a8,
+            return launch_pdl(gemv_plain_kernel<true, SUMS>, grid, dim3(PLAIN_WARPS * 32), 0, ctx.stream, w8, a8,
                               y, sums, rows, nblk, batch);
-        return launch_pdl(gemv_plain_kernel<false, SUMS>, grid, dim3(256), 0, ctx.stream, w8, a8, y,
+        return launch_pdl(gemv_plain_kernel<false, SUMS>, grid, dim3(PLAIN_WARPS * 32), 0, ctx.stream, w8, a8, y,
                           sums, rows, nblk, batch);
     }
     if (wtype == GQ_Q4_0)
