@@ -49,7 +49,7 @@ constexpr unsigned FULL = 0xffffffffu;
 #define GQ_GEMV_RING_BUDGET (150 * 1024)
 #endif
 #ifndef GQ_GEMV_EARLY_TRIGGER
-#define GQ_GEMV_EARLY_TRIGGER 0
+#define GQ_GEMV_EARLY_TRIGGER 1
 #endif
 #ifndef GQ_GEMV_WARPS
 #define GQ_GEMV_WARPS 8
@@ -225,6 +225,27 @@ __device__ __forceinline__ float clamp127(float v) {
     return v < -127.0f ? -127.0f : (v > 127.0f ? 127.0f : v);
 }
 
+// Code of x in a block with scale d != 0 and r = RN(1/d): roundf of the
+// IEEE quotient x / d, clamped to [-127, 127].  For |x / d| <= 128 the
+// product p = RN(x * r) lies within 2^-16 of x / d and RN(x / d) within
+// 2^-17, so the two round alike under roundf unless p is within 2^-15 of a
+// half-integer; p's distance is tested against 2^-14 and the near cases
+// (and a non-finite r, which makes the test fail through a NaN) take the
+// IEEE division.  Away from a half-integer, roundf(|p|) = floor(|p|) + (frac
+// > 1/2) exactly.
+__device__ __forceinline__ float q8_code(float x, float d, float r) {
+    const float p = __fmul_rn(x, r);
+    const float a = fabsf(p);
+    const float fl = floorf(a);
+    const float f = a - fl;
+    float q;
+    if (fabsf(f - 0.5f) > 0x1p-14f)
+        q = copysignf(fl + (f > 0.5f ? 1.0f : 0.0f), p);
+    else
+        q = roundf(__fdiv_rn(x, d));
+    return clamp127(q);
+}
+
 // Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
 // (= code group l of the layout).
 __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks, int nsb) {
@@ -251,11 +272,12 @@ __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int 
             for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(e[i]));
             amax = warp_max(amax);
             const float d = __fdiv_rn(amax, 127.0f);
+            const float rcp = __frcp_rn(d);
             uint32_t w0 = 0, w1 = 0;
             int sum = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float q = (d == 0.0f) ? 0.0f : clamp127(roundf(__fdiv_rn(e[i], d)));
+                const float q = (d == 0.0f) ? 0.0f : q8_code(e[i], d, rcp);
                 const int qi = (int)q;
                 sum += qi;
                 if (i < 4)
@@ -294,7 +316,7 @@ __device__ void quant_stage_q8_0(const Act &a, const float *__restrict__ x, int 
             if (blk >= nblocks) break;  // warp-uniform
             const float amax = warp_max(fabsf(v[u]));
             const float d = __half2float(__float2half_rn(__fdiv_rn(amax, 127.0f)));
-            const float q = (d == 0.0f) ? 0.0f : clamp127(roundf(__fdiv_rn(v[u], d)));
+            const float q = (d == 0.0f) ? 0.0f : q8_code(v[u], d, __frcp_rn(d));
             int qi = (int)q;
             a.codes[(size_t)blk * 32 + pos] = (uint8_t)(qi & 0xff);
 #pragma unroll
@@ -779,8 +801,10 @@ size_t smem_bytes(const Geo &g, int nb, int nblk) {
 }
 
 // Ring geometry for `rows` rows of `nblk` blocks streamed by `warps` warps:
-// the most rows per bulk copy (up to 4) that still gives every warp an item,
-// then as many stages as the warp has items, within the per-CTA budget.
+// the most rows per bulk copy (up to 4) that still gives every warp an item
+// (bigger copies stream better; spreading a short matrix over all warps
+// finishes it sooner), then as many stages as the warp has items, within the
+// per-CTA budget.
 template <int WT, int NW>
 Geo pick_geo(int rows, int nblk, int warps) {
     using F = Fmt<WT>;

@@ -268,6 +268,42 @@ def test_fused_f32_matches_unfused_and_oracle(wtype, rows, cols, batch):
     assert_close(y_f, y_ref, T)
 
 
+def tie_heavy_activations(cols, blk, seed):
+    """fp32 rows whose codes sit on or next to rounding ties: per block the
+    scale is either a power of two (ties exact) or arbitrary (quotients a few
+    ulps from a half-integer), and most entries are (k + 1/2) * scale or one
+    ulp to either side."""
+    g = np.random.default_rng(seed)
+    x = np.empty(cols, dtype=np.float32)
+    for b0 in range(0, cols, blk):
+        if (b0 // blk) % 2 == 0:
+            d = np.float32(2.0 ** int(g.integers(-12, 3)))
+        else:
+            d = np.float32(g.uniform(0.01, 3.0) / 127.0)
+        v = ((g.integers(-126, 126, blk) + 0.5) * d).astype(np.float32)
+        nudge = g.integers(-1, 2, blk)
+        v = np.where(nudge > 0, np.nextafter(v, np.float32(np.inf)), v)
+        v = np.where(nudge < 0, np.nextafter(v, np.float32(-np.inf)), v)
+        v[0] = np.float32(127.0) * d  # the block maximum fixes the scale
+        x[b0:b0 + blk] = v
+    return x
+
+
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
+def test_fused_quantize_ties_match_oracle(wtype):
+    """Identity weights make each block sum expose single activation codes,
+    so the in-kernel quantizer is checked code by code on tie cases."""
+    cols = 1024
+    blk = 256 if wtype == Q4_K else 32
+    X = np.stack([tie_heavy_activations(cols, blk, 40 + i) for i in range(2)])
+    Wq = orc.quantize(wtype, np.eye(cols, dtype=np.float32))
+    Xq = orc.quantize(orc.ACT_TYPE[wtype], X)
+    s = host(gq.block_sums_f32(wtype, dev(Wq), dev(X), cols, cols, 2))
+    np.testing.assert_array_equal(s, orc.block_sums(wtype, Wq, Xq, cols, cols, 2))
+    # and the standalone quantizer gives the same bytes
+    assert host(gq.quantize(orc.ACT_TYPE[wtype], dev(X))).tobytes() == Xq.tobytes()
+
+
 @pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
 def test_w_static_flag_same_result(wtype):
     rows, cols, batch = 300, 4096, 2
