@@ -20,17 +20,25 @@
 //
 // CTA tile: 128 weight rows x 128 batch columns, one super-block (K = 256) per
 // step, 28 warps:
-//   warp 0     activation producer: 1-D bulk copies of the packed B tiles
-//              into their own 6-slot ring (1.5 super-blocks ahead);
+//   warps 0, 3 activation producers: one 1-D bulk copy each per
+//              super-block of the packed unit's half 0 (B stages 0-1) or half
+//              1 (stages 2-3 and the min-term B tile) into a 4-slot ring (two
+//              super-blocks ahead);
 //   warp 1     MMA issuer (one thread) and tensor-memory owner;
 //   warp 2     weight producer: one 2-D tiled TMA load per super-block of
-//              the raw Q4_K rows (box 144 bytes x 128 rows; rows past the
-//              matrix read as zeros), the min-term B tile and the scales;
+//              the raw Q4_K rows, two super-blocks ahead (box 144 bytes x
+//              128 rows; rows past the matrix read as zeros);
 //   warps 4-11 A builders: two threads per weight row, each turning half of
-//              the raw super-block into two fp16 A stages (128-byte swizzled
-//              K-major); the first half also writes the min-term row and the
-//              row scales d, dmin;
-//   warps 12-27 epilogue: four threads per row, 32 columns each.
+//              the raw super-block into fp16 sc*q and storing it straight
+//              from registers into tensor memory (tcgen05.st), where the MMA
+//              reads the A operand -- double-buffered by super-block, so
+//              building the next super-block overlaps the current one's
+//              MMAs and no shared-memory bandwidth is spent on A; the first
+//              half then writes the min-term row and the row scales d, dmin;
+//   warps 12-27 epilogue: four threads per row, 32 columns each; it frees the
+//              accumulators once they are in registers.
+// Tensor memory (512 columns): S1 and S2 of the current super-block (128
+// each) and two 128-column A buffers.
 // The activation operand is packed once per call by pack_kernel into a
 // caller-provided workspace, already in the swizzled shared-memory image, so
 // each operand tile is a single 1-D bulk copy.
@@ -51,51 +59,63 @@ namespace {
 
 constexpr int TM = 128;   // weight rows per tile (MMA M)
 constexpr int TN = 128;   // batch columns per tile (MMA N)
-constexpr int KS = 64;    // K per operand stage (one 128-byte swizzle atom)
-constexpr int NOP = 4;    // A operand stages (= one super-block)
-constexpr int NBR = 6;    // B operand stages (1.5 super-blocks of lookahead)
-constexpr int NRAW = 2;   // raw weight stages
+constexpr int KS = 64;    // K per B operand stage (one 128-byte swizzle atom)
+constexpr int NKS = 4;    // B operand stages per super-block
+constexpr int NBS = 4;    // B ring slots: two halves per super-block, two super-blocks
+constexpr int NRAW = 3;   // raw weight stages (two super-blocks of lookahead)
 constexpr int KMIN = 16;  // min-term K per super-block (8 mins, two halves of t)
+constexpr int NSM = 4;    // ring depth of the per-super-block scales and min-term A rows
 
-// Shared-memory layout (bytes from a 1024-aligned base).
-constexpr int OP_A = TM * KS * 2;                 // 16 KB
+// Workspace (packed activations) per (column tile, super-block): the four B
+// stage images, the min-term B tile and the column scales, contiguous.
 constexpr int OP_B = TN * KS * 2;                 // 16 KB
 constexpr int MIN_A = TM * KMIN * 2;              // 4 KB
 constexpr int MIN_B = TN * KMIN * 2;              // 4 KB
-constexpr int MIN_STAGE = MIN_A + MIN_B;          // 8 KB
-constexpr int RAW_STAGE = TM * Q4_K_BYTES;        // 18 KB
+constexpr size_t WS_B = (size_t)NKS * OP_B;       // 64 KB
+constexpr size_t WS_MIN = MIN_B;
+constexpr size_t WS_DX = TN * 4;                  // 512 B
+constexpr size_t WS_UNIT = WS_B + WS_MIN + WS_DX;
+
+// Each unit arrives as two bulk copies, issued by two producer warps (a warp
+// completes about one bulk copy per half microsecond however large, so one
+// copy per warp per super-block keeps the copies off the critical path):
+// half 0 = stages 0-1; half 1 = stages 2-3 and the min-term B tile.  The
+// column scales are fetched by builder threads with plain loads.
+constexpr int HALF0_BYTES = 2 * OP_B;                          // 32 KB
+constexpr int HALF1_BYTES = 2 * OP_B + MIN_B;                  // 36 KB
+constexpr int SLOT_B = (HALF1_BYTES + 1023) / 1024 * 1024;     // ring slot stride
+constexpr int SLOT_MIN = 2 * OP_B;                             // inside a half-1 slot
+constexpr int RAW_STAGE = TM * Q4_K_BYTES;                     // 18 KB
 // per super-block scales: d and dmin per row, dx per column (all fp32)
 constexpr int META_D = 0, META_DMIN = TM * 4, META_DX = 2 * TM * 4;
 constexpr int META_STAGE = 2 * TM * 4 + TN * 4;
 
-constexpr int OFF_A = 0;                                  // NOP x 16 KB
-constexpr int OFF_B = OFF_A + NOP * OP_A;                 // NBR x 16 KB
-constexpr int OFF_MIN = OFF_B + NBR * OP_B;
-constexpr int OFF_RAW = OFF_MIN + 2 * MIN_STAGE;          // 163840
-constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;      // 200704
-constexpr int OFF_BAR = OFF_META + 2 * META_STAGE;        // 202752
-// A: full (builders), empty; B: full-tx (producer), empty; min: full
-// (builders), full-tx, empty; raw: full, empty; meta: full (builders),
-// full-tx, empty; acc: full, empty; final.
-constexpr int NBARS = 2 * NOP + 2 * NBR + 3 * 2 + 2 * NRAW + 3 * 2 + 2 * 2 + 1;
+// Shared-memory layout (bytes from a 1024-aligned base).  The A operand
+// lives in tensor memory, not here.
+constexpr int OFF_B = 0;                                  // NBS x SLOT_B
+constexpr int OFF_MINA = OFF_B + NBS * SLOT_B;            // NSM x 4 KB min-term A rows
+constexpr int OFF_RAW = OFF_MINA + NSM * MIN_A;           // NRAW x 18 KB
+constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;      // NSM x 1.5 KB scales
+constexpr int OFF_BAR = OFF_META + NSM * META_STAGE;
+// A: full (builders), empty (by parity); B: full-tx (producers), empty; min:
+// full (builders), empty; raw: full, empty; meta: full (builders), empty;
+// acc: full, empty; final.
+constexpr int NBARS = 2 * 2 + 2 * NBS + 2 * NSM + 2 * NRAW + 2 * NSM + 2 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-static_assert(OFF_A % 1024 == 0 && OFF_B % 1024 == 0 && OP_A % 1024 == 0 && OP_B % 1024 == 0,
-              "SW128 tiles need 1024-byte alignment");
+static_assert(SLOT_B % 1024 == 0 && OP_B % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+static_assert(OFF_RAW % 128 == 0 && RAW_STAGE % 128 == 0, "tiled TMA destinations are 128-byte aligned");
+static_assert(WS_UNIT % 16 == 0 && HALF1_BYTES % 16 == 0 && SLOT_MIN % 16 == 0, "bulk copies move 16-byte units");
 
-// Workspace (packed activations) per (column tile, super-block).
-constexpr size_t WS_B = (size_t)NOP * OP_B;   // 64 KB, the four B stage images
-constexpr size_t WS_MIN = MIN_B;              // 4 KB
-constexpr size_t WS_DX = TN * 4;              // 512 B
-constexpr size_t WS_UNIT = WS_B + WS_MIN + WS_DX;
-
-// Tensor-memory columns: S1 and S2 accumulators, each double-buffered by
-// super-block parity.
+// Tensor-memory columns: the S1 and S2 accumulators of the current
+// super-block (128 each), and the A operand (one super-block, 256 K as fp16
+// pairs = 128 columns) double-buffered by super-block parity, so the
+// builders work a whole super-block ahead of the MMAs.
 constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t col_s1(int p) { return 128u * (uint32_t)p; }
-__host__ __device__ constexpr uint32_t col_s2(int p) { return 256u + 128u * (uint32_t)p; }
+constexpr uint32_t COL_S1 = 0, COL_S2 = 128;
+__host__ __device__ constexpr uint32_t col_a(int p) { return 256u + 128u * (uint32_t)p; }
 
 constexpr int NTHREADS = 896;
 constexpr int EPI_WARP0 = 12, EPI_WARPS = 16, BLD_WARP0 = 4, BLD_THREADS = 256;
@@ -132,6 +152,17 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
         : "memory");
 }
 
+// The same with the A operand in tensor memory (lane = row, K along the
+// columns, two fp16 per 32-bit column with the lower K in the low half).
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -152,19 +183,38 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// 16 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z),
+        "r"(v[1].w), "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y),
+        "r"(v[3].z), "r"(v[3].w)
+        : "memory");
+}
+
+// Two runs of 16 consecutive fp32 columns of this warp's 32 tensor-memory
+// lanes, both loads in flight before one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
+    uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(r[i]);
+        vb[i] = __uint_as_float(r[16 + i]);
+    }
 }
 
 // Bounded wait that also gives up as soon as another role of the CTA set
@@ -184,6 +234,11 @@ __device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volati
     const bool ok = wait_or_abort(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
 }
+
+// Super-block visited at step i of a CTA's K loop: every row tile starts at
+// its own super-block (rot), so the CTAs running at the same time read
+// different activation tiles instead of all hitting the same L2 lines.
+__device__ __forceinline__ int kslot(int i, int rot, int nsb) { return i + rot < nsb ? i + rot : i + rot - nsb; }
 
 // Ring position: stage index and the parity of its current use.
 struct RingPos {
@@ -267,123 +322,91 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
 // ------------------------------------------------------------- main kernel
 
 constexpr uint32_t IDESC_F16 = idesc_f16(TM, TN, 0);
-constexpr uint32_t IDESC_BF16 = idesc_f16(TM, TN, 1);
 
-// Barriers whose only arrival is a transfer's transaction count (the *_tx
-// ones and raw_full) tell the producer that a copy has landed; the builders
-// arrive on the plain *_full ones.
+// Barriers whose only arrival is a transfer's transaction count (b_tx,
+// raw_full) tell the consumer that a copy has landed; the builders arrive on
+// the plain *_full ones.
 struct Bars {
-    uint64_t *a_full, *a_empty, *b_tx, *b_empty, *min_full, *min_tx, *min_empty, *raw_full, *raw_empty;
-    uint64_t *meta_full, *meta_tx, *meta_empty, *acc_full, *acc_empty, *fin;
+    uint64_t *a_full, *a_empty, *b_tx, *b_empty, *min_full, *min_empty, *raw_full, *raw_empty;
+    uint64_t *meta_full, *meta_empty, *acc_full, *acc_empty, *fin;
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     Bars r;
     r.a_full = b;
-    r.a_empty = r.a_full + NOP;
-    r.b_tx = r.a_empty + NOP;
-    r.b_empty = r.b_tx + NBR;
-    r.min_full = r.b_empty + NBR;
-    r.min_tx = r.min_full + 2;
-    r.min_empty = r.min_tx + 2;
-    r.raw_full = r.min_empty + 2;
+    r.a_empty = r.a_full + 2;
+    r.b_tx = r.a_empty + 2;
+    r.b_empty = r.b_tx + NBS;
+    r.min_full = r.b_empty + NBS;
+    r.min_empty = r.min_full + NSM;
+    r.raw_full = r.min_empty + NSM;
     r.raw_empty = r.raw_full + NRAW;
     r.meta_full = r.raw_empty + NRAW;
-    r.meta_tx = r.meta_full + 2;
-    r.meta_empty = r.meta_tx + 2;
-    r.acc_full = r.meta_empty + 2;
-    r.acc_empty = r.acc_full + 2;
-    r.fin = r.acc_empty + 2;
+    r.meta_empty = r.meta_full + NSM;
+    r.acc_full = r.meta_empty + NSM;
+    r.acc_empty = r.acc_full + 1;
+    r.fin = r.acc_empty + 1;
     return r;
 }
 
-// Producer of the activation operand (warp 0): the four B stage images of
-// every super-block, through a ring of NBR slots.  On abort it waits
-// (bounded) for every copy it started before the CTA may exit.
+// B ring slot of half h of super-block step sb; it is reused every second
+// step, so its parity is that of sb / 2.
+__device__ __forceinline__ int b_slot(int sb, int h) { return 2 * (sb & 1) + h; }
+
+// Producer of half h of the activation units (warps 0 and 3): one bulk copy
+// per super-block into the B ring.  On abort it waits (bounded) for every
+// copy it started before the CTA may exit.
 __device__ void role_producer_b(uint8_t *smem, const Bars &B, const uint8_t *__restrict__ ws, int nsb,
-                                int ct, volatile uint32_t *abort) {
+                                int ct, int rot, int h, volatile uint32_t *abort) {
     const int lane = threadIdx.x & 31;
-    int last[NBR];
-    for (int i = 0; i < NBR; ++i) last[i] = -1;
-    RingPos br(NBR);
+    const uint32_t bytes = h ? (uint32_t)HALF1_BYTES : (uint32_t)HALF0_BYTES;
+    int last[2] = {-1, -1};
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
-        const uint8_t *unit = ws + ((size_t)ct * nsb + sb) * WS_UNIT;
-        for (int q = 0; q < NOP; ++q) {
-            if (!(ok = wait_warp(B.b_empty + br.idx, br.phase ^ 1u, abort))) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(B.b_tx + br.idx, OP_B);
-                bulk_g2s(smem + OFF_B + br.idx * OP_B, unit + (size_t)q * OP_B, OP_B, B.b_tx + br.idx);
-            }
-            last[br.idx] = (int)br.phase;
-            br.next();
+        const int s = b_slot(sb, h);
+        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
+        if (!(ok = wait_warp(B.b_empty + s, ph ^ 1u, abort))) break;
+        if (lane == 0) {
+            const uint8_t *src = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * WS_UNIT + (h ? HALF0_BYTES : 0);
+            mbar_arrive_expect_tx(B.b_tx + s, bytes);
+            bulk_g2s(smem + OFF_B + s * SLOT_B, src, bytes, B.b_tx + s);
         }
+        last[sb & 1] = (int)ph;
     }
     if (!ok)
-        for (int i = 0; i < NBR; ++i)
-            if (last[i] >= 0) mbar_wait_bounded(B.b_tx + i, (uint32_t)last[i]);
+        for (int i = 0; i < 2; ++i)
+            if (last[i] >= 0) mbar_wait_bounded(B.b_tx + 2 * i + h, (uint32_t)last[i]);
 }
 
-// Producer of the weight side and the small per-super-block operands
-// (warp 2): the raw Q4_K rows one super-block ahead (one 2-D tiled TMA load,
-// box 144 bytes x 128 rows; rows past the matrix read as zeros), then the
-// min-term B tile and the column scales of the current super-block.
-__device__ void role_producer_w(uint8_t *smem, const Bars &B, const CUtensorMap *tmap_w,
-                                const uint8_t *__restrict__ ws, int row0, int nsb, int ct,
-                                volatile uint32_t *abort) {
+// Producer of the raw weight rows (warp 2): one 2-D tiled TMA load per
+// super-block (box 144 bytes x 128 rows; rows past the matrix read as
+// zeros), NRAW - 1 super-blocks ahead of the builders.
+__device__ void role_producer_w(uint8_t *smem, const Bars &B, const CUtensorMap *tmap_w, int row0, int nsb,
+                                int rot, volatile uint32_t *abort) {
     const int lane = threadIdx.x & 31;
-    int raw_last[NRAW], min_last[2], meta_last[2];
+    int raw_last[NRAW];
     for (int i = 0; i < NRAW; ++i) raw_last[i] = -1;
-    for (int i = 0; i < 2; ++i) min_last[i] = meta_last[i] = -1;
-    RingPos rr(NRAW), mr(2);
-
-    auto issue_raw = [&](int sb) -> bool {
-        if (!wait_warp(B.raw_empty + rr.idx, rr.phase ^ 1u, abort)) return false;
+    RingPos rr(NRAW);
+    bool ok = true;
+    for (int sb = 0; ok && sb < nsb; ++sb) {
+        if (!(ok = wait_warp(B.raw_empty + rr.idx, rr.phase ^ 1u, abort))) break;
         if (lane == 0) {
             mbar_arrive_expect_tx(B.raw_full + rr.idx, RAW_STAGE);
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
                 " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + OFF_RAW + rr.idx * RAW_STAGE)),
-                "l"(reinterpret_cast<uint64_t>(tmap_w)), "r"(sb * Q4_K_BYTES), "r"(row0),
+                "l"(reinterpret_cast<uint64_t>(tmap_w)), "r"(kslot(sb, rot, nsb) * Q4_K_BYTES), "r"(row0),
                 "r"(smem_u32(B.raw_full + rr.idx))
                 : "memory");
         }
         __syncwarp();
         raw_last[rr.idx] = (int)rr.phase;
         rr.next();
-        return true;
-    };
-
-    bool ok = issue_raw(0);
-    for (int sb = 0; ok && sb < nsb; ++sb) {
-        if (sb + 1 < nsb && !(ok = issue_raw(sb + 1))) break;
-        const uint8_t *unit = ws + ((size_t)ct * nsb + sb) * WS_UNIT;
-        if (!(ok = wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort))) break;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(B.min_tx + mr.idx, MIN_B);
-            bulk_g2s(smem + OFF_MIN + mr.idx * MIN_STAGE + MIN_A, unit + WS_B, MIN_B, B.min_tx + mr.idx);
-        }
-        min_last[mr.idx] = (int)mr.phase;
-        mr.next();
-        const int mp = sb & 1;
-        const uint32_t mph = (uint32_t)(sb >> 1) & 1u;
-        if (!(ok = wait_warp(B.meta_empty + mp, mph ^ 1u, abort))) break;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(B.meta_tx + mp, TN * 4);
-            bulk_g2s(smem + OFF_META + mp * META_STAGE + META_DX, unit + WS_B + WS_MIN, TN * 4,
-                     B.meta_tx + mp);
-        }
-        meta_last[mp] = (int)mph;
     }
-    if (!ok) {
+    if (!ok)
         for (int i = 0; i < NRAW; ++i)
             if (raw_last[i] >= 0) mbar_wait_bounded(B.raw_full + i, (uint32_t)raw_last[i]);
-        for (int i = 0; i < 2; ++i) {
-            if (min_last[i] >= 0) mbar_wait_bounded(B.min_tx + i, (uint32_t)min_last[i]);
-            if (meta_last[i] >= 0) mbar_wait_bounded(B.meta_tx + i, (uint32_t)meta_last[i]);
-        }
-    }
 }
 
 // fp16x2 value of the two halves of an integer-coded word (bit pattern).
@@ -406,20 +429,21 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
                       bits_h2(__hfma2(p2, s1, c1)), bits_h2(__hfma2(p3, s16, c16)));
 }
 
-// A builders (warps 4-11): thread idx -> tile row t = idx % 128 and half
-// hh = idx / 128, which builds operand stages 2hh and 2hh + 1 (sub-blocks
-// 4hh .. 4hh + 3).  Stage q of every super-block uses ring slot q, so each
-// half owns its two slots; the ring parity is the super-block's.
-__device__ void role_builder(uint8_t *smem, const Bars &B, int idx, int nvalid, int nsb,
-                             volatile uint32_t *abort) {
-    const int lane = threadIdx.x & 31;
-    const int t = idx & (TM - 1), hh = idx >> 7;
+// A builders (warps 4-11): warp w builds tile rows 32 (w % 4) .. + 31 (its
+// tensor-memory lanes; row t = 32 (w % 4) + lane) for half hh = (w - 4) / 4
+// of every super-block, i.e. sub-blocks 4hh .. 4hh + 3 = K 128hh .. + 127 =
+// A columns 64hh .. + 63 of the buffer of the super-block's parity.  Each
+// sub-block is 16 columns, written by one tcgen05.st from registers.  The
+// hh = 0 threads then write the row scales and the min-term row, the hh = 1
+// threads the scale of column t (read from the workspace).
+__device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const uint8_t *__restrict__ ws,
+                             int ct, int rot, int nvalid, int nsb, volatile uint32_t *abort) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = 32 * (warp & 3) + lane, hh = (warp - BLD_WARP0) >> 2;
     const bool valid = t < nvalid;
-    RingPos rr(NRAW), mr(2);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    RingPos rr(NRAW), mr(NSM);
     for (int sb = 0; sb < nsb; ++sb) {
-        const int mp = sb & 1;
-        const uint32_t par = (uint32_t)sb & 1u;
-        const uint32_t mph = (uint32_t)(sb >> 1) & 1u;
         if (!wait_warp(B.raw_full + rr.idx, rr.phase, abort)) return;
         const uint8_t *raw = smem + OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
         uint4 h = make_uint4(0, 0, 0, 0), q[4];
@@ -433,110 +457,117 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, int idx, int nvalid, 
         mbar_arrive(B.raw_empty + rr.idx);
         rr.next();
 
-        if (hh == 0) {
+        // this half of the A operand: sc_j * q for sub-blocks 4hh .. 4hh + 3
+        const int p = sb & 1;
+        if (!wait_warp(B.a_empty + p, ((uint32_t)(sb >> 1) & 1u) ^ 1u, abort)) return;
+        tc_fence_after();
+        const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float sc = (float)(int)((lo64 >> (6 * (4 * hh + j))) & 63);
+            const __half2 s1 = __float2half2_rn(sc), c1 = __float2half2_rn(-1024.0f * sc);
+            const __half2 s16 = __float2half2_rn(sc * 0.0625f), c16 = __float2half2_rn(-64.0f * sc);
+            uint4 v[4];
+            v[0] = nibbles_to_f16(q[j].x, s1, c1, s16, c16);
+            v[1] = nibbles_to_f16(q[j].y, s1, c1, s16, c16);
+            v[2] = nibbles_to_f16(q[j].z, s1, c1, s16, c16);
+            v[3] = nibbles_to_f16(q[j].w, s1, c1, s16, c16);
+            tmem_st16(lane_base + col_a(p) + 64u * hh + 16u * j, v);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(B.a_full + p);
+
+        // then (off the MMA's critical path) the scales and the min-term row
+        if (hh == 1) {
+            const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * WS_UNIT;
+            const float dx = __ldg(reinterpret_cast<const float *>(unit + WS_B + WS_MIN) + t);
+            if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
+            reinterpret_cast<float *>(smem + OFF_META + mr.idx * META_STAGE + META_DX)[t] = dx;
+            mbar_arrive(B.meta_full + mr.idx);
+            mr.next();
+        } else {
             // row scales and the min-term row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
             const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);
             int mn[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) mn[j] = (int)((hi64 >> (6 * j + 16)) & 63);
-            if (!wait_warp(B.meta_empty + mp, mph ^ 1u, abort)) return;
-            uint8_t *meta = smem + OFF_META + mp * META_STAGE;
+            if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
+            uint8_t *meta = smem + OFF_META + mr.idx * META_STAGE;
             reinterpret_cast<float *>(meta + META_D)[t] = half_bits_to_float(h.x);
             reinterpret_cast<float *>(meta + META_DMIN)[t] = half_bits_to_float(h.x >> 16);
-            mbar_arrive(B.meta_full + mp);
+            mbar_arrive(B.meta_full + mr.idx);
             if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-            uint8_t *ma = smem + OFF_MIN + mr.idx * MIN_STAGE;
-            if (valid) {
-                uint32_t lo[4], hi[4];
+            uint8_t *ma = smem + OFF_MINA + mr.idx * MIN_A;
+            uint32_t lo[4], hi[4];
 #pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    lo[j >> 1] = pack_h2((float)mn[j], (float)mn[j + 1]);
-                    hi[j >> 1] = pack_h2(64.0f * (float)mn[j], 64.0f * (float)mn[j + 1]);
-                }
-                *reinterpret_cast<uint4 *>(ma + plain_off(t, 0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                *reinterpret_cast<uint4 *>(ma + plain_off(t, 1)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            for (int j = 0; j < 8; j += 2) {
+                lo[j >> 1] = pack_h2((float)mn[j], (float)mn[j + 1]);
+                hi[j >> 1] = pack_h2(64.0f * (float)mn[j], 64.0f * (float)mn[j + 1]);
             }
+            *reinterpret_cast<uint4 *>(ma + plain_off(t, 0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(ma + plain_off(t, 1)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.min_full + mr.idx);
             mr.next();
         }
-
-        // this half's two operand stages of 64 K (two sub-blocks each)
-        const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int slot = 2 * hh + k;
-            if (!wait_warp(B.a_empty + slot, par ^ 1u, abort)) return;
-            uint8_t *A = smem + OFF_A + slot * OP_A;
-            if (valid) {
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * k + jj;  // sub-block within this half
-                    const float sc = (float)(int)((lo64 >> (6 * (4 * hh + j))) & 63);
-                    const __half2 s1 = __float2half2_rn(sc), c1 = __float2half2_rn(-1024.0f * sc);
-                    const __half2 s16 = __float2half2_rn(sc * 0.0625f), c16 = __float2half2_rn(-64.0f * sc);
-                    const uint32_t wd[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        *reinterpret_cast<uint4 *>(A + sw128_off(t, 4 * jj + i)) =
-                            nibbles_to_f16(wd[i], s1, c1, s16, c16);
-                }
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.a_full + slot);
-        }
     }
 }
 
-// MMA issuer (warp 1, one thread).  Per super-block: sixteen K=16 steps into
-// the S1 accumulator of this super-block's parity, committed to the stage
-// barriers and to acc_full; then two K=16 bf16 steps into the min-term
-// accumulator.  Always ends with a commit to `fin` so the epilogue (and the
-// teardown) can wait for every MMA to finish.
+// MMA issuer (warp 1, one thread).  Per super-block: sixteen K=16 steps of
+// the S1 product (A from the tensor-memory buffer of the super-block's
+// parity, B from the two halves of the unit in the ring), then one K=16 step
+// of the min-term product S2 (A rows from the builders, B tile from half 1),
+// both into the accumulator pair, which the epilogue must have drained first.
+// Always ends with a commit to `fin` so the teardown can wait for every MMA
+// to finish.
 __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, volatile uint32_t *abort) {
-    RingPos orr(NOP), br(NBR), mr(2);
+    RingPos mr(NSM);
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
         const int p = sb & 1;
-        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
-        if (!(ok = wait_or_abort(B.acc_empty + p, ph ^ 1u, abort))) break;
-        tc_fence_after();
-        for (int qq = 0; qq < NOP; ++qq) {
-            if (!(ok = wait_or_abort(B.a_full + orr.idx, orr.phase, abort))) break;
-            if (!(ok = wait_or_abort(B.b_tx + br.idx, br.phase, abort))) break;
+        const uint32_t ph = (uint32_t)(sb >> 1) & 1u, sp = (uint32_t)sb & 1u;
+        if (!(ok = wait_or_abort(B.a_full + p, ph, abort))) break;
+        if (!(ok = wait_or_abort(B.acc_empty, sp ^ 1u, abort))) break;
+        for (int h = 0; h < 2; ++h) {
+            const int sl = b_slot(sb, h);
+            if (!(ok = wait_or_abort(B.b_tx + sl, ph, abort))) break;
             tc_fence_after();
-            const uint32_t a = smem_u32(smem + OFF_A + orr.idx * OP_A);
-            const uint32_t b = smem_u32(smem + OFF_B + br.idx * OP_B);
+            const uint32_t base = smem_u32(smem + OFF_B + sl * SLOT_B);
 #pragma unroll
-            for (int kk = 0; kk < KS / 16; ++kk)
-                mma_f16(tmem + col_s1(p), desc_sw128(a + 32 * kk), desc_sw128(b + 32 * kk), IDESC_F16,
-                        (qq | kk) != 0);
-            mma_commit(B.a_empty + orr.idx);  // both slots free once these MMAs complete
-            mma_commit(B.b_empty + br.idx);
-            orr.next();
-            br.next();
+            for (int q = 0; q < 2; ++q) {
+#pragma unroll
+                for (int kk = 0; kk < KS / 16; ++kk)
+                    mma_f16_ta(tmem + COL_S1, tmem + col_a(p) + 64u * h + 32u * q + 8u * kk,
+                               desc_sw128(base + q * OP_B + 32 * kk), IDESC_F16, (h | q | kk) != 0);
+            }
+            if (h == 0) mma_commit(B.b_empty + sl);  // half 0 is free once these MMAs complete
         }
         if (!ok) break;
+        mma_commit(B.a_empty + p);
         if (!(ok = wait_or_abort(B.min_full + mr.idx, mr.phase, abort))) break;
-        if (!(ok = wait_or_abort(B.min_tx + mr.idx, mr.phase, abort))) break;
         tc_fence_after();
-        const uint32_t a = smem_u32(smem + OFF_MIN + mr.idx * MIN_STAGE);
-        mma_f16(tmem + col_s2(p), desc_plain(a, 128, 256), desc_plain(a + MIN_A, 128, 256), IDESC_F16, 0u);
+        const uint32_t a2 = smem_u32(smem + OFF_MINA + mr.idx * MIN_A);
+        const uint32_t b2 = smem_u32(smem + OFF_B + b_slot(sb, 1) * SLOT_B + SLOT_MIN);
+        mma_f16(tmem + COL_S2, desc_plain(a2, 128, 256), desc_plain(b2, 128, 256), IDESC_F16, 0u);
         mma_commit(B.min_empty + mr.idx);
         mr.next();
-        mma_commit(B.acc_full + p);  // S1 and S2 of this super-block are ready
+        mma_commit(B.b_empty + b_slot(sb, 1));
+        mma_commit(B.acc_full);  // S1 and S2 of this super-block are ready
     }
     mma_commit(B.fin);
 }
 
 // Epilogue (warps 12-27): warp w reads tensor-memory lanes 32 (w % 4) .. + 31
-// (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4.
+// (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4.  It frees the
+// accumulators as soon as they are in registers and promotes them while the
+// tensor core runs the next super-block.
 template <bool SUMS>
 __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int row0, int rows, int ct,
-                              int nsb, int batch, float *__restrict__ y, int32_t *__restrict__ sums,
-                              const uint8_t *__restrict__ xq, volatile uint32_t *abort) {
+                              int nsb, int rot, int batch, float *__restrict__ y,
+                              int32_t *__restrict__ sums, volatile uint32_t *abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int lq = warp & 3, h = (warp - EPI_WARP0) >> 2;
     const int r = lq * 32 + lane;
@@ -547,27 +578,31 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
     for (int c = 0; c < 32; ++c) yacc[c] = 0.0f;
     bool ok = true;
     for (int sb = 0; sb < nsb; ++sb) {
-        const int p = sb & 1;
-        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
-        if (!(ok = wait_warp(B.acc_full + p, ph, abort))) break;
-        if (!(ok = wait_warp(B.meta_full + p, ph, abort))) break;
-        if (!(ok = wait_warp(B.meta_tx + p, ph, abort))) break;
+        const int mi = sb % NSM;
+        const uint32_t mph = (uint32_t)(sb / NSM) & 1u;
+        if (!(ok = wait_warp(B.meta_full + mi, mph, abort))) break;
+        if (!(ok = wait_warp(B.acc_full, (uint32_t)sb & 1u, abort))) break;
         tc_fence_after();
-        const uint8_t *meta = smem + OFF_META + p * META_STAGE;
+        const uint8_t *meta = smem + OFF_META + mi * META_STAGE;
         const float d = reinterpret_cast<const float *>(meta + META_D)[r];
         const float dmin = reinterpret_cast<const float *>(meta + META_DMIN)[r];
         const float *dx = reinterpret_cast<const float *>(meta + META_DX) + 32 * h;
 #pragma unroll
         for (int c0 = 0; c0 < 32; c0 += 16) {
             float s1[16], s2[16];
-            tmem_ld16(lane_addr + col_s1(p) + c0, s1);
-            tmem_ld16(lane_addr + col_s2(p) + c0, s2);
+            tmem_ld16x2(lane_addr + COL_S1 + c0, lane_addr + COL_S2 + c0, s1, s2);
+            if (c0 == 16) {
+                // both halves are in registers: the accumulators may be reused
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B.acc_empty);
+            }
             if (SUMS) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int b = ct * TN + 32 * h + c0 + i;
                     if (row < rows && b < batch) {
-                        int32_t *o = sums + (((size_t)b * rows + row) * nsb + sb) * 2;
+                        int32_t *o = sums + (((size_t)b * rows + row) * nsb + kslot(sb, rot, nsb)) * 2;
                         o[0] = (int32_t)s1[i];
                         o[1] = (int32_t)s2[i];
                     }
@@ -578,12 +613,8 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
                     yacc[c0 + i] = fmaf(dx[c0 + i], d * s1[i] - dmin * s2[i], yacc[c0 + i]);
             }
         }
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(B.acc_empty + p);
-            mbar_arrive(B.meta_empty + p);
-        }
+        if (lane == 0) mbar_arrive(B.meta_empty + mi);
     }
     if (!ok || SUMS) return;
     if (row < rows) {
@@ -612,27 +643,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     // column tiles vary fastest, so the CTAs that read the same weight rows
     // run together and share them through L2
     const int row0 = blockIdx.y * TM, ct = blockIdx.x;
+    const int rot = (int)(blockIdx.y % (unsigned)nsb);
     const int nvalid = min(TM, rows - row0);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NOP; ++i) {
-            mbar_init(B.a_full + i, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(B.a_full + i, BLD_THREADS / 32);  // one arrival per builder warp
             mbar_init(B.a_empty + i, 1);
         }
-        for (int i = 0; i < NBR; ++i) {
+        for (int i = 0; i < NSM; ++i) {
+            mbar_init(B.min_full + i, 4);                // the four hh = 0 builder warps
+            mbar_init(B.min_empty + i, 1);
+            mbar_init(B.meta_full + i, BLD_THREADS);  // row scales (hh = 0) and column scales (hh = 1)
+            mbar_init(B.meta_empty + i, EPI_WARPS);
+        }
+        for (int i = 0; i < NBS; ++i) {
             mbar_init(B.b_tx + i, 1);
             mbar_init(B.b_empty + i, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(B.min_full + i, 4);
-            mbar_init(B.min_tx + i, 1);
-            mbar_init(B.min_empty + i, 1);
-            mbar_init(B.meta_full + i, TM);
-            mbar_init(B.meta_tx + i, 1);
-            mbar_init(B.meta_empty + i, EPI_WARPS);
-            mbar_init(B.acc_full + i, 1);
-            mbar_init(B.acc_empty + i, EPI_WARPS);
-        }
+        mbar_init(B.acc_full, 1);
+        mbar_init(B.acc_empty, EPI_WARPS);
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
             mbar_init(B.raw_empty + i, BLD_THREADS);
@@ -653,17 +683,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     const uint32_t tmem = *tmem_slot;
     pdl_wait();  // the packed activations come from the preceding kernel
 
-    if (warp == 0) {
-        role_producer_b(smem, B, ws, nsb, ct, abort);
+    if (warp == 0 || warp == 3) {
+        role_producer_b(smem, B, ws, nsb, ct, rot, warp == 3 ? 1 : 0, abort);
     } else if (warp == 2) {
-        role_producer_w(smem, B, &tmap_w, ws, row0, nsb, ct, abort);
+        role_producer_w(smem, B, &tmap_w, row0, nsb, rot, abort);
     } else if (warp == 1) {
         if (lane == 0) role_mma(smem, B, tmem, nsb, abort);
         __syncwarp();
     } else if (warp >= BLD_WARP0 && warp < EPI_WARP0) {
-        role_builder(smem, B, threadIdx.x - 32 * BLD_WARP0, nvalid, nsb, abort);
+        role_builder(smem, B, tmem, ws, ct, rot, nvalid, nsb, abort);
     } else if (warp >= EPI_WARP0) {
-        role_epilogue<SUMS>(smem, B, tmem, row0, rows, ct, nsb, batch, y, sums, xq, abort);
+        role_epilogue<SUMS>(smem, B, tmem, row0, rows, ct, nsb, rot, batch, y, sums, abort);
     }
     pdl_launch_dependents();
 
