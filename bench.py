@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode"], default=None,
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream"], default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
 
@@ -253,7 +253,9 @@ def run_gpu(args, world, rank):
     if args.only:
         fn = {"prefill": lambda: bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak),
               "sweep": lambda: bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph),
-              "decode": lambda: bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world)}
+              "decode": lambda: bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world),
+              "stream": lambda: bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak,
+                                             args.steps)}
         if rank == 0:
             print(json.dumps({"only": args.only, "result": fn[args.only]()}))
         else:
@@ -376,6 +378,29 @@ def run_gpu(args, world, rank):
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak, steps):
+    """Streaming capability of the fused Q4_K GEMV: one launch over 64
+    concatenated 4096x4096 matrices (262144 x 4096, 604 MB), timed over
+    back-to-back launches."""
+    W, x0 = inputs.gemv_q4_k(0)
+    Wq1 = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
+    del W
+    Wall = Wq1.reshape(1, -1).repeat(COPIES, 1)
+    x = torch.from_numpy(x0).to(dev)
+    y = torch.empty(1, GEMV_ROWS * COPIES, dtype=torch.float32, device=dev)
+
+    def body():
+        gq.gq_matmul_f32(gq.Q4_K, Wall, x, y, GEMV_ROWS * COPIES, GEMV_COLS, 1, gq.FLAG_W_STATIC)
+
+    k = max(2, min(steps, 50))
+    t, _ = time_graph(capture(body), k, 2)
+    gbs = Wall.numel() / (t / k) / 1e9
+    del Wall
+    torch.cuda.empty_cache()
+    return {"workload": "one launch over 262144 x 4096 Q4_K rows (604 MB)", "us": t / k * 1e6,
+            "weight_gbps": gbs, "frac": gbs / hbm_peak}
 
 
 def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
@@ -513,6 +538,7 @@ def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
         res[pname] = {"ms": per * 1e3, "tops": tops}
     res["mma"]["roofline"] = {"bound": "tensor", "achieved": res["mma"]["tops"], "peak": bf16_peak,
                               "unit": "TFLOP/s", "frac": res["mma"]["tops"] / bf16_peak,
+                              "traffic": kernel_traffic("mma_q4k"),
                               "note": "int ops counted as 2 per multiply-add; fp16 tensor kind"}
     del Wq, Xq, Y, wsb
     torch.cuda.empty_cache()
