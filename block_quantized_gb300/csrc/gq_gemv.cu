@@ -60,6 +60,9 @@ constexpr unsigned FULL = 0xffffffffu;
 #ifndef GQ_GEMV_MIN_BLOCKS
 #define GQ_GEMV_MIN_BLOCKS 1
 #endif
+#ifndef GQ_GEMV_PREFETCH
+#define GQ_GEMV_PREFETCH 1
+#endif
 
 constexpr int WARPS = GQ_GEMV_WARPS;      // warps per CTA
 
@@ -134,14 +137,16 @@ __device__ __forceinline__ uint2 split8(uint32_t a0, uint32_t a1) {
 // All loads of a pass are issued before any store, so a pass costs one
 // L2 round trip.
 
+constexpr int SG_BATCH = 6;  // code groups per thread per pass
+
 __device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nblocks, int nsb) {
     const int groups = nblocks * 32;
-    // pass p copies groups [4p*T, 4(p+1)*T) and block headers [p*T, (p+1)*T)
-    // (T = blockDim.x); there are at least as many group passes as header
-    // passes since every block has 32 groups.
+    // pass p copies groups [SG_BATCH*p*T, SG_BATCH*(p+1)*T) and block headers
+    // [p*T, (p+1)*T) (T = blockDim.x); there are at least as many group
+    // passes as header passes since every block has 32 groups.
     int pass = 0;
-    for (int base = 0; base < groups; base += 4 * blockDim.x, ++pass) {
-        uint32_t w0[4], w1[4], hd[5];
+    for (int base = 0; base < groups; base += SG_BATCH * blockDim.x, ++pass) {
+        uint32_t w0[SG_BATCH], w1[SG_BATCH], hd[5];
         const int hb = pass * blockDim.x + threadIdx.x;
         const bool has_h = hb < nblocks;
         if (has_h) {
@@ -151,7 +156,7 @@ __device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nbl
             for (int i = 0; i < 4; ++i) hd[1 + i] = __ldg(reinterpret_cast<const uint32_t *>(src + 260) + i);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < SG_BATCH; ++u) {
             const int g = base + u * blockDim.x + threadIdx.x;
             if (g < groups) {
                 const uint32_t *src = reinterpret_cast<const uint32_t *>(
@@ -161,7 +166,7 @@ __device__ void stage_q8_k(const Act &a, const uint8_t *__restrict__ xq, int nbl
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < SG_BATCH; ++u) {
             const int g = base + u * blockDim.x + threadIdx.x;
             if (g < groups) {
                 const int blk = g >> 5;
@@ -248,12 +253,16 @@ __device__ __forceinline__ float q8_code(float x, float d, float r) {
 
 // Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
 // (= code group l of the layout).
+// Each warp loads up to QS_BATCH of its blocks before quantizing any, so a
+// row of up to QS_BATCH * warps blocks costs one L2 round trip.
+constexpr int QS_BATCH = 6;
+
 __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks, int nsb) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    for (int b0 = warp; b0 < nblocks; b0 += 2 * nw) {
-        float4 v[2][2];
+    for (int b0 = warp; b0 < nblocks; b0 += QS_BATCH * nw) {
+        float4 v[QS_BATCH][2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < QS_BATCH; ++u) {
             const int blk = b0 + u * nw;
             if (blk < nblocks) {
                 const float4 *p = reinterpret_cast<const float4 *>(x + (size_t)blk * QK_K + 8 * lane);
@@ -262,7 +271,7 @@ __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int 
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < QS_BATCH; ++u) {
             const int blk = b0 + u * nw;
             if (blk >= nblocks) break;  // warp-uniform
             const float e[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
@@ -479,6 +488,92 @@ __device__ __forceinline__ float rows_q4_k_nb1(const uint8_t *ch, size_t row_byt
     return s;
 }
 
+// Transposed butterfly over V = 2^k values per lane (V <= 32): each level
+// halves the values a lane keeps, so the V warp sums cost V - 1 shuffles plus
+// 5 - k for the rest of the butterfly.  Afterwards lane l holds the sum of
+// value index sum_j bit(4 - j, l) << (k - 1 - j), j < k.
+template <int V>
+__device__ __forceinline__ float transpose_reduce(float (&v)[V], int lane) {
+#pragma unroll
+    for (int lvl = 0; (1 << lvl) < V; ++lvl) {
+        const int n = V >> lvl, o = 16 >> lvl;
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float recv = __shfl_xor_sync(FULL, up ? v[i] : v[i + n / 2], o);
+            v[i] = (up ? v[i + n / 2] : v[i]) + recv;
+        }
+    }
+    constexpr int K = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : V >= 2 ? 1 : 0;
+    float s = v[0];
+#pragma unroll
+    for (int o = 16 >> K; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+    return s;
+}
+
+__device__ __forceinline__ int transpose_index(int lane, int k) {
+    int idx = 0;
+    for (int j = 0; j < k; ++j) idx |= ((lane >> (4 - j)) & 1) << (k - 1 - j);
+    return idx;
+}
+
+// Q4_K product of NB > 1 vectors with an item of nr <= MR whole rows: per
+// chunk, the rows' nibbles and scales are loaded into registers once and each
+// vector's activation slice once, so the shared-memory traffic per row and
+// vector is the dot product's alone.  The MR x NB sums are reduced together
+// and written by the lanes that hold them.
+template <int NB, int MR>
+__device__ __forceinline__ void item_q4k_multi(const uint8_t *ch, size_t row_bytes, int nr, int nblk, int nvec,
+                                               const Act &a, float *__restrict__ y, int rows, int row0, int b0,
+                                               int lane) {
+    const int h = lane & 1, sbl = lane >> 1;
+    const uint32_t sel_sc = h ? 0x0543u : 0x0210u, sel_m = h ? 0x0765u : 0x0432u;
+    float v[MR * NB];
+#pragma unroll
+    for (int i = 0; i < MR * NB; ++i) v[i] = 0.0f;
+    const int nchunk = (nblk + 15) / 16;
+    for (int c = 0; c < nchunk; ++c) {
+        const int sb = 16 * c + sbl;
+        const bool active = sb < nblk;
+        uint4 hd[MR], q[MR][4];
+#pragma unroll
+        for (int r = 0; r < MR; ++r) {
+            hd[r] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) q[r][k] = make_uint4(0, 0, 0, 0);
+            if (active && r < nr) {
+                const uint8_t *p = ch + r * row_bytes + (size_t)sb * Q4_K_BYTES;
+                hd[r] = *reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) q[r][k] = *reinterpret_cast<const uint4 *>(p + 16 + 64 * h + 16 * k);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (b >= nvec) break;  // warp-uniform
+            Q4KAct act;
+            if (active) load_q4k_act(act, a, b * nblk + sb, h, lane & 7);
+#pragma unroll
+            for (int r = 0; r < MR; ++r) {
+                if (r >= nr) break;  // warp-uniform
+                int S1 = 0, S2 = 0;
+                if (active) {
+                    dot_q4k_half(q[r], act, __byte_perm(hd[r].y, hd[r].z, sel_sc), __byte_perm(hd[r].z, hd[r].w, sel_m),
+                                 S1, S2);
+                    const float d = half_bits_to_float(hd[r].x), dmin = half_bits_to_float(hd[r].x >> 16);
+                    v[r * NB + b] += act.dx * (d * (float)S1 - dmin * (float)S2);
+                }
+            }
+        }
+    }
+    constexpr int V = MR * NB;
+    constexpr int K = V >= 32 ? 5 : V >= 16 ? 4 : V >= 8 ? 3 : V >= 4 ? 2 : 1;
+    const float s = transpose_reduce<V>(v, lane);
+    const int idx = transpose_index(lane, K);
+    const int r = idx / NB, b = idx % NB;
+    if ((lane & ((1 << (5 - K)) - 1)) == 0 && r < nr && b < nvec) y[(size_t)(b0 + b) * rows + row0 + r] = s;
+}
+
 // Q4_0 / Q8_0 chunk of nb_c blocks starting at block blk0 of the row; lane k
 // takes blocks k, k + 32, ...  A block starting `off` bytes into the chunk is
 // read as aligned words from off & ~3; its code bytes begin 2 or 4 bytes into
@@ -541,12 +636,15 @@ __device__ __forceinline__ void chunk_q_0(const uint8_t *ch, int nb_c, int blk0,
 // ------------------------------------------------------------- the kernel
 
 // Ring geometry, chosen per launch.  A ring item is R whole rows (one bulk
-// copy of R * row_bytes contiguous bytes) when a row fits in one chunk, else
-// one chunk of one row (R = 1).  Each warp owns `ns` stages of `stage_bytes`.
+// copy of R * row_bytes contiguous bytes) when two stages of a row fit the
+// ring budget, else one chunk of one row (R = 1).  A bulk copy costs about
+// the same issue time whatever its size, so whole rows stream better than
+// chunks.  Each warp owns `ns` stages of `stage_bytes`.
 struct Geo {
     int R;            // rows per item (1, 2 or 4)
     int ns;           // stages per warp, 1..MAX_STAGE
     int stage_bytes;  // bytes per stage: a 16-byte multiple with 16 bytes of over-read slack
+    int whole;        // 1: items are whole rows; 0: items are single chunks of one row
 };
 constexpr int MAX_STAGE = 8;
 constexpr int MAX_R = GQ_GEMV_MAX_R;
@@ -579,24 +677,26 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
     const int wg = blockIdx.x * NW + warp;
     const int nchunk = (nblk + F::CH - 1) / F::CH;
     const int R = geo.R, ns = geo.ns;
+    const int ipg = geo.whole ? 1 : nchunk;  // ring items per row group
     const int ngroups = (rows + R - 1) / R;
     const int mine = wg < ngroups ? (ngroups - 1 - wg) / warps_total + 1 : 0;
-    const int total = mine * nchunk;
+    const int total = mine * ipg;
     const size_t row_bytes = (size_t)nblk * F::BB;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * MAX_STAGE;
     uint8_t *ring = smem + bufs_off<NW>() + (size_t)warp * ns * geo.stage_bytes;
 
-    // item i of this warp = chunk (i % nchunk) of row group wg + (i / nchunk) * warps_total
+    // item i of this warp = row group wg + (i / ipg) * warps_total, whole or
+    // its chunk i % ipg
     auto issue = [&](int i, int st) {
-        const int g = wg + (i / nchunk) * warps_total;
+        const int g = wg + (i / ipg) * warps_total;
         const uint8_t *src;
         uint32_t bytes;
-        if (nchunk == 1) {
+        if (geo.whole) {
             const int nr = min(R, rows - g * R);
             src = W + (size_t)g * R * row_bytes;
             bytes = (uint32_t)(nr * row_bytes);
         } else {
-            const int c = i % nchunk;
+            const int c = i % ipg;
             src = W + (size_t)g * row_bytes + (size_t)c * F::CH * F::BB;
             bytes = (uint32_t)(min(F::CH, nblk - c * F::CH) * F::BB);
         }
@@ -609,15 +709,19 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
     // kernel produces); otherwise it launches once this kernel's activations
     // are staged.
     if (GQ_GEMV_EARLY_TRIGGER) pdl_launch_dependents();
+    // Items requested before the activations are staged; the rest of the
+    // first ring fill follows the staging, so the activation loads do not
+    // queue behind a full ring of weight copies.
+    const int pre = min(ns, GQ_GEMV_PREFETCH);
     if (lane == 0 && total > 0) {
         for (int s = 0; s < ns; ++s) mbar_init(bar + s, 1);
         fence_mbar_init();
         if (w_static)
-            for (int i = 0; i < ns && i < total; ++i) issue(i, i);
+            for (int i = 0; i < pre && i < total; ++i) issue(i, i);
     }
     pdl_wait();  // activations (and, unless static, W) may come from the preceding kernel
     if (lane == 0 && !w_static)
-        for (int i = 0; i < ns && i < total; ++i) issue(i, i);
+        for (int i = 0; i < pre && i < total; ++i) issue(i, i);
 
     const Act a = act_layout<WT>(smem + bufs_off<NW>() + (size_t)NW * ns * geo.stage_bytes, NB, nblk);
     const int nact = nvec * nblk;
@@ -636,6 +740,8 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
     }
     __syncthreads();
     if (!GQ_GEMV_EARLY_TRIGGER) pdl_launch_dependents();
+    if (lane == 0)
+        for (int i = pre; i < ns && i < total; ++i) issue(i, i);
 
     float acc[NB];
 #pragma unroll
@@ -688,7 +794,7 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
             }
             return;
         }
-        const int g = wg + (i / nchunk) * warps_total;
+        const int g = wg + (i / ipg) * warps_total;
         const uint8_t *ch = ring + (size_t)st * geo.stage_bytes;
         if (WT == GQ_Q4_K && NB == 1 && !SUMS && nchunk == 1) {
             // batch-1 hot path: the item's rows interleaved (act_resident holds)
@@ -707,14 +813,19 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
             }
             if ((lane & 7) == 0 && rr < nr && (R == 4 || (lane & 8) == 0) && (R >= 2 || lane == 0))
                 y[(size_t)b0 * rows + r0 + rr] = v;
-        } else if (nchunk == 1) {
+        } else if (WT == GQ_Q4_K && NB > 1 && !SUMS && geo.whole) {
+            // batch 2..8: rows in registers, each vector's slice loaded once per chunk
+            item_q4k_multi<NB, (NB * MAX_R <= 32 ? MAX_R : 32 / NB)>(ch, row_bytes, min(R, rows - g * R), nblk,
+                                                                     nvec, a, y, rows, g * R, b0, lane);
+        } else if (geo.whole) {
             const int nr = min(R, rows - g * R);
             for (int r = 0; r < nr; ++r) {
-                segment(ch + r * row_bytes, g * R + r, 0);
+                for (int c = 0; c < nchunk; ++c)
+                    segment(ch + r * row_bytes + (size_t)c * F::CH * F::BB, g * R + r, c);
                 finish_row(g * R + r);
             }
         } else {
-            const int c = i % nchunk;
+            const int c = i % ipg;
             segment(ch, g, c);
             if (c == nchunk - 1) finish_row(g);
         }
@@ -800,11 +911,13 @@ size_t smem_bytes(const Geo &g, int nb, int nblk) {
     return (size_t)bufs_off<NW>() + (size_t)NW * g.ns * g.stage_bytes + act_bytes<WT>(nb, nblk);
 }
 
-// Ring geometry for `rows` rows of `nblk` blocks streamed by `warps` warps:
-// the most rows per bulk copy (up to 4) that still gives every warp an item
-// (bigger copies stream better; spreading a short matrix over all warps
-// finishes it sooner), then as many stages as the warp has items, within the
-// per-CTA budget.
+// Ring geometry for `rows` rows of `nblk` blocks streamed by `warps` warps.
+// Items are whole rows when two stages of one row per warp fit the ring
+// budget.  Then R is the most rows per bulk copy (up to 4) that still gives
+// every warp an item and keeps two stages per warp within the budget (bigger
+// copies stream better; spreading a short matrix over all warps finishes it
+// sooner).  Finally there are as many stages as the warp has items, within the
+// budget.
 template <int WT, int NW>
 Geo pick_geo(int rows, int nblk, int warps) {
     using F = Fmt<WT>;
@@ -812,14 +925,15 @@ Geo pick_geo(int rows, int nblk, int warps) {
     const size_t row_bytes = (size_t)nblk * F::BB;
     Geo g;
     g.R = 1;
-    if (nchunk == 1)
+    g.whole = (size_t)NW * 2 * (size_t)round16(row_bytes + 16) <= (size_t)RING_BUDGET ? 1 : 0;
+    if (g.whole)
         for (int r = MAX_R; r > 1; r >>= 1)
-            if ((rows + r - 1) / r >= warps) {
+            if ((rows + r - 1) / r >= warps && (size_t)NW * 2 * (size_t)round16(r * row_bytes + 16) <= (size_t)RING_BUDGET) {
                 g.R = r;
                 break;
             }
-    g.stage_bytes = round16((nchunk == 1 ? g.R * row_bytes : (size_t)F::CH * F::BB) + 16);
-    const int items = (rows + g.R - 1) / g.R * nchunk;
+    g.stage_bytes = round16((g.whole ? g.R * row_bytes : (size_t)F::CH * F::BB) + 16);
+    const int items = (rows + g.R - 1) / g.R * (g.whole ? 1 : nchunk);
     const int per_warp = (items + warps - 1) / warps;
     const int ns_budget = std::max(1, RING_BUDGET / (NW * g.stage_bytes));
     g.ns = std::max(1, std::min(std::min(per_warp, ns_budget), MAX_STAGE));
@@ -832,6 +946,13 @@ cudaError_t launch_one(const void *W, const void *act, float *y, int32_t *sums, 
     auto k = gemv_kernel<WT, NB, SUMS, FUSED, NW>;
     Geo geo = pick_geo<WT, NW>(rows, nblk, ctx.num_sms * CTAS_PER_SM * NW);
     while (geo.ns > 1 && smem_bytes<WT, NW>(geo, NB, nblk) > (size_t)SMEM_MAX) --geo.ns;
+    if (geo.whole && smem_bytes<WT, NW>(geo, NB, nblk) > (size_t)SMEM_MAX) {
+        // many staged vectors leave no room for whole rows: stream chunks
+        geo.whole = 0;
+        geo.R = 1;
+        geo.ns = 1;
+        geo.stage_bytes = round16((size_t)Fmt<WT>::CH * Fmt<WT>::BB + 16);
+    }
     const size_t smem = smem_bytes<WT, NW>(geo, NB, nblk);
     if (smem > (size_t)SMEM_MAX) return cudaErrorInvalidValue;
     if (smem > 48 * 1024) {
@@ -860,6 +981,7 @@ int pick_nb(int batch, int nblk) {
     Geo g1;
     g1.R = 1;
     g1.ns = 1;
+    g1.whole = 0;
     g1.stage_bytes = round16((size_t)F::CH * F::BB + 16);
     for (int nb = 8; nb >= 1; nb >>= 1)
         if (nb <= std::max(batch, 1) && smem_bytes<WT, WARPS>(g1, nb, nblk) <= (size_t)SMEM_MAX) return nb;
