@@ -11,8 +11,8 @@
 // super-block is exact while partial sums stay below 2^24, so the tensor core
 // returns the integer S1 = sum_j sc_j * s_j of "llama.cpp 推理引擎" §5.5's
 // two-level scheme.  The min-term integer S2 = sum_j m_j * t_j (t_j the
-// activation sub-block sums) is one more K=16 step per super-block into a
-// second accumulator, with t_j split exactly as t_lo + 64 t_hi:
+// activation sub-block sums) is one more K=16 step per super-block, with t_j
+// split exactly as t_lo + 64 t_hi:
 //   A2[r] = [m_0..m_7 | 64 m_0..64 m_7]   B2[b] = [t_lo_0..t_lo_7 | t_hi_0..t_hi_7]
 // (all exact in fp16, |S2| < 2^21).  Per super-block the epilogue promotes
 // both exact integers:
@@ -20,10 +20,10 @@
 //
 // CTA tile: 128 weight rows x 128 batch columns, one super-block (K = 256) per
 // step, 28 warps:
-//   warps 0, 3 activation producers: one 1-D bulk copy each per
-//              super-block of the packed unit's half 0 (B stages 0-1) or half
-//              1 (stages 2-3 and the min-term B tile) into a 4-slot ring (two
-//              super-blocks ahead);
+//   warps 0, 3 activation producers: one bulk copy each per super-block of
+//              the packed unit's half 0 (B stages 0-1) or half 1 (stages 2-3
+//              and the min-term B tile) into a 4-slot ring, two super-blocks
+//              ahead;
 //   warp 1     MMA issuer (one thread) and tensor-memory owner;
 //   warp 2     weight producer: one 2-D tiled TMA load per super-block of
 //              the raw Q4_K rows, two super-blocks ahead (box 144 bytes x
@@ -31,14 +31,14 @@
 //   warps 4-11 A builders: two threads per weight row, each turning half of
 //              the raw super-block into fp16 sc*q and storing it straight
 //              from registers into tensor memory (tcgen05.st), where the MMA
-//              reads the A operand -- double-buffered by super-block, so
-//              building the next super-block overlaps the current one's
-//              MMAs and no shared-memory bandwidth is spent on A; the first
-//              half then writes the min-term row and the row scales d, dmin;
-//   warps 12-27 epilogue: four threads per row, 32 columns each; it frees the
-//              accumulators once they are in registers.
-// Tensor memory (512 columns): S1 and S2 of the current super-block (128
-// each) and two 128-column A buffers.
+//              reads the A operand; then the row scales and min-term row
+//              (first half) or the column scales (second half);
+//   warps 12-27 epilogue: four threads per row, 32 columns each.
+// Tensor memory (512 columns): the S1 accumulator and the A operand, each
+// double-buffered by super-block (4 x 128 columns).  The min-term step writes
+// S2 over the A buffer its super-block has just consumed, so the builders run
+// a super-block ahead of the MMAs and the MMAs a super-block ahead of the
+// epilogue.
 // The activation operand is packed once per call by pack_kernel into a
 // caller-provided workspace, already in the swizzled shared-memory image, so
 // each operand tile is a single 1-D bulk copy.
@@ -97,10 +97,10 @@ constexpr int OFF_MINA = OFF_B + NBS * SLOT_B;            // NSM x 4 KB min-term
 constexpr int OFF_RAW = OFF_MINA + NSM * MIN_A;           // NRAW x 18 KB
 constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;      // NSM x 1.5 KB scales
 constexpr int OFF_BAR = OFF_META + NSM * META_STAGE;
-// A: full (builders), empty (by parity); B: full-tx (producers), empty; min:
+// A: full (builders), empty (epilogue); B: full-tx (producers), empty; min:
 // full (builders), empty; raw: full, empty; meta: full (builders), empty;
 // acc: full, empty; final.
-constexpr int NBARS = 2 * 2 + 2 * NBS + 2 * NSM + 2 * NRAW + 2 * NSM + 2 + 1;
+constexpr int NBARS = 2 * 2 + 2 * NBS + 2 * NSM + 2 * NRAW + 2 * NSM + 2 * 2 + 1;
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
@@ -109,12 +109,14 @@ static_assert(SLOT_B % 1024 == 0 && OP_B % 1024 == 0, "SW128 tiles need 1024-byt
 static_assert(OFF_RAW % 128 == 0 && RAW_STAGE % 128 == 0, "tiled TMA destinations are 128-byte aligned");
 static_assert(WS_UNIT % 16 == 0 && HALF1_BYTES % 16 == 0 && SLOT_MIN % 16 == 0, "bulk copies move 16-byte units");
 
-// Tensor-memory columns: the S1 and S2 accumulators of the current
-// super-block (128 each), and the A operand (one super-block, 256 K as fp16
-// pairs = 128 columns) double-buffered by super-block parity, so the
-// builders work a whole super-block ahead of the MMAs.
+// Tensor-memory columns: the S1 accumulator double-buffered by super-block
+// parity (2 x 128), and the A operand (one super-block, 256 K as fp16 pairs =
+// 128 columns) double-buffered the same way.  Once the sixteen S1 steps of a
+// super-block have read its A buffer, the min-term step writes S2 over it
+// (the tensor core executes one thread's MMAs in issue order), and the
+// epilogue frees the buffer for the builders when it has read S2.
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S1 = 0, COL_S2 = 128;
+__host__ __device__ constexpr uint32_t col_s1(int p) { return 128u * (uint32_t)p; }
 __host__ __device__ constexpr uint32_t col_a(int p) { return 256u + 128u * (uint32_t)p; }
 
 constexpr int NTHREADS = 896;
@@ -178,7 +180,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -345,8 +346,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     r.meta_full = r.raw_empty + NRAW;
     r.meta_empty = r.meta_full + NSM;
     r.acc_full = r.meta_empty + NSM;
-    r.acc_empty = r.acc_full + 1;
-    r.fin = r.acc_empty + 1;
+    r.acc_empty = r.acc_full + 2;
+    r.fin = r.acc_empty + 2;
     return r;
 }
 
@@ -433,9 +434,11 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
 // tensor-memory lanes; row t = 32 (w % 4) + lane) for half hh = (w - 4) / 4
 // of every super-block, i.e. sub-blocks 4hh .. 4hh + 3 = K 128hh .. + 127 =
 // A columns 64hh .. + 63 of the buffer of the super-block's parity.  Each
-// sub-block is 16 columns, written by one tcgen05.st from registers.  The
-// hh = 0 threads then write the row scales and the min-term row, the hh = 1
-// threads the scale of column t (read from the workspace).
+// sub-block is 16 columns, written by one tcgen05.st from registers; the
+// buffer is free again once the epilogue has read the S2 written over it.
+// Then the hh = 0 threads write row t's scales d, dmin and its min-term A row,
+// the hh = 1 threads column t's scale (read from the workspace, requested
+// before the raw weights are waited for).
 __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const uint8_t *__restrict__ ws,
                              int ct, int rot, int nvalid, int nsb, volatile uint32_t *abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -444,6 +447,13 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     RingPos rr(NRAW), mr(NSM);
     for (int sb = 0; sb < nsb; ++sb) {
+        const int p = sb & 1;
+        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
+        float dx = 0.0f;
+        if (hh == 1) {
+            const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * WS_UNIT;
+            dx = __ldg(reinterpret_cast<const float *>(unit + WS_B + WS_MIN) + t);
+        }
         if (!wait_warp(B.raw_full + rr.idx, rr.phase, abort)) return;
         const uint8_t *raw = smem + OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
         uint4 h = make_uint4(0, 0, 0, 0), q[4];
@@ -458,8 +468,7 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         rr.next();
 
         // this half of the A operand: sc_j * q for sub-blocks 4hh .. 4hh + 3
-        const int p = sb & 1;
-        if (!wait_warp(B.a_empty + p, ((uint32_t)(sb >> 1) & 1u) ^ 1u, abort)) return;
+        if (!wait_warp(B.a_empty + p, ph ^ 1u, abort)) return;
         tc_fence_after();
         const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
 #pragma unroll
@@ -479,48 +488,44 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         __syncwarp();
         if (lane == 0) mbar_arrive(B.a_full + p);
 
-        // then (off the MMA's critical path) the scales and the min-term row
-        if (hh == 1) {
-            const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * WS_UNIT;
-            const float dx = __ldg(reinterpret_cast<const float *>(unit + WS_B + WS_MIN) + t);
-            if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-            reinterpret_cast<float *>(smem + OFF_META + mr.idx * META_STAGE + META_DX)[t] = dx;
-            mbar_arrive(B.meta_full + mr.idx);
-            mr.next();
-        } else {
-            // row scales and the min-term row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
-            const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);
-            int mn[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) mn[j] = (int)((hi64 >> (6 * j + 16)) & 63);
-            if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-            uint8_t *meta = smem + OFF_META + mr.idx * META_STAGE;
+        // then (off the MMA's critical path) the epilogue's scales and, for
+        // hh = 0, the min-term A row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
+        if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
+        uint8_t *meta = smem + OFF_META + mr.idx * META_STAGE;
+        if (hh == 0) {
             reinterpret_cast<float *>(meta + META_D)[t] = half_bits_to_float(h.x);
             reinterpret_cast<float *>(meta + META_DMIN)[t] = half_bits_to_float(h.x >> 16);
-            mbar_arrive(B.meta_full + mr.idx);
-            if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-            uint8_t *ma = smem + OFF_MINA + mr.idx * MIN_A;
+        } else {
+            reinterpret_cast<float *>(meta + META_DX)[t] = dx;
+        }
+        mbar_arrive(B.meta_full + mr.idx);
+        if (hh == 0) {
+            const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);  // header bits 32..95
             uint32_t lo[4], hi[4];
 #pragma unroll
             for (int j = 0; j < 8; j += 2) {
-                lo[j >> 1] = pack_h2((float)mn[j], (float)mn[j + 1]);
-                hi[j >> 1] = pack_h2(64.0f * (float)mn[j], 64.0f * (float)mn[j + 1]);
+                const float m0 = (float)(int)((hi64 >> (6 * j + 16)) & 63);
+                const float m1 = (float)(int)((hi64 >> (6 * (j + 1) + 16)) & 63);
+                lo[j >> 1] = pack_h2(m0, m1);
+                hi[j >> 1] = pack_h2(64.0f * m0, 64.0f * m1);
             }
+            if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
+            uint8_t *ma = smem + OFF_MINA + mr.idx * MIN_A;
             *reinterpret_cast<uint4 *>(ma + plain_off(t, 0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             *reinterpret_cast<uint4 *>(ma + plain_off(t, 1)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.min_full + mr.idx);
-            mr.next();
         }
+        mr.next();
     }
 }
 
 // MMA issuer (warp 1, one thread).  Per super-block: sixteen K=16 steps of
 // the S1 product (A from the tensor-memory buffer of the super-block's
-// parity, B from the two halves of the unit in the ring), then one K=16 step
-// of the min-term product S2 (A rows from the builders, B tile from half 1),
-// both into the accumulator pair, which the epilogue must have drained first.
+// parity, B from the two halves of the unit in the ring) into the S1 buffer of
+// the same parity, then one K=16 step of the min-term product S2 (A rows from
+// the builders, B tile from half 1) written over the consumed A buffer.
 // Always ends with a commit to `fin` so the teardown can wait for every MMA
 // to finish.
 __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, volatile uint32_t *abort) {
@@ -528,9 +533,9 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
         const int p = sb & 1;
-        const uint32_t ph = (uint32_t)(sb >> 1) & 1u, sp = (uint32_t)sb & 1u;
+        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
         if (!(ok = wait_or_abort(B.a_full + p, ph, abort))) break;
-        if (!(ok = wait_or_abort(B.acc_empty, sp ^ 1u, abort))) break;
+        if (!(ok = wait_or_abort(B.acc_empty + p, ph ^ 1u, abort))) break;
         for (int h = 0; h < 2; ++h) {
             const int sl = b_slot(sb, h);
             if (!(ok = wait_or_abort(B.b_tx + sl, ph, abort))) break;
@@ -540,30 +545,30 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
             for (int q = 0; q < 2; ++q) {
 #pragma unroll
                 for (int kk = 0; kk < KS / 16; ++kk)
-                    mma_f16_ta(tmem + COL_S1, tmem + col_a(p) + 64u * h + 32u * q + 8u * kk,
+                    mma_f16_ta(tmem + col_s1(p), tmem + col_a(p) + 64u * h + 32u * q + 8u * kk,
                                desc_sw128(base + q * OP_B + 32 * kk), IDESC_F16, (h | q | kk) != 0);
             }
             if (h == 0) mma_commit(B.b_empty + sl);  // half 0 is free once these MMAs complete
         }
         if (!ok) break;
-        mma_commit(B.a_empty + p);
         if (!(ok = wait_or_abort(B.min_full + mr.idx, mr.phase, abort))) break;
         tc_fence_after();
         const uint32_t a2 = smem_u32(smem + OFF_MINA + mr.idx * MIN_A);
         const uint32_t b2 = smem_u32(smem + OFF_B + b_slot(sb, 1) * SLOT_B + SLOT_MIN);
-        mma_f16(tmem + COL_S2, desc_plain(a2, 128, 256), desc_plain(b2, 128, 256), IDESC_F16, 0u);
+        mma_f16(tmem + col_a(p), desc_plain(a2, 128, 256), desc_plain(b2, 128, 256), IDESC_F16, 0u);
         mma_commit(B.min_empty + mr.idx);
         mr.next();
         mma_commit(B.b_empty + b_slot(sb, 1));
-        mma_commit(B.acc_full);  // S1 and S2 of this super-block are ready
+        mma_commit(B.acc_full + p);  // S1 and S2 of this super-block are ready
     }
     mma_commit(B.fin);
 }
 
 // Epilogue (warps 12-27): warp w reads tensor-memory lanes 32 (w % 4) .. + 31
-// (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4.  It frees the
-// accumulators as soon as they are in registers and promotes them while the
-// tensor core runs the next super-block.
+// (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4, of S1 and of the
+// S2 written over the A buffer.  It frees both as soon as they are in
+// registers and promotes them while the tensor core runs the next
+// super-block.
 template <bool SUMS>
 __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int row0, int rows, int ct,
                               int nsb, int rot, int batch, float *__restrict__ y,
@@ -578,10 +583,12 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
     for (int c = 0; c < 32; ++c) yacc[c] = 0.0f;
     bool ok = true;
     for (int sb = 0; sb < nsb; ++sb) {
+        const int p = sb & 1;
+        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
         const int mi = sb % NSM;
         const uint32_t mph = (uint32_t)(sb / NSM) & 1u;
         if (!(ok = wait_warp(B.meta_full + mi, mph, abort))) break;
-        if (!(ok = wait_warp(B.acc_full, (uint32_t)sb & 1u, abort))) break;
+        if (!(ok = wait_warp(B.acc_full + p, ph, abort))) break;
         tc_fence_after();
         const uint8_t *meta = smem + OFF_META + mi * META_STAGE;
         const float d = reinterpret_cast<const float *>(meta + META_D)[r];
@@ -590,12 +597,15 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
 #pragma unroll
         for (int c0 = 0; c0 < 32; c0 += 16) {
             float s1[16], s2[16];
-            tmem_ld16x2(lane_addr + COL_S1 + c0, lane_addr + COL_S2 + c0, s1, s2);
+            tmem_ld16x2(lane_addr + col_s1(p) + c0, lane_addr + col_a(p) + c0, s1, s2);
             if (c0 == 16) {
-                // both halves are in registers: the accumulators may be reused
+                // both halves are in registers: S1 and the A buffer may be reused
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(B.acc_empty);
+                if (lane == 0) {
+                    mbar_arrive(B.acc_empty + p);
+                    mbar_arrive(B.a_empty + p);
+                }
             }
             if (SUMS) {
 #pragma unroll
@@ -649,23 +659,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(B.a_full + i, BLD_THREADS / 32);  // one arrival per builder warp
-            mbar_init(B.a_empty + i, 1);
-        }
-        for (int i = 0; i < NSM; ++i) {
-            mbar_init(B.min_full + i, 4);                // the four hh = 0 builder warps
-            mbar_init(B.min_empty + i, 1);
-            mbar_init(B.meta_full + i, BLD_THREADS);  // row scales (hh = 0) and column scales (hh = 1)
-            mbar_init(B.meta_empty + i, EPI_WARPS);
+            mbar_init(B.a_empty + i, EPI_WARPS);        // the epilogue has read the S2 over it
+            mbar_init(B.acc_full + i, 1);
+            mbar_init(B.acc_empty + i, EPI_WARPS);
         }
         for (int i = 0; i < NBS; ++i) {
             mbar_init(B.b_tx + i, 1);
             mbar_init(B.b_empty + i, 1);
         }
-        mbar_init(B.acc_full, 1);
-        mbar_init(B.acc_empty, EPI_WARPS);
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
             mbar_init(B.raw_empty + i, BLD_THREADS);
+        }
+        for (int i = 0; i < NSM; ++i) {
+            mbar_init(B.meta_full + i, BLD_THREADS);  // every builder thread writes one entry
+            mbar_init(B.meta_empty + i, EPI_WARPS);
+            mbar_init(B.min_full + i, 4);             // the four hh = 0 builder warps
+            mbar_init(B.min_empty + i, 1);
         }
         mbar_init(B.fin, 1);
         *abort = 0u;
