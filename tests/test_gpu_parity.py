@@ -140,6 +140,23 @@ def test_gemv_block_sums_and_y(wtype, rows, cols, batch):
     assert_close(y, y_ref, T)
 
 
+# Tall enough that the GEMV ring carries two or four whole rows per bulk copy
+# (rows >= 2 x warps on the GPU), rows spanning several 16-super-block chunks,
+# ragged last row groups, and batches through the multi-vector item path.
+TALL_SHAPES = [(4867, 4096, 1), (4867, 4096, 5), (2435, 8192, 1), (2435, 8192, 3), (2435, 8192, 8)]
+
+
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
+@pytest.mark.parametrize("rows,cols,batch", TALL_SHAPES)
+def test_gemv_tall_whole_row_items(wtype, rows, cols, batch):
+    W, X, Wq, Xq = make_case(wtype, rows, cols, batch, seed=rows + cols + 31 * batch, outliers=False)
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = host(gq.block_sums(wtype, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    np.testing.assert_array_equal(s, orc.block_sums(wtype, Wq, Xq, rows, cols, batch))
+    y_ref, T = orc.matmul_ref(wtype, Wq, Xq, rows, cols, batch)
+    assert_close(host(gq.matmul(wtype, Wd, Xd, rows, cols, batch, gq.PATH_GEMV)), y_ref, T)
+
+
 @pytest.mark.parametrize("wtype", [Q4_0, Q8_0])
 @pytest.mark.parametrize("rows,cols,batch", [(5, 32, 1), (11, 96, 2), (9, 4128, 3)])
 def test_gemv_unaligned_rows(wtype, rows, cols, batch):
