@@ -456,21 +456,18 @@ def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
 
     # the same weights stored as fused matrices -- wq|wk|wv (12288 rows) and
     # w1|w3 (22016 rows) concatenated by rows -- so each group sharing an input
-    # is one launch: 4 products (and one standalone quantize) per layer
+    # is one launch: 4 products per layer
     fused_w = [{"qkv": torch.cat([lw["wq"], lw["wk"], lw["wv"]]), "wo": lw["wo"],
                 "w13": torch.cat([lw["w1"], lw["w3"]]), "w2": lw["w2"]} for lw in layers]
     y_qkv = torch.empty(3 * 4096, dtype=torch.float32, device=dev)
     y_13 = torch.empty(2 * 11008, dtype=torch.float32, device=dev)
 
     def token_grouped():
-        # the 11008-wide input of w2 is quantized by the standalone kernel: at
-        # that width one quantize beats every CTA quantizing it again
         for lw in fused_w:
             gq.gq_matmul_f32(gq.Q4_K, lw["qkv"], xin["attn"], y_qkv, 3 * 4096, 4096, 1, F)
             gq.gq_matmul_f32(gq.Q4_K, lw["wo"], xin["o"], outs["wo"], 4096, 4096, 1, F)
             gq.gq_matmul_f32(gq.Q4_K, lw["w13"], xin["ffn"], y_13, 2 * 11008, 4096, 1, F)
-            gq.gq_quantize_rows_async(gq.Q8_K, xin["down"], xq["down"], 11008)
-            gq.gq_matmul_ex(gq.Q4_K, lw["w2"], xq["down"], outs["w2"], 4096, 11008, 1, G, F)
+            gq.gq_matmul_f32(gq.Q4_K, lw["w2"], xin["down"], outs["w2"], 4096, 11008, 1, F)
         gq.gq_matmul_f32(gq.Q8_0, head, xin["head"], yh, hr, hc, 1, F)
 
     bytes_tok = sum(v.numel() for v in layers[0].values()) * L + head.numel()
@@ -478,7 +475,7 @@ def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
            "workload": "7B shapes: 32 x (4 x 4096x4096, 2 x 11008x4096, 4096x11008) Q4_K + "
                        "32000x4096 Q8_0 head, batch 1"}
     for name, fn, launches in (("unfused", token_unfused, 32 * 11 + 2), ("fused", token_fused, 32 * 7 + 1),
-                               ("fused_weights", token_grouped, 32 * 5 + 1)):
+                               ("fused_weights", token_grouped, 32 * 4 + 1)):
         t, _ = time_graph(capture(fn), 40, 3)
         per_tok = t / 40
         res[name] = {"tok_s": world / per_tok, "ms_per_token": per_tok * 1e3,

@@ -60,6 +60,11 @@ constexpr unsigned FULL = 0xffffffffu;
 #ifndef GQ_GEMV_MIN_BLOCKS
 #define GQ_GEMV_MIN_BLOCKS 1
 #endif
+// Weight copies carry an evict-first L2 policy (the weights are streamed
+// once per pass; activations and outputs are what later launches reuse).
+#ifndef GQ_GEMV_W_EVICT_FIRST
+#define GQ_GEMV_W_EVICT_FIRST 1
+#endif
 #ifndef GQ_GEMV_PREFETCH
 #define GQ_GEMV_PREFETCH 1
 #endif
@@ -251,11 +256,56 @@ __device__ __forceinline__ float q8_code(float x, float d, float r) {
     return clamp127(q);
 }
 
+// Codes of eight elements of a block with scale d and r = RN(1/d), packed as
+// signed bytes (lowest element in the lowest byte), each equal to
+// q8_code(e[i], d, r), and zero when d == 0.  Away from a half-integer the
+// product p = RN(e * r) rounds the same to nearest-even (rintf) as half away
+// from zero, and |p - rintf(p)| is exact, so the fast path tests the same
+// 2^-14 window as q8_code and falls back to it for the whole group when any
+// element lies in the window (or r is not finite, which makes the test fail).
+// Every |e| <= 127 d up to the rounding of d (at most 2^-11 relative, for an
+// fp16 scale), so |p| < 127.5 and the fast codes need no clamp.
+__device__ __forceinline__ void q8_codes8(const float (&e)[8], float d, float r, uint32_t &w0,
+                                          uint32_t &w1) {
+    int q[8];
+    bool slow = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float p = __fmul_rn(e[i], r);
+        const float t = rintf(p);
+        slow |= !(fabsf(fabsf(p - t) - 0.5f) > 0x1p-14f);
+        q[i] = (int)t;
+    }
+    if (d == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+    } else if (slow) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = (int)q8_code(e[i], d, r);
+    }
+    w0 = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+    w1 = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+}
+
+__device__ __forceinline__ void unpack8(const float4 (&v)[2], float (&e)[8]) {
+    e[0] = v[0].x; e[1] = v[0].y; e[2] = v[0].z; e[3] = v[0].w;
+    e[4] = v[1].x; e[5] = v[1].y; e[6] = v[1].z; e[7] = v[1].w;
+}
+
+__device__ __forceinline__ float absmax8(const float (&e)[8]) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(e[i]));
+    return m;
+}
+
 // Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
 // (= code group l of the layout).
 // Each warp loads up to QS_BATCH of its blocks before quantizing any, so a
-// row of up to QS_BATCH * warps blocks costs one L2 round trip.
+// row of up to QS_BATCH * warps blocks costs one L2 round trip, and then
+// quantizes them two at a time with the two dependency chains interleaved.
 constexpr int QS_BATCH = 6;
+static_assert(QS_BATCH % 2 == 0, "blocks are quantized in pairs");
 
 __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int nblocks, int nsb) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -268,71 +318,109 @@ __device__ void quant_stage_q8_k(const Act &a, const float *__restrict__ x, int 
                 const float4 *p = reinterpret_cast<const float4 *>(x + (size_t)blk * QK_K + 8 * lane);
                 v[u][0] = __ldg(p);
                 v[u][1] = __ldg(p + 1);
+            } else {
+                v[u][0] = v[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             }
         }
 #pragma unroll
-        for (int u = 0; u < QS_BATCH; ++u) {
-            const int blk = b0 + u * nw;
-            if (blk >= nblocks) break;  // warp-uniform
-            const float e[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
-                                v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
-            float amax = 0.0f;
+        for (int u = 0; u < QS_BATCH; u += 2) {
+            if (b0 + u * nw >= nblocks) break;  // warp-uniform
+            float e[2][8], am[2], d[2], r[2];
+            uint32_t w0[2], w1[2];
+            int sum[2];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(e[i]));
-            amax = warp_max(amax);
-            const float d = __fdiv_rn(amax, 127.0f);
-            const float rcp = __frcp_rn(d);
-            uint32_t w0 = 0, w1 = 0;
-            int sum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float q = (d == 0.0f) ? 0.0f : q8_code(e[i], d, rcp);
-                const int qi = (int)q;
-                sum += qi;
-                if (i < 4)
-                    w0 |= (uint32_t)(qi & 0xff) << (8 * i);
-                else
-                    w1 |= (uint32_t)(qi & 0xff) << (8 * (i - 4));
+            for (int k = 0; k < 2; ++k) {
+                unpack8(v[u + k], e[k]);
+                am[k] = absmax8(e[k]);
             }
-            *reinterpret_cast<uint2 *>(a.codes + (size_t)blk * 256 + q8k_group_off(blk % nsb, lane)) =
-                split8(w0, w1);
-            sum += __shfl_xor_sync(FULL, sum, 1);
-            sum += __shfl_xor_sync(FULL, sum, 2);
-            if ((lane & 3) == 0) a.isum[blk * 8 + (lane >> 2)] = sum;
-            if (lane == 0) a.dx[blk] = d;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) am[k] = fmaxf(am[k], __shfl_xor_sync(FULL, am[k], o));
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                d[k] = __fdiv_rn(am[k], 127.0f);
+                r[k] = __frcp_rn(d[k]);
+                q8_codes8(e[k], d[k], r[k], w0[k], w1[k]);
+                sum[k] = dp4a((int)w0[k], 0x01010101, dp4a((int)w1[k], 0x01010101, 0));
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) sum[k] += __shfl_xor_sync(FULL, sum[k], o);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int blk = b0 + (u + k) * nw;
+                if (blk < nblocks) {
+                    *reinterpret_cast<uint2 *>(a.codes + (size_t)blk * 256 + q8k_group_off(blk % nsb, lane)) =
+                        split8(w0[k], w1[k]);
+                    if ((lane & 3) == 0) a.isum[blk * 8 + (lane >> 2)] = sum[k];
+                    if (lane == 0) a.dx[blk] = d[k];
+                }
+            }
         }
     }
 }
 
-// Q8_0: one warp per 32-element block, lane = element.
+// Q8_0: a warp pass covers eight consecutive 32-element blocks, four lanes
+// per block and eight elements per lane (two 16-byte loads, 1 KB per warp,
+// coalesced).  Passes are batched and quantized in interleaved pairs as for
+// Q8_K.
 template <bool SPLIT>
 __device__ void quant_stage_q8_0(const Act &a, const float *__restrict__ x, int nblocks) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // position of this lane's code in the staged block
-    const int e = lane & 7;
-    const int pos = SPLIT ? ((lane & ~7) | ((e & 1) ? 4 + (e >> 1) : (e >> 1))) : lane;
-    const int nw = blockDim.x >> 5;
-    for (int b0 = warp; b0 < nblocks; b0 += 8 * nw) {
-        float v[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int sub = lane & 3;  // eight-element group within the block
+    const int npass = (nblocks + 7) / 8;
+    for (int p0 = warp; p0 < npass; p0 += QS_BATCH * nw) {
+        float4 v[QS_BATCH][2];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int blk = b0 + u * nw;
-            v[u] = blk < nblocks ? __ldg(x + (size_t)blk * 32 + lane) : 0.0f;
+        for (int u = 0; u < QS_BATCH; ++u) {
+            const int blk = (p0 + u * nw) * 8 + (lane >> 2);
+            if (blk < nblocks) {
+                const float4 *p = reinterpret_cast<const float4 *>(x + (size_t)blk * 32 + 8 * sub);
+                v[u][0] = __ldg(p);
+                v[u][1] = __ldg(p + 1);
+            } else {
+                v[u][0] = v[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int blk = b0 + u * nw;
-            if (blk >= nblocks) break;  // warp-uniform
-            const float amax = warp_max(fabsf(v[u]));
-            const float d = __half2float(__float2half_rn(__fdiv_rn(amax, 127.0f)));
-            const float q = (d == 0.0f) ? 0.0f : q8_code(v[u], d, __frcp_rn(d));
-            int qi = (int)q;
-            a.codes[(size_t)blk * 32 + pos] = (uint8_t)(qi & 0xff);
+        for (int u = 0; u < QS_BATCH; u += 2) {
+            if (p0 + u * nw >= npass) break;  // warp-uniform
+            float e[2][8], am[2], d[2], r[2];
+            uint32_t w0[2], w1[2];
+            int sum[2];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) qi += __shfl_xor_sync(FULL, qi, o);
-            if (lane == 0) {
-                a.isum[blk] = qi;
-                a.dx[blk] = d;
+            for (int k = 0; k < 2; ++k) {
+                unpack8(v[u + k], e[k]);
+                am[k] = absmax8(e[k]);
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) am[k] = fmaxf(am[k], __shfl_xor_sync(FULL, am[k], o));
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                d[k] = __half2float(__float2half_rn(__fdiv_rn(am[k], 127.0f)));
+                r[k] = __frcp_rn(d[k]);
+                q8_codes8(e[k], d[k], r[k], w0[k], w1[k]);
+                sum[k] = dp4a((int)w0[k], 0x01010101, dp4a((int)w1[k], 0x01010101, 0));
+            }
+#pragma unroll
+            for (int o = 1; o <= 2; o <<= 1)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) sum[k] += __shfl_xor_sync(FULL, sum[k], o);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int blk = (p0 + (u + k) * nw) * 8 + (lane >> 2);
+                if (blk < nblocks) {
+                    *reinterpret_cast<uint2 *>(a.codes + (size_t)blk * 32 + 8 * sub) =
+                        SPLIT ? split8(w0[k], w1[k]) : make_uint2(w0[k], w1[k]);
+                    if (sub == 0) {
+                        a.isum[blk] = sum[k];
+                        a.dx[blk] = d[k];
+                    }
+                }
             }
         }
     }
@@ -685,6 +773,7 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * MAX_STAGE;
     uint8_t *ring = smem + bufs_off<NW>() + (size_t)warp * ns * geo.stage_bytes;
 
+    const uint64_t wpol = GQ_GEMV_W_EVICT_FIRST ? l2_evict_first_policy() : 0ull;
     // item i of this warp = row group wg + (i / ipg) * warps_total, whole or
     // its chunk i % ipg
     auto issue = [&](int i, int st) {
@@ -701,7 +790,10 @@ __global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const
             bytes = (uint32_t)(min(F::CH, nblk - c * F::CH) * F::BB);
         }
         mbar_arrive_expect_tx(bar + st, bytes);
-        bulk_g2s(ring + (size_t)st * geo.stage_bytes, src, bytes, bar + st);
+        if (GQ_GEMV_W_EVICT_FIRST)
+            bulk_g2s_hint(ring + (size_t)st * geo.stage_bytes, src, bytes, bar + st, wpol);
+        else
+            bulk_g2s(ring + (size_t)st * geo.stage_bytes, src, bytes, bar + st);
     };
 
     // With the early trigger the next kernel in the stream may launch right

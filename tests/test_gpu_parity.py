@@ -285,6 +285,18 @@ def test_fused_f32_matches_unfused_and_oracle(wtype, rows, cols, batch):
     assert_close(y_f, y_ref, T)
 
 
+# 32-element formats: the fused quantizer takes eight blocks per warp pass,
+# six passes per batch, two at a time; these pass counts (1, 9, 49, 51) leave
+# a batch, or the second pass of a pair, empty
+RAGGED_FUSED_SHAPES = [(2, 256, 3), (5, 2304, 2), (3, 12544, 1), (4, 13056, 9)]
+
+
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0])
+@pytest.mark.parametrize("rows,cols,batch", RAGGED_FUSED_SHAPES)
+def test_fused_f32_ragged_blocks(wtype, rows, cols, batch):
+    test_fused_f32_matches_unfused_and_oracle(wtype, rows, cols, batch)
+
+
 def tie_heavy_activations(cols, blk, seed):
     """fp32 rows whose codes sit on or next to rounding ties: per block the
     scale is either a power of two (ties exact) or arbitrary (quotients a few
@@ -310,7 +322,11 @@ def tie_heavy_activations(cols, blk, seed):
 def test_fused_quantize_ties_match_oracle(wtype):
     """Identity weights make each block sum expose single activation codes,
     so the in-kernel quantizer is checked code by code on tie cases."""
-    cols = 1024
+    for cols in ((1024,) if wtype == Q4_K else (1024, 2304)):
+        check_fused_ties(wtype, cols)
+
+
+def check_fused_ties(wtype, cols):
     blk = 256 if wtype == Q4_K else 32
     X = np.stack([tie_heavy_activations(cols, blk, 40 + i) for i in range(2)])
     Wq = orc.quantize(wtype, np.eye(cols, dtype=np.float32))
