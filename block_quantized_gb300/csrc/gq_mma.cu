@@ -18,7 +18,7 @@
 // both exact integers:
 //   y[b][r] += dx(b) * (d(r) * S1 - dmin(r) * S2)      (fp32, in registers)
 //
-// CTA tile: 128 weight rows x 128 batch columns, one super-block (K = 256) per
+// CTA tile: 128 weight rows x TN batch columns, one super-block (K = 256) per
 // step, 28 warps:
 //   warps 0, 3 activation producers: one bulk copy each per super-block of
 //              the packed unit's half 0 (B stages 0-1) or half 1 (stages 2-3
@@ -34,11 +34,13 @@
 //              reads the A operand; then the row scales and min-term row
 //              (first half) or the column scales (second half);
 //   warps 12-27 epilogue: four threads per row, 32 columns each.
-// Tensor memory (512 columns): the S1 accumulator and the A operand, each
-// double-buffered by super-block (4 x 128 columns).  The min-term step writes
-// S2 over the A buffer its super-block has just consumed, so the builders run
-// a super-block ahead of the MMAs and the MMAs a super-block ahead of the
-// epilogue.
+// Tensor memory (512 columns): the S1 accumulator, double-buffered by
+// super-block, and two or three buffers of the A operand.  The min-term step
+// writes S2 over the A buffer its super-block has just consumed, so the
+// builders run one or two super-blocks ahead of the MMAs and the MMAs a
+// super-block ahead of the epilogue.
+// The tile width TN (32, 64 or 128 batch columns) is chosen per call: the
+// narrowest that covers the batch, 128 beyond 64.
 // The activation operand is packed once per call by pack_kernel into a
 // caller-provided workspace, already in the swizzled shared-memory image, so
 // each operand tile is a single 1-D bulk copy.
@@ -58,69 +60,25 @@ namespace gq {
 namespace {
 
 constexpr int TM = 128;   // weight rows per tile (MMA M)
-constexpr int TN = 128;   // batch columns per tile (MMA N)
 constexpr int KS = 64;    // K per B operand stage (one 128-byte swizzle atom)
 constexpr int NKS = 4;    // B operand stages per super-block
-constexpr int NBS = 4;    // B ring slots: two halves per super-block, two super-blocks
-constexpr int NRAW = 3;   // raw weight stages (two super-blocks of lookahead)
 constexpr int KMIN = 16;  // min-term K per super-block (8 mins, two halves of t)
 constexpr int NSM = 4;    // ring depth of the per-super-block scales and min-term A rows
-
-// Workspace (packed activations) per (column tile, super-block): the four B
-// stage images, the min-term B tile and the column scales, contiguous.
-constexpr int OP_B = TN * KS * 2;                 // 16 KB
-constexpr int MIN_A = TM * KMIN * 2;              // 4 KB
-constexpr int MIN_B = TN * KMIN * 2;              // 4 KB
-constexpr size_t WS_B = (size_t)NKS * OP_B;       // 64 KB
-constexpr size_t WS_MIN = MIN_B;
-constexpr size_t WS_DX = TN * 4;                  // 512 B
-constexpr size_t WS_UNIT = WS_B + WS_MIN + WS_DX;
-
-// Each unit arrives as two bulk copies, issued by two producer warps (a warp
-// completes about one bulk copy per half microsecond however large, so one
-// copy per warp per super-block keeps the copies off the critical path):
-// half 0 = stages 0-1; half 1 = stages 2-3 and the min-term B tile.  The
-// column scales are fetched by builder threads with plain loads.
-constexpr int HALF0_BYTES = 2 * OP_B;                          // 32 KB
-constexpr int HALF1_BYTES = 2 * OP_B + MIN_B;                  // 36 KB
-constexpr int SLOT_B = (HALF1_BYTES + 1023) / 1024 * 1024;     // ring slot stride
-constexpr int SLOT_MIN = 2 * OP_B;                             // inside a half-1 slot
-constexpr int RAW_STAGE = TM * Q4_K_BYTES;                     // 18 KB
-// per super-block scales: d and dmin per row, dx per column (all fp32)
-constexpr int META_D = 0, META_DMIN = TM * 4, META_DX = 2 * TM * 4;
-constexpr int META_STAGE = 2 * TM * 4 + TN * 4;
-
-// Shared-memory layout (bytes from a 1024-aligned base).  The A operand
-// lives in tensor memory, not here.
-constexpr int OFF_B = 0;                                  // NBS x SLOT_B
-constexpr int OFF_MINA = OFF_B + NBS * SLOT_B;            // NSM x 4 KB min-term A rows
-constexpr int OFF_RAW = OFF_MINA + NSM * MIN_A;           // NRAW x 18 KB
-constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;      // NSM x 1.5 KB scales
-constexpr int OFF_BAR = OFF_META + NSM * META_STAGE;
-// A: full (builders), empty (epilogue); B: full-tx (producers), empty; min:
-// full (builders), empty; raw: full, empty; meta: full (builders), empty;
-// acc: full, empty; final.
-constexpr int NBARS = 2 * 2 + 2 * NBS + 2 * NSM + 2 * NRAW + 2 * NSM + 2 * 2 + 1;
-constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
-static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-static_assert(SLOT_B % 1024 == 0 && OP_B % 1024 == 0, "SW128 tiles need 1024-byte alignment");
-static_assert(OFF_RAW % 128 == 0 && RAW_STAGE % 128 == 0, "tiled TMA destinations are 128-byte aligned");
-static_assert(WS_UNIT % 16 == 0 && HALF1_BYTES % 16 == 0 && SLOT_MIN % 16 == 0, "bulk copies move 16-byte units");
-
-// Tensor-memory columns: the S1 accumulator double-buffered by super-block
-// parity (2 x 128), and the A operand (one super-block, 256 K as fp16 pairs =
-// 128 columns) double-buffered the same way.  Once the sixteen S1 steps of a
-// super-block have read its A buffer, the min-term step writes S2 over it
-// (the tensor core executes one thread's MMAs in issue order), and the
-// epilogue frees the buffer for the builders when it has read S2.
-constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t col_s1(int p) { return 128u * (uint32_t)p; }
-__host__ __device__ constexpr uint32_t col_a(int p) { return 256u + 128u * (uint32_t)p; }
-
+constexpr int MIN_A = TM * KMIN * 2;           // 4 KB min-term A rows
+constexpr int RAW_STAGE = TM * Q4_K_BYTES;     // 18 KB raw weight rows
 constexpr int NTHREADS = 896;
 constexpr int EPI_WARP0 = 12, EPI_WARPS = 16, BLD_WARP0 = 4, BLD_THREADS = 256;
+
+// Tensor memory (512 columns): the S1 accumulator double-buffered by
+// super-block parity (2 x TN columns from 0), and NA buffers of the A operand
+// (one super-block, 256 K as fp16 pairs = 128 columns each) from column
+// COL_A0, used in turn.  Once the sixteen S1 steps of a super-block have read
+// its A buffer, the min-term step writes S2 over it (the tensor core executes
+// one thread's MMAs in issue order), and the epilogue frees the buffer for
+// the builders when it has read S2.  Tiles of up to 64 columns leave room for
+// a third A buffer, so the builders may run two super-blocks ahead of the
+// MMAs.
+constexpr uint32_t TMEM_COLS = 512;
 
 // ------------------------------------------------------------ tcgen05 helpers
 
@@ -144,6 +102,72 @@ __device__ __forceinline__ uint64_t desc_plain(uint32_t saddr, uint32_t lbo, uin
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, uint32_t fmt) {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
+
+// Tile-width configuration.  A CTA computes TM weight rows x TN batch
+// columns (MMA N = TN).  Per (column tile, super-block) the workspace holds
+// one unit: the four B stage images (TN x 64 K fp16, 128-byte swizzled), the
+// min-term B tile and the column scales, contiguous.  Each unit arrives as
+// two bulk copies, issued by two producer warps (a warp completes about one
+// bulk copy per half microsecond however large, so one copy per warp per
+// super-block keeps the copies off the critical path): half 0 = stages 0-1;
+// half 1 = stages 2-3 and the min-term B tile.  The column scales are fetched
+// by builder threads with plain loads.  Narrow tiles (small batches) move
+// little activation data per super-block, so their period is set by the
+// weight rows; they get deeper activation (NBSB super-blocks) and weight
+// (NRAW) rings to cover the copy latency.
+template <int TN_>
+struct Cfg {
+    static constexpr int TN = TN_;
+    static constexpr int NBSB = TN_ == 32 ? 4 : (TN_ == 64 ? 3 : 2);
+    static constexpr int NBS = 2 * NBSB;   // B ring slots: two halves per super-block
+    static constexpr int NRAW = TN_ == 32 ? 6 : (TN_ == 64 ? 4 : 3);
+    // tensor memory: S1 buffers at 0 and TN, A buffers from COL_A0
+    static constexpr int NA = TN_ <= 64 ? 3 : 2;
+    static constexpr uint32_t COL_A0 = TN_ <= 64 ? 128u : 256u;
+    static constexpr int OP_B = TN * KS * 2;                       // one B stage
+    static constexpr int MIN_B = TN * KMIN * 2;
+    static constexpr size_t WS_B = (size_t)NKS * OP_B;
+    static constexpr size_t WS_MIN = MIN_B;
+    static constexpr size_t WS_DX = TN * 4;
+    static constexpr size_t WS_UNIT = WS_B + WS_MIN + WS_DX;
+    static constexpr int HALF0_BYTES = 2 * OP_B;
+    static constexpr int HALF1_BYTES = 2 * OP_B + MIN_B;
+    static constexpr int SLOT_B = (HALF1_BYTES + 1023) / 1024 * 1024;  // ring slot stride
+    static constexpr int SLOT_MIN = 2 * OP_B;                          // inside a half-1 slot
+    // per super-block scales: d and dmin per row, dx per column (all fp32)
+    static constexpr int META_D = 0, META_DMIN = TM * 4, META_DX = 2 * TM * 4;
+    static constexpr int META_STAGE = 2 * TM * 4 + TN * 4;
+    // Shared-memory layout (bytes from a 1024-aligned base).  The A operand
+    // lives in tensor memory, not here.
+    static constexpr int OFF_B = 0;                               // NBS x SLOT_B
+    static constexpr int OFF_MINA = OFF_B + NBS * SLOT_B;         // NSM x 4 KB min-term A rows
+    static constexpr int OFF_RAW = OFF_MINA + NSM * MIN_A;        // NRAW x 18 KB
+    static constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;   // NSM scale stages
+    static constexpr int OFF_BAR = OFF_META + NSM * META_STAGE;
+    // A: full (builders), empty (epilogue); B: full-tx (producers), empty;
+    // min: full (builders), empty; raw: full, empty; meta: full (builders),
+    // empty; acc: full, empty; final.
+    static constexpr int NBARS = 2 * NA + 2 * NBS + 2 * NSM + 2 * NRAW + 2 * NSM + 2 * 2 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
+    // epilogue warps that own columns (four per 32 columns)
+    static constexpr int EPI_ACTIVE = 4 * (TN / 32);
+    static_assert(COL_A0 + 128u * NA <= TMEM_COLS && 2 * TN <= (int)COL_A0, "tensor-memory columns");
+    __host__ __device__ static constexpr uint32_t col_s1(int p) { return (uint32_t)(TN * p); }
+    __host__ __device__ static constexpr uint32_t col_a(int i) { return COL_A0 + 128u * (uint32_t)i; }
+    static constexpr uint32_t IDESC = idesc_f16(TM, TN, 0);
+    static_assert(TN == 32 || TN == 64 || TN == 128, "tile widths");
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(SLOT_B % 1024 == 0 && OP_B % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+    static_assert(OFF_RAW % 128 == 0 && RAW_STAGE % 128 == 0, "tiled TMA destinations are 128-byte aligned");
+    static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+    static_assert(WS_UNIT % 16 == 0 && HALF0_BYTES % 16 == 0 && HALF1_BYTES % 16 == 0 && SLOT_MIN % 16 == 0,
+                  "bulk copies move 16-byte units");
+};
+
+// Tile width for a batch: the narrowest tile that covers it, 128 beyond 64.
+inline int pick_tn(int64_t batch) { return batch <= 32 ? 32 : (batch <= 64 ? 64 : 128); }
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -280,11 +304,13 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // split exactly as t_lo = t mod 64 (K position j) and t_hi = floor(t / 64)
 // (K position 8 + j) of the min-term tile, and lane 0 the column scale dx.
 // Columns past the batch are zero.
+template <int TN>
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ xq,
                                                    uint8_t *__restrict__ ws, int nsb, int batch) {
+    using C = Cfg<TN>;
     const int sb = blockIdx.x, ct = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *unit = ws + ((size_t)ct * nsb + sb) * WS_UNIT;
+    uint8_t *unit = ws + ((size_t)ct * nsb + sb) * C::WS_UNIT;
     pdl_launch_dependents();
     pdl_wait();
     for (int c = warp; c < TN; c += 8) {
@@ -304,25 +330,23 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
         }
         const uint4 chunk = make_uint4(pack_h2(a[0], a[4]), pack_h2(a[1], a[5]), pack_h2(a[2], a[6]),
                                        pack_h2(a[3], a[7]));
-        *reinterpret_cast<uint4 *>(unit + (lane >> 3) * OP_B + sw128_off(c, lane & 7)) = chunk;
+        *reinterpret_cast<uint4 *>(unit + (lane >> 3) * C::OP_B + sw128_off(c, lane & 7)) = chunk;
         if (lane < 8) {
             int t = 0;
             if (valid) t = __ldg(reinterpret_cast<const int16_t *>(src + 260) + lane);
             const int thi = t >> 6;          // floor(t / 64), in [-64, 63]
             const int tlo = t - 64 * thi;    // in [0, 63]
-            uint8_t *mb = unit + WS_B;
+            uint8_t *mb = unit + C::WS_B;
             *reinterpret_cast<__half *>(mb + plain_off(c, 0) + 2 * lane) = __int2half_rn(tlo);
             *reinterpret_cast<__half *>(mb + plain_off(c, 1) + 2 * lane) = __int2half_rn(thi);
         }
         if (lane == 0)
-            reinterpret_cast<float *>(unit + WS_B + WS_MIN)[c] =
+            reinterpret_cast<float *>(unit + C::WS_B + C::WS_MIN)[c] =
                 valid ? __ldg(reinterpret_cast<const float *>(src)) : 0.0f;
     }
 }
 
 // ------------------------------------------------------------- main kernel
-
-constexpr uint32_t IDESC_F16 = idesc_f16(TM, TN, 0);
 
 // Barriers whose only arrival is a transfer's transaction count (b_tx,
 // raw_full) tell the consumer that a copy has landed; the builders arrive on
@@ -332,18 +356,19 @@ struct Bars {
     uint64_t *meta_full, *meta_empty, *acc_full, *acc_empty, *fin;
 };
 
+template <class C>
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
-    uint64_t *b = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+    uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     Bars r;
     r.a_full = b;
-    r.a_empty = r.a_full + 2;
-    r.b_tx = r.a_empty + 2;
-    r.b_empty = r.b_tx + NBS;
-    r.min_full = r.b_empty + NBS;
+    r.a_empty = r.a_full + C::NA;
+    r.b_tx = r.a_empty + C::NA;
+    r.b_empty = r.b_tx + C::NBS;
+    r.min_full = r.b_empty + C::NBS;
     r.min_empty = r.min_full + NSM;
     r.raw_full = r.min_empty + NSM;
-    r.raw_empty = r.raw_full + NRAW;
-    r.meta_full = r.raw_empty + NRAW;
+    r.raw_empty = r.raw_full + C::NRAW;
+    r.meta_full = r.raw_empty + C::NRAW;
     r.meta_empty = r.meta_full + NSM;
     r.acc_full = r.meta_empty + NSM;
     r.acc_empty = r.acc_full + 2;
@@ -351,44 +376,51 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     return r;
 }
 
-// B ring slot of half h of super-block step sb; it is reused every second
-// step, so its parity is that of sb / 2.
-__device__ __forceinline__ int b_slot(int sb, int h) { return 2 * (sb & 1) + h; }
+// B ring slot of half h of super-block step sb; it is reused every NBSB-th
+// step, so the parity of its current use is that of sb / NBSB.
+template <class C>
+__device__ __forceinline__ int b_slot(int sb, int h) { return 2 * (sb % C::NBSB) + h; }
+template <class C>
+__device__ __forceinline__ uint32_t b_phase(int sb) { return (uint32_t)(sb / C::NBSB) & 1u; }
 
 // Producer of half h of the activation units (warps 0 and 3): one bulk copy
 // per super-block into the B ring.  On abort it waits (bounded) for every
 // copy it started before the CTA may exit.
+template <class C>
 __device__ void role_producer_b(uint8_t *smem, const Bars &B, const uint8_t *__restrict__ ws, int nsb,
                                 int ct, int rot, int h, volatile uint32_t *abort) {
     const int lane = threadIdx.x & 31;
-    const uint32_t bytes = h ? (uint32_t)HALF1_BYTES : (uint32_t)HALF0_BYTES;
-    int last[2] = {-1, -1};
+    const uint32_t bytes = h ? (uint32_t)C::HALF1_BYTES : (uint32_t)C::HALF0_BYTES;
+    int last[C::NBSB];
+    for (int i = 0; i < C::NBSB; ++i) last[i] = -1;
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
-        const int s = b_slot(sb, h);
-        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
+        const int s = b_slot<C>(sb, h);
+        const uint32_t ph = b_phase<C>(sb);
         if (!(ok = wait_warp(B.b_empty + s, ph ^ 1u, abort))) break;
         if (lane == 0) {
-            const uint8_t *src = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * WS_UNIT + (h ? HALF0_BYTES : 0);
+            const uint8_t *src =
+                ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * C::WS_UNIT + (h ? C::HALF0_BYTES : 0);
             mbar_arrive_expect_tx(B.b_tx + s, bytes);
-            bulk_g2s(smem + OFF_B + s * SLOT_B, src, bytes, B.b_tx + s);
+            bulk_g2s(smem + C::OFF_B + s * C::SLOT_B, src, bytes, B.b_tx + s);
         }
-        last[sb & 1] = (int)ph;
+        last[sb % C::NBSB] = (int)ph;
     }
     if (!ok)
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < C::NBSB; ++i)
             if (last[i] >= 0) mbar_wait_bounded(B.b_tx + 2 * i + h, (uint32_t)last[i]);
 }
 
 // Producer of the raw weight rows (warp 2): one 2-D tiled TMA load per
 // super-block (box 144 bytes x 128 rows; rows past the matrix read as
 // zeros), NRAW - 1 super-blocks ahead of the builders.
+template <class C>
 __device__ void role_producer_w(uint8_t *smem, const Bars &B, const CUtensorMap *tmap_w, int row0, int nsb,
                                 int rot, volatile uint32_t *abort) {
     const int lane = threadIdx.x & 31;
-    int raw_last[NRAW];
-    for (int i = 0; i < NRAW; ++i) raw_last[i] = -1;
-    RingPos rr(NRAW);
+    int raw_last[C::NRAW];
+    for (int i = 0; i < C::NRAW; ++i) raw_last[i] = -1;
+    RingPos rr(C::NRAW);
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
         if (!(ok = wait_warp(B.raw_empty + rr.idx, rr.phase ^ 1u, abort))) break;
@@ -396,7 +428,7 @@ __device__ void role_producer_w(uint8_t *smem, const Bars &B, const CUtensorMap 
             mbar_arrive_expect_tx(B.raw_full + rr.idx, RAW_STAGE);
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + OFF_RAW + rr.idx * RAW_STAGE)),
+                " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + C::OFF_RAW + rr.idx * RAW_STAGE)),
                 "l"(reinterpret_cast<uint64_t>(tmap_w)), "r"(kslot(sb, rot, nsb) * Q4_K_BYTES), "r"(row0),
                 "r"(smem_u32(B.raw_full + rr.idx))
                 : "memory");
@@ -406,7 +438,7 @@ __device__ void role_producer_w(uint8_t *smem, const Bars &B, const CUtensorMap 
         rr.next();
     }
     if (!ok)
-        for (int i = 0; i < NRAW; ++i)
+        for (int i = 0; i < C::NRAW; ++i)
             if (raw_last[i] >= 0) mbar_wait_bounded(B.raw_full + i, (uint32_t)raw_last[i]);
 }
 
@@ -437,25 +469,26 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
 // sub-block is 16 columns, written by one tcgen05.st from registers; the
 // buffer is free again once the epilogue has read the S2 written over it.
 // Then the hh = 0 threads write row t's scales d, dmin and its min-term A row,
-// the hh = 1 threads column t's scale (read from the workspace, requested
-// before the raw weights are waited for).
+// the hh = 1 threads (t < TN) column t's scale (read from the workspace,
+// requested before the raw weights are waited for).
+template <class C>
 __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const uint8_t *__restrict__ ws,
                              int ct, int rot, int nvalid, int nsb, volatile uint32_t *abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = 32 * (warp & 3) + lane, hh = (warp - BLD_WARP0) >> 2;
     const bool valid = t < nvalid;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    RingPos rr(NRAW), mr(NSM);
+    RingPos rr(C::NRAW), mr(NSM);
     for (int sb = 0; sb < nsb; ++sb) {
-        const int p = sb & 1;
-        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
+        const int ai = sb % C::NA;                              // A buffer
+        const uint32_t aph = (uint32_t)(sb / C::NA) & 1u;       // parity of its use
         float dx = 0.0f;
-        if (hh == 1) {
-            const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * WS_UNIT;
-            dx = __ldg(reinterpret_cast<const float *>(unit + WS_B + WS_MIN) + t);
+        if (hh == 1 && t < C::TN) {
+            const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * C::WS_UNIT;
+            dx = __ldg(reinterpret_cast<const float *>(unit + C::WS_B + C::WS_MIN) + t);
         }
         if (!wait_warp(B.raw_full + rr.idx, rr.phase, abort)) return;
-        const uint8_t *raw = smem + OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
+        const uint8_t *raw = smem + C::OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
         uint4 h = make_uint4(0, 0, 0, 0), q[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) q[j] = make_uint4(0, 0, 0, 0);
@@ -468,7 +501,7 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         rr.next();
 
         // this half of the A operand: sc_j * q for sub-blocks 4hh .. 4hh + 3
-        if (!wait_warp(B.a_empty + p, ph ^ 1u, abort)) return;
+        if (!wait_warp(B.a_empty + ai, aph ^ 1u, abort)) return;
         tc_fence_after();
         const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
 #pragma unroll
@@ -481,22 +514,22 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
             v[1] = nibbles_to_f16(q[j].y, s1, c1, s16, c16);
             v[2] = nibbles_to_f16(q[j].z, s1, c1, s16, c16);
             v[3] = nibbles_to_f16(q[j].w, s1, c1, s16, c16);
-            tmem_st16(lane_base + col_a(p) + 64u * hh + 16u * j, v);
+            tmem_st16(lane_base + C::col_a(ai) + 64u * hh + 16u * j, v);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.a_full + p);
+        if (lane == 0) mbar_arrive(B.a_full + ai);
 
         // then (off the MMA's critical path) the epilogue's scales and, for
         // hh = 0, the min-term A row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
         if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-        uint8_t *meta = smem + OFF_META + mr.idx * META_STAGE;
+        uint8_t *meta = smem + C::OFF_META + mr.idx * C::META_STAGE;
         if (hh == 0) {
-            reinterpret_cast<float *>(meta + META_D)[t] = half_bits_to_float(h.x);
-            reinterpret_cast<float *>(meta + META_DMIN)[t] = half_bits_to_float(h.x >> 16);
-        } else {
-            reinterpret_cast<float *>(meta + META_DX)[t] = dx;
+            reinterpret_cast<float *>(meta + C::META_D)[t] = half_bits_to_float(h.x);
+            reinterpret_cast<float *>(meta + C::META_DMIN)[t] = half_bits_to_float(h.x >> 16);
+        } else if (t < C::TN) {
+            reinterpret_cast<float *>(meta + C::META_DX)[t] = dx;
         }
         mbar_arrive(B.meta_full + mr.idx);
         if (hh == 0) {
@@ -510,7 +543,7 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
                 hi[j >> 1] = pack_h2(64.0f * m0, 64.0f * m1);
             }
             if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-            uint8_t *ma = smem + OFF_MINA + mr.idx * MIN_A;
+            uint8_t *ma = smem + C::OFF_MINA + mr.idx * MIN_A;
             *reinterpret_cast<uint4 *>(ma + plain_off(t, 0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             *reinterpret_cast<uint4 *>(ma + plain_off(t, 1)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             fence_async_smem();
@@ -521,44 +554,78 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
     }
 }
 
+// Eight K=16 steps into accumulator d, the A operand of step i at tensor
+// memory column a[i] and its B operand at descriptor b[i], in one asm block
+// whose operands are all computed beforehand.  Issued back to back this way
+// one thread feeds the tensor core about one M=128 step per 60 clocks; with
+// each step's addresses and predicate formed just before it, about one per
+// 100-150.  Only the first step may start a fresh accumulation
+// (accumulate == 0).
+__device__ __forceinline__ void mma8_ta(uint32_t d, const uint32_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, t;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.eq.b32 t, %18, %18;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, t;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, t;\n\t}" ::"r"(d),
+        "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc),
+        "r"(accumulate)
+        : "memory");
+}
+
+
 // MMA issuer (warp 1, one thread).  Per super-block: sixteen K=16 steps of
-// the S1 product (A from the tensor-memory buffer of the super-block's
-// parity, B from the two halves of the unit in the ring) into the S1 buffer of
-// the same parity, then one K=16 step of the min-term product S2 (A rows from
-// the builders, B tile from half 1) written over the consumed A buffer.
-// Always ends with a commit to `fin` so the teardown can wait for every MMA
-// to finish.
+// the S1 product (A from the tensor-memory buffer of the super-block, B from
+// the two halves of the unit in the ring) into the S1 buffer of its parity,
+// eight per half in one asm block, then one K=16 step of the min-term product
+// S2 (A rows from the builders, B tile from half 1) written over the consumed
+// A buffer.  Always ends with a commit to `fin` so the teardown can wait for
+// every MMA to finish.
+template <class C>
 __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, volatile uint32_t *abort) {
-    RingPos mr(NSM);
+    constexpr uint64_t OPB16 = C::OP_B >> 4;  // one B stage in descriptor address units
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
-        const int p = sb & 1;
+        const int p = sb & 1;                                   // S1 buffer
         const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
-        if (!(ok = wait_or_abort(B.a_full + p, ph, abort))) break;
+        const int ai = sb % C::NA;                              // A buffer
+        const uint32_t aph = (uint32_t)(sb / C::NA) & 1u;
+        const int mi = sb % NSM;
+        const uint32_t mph = (uint32_t)(sb / NSM) & 1u;
+        if (!(ok = wait_or_abort(B.a_full + ai, aph, abort))) break;
         if (!(ok = wait_or_abort(B.acc_empty + p, ph ^ 1u, abort))) break;
         for (int h = 0; h < 2; ++h) {
-            const int sl = b_slot(sb, h);
-            if (!(ok = wait_or_abort(B.b_tx + sl, ph, abort))) break;
+            const int sl = b_slot<C>(sb, h);
+            if (!(ok = wait_or_abort(B.b_tx + sl, b_phase<C>(sb), abort))) break;
             tc_fence_after();
-            const uint32_t base = smem_u32(smem + OFF_B + sl * SLOT_B);
+            const uint64_t b0 = desc_sw128(smem_u32(smem + C::OFF_B + sl * C::SLOT_B));
+            const uint32_t a0 = tmem + C::col_a(ai) + 64u * h;
+            uint32_t av[8];
+            uint64_t bv[8];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-#pragma unroll
-                for (int kk = 0; kk < KS / 16; ++kk)
-                    mma_f16_ta(tmem + col_s1(p), tmem + col_a(p) + 64u * h + 32u * q + 8u * kk,
-                               desc_sw128(base + q * OP_B + 32 * kk), IDESC_F16, (h | q | kk) != 0);
+            for (int i = 0; i < 8; ++i) {  // stage i / 4 of the half, K step i % 4
+                av[i] = a0 + 32u * (i >> 2) + 8u * (i & 3);
+                bv[i] = b0 + OPB16 * (uint64_t)(i >> 2) + 2u * (uint64_t)(i & 3);
             }
+            mma8_ta(tmem + C::col_s1(p), av, bv, C::IDESC, (uint32_t)h);
             if (h == 0) mma_commit(B.b_empty + sl);  // half 0 is free once these MMAs complete
         }
         if (!ok) break;
-        if (!(ok = wait_or_abort(B.min_full + mr.idx, mr.phase, abort))) break;
+        if (!(ok = wait_or_abort(B.min_full + mi, mph, abort))) break;
         tc_fence_after();
-        const uint32_t a2 = smem_u32(smem + OFF_MINA + mr.idx * MIN_A);
-        const uint32_t b2 = smem_u32(smem + OFF_B + b_slot(sb, 1) * SLOT_B + SLOT_MIN);
-        mma_f16(tmem + col_a(p), desc_plain(a2, 128, 256), desc_plain(b2, 128, 256), IDESC_F16, 0u);
-        mma_commit(B.min_empty + mr.idx);
-        mr.next();
-        mma_commit(B.b_empty + b_slot(sb, 1));
+        const uint32_t a2 = smem_u32(smem + C::OFF_MINA + mi * MIN_A);
+        const uint32_t b2 = smem_u32(smem + C::OFF_B + b_slot<C>(sb, 1) * C::SLOT_B + C::SLOT_MIN);
+        mma_f16(tmem + C::col_a(ai), desc_plain(a2, 128, 256), desc_plain(b2, 128, 256), C::IDESC, 0u);
+        mma_commit(B.min_empty + mi);
+        mma_commit(B.b_empty + b_slot<C>(sb, 1));
         mma_commit(B.acc_full + p);  // S1 and S2 of this super-block are ready
     }
     mma_commit(B.fin);
@@ -568,13 +635,16 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
 // (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4, of S1 and of the
 // S2 written over the A buffer.  It frees both as soon as they are in
 // registers and promotes them while the tensor core runs the next
-// super-block.
-template <bool SUMS>
+// super-block.  Warps whose columns lie past TN have nothing to do (the
+// barriers count EPI_ACTIVE warps).
+template <class C, bool SUMS>
 __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int row0, int rows, int ct,
                               int nsb, int rot, int batch, float *__restrict__ y,
                               int32_t *__restrict__ sums, volatile uint32_t *abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int lq = warp & 3, h = (warp - EPI_WARP0) >> 2;
+    if (32 * h >= C::TN) return;
+    constexpr int TN = C::TN;
     const int r = lq * 32 + lane;
     const int row = row0 + r;
     const uint32_t lane_addr = tmem + ((uint32_t)(lq * 32) << 16) + (uint32_t)(32 * h);
@@ -585,26 +655,27 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
     for (int sb = 0; sb < nsb; ++sb) {
         const int p = sb & 1;
         const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
+        const int ai = sb % C::NA;
         const int mi = sb % NSM;
         const uint32_t mph = (uint32_t)(sb / NSM) & 1u;
         if (!(ok = wait_warp(B.meta_full + mi, mph, abort))) break;
         if (!(ok = wait_warp(B.acc_full + p, ph, abort))) break;
         tc_fence_after();
-        const uint8_t *meta = smem + OFF_META + mi * META_STAGE;
-        const float d = reinterpret_cast<const float *>(meta + META_D)[r];
-        const float dmin = reinterpret_cast<const float *>(meta + META_DMIN)[r];
-        const float *dx = reinterpret_cast<const float *>(meta + META_DX) + 32 * h;
+        const uint8_t *meta = smem + C::OFF_META + mi * C::META_STAGE;
+        const float d = reinterpret_cast<const float *>(meta + C::META_D)[r];
+        const float dmin = reinterpret_cast<const float *>(meta + C::META_DMIN)[r];
+        const float *dx = reinterpret_cast<const float *>(meta + C::META_DX) + 32 * h;
 #pragma unroll
         for (int c0 = 0; c0 < 32; c0 += 16) {
             float s1[16], s2[16];
-            tmem_ld16x2(lane_addr + col_s1(p) + c0, lane_addr + col_a(p) + c0, s1, s2);
+            tmem_ld16x2(lane_addr + C::col_s1(p) + c0, lane_addr + C::col_a(ai) + c0, s1, s2);
             if (c0 == 16) {
                 // both halves are in registers: S1 and the A buffer may be reused
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(B.acc_empty + p);
-                    mbar_arrive(B.a_empty + p);
+                    mbar_arrive(B.a_empty + ai);
                 }
             }
             if (SUMS) {
@@ -636,7 +707,7 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
     }
 }
 
-template <bool SUMS>
+template <int TN, bool SUMS>
 __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                                               const uint8_t *__restrict__ ws,
                                                               const uint8_t *__restrict__ xq,
@@ -644,11 +715,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
                                                               int32_t *__restrict__ sums, int rows,
                                                               int nsb, int batch,
                                                               uint32_t *__restrict__ status) {
+    using C = Cfg<TN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const Bars B = bars_at(smem);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-    volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC + 4);
+    const Bars B = bars_at<C>(smem);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile uint32_t *abort = reinterpret_cast<volatile uint32_t *>(smem + C::OFF_MISC + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // column tiles vary fastest, so the CTAs that read the same weight rows
     // run together and share them through L2
@@ -657,23 +729,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     const int nvalid = min(TM, rows - row0);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NA; ++i) {
             mbar_init(B.a_full + i, BLD_THREADS / 32);  // one arrival per builder warp
-            mbar_init(B.a_empty + i, EPI_WARPS);        // the epilogue has read the S2 over it
-            mbar_init(B.acc_full + i, 1);
-            mbar_init(B.acc_empty + i, EPI_WARPS);
+            mbar_init(B.a_empty + i, C::EPI_ACTIVE);    // the epilogue has read the S2 over it
         }
-        for (int i = 0; i < NBS; ++i) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(B.acc_full + i, 1);
+            mbar_init(B.acc_empty + i, C::EPI_ACTIVE);
+        }
+        for (int i = 0; i < C::NBS; ++i) {
             mbar_init(B.b_tx + i, 1);
             mbar_init(B.b_empty + i, 1);
         }
-        for (int i = 0; i < NRAW; ++i) {
+        for (int i = 0; i < C::NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
             mbar_init(B.raw_empty + i, BLD_THREADS);
         }
         for (int i = 0; i < NSM; ++i) {
             mbar_init(B.meta_full + i, BLD_THREADS);  // every builder thread writes one entry
-            mbar_init(B.meta_empty + i, EPI_WARPS);
+            mbar_init(B.meta_empty + i, C::EPI_ACTIVE);
             mbar_init(B.min_full + i, 4);             // the four hh = 0 builder warps
             mbar_init(B.min_empty + i, 1);
         }
@@ -694,16 +768,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     pdl_wait();  // the packed activations come from the preceding kernel
 
     if (warp == 0 || warp == 3) {
-        role_producer_b(smem, B, ws, nsb, ct, rot, warp == 3 ? 1 : 0, abort);
+        role_producer_b<C>(smem, B, ws, nsb, ct, rot, warp == 3 ? 1 : 0, abort);
     } else if (warp == 2) {
-        role_producer_w(smem, B, &tmap_w, row0, nsb, rot, abort);
+        role_producer_w<C>(smem, B, &tmap_w, row0, nsb, rot, abort);
     } else if (warp == 1) {
-        if (lane == 0) role_mma(smem, B, tmem, nsb, abort);
+        if (lane == 0) role_mma<C>(smem, B, tmem, nsb, abort);
         __syncwarp();
     } else if (warp >= BLD_WARP0 && warp < EPI_WARP0) {
-        role_builder(smem, B, tmem, ws, ct, rot, nvalid, nsb, abort);
+        role_builder<C>(smem, B, tmem, ws, ct, rot, nvalid, nsb, abort);
     } else if (warp >= EPI_WARP0) {
-        role_epilogue<SUMS>(smem, B, tmem, row0, rows, ct, nsb, rot, batch, y, sums, abort);
+        role_epilogue<C, SUMS>(smem, B, tmem, row0, rows, ct, nsb, rot, batch, y, sums, abort);
     }
     pdl_launch_dependents();
 
@@ -731,7 +805,9 @@ bool mma_supported(int64_t rows, int64_t cols, int64_t batch) {
 size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch) {
     (void)rows;
     if (cols % QK_K != 0 || batch < 1) return 0;
-    return (size_t)((batch + TN - 1) / TN) * (size_t)(cols / QK_K) * WS_UNIT;
+    const int tn = pick_tn(batch);
+    const size_t unit = tn == 32 ? Cfg<32>::WS_UNIT : (tn == 64 ? Cfg<64>::WS_UNIT : Cfg<128>::WS_UNIT);
+    return (size_t)((batch + tn - 1) / tn) * (size_t)(cols / QK_K) * unit;
 }
 
 // Static scratch for callers that cannot allocate device memory (see
@@ -766,10 +842,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+template <int TN>
+cudaError_t launch_tiles(const CUtensorMap &tmap, const void *xq, float *y, int32_t *sums, int64_t rows,
+                         int nsb, int64_t batch, uint8_t *ws, const LaunchCtx &ctx) {
+    using C = Cfg<TN>;
+    const int ctiles = (int)((batch + TN - 1) / TN);
+    const int rtiles = (int)((rows + TM - 1) / TM);
+    cudaError_t e = launch_pdl(pack_kernel<TN>, dim3(nsb, ctiles), dim3(256), 0, ctx.stream,
+                               static_cast<const uint8_t *>(xq), ws, nsb, (int)batch);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)ctiles, (unsigned)rtiles);
+    auto k = sums ? mma_q4k_kernel<TN, true> : mma_q4k_kernel<TN, false>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, grid, dim3(NTHREADS), C::SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
+                      static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb, (int)batch, ctx.status);
+}
+
 cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
                            int64_t cols, int64_t batch, void *workspace, const LaunchCtx &ctx) {
     const int nsb = (int)(cols / QK_K);
-    const int ctiles = (int)((batch + TN - 1) / TN);
     const int rtiles = (int)((rows + TM - 1) / TM);
     if (rtiles > 65535) return cudaErrorInvalidConfiguration;
     // W as a 2-D byte tensor: rows of nsb * 144 bytes; box = one super-block
@@ -785,24 +877,12 @@ cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sum
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    cudaError_t e = launch_pdl(pack_kernel, dim3(nsb, ctiles), dim3(256), 0, ctx.stream,
-                               static_cast<const uint8_t *>(xq), ws, nsb, (int)batch);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)ctiles, (unsigned)rtiles);
-    if (sums) {
-        auto k = mma_q4k_kernel<true>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
-                          static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb, (int)batch, ctx.status);
+    switch (pick_tn(batch)) {
+    case 32: return launch_tiles<32>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
+    case 64: return launch_tiles<64>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
+    default: return launch_tiles<128>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
     }
-    auto k = mma_q4k_kernel<false>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k, grid, dim3(NTHREADS), SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
-                      static_cast<const uint8_t *>(xq), y, sums, (int)rows, nsb, (int)batch, ctx.status);
 }
 
 size_t mma_noalloc_scratch_bytes() { return NOALLOC_SCRATCH_BYTES; }

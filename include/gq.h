@@ -193,7 +193,9 @@ gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y,
  * Bytes of workspace the tensor-core path needs for this product (0 when the
  * shape or type has no tensor-core path).  The workspace holds the activation
  * operand repacked once per call as fp16 tiles (plus per-block scales and
- * the min-term operand): ceil(batch / 128) * (cols / 256) * 70144 bytes.
+ * the min-term operand), per column tile of tn = 32 (batch <= 32), 64
+ * (batch <= 64) or 128 columns and per super-block: ceil(batch / tn) *
+ * (cols / 256) * 548 tn bytes (17536, 35072 or 70144 per unit).
  */
 size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int64_t batch);
 

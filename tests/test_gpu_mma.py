@@ -41,8 +41,11 @@ def assert_close(y, y_ref, T):
         f"{bad.sum()} outputs out of tolerance; worst ratio {np.max(err / np.maximum(T, 1e-300)):.3g}")
 
 
+# tile widths 32 (batch <= 32), 64 (<= 64) and 128; ragged row tiles and
+# column tiles; K loops longer than the activation and weight rings
 SHAPES = [(128, 256, 128), (128, 512, 16), (200, 768, 40), (256, 1024, 130), (77, 256, 1),
-          (384, 4096, 64)]
+          (384, 4096, 64), (130, 2048, 32), (300, 1280, 33), (64, 512, 65), (513, 4096, 7),
+          (257, 3072, 50)]
 
 
 @pytest.mark.parametrize("rows,cols,batch", SHAPES)
@@ -68,7 +71,7 @@ def test_mma_auto_dispatch_and_workspace_rules():
     Wq = orc.quantize(Q4_K, inputs.normal(g, (rows, cols), 0.02))
     Xq = orc.quantize(Q8_K, inputs.normal(g, (batch, cols)))
     need = gq.gq_matmul_workspace_bytes(Q4_K, rows, cols, batch)
-    assert need == 1 * 2 * 70144
+    assert need == 1 * 2 * 35072  # one 64-column tile
     assert gq.gq_matmul_workspace_bytes(0, rows, cols, batch) == 0
     y = torch.empty(batch, rows, device="cuda")
     with pytest.raises(gq.GQError):  # MMA without a workspace
