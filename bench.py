@@ -145,22 +145,37 @@ def oracle_gemv_sample():
     return orc, Wq, x
 
 
-def run_cpu_baseline(seconds=10.0):
+def run_cpu_baseline(seconds=10.0, seconds_one=4.0):
     """The oracle, as it stands, on the host cores: act-quantize + GEMV of the
-    4096x4096 Q4_K matrix, repeated for about `seconds`."""
+    4096x4096 Q4_K matrix, repeated for about `seconds` on all cores, then for
+    about `seconds_one` on one core; and the act-quantize alone."""
     orc, Wq, x = oracle_gemv_sample()
     nt = orc.max_threads()
-    n = 0
+
+    def timed(threads, budget):
+        n = 0
+        t0 = time.perf_counter()
+        while True:
+            xq = orc.quantize(orc.Q8_K, x)
+            orc.matmul_ref(orc.Q4_K, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, threads)
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget:
+                return n, dt
+
+    n, dt = timed(nt, seconds)
+    n1, dt1 = timed(1, seconds_one)
+    nq = 0
     t0 = time.perf_counter()
-    while True:
-        xq = orc.quantize(orc.Q8_K, x)
-        orc.matmul_ref(orc.Q4_K, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, nt)
-        n += 1
-        dt = time.perf_counter() - t0
-        if dt >= seconds:
-            break
+    while time.perf_counter() - t0 < 0.5:
+        orc.quantize(orc.Q8_K, x)
+        nq += 1
+    tq = (time.perf_counter() - t0) / nq
     return {"value": n * Wq.nbytes / dt / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
-            "sample": f"{n} x (Q8_K act-quant + Q4_K GEMV 4096x4096, batch 1) in {dt:.1f} s"}
+            "sample": f"{n} x (Q8_K act-quant + Q4_K GEMV 4096x4096, batch 1) in {dt:.1f} s",
+            "single_core": {"value": n1 * Wq.nbytes / dt1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"{n1} x the same in {dt1:.1f} s"},
+            "act_quantize_us": tq * 1e6}
 
 
 def run_reference(args):
