@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream"], default=None,
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv"], default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
 
@@ -270,7 +270,8 @@ def run_gpu(args, world, rank):
               "sweep": lambda: bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph),
               "decode": lambda: bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world),
               "stream": lambda: bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak,
-                                             args.steps)}
+                                             args.steps),
+              "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak)}
         if rank == 0:
             print(json.dumps({"only": args.only, "result": fn[args.only]()}))
         else:
@@ -361,6 +362,7 @@ def run_gpu(args, world, rank):
         extras["decode"] = bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world)
         extras["batch_sweep"] = bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph)
         extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
+        extras["kv_cache"] = bench_kv(gq, torch, dev, capture, time_graph, hbm_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -416,6 +418,46 @@ def bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak, s
     torch.cuda.empty_cache()
     return {"workload": "one launch over 262144 x 4096 Q4_K rows (604 MB)", "us": t / k * 1e6,
             "weight_gbps": gbs, "frac": gbs / hbm_peak}
+
+
+def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak):
+    """Quantized KV cache at 7B shape: 32 heads x 4096 positions x 128, keys
+    as Q8_0 and as Q4_0.  Scores of one query against every cached key,
+    rotated over 16 layer caches (larger than L2) and timed back to back; and
+    the append of one position (all heads)."""
+    n_heads, capacity, head_dim, layers = 32, 4096, 128, 16
+    out = {"workload": f"{n_heads} heads x {capacity} positions x {head_dim}, {layers} layer caches"}
+    g = torch.Generator(device=dev).manual_seed(5)
+    q = torch.randn(n_heads, head_dim, device=dev, generator=g)
+    x = torch.randn(n_heads, head_dim, device=dev, generator=g)
+    for name, t in (("q8_0", gq.Q8_0), ("q4_0", gq.Q4_0)):
+        caches = [gq.kv_cache(t, n_heads, capacity, head_dim, dev) for _ in range(layers)]
+        keys = torch.randn(capacity, n_heads, head_dim, device=dev, generator=g)
+        for p in range(capacity):
+            gq.gq_kv_append(t, keys[p], caches[0], n_heads, head_dim, capacity, p)
+        for c in caches[1:]:
+            c.copy_(caches[0])
+        del keys
+        sc = torch.empty(n_heads, capacity, dtype=torch.float32, device=dev)
+
+        def body():
+            for c in caches:
+                gq.gq_kv_scores(t, c, q, sc, n_heads, head_dim, capacity, capacity)
+
+        t_s, _ = time_graph(capture(body), 20, 3)
+        per = t_s / (20 * layers)
+        kbytes = caches[0].numel()
+
+        def app():
+            for i, c in enumerate(caches):
+                gq.gq_kv_append(t, x, c, n_heads, head_dim, capacity, i)
+
+        t_a, _ = time_graph(capture(app), 20, 3)
+        out[name] = {"scores_us": per * 1e6, "key_bytes": kbytes, "key_gbps": kbytes / per / 1e9,
+                     "frac": kbytes / per / 1e9 / hbm_peak, "append_us": t_a / (20 * layers) * 1e6}
+        del caches
+        torch.cuda.empty_cache()
+    return out
 
 
 def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):

@@ -301,6 +301,55 @@ gq_status gq_matmul_noalloc(gq_type wtype, const void *W, const void *xq, float 
 
 int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }
 
+}  // extern "C"
+
+namespace {
+// Shape and pointer rules shared by the KV-cache calls.
+gq_status check_kv(gq_type type, const void *cache, int64_t n_heads, int64_t head_dim, int64_t capacity) {
+    if (type != GQ_Q8_0 && type != GQ_Q4_0) return GQ_ERR_TYPE;
+    if (n_heads < 0 || n_heads > 65535 || head_dim < 32 || head_dim > 256 || head_dim % 32 != 0)
+        return GQ_ERR_SHAPE;
+    if (capacity < 32 || capacity % 32 != 0 || capacity > ((int64_t)1 << 30)) return GQ_ERR_SHAPE;
+    if (n_heads > 0 && !cache) return GQ_ERR_NULL;
+    if (!aligned(cache, 16)) return GQ_ERR_ALIGN;
+    return GQ_OK;
+}
+}  // namespace
+
+extern "C" {
+
+gq_status gq_kv_append(gq_type type, const float *x, void *cache, int64_t n_heads, int64_t head_dim,
+                       int64_t capacity, int64_t pos, gq_stream_t stream) {
+    gq_status st = check_kv(type, cache, n_heads, head_dim, capacity);
+    if (st != GQ_OK) return st;
+    if (pos < 0 || pos >= capacity) return GQ_ERR_SHAPE;
+    if (n_heads == 0) return GQ_OK;
+    if (!x) return GQ_ERR_NULL;
+    if (!aligned(x, 4)) return GQ_ERR_ALIGN;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    const int64_t nb = head_dim / 32;
+    uint8_t *dst = static_cast<uint8_t *>(cache) + pos * nb * block_bytes(type);
+    cudaError_t e = launch_quantize_rows_strided(type, x, dst, n_heads, nb, capacity * nb, ctx);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e);
+}
+
+gq_status gq_kv_scores(gq_type type, const void *cache, const float *q, float *scores, int64_t n_heads,
+                       int64_t head_dim, int64_t capacity, int64_t n_pos, gq_stream_t stream) {
+    gq_status st = check_kv(type, cache, n_heads, head_dim, capacity);
+    if (st != GQ_OK) return st;
+    if (n_pos < 0 || n_pos > capacity) return GQ_ERR_SHAPE;
+    if (n_heads == 0 || n_pos == 0) return GQ_OK;
+    if (!q || !scores) return GQ_ERR_NULL;
+    if (!aligned(q, 4) || !aligned(scores, 4)) return GQ_ERR_ALIGN;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    cudaError_t e = launch_kv_scores(type, cache, q, scores, n_heads, head_dim, capacity, n_pos, ctx);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e);
+}
+
 gq_status gq_device_status(uint32_t *word, int reset) {
     LaunchCtx ctx;
     gq_status st = make_ctx(nullptr, &ctx);

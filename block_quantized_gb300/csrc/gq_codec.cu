@@ -16,6 +16,8 @@
 // Work split: one warp per block.  Q8_0 / Q4_0: lane i owns element i.
 // Q4_K / Q8_K: lane l owns elements 8l..8l+7, so the four lanes 4j..4j+3 own
 // sub-block j and sub-block statistics are 2-step shuffle reductions.
+#include <algorithm>
+
 #include "gq_common.cuh"
 #include "gq_internal.h"
 
@@ -34,11 +36,15 @@ __device__ __forceinline__ float clampf(float v, float lo, float hi) {
     return v < lo ? lo : (v > hi ? hi : v);
 }
 
-// Symmetric block of 32 (Q8_0 when QMAX = 127, Q4_0 when QMAX = 7).
+// Symmetric block of 32 (Q8_0 when QMAX = 127, Q4_0 when QMAX = 7).  Source
+// block b is element row b / row_blocks, block b % row_blocks of that row;
+// destination rows are dst_row_stride blocks apart (row_blocks = nblocks for
+// one contiguous run).
 template <int QMAX>
 __global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict__ x,
                                                          uint8_t *__restrict__ dst,
-                                                         int64_t nblocks) {
+                                                         int64_t nblocks, int64_t row_blocks,
+                                                         int64_t dst_row_stride) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     pdl_launch_dependents();  // dependents still wait for this grid's completion
@@ -46,6 +52,7 @@ __global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict
     for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks;
          b += warps) {
         const float v = x[b * 32 + lane];
+        const int64_t ob = (b / row_blocks) * dst_row_stride + b % row_blocks;  // destination block
         // max|x| (fabsf never yields -0, so the max of the block is well defined)
         const float amax = warp_max(fabsf(v));
         const __half dh = __float2half_rn(__fdiv_rn(amax, (float)QMAX));
@@ -54,7 +61,7 @@ __global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict
             const float q = (d == 0.0f) ? 0.0f : clampf(roundf(__fdiv_rn(v, d)), -127.0f, 127.0f);
             const int qi = (int)q & 0xff;
             const int nxt = __shfl_down_sync(FULL, qi, 1);
-            uint8_t *blk = dst + b * Q8_0_BYTES;
+            uint8_t *blk = dst + ob * Q8_0_BYTES;
             if ((lane & 1) == 0)
                 *reinterpret_cast<uint16_t *>(blk + 2 + lane) = (uint16_t)(qi | (nxt << 8));
             if (lane == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(dh);
@@ -64,7 +71,7 @@ __global__ void __launch_bounds__(256) quantize32_kernel(const float *__restrict
             const int hi = __shfl_down_sync(FULL, c, 1);
             const int byte = c | (hi << 4);  // valid on even lanes: element 2j low, 2j+1 high
             const int byte2 = __shfl_down_sync(FULL, byte, 2);
-            uint8_t *blk = dst + b * Q4_0_BYTES;
+            uint8_t *blk = dst + ob * Q4_0_BYTES;
             if ((lane & 3) == 0)
                 *reinterpret_cast<uint16_t *>(blk + 2 + (lane >> 1)) =
                     (uint16_t)((byte & 0xff) | ((byte2 & 0xff) << 8));
@@ -267,15 +274,32 @@ cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
     uint8_t *d8 = static_cast<uint8_t *>(dst);
     switch (t) {
     case GQ_Q8_0:
-        return launch_pdl(quantize32_kernel<127>, grid, 256, 0, ctx.stream, src, d8, nb);
+        return launch_pdl(quantize32_kernel<127>, grid, 256, 0, ctx.stream, src, d8, nb, std::max<int64_t>(nb, 1),
+                          (int64_t)0);
     case GQ_Q4_0:
-        return launch_pdl(quantize32_kernel<7>, grid, 256, 0, ctx.stream, src, d8, nb);
+        return launch_pdl(quantize32_kernel<7>, grid, 256, 0, ctx.stream, src, d8, nb, std::max<int64_t>(nb, 1),
+                          (int64_t)0);
     case GQ_Q4_K:
         return launch_pdl(quantize_q4_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
     case GQ_Q8_K:
         return launch_pdl(quantize_q8_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_rows_strided(gq_type t, const float *src, void *dst, int64_t rows,
+                                         int64_t row_blocks, int64_t dst_row_stride, const LaunchCtx &ctx) {
+    const int64_t nb = rows * row_blocks;
+    const int grid = grid_for(nb, 8, ctx.num_sms);
+    uint8_t *d8 = static_cast<uint8_t *>(dst);
+    switch (t) {
+    case GQ_Q8_0:
+        return launch_pdl(quantize32_kernel<127>, grid, 256, 0, ctx.stream, src, d8, nb, row_blocks, dst_row_stride);
+    case GQ_Q4_0:
+        return launch_pdl(quantize32_kernel<7>, grid, 256, 0, ctx.stream, src, d8, nb, row_blocks, dst_row_stride);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_dequantize(gq_type t, const void *src, float *dst, int64_t n,

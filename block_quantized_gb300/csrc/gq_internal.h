@@ -37,6 +37,15 @@ cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
                             const LaunchCtx &ctx);
 cudaError_t launch_dequantize(gq_type t, const void *src, float *dst, int64_t n,
                               const LaunchCtx &ctx);
+// Q8_0 / Q4_0 quantize of `rows` rows of row_blocks blocks each, destination
+// rows dst_row_stride blocks apart (the KV-cache append).
+cudaError_t launch_quantize_rows_strided(gq_type t, const float *src, void *dst, int64_t rows,
+                                         int64_t row_blocks, int64_t dst_row_stride, const LaunchCtx &ctx);
+
+// Quantized KV cache: scores[h][p] = dot of key row (h, p) of the cache with
+// the Q8_0-quantized query q[h], for p < n_pos.
+cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float *scores, int64_t n_heads,
+                             int64_t head_dim, int64_t capacity, int64_t n_pos, const LaunchCtx &ctx);
 
 // dp4a GEMV family.  sums != nullptr selects the block-sum diagnostic output
 // instead of y.  fused_f32: `act` is fp32 activations quantized inside the

@@ -51,6 +51,8 @@ SIGNATURES = {
     "gq_block_sums_ws": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, ctypes.c_size_t,
                           _vp], _i32),
     "gq_matmul_noalloc": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
+    "gq_kv_append": ([_i32, _vp, _vp, _i64, _i64, _i64, _i64, _vp], _i32),
+    "gq_kv_scores": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp], _i32),
     "gq_tc_min_batch": ([], _i64),
     "gq_device_status": ([_u32p, _i32], _i32),
 }
@@ -203,6 +205,18 @@ def gq_matmul_noalloc(wtype: int, W, xq, y, rows: int, cols: int, batch: int,
                                                          batch, _s(stream)))
 
 
+def gq_kv_append(t: int, x, cache, n_heads: int, head_dim: int, capacity: int, pos: int,
+                 stream=None) -> None:
+    _check("gq_kv_append", load().gq_kv_append(t, _p(x), _p(cache), n_heads, head_dim, capacity, pos,
+                                               _s(stream)))
+
+
+def gq_kv_scores(t: int, cache, q, scores, n_heads: int, head_dim: int, capacity: int, n_pos: int,
+                 stream=None) -> None:
+    _check("gq_kv_scores", load().gq_kv_scores(t, _p(cache), _p(q), _p(scores), n_heads, head_dim, capacity,
+                                               n_pos, _s(stream)))
+
+
 def gq_tc_min_batch() -> int:
     return int(load().gq_tc_min_batch())
 
@@ -299,3 +313,22 @@ def block_sums_f32(wtype: int, W, x, rows: int, cols: int, batch: int, stream=No
     s = _sums_buffer(wtype, W, rows, cols, batch)
     gq_block_sums_f32(wtype, W, x, s, rows, cols, batch, stream)
     return s
+
+
+def kv_cache(t: int, n_heads: int, capacity: int, head_dim: int, device=None):
+    """A zeroed uint8 device tensor [n_heads, capacity, head_dim / 32 * block_bytes]
+    laid out as gq_kv_append / gq_kv_scores expect."""
+    import torch
+    return torch.zeros(n_heads, capacity, head_dim // BLOCK_ELEMS[t] * BLOCK_BYTES[t], dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def kv_scores(t: int, cache, q, n_pos: int, stream=None):
+    """Scores [n_heads, n_pos] of fp32 queries q [n_heads, head_dim] against the
+    first n_pos cached keys of each head."""
+    import torch
+    n_heads, capacity = cache.shape[0], cache.shape[1]
+    head_dim = q.shape[-1]
+    out = torch.empty(n_heads, n_pos, dtype=torch.float32, device=q.device)
+    gq_kv_scores(t, cache, q, out, n_heads, head_dim, capacity, n_pos, stream)
+    return out

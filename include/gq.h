@@ -281,6 +281,43 @@ gq_status gq_block_sums_f32(gq_type wtype, const void *W, const float *x, int32_
 gq_status gq_matmul_noalloc(gq_type wtype, const void *W, const void *xq, float *y,
                             int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
 
+/*
+ * Quantized KV cache ("llama.cpp 推理引擎" §3.7.3, KV Cache 量化: keys and
+ * values cached as Q8_0 or Q4_0 blocks; §6.4 for the block dot).
+ *
+ * Cache layout (device, owned by the caller, 16-byte aligned):
+ * [n_heads][capacity][head_dim / 32] blocks of `type`, so row (h, p) -- the
+ * key (or value) of head h at position p -- is head_dim / 32 consecutive
+ * blocks and the rows of a head are consecutive.  Size:
+ * n_heads * capacity * head_dim / 32 * gq_block_bytes(type) bytes.
+ *   type     : GQ_Q8_0 or GQ_Q4_0 (GQ_ERR_TYPE otherwise).
+ *   head_dim : a multiple of 32, 32 .. 256.
+ *   capacity : positions per head, a multiple of 32 (the scores kernel reads
+ *              whole groups of 32 rows), at most 2^30.
+ *   n_heads  : 0 .. 65535 (0 is a no-op returning GQ_OK).
+ * Asynchronous on `stream`; the cache bytes of other rows are never written.
+ */
+
+/* Quantizes x = float[n_heads][head_dim] (device, 4-byte aligned) into row
+ * (h, pos) of every head, with exactly the arithmetic of gq_quantize_rows:
+ * the bytes equal gq_quantize_rows of x[h] written at that row.  pos in
+ * [0, capacity) (GQ_ERR_SHAPE otherwise). */
+gq_status gq_kv_append(gq_type type, const float *x, void *cache, int64_t n_heads, int64_t head_dim,
+                       int64_t capacity, int64_t pos, gq_stream_t stream);
+
+/* Attention scores against the cached keys: for every head h and position
+ * p < n_pos,
+ *   scores[h][p] = sum over the blocks k of row (h, p) of d_k * d_q * s_k,
+ * s_k the integer dot of the key codes (c - 8 for Q4_0) with the codes of
+ * q[h] quantized to Q8_0 in the kernel (the arithmetic of gq_quantize_rows),
+ * i.e. gq_matmul of head h's first n_pos rows with q[h] as one vector.  The
+ * 1/sqrt(head_dim) factor and the softmax are the caller's.
+ *   q      : device float[n_heads][head_dim], 4-byte aligned.
+ *   scores : device float[n_heads][n_pos], 4-byte aligned.
+ *   n_pos  : 0 .. capacity (0 is a no-op). */
+gq_status gq_kv_scores(gq_type type, const void *cache, const float *q, float *scores, int64_t n_heads,
+                       int64_t head_dim, int64_t capacity, int64_t n_pos, gq_stream_t stream);
+
 /* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
  * Q4_K (the measured crossover; the environment variable GQ_TC_MIN_BATCH,
  * read once, overrides it). */

@@ -194,3 +194,36 @@ def matmul_ref(wtype: int, W: np.ndarray, xq: np.ndarray, rows: int, cols: int,
 
 def max_threads() -> int:
     return int(lib().or_max_threads())
+
+
+# ------------------------------------------------------------ KV cache
+# "llama.cpp 推理引擎" §3.7.3 (KV Cache 量化): the attention keys and values
+# are cached as Q8_0 or Q4_0 blocks.  A cache is a uint8 array
+# [n_heads, capacity, head_dim / 32 * block_bytes]: row (h, p) holds head h's
+# key (or value) at position p.
+
+def kv_append(t: int, x: np.ndarray, cache: np.ndarray, pos: int) -> np.ndarray:
+    """Writes x [n_heads, head_dim], each head's row quantized with the block
+    encoding of type t (§5.1), into row (h, pos) of every head; returns cache."""
+    if t not in (Q8_0, Q4_0):
+        raise ValueError("KV cache blocks are Q8_0 or Q4_0")
+    for h in range(cache.shape[0]):
+        cache[h, pos] = quantize(t, x[h]).reshape(-1)
+    return cache
+
+
+def kv_scores_ref(t: int, cache: np.ndarray, q: np.ndarray, n_pos: int):
+    """Scores of the queries q [n_heads, head_dim] against the first n_pos keys
+    of each head: the query quantized to Q8_0, then per head the block-dot
+    product of §6.4 with the key rows as the weight rows (matmul_ref).
+    Returns (scores, T), each [n_heads, n_pos] in double, T the sum of
+    |block terms| per output for the tolerance."""
+    n_heads = cache.shape[0]
+    head_dim = q.shape[1]
+    S = np.empty((n_heads, n_pos))
+    T = np.empty((n_heads, n_pos))
+    for h in range(n_heads):
+        qq = quantize(Q8_0, q[h:h + 1])
+        y, tt = matmul_ref(t, cache[h, :n_pos], qq, n_pos, head_dim, 1)
+        S[h], T[h] = y[0], tt[0]
+    return S, T

@@ -142,3 +142,31 @@ def test_workspace_rules_on_host(lib):
     assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, A16 + 8, need, None) == ALIGN
     assert m(0, A16, A16, A16, 128, 256, 64, 2, 0, A16, need, None) == TYPE
     assert lib.gq_matmul_path(2, A16, A16, A16, 128, 256, 64, 2, None) == NULL
+
+
+def test_kv_validation(lib):
+    ap, sc = lib.gq_kv_append, lib.gq_kv_scores
+    A16 = 1 << 20
+    # append(type, x, cache, n_heads, head_dim, capacity, pos, stream)
+    assert ap(2, A16, A16, 4, 128, 64, 0, None) == TYPE          # Q4_K cache
+    assert ap(3, A16, A16, 4, 128, 64, 0, None) == TYPE
+    assert ap(1, A16, A16, 4, 48, 64, 0, None) == SHAPE          # head_dim not a multiple of 32
+    assert ap(1, A16, A16, 4, 288, 64, 0, None) == SHAPE         # head_dim > 256
+    assert ap(1, A16, A16, 4, 128, 48, 0, None) == SHAPE         # capacity not a multiple of 32
+    assert ap(1, A16, A16, 4, 128, 64, 64, None) == SHAPE        # pos past the capacity
+    assert ap(1, A16, A16, 4, 128, 64, -1, None) == SHAPE
+    assert ap(1, A16, A16, -1, 128, 64, 0, None) == SHAPE
+    assert ap(1, A16, 0, 4, 128, 64, 0, None) == NULL
+    assert ap(1, 0, A16, 4, 128, 64, 0, None) == NULL
+    assert ap(1, A16, A16 + 8, 4, 128, 64, 0, None) == ALIGN     # cache 16-byte aligned
+    assert ap(1, A16 + 2, A16, 4, 128, 64, 0, None) == ALIGN     # x 4-byte aligned
+    assert ap(1, A16, A16, 0, 128, 64, 0, None) == OK            # no heads: nothing to do
+    # scores(type, cache, q, scores, n_heads, head_dim, capacity, n_pos, stream)
+    assert sc(2, A16, A16, A16, 4, 128, 64, 10, None) == TYPE
+    assert sc(0, A16, A16, A16, 4, 128, 64, 65, None) == SHAPE   # n_pos past the capacity
+    assert sc(0, A16, A16, A16, 4, 128, 50, 10, None) == SHAPE
+    assert sc(0, A16, 0, A16, 4, 128, 64, 10, None) == NULL
+    assert sc(0, A16, A16, 0, 4, 128, 64, 10, None) == NULL
+    assert sc(0, A16 + 4, A16, A16, 4, 128, 64, 10, None) == ALIGN
+    assert sc(0, A16, A16, A16 + 2, 4, 128, 64, 10, None) == ALIGN
+    assert sc(0, A16, A16, A16, 4, 128, 64, 0, None) == OK       # no positions

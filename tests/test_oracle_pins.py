@@ -394,3 +394,46 @@ def test_multithreaded_quantize_equals_blockwise(t):
     be = orc.block_elems(t)
     x = inputs.outlier_weights(inputs.rng(17), 33, 4 * be, frac=0.01)
     np.testing.assert_array_equal(orc.quantize_rows_mt(t, x, 4), orc.quantize(t, x))
+
+
+# --------------------------------------------------------------------------
+# Quantized KV cache: append is the block encoding written at one position;
+# the scores are the dot of dequantized keys and dequantized query
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("t", [Q8_0, Q4_0])
+def test_kv_append_writes_one_row_per_head(t):
+    g = inputs.rng(7)
+    n_heads, capacity, head_dim = 3, 32, 64
+    cache = np.full((n_heads, capacity, head_dim // 32 * orc.block_bytes(t)), 0xA5, np.uint8)
+    before = cache.copy()
+    x = inputs.normal(g, (n_heads, head_dim))
+    orc.kv_append(t, x, cache, 5)
+    for h in range(n_heads):
+        # the row round-trips within half a step of its block scale ...
+        xd = orc.dequantize_f64(t, cache[h, 5], head_dim)
+        for b in range(head_dim // 32):
+            blk = x[h, 32 * b:32 * b + 32].astype(np.float64)
+            d = np.abs(blk).max() / (127.0 if t == Q8_0 else 7.0)
+            # the fp16 rounding of d moves a step by at most 2^-11 relative
+            assert np.all(np.abs(xd[32 * b:32 * b + 32] - blk) <= d * (0.5 + 2.0 ** -10))
+        # ... and every other row is untouched
+        np.testing.assert_array_equal(np.delete(cache[h], 5, axis=0), np.delete(before[h], 5, axis=0))
+
+
+@pytest.mark.parametrize("t", [Q8_0, Q4_0])
+def test_kv_scores_vs_bruteforce(t):
+    g = inputs.rng(8)
+    n_heads, capacity, head_dim, n_pos = 3, 64, 96, 37
+    cache = np.zeros((n_heads, capacity, head_dim // 32 * orc.block_bytes(t)), np.uint8)
+    # per-head scale spread so a head mix-up cannot hide
+    for p in range(n_pos):
+        orc.kv_append(t, inputs.normal(g, (n_heads, head_dim)) * np.array([[0.5], [1.0], [4.0]]), cache, p)
+    q = inputs.normal(g, (n_heads, head_dim)) * np.array([[3.0], [0.25], [1.0]])
+    S, T = orc.kv_scores_ref(t, cache, q, n_pos)
+    for h in range(n_heads):
+        K = np.stack([orc.dequantize_f64(t, cache[h, p], head_dim) for p in range(n_pos)])
+        qd = orc.dequantize_f64(Q8_0, orc.quantize(Q8_0, q[h]), head_dim)
+        naive = np.array([sum(K[p, i] * qd[i] for i in range(head_dim)) for p in range(n_pos)])
+        assert np.all(T[h] > 0)
+        np.testing.assert_allclose(S[h], naive, rtol=0, atol=1e-12 * T[h].max())
