@@ -37,9 +37,18 @@ __device__ __forceinline__ uint32_t lds_u16(const uint8_t *p) {
     return *reinterpret_cast<const uint16_t *>(p);
 }
 
-// Four bytes at a 2-byte aligned shared-memory address (two 16-bit loads).
-__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t *p) {
-    return lds_u16(p) | (lds_u16(p + 2) << 16);
+// The NW 32-bit words starting at the 2-byte aligned shared-memory address
+// p, read as NW + 1 aligned words and funnel-shifted into place (reads up to
+// 4 bytes past the last word: the staging area carries a tail pad).
+template <int NW>
+__device__ __forceinline__ void lds_words_a2(const uint8_t *p, uint32_t (&w)[NW]) {
+    const uint32_t *a = reinterpret_cast<const uint32_t *>(reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)3);
+    const uint32_t sh = (uint32_t)(reinterpret_cast<uintptr_t>(p) & 3u) * 8u;  // 0 or 16
+    uint32_t r[NW + 1];
+#pragma unroll
+    for (int i = 0; i <= NW; ++i) r[i] = a[i];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
 }
 
 // WT = GQ_Q8_0 or GQ_Q4_0 key blocks.  Q4_0 codes are c - 8 with c the stored
@@ -112,14 +121,17 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
         const int *qw = reinterpret_cast<const int *>(qc[j]);
         int s = 0;
         if (WT == GQ_Q8_0) {
+            uint32_t w[8];
+            lds_words_a2<8>(blk + 2, w);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s = dp4a((int)lds_u32_a2(blk + 2 + 4 * k), qw[k], s);
+            for (int k = 0; k < 8; ++k) s = dp4a((int)w[k], qw[k], s);
         } else {
+            uint32_t w[4];
+            lds_words_a2<4>(blk + 2, w);  // word k: elements 8k .. 8k + 7
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint32_t w = lds_u32_a2(blk + 2 + 4 * k);  // elements 8k .. 8k + 7
-                s = dp4a_us(w & NIB, qw[2 * k], s);
-                s = dp4a_us((w >> 4) & NIB, qw[2 * k + 1], s);
+                s = dp4a_us(w[k] & NIB, qw[2 * k], s);
+                s = dp4a_us((w[k] >> 4) & NIB, qw[2 * k + 1], s);
             }
             s -= 8 * qsum[j];
         }
@@ -135,7 +147,7 @@ cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float
     const int nb = (int)(head_dim / 32);
     if (nb < 1 || nb > KV_MAX_NB || capacity % KV_POS != 0 || n_heads > 65535) return cudaErrorInvalidValue;
     const int bb = t == GQ_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES;
-    const size_t smem = (size_t)KV_WARPS * KV_POS * nb * bb;
+    const size_t smem = (size_t)KV_WARPS * KV_POS * nb * bb + 16;  // + tail pad for the word reads
     const dim3 grid((unsigned)((n_pos + KV_WARPS * KV_POS - 1) / (KV_WARPS * KV_POS)), (unsigned)n_heads);
     const uint8_t *c8 = static_cast<const uint8_t *>(cache);
     if (t == GQ_Q8_0) {
