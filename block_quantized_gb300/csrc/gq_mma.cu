@@ -64,6 +64,8 @@ constexpr int KS = 64;    // K per B operand stage (one 128-byte swizzle atom)
 constexpr int NKS = 4;    // B operand stages per super-block
 constexpr int KMIN = 16;  // min-term K per super-block (8 mins, two halves of t)
 constexpr int NSM = 4;    // ring depth of the per-super-block scales and min-term A rows
+constexpr int NF = 4;     // ring of per-super-block ready / done barriers (= NSM)
+static_assert(NF == NSM, "the min-term rows share the ready/done ring");
 constexpr int MIN_A = TM * KMIN * 2;           // 4 KB min-term A rows
 constexpr int RAW_STAGE = TM * Q4_K_BYTES;     // 18 KB raw weight rows
 constexpr int NTHREADS = 896;
@@ -144,10 +146,10 @@ struct Cfg {
     static constexpr int OFF_RAW = OFF_MINA + NSM * MIN_A;        // NRAW x 18 KB
     static constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;   // NSM scale stages
     static constexpr int OFF_BAR = OFF_META + NSM * META_STAGE;
-    // A: full (builders), empty (epilogue); B: full-tx (producers), empty;
-    // min: full (builders), empty; raw: full, empty; meta: full (builders),
-    // empty; acc: full, empty; final.
-    static constexpr int NBARS = 2 * NA + 2 * NBS + 2 * NSM + 2 * NRAW + 2 * NSM + 2 * 2 + 1;
+    // per super-block ready (A and min-term rows built) and done (all its
+    // MMAs complete), A empty, B tx, raw full/empty, meta full/empty, S1
+    // empty, final.
+    static constexpr int NBARS = 2 * NF + NA + NBS + 2 * NRAW + 2 * NSM + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
@@ -348,30 +350,34 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
 
 // ------------------------------------------------------------- main kernel
 
-// Barriers whose only arrival is a transfer's transaction count (b_tx,
-// raw_full) tell the consumer that a copy has landed; the builders arrive on
-// the plain *_full ones.
+// Barriers.  b_tx and raw_full complete when a copy has landed (their only
+// arrival is the producer's expect-tx).  Per super-block sb, in a ring of NF:
+//   sb_full[sb % NF]: its A operand (one arrival per builder warp) and its
+//                     min-term A rows (one per hh = 0 builder warp) are in place;
+//   sb_done[sb % NF]: every MMA of sb has completed (one commit) -- its S1 and
+//                     S2 may be read, and its two B slots and min-term rows
+//                     reused.
+// A waiter on sb_done for super-block x uses parity (x / NF) & 1; the ring
+// cannot run a lap ahead of it, since super-block x + NF needs, through the
+// waiter itself, a resource that x releases.
 struct Bars {
-    uint64_t *a_full, *a_empty, *b_tx, *b_empty, *min_full, *min_empty, *raw_full, *raw_empty;
-    uint64_t *meta_full, *meta_empty, *acc_full, *acc_empty, *fin;
+    uint64_t *sb_full, *sb_done, *a_empty, *b_tx, *raw_full, *raw_empty;
+    uint64_t *meta_full, *meta_empty, *acc_empty, *fin;
 };
 
 template <class C>
 __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     uint64_t *b = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     Bars r;
-    r.a_full = b;
-    r.a_empty = r.a_full + C::NA;
+    r.sb_full = b;
+    r.sb_done = r.sb_full + NF;
+    r.a_empty = r.sb_done + NF;
     r.b_tx = r.a_empty + C::NA;
-    r.b_empty = r.b_tx + C::NBS;
-    r.min_full = r.b_empty + C::NBS;
-    r.min_empty = r.min_full + NSM;
-    r.raw_full = r.min_empty + NSM;
+    r.raw_full = r.b_tx + C::NBS;
     r.raw_empty = r.raw_full + C::NRAW;
     r.meta_full = r.raw_empty + C::NRAW;
     r.meta_empty = r.meta_full + NSM;
-    r.acc_full = r.meta_empty + NSM;
-    r.acc_empty = r.acc_full + 2;
+    r.acc_empty = r.meta_empty + NSM;
     r.fin = r.acc_empty + 2;
     return r;
 }
@@ -397,7 +403,8 @@ __device__ void role_producer_b(uint8_t *smem, const Bars &B, const uint8_t *__r
     for (int sb = 0; ok && sb < nsb; ++sb) {
         const int s = b_slot<C>(sb, h);
         const uint32_t ph = b_phase<C>(sb);
-        if (!(ok = wait_warp(B.b_empty + s, ph ^ 1u, abort))) break;
+        const int prev = sb - C::NBSB;  // the super-block that last used this slot
+        if (prev >= 0 && !(ok = wait_warp(B.sb_done + prev % NF, (uint32_t)(prev / NF) & 1u, abort))) break;
         if (lane == 0) {
             const uint8_t *src =
                 ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * C::WS_UNIT + (h ? C::HALF0_BYTES : 0);
@@ -519,7 +526,7 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(B.a_full + ai);
+        if (lane == 0) mbar_arrive(B.sb_full + sb % NF);
 
         // then (off the MMA's critical path) the epilogue's scales and, for
         // hh = 0, the min-term A row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
@@ -542,13 +549,14 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
                 lo[j >> 1] = pack_h2(m0, m1);
                 hi[j >> 1] = pack_h2(64.0f * m0, 64.0f * m1);
             }
-            if (!wait_warp(B.min_empty + mr.idx, mr.phase ^ 1u, abort)) return;
+            // the min-term rows of sb - NF (same slot) have been consumed
+            if (sb >= NF && !wait_warp(B.sb_done + sb % NF, (uint32_t)(sb / NF - 1) & 1u, abort)) return;
             uint8_t *ma = smem + C::OFF_MINA + mr.idx * MIN_A;
             *reinterpret_cast<uint4 *>(ma + plain_off(t, 0)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             *reinterpret_cast<uint4 *>(ma + plain_off(t, 1)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(B.min_full + mr.idx);
+            if (lane == 0) mbar_arrive(B.sb_full + sb % NF);
         }
         mr.next();
     }
@@ -582,12 +590,16 @@ __device__ __forceinline__ void mma8_ta(uint32_t d, const uint32_t (&a)[8], cons
 }
 
 
-// MMA issuer (warp 1, one thread).  Per super-block: sixteen K=16 steps of
-// the S1 product (A from the tensor-memory buffer of the super-block, B from
-// the two halves of the unit in the ring) into the S1 buffer of its parity,
-// eight per half in one asm block, then one K=16 step of the min-term product
-// S2 (A rows from the builders, B tile from half 1) written over the consumed
-// A buffer.  Always ends with a commit to `fin` so the teardown can wait for
+// MMA issuer (warp 1, one thread).  Per super-block: once its A operand and
+// min-term rows are built (sb_full), the S1 buffer of its parity is drained
+// and the first B half has landed, eight K=16 steps of the S1 product (A from
+// the super-block's tensor-memory buffer, B from the ring), then after the
+// second half has landed eight more, then one K=16 step of the min-term
+// product S2 written over the consumed A buffer; then a single commit
+// (sb_done) that the epilogue, the B producers and the min-term builders all
+// wait on.  A wait or a commit costs the issuing thread about as much as one
+// to two MMAs, so the super-block has as few of them as its dependencies
+// allow.  Always ends with a commit to `fin` so the teardown can wait for
 // every MMA to finish.
 template <class C>
 __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, volatile uint32_t *abort) {
@@ -597,15 +609,13 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
         const int p = sb & 1;                                   // S1 buffer
         const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
         const int ai = sb % C::NA;                              // A buffer
-        const uint32_t aph = (uint32_t)(sb / C::NA) & 1u;
-        const int mi = sb % NSM;
-        const uint32_t mph = (uint32_t)(sb / NSM) & 1u;
-        if (!(ok = wait_or_abort(B.a_full + ai, aph, abort))) break;
+        const int f = sb % NF;                                  // ready / done ring, min-term rows
+        if (!(ok = wait_or_abort(B.sb_full + f, (uint32_t)(sb / NF) & 1u, abort))) break;
         if (!(ok = wait_or_abort(B.acc_empty + p, ph ^ 1u, abort))) break;
         for (int h = 0; h < 2; ++h) {
             const int sl = b_slot<C>(sb, h);
             if (!(ok = wait_or_abort(B.b_tx + sl, b_phase<C>(sb), abort))) break;
-            tc_fence_after();
+            if (h == 0) tc_fence_after();
             const uint64_t b0 = desc_sw128(smem_u32(smem + C::OFF_B + sl * C::SLOT_B));
             const uint32_t a0 = tmem + C::col_a(ai) + 64u * h;
             uint32_t av[8];
@@ -616,17 +626,12 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
                 bv[i] = b0 + OPB16 * (uint64_t)(i >> 2) + 2u * (uint64_t)(i & 3);
             }
             mma8_ta(tmem + C::col_s1(p), av, bv, C::IDESC, (uint32_t)h);
-            if (h == 0) mma_commit(B.b_empty + sl);  // half 0 is free once these MMAs complete
         }
         if (!ok) break;
-        if (!(ok = wait_or_abort(B.min_full + mi, mph, abort))) break;
-        tc_fence_after();
-        const uint32_t a2 = smem_u32(smem + C::OFF_MINA + mi * MIN_A);
+        const uint32_t a2 = smem_u32(smem + C::OFF_MINA + f * MIN_A);
         const uint32_t b2 = smem_u32(smem + C::OFF_B + b_slot<C>(sb, 1) * C::SLOT_B + C::SLOT_MIN);
         mma_f16(tmem + C::col_a(ai), desc_plain(a2, 128, 256), desc_plain(b2, 128, 256), C::IDESC, 0u);
-        mma_commit(B.min_empty + mi);
-        mma_commit(B.b_empty + b_slot<C>(sb, 1));
-        mma_commit(B.acc_full + p);  // S1 and S2 of this super-block are ready
+        mma_commit(B.sb_done + f);  // S1 and S2 ready; both B slots and the min-term rows free
     }
     mma_commit(B.fin);
 }
@@ -659,7 +664,7 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
         const int mi = sb % NSM;
         const uint32_t mph = (uint32_t)(sb / NSM) & 1u;
         if (!(ok = wait_warp(B.meta_full + mi, mph, abort))) break;
-        if (!(ok = wait_warp(B.acc_full + p, ph, abort))) break;
+        if (!(ok = wait_warp(B.sb_done + sb % NF, (uint32_t)(sb / NF) & 1u, abort))) break;
         tc_fence_after();
         const uint8_t *meta = smem + C::OFF_META + mi * C::META_STAGE;
         const float d = reinterpret_cast<const float *>(meta + C::META_D)[r];
@@ -729,18 +734,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     const int nvalid = min(TM, rows - row0);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < C::NA; ++i) {
-            mbar_init(B.a_full + i, BLD_THREADS / 32);  // one arrival per builder warp
-            mbar_init(B.a_empty + i, C::EPI_ACTIVE);    // the epilogue has read the S2 over it
+        for (int i = 0; i < NF; ++i) {
+            // one arrival per builder warp (A) and per hh = 0 builder warp (min-term rows)
+            mbar_init(B.sb_full + i, BLD_THREADS / 32 + 4);
+            mbar_init(B.sb_done + i, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(B.acc_full + i, 1);
-            mbar_init(B.acc_empty + i, C::EPI_ACTIVE);
-        }
-        for (int i = 0; i < C::NBS; ++i) {
-            mbar_init(B.b_tx + i, 1);
-            mbar_init(B.b_empty + i, 1);
-        }
+        for (int i = 0; i < C::NA; ++i) mbar_init(B.a_empty + i, C::EPI_ACTIVE);  // S2 over it read
+        for (int i = 0; i < 2; ++i) mbar_init(B.acc_empty + i, C::EPI_ACTIVE);
+        for (int i = 0; i < C::NBS; ++i) mbar_init(B.b_tx + i, 1);
         for (int i = 0; i < C::NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
             mbar_init(B.raw_empty + i, BLD_THREADS);
@@ -748,8 +749,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
         for (int i = 0; i < NSM; ++i) {
             mbar_init(B.meta_full + i, BLD_THREADS);  // every builder thread writes one entry
             mbar_init(B.meta_empty + i, C::EPI_ACTIVE);
-            mbar_init(B.min_full + i, 4);             // the four hh = 0 builder warps
-            mbar_init(B.min_empty + i, 1);
         }
         mbar_init(B.fin, 1);
         *abort = 0u;
