@@ -475,9 +475,9 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
 // A columns 64hh .. + 63 of the buffer of the super-block's parity.  Each
 // sub-block is 16 columns, written by one tcgen05.st from registers; the
 // buffer is free again once the epilogue has read the S2 written over it.
-// Then the hh = 0 threads write row t's scales d, dmin and its min-term A row,
-// the hh = 1 threads (t < TN) column t's scale (read from the workspace,
-// requested before the raw weights are waited for).
+// Then the hh = 0 threads write row t's min-term A row, the hh = 1 threads
+// row t's scales d, dmin and (t < TN) column t's scale dx (read from the
+// workspace, requested before the raw weights are waited for).
 template <class C>
 __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const uint8_t *__restrict__ ws,
                              int ct, int rot, int nvalid, int nsb, volatile uint32_t *abort) {
@@ -528,18 +528,17 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         __syncwarp();
         if (lane == 0) mbar_arrive(B.sb_full + sb % NF);
 
-        // then (off the MMA's critical path) the epilogue's scales and, for
-        // hh = 0, the min-term A row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
-        if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
-        uint8_t *meta = smem + C::OFF_META + mr.idx * C::META_STAGE;
-        if (hh == 0) {
+        // then (off the MMA's critical path) the hh = 1 threads write the
+        // epilogue's scales (row t's d and dmin, column t's dx), the hh = 0
+        // threads row t's min-term A row [m_0..m_7 | 64 m_0..64 m_7] (fp16, exact)
+        if (hh == 1) {
+            if (!wait_warp(B.meta_empty + mr.idx, mr.phase ^ 1u, abort)) return;
+            uint8_t *meta = smem + C::OFF_META + mr.idx * C::META_STAGE;
             reinterpret_cast<float *>(meta + C::META_D)[t] = half_bits_to_float(h.x);
             reinterpret_cast<float *>(meta + C::META_DMIN)[t] = half_bits_to_float(h.x >> 16);
-        } else if (t < C::TN) {
-            reinterpret_cast<float *>(meta + C::META_DX)[t] = dx;
-        }
-        mbar_arrive(B.meta_full + mr.idx);
-        if (hh == 0) {
+            if (t < C::TN) reinterpret_cast<float *>(meta + C::META_DX)[t] = dx;
+            mbar_arrive(B.meta_full + mr.idx);
+        } else {
             const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);  // header bits 32..95
             uint32_t lo[4], hi[4];
 #pragma unroll
@@ -747,7 +746,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
             mbar_init(B.raw_empty + i, BLD_THREADS);
         }
         for (int i = 0; i < NSM; ++i) {
-            mbar_init(B.meta_full + i, BLD_THREADS);  // every builder thread writes one entry
+            mbar_init(B.meta_full + i, BLD_THREADS / 2);  // every hh = 1 builder thread
             mbar_init(B.meta_empty + i, C::EPI_ACTIVE);
         }
         mbar_init(B.fin, 1);
