@@ -454,7 +454,8 @@ def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak):
 
         t_a, _ = time_graph(capture(app), 20, 3)
         out[name] = {"scores_us": per * 1e6, "key_bytes": kbytes, "key_gbps": kbytes / per / 1e9,
-                     "frac": kbytes / per / 1e9 / hbm_peak, "append_us": t_a / (20 * layers) * 1e6}
+                     "frac": kbytes / per / 1e9 / hbm_peak, "append_us": t_a / (20 * layers) * 1e6,
+                     "traffic": kernel_traffic("kv_scores_q8_0") if t == gq.Q8_0 else None}
         del caches
         torch.cuda.empty_cache()
     return out
