@@ -65,6 +65,13 @@ constexpr unsigned FULL = 0xffffffffu;
 #ifndef GQ_GEMV_W_EVICT_FIRST
 #define GQ_GEMV_W_EVICT_FIRST 1
 #endif
+// R rows per item need at least warps / GQ_GEMV_R_SPREAD items: on a
+// 4096-row matrix, four-row items (one 9.2 KB copy per warp, some warps idle)
+// beat two-row items (two copies on most warps), since a warp completes only
+// about one bulk copy per 0.6 us.
+#ifndef GQ_GEMV_R_SPREAD
+#define GQ_GEMV_R_SPREAD 2
+#endif
 #ifndef GQ_GEMV_PREFETCH
 #define GQ_GEMV_PREFETCH 1
 #endif
@@ -1006,9 +1013,9 @@ size_t smem_bytes(const Geo &g, int nb, int nblk) {
 // Ring geometry for `rows` rows of `nblk` blocks streamed by `warps` warps.
 // Items are whole rows when two stages of one row per warp fit the ring
 // budget.  Then R is the most rows per bulk copy (up to 4) that still gives
-// every warp an item and keeps two stages per warp within the budget (bigger
-// copies stream better; spreading a short matrix over all warps finishes it
-// sooner).  Finally there are as many stages as the warp has items, within the
+// at least half the warps an item and keeps two stages per warp within the
+// budget (bigger copies stream better, and fewer copies per warp finish a
+// short matrix sooner).  Finally there are as many stages as the warp has items, within the
 // budget.
 template <int WT, int NW>
 Geo pick_geo(int rows, int nblk, int warps) {
@@ -1020,7 +1027,8 @@ Geo pick_geo(int rows, int nblk, int warps) {
     g.whole = (size_t)NW * 2 * (size_t)round16(row_bytes + 16) <= (size_t)RING_BUDGET ? 1 : 0;
     if (g.whole)
         for (int r = MAX_R; r > 1; r >>= 1)
-            if ((rows + r - 1) / r >= warps && (size_t)NW * 2 * (size_t)round16(r * row_bytes + 16) <= (size_t)RING_BUDGET) {
+            if ((rows + r - 1) / r * GQ_GEMV_R_SPREAD >= warps &&
+                (size_t)NW * 2 * (size_t)round16(r * row_bytes + 16) <= (size_t)RING_BUDGET) {
                 g.R = r;
                 break;
             }
