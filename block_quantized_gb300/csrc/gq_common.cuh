@@ -17,6 +17,7 @@ constexpr int Q4_0_BYTES = 18, Q8_0_BYTES = 34, Q4_K_BYTES = 144, Q8_K_BYTES = 2
 // Bits of the device status word (one per kernel family that waits).
 constexpr uint32_t STATUS_GEMV_TMA_TIMEOUT = 1u << 0;
 constexpr uint32_t STATUS_MMA_TIMEOUT = 1u << 1;
+constexpr uint32_t STATUS_KV_TMA_TIMEOUT = 1u << 2;
 
 // Poll limit for every mbarrier wait.  One try_wait may suspend the thread
 // for a while, so this bounds a wait well above any legitimate transfer time

@@ -11,8 +11,9 @@
 // Work split: one CTA per (256 positions, head); each warp takes 32
 // consecutive positions, whose key rows are one contiguous span (32 rows x
 // row_bytes, a multiple of 16 bytes).  The warp copies the span into shared
-// memory with coalesced 16-byte loads, then lane l computes the dot of row
-// p0 + l.  The query is quantized once per CTA (warp j: block j) with the
+// memory -- one bulk copy (TMA) when it is at least 4 KB, else coalesced
+// 16-byte loads, which measured faster for the 2.3 KB spans of 128-wide Q4_0
+// keys -- then lane l computes the dot of row p0 + l.  The query is quantized once per CTA (warp j: block j) with the
 // standalone quantizer's arithmetic, so its codes equal gq_quantize_rows'.
 #include "gq_common.cuh"
 #include "gq_internal.h"
@@ -51,25 +52,94 @@ __device__ __forceinline__ void lds_words_a2(const uint8_t *p, uint32_t (&w)[NW]
     for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(r[i], r[i + 1], sh);
 }
 
+// 32 bits at byte offset O of a row held as 64-bit words (O a compile-time
+// constant once the loops are unrolled).
+template <int O, int N64>
+__device__ __forceinline__ uint32_t row_u32(const uint64_t (&r)[N64]) {
+    constexpr int W = O / 8, B = O % 8;
+    if (B <= 4) return (uint32_t)(r[W] >> (8 * B));
+    return (uint32_t)((r[W] >> (8 * B)) | (r[W + 1] << (64 - 8 * B)));
+}
+
+// Dot of the key row (NB blocks, held as 64-bit words) with the query codes.
+template <int WT, int NB, int J = 0, int N64>
+__device__ __forceinline__ float row_dot(const uint64_t (&r)[N64], const int8_t (*qc)[32], const float *qd,
+                                         const int *qsum, float acc) {
+    if constexpr (J == NB) {
+        return acc;
+    } else {
+        constexpr int BB = WT == GQ_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES;
+        constexpr int O = J * BB;
+        const float dk = half_bits_to_float(row_u32<O, N64>(r) & 0xffffu);
+        const int *qw = reinterpret_cast<const int *>(qc[J]);
+        int s = 0;
+        if constexpr (WT == GQ_Q8_0) {
+            s = dp4a((int)row_u32<O + 2, N64>(r), qw[0], s);
+            s = dp4a((int)row_u32<O + 6, N64>(r), qw[1], s);
+            s = dp4a((int)row_u32<O + 10, N64>(r), qw[2], s);
+            s = dp4a((int)row_u32<O + 14, N64>(r), qw[3], s);
+            s = dp4a((int)row_u32<O + 18, N64>(r), qw[4], s);
+            s = dp4a((int)row_u32<O + 22, N64>(r), qw[5], s);
+            s = dp4a((int)row_u32<O + 26, N64>(r), qw[6], s);
+            s = dp4a((int)row_u32<O + 30, N64>(r), qw[7], s);
+        } else {
+            const uint32_t w0 = row_u32<O + 2, N64>(r), w1 = row_u32<O + 6, N64>(r);
+            const uint32_t w2 = row_u32<O + 10, N64>(r), w3 = row_u32<O + 14, N64>(r);
+            s = dp4a_us(w0 & NIB, qw[0], s);
+            s = dp4a_us((w0 >> 4) & NIB, qw[1], s);
+            s = dp4a_us(w1 & NIB, qw[2], s);
+            s = dp4a_us((w1 >> 4) & NIB, qw[3], s);
+            s = dp4a_us(w2 & NIB, qw[4], s);
+            s = dp4a_us((w2 >> 4) & NIB, qw[5], s);
+            s = dp4a_us(w3 & NIB, qw[6], s);
+            s = dp4a_us((w3 >> 4) & NIB, qw[7], s);
+            s -= 8 * qsum[J];
+        }
+        acc = fmaf(dk * qd[J], (float)s, acc);
+        return row_dot<WT, NB, J + 1>(r, qc, qd, qsum, acc);
+    }
+}
+
 // WT = GQ_Q8_0 or GQ_Q4_0 key blocks.  Q4_0 codes are c - 8 with c the stored
 // nibble (element 2j low, 2j + 1 high in byte j), so the block sum is
 // sum c a - 8 sum a; the query codes are kept split per group of eight as
 // (a0, a2, a4, a6 | a1, a3, a5, a7) so a nibble word feeds dp4a directly.
-template <int WT>
+// NBC = 4 or 8 (head_dim 128 or 256): rows are 8-byte aligned and each lane
+// reads its row with 64-bit shared-memory loads (conflict-free at 128),
+// block fields extracted by compile-time shifts; NBC = 0: any head_dim, block
+// fields read as funnel-shifted 32-bit words.
+template <int WT, int NBC>
 __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t *__restrict__ cache,
                                                                   const float *__restrict__ q,
                                                                   float *__restrict__ scores, int nb,
-                                                                  int capacity, int n_pos) {
+                                                                  int capacity, int n_pos,
+                                                                  uint32_t *__restrict__ status) {
     constexpr int BB = WT == GQ_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES;
     constexpr bool SPLIT = WT == GQ_Q4_0;
     extern __shared__ __align__(16) uint8_t kv_smem[];
     __shared__ __align__(16) int8_t qc[KV_MAX_NB][32];
     __shared__ float qd[KV_MAX_NB];
     __shared__ int qsum[KV_MAX_NB];
+    __shared__ uint64_t span_bar[KV_WARPS];
     const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_bytes = nb * BB;
+    const int p0 = (blockIdx.x * KV_WARPS + warp) * KV_POS;
+    const uint32_t span = (uint32_t)(KV_POS * row_bytes);  // a multiple of 16
+    const bool bulk = span >= 4096;
+    uint8_t *st = kv_smem + (size_t)warp * span;
+    if (lane == 0) {
+        mbar_init(span_bar + warp, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
     pdl_launch_dependents();
     pdl_wait();  // the cache and the query may come from the preceding kernels
+    // the 32 key rows of positions p0 .. p0 + 31 (inside the cache: capacity
+    // is a multiple of 32) into this warp's staging area, one bulk copy
+    if (bulk && lane == 0 && p0 < n_pos) {
+        mbar_arrive_expect_tx(span_bar + warp, span);
+        bulk_g2s(st, cache + ((size_t)h * capacity + p0) * row_bytes, span, span_bar + warp);
+    }
 
     // query block `warp`: amax, d = fp16(amax / 127), code = roundf(x / d)
     if (warp < nb) {
@@ -91,30 +161,46 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     }
     __syncthreads();
 
-    const int p0 = (blockIdx.x * KV_WARPS + warp) * KV_POS;
     if (p0 >= n_pos) return;
-    // the 32 key rows of positions p0 .. p0 + 31 (inside the cache: capacity
-    // is a multiple of 32) into this warp's staging area
-    const uint8_t *src = cache + ((size_t)h * capacity + p0) * row_bytes;
-    uint8_t *st = kv_smem + (size_t)warp * KV_POS * row_bytes;
-    const int nchunk = KV_POS * row_bytes / 16;
-    for (int c0 = 0; c0 < nchunk; c0 += 8 * 32) {
-        uint4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = c0 + u * 32 + lane;
-            if (c < nchunk) v[u] = ldg_nc_v4(src + (size_t)c * 16);
+    if (bulk) {
+        if (!mbar_wait_bounded(span_bar + warp, 0u)) {
+            // the copy never completed: flag it, give it one more bounded
+            // wait before the CTA may exit, and leave these scores unwritten
+            if (lane == 0) atomicOr(status, STATUS_KV_TMA_TIMEOUT);
+            mbar_wait_bounded(span_bar + warp, 0u);
+            return;
         }
+    } else {
+        const uint8_t *src = cache + ((size_t)h * capacity + p0) * row_bytes;
+        const int nchunk = (int)(span / 16);
+        for (int c0 = 0; c0 < nchunk; c0 += 8 * 32) {
+            uint4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = c0 + u * 32 + lane;
-            if (c < nchunk) reinterpret_cast<uint4 *>(st)[c] = v[u];
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < nchunk) v[u] = ldg_nc_v4(src + (size_t)c * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < nchunk) reinterpret_cast<uint4 *>(st)[c] = v[u];
+            }
         }
+        __syncwarp();
     }
-    __syncwarp();
 
     const uint8_t *row = st + lane * row_bytes;
     float acc = 0.0f;
+    if constexpr (NBC != 0) {
+        constexpr int N64 = NBC * BB / 8;
+        uint64_t r[N64];
+        const uint64_t *rp = reinterpret_cast<const uint64_t *>(row);
+#pragma unroll
+        for (int i = 0; i < N64; ++i) r[i] = rp[i];
+        acc = row_dot<WT, NBC>(r, qc, qd, qsum, 0.0f);
+        if (p0 + lane < n_pos) scores[(size_t)h * n_pos + p0 + lane] = acc;
+        return;
+    }
     for (int j = 0; j < nb; ++j) {
         const uint8_t *blk = row + j * BB;
         const float dk = half_bits_to_float(lds_u16(blk));
@@ -140,6 +226,18 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     if (p0 + lane < n_pos) scores[(size_t)h * n_pos + p0 + lane] = acc;
 }
 
+template <int WT, int NBC>
+cudaError_t launch_kv(dim3 grid, size_t smem, const LaunchCtx &ctx, const uint8_t *cache, const float *q,
+                      float *scores, int nb, int64_t capacity, int64_t n_pos) {
+    auto k = kv_scores_kernel<WT, NBC>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(k, grid, dim3(KV_WARPS * 32), smem, ctx.stream, cache, q, scores, nb, (int)capacity,
+                      (int)n_pos, ctx.status);
+}
+
 }  // namespace
 
 cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float *scores, int64_t n_heads,
@@ -151,22 +249,14 @@ cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float
     const dim3 grid((unsigned)((n_pos + KV_WARPS * KV_POS - 1) / (KV_WARPS * KV_POS)), (unsigned)n_heads);
     const uint8_t *c8 = static_cast<const uint8_t *>(cache);
     if (t == GQ_Q8_0) {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(kv_scores_kernel<GQ_Q8_0>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
-        return launch_pdl(kv_scores_kernel<GQ_Q8_0>, grid, dim3(KV_WARPS * 32), smem, ctx.stream, c8, q, scores,
-                          nb, (int)capacity, (int)n_pos);
+        if (nb == 4) return launch_kv<GQ_Q8_0, 4>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
+        if (nb == 8) return launch_kv<GQ_Q8_0, 8>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
+        return launch_kv<GQ_Q8_0, 0>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
     }
     if (t == GQ_Q4_0) {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(kv_scores_kernel<GQ_Q4_0>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
-        return launch_pdl(kv_scores_kernel<GQ_Q4_0>, grid, dim3(KV_WARPS * 32), smem, ctx.stream, c8, q, scores,
-                          nb, (int)capacity, (int)n_pos);
+        if (nb == 4) return launch_kv<GQ_Q4_0, 4>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
+        if (nb == 8) return launch_kv<GQ_Q4_0, 8>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
+        return launch_kv<GQ_Q4_0, 0>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
     }
     return cudaErrorInvalidValue;
 }
