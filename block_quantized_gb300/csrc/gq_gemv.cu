@@ -232,11 +232,6 @@ __device__ void stage_q8_0(const Act &a, const uint8_t *__restrict__ xq, int nbl
 // quantizers (round-to-nearest division, roundf, fp16 round-to-nearest for
 // the Q8_0 scale), so the codes equal theirs bit for bit.
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
-    return v;
-}
 
 __device__ __forceinline__ float clamp127(float v) {
     return v < -127.0f ? -127.0f : (v > 127.0f ? 127.0f : v);
