@@ -22,18 +22,22 @@
 // step, 28 warps:
 //   warps 0, 3 activation producers: one bulk copy each per super-block of
 //              the packed unit's half 0 (B stages 0-1) or half 1 (stages 2-3
-//              and the min-term B tile) into a 4-slot ring, two super-blocks
-//              ahead;
+//              and the min-term B tile) into a ring of NBSB super-blocks
+//              (4 / 3 / 2 for TN = 32 / 64 / 128);
 //   warp 1     MMA issuer (one thread) and tensor-memory owner;
 //   warp 2     weight producer: one 2-D tiled TMA load per super-block of
-//              the raw Q4_K rows, two super-blocks ahead (box 144 bytes x
+//              the raw Q4_K rows into a ring of NRAW stages (box 144 bytes x
 //              128 rows; rows past the matrix read as zeros);
 //   warps 4-11 A builders: two threads per weight row, each turning half of
 //              the raw super-block into fp16 sc*q and storing it straight
 //              from registers into tensor memory (tcgen05.st), where the MMA
-//              reads the A operand; then the row scales and min-term row
-//              (first half) or the column scales (second half);
-//   warps 12-27 epilogue: four threads per row, 32 columns each.
+//              reads the A operand; then the min-term row (first half) or
+//              the row and column scales (second half);
+//   warps 12-27 epilogue: four threads per row, 32 columns each (the warps
+//              whose columns lie past TN idle).
+// Per super-block a ready barrier (A and min-term rows built) and a done
+// barrier (one commit after its MMAs, which frees its S1/S2 for the
+// epilogue and its activation slots and min-term rows for reuse), in a ring.
 // Tensor memory (512 columns): the S1 accumulator, double-buffered by
 // super-block, and two or three buffers of the A operand.  The min-term step
 // writes S2 over the A buffer its super-block has just consumed, so the
