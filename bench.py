@@ -135,6 +135,36 @@ def main():
     run_gpu(args, world, rank)
 
 
+class Ranks:
+    """Replica bookkeeping for `--gpus N` (one process per GPU, no data-path
+    collective): a barrier, and the max over ranks of a duration -- the job
+    took as long as its slowest rank.  `dist` is torch.distributed after
+    init_process_group (nccl on GPUs, gloo in the CPU tests), or None for one
+    process; reductions run on `device`."""
+
+    def __init__(self, dist=None, device="cpu"):
+        self.dist = dist
+        self.device = device
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.dist is None:
+            return v
+        import torch
+        t = torch.tensor([v], device=self.device, dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds_max: float) -> float:
+    """Units per second of the whole job: every rank did units_per_rank in
+    its own time, and the slowest rank's time (max over ranks) counts."""
+    return world * units_per_rank / seconds_max
+
+
 # ---------------------------------------------------------------- CPU oracle
 
 def oracle_gemv_sample():
@@ -224,17 +254,13 @@ def run_gpu(args, world, rank):
     dev = torch.device("cuda", local)
     hbm_peak, bf16_peak, peak_src = measured_peaks()
 
+    ranks = Ranks(dist, dev)
+
     def barrier():
-        if dist is not None:
-            dist.barrier()
+        ranks.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(v: float) -> float:
-        if dist is None:
-            return v
-        t = torch.tensor([v], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = ranks.max
 
     s = torch.cuda.Stream(device=dev)
 
@@ -306,7 +332,7 @@ def run_gpu(args, world, rank):
     sampler = ClockSampler(local)
     t_total, clk = time_graph(step_graph, args.steps, max(3, args.warmup), sampler)
     ms_step = t_total / args.steps * 1e3
-    value = world * args.steps * COPIES * w_bytes / t_total / 1e9
+    value = whole_job_rate(args.steps * COPIES * w_bytes, world, t_total) / 1e9
     if not torch.isfinite(Y).all():
         raise RuntimeError("non-finite GEMV output")
 
