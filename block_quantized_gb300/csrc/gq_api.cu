@@ -301,6 +301,14 @@ gq_status gq_matmul_noalloc(gq_type wtype, const void *W, const void *xq, float 
 
 int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }
 
+gq_status gq_debug_kv_timeout(int on) {
+    LaunchCtx ctx;
+    gq_status st = make_ctx(nullptr, &ctx);
+    if (st != GQ_OK) return st;
+    cudaError_t e = kv_debug_timeout(on);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e);
+}
+
 }  // extern "C"
 
 namespace {

@@ -44,6 +44,8 @@ cudaError_t launch_quantize_rows_strided(gq_type t, const float *src, void *dst,
 
 // Quantized KV cache: scores[h][p] = dot of key row (h, p) of the cache with
 // the Q8_0-quantized query q[h], for p < n_pos.
+// Test switch of the scores kernel's timeout path (see gq_debug_kv_timeout).
+cudaError_t kv_debug_timeout(int on);
 cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float *scores, int64_t n_heads,
                              int64_t head_dim, int64_t capacity, int64_t n_pos, const LaunchCtx &ctx);
 

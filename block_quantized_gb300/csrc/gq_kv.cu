@@ -27,6 +27,14 @@ constexpr int KV_WARPS = 8;
 constexpr int KV_POS = 32;     // positions per warp
 constexpr int KV_MAX_NB = 8;   // head_dim <= 256
 
+// Test switch for the timeout path (set by gq_debug_kv_timeout): warp 0 of
+// every CTA expects 16 bytes more than its span copy delivers, so its
+// barrier never completes and its bounded wait -- shortened to
+// DEBUG_WAIT_LIMIT polls -- runs out.  The copy itself is the ordinary,
+// in-bounds one; nothing faults or hangs.
+__device__ uint32_t g_kv_debug_timeout = 0;
+constexpr uint32_t DEBUG_WAIT_LIMIT = 4096;
+
 __device__ __forceinline__ float warp_max32(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
@@ -136,8 +144,10 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     pdl_wait();  // the cache and the query may come from the preceding kernels
     // the 32 key rows of positions p0 .. p0 + 31 (inside the cache: capacity
     // is a multiple of 32) into this warp's staging area, one bulk copy
+    const bool starve = g_kv_debug_timeout != 0 && warp == 0;
+    const uint32_t limit = starve ? DEBUG_WAIT_LIMIT : WAIT_LIMIT;
     if (bulk && lane == 0 && p0 < n_pos) {
-        mbar_arrive_expect_tx(span_bar + warp, span);
+        mbar_arrive_expect_tx(span_bar + warp, span + (starve ? 16u : 0u));
         bulk_g2s(st, cache + ((size_t)h * capacity + p0) * row_bytes, span, span_bar + warp);
     }
 
@@ -163,11 +173,11 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
 
     if (p0 >= n_pos) return;
     if (bulk) {
-        if (!mbar_wait_bounded(span_bar + warp, 0u)) {
+        if (!mbar_wait_limit(span_bar + warp, 0u, limit)) {
             // the copy never completed: flag it, give it one more bounded
             // wait before the CTA may exit, and leave these scores unwritten
             if (lane == 0) atomicOr(status, STATUS_KV_TMA_TIMEOUT);
-            mbar_wait_bounded(span_bar + warp, 0u);
+            mbar_wait_limit(span_bar + warp, 0u, limit);
             return;
         }
     } else {
@@ -239,6 +249,11 @@ cudaError_t launch_kv(dim3 grid, size_t smem, const LaunchCtx &ctx, const uint8_
 }
 
 }  // namespace
+
+cudaError_t kv_debug_timeout(int on) {
+    const uint32_t v = on ? 1u : 0u;
+    return cudaMemcpyToSymbol(g_kv_debug_timeout, &v, sizeof(v));
+}
 
 cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float *scores, int64_t n_heads,
                              int64_t head_dim, int64_t capacity, int64_t n_pos, const LaunchCtx &ctx) {

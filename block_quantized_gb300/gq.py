@@ -53,6 +53,7 @@ SIGNATURES = {
     "gq_matmul_noalloc": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
     "gq_kv_append": ([_i32, _vp, _vp, _i64, _i64, _i64, _i64, _vp], _i32),
     "gq_kv_scores": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp], _i32),
+    "gq_debug_kv_timeout": ([_i32], _i32),
     "gq_tc_min_batch": ([], _i64),
     "gq_device_status": ([_u32p, _i32], _i32),
 }
@@ -215,6 +216,11 @@ def gq_kv_scores(t: int, cache, q, scores, n_heads: int, head_dim: int, capacity
                  stream=None) -> None:
     _check("gq_kv_scores", load().gq_kv_scores(t, _p(cache), _p(q), _p(scores), n_heads, head_dim, capacity,
                                                n_pos, _s(stream)))
+
+
+def gq_debug_kv_timeout(on: bool) -> None:
+    """Test switch: make gq_kv_scores' bounded waits run out (see gq.h)."""
+    _check("gq_debug_kv_timeout", load().gq_debug_kv_timeout(1 if on else 0))
 
 
 def gq_tc_min_batch() -> int:

@@ -105,6 +105,7 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert lib.gq_matmul(2, A16, A16, A16, 8, 256, 1, None) == CUDA
+    assert lib.gq_debug_kv_timeout(1) == CUDA
     assert lib.gq_last_cuda_error() != 0
     with pytest.raises(gq.GQError):
         gq.gq_matmul(2, A16, A16, A16, 8, 256, 1, stream=0)

@@ -122,3 +122,26 @@ def test_kv_scores_full_size_sampled():
     kh = host(keys)
     for p in pick[:4]:
         np.testing.assert_array_equal(ch[:, p], orc.quantize(t, kh[p]).reshape(n_heads, -1))
+
+
+def test_bounded_wait_runs_out_and_device_stays_usable():
+    """Failure detection without a fault: with the test switch on, one warp
+    per CTA waits on a barrier that expects 16 bytes more than its copy
+    delivers; its short bounded wait runs out, the status word says so, and
+    the next (normal) call on the same context is correct."""
+    t, n_heads, capacity, head_dim, n_pos = Q8_0, 2, 64, 128, 64
+    ref, cache = filled_cache(t, n_heads, capacity, head_dim, n_fill=n_pos, seed=5)
+    q = inputs.normal(inputs.rng(6), (n_heads, head_dim))
+    assert gq.gq_device_status(reset=True) == 0
+    gq.gq_debug_kv_timeout(True)
+    try:
+        gq.kv_scores(t, cache, dev(q), n_pos)
+        torch.cuda.synchronize()
+        word = gq.gq_device_status(reset=True)
+    finally:
+        gq.gq_debug_kv_timeout(False)
+    assert word & (1 << 2), word  # the KV transfer-timeout bit
+    s = host(gq.kv_scores(t, cache, dev(q), n_pos))
+    S, T = orc.kv_scores_ref(t, ref, q, n_pos)
+    assert_close(s, S, T)
+    assert gq.gq_device_status(reset=True) == 0
