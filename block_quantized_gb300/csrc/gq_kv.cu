@@ -15,6 +15,8 @@
 // 16-byte loads, which measured faster for the 2.3 KB spans of 128-wide Q4_0
 // keys -- then lane l computes the dot of row p0 + l.  The query is quantized once per CTA (warp j: block j) with the
 // standalone quantizer's arithmetic, so its codes equal gq_quantize_rows'.
+#include <atomic>
+
 #include "gq_common.cuh"
 #include "gq_internal.h"
 
@@ -27,12 +29,12 @@ constexpr int KV_WARPS = 8;
 constexpr int KV_POS = 32;     // positions per warp
 constexpr int KV_MAX_NB = 8;   // head_dim <= 256
 
-// Test switch for the timeout path (set by gq_debug_kv_timeout): warp 0 of
-// every CTA expects 16 bytes more than its span copy delivers, so its
-// barrier never completes and its bounded wait -- shortened to
-// DEBUG_WAIT_LIMIT polls -- runs out.  The copy itself is the ordinary,
-// in-bounds one; nothing faults or hangs.
-__device__ uint32_t g_kv_debug_timeout = 0;
+// Test switch for the timeout path (set by gq_debug_kv_timeout, passed to
+// the kernel as an argument): warp 0 of every CTA expects 16 bytes more than
+// its span copy delivers, so its barrier never completes and its bounded
+// wait -- shortened to DEBUG_WAIT_LIMIT polls -- runs out.  The copy itself
+// is the ordinary, in-bounds one; nothing faults or hangs.
+std::atomic<int> g_kv_debug_timeout{0};
 constexpr uint32_t DEBUG_WAIT_LIMIT = 4096;
 
 __device__ __forceinline__ float warp_max32(float v) {
@@ -121,7 +123,8 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
                                                                   const float *__restrict__ q,
                                                                   float *__restrict__ scores, int nb,
                                                                   int capacity, int n_pos,
-                                                                  uint32_t *__restrict__ status) {
+                                                                  uint32_t *__restrict__ status,
+                                                                  int debug_starve) {
     constexpr int BB = WT == GQ_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES;
     constexpr bool SPLIT = WT == GQ_Q4_0;
     extern __shared__ __align__(16) uint8_t kv_smem[];
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     pdl_wait();  // the cache and the query may come from the preceding kernels
     // the 32 key rows of positions p0 .. p0 + 31 (inside the cache: capacity
     // is a multiple of 32) into this warp's staging area, one bulk copy
-    const bool starve = g_kv_debug_timeout != 0 && warp == 0;
+    const bool starve = debug_starve != 0 && warp == 0;
     const uint32_t limit = starve ? DEBUG_WAIT_LIMIT : WAIT_LIMIT;
     if (bulk && lane == 0 && p0 < n_pos) {
         mbar_arrive_expect_tx(span_bar + warp, span + (starve ? 16u : 0u));
@@ -245,14 +248,14 @@ cudaError_t launch_kv(dim3 grid, size_t smem, const LaunchCtx &ctx, const uint8_
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(k, grid, dim3(KV_WARPS * 32), smem, ctx.stream, cache, q, scores, nb, (int)capacity,
-                      (int)n_pos, ctx.status);
+                      (int)n_pos, ctx.status, g_kv_debug_timeout.load());
 }
 
 }  // namespace
 
 cudaError_t kv_debug_timeout(int on) {
-    const uint32_t v = on ? 1u : 0u;
-    return cudaMemcpyToSymbol(g_kv_debug_timeout, &v, sizeof(v));
+    g_kv_debug_timeout.store(on ? 1 : 0);
+    return cudaSuccess;
 }
 
 cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float *scores, int64_t n_heads,

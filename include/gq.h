@@ -319,13 +319,13 @@ gq_status gq_kv_scores(gq_type type, const void *cache, const float *q, float *s
                        int64_t head_dim, int64_t capacity, int64_t n_pos, gq_stream_t stream);
 
 /* Test switch for the device timeout path (not for production use).  With
- * on != 0, subsequent gq_kv_scores launches on the current device make one
+ * on != 0, subsequent gq_kv_scores launches (process-wide) make one
  * warp per CTA wait, with a short poll limit, on a transfer barrier that
  * expects 16 bytes more than its copy delivers: the wait runs out, those
  * scores are left unwritten and gq_device_status() reports GQ_ERR_TIMEOUT.
  * Nothing faults or hangs, and the device stays usable.  on = 0 restores
  * normal operation.  Applies to key spans of 4 KB or more (Q8_0 keys at
- * head_dim >= 128).  Returns GQ_ERR_CUDA if the switch cannot be written. */
+ * head_dim >= 128).  Returns GQ_ERR_CUDA without a usable CUDA device. */
 gq_status gq_debug_kv_timeout(int on);
 
 /* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
