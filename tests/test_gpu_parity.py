@@ -119,7 +119,7 @@ SHAPES = [
     # rows, cols, batch -- several CTAs, a ragged row tail, chunk tails
     (1, 256, 1), (7, 256, 1), (8, 512, 1), (37, 1024, 1), (130, 4096, 1),
     (64, 11008, 1), (19, 2816, 3), (40, 4096, 2), (33, 768, 5), (24, 1280, 8),
-    (17, 512, 13), (9, 4352, 16),
+    (17, 512, 13), (9, 4352, 16), (21, 1024, 65),
 ]
 
 
