@@ -1068,8 +1068,12 @@ cudaError_t launch_one(const void *W, const void *act, float *y, int32_t *sums, 
                       y, sums, rows, nblk, batch, w_static, geo, ctx.status);
 }
 
-// Largest batch chunk in {8, 4, 2, 1} not above `batch` whose staged
-// activations fit in shared memory next to a one-stage ring; 0 if none fits.
+// Vectors per launch chunk: the smallest of {1, 2, 4, 8} that covers the
+// batch, so a batch of up to 8 streams the weights once (a batch of 3 runs as
+// one chunk of 4 with the last slot unused, not as 2 + 1 with two passes);
+// larger batches take chunks of 8.  A smaller chunk is taken when the staged
+// activations would not fit in shared memory next to a one-stage ring; 0 if
+// none fits.
 template <int WT>
 int pick_nb(int batch, int nblk) {
     using F = Fmt<WT>;
@@ -1078,8 +1082,14 @@ int pick_nb(int batch, int nblk) {
     g1.ns = 1;
     g1.whole = 0;
     g1.stage_bytes = round16((size_t)F::CH * F::BB + 16);
-    for (int nb = 8; nb >= 1; nb >>= 1)
-        if (nb <= std::max(batch, 1) && smem_bytes<WT, WARPS>(g1, nb, nblk) <= (size_t)SMEM_MAX) return nb;
+    int want = 8;
+    for (int nb = 1; nb <= 8; nb <<= 1)
+        if (nb >= batch) {
+            want = nb;
+            break;
+        }
+    for (int nb = want; nb >= 1; nb >>= 1)
+        if (smem_bytes<WT, WARPS>(g1, nb, nblk) <= (size_t)SMEM_MAX) return nb;
     return 0;
 }
 
