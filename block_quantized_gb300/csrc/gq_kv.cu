@@ -118,7 +118,7 @@ __device__ __forceinline__ float row_dot(const uint64_t (&r)[N64], const int8_t 
 // reads its row with 64-bit shared-memory loads (conflict-free at 128),
 // block fields extracted by compile-time shifts; NBC = 0: any head_dim, block
 // fields read as funnel-shifted 32-bit words.
-template <int WT, int NBC>
+template <int WT, int NBC, int PW>
 __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t *__restrict__ cache,
                                                                   const float *__restrict__ q,
                                                                   float *__restrict__ scores, int nb,
@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     __shared__ uint64_t span_bar[KV_WARPS];
     const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_bytes = nb * BB;
-    const int p0 = (blockIdx.x * KV_WARPS + warp) * KV_POS;
-    const uint32_t span = (uint32_t)(KV_POS * row_bytes);  // a multiple of 16
+    const int p0 = (blockIdx.x * KV_WARPS + warp) * PW;
+    const uint32_t span = (uint32_t)(PW * row_bytes);  // a multiple of 16
     const bool bulk = span >= 4096;
     uint8_t *st = kv_smem + (size_t)warp * span;
     if (lane == 0) {
@@ -145,8 +145,9 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     __syncwarp();
     pdl_launch_dependents();
     pdl_wait();  // the cache and the query may come from the preceding kernels
-    // the 32 key rows of positions p0 .. p0 + 31 (inside the cache: capacity
-    // is a multiple of 32) into this warp's staging area, one bulk copy
+    // the PW key rows of positions p0 .. p0 + PW - 1 (inside the cache:
+    // capacity is a multiple of PW) into this warp's staging area, one bulk
+    // copy
     const bool starve = debug_starve != 0 && warp == 0;
     const uint32_t limit = starve ? DEBUG_WAIT_LIMIT : WAIT_LIMIT;
     if (bulk && lane == 0 && p0 < n_pos) {
@@ -202,53 +203,68 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
         __syncwarp();
     }
 
-    const uint8_t *row = st + lane * row_bytes;
-    float acc = 0.0f;
-    if constexpr (NBC != 0) {
-        constexpr int N64 = NBC * BB / 8;
-        uint64_t r[N64];
-        const uint64_t *rp = reinterpret_cast<const uint64_t *>(row);
 #pragma unroll
-        for (int i = 0; i < N64; ++i) r[i] = rp[i];
-        acc = row_dot<WT, NBC>(r, qc, qd, qsum, 0.0f);
-        if (p0 + lane < n_pos) scores[(size_t)h * n_pos + p0 + lane] = acc;
-        return;
-    }
-    for (int j = 0; j < nb; ++j) {
-        const uint8_t *blk = row + j * BB;
-        const float dk = half_bits_to_float(lds_u16(blk));
-        const int *qw = reinterpret_cast<const int *>(qc[j]);
-        int s = 0;
-        if (WT == GQ_Q8_0) {
-            uint32_t w[8];
-            lds_words_a2<8>(blk + 2, w);
+    for (int rr = 0; rr < PW / 32; ++rr) {  // lane scores rows lane, lane + 32, ...
+        const int pr = lane + 32 * rr;
+        const uint8_t *row = st + pr * row_bytes;
+        float acc = 0.0f;
+        if constexpr (NBC != 0) {
+            constexpr int N64 = NBC * BB / 8;
+            uint64_t r[N64];
+            const uint64_t *rp = reinterpret_cast<const uint64_t *>(row);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s = dp4a((int)w[k], qw[k], s);
+            for (int i = 0; i < N64; ++i) r[i] = rp[i];
+            acc = row_dot<WT, NBC>(r, qc, qd, qsum, 0.0f);
         } else {
-            uint32_t w[4];
-            lds_words_a2<4>(blk + 2, w);  // word k: elements 8k .. 8k + 7
+            for (int j = 0; j < nb; ++j) {
+                const uint8_t *blk = row + j * BB;
+                const float dk = half_bits_to_float(lds_u16(blk));
+                const int *qw = reinterpret_cast<const int *>(qc[j]);
+                int s = 0;
+                if (WT == GQ_Q8_0) {
+                    uint32_t w[8];
+                    lds_words_a2<8>(blk + 2, w);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                s = dp4a_us(w[k] & NIB, qw[2 * k], s);
-                s = dp4a_us((w[k] >> 4) & NIB, qw[2 * k + 1], s);
+                    for (int k = 0; k < 8; ++k) s = dp4a((int)w[k], qw[k], s);
+                } else {
+                    uint32_t w[4];
+                    lds_words_a2<4>(blk + 2, w);  // word k: elements 8k .. 8k + 7
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        s = dp4a_us(w[k] & NIB, qw[2 * k], s);
+                        s = dp4a_us((w[k] >> 4) & NIB, qw[2 * k + 1], s);
+                    }
+                    s -= 8 * qsum[j];
+                }
+                acc = fmaf(dk * qd[j], (float)s, acc);
             }
-            s -= 8 * qsum[j];
         }
-        acc = fmaf(dk * qd[j], (float)s, acc);
+        if (p0 + pr < n_pos) scores[(size_t)h * n_pos + p0 + pr] = acc;
     }
-    if (p0 + lane < n_pos) scores[(size_t)h * n_pos + p0 + lane] = acc;
 }
 
-template <int WT, int NBC>
-cudaError_t launch_kv(dim3 grid, size_t smem, const LaunchCtx &ctx, const uint8_t *cache, const float *q,
-                      float *scores, int nb, int64_t capacity, int64_t n_pos) {
-    auto k = kv_scores_kernel<WT, NBC>;
+template <int WT, int NBC, int PW>
+cudaError_t launch_kv1(size_t row_bytes, int64_t n_heads, const LaunchCtx &ctx, const uint8_t *cache,
+                       const float *q, float *scores, int nb, int64_t capacity, int64_t n_pos) {
+    auto k = kv_scores_kernel<WT, NBC, PW>;
+    const size_t smem = (size_t)KV_WARPS * PW * row_bytes + 16;  // + tail pad for the word reads
+    const dim3 grid((unsigned)((n_pos + KV_WARPS * PW - 1) / (KV_WARPS * PW)), (unsigned)n_heads);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(k, grid, dim3(KV_WARPS * 32), smem, ctx.stream, cache, q, scores, nb, (int)capacity,
                       (int)n_pos, ctx.status, g_kv_debug_timeout.load());
+}
+
+// Positions per warp: 64 when a 32-row span is under 4 KB (so the bulk copy
+// applies) and the capacity allows whole 64-row spans, else 32.
+template <int WT, int NBC>
+cudaError_t launch_kv(size_t row_bytes, int64_t n_heads, const LaunchCtx &ctx, const uint8_t *cache,
+                      const float *q, float *scores, int nb, int64_t capacity, int64_t n_pos) {
+    if (KV_POS * row_bytes < 4096 && capacity % (2 * KV_POS) == 0)
+        return launch_kv1<WT, NBC, 2 * KV_POS>(row_bytes, n_heads, ctx, cache, q, scores, nb, capacity, n_pos);
+    return launch_kv1<WT, NBC, KV_POS>(row_bytes, n_heads, ctx, cache, q, scores, nb, capacity, n_pos);
 }
 
 }  // namespace
@@ -262,19 +278,17 @@ cudaError_t launch_kv_scores(gq_type t, const void *cache, const float *q, float
                              int64_t head_dim, int64_t capacity, int64_t n_pos, const LaunchCtx &ctx) {
     const int nb = (int)(head_dim / 32);
     if (nb < 1 || nb > KV_MAX_NB || capacity % KV_POS != 0 || n_heads > 65535) return cudaErrorInvalidValue;
-    const int bb = t == GQ_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES;
-    const size_t smem = (size_t)KV_WARPS * KV_POS * nb * bb + 16;  // + tail pad for the word reads
-    const dim3 grid((unsigned)((n_pos + KV_WARPS * KV_POS - 1) / (KV_WARPS * KV_POS)), (unsigned)n_heads);
+    const size_t rb = (size_t)nb * (t == GQ_Q8_0 ? Q8_0_BYTES : Q4_0_BYTES);
     const uint8_t *c8 = static_cast<const uint8_t *>(cache);
     if (t == GQ_Q8_0) {
-        if (nb == 4) return launch_kv<GQ_Q8_0, 4>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
-        if (nb == 8) return launch_kv<GQ_Q8_0, 8>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
-        return launch_kv<GQ_Q8_0, 0>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
+        if (nb == 4) return launch_kv<GQ_Q8_0, 4>(rb, n_heads, ctx, c8, q, scores, nb, capacity, n_pos);
+        if (nb == 8) return launch_kv<GQ_Q8_0, 8>(rb, n_heads, ctx, c8, q, scores, nb, capacity, n_pos);
+        return launch_kv<GQ_Q8_0, 0>(rb, n_heads, ctx, c8, q, scores, nb, capacity, n_pos);
     }
     if (t == GQ_Q4_0) {
-        if (nb == 4) return launch_kv<GQ_Q4_0, 4>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
-        if (nb == 8) return launch_kv<GQ_Q4_0, 8>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
-        return launch_kv<GQ_Q4_0, 0>(grid, smem, ctx, c8, q, scores, nb, capacity, n_pos);
+        if (nb == 4) return launch_kv<GQ_Q4_0, 4>(rb, n_heads, ctx, c8, q, scores, nb, capacity, n_pos);
+        if (nb == 8) return launch_kv<GQ_Q4_0, 8>(rb, n_heads, ctx, c8, q, scores, nb, capacity, n_pos);
+        return launch_kv<GQ_Q4_0, 0>(rb, n_heads, ctx, c8, q, scores, nb, capacity, n_pos);
     }
     return cudaErrorInvalidValue;
 }
