@@ -116,7 +116,8 @@ gq_status check_matmul(gq_type wtype, const void *W, const void *xq, const void 
     return GQ_OK;
 }
 
-int64_t tc_min_batch_value() {
+// GQ_TC_MIN_BATCH from the environment (read once), 0 when unset or invalid.
+int64_t tc_min_batch_env() {
     static int64_t v = []() -> int64_t {
         const char *s = std::getenv("GQ_TC_MIN_BATCH");
         if (s && *s) {
@@ -124,9 +125,22 @@ int64_t tc_min_batch_value() {
             long long x = std::strtoll(s, &end, 10);
             if (end && *end == '\0' && x > 0) return (int64_t)x;
         }
-        return 16;
+        return 0;
     }();
     return v;
+}
+
+int64_t tc_min_batch_value() { return tc_min_batch_env() ? tc_min_batch_env() : 16; }
+
+// GQ_PATH_AUTO's choice of the tensor-core kernel for Q4_K.  Measured on
+// 14336 x 4096: the tensor-core product takes about the same time at any
+// batch up to 64 (its row tiles run side by side), while the GEMV grows with
+// every vector, so the tensor path wins from batch 9 on matrices of 14336
+// rows or more and from batch 16 on the rest.  GQ_TC_MIN_BATCH replaces the
+// rule by a plain threshold.
+bool tc_auto(int64_t rows, int64_t batch) {
+    if (tc_min_batch_env()) return batch >= tc_min_batch_env();
+    return batch >= 16 || (batch >= 9 && rows >= 14336);
 }
 
 // One product call.  act is xq (quantized blocks) or, with fused_f32, fp32
@@ -154,7 +168,7 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
     bool use_mma = path == GQ_PATH_MMA;
     if (path == GQ_PATH_AUTO)
-        use_mma = !fused_f32 && wtype == GQ_Q4_K && batch >= tc_min_batch_value() &&
+        use_mma = !fused_f32 && wtype == GQ_Q4_K && tc_auto(rows, batch) &&
                   mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
     if (!use_mma && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;

@@ -204,7 +204,9 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * least gq_matmul_workspace_bytes bytes, owned by the caller, contents
  * overwritten; calls that share a workspace must not overlap on the GPU).
  * GQ_PATH_AUTO runs the tcgen05 tensor-core kernel for Q4_K when batch >=
- * gq_tc_min_batch() and the workspace suffices, the GEMV kernels otherwise.
+ * gq_tc_min_batch(), or batch >= 9 on matrices of 14336 rows or more (the
+ * measured crossovers), and the workspace suffices; the GEMV kernels
+ * otherwise.  With GQ_TC_MIN_BATCH set, batch >= that value alone decides.
  * The tensor-core path computes the same y (within the tolerance above); its
  * integer super-block sums S1 are exact while partial sums of one super-block
  * stay below 2^24 in magnitude (always, unless codes and scales sit at their
@@ -329,8 +331,10 @@ gq_status gq_kv_scores(gq_type type, const void *cache, const float *q, float *s
 gq_status gq_debug_kv_timeout(int on);
 
 /* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
- * Q4_K (the measured crossover; the environment variable GQ_TC_MIN_BATCH,
- * read once, overrides it). */
+ * Q4_K at any row count (16, the measured crossover for the smaller
+ * matrices; from batch 9 it does so on matrices of 14336 rows or more).  The
+ * environment variable GQ_TC_MIN_BATCH, read once, replaces both with a
+ * plain threshold, which this then returns. */
 int64_t gq_tc_min_batch(void);
 
 /*

@@ -1,6 +1,8 @@
 """GPU parity of the tcgen05 tensor-core path (Q4_K x Q8_K, batched) against
 the CPU oracle: integer super-block sums S1 / S2 bit-identical, y within
 1e-4 * sum|terms|, and the same y as the GEMV path within that tolerance."""
+import os
+
 import numpy as np
 import pytest
 
@@ -125,3 +127,19 @@ def test_mma_full_size(rows, cols, batch):
     Xq = orc.quantize(Q8_K, X)
     y_ref, T = orc.matmul_ref(Q4_K, Wq_s, Xq, len(idx), cols, batch, nthreads=orc.max_threads())
     assert_close(y[:, idx], y_ref, T)
+
+
+@pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
+@pytest.mark.parametrize("rows,batch,want", [(14336, 9, "mma"), (4096, 9, "gemv"), (4096, 16, "mma"),
+                                             (14336, 8, "gemv")])
+def test_auto_dispatch_rule(rows, batch, want):
+    """GQ_PATH_AUTO: the tensor-core kernel from batch 9 on 14336 rows or
+    more, from batch 16 otherwise.  Both kernel families are deterministic, so
+    the AUTO result equals the chosen family's bit for bit."""
+    cols = 1024
+    g = inputs.rng(rows + batch)
+    Wd = gq.quantize(Q4_K, torch.from_numpy(inputs.normal(g, (rows, cols), 0.02)).cuda())
+    Xd = gq.quantize(Q8_K, torch.from_numpy(inputs.normal(g, (batch, cols))).cuda())
+    y_auto = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_AUTO))
+    y_want = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA if want == "mma" else gq.PATH_GEMV))
+    assert y_auto.tobytes() == y_want.tobytes()
