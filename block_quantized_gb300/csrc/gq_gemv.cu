@@ -9,14 +9,16 @@
 // integers (sc_j * s_j, m_j * t_j) before one float scaling per super-block.
 // Token generation is bound by memory bandwidth ("llama.cpp 推理引擎" §7.3),
 // so the kernels are built to stream the weights once at HBM speed:
-//   - a persistent grid of one CTA per SM; every warp owns whole row groups
-//     (grid-stride) and streams them through its own shared-memory ring,
-//     filled by the TMA engine (cp.async.bulk, completion on an mbarrier,
-//     every wait bounded).  A ring item is up to four whole rows in one bulk
-//     copy (9 KB at 4096 columns) when a row fits in one 16-super-block
-//     chunk, else one chunk of one row; the ring depth per warp is chosen per
-//     launch so a small matrix is requested in full before the dependency
-//     wait and a tall one keeps ~150 KB per SM in flight;
+//   - a persistent grid of at most one CTA per SM; every warp owns whole row
+//     groups (grid-stride) and streams them through its own shared-memory
+//     ring, filled by the TMA engine (cp.async.bulk with an evict-first L2
+//     policy, completion on an mbarrier, every wait bounded).  A ring item
+//     is R whole rows in one bulk copy (R <= 4; 9.2 KB for four 4096-column
+//     rows) when two such items per warp fit the ring budget, else one
+//     16-super-block chunk of one row.  The ring depth is chosen per launch
+//     (a tall matrix keeps ~150 KB per SM in flight); the first stage is
+//     requested before the dependency wait, the rest once the activations
+//     are staged;
 //   - the CTA's activation vectors are staged once in shared memory, each
 //     group of 8 int8 codes stored as (a0,a2,a4,a6 | a1,a3,a5,a7) so a
 //     packed nibble word w feeds dp4a as (w & 0x0F0F0F0F) and
