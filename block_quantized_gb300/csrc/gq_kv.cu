@@ -8,12 +8,13 @@
 // Cache layout: [n_heads][capacity][head_dim / 32] blocks; key row (h, p) is
 // head_dim / 32 consecutive blocks, rows of a head are consecutive.
 //
-// Work split: one CTA per (256 positions, head); each warp takes 32
-// consecutive positions, whose key rows are one contiguous span (32 rows x
-// row_bytes, a multiple of 16 bytes).  The warp copies the span into shared
-// memory -- one bulk copy (TMA) when it is at least 4 KB, else coalesced
-// 16-byte loads, which measured faster for the 2.3 KB spans of 128-wide Q4_0
-// keys -- then lane l computes the dot of row p0 + l.  The query is quantized once per CTA (warp j: block j) with the
+// Work split: one CTA per (8 x PW positions, head); each warp takes PW
+// consecutive positions (PW = 32, or 64 when 32 rows are under 4 KB and the
+// capacity is a multiple of 64), whose key rows are one contiguous span (PW
+// rows x row_bytes, a multiple of 16 bytes).  The warp copies the span into
+// shared memory -- one bulk copy (TMA) when it is at least 4 KB, else
+// coalesced 16-byte loads -- then lane l computes the dots of rows l, l + 32,
+// ... of the span.  The query is quantized once per CTA (warp j: block j) with the
 // standalone quantizer's arithmetic, so its codes equal gq_quantize_rows'.
 #include <atomic>
 
