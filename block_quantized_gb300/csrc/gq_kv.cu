@@ -14,8 +14,9 @@
 // rows x row_bytes, a multiple of 16 bytes).  The warp copies the span into
 // shared memory -- one bulk copy (TMA) when it is at least 4 KB, else
 // coalesced 16-byte loads -- then lane l computes the dots of rows l, l + 32,
-// ... of the span.  The query is quantized once per CTA (warp j: block j) with the
-// standalone quantizer's arithmetic, so its codes equal gq_quantize_rows'.
+// ... of the span.  The query is quantized once per CTA (warp j: block j)
+// with the standalone quantizer's arithmetic, so its codes equal
+// gq_quantize_rows'.
 #include <atomic>
 
 #include "gq_common.cuh"
