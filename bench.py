@@ -9,12 +9,17 @@ Headline (one JSON line on stdout, rank 0):
           weights per step is larger than L2, so no step is served from L2.
   value   weight bytes streamed per second over the timed steps (device
           resident inputs; CUDA-event timing of a CUDA graph of the step).
-Also in the line: roofline of the GEMV kernel, the 7B-shape decode sweep
-(tok/s), the batch sweep on 14336x4096, the 512-column prefill GEMM, the
-end-to-end figure with host buffers, the CPU oracle baseline, and the SM
-clocks sampled during the timed region.
+Also in the line: roofline of the GEMV kernel (with its ncu DRAM traffic
+when the kernel source matches the committed capture), the one-launch
+streaming point, the unfused step, the end-to-end figure with host buffers,
+the 7B-shape decode (tok/s), the batch sweep on 14336x4096 through both
+kernel families, the 512-column prefill GEMM, the quantized KV cache
+(scores and append), the CPU oracle baseline (all cores and one core), the
+number of library kernel launches in the timed region, and the SM clocks
+sampled during it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
+                  [--only prefill|sweep|decode|stream|kv] [--no-cpu]
 """
 from __future__ import annotations
 
