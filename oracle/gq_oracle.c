@@ -39,7 +39,11 @@
  *     below always cover the sub-block's range.
  *   - Q4_K: non-iterative min/max fit (the asymmetric formula of [P2] §5.2
  *     with the minimum clamped to <= 0 because the min term is subtracted).
- *   - A zero scale yields zero codes (Q4_0 code 8).
+ *   - Q6_K (6-bit K blocks, no sub-blocks, as the discosf.com page's §4
+ *     describes them): symmetric rule with scale = max|x| / 31, codes
+ *     c = q + 32 with q clamped to [-32, 31]; layout this library's own (see
+ *     quantize_q6_k_block).  It pairs with Q8_K activations.
+ *   - A zero scale yields zero codes (Q4_0 code 8, Q6_K code 32).
  *   - Non-finite inputs are rejected (return -2).
  *
  * parity pins: every function here is pinned by tests under tests/ that do
@@ -54,7 +58,7 @@
 #endif
 
 /* Type codes, in the order of the public type enumeration. */
-enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q8_K = 3 };
+enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q8_K = 3, OR_Q6_K = 4 };
 
 /* ------------------------------------------------------------------ */
 /* Bit-level helpers                                                    */
@@ -186,7 +190,7 @@ int64_t or_block_elems(int type)
 {
     switch (type) {
     case OR_Q4_0: case OR_Q8_0: return 32;
-    case OR_Q4_K: case OR_Q8_K: return 256;
+    case OR_Q4_K: case OR_Q8_K: case OR_Q6_K: return 256;
     }
     return -1;
 }
@@ -195,7 +199,9 @@ int64_t or_block_elems(int type)
  * Q8_0: fp16 d + 32 int8.
  * Q4_K: fp16 d, fp16 dmin, 12 bytes of 6-bit scales/mins, 128 bytes of
  *       nibbles.
- * Q8_K: fp32 d, 256 int8, eight int16 sub-block sums. */
+ * Q8_K: fp32 d, 256 int8, eight int16 sub-block sums.
+ * Q6_K: fp16 d, 128 bytes holding the low four bits of the 256 codes, 64
+ *       bytes holding their top two bits. */
 int64_t or_block_bytes(int type)
 {
     switch (type) {
@@ -203,6 +209,7 @@ int64_t or_block_bytes(int type)
     case OR_Q8_0: return 2 + 32;
     case OR_Q4_K: return 2 + 2 + 12 + 128;
     case OR_Q8_K: return 4 + 256 + 2 * 8;
+    case OR_Q6_K: return 2 + 128 + 64;
     }
     return -1;
 }
@@ -373,6 +380,50 @@ static void quantize_q8_k_block(const float *x, uint8_t *blk)
     }
 }
 
+/* Q6_K: the 6-bit K-quant as the discosf.com page ("为什么说 llama.cpp
+ * 是'裸引擎'——从模型加载的每一行代码说起", §4 量化不是"压缩"，而是"精度重分配")
+ * describes it: K blocks only (256 elements, the K-quant block of [P4]
+ * 第二层：量化引擎), no sub-blocks, 6-bit main quantization.  The pages give
+ * no formula or layout; the reading taken is the symmetric rule of [P2]
+ * §5.1 with b = 6 (scale = max|x| / 31, fp16
+ * rounded to nearest-even, the same pattern as Q4_0 with b = 4), codes
+ * q = round(x / d) clamped to [-32, 31] and stored as c = q + 32 in [0, 63].
+ * Packing (this library's own): byte l of the 128-byte low part holds the low
+ * four bits of element 2l (low nibble) and 2l+1 (high nibble), the Q4_0 / Q4_K
+ * order; byte l of the 64-byte high part holds the top two bits of elements
+ * 4l..4l+3, element 4l+k in bits 2k..2k+1.  w = d * (c - 32). */
+static void quantize_q6_k_block(const float *x, uint8_t *blk)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 256; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    uint16_t dh = or_f16_rn(amax / 31.0f);
+    float d = or_f16_to_f32(dh);
+    put_u16(blk, dh);
+    uint8_t c[256];
+    for (int i = 0; i < 256; i++) {
+        float q = (d == 0.0f) ? 0.0f : clampf(rha(x[i] / d), -32.0f, 31.0f);
+        c[i] = (uint8_t)((int)q + 32);
+    }
+    for (int l = 0; l < 128; l++)
+        blk[2 + l] = (uint8_t)((c[2 * l] & 15) | ((c[2 * l + 1] & 15) << 4));
+    for (int l = 0; l < 64; l++) {
+        int h = 0;
+        for (int k = 0; k < 4; k++) h |= (c[4 * l + k] >> 4) << (2 * k);
+        blk[130 + l] = (uint8_t)h;
+    }
+}
+
+/* The stored 6-bit code of element e of a Q6_K block (0..63). */
+static int q6_k_code(const uint8_t *blk, int e)
+{
+    int lo = (e & 1) ? (blk[2 + e / 2] >> 4) : (blk[2 + e / 2] & 15);
+    int hi = (blk[130 + e / 4] >> (2 * (e & 3))) & 3;
+    return lo | (hi << 4);
+}
+
 int or_quantize(int type, const float *x, uint8_t *dst, int64_t n)
 {
     int64_t be = or_block_elems(type), bb = or_block_bytes(type);
@@ -386,6 +437,7 @@ int or_quantize(int type, const float *x, uint8_t *dst, int64_t n)
         case OR_Q8_0: quantize_q8_0_block(xb, ob); break;
         case OR_Q4_K: quantize_q4_k_block(xb, ob); break;
         case OR_Q8_K: quantize_q8_k_block(xb, ob); break;
+        case OR_Q6_K: quantize_q6_k_block(xb, ob); break;
         }
     }
     return 0;
@@ -397,6 +449,7 @@ int or_quantize(int type, const float *x, uint8_t *dst, int64_t n)
 
 /* Per-element reconstruction of one block, exact in double:
  *   Q4_0: d * (c - 8)      Q8_0, Q8_K: d * q      Q4_K: d*sc_j*q - dmin*m_j
+ *   Q6_K: d * (c - 32)
  * Every product of an fp16 (or fp32) scale with these small integers, and
  * the Q4_K difference, fits in the 53-bit double significand. */
 static void decode_block_f64(int type, const uint8_t *blk, double *out)
@@ -431,6 +484,11 @@ static void decode_block_f64(int type, const uint8_t *blk, double *out)
     case OR_Q8_K: {
         double d = get_f32(blk);
         for (int i = 0; i < 256; i++) out[i] = d * (double)(int8_t)blk[4 + i];
+        break;
+    }
+    case OR_Q6_K: {
+        double d = or_f16_to_f32(get_u16(blk));
+        for (int e = 0; e < 256; e++) out[e] = d * (double)(q6_k_code(blk, e) - 32);
         break;
     }
     }
@@ -469,7 +527,7 @@ static int pairing_ok(int wtype, int *atype)
 {
     switch (wtype) {
     case OR_Q4_0: case OR_Q8_0: *atype = OR_Q8_0; return 1;
-    case OR_Q4_K: *atype = OR_Q8_K; return 1;
+    case OR_Q4_K: case OR_Q6_K: *atype = OR_Q8_K; return 1;
     }
     return 0;
 }
@@ -480,9 +538,16 @@ static int pairing_ok(int wtype, int *atype)
  *   Q4_K x Q8_K: s_j = sum_{i in j} q_i * a_i per sub-block,
  *                S1 = sum_j sc_j * s_j,  S2 = sum_j m_j * t_j
  *                with t_j the activation sub-block sum (stored bsums).
+ *   Q6_K x Q8_K: s = sum_i (c_i - 32) * a_i over the 256 elements.
  * out[0] (and out[1] for Q4_K) receive the sums; returns the number written. */
 static int block_int_dot(int wtype, const uint8_t *w, const uint8_t *a, int32_t *out)
 {
+    if (wtype == OR_Q6_K) {
+        int32_t s = 0;
+        for (int e = 0; e < 256; e++) s += (q6_k_code(w, e) - 32) * (int8_t)a[4 + e];
+        out[0] = s;
+        return 1;
+    }
     if (wtype == OR_Q4_0) {
         int32_t s = 0;
         for (int j = 0; j < 16; j++) {
@@ -541,7 +606,8 @@ int or_block_sums(int wtype, const uint8_t *W, const uint8_t *xq, int64_t rows,
 }
 
 /* Scale terms of one block pair in double:
- *   Q4_0 / Q8_0: d_w * d_x * s
+ *   Q4_0 / Q8_0: d_w * d_x * s      (d_x the fp16 Q8_0 scale)
+ *   Q6_K:        d_w * d_x * s      (d_x the fp32 Q8_K scale)
  *   Q4_K:        d_x * d * S1   and   -(d_x * dmin * S2)
  * y accumulates the terms, T their absolute values. */
 static void block_terms(int wtype, const uint8_t *w, const uint8_t *a, double *y, double *T)
@@ -556,6 +622,12 @@ static void block_terms(int wtype, const uint8_t *w, const uint8_t *a, double *y
         double t2 = -(dx * dmin * (double)s[1]);
         *y += t1 + t2;
         *T += fabs(t1) + fabs(t2);
+    } else if (wtype == OR_Q6_K) {
+        double dw = or_f16_to_f32(get_u16(w));
+        double dx = get_f32(a);
+        double t = dw * dx * (double)s[0];
+        *y += t;
+        *T += fabs(t);
     } else {
         double dw = or_f16_to_f32(get_u16(w));
         double dx = or_f16_to_f32(get_u16(a));

@@ -13,7 +13,7 @@ import oracle as orc
 from block_quantized_gb300 import inputs
 from conftest import read_golden
 
-Q4_0, Q8_0, Q4_K, Q8_K = orc.Q4_0, orc.Q8_0, orc.Q4_K, orc.Q8_K
+Q4_0, Q8_0, Q4_K, Q8_K, Q6_K = orc.Q4_0, orc.Q8_0, orc.Q4_K, orc.Q8_K, orc.Q6_K
 
 
 def hexbytes(tokens):
@@ -31,7 +31,10 @@ def test_block_sizes():
     assert orc.block_bytes(Q4_0) * 8 / 32 == 4.5
     assert orc.block_bytes(Q4_0) * 8 == 144
     assert orc.block_bytes(Q4_K) * 8 / 256 == 4.5
-    for t in (Q4_0, Q8_0, Q4_K, Q8_K):
+    # Q6_K: 256 six-bit codes (192 bytes) and one fp16 scale
+    assert (orc.block_elems(Q6_K), orc.block_bytes(Q6_K)) == (256, 194)
+    assert orc.block_bytes(Q6_K) == 256 * 6 // 8 + 2
+    for t in (Q4_0, Q8_0, Q4_K, Q8_K, Q6_K):
         x = np.zeros(orc.block_elems(t) * 3, np.float32)
         assert orc.quantize(t, x).shape == (3, orc.block_bytes(t))
 
@@ -105,6 +108,34 @@ def test_q4_k_handmade_block():
     assert blk.tobytes() == expect.tobytes()
     # every element lies on its grid, so the reconstruction is exact
     np.testing.assert_array_equal(orc.dequantize(Q4_K, blk, 256), x)
+
+
+def test_q6_k_handmade_block():
+    g = read_golden("q6_k_handmade.txt")
+    q1 = np.array(g["q_first"], np.int64)
+    q2 = np.array(g["q_second"], np.int64)
+    x = np.concatenate([np.tile(q1, 32), np.tile(q2, 32)]).astype(np.float32) / 16.0
+    blk = orc.quantize(Q6_K, x)[0]
+    expect = np.concatenate([hexbytes(g["d"]),
+                             np.tile(hexbytes(g["ql_first"]), 32), np.tile(hexbytes(g["ql_second"]), 32),
+                             np.tile(hexbytes(g["qh_first"]), 32), np.tile(hexbytes(g["qh_second"]), 32)])
+    assert blk.tobytes() == expect.tobytes()
+    # every element is a multiple of the scale, so the reconstruction is exact
+    np.testing.assert_array_equal(orc.dequantize(Q6_K, blk, 256), x)
+
+
+def test_q6_k_ties_round_half_away():
+    """Codes round half away from zero: with d = 1/16 (max|x| = 31/16), x = +-2.5 d
+    gives +-3, x = +-0.5 d gives +-1 and 1.5 d gives 2 (ties-to-even would give
+    +-2, 0 and 2).  Codes are read back through the exact reconstruction."""
+    x = np.zeros(256, np.float32)
+    x[0] = 31 / 16
+    x[1:7] = np.array([2.5, -2.5, 0.5, -0.5, 1.5, -1.5], np.float32) / 16
+    blk = orc.quantize(Q6_K, x)[0]
+    assert blk[0] == 0x00 and blk[1] == 0x2C
+    q = orc.dequantize_f64(Q6_K, blk, 256) * 16
+    np.testing.assert_array_equal(q[:7], [31, 3, -3, 1, -1, 2, -2])
+    assert np.all(q[7:] == 0)
 
 
 # --------------------------------------------------------------------------
@@ -194,7 +225,7 @@ def _blocks_zoo(be, seed=1):
     return np.ascontiguousarray(x.reshape(-1))
 
 
-@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q8_K])
+@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q8_K, Q6_K])
 def test_roundtrip_symmetric(t):
     be, bb = orc.block_elems(t), orc.block_bytes(t)
     x = _blocks_zoo(be)
@@ -211,8 +242,8 @@ def test_roundtrip_symmetric(t):
     # Within the code range the nearest code is at most d/2 away; a value
     # beyond the extreme code (possible when the fp16 scale rounded down, or
     # underflowed to 0 for a tiny block) is clipped, adding its excess.
-    top_pos = (7.0 if t == Q4_0 else 127.0) * d
-    top_neg = (8.0 if t == Q4_0 else 127.0) * d
+    top_pos = {Q4_0: 7.0, Q6_K: 31.0}.get(t, 127.0) * d
+    top_neg = {Q4_0: 8.0, Q6_K: 32.0}.get(t, 127.0) * d
     top = np.where(x64 >= 0, top_pos[:, None], top_neg[:, None])
     excess = np.maximum(0.0, np.abs(x64) - top)
     assert np.all(err <= d[:, None] / 2 * (1 + 1e-6) + excess + 1e-7 * amax[:, None])
@@ -230,6 +261,18 @@ def test_roundtrip_symmetric(t):
         codes = q[:, 4:260].view(np.int8).astype(np.int32)
         bs = q[:, 260:276].copy().view(np.int16).astype(np.int32)
         np.testing.assert_array_equal(bs, codes.reshape(-1, 8, 32).sum(axis=2))
+    if t == Q6_K:
+        # codes read straight from the bytes: with a normal fp16 scale max|x|
+        # maps to +-31 and code 0 (q = -32) never occurs; a zero block stores 32
+        lo = np.stack([q[:, 2:130] & 15, q[:, 2:130] >> 4], axis=2).reshape(-1, 256)
+        hi = np.stack([(q[:, 130:194] >> (2 * k)) & 3 for k in range(4)], axis=2).reshape(-1, 256)
+        c = (lo | (hi << 4)).astype(np.int64)
+        np.testing.assert_array_equal(c - 32, np.round(xh / np.where(d == 0, 1, d)[:, None]))
+        nz = d >= 2.0 ** -14
+        i = np.abs(xb).argmax(axis=1)
+        assert np.all(np.abs(c[np.arange(len(i)), i][nz] - 32) == 31)
+        assert np.all(c[d == 0] == 32)
+        assert c[nz].min() >= 1
 
 
 def _q4k_fields(q):
@@ -273,7 +316,7 @@ def test_nonfinite_rejected():
 # The product: brute force in float64 on tiny inputs, and exact integer cases
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K])
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K, Q6_K])
 @pytest.mark.parametrize("rows,cols,batch", [(1, 256, 1), (5, 512, 3), (7, 1024, 2)])
 def test_matmul_ref_vs_bruteforce(wtype, rows, cols, batch):
     atype = orc.ACT_TYPE[wtype]
@@ -378,6 +421,35 @@ def test_integer_special_case_q4_k():
     np.testing.assert_array_equal(s[..., 1], S2)
 
 
+def test_integer_special_case_q6_k():
+    """Q6_K with d = 1 and a Q8_K scale of 1: codes c in [0, 63] stand for c - 32,
+    so y and the per-block sums are a pure integer product (numpy int64).  The
+    blocks are packed here from the format definition, independently of the
+    oracle's encoder."""
+    g = inputs.rng(9)
+    rows, cols, batch = 5, 768, 3
+    nb = cols // 256
+    C = g.integers(0, 64, size=(rows, cols))
+    Xc = g.integers(-127, 128, size=(batch, cols))
+    Cb = C.reshape(rows * nb, 256)
+    Wq = np.zeros((rows * nb, 194), np.uint8)
+    Wq[:, 1] = 0x3C                                          # fp16 1.0
+    Wq[:, 2:130] = ((Cb[:, 0::2] & 15) | ((Cb[:, 1::2] & 15) << 4)).astype(np.uint8)
+    top = Cb >> 4
+    Wq[:, 130:194] = (top[:, 0::4] | (top[:, 1::4] << 2) | (top[:, 2::4] << 4) |
+                      (top[:, 3::4] << 6)).astype(np.uint8)
+    Xb = Xc.reshape(batch * nb, 256)
+    Xq = np.zeros((batch * nb, 276), np.uint8)
+    Xq[:, 0:4] = np.frombuffer(np.float32(1.0).tobytes(), np.uint8)
+    Xq[:, 4:260] = Xb.astype(np.int8).view(np.uint8)
+    Xq[:, 260:276] = Xb.reshape(-1, 8, 32).sum(-1).astype(np.int16).view(np.uint8)
+    y, _ = orc.matmul_ref(Q6_K, Wq.reshape(rows, -1), Xq.reshape(batch, -1), rows, cols, batch)
+    np.testing.assert_array_equal(y, (Xc @ (C - 32).T).astype(np.float64))
+    s = orc.block_sums(Q6_K, Wq.reshape(rows, -1), Xq.reshape(batch, -1), rows, cols, batch)
+    ref = (Xc.reshape(batch, 1, nb, 256) * (C - 32).reshape(1, rows, nb, 256)).sum(-1)
+    np.testing.assert_array_equal(s, ref)
+
+
 def test_tolerance_scale_is_sum_of_magnitudes():
     """T is at least |y| (triangle inequality) and equals |y| when every term
     has the same sign (all-positive weights and activations, Q8_0 x Q8_0)."""
@@ -391,7 +463,7 @@ def test_tolerance_scale_is_sum_of_magnitudes():
     assert np.all(T2 >= np.abs(y2))
 
 
-@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q4_K, Q8_K])
+@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q4_K, Q8_K, Q6_K])
 def test_multithreaded_quantize_equals_blockwise(t):
     """The row-parallel quantizer used for timing is the pinned one, row by row."""
     be = orc.block_elems(t)
