@@ -19,7 +19,7 @@ number of library kernel launches in the timed region, and the SM clocks
 sampled during it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
-                  [--only prefill|sweep|decode|stream|kv] [--no-cpu]
+                  [--only prefill|sweep|decode|stream|kv|q6k] [--no-cpu]
 """
 from __future__ import annotations
 
@@ -49,7 +49,7 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv"], default=None,
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "q6k"], default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
 
@@ -302,7 +302,8 @@ def run_gpu(args, world, rank):
               "decode": lambda: bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world),
               "stream": lambda: bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak,
                                              args.steps),
-              "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak)}
+              "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak),
+              "q6k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak)}
         if rank == 0:
             print(json.dumps({"only": args.only, "result": fn[args.only]()}))
         else:
@@ -394,6 +395,7 @@ def run_gpu(args, world, rank):
         extras["batch_sweep"] = bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph)
         extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
         extras["kv_cache"] = bench_kv(gq, torch, dev, capture, time_graph, hbm_peak)
+        extras["q6k"] = bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -449,6 +451,47 @@ def bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak, s
     torch.cuda.empty_cache()
     return {"workload": "one launch over 262144 x 4096 Q4_K rows (604 MB)", "us": t / k * 1e6,
             "weight_gbps": gbs, "frac": gbs / hbm_peak}
+
+
+def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak):
+    """Q6_K x Q8_K GEMV on the 4096x4096 row-spread + outlier weights: 64
+    distinct copies (203 MB, larger than L2) as dependent back-to-back
+    launches on pre-quantized activations, and the same bytes as one tall
+    launch (262144 x 4096 rows)."""
+    W, _ = inputs.gemv_q4_k(0)
+    Wq1 = gq.quantize(gq.Q6_K, torch.from_numpy(W).to(dev))
+    del W
+    Wall = Wq1.reshape(1, -1).repeat(COPIES, 1)
+    X = torch.from_numpy(inputs.normal(inputs.rng(2), (COPIES, GEMV_COLS))).to(dev)
+    XQ = gq.quantize(gq.Q8_K, X)
+    Y = torch.empty(COPIES, GEMV_ROWS, dtype=torch.float32, device=dev)
+    Yt = torch.empty(1, GEMV_ROWS * COPIES, dtype=torch.float32, device=dev)
+    w_bytes = Wq1.numel()
+
+    def chain():
+        for i in range(COPIES):
+            gq.gq_matmul(gq.Q6_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
+
+    def tall():
+        gq.gq_matmul(gq.Q6_K, Wall, XQ[0], Yt, GEMV_ROWS * COPIES, GEMV_COLS, 1)
+
+    k = 200
+    t_c, _ = time_graph(capture(chain), k, 5)
+    t_t, _ = time_graph(capture(tall), 50, 3)
+    if not (torch.isfinite(Y).all() and torch.isfinite(Yt).all()):
+        raise RuntimeError("non-finite Q6_K GEMV output")
+    per = t_c / (k * COPIES)
+    alg = w_bytes + GEMV_COLS // 256 * 276 + GEMV_ROWS * 4
+    tall_s = t_t / 50
+    del Wall, XQ
+    torch.cuda.empty_cache()
+    return {"workload": "Q6_K x Q8_K GEMV 4096x4096 batch 1, 64 distinct matrices (203 MB)",
+            "kernel": "gemv_q6k_kernel (whole-row bulk copies, per-warp ring)",
+            "launch_us": per * 1e6, "alg_bytes_per_launch": alg, "weight_gbps": w_bytes / per / 1e9,
+            "achieved": alg / per / 1e9, "frac": alg / per / 1e9 / hbm_peak,
+            "streaming": {"workload": "one launch over 262144 x 4096 Q6_K rows (814 MB)",
+                          "us": tall_s * 1e6, "weight_gbps": COPIES * w_bytes / tall_s / 1e9,
+                          "frac": COPIES * w_bytes / tall_s / 1e9 / hbm_peak}}
 
 
 def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak):

@@ -22,8 +22,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]
 # The codecs must reproduce the reference bit for bit: no FMA contraction.
-PER_FILE = {"gq_codec.cu": ["-fmad=false"]}
-SOURCES = ["gq_api.cu", "gq_codec.cu", "gq_gemv.cu", "gq_mma.cu", "gq_kv.cu"]
+PER_FILE = {"gq_codec.cu": ["-fmad=false"], "gq_q6k.cu": ["-fmad=false"]}
+SOURCES = ["gq_api.cu", "gq_codec.cu", "gq_gemv.cu", "gq_mma.cu", "gq_kv.cu", "gq_q6k.cu"]
 HEADERS = ["gq_common.cuh", "gq_internal.h"]
 
 

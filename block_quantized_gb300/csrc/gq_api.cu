@@ -61,12 +61,12 @@ gq_status make_ctx(gq_stream_t stream, LaunchCtx *ctx) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-bool valid_type(int t) { return t >= GQ_Q4_0 && t <= GQ_Q8_K; }
+bool valid_type(int t) { return t >= GQ_Q4_0 && t <= GQ_Q6_K; }
 
 int64_t block_elems(int t) {
     switch (t) {
     case GQ_Q4_0: case GQ_Q8_0: return 32;
-    case GQ_Q4_K: case GQ_Q8_K: return 256;
+    case GQ_Q4_K: case GQ_Q8_K: case GQ_Q6_K: return 256;
     }
     return -1;
 }
@@ -77,6 +77,7 @@ int64_t block_bytes(int t) {
     case GQ_Q8_0: return Q8_0_BYTES;
     case GQ_Q4_K: return Q4_K_BYTES;
     case GQ_Q8_K: return Q8_K_BYTES;
+    case GQ_Q6_K: return Q6_K_BYTES;
     }
     return -1;
 }
@@ -103,7 +104,7 @@ gq_status check_codec(gq_type type, const void *x, const void *q, int64_t n, boo
 
 gq_status check_matmul(gq_type wtype, const void *W, const void *xq, const void *out,
                        int64_t rows, int64_t cols, int64_t batch, uintptr_t out_align) {
-    if (wtype != GQ_Q4_0 && wtype != GQ_Q8_0 && wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+    if (wtype != GQ_Q4_0 && wtype != GQ_Q8_0 && wtype != GQ_Q4_K && wtype != GQ_Q6_K) return GQ_ERR_TYPE;
     if (rows < 0 || cols < 0 || batch < 0) return GQ_ERR_SHAPE;
     if (cols % block_elems(wtype) != 0) return GQ_ERR_SHAPE;
     if (rows > MAX_DIM || batch > MAX_DIM || cols > MAX_COLS) return GQ_ERR_SHAPE;
@@ -154,7 +155,7 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
                         : check_matmul(wtype, W, act, y, rows, cols, batch, 4);
     if (st != GQ_OK) return st;
     if (fused_f32) {
-        if (path == GQ_PATH_MMA) return GQ_ERR_TYPE;
+        if (path == GQ_PATH_MMA || wtype == GQ_Q6_K) return GQ_ERR_TYPE;
         if (cols % 256 != 0) return GQ_ERR_SHAPE;
     }
     if (path == GQ_PATH_MMA) {
@@ -171,13 +172,14 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         use_mma = !fused_f32 && wtype == GQ_Q4_K && tc_auto(rows, batch) &&
                   mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
-    if (!use_mma && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
+    if (!use_mma && wtype != GQ_Q6_K && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = use_mma ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
-                            : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
-                                          (flags & GQ_FLAG_W_STATIC) != 0, ctx);
+    cudaError_t e = use_mma            ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
+                    : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, ctx)
+                                       : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
+                                                     (flags & GQ_FLAG_W_STATIC) != 0, ctx);
     if (e != cudaSuccess) return cuda_fail(e);
     return GQ_OK;
 }
@@ -215,7 +217,7 @@ gq_status gq_quantize_rows_async(gq_type type, const float *src, void *dst, int6
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = launch_quantize(type, src, dst, n, ctx);
+    cudaError_t e = type == GQ_Q6_K ? launch_quantize_q6k(src, dst, n, ctx) : launch_quantize(type, src, dst, n, ctx);
     return e == cudaSuccess ? GQ_OK : cuda_fail(e);
 }
 
@@ -230,7 +232,8 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = launch_dequantize(type, src, dst, n, ctx);
+    cudaError_t e = type == GQ_Q6_K ? launch_dequantize_q6k(src, dst, n, ctx)
+                                    : launch_dequantize(type, src, dst, n, ctx);
     return e == cudaSuccess ? GQ_OK : cuda_fail(e);
 }
 

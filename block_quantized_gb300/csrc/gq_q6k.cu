@@ -1,0 +1,413 @@
+// gq_q6k.cu -- Q6_K weights: codec kernels and the Q6_K x Q8_K GEMV.
+//
+// Q6_K is the 6-bit K-quant as the discosf.com page ("为什么说 llama.cpp
+// 是'裸引擎'——从模型加载的每一行代码说起", §4 量化不是"压缩"，而是"精度重分配")
+// describes it: K blocks only (the 256-element K-quant block of
+// "llama.cpp：一个人、一个周末…" 第二层：量化引擎), no sub-blocks, 6-bit main
+// quantization.  The scale follows the symmetric rule of "llama.cpp 推理引擎"
+// (runguoli.com) §5.1 with b = 6: d = fp16(max|x| / 31), q = round(x / d)
+// clamped to [-32, 31] (half away from zero), stored as c = q + 32; w =
+// d * (c - 32).  Block (194 B): fp16 d @0; 128 bytes @2 with the low four
+// bits of element 2l (low nibble) and 2l+1 (high nibble) in byte l; 64 bytes
+// @130 with the top two bits of elements 4l..4l+3 in byte l (element 4l+k in
+// bits 2k..2k+1).  The product pairs Q6_K weights with Q8_K activations:
+// per block s = sum_i (c_i - 32) * a_i (int32), y = sum_blocks d_w * d_x * s.
+//
+// This file is compiled with -fmad=false, and every division is __fdiv_rn,
+// so the codec's bytes equal the reference definition's.
+//
+// GEMV.  Decode is bound by the bytes of W streamed ("llama.cpp 推理引擎"
+// §7.3), so the kernel streams each row once:
+//   - a persistent grid of at most one CTA per SM, 8 warps; warp w of the
+//     grid owns rows w, w + warps, ...  Each warp streams its rows through a
+//     private shared-memory ring of 2-4 whole-row stages, one bulk copy
+//     (cp.async.bulk, evict-first L2 policy) per row completing on an
+//     mbarrier; every wait is bounded;
+//   - the CTA stages its Q8_K activation vector once: codes in 128-byte
+//     half-super-block units, each 8-code group stored as (a0 a2 a4 a6 |
+//     a1 a3 a5 a7) so that the masked low nibbles of a packed word line up
+//     with dp4a operands, and the 16-byte pieces of a unit XOR-swizzled by
+//     the unit index so that the lanes of a quarter-warp hit distinct banks;
+//     then the sum of each unit's 128 codes and the per-block scales;
+//   - a lane takes half a block (128 elements): 17 + 9 aligned 32-bit shared
+//     loads realigned with funnel shifts (blocks are 194 bytes, so half of
+//     them start 2 bytes off a word), the top bits spread into the code bytes
+//     with shifts and masks, 32 dp4a; the offset 32 is applied once per half
+//     through the code sum (s = sum c a - 32 sum a, exact in int32);
+//   - fp32 partial sums per lane, one warp-shuffle reduction per row.
+// Rows whose byte length is not a multiple of 16 (cols not a multiple of
+// 2048), or too long for a two-stage ring, take a plain warp-per-row kernel
+// with byte loads from global memory.
+#include <algorithm>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr uint32_t NIB = 0x0F0F0F0Fu;
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float clamp_f(float v, float lo, float hi) {
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+// ------------------------------------------------------------------ codecs
+
+// One warp per block; lane l owns elements 8l..8l+7, i.e. low-nibble bytes
+// 4l..4l+3 and top-bit bytes 2l, 2l+1 of the block.
+__global__ void __launch_bounds__(256) quantize_q6_k_kernel(const float *__restrict__ x,
+                                                            uint8_t *__restrict__ dst, int64_t nblocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    pdl_launch_dependents();  // dependents still wait for this grid's completion
+    pdl_wait();
+    for (int64_t b = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += warps) {
+        const float *src = x + b * QK_K + lane * 8;
+        float v[8];
+        float amax = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            v[k] = src[k];
+            amax = fmaxf(amax, fabsf(v[k]));
+        }
+        amax = warp_max_f(amax);
+        const __half dh = __float2half_rn(__fdiv_rn(amax, 31.0f));
+        const float d = __half2float(dh);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float q = (d == 0.0f) ? 0.0f : clamp_f(roundf(__fdiv_rn(v[k], d)), -32.0f, 31.0f);
+            const uint32_t c = (uint32_t)((int)q + 32);  // 0..63
+            lo |= (c & 15u) << (4 * k);                   // element 8l+k: byte 4l + k/2, nibble k&1
+            hi |= (c >> 4) << (2 * k);                    // byte 2l + k/4, bits 2(k&3)
+        }
+        uint8_t *blk = dst + b * Q6_K_BYTES;  // 2-byte aligned
+        uint16_t *ql = reinterpret_cast<uint16_t *>(blk + 2 + 4 * lane);
+        ql[0] = (uint16_t)(lo & 0xffffu);
+        ql[1] = (uint16_t)(lo >> 16);
+        *reinterpret_cast<uint16_t *>(blk + 130 + 2 * lane) = (uint16_t)hi;
+        if (lane == 0) *reinterpret_cast<uint16_t *>(blk) = __half_as_ushort(dh);
+    }
+}
+
+// One thread per element: d * (c - 32), exact in fp32.
+__global__ void dequantize_q6_k_kernel(const uint8_t *__restrict__ src, float *__restrict__ dst, int64_t n) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) {
+        const uint8_t *blk = src + (e >> 8) * Q6_K_BYTES;
+        const int i = (int)(e & 255);
+        const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
+        const int byte = blk[2 + (i >> 1)];
+        const int lo = (i & 1) ? (byte >> 4) : (byte & 15);
+        const int hi = (blk[130 + (i >> 2)] >> (2 * (i & 3))) & 3;
+        dst[e] = __fmul_rn(d, (float)((lo | (hi << 4)) - 32));
+    }
+}
+
+// ------------------------------------------------------------------- GEMV
+
+constexpr int GW = 8;      // warps per CTA of the streaming kernel
+constexpr int MAX_NS = 4;  // ring stages per warp
+constexpr int BARS_BYTES = GW * MAX_NS * 8;  // the mbarriers, at the start of shared memory (256 B)
+
+// Shared-memory footprint of one staged Q8_K vector of nblk blocks: codes,
+// then one int32 code sum per half block, then one fp32 scale per block.
+__host__ __device__ constexpr size_t act_smem_bytes(int nblk) {
+    return (size_t)nblk * 256 + (size_t)nblk * 2 * 4 + (size_t)nblk * 4;
+}
+
+// Split-order words of 8 codes: (a0 a2 a4 a6) and (a1 a3 a5 a7).
+__device__ __forceinline__ uint2 split8(uint32_t w0, uint32_t w1) {
+    return make_uint2(__byte_perm(w0, w1, 0x6420), __byte_perm(w0, w1, 0x7531));
+}
+
+// Stage one Q8_K vector (nblk blocks at xq) into shared memory at `act`.
+// Unit u (16 codes: elements 128h + 16u .. +15) of half-block hb = 2k + h is
+// stored at hb * 128 + (u ^ (hb & 7)) * 16 as {split(g0).x, .y, split(g1).x, .y}.
+__device__ void stage_q8_k_vec(uint8_t *act, const uint8_t *__restrict__ xq, int nblk) {
+    int32_t *asum = reinterpret_cast<int32_t *>(act + (size_t)nblk * 256);
+    float *dx = reinterpret_cast<float *>(asum + 2 * nblk);
+    for (int idx = threadIdx.x; idx < nblk * 16; idx += blockDim.x) {
+        const int hb = idx >> 3, u = idx & 7;
+        const uint8_t *blk = xq + (size_t)(hb >> 1) * Q8_K_BYTES;  // 4-byte aligned
+        const uint32_t *c = reinterpret_cast<const uint32_t *>(blk + 4 + (hb & 1) * 128 + u * 16);
+        const uint2 g0 = split8(c[0], c[1]), g1 = split8(c[2], c[3]);
+        *reinterpret_cast<uint4 *>(act + (size_t)hb * 128 + ((u ^ (hb & 7)) << 4)) =
+            make_uint4(g0.x, g0.y, g1.x, g1.y);
+    }
+    for (int hb = threadIdx.x; hb < 2 * nblk; hb += blockDim.x) {
+        const uint8_t *blk = xq + (size_t)(hb >> 1) * Q8_K_BYTES;
+        const int16_t *bs = reinterpret_cast<const int16_t *>(blk + 260) + (hb & 1) * 4;
+        asum[hb] = (int32_t)bs[0] + bs[1] + bs[2] + bs[3];
+        if ((hb & 1) == 0) dx[hb >> 1] = *reinterpret_cast<const float *>(blk);
+    }
+}
+
+// The top two bits of 4 elements (nibbles 0..3 of t, two bits each) moved to
+// bits 4..5 of bytes 0..3.
+__device__ __forceinline__ uint32_t spread_top(uint32_t t) {
+    uint32_t x = (t & 0xffu) | ((t & 0xff00u) << 8);
+    x = (x & 0x000f000fu) | ((x & 0x00f000f0u) << 4);
+    return x << 4;
+}
+
+// Integer sum of half block h of the block at `blk` (shared memory, 2-byte
+// aligned, at least 4 readable bytes past its end) against the staged codes
+// of half-block hb: sum_i c_i a_i over the 128 elements (offset not applied).
+__device__ __forceinline__ int half_dot(const uint8_t *stage, uint32_t blk_off, int h, const uint8_t *act,
+                                        int hb) {
+    const uint32_t offa = blk_off + 2 + 64 * h;    // low-nibble bytes of the half
+    const uint32_t offb = blk_off + 130 + 32 * h;  // top-bit bytes of the half
+    const uint32_t *wa = reinterpret_cast<const uint32_t *>(stage + (offa & ~3u));
+    const uint32_t *wb = reinterpret_cast<const uint32_t *>(stage + (offb & ~3u));
+    const uint32_t sha = (offa & 3u) * 8, shb = (offb & 3u) * 8;
+    uint32_t va[17], vb[9];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) va[i] = wa[i];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) vb[i] = wb[i];
+    const uint8_t *ah = act + (size_t)hb * 128;
+    const int sw = hb & 7;
+    int s = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(ah + ((u ^ sw) << 4));
+        const uint32_t top = __funnelshift_rc(vb[u], vb[u + 1], shb);  // top bits of elements 16u..16u+15
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+            const int g = 2 * u + g2;
+            const uint32_t w = __funnelshift_rc(va[g], va[g + 1], sha);  // low nibbles of elements 8g..8g+7
+            const uint32_t t = g2 ? (top >> 16) : (top & 0xffffu);
+            const uint32_t ca = (w & NIB) | spread_top(t & 0x3333u);          // elements 0, 2, 4, 6
+            const uint32_t cb = ((w >> 4) & NIB) | spread_top((t >> 2) & 0x3333u);  // elements 1, 3, 5, 7
+            s = dp4a((int)ca, (int)(g2 ? a.z : a.x), s);
+            s = dp4a((int)cb, (int)(g2 ? a.w : a.y), s);
+        }
+    }
+    return s;
+}
+
+// Streaming kernel: cols a multiple of 2048 (rows are 16-byte multiples);
+// one activation vector per blockIdx.y.  SUMS: write the int32 block sums
+// instead of y.
+template <bool SUMS>
+__global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__restrict__ W,
+                                                             const uint8_t *__restrict__ xq,
+                                                             float *__restrict__ y, int32_t *__restrict__ sums,
+                                                             int rows, int nblk, int ns, int stage_bytes,
+                                                             uint32_t *__restrict__ status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int warps_total = gridDim.x * GW;
+    const int wg = blockIdx.x * GW + warp;
+    const int total = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
+    const uint32_t row_bytes = (uint32_t)nblk * Q6_K_BYTES;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * MAX_NS;
+    uint8_t *ring = smem + BARS_BYTES + (size_t)warp * ns * stage_bytes;
+    uint8_t *act = smem + BARS_BYTES + (size_t)GW * ns * stage_bytes;
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int i, int st) {
+        const size_t row = (size_t)wg + (size_t)i * warps_total;
+        mbar_arrive_expect_tx(bar + st, row_bytes);
+        bulk_g2s_hint(ring + (size_t)st * stage_bytes, W + row * row_bytes, row_bytes, bar + st, pol);
+    };
+
+    pdl_launch_dependents();
+    if (lane == 0 && total > 0) {
+        for (int s = 0; s < ns; ++s) mbar_init(bar + s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();  // W and xq may come from the preceding kernel in the stream
+    if (lane == 0)
+        for (int i = 0; i < ns && i < total; ++i) issue(i, i);
+    stage_q8_k_vec(act, xq + (size_t)b * nblk * Q8_K_BYTES, nblk);
+    __syncthreads();
+
+    const int32_t *asum = reinterpret_cast<const int32_t *>(act + (size_t)nblk * 256);
+    const float *dx = reinterpret_cast<const float *>(asum + 2 * nblk);
+    const int iters = (2 * nblk + 31) / 32;
+    int st = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < total; ++i) {
+        if (!mbar_wait_bounded(bar + st, ph)) {
+            // A transfer never completed: flag it, let the other issued
+            // stages drain (bounded) and leave this warp's remaining rows.
+            if (lane == 0) atomicOr(status, STATUS_GEMV_TMA_TIMEOUT);
+            int s2 = st;
+            uint32_t p2 = ph;
+            for (int k = i + 1; k < total && k < i + ns; ++k) {
+                if (++s2 == ns) {
+                    s2 = 0;
+                    p2 ^= 1u;
+                }
+                mbar_wait_bounded(bar + s2, p2);
+            }
+            return;
+        }
+        const int row = wg + i * warps_total;
+        const uint8_t *stage = ring + (size_t)st * stage_bytes;
+        float acc = 0.0f;
+        for (int t = 0; t < iters; ++t) {
+            const int hb = lane + 32 * t;
+            int s = 0;
+            if (hb < 2 * nblk) {
+                const int k = hb >> 1;
+                s = half_dot(stage, (uint32_t)k * Q6_K_BYTES, hb & 1, act, hb) - 32 * asum[hb];
+                if (!SUMS) {
+                    const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t *>(stage + k * Q6_K_BYTES));
+                    acc += dw * dx[k] * (float)s;
+                }
+            }
+            if (SUMS) {
+                const int both = s + __shfl_xor_sync(FULL, s, 1);  // the two halves of block hb / 2
+                if (hb < 2 * nblk && (hb & 1) == 0)
+                    sums[((size_t)b * rows + row) * nblk + (hb >> 1)] = both;
+            }
+        }
+        if (!SUMS) {
+            acc = warp_sum(acc);
+            if (lane == 0) y[(size_t)b * rows + row] = acc;
+        }
+        __syncwarp();
+        if (lane == 0 && i + ns < total) issue(i + ns, st);
+        if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// Plain kernel for any cols (a multiple of 256): warp per (row, vector), lane
+// per half block, byte loads from global memory.
+constexpr int PW = 8;
+
+template <bool SUMS>
+__global__ void __launch_bounds__(PW * 32) gemv_q6k_plain_kernel(const uint8_t *__restrict__ W,
+                                                                 const uint8_t *__restrict__ xq,
+                                                                 float *__restrict__ y,
+                                                                 int32_t *__restrict__ sums, int rows, int nblk) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * PW + warp;
+    const int b = blockIdx.y;
+    pdl_launch_dependents();
+    pdl_wait();
+    if (row >= rows) return;
+    const int iters = (2 * nblk + 31) / 32;
+    float acc = 0.0f;
+    for (int t = 0; t < iters; ++t) {
+        const int hb = lane + 32 * t;
+        int s = 0;
+        float scale = 0.0f;
+        if (hb < 2 * nblk) {
+            const int k = hb >> 1, h = hb & 1;
+            const uint8_t *wb = W + ((size_t)row * nblk + k) * Q6_K_BYTES;
+            const uint8_t *ab = xq + ((size_t)b * nblk + k) * Q8_K_BYTES;
+            for (int e = 128 * h; e < 128 * h + 128; ++e) {
+                const int lo = (__ldg(wb + 2 + (e >> 1)) >> (4 * (e & 1))) & 15;
+                const int hi = (__ldg(wb + 130 + (e >> 2)) >> (2 * (e & 3))) & 3;
+                s += ((lo | (hi << 4)) - 32) * (int)(int8_t)__ldg(ab + 4 + e);
+            }
+            scale = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(wb))) *
+                    __ldg(reinterpret_cast<const float *>(ab));
+        }
+        if (SUMS) {
+            const int both = s + __shfl_xor_sync(FULL, s, 1);
+            if (hb < 2 * nblk && (hb & 1) == 0) sums[((size_t)b * rows + row) * nblk + (hb >> 1)] = both;
+        } else {
+            acc += scale * (float)s;
+        }
+    }
+    if (!SUMS) {
+        acc = warp_sum(acc);
+        if (lane == 0) y[(size_t)b * rows + row] = acc;
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA on sm_103
+constexpr int64_t Y_MAX = 65535;    // vectors per launch (grid.y)
+
+// Ring stages per warp for the streaming kernel: as many as fit (2..4) next
+// to the staged vector; 0 when rows are not 16-byte multiples or two stages
+// do not fit (the plain kernel runs instead).
+int pick_ns(int nblk) {
+    if (nblk % 8 != 0) return 0;
+    const size_t stage = (size_t)nblk * Q6_K_BYTES + 16;
+    for (int ns = MAX_NS; ns >= 2; --ns)
+        if (BARS_BYTES + (size_t)GW * ns * stage + act_smem_bytes(nblk) <= (size_t)SMEM_LIMIT) return ns;
+    return 0;
+}
+
+int codec_grid(int64_t items, int per_cta, int num_sms) {
+    int64_t g = (items + per_cta - 1) / per_cta;
+    g = std::min<int64_t>(g, (int64_t)num_sms * 16);
+    return (int)std::max<int64_t>(g, 1);
+}
+
+template <bool SUMS>
+cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+                     int64_t batch, const LaunchCtx &ctx) {
+    const int nblk = (int)(cols / QK_K);
+    const int ns = pick_ns(nblk);
+    if (ns) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_q6k_kernel<SUMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             SMEM_LIMIT);
+        if (e != cudaSuccess) return e;
+    }
+    for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
+        const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
+        const uint8_t *xb = xq + b0 * nblk * Q8_K_BYTES;
+        float *yb = SUMS ? nullptr : y + b0 * rows;
+        int32_t *sb = SUMS ? sums + b0 * rows * nblk : nullptr;
+        cudaError_t e;
+        if (ns) {
+            const int stage = nblk * Q6_K_BYTES + 16;
+            const size_t smem = BARS_BYTES + (size_t)GW * ns * stage + act_smem_bytes(nblk);
+            const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + GW - 1) / GW);
+            e = launch_pdl(gemv_q6k_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(GW * 32), smem, ctx.stream, W, xb,
+                           yb, sb, (int)rows, nblk, ns, stage, ctx.status);
+        } else {
+            const int64_t gx = (rows + PW - 1) / PW;
+            e = launch_pdl(gemv_q6k_plain_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(PW * 32), 0, ctx.stream, W,
+                           xb, yb, sb, (int)rows, nblk);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q6k(const float *src, void *dst, int64_t n, const LaunchCtx &ctx) {
+    const int64_t nb = n / QK_K;
+    return launch_pdl(quantize_q6_k_kernel, codec_grid(nb, 8, ctx.num_sms), 256, 0, ctx.stream, src,
+                      static_cast<uint8_t *>(dst), nb);
+}
+
+cudaError_t launch_dequantize_q6k(const void *src, float *dst, int64_t n, const LaunchCtx &ctx) {
+    return launch_pdl(dequantize_q6_k_kernel, codec_grid(n, 256, ctx.num_sms), 256, 0, ctx.stream,
+                      static_cast<const uint8_t *>(src), dst, n);
+}
+
+cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+                            int64_t batch, const LaunchCtx &ctx) {
+    const uint8_t *w8 = static_cast<const uint8_t *>(W);
+    const uint8_t *x8 = static_cast<const uint8_t *>(xq);
+    return sums ? run_gemv<true>(w8, x8, y, sums, rows, cols, batch, ctx)
+                : run_gemv<false>(w8, x8, y, sums, rows, cols, batch, ctx);
+}
+
+}  // namespace gq

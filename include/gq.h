@@ -27,17 +27,28 @@
  *                              q @16 in the Q4_0 nibble order;
  *                              w = d * sc_j * q - dmin * m_j for element i
  *                              of sub-block j = i / 32.
+ *   Q6_K 194 B / 256 elements: fp16 d @0, 128 bytes @2 holding the low
+ *                              four bits of the codes c in the Q4_0 nibble
+ *                              order, 64 bytes @130 holding their top two
+ *                              bits (byte l: elements 4l..4l+3, element 4l+k
+ *                              in bits 2k..2k+1); w = d * (c - 32).  The
+ *                              6-bit K-quant of the discosf.com page ("为什么说
+ *                              llama.cpp 是'裸引擎'…", §4): K blocks only, no
+ *                              sub-blocks, 6-bit main quantization; the
+ *                              symmetric rule and this layout are this
+ *                              library's reading.
  *   Q8_K 276 B / 256 elements: fp32 d @0, int8 q[256] @4, int16 bsums[8]
  *                              @260 (bsums[j] = sum of q over sub-block j);
  *                              w = d * q.
  * Quantization rounds codes half away from zero.  Q8_0 and Q8_K use
- * d = max|x| / 127, Q4_0 uses d = max|x| / 7 (fp16 scales rounded to
- * nearest-even); Q4_K fits each 32-element sub-block by its min/max with fp16
+ * d = max|x| / 127, Q4_0 uses d = max|x| / 7, Q6_K d = max|x| / 31 (fp16
+ * scales rounded to nearest-even; codes clamped to [-8, 7] and [-32, 31]
+ * before the offsets 8 and 32); Q4_K fits each 32-element sub-block by its min/max with fp16
  * d and dmin rounded toward +infinity (so that the ceilinged 6-bit scale and
  * min always cover the sub-block) -- see the quantize entry point below.
  *
  * Pairings for the product: Q4_0 and Q8_0 weights take Q8_0 activations;
- * Q4_K weights take Q8_K activations.
+ * Q4_K and Q6_K weights take Q8_K activations.
  *
  * General rules for every entry point:
  *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
@@ -74,7 +85,8 @@ typedef enum {
     GQ_Q4_0 = 0,
     GQ_Q8_0 = 1,
     GQ_Q4_K = 2,
-    GQ_Q8_K = 3
+    GQ_Q8_K = 3,
+    GQ_Q6_K = 4
 } gq_type;
 
 typedef enum {
@@ -106,9 +118,10 @@ typedef enum {
     GQ_PATH_MMA = 2     /* tcgen05 tensor-core kernel (Q4_K weights only) */
 } gq_path;
 
-/* Elements per block: 32, 32, 256, 256.  -1 for an unknown type. */
+/* Elements per block: 32, 32, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K, Q6_K).
+ * -1 for an unknown type. */
 int64_t gq_block_elems(gq_type type);
-/* Bytes per block: 18, 34, 144, 276.  -1 for an unknown type. */
+/* Bytes per block: 18, 34, 144, 276, 194.  -1 for an unknown type. */
 int64_t gq_block_bytes(gq_type type);
 /* Static text for a status code (never NULL). */
 const char *gq_status_string(gq_status status);
@@ -120,9 +133,9 @@ int gq_last_cuda_error(void);
  *   src : device, n floats, 4-byte aligned, finite values (non-finite input
  *         gives unspecified codes; magnitudes must keep the fp16 scales in
  *         range: |x| < 65504 * 127 for Q8_0, 65504 * 7 for Q4_0, 65504 * 945
- *         for Q4_K).
+ *         for Q4_K, 65504 * 31 for Q6_K).
  *   dst : device, n / block_elems * block_bytes bytes; 4-byte aligned for
- *         Q8_K and Q4_K, 2-byte aligned for Q4_0 / Q8_0 (the product needs
+ *         Q8_K and Q4_K, 2-byte aligned for Q4_0 / Q8_0 / Q6_K (the product needs
  *         16-byte aligned weights, see gq_matmul).
  *   n   : element count, >= 0 and a multiple of block_elems(type).
  * Results are bit-identical to the reference definition of each format
@@ -156,16 +169,19 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *   Q8_0 x Q8_0 : d_w * d_x * sum_i w_i * a_i
  *   Q4_K x Q8_K : d_x * (d * sum_j sc_j * s_j - dmin * sum_j m_j * t_j),
  *                 s_j = sum_{i in j} q_i * a_i, t_j = bsums[j]
- *   wtype : GQ_Q4_0, GQ_Q8_0 or GQ_Q4_K.
+ *   Q6_K x Q8_K : d_w * d_x * sum_i (c_i - 32) * a_i   (per 256-element block)
+ *   wtype : GQ_Q4_0, GQ_Q8_0, GQ_Q4_K or GQ_Q6_K.
  *   W     : device, rows x (cols / block_elems) weight blocks, 16-byte aligned.
  *   xq    : device, batch x (cols / block_elems) activation blocks (Q8_0 for
- *           Q4_0 / Q8_0 weights, Q8_K for Q4_K), one vector after another;
+ *           Q4_0 / Q8_0 weights, Q8_K for Q4_K / Q6_K), one vector after another;
  *           16-byte aligned.
  *   y     : device, float[batch][rows], 4-byte aligned; fully overwritten.
  *   rows, cols, batch : > 0 (a zero size is a no-op returning GQ_OK);
- *           cols a multiple of 256 for Q4_K and of 32 for Q4_0 / Q8_0 (the
- *           fast kernels need cols % 256 == 0; other multiples of 32 run a
- *           plain per-block kernel); cols at most 131072 (and small
+ *           cols a multiple of 256 for Q4_K / Q6_K and of 32 for Q4_0 / Q8_0
+ *           (the fast kernels need cols % 256 == 0, and cols % 2048 == 0 up
+ *           to 16384 for Q6_K; other shapes run a plain per-block kernel);
+ *           Q6_K runs one pass over W per activation vector; cols at most
+ *           131072 (and small
  *           enough for one activation vector to fit the kernels' shared
  *           memory: every cols up to that bound does).
  * The integer block sums are exact (int32); y matches the double-precision
@@ -227,7 +243,8 @@ gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y,
  * for bit, with one launch instead of two and no quantized activation buffer
  * ("llama.cpp：一个人、一个周末…", 第一层：GGML 张量库: operators fused over
  * the computation graph).  GEMV kernels only (any batch); cols must be a
- * multiple of 256 (GQ_ERR_SHAPE otherwise).  Other arguments as gq_matmul.
+ * multiple of 256 (GQ_ERR_SHAPE otherwise).  Q4_0, Q8_0 and Q4_K weights
+ * (GQ_ERR_TYPE for Q6_K).  Other arguments as gq_matmul.
  */
 gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
                         int64_t rows, int64_t cols, int64_t batch, unsigned flags,
@@ -238,7 +255,8 @@ gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
  * chosen kernel family, without the float scaling.
  *   sums : device, int32, 4-byte aligned, laid out [batch][rows][nblk][c] with
  *          nblk = cols / block_elems(wtype) and c = 1 (Q4_0, Q8_0: the block
- *          dot) or c = 2 (Q4_K: S1 = sum_j sc_j * s_j, S2 = sum_j m_j * t_j).
+ *          dot; Q6_K: sum_i (c_i - 32) * a_i) or c = 2 (Q4_K:
+ *          S1 = sum_j sc_j * s_j, S2 = sum_j m_j * t_j).
  * Other arguments and errors as gq_matmul_path.
  */
 gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *sums,

@@ -37,8 +37,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_block_geometry(lib):
-    assert [gq.gq_block_elems(t) for t in range(4)] == [32, 32, 256, 256]
-    assert [gq.gq_block_bytes(t) for t in range(4)] == [18, 34, 144, 276]
+    assert [gq.gq_block_elems(t) for t in range(5)] == [32, 32, 256, 256, 256]
+    assert [gq.gq_block_bytes(t) for t in range(5)] == [18, 34, 144, 276, 194]
     assert gq.gq_block_elems(9) == -1 and gq.gq_block_bytes(-1) == -1
 
 
@@ -77,6 +77,9 @@ def test_matmul_validation(lib):
     g = lib.gq_matmul_path
     assert g(2, A16, A16, A16, 8, 256, 1, 9, None) == TYPE
     assert g(0, A16, A16, A16, 8, 256, 64, 2, None) == TYPE      # MMA is Q4_K only
+    assert g(4, A16, A16, A16, 8, 256, 64, 2, None) == TYPE
+    assert f(4, A16, A16, A16, 8, 32, 1, None) == SHAPE          # Q6_K needs 256-multiples
+    assert f(4, 0, 0, 0, 8, 256, 0, None) == OK
     assert lib.gq_block_sums(2, A16, A16, 0, 8, 256, 1, 1, None) == NULL
 
 
@@ -91,6 +94,8 @@ def test_codec_validation(lib):
     assert q(1, A16 + 2, A16, 32) == ALIGN                      # src must be 4-aligned
     assert q(3, A16, A16 + 2, 256) == ALIGN                     # Q8_K dst 4-aligned
     assert q(1, A16, A16 + 1, 32) == ALIGN                      # Q8_0 dst 2-aligned
+    assert q(4, A16, A16 + 1, 256) == ALIGN                     # Q6_K dst 2-aligned
+    assert q(4, A16, A16, 32) == SHAPE
     assert q(1, 0, 0, 0) == OK
     d = lib.gq_dequantize_rows
     assert d(0, A16, A16, 31) == SHAPE
@@ -117,6 +122,7 @@ def test_fused_and_flag_validation(lib):
     assert f(0, A16, A16, A16, 8, 96, 1, 0, None) == SHAPE          # fused needs cols % 256 == 0
     assert f(2, A16, A16, A16, 8, 256, 1, 2, None) == TYPE          # unknown flag bit
     assert f(3, A16, A16, A16, 8, 256, 1, 0, None) == TYPE
+    assert f(4, A16, A16, A16, 8, 256, 1, 0, None) == TYPE          # no fused Q6_K kernel
     assert f(2, 0, 0, 0, 0, 256, 1, 0, None) == OK
     e = lib.gq_matmul_ex
     assert e(2, A16, A16, A16, 8, 256, 1, 1, 4, None) == TYPE
