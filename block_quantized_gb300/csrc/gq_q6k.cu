@@ -116,9 +116,18 @@ __global__ void dequantize_q6_k_kernel(const uint8_t *__restrict__ src, float *_
 
 // ------------------------------------------------------------------- GEMV
 
-constexpr int GW = 8;      // warps per CTA of the streaming kernel
+// Warps per CTA of the streaming kernel: the widest of GQ_Q6K_MAX_WARPS, 16
+// and 8 whose rings (two stages or more) fit.
+#ifndef GQ_Q6K_MAX_WARPS
+#define GQ_Q6K_MAX_WARPS 16
+#endif
+// Independent dp4a accumulator chains per lane (1 or 2).
+#ifndef GQ_Q6K_CHAINS
+#define GQ_Q6K_CHAINS 1
+#endif
 constexpr int MAX_NS = 4;  // ring stages per warp
-constexpr int BARS_BYTES = GW * MAX_NS * 8;  // the mbarriers, at the start of shared memory (256 B)
+// the mbarriers, at the start of shared memory
+__host__ __device__ constexpr int bars_bytes(int nw) { return nw * MAX_NS * 8; }
 
 // Shared-memory footprint of one staged Q8_K vector of nblk blocks: codes,
 // then one int32 code sum per half block, then one fp32 scale per block.
@@ -178,7 +187,7 @@ __device__ __forceinline__ int half_dot(const uint8_t *stage, uint32_t blk_off, 
     for (int i = 0; i < 9; ++i) vb[i] = wb[i];
     const uint8_t *ah = act + (size_t)hb * 128;
     const int sw = hb & 7;
-    int s = 0;
+    int s = 0, s2 = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const uint4 a = *reinterpret_cast<const uint4 *>(ah + ((u ^ sw) << 4));
@@ -191,16 +200,19 @@ __device__ __forceinline__ int half_dot(const uint8_t *stage, uint32_t blk_off, 
             const uint32_t ca = (w & NIB) | spread_top(t & 0x3333u);          // elements 0, 2, 4, 6
             const uint32_t cb = ((w >> 4) & NIB) | spread_top((t >> 2) & 0x3333u);  // elements 1, 3, 5, 7
             s = dp4a((int)ca, (int)(g2 ? a.z : a.x), s);
-            s = dp4a((int)cb, (int)(g2 ? a.w : a.y), s);
+            if (GQ_Q6K_CHAINS == 2)
+                s2 = dp4a((int)cb, (int)(g2 ? a.w : a.y), s2);
+            else
+                s = dp4a((int)cb, (int)(g2 ? a.w : a.y), s);
         }
     }
-    return s;
+    return s + s2;
 }
 
 // Streaming kernel: cols a multiple of 2048 (rows are 16-byte multiples);
 // one activation vector per blockIdx.y.  SUMS: write the int32 block sums
 // instead of y.
-template <bool SUMS>
+template <bool SUMS, int GW>
 __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__restrict__ W,
                                                              const uint8_t *__restrict__ xq,
                                                              float *__restrict__ y, int32_t *__restrict__ sums,
@@ -214,8 +226,8 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__r
     const int total = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
     const uint32_t row_bytes = (uint32_t)nblk * Q6_K_BYTES;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * MAX_NS;
-    uint8_t *ring = smem + BARS_BYTES + (size_t)warp * ns * stage_bytes;
-    uint8_t *act = smem + BARS_BYTES + (size_t)GW * ns * stage_bytes;
+    uint8_t *ring = smem + bars_bytes(GW) + (size_t)warp * ns * stage_bytes;
+    uint8_t *act = smem + bars_bytes(GW) + (size_t)GW * ns * stage_bytes;
     const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int i, int st) {
         const size_t row = (size_t)wg + (size_t)i * warps_total;
@@ -340,15 +352,29 @@ __global__ void __launch_bounds__(PW * 32) gemv_q6k_plain_kernel(const uint8_t *
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA on sm_103
 constexpr int64_t Y_MAX = 65535;    // vectors per launch (grid.y)
 
-// Ring stages per warp for the streaming kernel: as many as fit (2..4) next
-// to the staged vector; 0 when rows are not 16-byte multiples or two stages
-// do not fit (the plain kernel runs instead).
-int pick_ns(int nblk) {
+size_t stream_smem(int nw, int ns, int nblk) {
+    return bars_bytes(nw) + (size_t)nw * ns * ((size_t)nblk * Q6_K_BYTES + 16) + act_smem_bytes(nblk);
+}
+
+// Ring stages per warp for the streaming kernel with nw warps: as many as fit
+// (2..4) next to the staged vector; 0 when rows are not 16-byte multiples or
+// two stages do not fit.
+int pick_ns(int nw, int nblk) {
     if (nblk % 8 != 0) return 0;
-    const size_t stage = (size_t)nblk * Q6_K_BYTES + 16;
     for (int ns = MAX_NS; ns >= 2; --ns)
-        if (BARS_BYTES + (size_t)GW * ns * stage + act_smem_bytes(nblk) <= (size_t)SMEM_LIMIT) return ns;
+        if (stream_smem(nw, ns, nblk) <= (size_t)SMEM_LIMIT) return ns;
     return 0;
+}
+
+template <bool SUMS, int NW>
+cudaError_t launch_stream(const uint8_t *W, const uint8_t *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
+                          int nb, int ns, const LaunchCtx &ctx) {
+    auto k = gemv_q6k_kernel<SUMS, NW>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+    if (e != cudaSuccess) return e;
+    const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
+    return launch_pdl(k, dim3((unsigned)gx, nb), dim3(NW * 32), stream_smem(NW, ns, nblk), ctx.stream, W, xb,
+                      yb, sb, (int)rows, nblk, ns, nblk * Q6_K_BYTES + 16, ctx.status);
 }
 
 int codec_grid(int64_t items, int per_cta, int num_sms) {
@@ -361,24 +387,22 @@ template <bool SUMS>
 cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
                      int64_t batch, const LaunchCtx &ctx) {
     const int nblk = (int)(cols / QK_K);
-    const int ns = pick_ns(nblk);
-    if (ns) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_q6k_kernel<SUMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             SMEM_LIMIT);
-        if (e != cudaSuccess) return e;
-    }
+    // the widest instantiation whose rings fit: GQ_Q6K_MAX_WARPS, 16 or 8 warps
+    int nw = GQ_Q6K_MAX_WARPS, ns = pick_ns(nw, nblk);
+    if (!ns && nw > 16) ns = pick_ns(nw = 16, nblk);
+    if (!ns && nw > 8) ns = pick_ns(nw = 8, nblk);
     for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
         const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
         const uint8_t *xb = xq + b0 * nblk * Q8_K_BYTES;
         float *yb = SUMS ? nullptr : y + b0 * rows;
         int32_t *sb = SUMS ? sums + b0 * rows * nblk : nullptr;
         cudaError_t e;
-        if (ns) {
-            const int stage = nblk * Q6_K_BYTES + 16;
-            const size_t smem = BARS_BYTES + (size_t)GW * ns * stage + act_smem_bytes(nblk);
-            const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + GW - 1) / GW);
-            e = launch_pdl(gemv_q6k_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(GW * 32), smem, ctx.stream, W, xb,
-                           yb, sb, (int)rows, nblk, ns, stage, ctx.status);
+        if (ns && nw == GQ_Q6K_MAX_WARPS) {
+            e = launch_stream<SUMS, GQ_Q6K_MAX_WARPS>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+        } else if (ns && nw == 16) {
+            e = launch_stream<SUMS, 16>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+        } else if (ns) {
+            e = launch_stream<SUMS, 8>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
         } else {
             const int64_t gx = (rows + PW - 1) / PW;
             e = launch_pdl(gemv_q6k_plain_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(PW * 32), 0, ctx.stream, W,
