@@ -1,6 +1,7 @@
 """Planted mistakes: each case copies the CPU oracle, plants one plausible slip
 in the copy's C source (a swapped nibble, a wrong rounding rule, a dropped or
-sign-flipped term, a transposed operand, ...), rebuilds it, and runs the pins
+sign-flipped term, a transposed operand, ...) or in its Python KV-cache layer
+(a wrong position, head or query), rebuilds it, and runs the pins
 of tests/test_oracle_pins.py that should catch it against the mutant.  The
 pins pass on the real oracle (that file's own run); here every mutant must
 make at least one of them fail.
@@ -11,7 +12,6 @@ repository on its path (checked before the run); the real oracle is never
 modified.
 """
 import os
-import shutil
 import subprocess
 import sys
 
@@ -93,14 +93,43 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("name,orig,planted,pins", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_planted_mistake(tmp_path, name, orig, planted, pins):
-    src = open(os.path.join(ORACLE, "gq_oracle.c"), encoding="utf-8").read()
+# Slips in the oracle's Python layer (the KV-cache functions over the C codec).
+PY_MUTANTS = [
+    ("kv append writes the next position",
+     "cache[h, pos] = quantize(t, x[h]).reshape(-1)",
+     "cache[h, min(pos + 1, cache.shape[1] - 1)] = quantize(t, x[h]).reshape(-1)",
+     "kv_append"),
+    ("kv append quantizes every head with head 0's values",
+     "cache[h, pos] = quantize(t, x[h]).reshape(-1)",
+     "cache[h, pos] = quantize(t, x[0]).reshape(-1)",
+     "kv_append"),
+    ("kv scores pair every head's keys with head 0's query",
+     "qq = quantize(Q8_0, q[h:h + 1])",
+     "qq = quantize(Q8_0, q[0:1])",
+     "kv_scores"),
+    ("kv scores skip the first position",
+     "y, tt = matmul_ref(t, cache[h, :n_pos], qq, n_pos, head_dim, 1)",
+     "y, tt = matmul_ref(t, cache[h, 1:n_pos + 1], qq, n_pos, head_dim, 1)",
+     "kv_scores"),
+]
+
+
+@pytest.mark.parametrize("name,orig,planted,pins,layer",
+                         [m + ("c",) for m in MUTANTS] + [m + ("py",) for m in PY_MUTANTS],
+                         ids=[m[0] for m in MUTANTS + PY_MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, orig, planted, pins, layer):
+    c_src = open(os.path.join(ORACLE, "gq_oracle.c"), encoding="utf-8").read()
+    py_src = open(os.path.join(ORACLE, "__init__.py"), encoding="utf-8").read()
+    src = c_src if layer == "c" else py_src
     assert src.count(orig) == 1, f"mutation site not unique or missing: {orig!r}"
+    if layer == "c":
+        c_src = c_src.replace(orig, planted)
+    else:
+        py_src = py_src.replace(orig, planted)
     pkg = tmp_path / "oracle"
     pkg.mkdir()
-    shutil.copy(os.path.join(ORACLE, "__init__.py"), pkg / "__init__.py")
-    (pkg / "gq_oracle.c").write_text(src.replace(orig, planted), encoding="utf-8")
+    (pkg / "__init__.py").write_text(py_src, encoding="utf-8")
+    (pkg / "gq_oracle.c").write_text(c_src, encoding="utf-8")
     # the mutant must compile (a build error must not pass for a caught mistake)
     (pkg / "_build").mkdir()
     cc = subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-std=c11",
