@@ -107,7 +107,8 @@ enum {
      * request their first weight chunks before waiting for the preceding
      * kernel in the stream to finish, overlapping the weight fetch with that
      * kernel's tail.  Without the flag every read of W happens after that
-     * wait. */
+     * wait.  Accepted with Q6_K weights, where it has no effect (that GEMV
+     * reads W only after the wait). */
     GQ_FLAG_W_STATIC = 1u
 };
 
