@@ -80,3 +80,6 @@ def test_reference_arm_prints_from_rank_zero_only(monkeypatch):
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # the reference arm names the GPU arm's metric and workload
+    assert line["metric"] == bench.METRIC and line["higher_is_better"] is True
+    assert line["config"] == bench.headline_config(line["n_gpus"])
