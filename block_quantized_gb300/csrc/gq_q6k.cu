@@ -18,11 +18,11 @@
 //
 // GEMV.  Decode is bound by the bytes of W streamed ("llama.cpp 推理引擎"
 // §7.3), so the kernel streams each row once:
-//   - a persistent grid of at most one CTA per SM, 8 warps; warp w of the
-//     grid owns rows w, w + warps, ...  Each warp streams its rows through a
-//     private shared-memory ring of 2-4 whole-row stages, one bulk copy
-//     (cp.async.bulk, evict-first L2 policy) per row completing on an
-//     mbarrier; every wait is bounded;
+//   - a persistent grid of at most one CTA per SM, 16 warps (8 when 16
+//     two-stage rings do not fit); warp w of the grid owns rows w, w + warps,
+//     ...  Each warp streams its rows through a private shared-memory ring of
+//     2-4 whole-row stages, one bulk copy (cp.async.bulk, evict-first L2
+//     policy) per row completing on an mbarrier; every wait is bounded;
 //   - the CTA stages its Q8_K activation vector once: codes in 128-byte
 //     half-super-block units, each 8-code group stored as (a0 a2 a4 a6 |
 //     a1 a3 a5 a7) so that the masked low nibbles of a packed word line up
