@@ -228,6 +228,29 @@ def run_cpu_baseline(seconds=10.0, seconds_one=4.0):
             "act_quantize_us": tq * 1e6}
 
 
+def run_cpu_q6k(seconds=3.0):
+    """The oracle, as it stands, on all host cores for the Q6_K workload:
+    Q8_K act-quant + Q6_K GEMV of the 4096x4096 matrix, repeated for about
+    `seconds`."""
+    import oracle as orc
+    from block_quantized_gb300 import inputs
+    W, _ = inputs.gemv_q4_k(0)
+    Wq = orc.quantize(orc.Q6_K, W)
+    x = inputs.normal(inputs.rng(2), (GEMV_COLS,))
+    nt = orc.max_threads()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        xq = orc.quantize(orc.Q8_K, x)
+        orc.matmul_ref(orc.Q6_K, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, nt)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": n * Wq.nbytes / dt / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
+            "sample": f"{n} x (Q8_K act-quant + Q6_K GEMV 4096x4096, batch 1) in {dt:.1f} s"}
+
+
 def run_reference(args):
     orc, Wq, x = oracle_gemv_sample()
     nt = orc.max_threads()
@@ -320,7 +343,8 @@ def run_gpu(args, world, rank):
               "stream": lambda: bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak,
                                              args.steps),
               "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak),
-              "q6k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak)}
+              "q6k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
+                                       cpu=rank == 0 and world == 1 and not args.no_cpu)}
         if rank == 0:
             print(json.dumps({"only": args.only, "result": fn[args.only]()}))
         else:
@@ -412,7 +436,8 @@ def run_gpu(args, world, rank):
         extras["batch_sweep"] = bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph)
         extras["prefill"] = bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
         extras["kv_cache"] = bench_kv(gq, torch, dev, capture, time_graph, hbm_peak)
-        extras["q6k"] = bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak)
+        extras["q6k"] = bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
+                                  cpu=rank == 0 and world == 1 and not args.no_cpu)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -465,7 +490,7 @@ def bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak, s
             "weight_gbps": gbs, "frac": gbs / hbm_peak}
 
 
-def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak):
+def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=False):
     """Q6_K x Q8_K GEMV on the 4096x4096 row-spread + outlier weights: 64
     distinct copies (203 MB, larger than L2) as dependent back-to-back
     launches on pre-quantized activations, and the same bytes as one tall
@@ -498,6 +523,7 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak):
     del Wall, XQ
     torch.cuda.empty_cache()
     return {"workload": "Q6_K x Q8_K GEMV 4096x4096 batch 1, 64 distinct matrices (203 MB)",
+            "cpu_baseline": run_cpu_q6k() if cpu else None,
             "kernel": "gemv_q6k_kernel (whole-row bulk copies, per-warp ring)",
             "launch_us": per * 1e6, "alg_bytes_per_launch": alg, "weight_gbps": w_bytes / per / 1e9,
             "achieved": alg / per / 1e9, "frac": alg / per / 1e9 / hbm_peak,

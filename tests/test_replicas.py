@@ -83,3 +83,9 @@ def test_reference_arm_prints_from_rank_zero_only(monkeypatch):
     # the reference arm names the GPU arm's metric and workload
     assert line["metric"] == bench.METRIC and line["higher_is_better"] is True
     assert line["config"] == bench.headline_config(line["n_gpus"])
+
+
+def test_q6k_cpu_baseline_times_the_oracle():
+    r = bench.run_cpu_q6k(0.2)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] >= 1
+    assert "Q6_K GEMV 4096x4096" in r["sample"]
