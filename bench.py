@@ -15,12 +15,13 @@ streaming point, the unfused step, the end-to-end figure with host buffers,
 the 7B-shape decode (tok/s), the batch sweep on 14336x4096 through both
 kernel families, the 512-column prefill GEMM, the quantized KV cache
 (scores and append), the Q6_K GEMV (dependent launches and one streaming
-launch), the CPU oracle baseline (all cores and one core), the
+launch), the 512x1024 Q4_0 GEMV (latency), the CPU oracle baseline (all
+cores and one core), the
 number of library kernel launches in the timed region, and the SM clocks
 sampled during it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
-                  [--only prefill|sweep|decode|stream|kv|q6k] [--no-cpu]
+                  [--only prefill|sweep|decode|stream|kv|q6k|q4_0] [--no-cpu]
 """
 from __future__ import annotations
 
@@ -50,7 +51,7 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "q6k"], default=None,
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "q6k", "q4_0"], default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
 
@@ -251,6 +252,26 @@ def run_cpu_q6k(seconds=3.0):
             "sample": f"{n} x (Q8_K act-quant + Q6_K GEMV 4096x4096, batch 1) in {dt:.1f} s"}
 
 
+def run_cpu_q4_0(seconds=1.0):
+    """The oracle on one core for the 512x1024 Q4_0 x Q8_0 GEMV (batch 1):
+    Q8_0 act-quant + GEMV, repeated for about `seconds`."""
+    import oracle as orc
+    from block_quantized_gb300 import inputs
+    W, x = inputs.gemv_q4_0(0)
+    Wq = orc.quantize(orc.Q4_0, W)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        xq = orc.quantize(orc.Q8_0, x)
+        orc.matmul_ref(orc.Q4_0, Wq, xq, 512, 1024, 1, 1)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"us_per_gemv": dt / n * 1e6, "cores": 1, "kind": "oracle",
+            "sample": f"{n} x (Q8_0 act-quant + Q4_0 GEMV 512x1024, batch 1) in {dt:.1f} s"}
+
+
 def run_reference(args):
     orc, Wq, x = oracle_gemv_sample()
     nt = orc.max_threads()
@@ -344,7 +365,9 @@ def run_gpu(args, world, rank):
                                              args.steps),
               "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak),
               "q6k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
-                                       cpu=rank == 0 and world == 1 and not args.no_cpu)}
+                                       cpu=rank == 0 and world == 1 and not args.no_cpu),
+              "q4_0": lambda: bench_q4_0(gq, inputs, torch, np, dev, capture, time_graph,
+                                         cpu=rank == 0 and world == 1 and not args.no_cpu)}
         if rank == 0:
             print(json.dumps({"only": args.only, "result": fn[args.only]()}))
         else:
@@ -438,6 +461,8 @@ def run_gpu(args, world, rank):
         extras["kv_cache"] = bench_kv(gq, torch, dev, capture, time_graph, hbm_peak)
         extras["q6k"] = bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
                                   cpu=rank == 0 and world == 1 and not args.no_cpu)
+        extras["q4_0_512x1024"] = bench_q4_0(gq, inputs, torch, np, dev, capture, time_graph,
+                                             cpu=rank == 0 and world == 1 and not args.no_cpu)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -488,6 +513,36 @@ def bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak, s
     torch.cuda.empty_cache()
     return {"workload": "one launch over 262144 x 4096 Q4_K rows (604 MB)", "us": t / k * 1e6,
             "weight_gbps": gbs, "frac": gbs / hbm_peak}
+
+
+def bench_q4_0(gq, inputs, torch, np, dev, capture, time_graph, cpu=False):
+    """The 512x1024 Q4_0 x Q8_0 GEMV at batch 1 (295 KB of weights, resident
+    in L2, so latency-bound: time reported, not graded against a roofline):
+    back-to-back dependent launches on a pre-quantized vector, and with the
+    activation quantize fused into each launch."""
+    rows, cols, n = 512, 1024, 256
+    W, x = inputs.gemv_q4_0(0)
+    Wq = gq.quantize(gq.Q4_0, torch.from_numpy(W).to(dev))
+    xd = torch.from_numpy(x).to(dev)
+    xq = gq.quantize(gq.Q8_0, xd)
+    y = torch.empty(1, rows, dtype=torch.float32, device=dev)
+
+    def chain():
+        for _ in range(n):
+            gq.gq_matmul(gq.Q4_0, Wq, xq, y, rows, cols, 1)
+
+    def chain_fused():
+        for _ in range(n):
+            gq.gq_matmul_f32(gq.Q4_0, Wq, xd, y, rows, cols, 1, gq.FLAG_W_STATIC)
+
+    k = 50
+    t, _ = time_graph(capture(chain), k, 3)
+    tf, _ = time_graph(capture(chain_fused), k, 3)
+    if not torch.isfinite(y).all():
+        raise RuntimeError("non-finite Q4_0 GEMV output")
+    return {"workload": "Q4_0 x Q8_0 GEMV 512x1024 batch 1 (weights resident in L2)",
+            "us_per_gemv": t / (k * n) * 1e6, "us_per_gemv_fused_quantize": tf / (k * n) * 1e6,
+            "weight_bytes": Wq.numel(), "cpu_baseline": run_cpu_q4_0() if cpu else None}
 
 
 def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=False):

@@ -89,3 +89,9 @@ def test_q6k_cpu_baseline_times_the_oracle():
     r = bench.run_cpu_q6k(0.2)
     assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0 and r["cores"] >= 1
     assert "Q6_K GEMV 4096x4096" in r["sample"]
+
+
+def test_q4_0_cpu_baseline_times_the_oracle():
+    r = bench.run_cpu_q4_0(0.1)
+    assert r["kind"] == "oracle" and r["cores"] == 1 and r["us_per_gemv"] > 0
+    assert "Q4_0 GEMV 512x1024" in r["sample"]
