@@ -32,10 +32,10 @@ constexpr int KV_POS = 32;     // positions per warp
 constexpr int KV_MAX_NB = 8;   // head_dim <= 256
 
 // Test switch for the timeout path (set by gq_debug_kv_timeout, passed to
-// the kernel as an argument): warp 0 of every CTA expects 16 bytes more than
-// its span copy delivers, so its barrier never completes and its bounded
-// wait -- shortened to DEBUG_WAIT_LIMIT polls -- runs out.  The copy itself
-// is the ordinary, in-bounds one; nothing faults or hangs.
+// the kernel as an argument): warp 0 of every CTA arms its transfer barrier
+// for its span but issues no copy, so the barrier never completes and its
+// bounded wait -- shortened to DEBUG_WAIT_LIMIT polls -- runs out.  No copy
+// is in flight when the warp gives up and leaves; nothing faults or hangs.
 std::atomic<int> g_kv_debug_timeout{0};
 constexpr uint32_t DEBUG_WAIT_LIMIT = 4096;
 
@@ -153,8 +153,8 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     const bool starve = debug_starve != 0 && warp == 0;
     const uint32_t limit = starve ? DEBUG_WAIT_LIMIT : WAIT_LIMIT;
     if (bulk && lane == 0 && p0 < n_pos) {
-        mbar_arrive_expect_tx(span_bar + warp, span + (starve ? 16u : 0u));
-        bulk_g2s(st, cache + ((size_t)h * capacity + p0) * row_bytes, span, span_bar + warp);
+        mbar_arrive_expect_tx(span_bar + warp, span);
+        if (!starve) bulk_g2s(st, cache + ((size_t)h * capacity + p0) * row_bytes, span, span_bar + warp);
     }
 
     // query block `warp`: amax, d = fp16(amax / 127), code = roundf(x / d)
@@ -180,10 +180,12 @@ __global__ void __launch_bounds__(KV_WARPS * 32) kv_scores_kernel(const uint8_t 
     if (p0 >= n_pos) return;
     if (bulk) {
         if (!mbar_wait_limit(span_bar + warp, 0u, limit)) {
-            // the copy never completed: flag it, give it one more bounded
-            // wait before the CTA may exit, and leave these scores unwritten
+            // the copy never completed: flag it and leave these scores
+            // unwritten.  A real copy still in flight gets one more bounded
+            // wait before the CTA may exit (after a timeout the scores and
+            // the context are suspect); the test switch issued none.
             if (lane == 0) atomicOr(status, STATUS_KV_TMA_TIMEOUT);
-            mbar_wait_limit(span_bar + warp, 0u, limit);
+            if (!starve) mbar_wait_limit(span_bar + warp, 0u, limit);
             return;
         }
     } else {

@@ -5,14 +5,21 @@
 //
 // sm_103a has no integer MMA kind, so the contraction runs on the fp16 kind
 // with operands that are small integers, exactly representable in fp16:
-//   A[r][k] = sc_j(r) * q_k(r)        (<= 63 * 15 = 945)
+//   A[r][k] = sc_j(r) * q_k(r) - 512  (in [-512, 433])
 //   B[b][k] = a_k(b)                  (|a| <= 127, the Q8_K code)
-// Every product is exact and the fp32 accumulation of one 256-element
-// super-block is exact while partial sums stay below 2^24, so the tensor core
-// returns the integer S1 = sum_j sc_j * s_j of "llama.cpp 推理引擎" §5.5's
-// two-level scheme.  The min-term integer S2 = sum_j m_j * t_j (t_j the
-// activation sub-block sums) is one more K=16 step per super-block, with t_j
-// split exactly as t_lo + 64 t_hi:
+// Every product is exact (|A * B| <= 65024) and every partial sum of one
+// 256-element super-block is an integer of magnitude at most
+// 256 * 512 * 127 = 16,646,144 < 2^24, so the fp32 accumulation is exact in
+// any order.  (Without the offset, sc * q * a reaches 945 * 127 and a
+// super-block sum 3.07e7 > 2^24, where fp32 keeps only even integers.)  The
+// epilogue restores the integer S1 = sum_j sc_j * s_j of "llama.cpp 推理引擎"
+// §5.5's two-level scheme as
+//   S1 = S1' + 512 * asum(b),   asum(b) = sum of the super-block's 256 codes,
+// asum being stored per column and super-block by the pack kernel
+// (|S1| <= 3.07e7: one int32 add, or one fp32 fma that rounds the exact S1
+// once).  The min-term integer S2 = sum_j m_j * t_j (t_j the activation
+// sub-block sums) is one more K=16 step per super-block, with t_j split
+// exactly as t_lo + 64 t_hi:
 //   A2[r] = [m_0..m_7 | 64 m_0..64 m_7]   B2[b] = [t_lo_0..t_lo_7 | t_hi_0..t_hi_7]
 // (all exact in fp16, |S2| < 2^21).  Per super-block the epilogue promotes
 // both exact integers:
@@ -29,10 +36,11 @@
 //              the raw Q4_K rows into a ring of NRAW stages (box 144 bytes x
 //              128 rows; rows past the matrix read as zeros);
 //   warps 4-11 A builders: two threads per weight row, each turning half of
-//              the raw super-block into fp16 sc*q and storing it straight
+//              the raw super-block into fp16 sc*q - 512 and storing it straight
 //              from registers into tensor memory (tcgen05.st), where the MMA
 //              reads the A operand; then the min-term row (first half) or
-//              the row and column scales (second half);
+//              the row scales, column scales and column code sums
+//              (second half);
 //   warps 12-27 epilogue: four threads per row, 32 columns each (the warps
 //              whose columns lie past TN idle).
 // Per super-block a ready barrier (A and min-term rows built) and a done
@@ -112,12 +120,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, uint32_t fmt) {
 // Tile-width configuration.  A CTA computes TM weight rows x TN batch
 // columns (MMA N = TN).  Per (column tile, super-block) the workspace holds
 // one unit: the four B stage images (TN x 64 K fp16, 128-byte swizzled), the
-// min-term B tile and the column scales, contiguous.  Each unit arrives as
-// two bulk copies, issued by two producer warps (a warp completes about one
-// bulk copy per half microsecond however large, so one copy per warp per
-// super-block keeps the copies off the critical path): half 0 = stages 0-1;
-// half 1 = stages 2-3 and the min-term B tile.  The column scales are fetched
-// by builder threads with plain loads.  Narrow tiles (small batches) move
+// min-term B tile, the column scales and the column code sums (fp32),
+// contiguous.  Each unit arrives as two bulk copies, issued by two producer
+// warps (a warp completes about one bulk copy per half microsecond however
+// large, so one copy per warp per super-block keeps the copies off the
+// critical path): half 0 = stages 0-1; half 1 = stages 2-3 and the min-term
+// B tile.  The column scales and code sums are fetched by builder threads
+// with plain loads.  Narrow tiles (small batches) move
 // little activation data per super-block, so their period is set by the
 // weight rows; they get deeper activation (NBSB super-blocks) and weight
 // (NRAW) rings to cover the copy latency.
@@ -135,14 +144,17 @@ struct Cfg {
     static constexpr size_t WS_B = (size_t)NKS * OP_B;
     static constexpr size_t WS_MIN = MIN_B;
     static constexpr size_t WS_DX = TN * 4;
-    static constexpr size_t WS_UNIT = WS_B + WS_MIN + WS_DX;
+    static constexpr size_t WS_AS = TN * 4;   // per column: sum of the super-block's 256 codes
+    static constexpr size_t WS_UNIT = WS_B + WS_MIN + WS_DX + WS_AS;
     static constexpr int HALF0_BYTES = 2 * OP_B;
     static constexpr int HALF1_BYTES = 2 * OP_B + MIN_B;
     static constexpr int SLOT_B = (HALF1_BYTES + 1023) / 1024 * 1024;  // ring slot stride
     static constexpr int SLOT_MIN = 2 * OP_B;                          // inside a half-1 slot
-    // per super-block scales: d and dmin per row, dx per column (all fp32)
-    static constexpr int META_D = 0, META_DMIN = TM * 4, META_DX = 2 * TM * 4;
-    static constexpr int META_STAGE = 2 * TM * 4 + TN * 4;
+    // per super-block scales: d and dmin per row; per column the pair
+    // (dx, 512 * code sum) (all fp32; 512 times a code sum is an integer
+    // below 2^24 in magnitude, exact)
+    static constexpr int META_D = 0, META_DMIN = TM * 4, META_COL = 2 * TM * 4;
+    static constexpr int META_STAGE = 2 * TM * 4 + 2 * TN * 4;
     // Shared-memory layout (bytes from a 1024-aligned base).  The A operand
     // lives in tensor memory, not here.
     static constexpr int OFF_B = 0;                               // NBS x SLOT_B
@@ -225,26 +237,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4]) {
         : "memory");
 }
 
-// Two runs of 16 consecutive fp32 columns of this warp's 32 tensor-memory
+// Two runs of 8 consecutive fp32 columns of this warp's 32 tensor-memory
 // lanes, both loads in flight before one wait.
-__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
-    uint32_t r[32];
+__device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t tb, float (&va)[8], float (&vb)[8]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[14]), "=r"(r[15])
         : "r"(ta), "r"(tb));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
         va[i] = __uint_as_float(r[i]);
-        vb[i] = __uint_as_float(r[16 + i]);
+        vb[i] = __uint_as_float(r[8 + i]);
     }
 }
 
@@ -308,8 +316,9 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // which the A builders emit the weight nibbles -- into the 128-byte-swizzled
 // image of operand stage l / 8.  Lanes 0..7 also write the sub-block sum t_j
 // split exactly as t_lo = t mod 64 (K position j) and t_hi = floor(t / 64)
-// (K position 8 + j) of the min-term tile, and lane 0 the column scale dx.
-// Columns past the batch are zero.
+// (K position 8 + j) of the min-term tile, and lane 0 the column scale dx
+// and the column's code sum (the sum of the eight t_j).  Columns past the
+// batch are zero.
 template <int TN>
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ xq,
                                                    uint8_t *__restrict__ ws, int nsb, int batch) {
@@ -337,18 +346,25 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
         const uint4 chunk = make_uint4(pack_h2(a[0], a[4]), pack_h2(a[1], a[5]), pack_h2(a[2], a[6]),
                                        pack_h2(a[3], a[7]));
         *reinterpret_cast<uint4 *>(unit + (lane >> 3) * C::OP_B + sw128_off(c, lane & 7)) = chunk;
+        int t = 0;
+        if (valid && lane < 8) t = __ldg(reinterpret_cast<const int16_t *>(src + 260) + lane);
         if (lane < 8) {
-            int t = 0;
-            if (valid) t = __ldg(reinterpret_cast<const int16_t *>(src + 260) + lane);
             const int thi = t >> 6;          // floor(t / 64), in [-64, 63]
             const int tlo = t - 64 * thi;    // in [0, 63]
             uint8_t *mb = unit + C::WS_B;
             *reinterpret_cast<__half *>(mb + plain_off(c, 0) + 2 * lane) = __int2half_rn(tlo);
             *reinterpret_cast<__half *>(mb + plain_off(c, 1) + 2 * lane) = __int2half_rn(thi);
         }
-        if (lane == 0)
-            reinterpret_cast<float *>(unit + C::WS_B + C::WS_MIN)[c] =
-                valid ? __ldg(reinterpret_cast<const float *>(src)) : 0.0f;
+        // code sum of the column's super-block: lanes 0..7 hold t_0..t_7,
+        // the other lanes zero
+        int asum = t;
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) asum += __shfl_xor_sync(0xffffffffu, asum, o);
+        if (lane == 0) {
+            float *cs = reinterpret_cast<float *>(unit + C::WS_B + C::WS_MIN);
+            cs[c] = valid ? __ldg(reinterpret_cast<const float *>(src)) : 0.0f;
+            cs[TN + c] = (float)asum;  // exact: |asum| <= 256 * 127
+        }
     }
 }
 
@@ -458,10 +474,12 @@ __device__ __forceinline__ __half2 h2_bits(uint32_t v) { return *reinterpret_cas
 __device__ __forceinline__ uint32_t bits_h2(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
 
 // One packed nibble word (elements e0..e7 in nibbles 0..7) to the fp16 chunk
-// (sc e0, sc e4, sc e1, sc e5, sc e2, sc e6, sc e3, sc e7).  A nibble placed in
-// mantissa bits 0-3 (4-7) of 0x6400 gives the exact fp16 value 1024 + e
-// (1024 + 16 e); one fma with (sc, -1024 sc) -- or (sc / 16, -64 sc) --
-// yields sc * e exactly (every operand and result is representable).
+// (v e0, v e4, v e1, v e5, v e2, v e6, v e3, v e7), v e = sc e - 512.  A nibble
+// placed in mantissa bits 0-3 (4-7) of 0x6400 gives the exact fp16 value
+// 1024 + e (1024 + 16 e); one fma with (sc, -512 (2 sc + 1)) -- or
+// (sc / 16, -64 (sc + 8)) -- yields sc e - 512 exactly: both addends have at
+// most 7 significant bits, and the fused result, an integer in [-512, 433],
+// is representable.
 __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 c1, __half2 s16,
                                                 __half2 c16) {
     const uint32_t w8 = w >> 8;
@@ -480,8 +498,8 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
 // sub-block is 16 columns, written by one tcgen05.st from registers; the
 // buffer is free again once the epilogue has read the S2 written over it.
 // Then the hh = 0 threads write row t's min-term A row, the hh = 1 threads
-// row t's scales d, dmin and (t < TN) column t's scale dx (read from the
-// workspace, requested before the raw weights are waited for).
+// row t's scales d, dmin and (t < TN) column t's scale dx and code sum (read
+// from the workspace, requested before the raw weights are waited for).
 template <class C>
 __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const uint8_t *__restrict__ ws,
                              int ct, int rot, int nvalid, int nsb, volatile uint32_t *abort) {
@@ -493,10 +511,12 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
     for (int sb = 0; sb < nsb; ++sb) {
         const int ai = sb % C::NA;                              // A buffer
         const uint32_t aph = (uint32_t)(sb / C::NA) & 1u;       // parity of its use
-        float dx = 0.0f;
+        float dx = 0.0f, as = 0.0f;
         if (hh == 1 && t < C::TN) {
             const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * C::WS_UNIT;
-            dx = __ldg(reinterpret_cast<const float *>(unit + C::WS_B + C::WS_MIN) + t);
+            const float *cs = reinterpret_cast<const float *>(unit + C::WS_B + C::WS_MIN);
+            dx = __ldg(cs + t);
+            as = __ldg(cs + C::TN + t);
         }
         if (!wait_warp(B.raw_full + rr.idx, rr.phase, abort)) return;
         const uint8_t *raw = smem + C::OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
@@ -511,15 +531,15 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         mbar_arrive(B.raw_empty + rr.idx);
         rr.next();
 
-        // this half of the A operand: sc_j * q for sub-blocks 4hh .. 4hh + 3
+        // this half of the A operand: sc_j * q - 512 for sub-blocks 4hh .. 4hh + 3
         if (!wait_warp(B.a_empty + ai, aph ^ 1u, abort)) return;
         tc_fence_after();
         const uint64_t lo64 = (uint64_t)h.y | ((uint64_t)h.z << 32);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float sc = (float)(int)((lo64 >> (6 * (4 * hh + j))) & 63);
-            const __half2 s1 = __float2half2_rn(sc), c1 = __float2half2_rn(-1024.0f * sc);
-            const __half2 s16 = __float2half2_rn(sc * 0.0625f), c16 = __float2half2_rn(-64.0f * sc);
+            const __half2 s1 = __float2half2_rn(sc), c1 = __float2half2_rn(-512.0f * (2.0f * sc + 1.0f));
+            const __half2 s16 = __float2half2_rn(sc * 0.0625f), c16 = __float2half2_rn(-64.0f * (sc + 8.0f));
             uint4 v[4];
             v[0] = nibbles_to_f16(q[j].x, s1, c1, s16, c16);
             v[1] = nibbles_to_f16(q[j].y, s1, c1, s16, c16);
@@ -540,7 +560,9 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
             uint8_t *meta = smem + C::OFF_META + mr.idx * C::META_STAGE;
             reinterpret_cast<float *>(meta + C::META_D)[t] = half_bits_to_float(h.x);
             reinterpret_cast<float *>(meta + C::META_DMIN)[t] = half_bits_to_float(h.x >> 16);
-            if (t < C::TN) reinterpret_cast<float *>(meta + C::META_DX)[t] = dx;
+            if (t < C::TN) {
+                reinterpret_cast<float2 *>(meta + C::META_COL)[t] = make_float2(dx, 512.0f * as);
+            }
             mbar_arrive(B.meta_full + mr.idx);
         } else {
             const uint64_t hi64 = (uint64_t)h.z | ((uint64_t)h.w << 32);  // header bits 32..95
@@ -672,13 +694,15 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
         const uint8_t *meta = smem + C::OFF_META + mi * C::META_STAGE;
         const float d = reinterpret_cast<const float *>(meta + C::META_D)[r];
         const float dmin = reinterpret_cast<const float *>(meta + C::META_DMIN)[r];
-        const float *dx = reinterpret_cast<const float *>(meta + C::META_DX) + 32 * h;
+        const float2 *col = reinterpret_cast<const float2 *>(meta + C::META_COL) + 32 * h;
+        // eight columns at a time: S1 and S2 of the group, plus the column
+        // pairs, stay within the register budget next to the 32 accumulators
 #pragma unroll
-        for (int c0 = 0; c0 < 32; c0 += 16) {
-            float s1[16], s2[16];
-            tmem_ld16x2(lane_addr + C::col_s1(p) + c0, lane_addr + C::col_a(ai) + c0, s1, s2);
-            if (c0 == 16) {
-                // both halves are in registers: S1 and the A buffer may be reused
+        for (int c0 = 0; c0 < 32; c0 += 8) {
+            float s1[8], s2[8];
+            tmem_ld8x2(lane_addr + C::col_s1(p) + c0, lane_addr + C::col_a(ai) + c0, s1, s2);
+            if (c0 == 24) {
+                // all of S1 and S2 is in registers: S1 and the A buffer may be reused
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -688,18 +712,21 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
             }
             if (SUMS) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const int b = ct * TN + 32 * h + c0 + i;
                     if (row < rows && b < batch) {
                         int32_t *o = sums + (((size_t)b * rows + row) * nsb + kslot(sb, rot, nsb)) * 2;
-                        o[0] = (int32_t)s1[i];
+                        o[0] = (int32_t)s1[i] + (int32_t)col[c0 + i].y;
                         o[1] = (int32_t)s2[i];
                     }
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    yacc[c0 + i] = fmaf(dx[c0 + i], d * s1[i] - dmin * s2[i], yacc[c0 + i]);
+                for (int i = 0; i < 8; ++i) {
+                    const float2 cv = col[c0 + i];   // (dx, 512 * code sum)
+                    const float S1 = s1[i] + cv.y;   // the exact S1, rounded once
+                    yacc[c0 + i] = fmaf(cv.x, d * S1 - dmin * s2[i], yacc[c0 + i]);
+                }
             }
         }
         __syncwarp();

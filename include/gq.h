@@ -67,6 +67,10 @@
  *   - Thread safety: every entry point may be called from several host
  *     threads at once; the only shared state is a per-device attribute cache
  *     and the device status word.
+ *   - The per-device cache (attributes, and the device addresses of the
+ *     status word and of gq_matmul_noalloc's scratch) is filled on the first
+ *     call on each device and kept for the life of the process: calling the
+ *     library on a device after cudaDeviceReset() on it is unsupported.
  */
 #ifndef GQ_H
 #define GQ_H
@@ -188,12 +192,20 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  * The integer block sums are exact (int32); y matches the double-precision
  * sum of the same terms within 1e-4 of the sum of their magnitudes.
  * Asynchronous on `stream`; allocates nothing.
+ * Dispatch: this call has no workspace, so it always runs the GEMV kernels
+ * (any batch; a batch is processed in chunks of up to eight vectors, one
+ * pass over W per chunk).  The tensor-core kernel, which is faster from
+ * about batch 9-16 on (see gq_matmul_ws), needs a workspace for its
+ * repacked activations: call gq_matmul_ws, or gq_matmul_noalloc to use the
+ * library's static scratch.
  */
 gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
                     int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
 
 /* gq_matmul with an explicit kernel family (crossover studies, tests).
- * GQ_PATH_MMA is defined for Q4_K only (GQ_ERR_TYPE otherwise). */
+ * Without a workspace GQ_PATH_AUTO runs the GEMV kernels, and GQ_PATH_MMA
+ * returns GQ_ERR_NULL for Q4_K weights (the tensor-core kernel needs the
+ * workspace of gq_matmul_ws) and GQ_ERR_TYPE for the other types. */
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
                          int64_t rows, int64_t cols, int64_t batch, gq_path path,
                          gq_stream_t stream);
@@ -209,10 +221,10 @@ gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y,
 /*
  * Bytes of workspace the tensor-core path needs for this product (0 when the
  * shape or type has no tensor-core path).  The workspace holds the activation
- * operand repacked once per call as fp16 tiles (plus per-block scales and
- * the min-term operand), per column tile of tn = 32 (batch <= 32), 64
- * (batch <= 64) or 128 columns and per super-block: ceil(batch / tn) *
- * (cols / 256) * 548 tn bytes (17536, 35072 or 70144 per unit).
+ * operand repacked once per call as fp16 tiles (plus per-block scales, code
+ * sums and the min-term operand), per column tile of tn = 32 (batch <= 32),
+ * 64 (batch <= 64) or 128 columns and per super-block: ceil(batch / tn) *
+ * (cols / 256) * 552 tn bytes (17664, 35328 or 70656 per unit).
  */
 size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int64_t batch);
 
@@ -224,11 +236,11 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * gq_tc_min_batch(), or batch >= 9 on matrices of 14336 rows or more (the
  * measured crossovers), and the workspace suffices; the GEMV kernels
  * otherwise.  With GQ_TC_MIN_BATCH set, batch >= that value alone decides.
- * The tensor-core path computes the same y (within the tolerance above); its
- * integer super-block sums S1 are exact while partial sums of one super-block
- * stay below 2^24 in magnitude (always, unless codes and scales sit at their
- * extremes together).  Errors as gq_matmul_path, plus GQ_ERR_NULL (MMA path
- * without workspace), GQ_ERR_SHAPE (workspace too small), GQ_ERR_ALIGN.
+ * The tensor-core path computes the same y (within the tolerance above) and
+ * the same exact integer super-block sums S1 and S2 as the GEMV kernels, for
+ * every input (its fp32 accumulation only ever holds integers below 2^24).
+ * Errors as gq_matmul_path, plus GQ_ERR_NULL (MMA path without workspace),
+ * GQ_ERR_SHAPE (workspace too small), GQ_ERR_ALIGN.
  */
 gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y,
                        int64_t rows, int64_t cols, int64_t batch, gq_path path,
@@ -341,12 +353,14 @@ gq_status gq_kv_scores(gq_type type, const void *cache, const float *q, float *s
 
 /* Test switch for the device timeout path (not for production use).  With
  * on != 0, subsequent gq_kv_scores launches (process-wide) make one
- * warp per CTA wait, with a short poll limit, on a transfer barrier that
- * expects 16 bytes more than its copy delivers: the wait runs out, those
- * scores are left unwritten and gq_device_status() reports GQ_ERR_TIMEOUT.
- * Nothing faults or hangs, and the device stays usable.  on = 0 restores
- * normal operation.  Applies to key spans of 4 KB or more (Q8_0 keys at
- * head_dim >= 128).  Returns GQ_ERR_CUDA without a usable CUDA device. */
+ * warp per CTA arm its transfer barrier for its key span without issuing the
+ * copy and wait on it with a short poll limit: the wait runs out with no copy
+ * in flight, those scores are left unwritten and gq_device_status() reports
+ * GQ_ERR_TIMEOUT.  Nothing faults or hangs, and the device stays usable.
+ * on = 0 restores normal operation.  Applies to key spans of 4 KB or more
+ * (Q8_0 keys at head_dim >= 128).  Returns GQ_ERR_CUDA without a usable CUDA
+ * device.  (After a real timeout, as opposed to this switch, the results of
+ * the call that timed out and the state of the context are suspect.) */
 gq_status gq_debug_kv_timeout(int on);
 
 /* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for

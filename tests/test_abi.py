@@ -133,14 +133,14 @@ def test_fused_and_flag_validation(lib):
 def test_workspace_rules_on_host(lib):
     wb = lib.gq_matmul_workspace_bytes
     # tiles of 32 columns up to batch 32, 64 up to 64, then 128; one unit per
-    # (column tile, super-block) of 4 * tn * 128 + tn * 36 bytes
-    assert wb(2, 14336, 4096, 8) == 1 * 16 * 17536
-    assert wb(2, 14336, 4096, 32) == 1 * 16 * 17536
-    assert wb(2, 14336, 4096, 33) == 1 * 16 * 35072
-    assert wb(2, 14336, 4096, 64) == 1 * 16 * 35072
-    assert wb(2, 14336, 4096, 65) == 1 * 16 * 70144
-    assert wb(2, 14336, 4096, 129) == 2 * 16 * 70144
-    assert wb(2, 28672, 8192, 512) == 4 * 32 * 70144
+    # (column tile, super-block) of 4 * tn * 128 + tn * 40 bytes
+    assert wb(2, 14336, 4096, 8) == 1 * 16 * 17664
+    assert wb(2, 14336, 4096, 32) == 1 * 16 * 17664
+    assert wb(2, 14336, 4096, 33) == 1 * 16 * 35328
+    assert wb(2, 14336, 4096, 64) == 1 * 16 * 35328
+    assert wb(2, 14336, 4096, 65) == 1 * 16 * 70656
+    assert wb(2, 14336, 4096, 129) == 2 * 16 * 70656
+    assert wb(2, 28672, 8192, 512) == 4 * 32 * 70656
     assert wb(0, 128, 256, 64) == 0 and wb(2, 128, 100, 64) == 0 and wb(2, 0, 256, 64) == 0
     m = lib.gq_matmul_ws
     need = wb(2, 128, 256, 64)

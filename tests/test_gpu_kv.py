@@ -126,9 +126,9 @@ def test_kv_scores_full_size_sampled():
 
 def test_bounded_wait_runs_out_and_device_stays_usable():
     """Failure detection without a fault: with the test switch on, one warp
-    per CTA waits on a barrier that expects 16 bytes more than its copy
-    delivers; its short bounded wait runs out, the status word says so, and
-    the next (normal) call on the same context is correct."""
+    per CTA arms its transfer barrier for its key span but issues no copy;
+    its short bounded wait runs out with nothing in flight, the status word
+    says so, and the next (normal) call on the same context is correct."""
     t, n_heads, capacity, head_dim, n_pos = Q8_0, 2, 64, 128, 64
     ref, cache = filled_cache(t, n_heads, capacity, head_dim, n_fill=n_pos, seed=5)
     q = inputs.normal(inputs.rng(6), (n_heads, head_dim))

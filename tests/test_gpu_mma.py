@@ -73,7 +73,7 @@ def test_mma_auto_dispatch_and_workspace_rules():
     Wq = orc.quantize(Q4_K, inputs.normal(g, (rows, cols), 0.02))
     Xq = orc.quantize(Q8_K, inputs.normal(g, (batch, cols)))
     need = gq.gq_matmul_workspace_bytes(Q4_K, rows, cols, batch)
-    assert need == 1 * 2 * 35072  # one 64-column tile
+    assert need == 1 * 2 * 35328  # one 64-column tile
     assert gq.gq_matmul_workspace_bytes(0, rows, cols, batch) == 0
     y = torch.empty(batch, rows, device="cuda")
     with pytest.raises(gq.GQError):  # MMA without a workspace
@@ -105,6 +105,49 @@ def test_mma_degenerate_blocks():
     y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
     assert np.all(y[0] == 0)
     assert_close(y, y_ref, T)
+
+
+@pytest.mark.parametrize("batch", [5, 40, 100])  # tile widths 32, 64 and 128
+def test_mma_sums_beyond_fp32_integers(batch):
+    """Super-block sums S1 = sum_j sc_j * s_j reach 63 * 15 * 127 * 256 =
+    30,723,840, beyond 2^24, where fp32 holds only even integers: constant
+    rows (every sc = 63, every code 15) with one or several codes lowered to
+    14, against constant activations (every code +-127), give odd S1 near
+    3.07e7.  The tensor-core sums must still equal the oracle's bit for bit
+    ("llama.cpp 推理引擎" §5.5: the two-level dequantization whose integer
+    sums are exact)."""
+    rows, cols = 131, 512
+    W = inputs.outlier_weights(inputs.rng(7), rows, cols, frac=0.001)
+    W[0] = 1.0
+    W[0, 5] = 0.93                                  # one code 14 among 15s
+    W[1] = 1.0                                      # every code 15
+    W[2] = 1.0
+    W[2, 1::2] = 0.93                               # alternating 15 / 14
+    W[3] = 1.0
+    W[3, 300] = 0.0                                 # one zero, second super-block
+    W[4] = np.where(np.arange(cols) % 3 == 0, 1.0, 0.55)
+    W[130] = 1.0                                    # last row of a ragged tile
+    W[130, 255] = 0.93
+    X = inputs.normal(inputs.rng(8), (batch, cols))
+    X[0] = 1.0                                      # every code +127
+    X[1] = -1.0                                     # every code -127
+    X[2] = 1.0
+    X[2, 7] = 0.99
+    X[3] = 1.0
+    X[3, ::5] = -1.0
+    X[batch - 1] = 1.0                              # last column of the tile
+    Wq, Xq = orc.quantize(Q4_K, W), orc.quantize(Q8_K, X)
+    s_ref = orc.block_sums(Q4_K, Wq, Xq, rows, cols, batch)
+    S1 = s_ref[..., 0]
+    assert np.sum((np.abs(S1) > 2**24) & (S1 % 2 != 0)) >= 10  # the case is exercised
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = host(gq.block_sums(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA))
+    np.testing.assert_array_equal(s, s_ref)
+    y = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA))
+    y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+    s_g = host(gq.block_sums(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    np.testing.assert_array_equal(s_g, s_ref)
 
 
 def sampled_rows(rows, k, seed):
