@@ -223,10 +223,119 @@ def run_cpu_baseline(seconds=10.0, seconds_one=4.0):
         nq += 1
     tq = (time.perf_counter() - t0) / nq
     return {"value": n * Wq.nbytes / dt / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{n} x (Q8_K act-quant + Q4_K GEMV 4096x4096, batch 1) in {dt:.1f} s",
             "single_core": {"value": n1 * Wq.nbytes / dt1 / 1e9, "unit": "GB/s", "cores": 1,
                             "sample": f"{n1} x the same in {dt1:.1f} s"},
             "act_quantize_us": tq * 1e6}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the
+    baselines' records."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _time_call(fn, budget):
+    """Median-free simple rate: repeat fn for about `budget` seconds; seconds
+    per call."""
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget:
+            return dt / n
+
+
+def run_cpu_configs(budget=0.25):
+    """The oracle, as it stands, timed on the host cores for the other
+    workloads, each on a bounded row sample scaled to the full shape (the
+    product's cost is linear in the rows): the 7B-shape decode token (every
+    layer matrix and the Q8_0 head, with their activation quantizes), the
+    14336x4096 batch sweep, and the 28672x8192x512 prefill.  One core and all
+    cores."""
+    import oracle as orc
+    from block_quantized_gb300 import inputs
+    nt = orc.max_threads()
+    g = inputs.rng(11)
+    cache = {}
+
+    def sample(wtype, rows, cols):
+        key = (wtype, rows, cols)
+        if key not in cache:
+            cache[key] = orc.quantize(wtype, inputs.normal(g, (rows, cols), 0.02))
+        return cache[key]
+
+    def act(atype, batch, cols):
+        return orc.quantize(atype, inputs.normal(g, (batch, cols)))
+
+    out = {"cores_all": nt, "cpu_model": cpu_model()}
+    # 7B decode token: rows sampled per matrix
+    R = 256
+    layer = [("wq", 4096, 4096), ("wk", 4096, 4096), ("wv", 4096, 4096), ("wo", 4096, 4096),
+             ("w1", 11008, 4096), ("w3", 11008, 4096), ("w2", 4096, 11008)]
+    xq = {c: act(orc.Q8_K, 1, c) for c in (4096, 11008)}
+    xh = act(orc.Q8_0, 1, 4096)
+    xf = {c: inputs.normal(g, (c,)) for c in (4096, 11008)}
+    dec = {}
+    for label, threads in (("all_cores", nt), ("one_core", 1)):
+        t_layer = 0.0
+        for _, rows, cols in layer:
+            W = sample(orc.Q4_K, R, cols)
+            t = _time_call(lambda: orc.matmul_ref(orc.Q4_K, W, xq[cols], R, cols, 1, threads), budget)
+            t_layer += t * rows / R
+        # four activation quantizes per layer (attention, o, ffn, down)
+        tq = sum(_time_call(lambda: orc.quantize(orc.Q8_K, xf[c]), budget / 4) for c in (4096, 4096, 4096, 11008))
+        Wh = sample(orc.Q8_0, R, 4096)
+        t_head = _time_call(lambda: orc.matmul_ref(orc.Q8_0, Wh, xh, R, 4096, 1, threads), budget) * 32000 / R
+        t_tok = 32 * (t_layer + tq) + t_head
+        dec[label] = {"tok_s": 1.0 / t_tok, "ms_per_token": t_tok * 1e3,
+                      "cores": threads}
+    dec["sample"] = (f"{R} rows of each layer matrix and of the 32000x4096 Q8_0 head, scaled by rows; "
+                     "32 layers + head; the act-quantize of the four layer inputs included")
+    out["decode_7b"] = dec
+    # batch sweep 14336 x 4096
+    R4 = 256
+    W4 = sample(orc.Q4_K, R4, 4096)
+    sweep = {}
+    for b in (1, 2, 4, 8, 16, 32, 64):
+        xb = act(orc.Q8_K, b, 4096)
+        row = {}
+        for label, threads in (("all_cores", nt), ("one_core", 1)):
+            t = _time_call(lambda: orc.matmul_ref(orc.Q4_K, W4, xb, R4, 4096, b, threads), budget / 2)
+            t_full = t * 14336 / R4
+            row[label] = {"us": t_full * 1e6, "tops": 2.0 * 14336 * 4096 * b / t_full / 1e12}
+        sweep[str(b)] = row
+    out["batch_sweep_14336x4096"] = {"results": sweep,
+                                     "sample": f"{R4} of the 14336 rows, scaled by rows"}
+    # prefill 28672 x 8192 x 512
+    R5 = 32
+    W5 = sample(orc.Q4_K, R5, 8192)
+    x5 = act(orc.Q8_K, 512, 8192)
+    pre = {}
+    for label, threads in (("all_cores", nt), ("one_core", 1)):
+        t = _time_call(lambda: orc.matmul_ref(orc.Q4_K, W5, x5, R5, 8192, 512, threads), budget)
+        t_full = t * 28672 / R5
+        pre[label] = {"ms": t_full * 1e3, "tops": 2.0 * 28672 * 8192 * 512 / t_full / 1e12}
+    pre["sample"] = f"{R5} of the 28672 rows x 512 columns, scaled by rows"
+    out["prefill_28672x8192x512"] = pre
+    return out
 
 
 def run_cpu_q6k(seconds=3.0):
@@ -471,9 +580,11 @@ def run_gpu(args, world, rank):
         extras["q6k"] = leg(bench_q6k, gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=cpu_leg)
         extras["q4_0_512x1024"] = leg(bench_q4_0, gq, inputs, torch, np, dev, capture, time_graph, cpu=cpu_leg)
 
-    cpu = None
+    cpu = cpu_configs = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = run_cpu_baseline()
+        if not args.quick:
+            cpu_configs = leg(run_cpu_configs)
 
     if rank == 0:
         line = {
@@ -494,9 +605,47 @@ def run_gpu(args, world, rank):
             "clocks": clk,
         }
         line.update(extras)
+        line["cpu_baseline_configs"] = cpu_configs
+        # the headline figures of every workload once more, last, in a few
+        # hundred bytes: records that keep only the end of the line keep these
+        line["summary"] = summary_keys(line)
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def summary_keys(line: dict) -> dict:
+    """A compact digest of the line's workloads (rounded), emitted as its last
+    key."""
+    def get(d, *path):
+        for k in path:
+            if not isinstance(d, dict) or k not in d:
+                return None
+            d = d[k]
+        return d
+
+    def r(v, n=3):
+        return None if v is None else round(float(v), n)
+
+    out = {"gemv_4096_gbps": r(line.get("value"), 1), "gemv_4096_frac": r(get(line, "roofline", "frac")),
+           "gemv_4096_launch_us": r(get(line, "roofline", "launch_us")),
+           "stream_frac": r(get(line, "roofline_streaming", "frac")),
+           "decode_tok_s": r(get(line, "decode", "tok_s"), 1),
+           "decode_fused_weights_tok_s": r(get(line, "decode", "fused_weights", "tok_s"), 1),
+           "prefill_ms": r(get(line, "prefill", "results", "mma", "ms"), 4),
+           "prefill_tops": r(get(line, "prefill", "results", "mma", "tops"), 1),
+           "prefill_frac": r(get(line, "prefill", "results", "mma", "roofline", "frac"))}
+    sweep = get(line, "batch_sweep", "results")
+    if isinstance(sweep, dict):
+        out["sweep_us_gemv_mma"] = {b: [r(get(v, "gemv", "us"), 1), r(get(v, "mma", "us"), 1)]
+                                    for b, v in sweep.items()}
+        mma_wins = [int(b) for b, v in sweep.items() if v.get("faster") == "mma"]
+        out["sweep_crossover_batch"] = min(mma_wins) if mma_wins else None
+    out["q6k_frac"] = r(get(line, "q6k", "frac"))
+    out["kv_q8_0_frac"] = r(get(line, "kv_cache", "q8_0", "frac"))
+    out["cpu_oracle_gbps_all_cores"] = r(get(line, "cpu_baseline", "value"))
+    out["cpu_oracle_decode_tok_s"] = r(get(line, "cpu_baseline_configs", "decode_7b", "all_cores", "tok_s"), 4)
+    return out
 
 
 def bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak, steps):

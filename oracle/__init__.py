@@ -20,9 +20,9 @@ import threading
 
 import numpy as np
 
-Q4_0, Q8_0, Q4_K, Q8_K, Q6_K = 0, 1, 2, 3, 4
-TYPE_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q8_K: "Q8_K", Q6_K: "Q6_K"}
-ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K}
+Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K = 0, 1, 2, 3, 4, 5
+TYPE_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q8_K: "Q8_K", Q6_K: "Q6_K", Q5_K: "Q5_K"}
+ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q5_K: Q8_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gq_oracle.c")
@@ -166,11 +166,11 @@ def dequantize_f64(t: int, q: np.ndarray, n: int) -> np.ndarray:
 def block_sums(wtype: int, W: np.ndarray, xq: np.ndarray, rows: int, cols: int,
                batch: int) -> np.ndarray:
     """Integer per-block sums, shape [batch, rows, cols/B] (Q4_0, Q8_0, Q6_K)
-    or [batch, rows, cols/256, 2] (Q4_K: S1, S2)."""
+    or [batch, rows, cols/256, 2] (Q4_K, Q5_K: S1, S2)."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
     xq = np.ascontiguousarray(xq, dtype=np.uint8)
     nb = cols // block_elems(wtype)
-    shape = (batch, rows, nb, 2) if wtype == Q4_K else (batch, rows, nb)
+    shape = (batch, rows, nb, 2) if wtype in (Q4_K, Q5_K) else (batch, rows, nb)
     out = np.empty(shape, dtype=np.int32)
     rc = lib().or_block_sums(wtype, _ptr(W), _ptr(xq), rows, cols, batch, _ptr(out))
     if rc != 0:

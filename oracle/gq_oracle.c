@@ -43,6 +43,11 @@
  *     describes them): symmetric rule with scale = max|x| / 31, codes
  *     c = q + 32 with q clamped to [-32, 31]; layout this library's own (see
  *     quantize_q6_k_block).  It pairs with Q8_K activations.
+ *   - Q5_K (the same page's §4: one bit more than the 4-bit K-quant): the
+ *     Q4_K super-block -- fp16 d and dmin, 6-bit sub-block scales and mins,
+ *     the same min/max fit -- with 5-bit codes q in [0, 31], whose fifth
+ *     bits sit in a bit plane of their own; layout this library's own (see
+ *     quantize_q5_k_block).  It pairs with Q8_K activations.
  *   - A zero scale yields zero codes (Q4_0 code 8, Q6_K code 32).
  *   - Non-finite inputs are rejected (return -2).
  *
@@ -58,7 +63,7 @@
 #endif
 
 /* Type codes, in the order of the public type enumeration. */
-enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q8_K = 3, OR_Q6_K = 4 };
+enum { OR_Q4_0 = 0, OR_Q8_0 = 1, OR_Q4_K = 2, OR_Q8_K = 3, OR_Q6_K = 4, OR_Q5_K = 5 };
 
 /* ------------------------------------------------------------------ */
 /* Bit-level helpers                                                    */
@@ -190,7 +195,7 @@ int64_t or_block_elems(int type)
 {
     switch (type) {
     case OR_Q4_0: case OR_Q8_0: return 32;
-    case OR_Q4_K: case OR_Q8_K: case OR_Q6_K: return 256;
+    case OR_Q4_K: case OR_Q8_K: case OR_Q6_K: case OR_Q5_K: return 256;
     }
     return -1;
 }
@@ -201,7 +206,9 @@ int64_t or_block_elems(int type)
  *       nibbles.
  * Q8_K: fp32 d, 256 int8, eight int16 sub-block sums.
  * Q6_K: fp16 d, 128 bytes holding the low four bits of the 256 codes, 64
- *       bytes holding their top two bits. */
+ *       bytes holding their top two bits.
+ * Q5_K: the Q4_K fields (144 bytes) and 32 bytes holding the fifth bit of
+ *       each of the 256 codes. */
 int64_t or_block_bytes(int type)
 {
     switch (type) {
@@ -210,6 +217,7 @@ int64_t or_block_bytes(int type)
     case OR_Q4_K: return 2 + 2 + 12 + 128;
     case OR_Q8_K: return 4 + 256 + 2 * 8;
     case OR_Q6_K: return 2 + 128 + 64;
+    case OR_Q5_K: return 2 + 2 + 12 + 128 + 32;
     }
     return -1;
 }
@@ -288,17 +296,21 @@ static void unpack6(const uint8_t in[12], uint8_t f[16])
     }
 }
 
-/* Q4_K ([P2] §5.2 asymmetric fit per 32-element sub-block, §5.5 two-level
- * scales; [P4] 256 = 8 x 32 super-block).  For sub-block j:
+/* The asymmetric K-quant fit of one 256-element super-block with codes in
+ * [0, qmax] ([P2] §5.2 asymmetric fit per 32-element sub-block, §5.5
+ * two-level scales; [P4] 256 = 8 x 32 super-block).  For sub-block j:
  *   lo_j = min(0, min x), hi_j = max x
  *   dmin = f16_ru(max_j(-lo_j) / 63),  m_j = min(63, ceil(-lo_j / dmin))
  *   base_j = -(dmin * m_j)                      (exact in fp32)
  *   r_j = hi_j - base_j
- *   d = f16_ru(max_j r_j / 945),  sc_j = min(63, ceil(r_j / (15 d)))
+ *   d = f16_ru(max_j r_j / (63 qmax)),  sc_j = min(63, ceil(r_j / (qmax d)))
  *   step_j = d * sc_j                           (exact in fp32)
- *   q_i = clamp(round((x_i - base_j) / step_j), 0, 15)
- * and the element is reconstructed as d*sc_j*q_i - dmin*m_j. */
-static void quantize_q4_k_block(const float *x, uint8_t *blk)
+ *   q_i = clamp(round((x_i - base_j) / step_j), 0, qmax)
+ * and the element is reconstructed as d*sc_j*q_i - dmin*m_j.  Q4_K takes
+ * qmax = 15 (63 qmax = 945), Q5_K qmax = 31 (1953).  Writes the fp16 d and
+ * dmin, the sixteen 6-bit fields (sc_0..sc_7, m_0..m_7) and the codes. */
+static void k_asym_fit(const float *x, float qmax, uint16_t *dh_out, uint16_t *dminh_out,
+                       uint8_t fields[16], uint8_t q[256])
 {
     float lo[8], hi[8];
     for (int j = 0; j < 8; j++) {
@@ -328,31 +340,76 @@ static void quantize_q4_k_block(const float *x, uint8_t *blk)
         r[j] = hi[j] - base[j];
         if (r[j] > r_max) r_max = r[j];
     }
-    uint16_t dh = or_f16_ru(r_max / 945.0f);
+    uint16_t dh = or_f16_ru(r_max / (63.0f * qmax));
     float d = or_f16_to_f32(dh);
     for (int j = 0; j < 8; j++) {
-        float s = (d == 0.0f) ? 0.0f : ceilf(r[j] / (15.0f * d));
+        float s = (d == 0.0f) ? 0.0f : ceilf(r[j] / (qmax * d));
         if (s > 63.0f) s = 63.0f;
         sc[j] = (uint8_t)s;
     }
-
-    put_u16(blk + 0, dh);
-    put_u16(blk + 2, dminh);
-    uint8_t fields[16];
-    for (int j = 0; j < 8; j++) { fields[j] = sc[j]; fields[8 + j] = m[j]; }
-    pack6(fields, blk + 4);
-
-    uint8_t q[256];
     for (int j = 0; j < 8; j++) {
         float step = d * (float)sc[j];
         for (int i = 0; i < 32; i++) {
             float v = (step == 0.0f) ? 0.0f
-                      : clampf(rha((x[32 * j + i] - base[j]) / step), 0.0f, 15.0f);
+                      : clampf(rha((x[32 * j + i] - base[j]) / step), 0.0f, qmax);
             q[32 * j + i] = (uint8_t)v;
         }
     }
+    *dh_out = dh;
+    *dminh_out = dminh;
+    for (int j = 0; j < 8; j++) { fields[j] = sc[j]; fields[8 + j] = m[j]; }
+}
+
+/* Q4_K: the fit with 4-bit codes; layout fp16 d @0, fp16 dmin @2, the
+ * sixteen 6-bit fields @4, then byte l of the 128 code bytes holds element
+ * 2l in its low nibble and 2l+1 in its high nibble. */
+static void quantize_q4_k_block(const float *x, uint8_t *blk)
+{
+    uint16_t dh, dminh;
+    uint8_t fields[16], q[256];
+    k_asym_fit(x, 15.0f, &dh, &dminh, fields, q);
+    put_u16(blk + 0, dh);
+    put_u16(blk + 2, dminh);
+    pack6(fields, blk + 4);
     for (int l = 0; l < 128; l++)
         blk[16 + l] = (uint8_t)(q[2 * l] | (q[2 * l + 1] << 4));
+}
+
+/* Q5_K: the 5-bit K-quant, one bit more than Q4_K (the discosf.com page
+ * "为什么说 llama.cpp 是'裸引擎'——从模型加载的每一行代码说起", §4 量化不是"压缩"，
+ * 而是"精度重分配": Q5_K_S carries one bit more than Q4_K_M).  The pages give
+ * no layout; the reading taken is the Q4_K super-block and fit with codes
+ * in [0, 31].  Layout (this library's own): the Q4_K fields and low four
+ * bits of the codes in bytes 0..143 exactly as Q4_K, then 32 bytes @144 with
+ * the fifth bits: byte 144 + 4j + i holds, in bit 2t + p, the fifth bit of
+ * element 32j + 8t + 2i + p (sub-block j, t = 0..3, i = 0..3, p = 0..1). */
+static void quantize_q5_k_block(const float *x, uint8_t *blk)
+{
+    uint16_t dh, dminh;
+    uint8_t fields[16], q[256];
+    k_asym_fit(x, 31.0f, &dh, &dminh, fields, q);
+    put_u16(blk + 0, dh);
+    put_u16(blk + 2, dminh);
+    pack6(fields, blk + 4);
+    for (int l = 0; l < 128; l++)
+        blk[16 + l] = (uint8_t)((q[2 * l] & 15) | ((q[2 * l + 1] & 15) << 4));
+    for (int k = 0; k < 32; k++) blk[144 + k] = 0;
+    for (int e = 0; e < 256; e++) {
+        int j = e / 32, t = (e % 32) / 8, i = (e % 8) / 2, p = e % 2;
+        if (q[e] >> 4) blk[144 + 4 * j + i] |= (uint8_t)(1u << (2 * t + p));
+    }
+}
+
+/* The stored code of element e of a Q4_K (0..15) or Q5_K (0..31) block. */
+static int k_code(int type, const uint8_t *blk, int e)
+{
+    int byte = blk[16 + e / 2];
+    int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);
+    if (type == OR_Q5_K) {
+        int j = e / 32, t = (e % 32) / 8, i = (e % 8) / 2, p = e % 2;
+        q |= ((blk[144 + 4 * j + i] >> (2 * t + p)) & 1) << 4;
+    }
+    return q;
 }
 
 /* Q8_K: the 256-element activation block.  Same symmetric rule as Q8_0 but
@@ -438,6 +495,7 @@ int or_quantize(int type, const float *x, uint8_t *dst, int64_t n)
         case OR_Q4_K: quantize_q4_k_block(xb, ob); break;
         case OR_Q8_K: quantize_q8_k_block(xb, ob); break;
         case OR_Q6_K: quantize_q6_k_block(xb, ob); break;
+        case OR_Q5_K: quantize_q5_k_block(xb, ob); break;
         }
     }
     return 0;
@@ -448,8 +506,8 @@ int or_quantize(int type, const float *x, uint8_t *dst, int64_t n)
 /* ------------------------------------------------------------------ */
 
 /* Per-element reconstruction of one block, exact in double:
- *   Q4_0: d * (c - 8)      Q8_0, Q8_K: d * q      Q4_K: d*sc_j*q - dmin*m_j
- *   Q6_K: d * (c - 32)
+ *   Q4_0: d * (c - 8)      Q8_0, Q8_K: d * q
+ *   Q4_K, Q5_K: d*sc_j*q - dmin*m_j      Q6_K: d * (c - 32)
  * Every product of an fp16 (or fp32) scale with these small integers, and
  * the Q4_K difference, fits in the 53-bit double significand. */
 static void decode_block_f64(int type, const uint8_t *blk, double *out)
@@ -468,15 +526,14 @@ static void decode_block_f64(int type, const uint8_t *blk, double *out)
         for (int i = 0; i < 32; i++) out[i] = d * (double)(int8_t)blk[2 + i];
         break;
     }
-    case OR_Q4_K: {
+    case OR_Q4_K: case OR_Q5_K: {
         double d = or_f16_to_f32(get_u16(blk + 0));
         double dmin = or_f16_to_f32(get_u16(blk + 2));
         uint8_t f[16];
         unpack6(blk + 4, f);
         for (int e = 0; e < 256; e++) {
             int j = e / 32;
-            int byte = blk[16 + e / 2];
-            int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);
+            int q = k_code(type, blk, e);
             out[e] = d * (double)f[j] * (double)q - dmin * (double)f[8 + j];
         }
         break;
@@ -527,7 +584,7 @@ static int pairing_ok(int wtype, int *atype)
 {
     switch (wtype) {
     case OR_Q4_0: case OR_Q8_0: *atype = OR_Q8_0; return 1;
-    case OR_Q4_K: case OR_Q6_K: *atype = OR_Q8_K; return 1;
+    case OR_Q4_K: case OR_Q6_K: case OR_Q5_K: *atype = OR_Q8_K; return 1;
     }
     return 0;
 }
@@ -535,7 +592,8 @@ static int pairing_ok(int wtype, int *atype)
 /* Integer dot of one weight block against one activation block.
  *   Q4_0 x Q8_0: s = sum_i (c_i - 8) * a_i          ([P2] §6.4)
  *   Q8_0 x Q8_0: s = sum_i w_i * a_i
- *   Q4_K x Q8_K: s_j = sum_{i in j} q_i * a_i per sub-block,
+ *   Q4_K x Q8_K (and Q5_K x Q8_K):
+ *                s_j = sum_{i in j} q_i * a_i per sub-block,
  *                S1 = sum_j sc_j * s_j,  S2 = sum_j m_j * t_j
  *                with t_j the activation sub-block sum (stored bsums).
  *   Q6_K x Q8_K: s = sum_i (c_i - 32) * a_i over the 256 elements.
@@ -564,7 +622,7 @@ static int block_int_dot(int wtype, const uint8_t *w, const uint8_t *a, int32_t 
         out[0] = s;
         return 1;
     }
-    /* Q4_K x Q8_K */
+    /* Q4_K / Q5_K x Q8_K */
     uint8_t f[16];
     unpack6(w + 4, f);
     int32_t S1 = 0, S2 = 0;
@@ -572,9 +630,7 @@ static int block_int_dot(int wtype, const uint8_t *w, const uint8_t *a, int32_t 
         int32_t s = 0;
         for (int i = 0; i < 32; i++) {
             int e = 32 * j + i;
-            int byte = w[16 + e / 2];
-            int q = (e & 1) ? (byte >> 4) : (byte & 0x0f);
-            s += q * (int8_t)a[4 + e];
+            s += k_code(wtype, w, e) * (int8_t)a[4 + e];
         }
         int16_t t = (int16_t)get_u16(a + 260 + 2 * j);
         S1 += (int32_t)f[j] * s;
@@ -587,7 +643,7 @@ static int block_int_dot(int wtype, const uint8_t *w, const uint8_t *a, int32_t 
 
 /* Per-block integer sums of the whole product.
  * Layout: out[b][r][k][c] with k over the weight blocks of a row and
- * c = 1 (Q4_0, Q8_0) or 2 (Q4_K: S1, S2). */
+ * c = 1 (Q4_0, Q8_0, Q6_K) or 2 (Q4_K, Q5_K: S1, S2). */
 int or_block_sums(int wtype, const uint8_t *W, const uint8_t *xq, int64_t rows,
                   int64_t cols, int64_t batch, int32_t *out)
 {
@@ -596,7 +652,7 @@ int or_block_sums(int wtype, const uint8_t *W, const uint8_t *xq, int64_t rows,
     int64_t be = or_block_elems(wtype);
     if (rows < 0 || batch < 0 || cols < 0 || cols % be) return -1;
     int64_t nb = cols / be, wbb = or_block_bytes(wtype), abb = or_block_bytes(atype);
-    int c = (wtype == OR_Q4_K) ? 2 : 1;
+    int c = (wtype == OR_Q4_K || wtype == OR_Q5_K) ? 2 : 1;
     for (int64_t b = 0; b < batch; b++)
         for (int64_t r = 0; r < rows; r++)
             for (int64_t k = 0; k < nb; k++)
@@ -608,13 +664,13 @@ int or_block_sums(int wtype, const uint8_t *W, const uint8_t *xq, int64_t rows,
 /* Scale terms of one block pair in double:
  *   Q4_0 / Q8_0: d_w * d_x * s      (d_x the fp16 Q8_0 scale)
  *   Q6_K:        d_w * d_x * s      (d_x the fp32 Q8_K scale)
- *   Q4_K:        d_x * d * S1   and   -(d_x * dmin * S2)
+ *   Q4_K, Q5_K:  d_x * d * S1   and   -(d_x * dmin * S2)
  * y accumulates the terms, T their absolute values. */
 static void block_terms(int wtype, const uint8_t *w, const uint8_t *a, double *y, double *T)
 {
     int32_t s[2];
     block_int_dot(wtype, w, a, s);
-    if (wtype == OR_Q4_K) {
+    if (wtype == OR_Q4_K || wtype == OR_Q5_K) {
         double dx = get_f32(a);
         double d = or_f16_to_f32(get_u16(w + 0));
         double dmin = or_f16_to_f32(get_u16(w + 2));

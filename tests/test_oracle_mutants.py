@@ -74,6 +74,18 @@ MUTANTS = [
      "double dw = or_f16_to_f32(get_u16(w));\n        double dx = get_f32(a);\n        double t = dw",
      "double dw = or_f16_to_f32(get_u16(w));\n        double dx = or_f16_to_f32(get_u16(a));\n        double t = dw",
      "bruteforce"),
+    ("q5_k fifth bits packed in the wrong bit positions",
+     "if (q[e] >> 4) blk[144 + 4 * j + i] |= (uint8_t)(1u << (2 * t + p));",
+     "if (q[e] >> 4) blk[144 + 4 * j + i] |= (uint8_t)(1u << (t + 4 * p));",
+     "q5_k_handmade"),
+    ("q5_k fit with 30 code steps instead of 31",
+     "k_asym_fit(x, 31.0f, &dh, &dminh, fields, q);",
+     "k_asym_fit(x, 30.0f, &dh, &dminh, fields, q);",
+     "q5_k_handmade"),
+    ("q5_k fifth bit weighted 8 instead of 16 when read",
+     "q |= ((blk[144 + 4 * j + i] >> (2 * t + p)) & 1) << 4;",
+     "q |= ((blk[144 + 4 * j + i] >> (2 * t + p)) & 1) << 3;",
+     "integer_special_case_q5_k"),
     ("q8_0 scale max/128 instead of max/127",
      "uint16_t dh = or_f16_rn(amax / 127.0f);",
      "uint16_t dh = or_f16_rn(amax / 128.0f);",

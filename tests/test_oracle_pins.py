@@ -13,7 +13,7 @@ import oracle as orc
 from block_quantized_gb300 import inputs
 from conftest import read_golden
 
-Q4_0, Q8_0, Q4_K, Q8_K, Q6_K = orc.Q4_0, orc.Q8_0, orc.Q4_K, orc.Q8_K, orc.Q6_K
+Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K = orc.Q4_0, orc.Q8_0, orc.Q4_K, orc.Q8_K, orc.Q6_K, orc.Q5_K
 
 
 def hexbytes(tokens):
@@ -34,7 +34,10 @@ def test_block_sizes():
     # Q6_K: 256 six-bit codes (192 bytes) and one fp16 scale
     assert (orc.block_elems(Q6_K), orc.block_bytes(Q6_K)) == (256, 194)
     assert orc.block_bytes(Q6_K) == 256 * 6 // 8 + 2
-    for t in (Q4_0, Q8_0, Q4_K, Q8_K, Q6_K):
+    # Q5_K: the 144 Q4_K bytes plus one bit per element (5.5 bits per weight)
+    assert (orc.block_elems(Q5_K), orc.block_bytes(Q5_K)) == (256, 176)
+    assert orc.block_bytes(Q5_K) == orc.block_bytes(Q4_K) + 256 // 8
+    for t in (Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K):
         x = np.zeros(orc.block_elems(t) * 3, np.float32)
         assert orc.quantize(t, x).shape == (3, orc.block_bytes(t))
 
@@ -108,6 +111,39 @@ def test_q4_k_handmade_block():
     assert blk.tobytes() == expect.tobytes()
     # every element lies on its grid, so the reconstruction is exact
     np.testing.assert_array_equal(orc.dequantize(Q4_K, blk, 256), x)
+
+
+def test_q5_k_handmade_block():
+    g = read_golden("q5_k_handmade.txt")
+    r = np.arange(32)
+    x = np.zeros(256, np.float32)
+    x[0:32] = (63 * r - 504) / 512.0
+    x[32:64] = 3 * (31 - r) / 512.0
+    x[64:96] = -0.5 + ((7 * r) % 32) / 256.0
+    blk = orc.quantize(Q5_K, x)[0]
+    expect = np.concatenate([hexbytes(g["header"]), hexbytes(g["scales"]), hexbytes(g["qs0"]),
+                             hexbytes(g["qs1"]), hexbytes(g["qs2"]), np.zeros(80, np.uint8),
+                             hexbytes(g["qh0"]), hexbytes(g["qh1"]), hexbytes(g["qh2"]), np.zeros(20, np.uint8)])
+    assert blk.tobytes() == expect.tobytes()
+    # every element lies on its grid, so the reconstruction is exact
+    np.testing.assert_array_equal(orc.dequantize(Q5_K, blk, 256), x)
+
+
+def test_q5_k_ties_round_half_away():
+    """Codes round half away from zero: in a sub-block with min 0 (m = 0) and
+    step 3/512 (sc = 3, d = 2^-9 set by a second sub-block of range 1953/512),
+    x = 0.5, 2.5 and 30.5 steps give codes 1, 3 and 31 (ties-to-even would
+    give 0, 2 and 30).  Codes are read back through the exact reconstruction
+    (x_hat = step * q when m = 0)."""
+    r = np.arange(32)
+    x = np.zeros(256, np.float32)
+    x[1:4] = np.array([0.5, 2.5, 30.5], np.float32) * 3 / 512
+    x[32:64] = (63 * r - 504) / 512.0
+    blk = orc.quantize(Q5_K, x)[0]
+    assert blk[:4].tobytes() == bytes([0x00, 0x18, 0x00, 0x24])
+    q = orc.dequantize_f64(Q5_K, blk, 256)[:32] / (3 / 512)
+    np.testing.assert_array_equal(q[:4], [0, 1, 3, 31])
+    assert np.all(q[4:] == 0)
 
 
 def test_q6_k_handmade_block():
@@ -286,10 +322,11 @@ def _q4k_fields(q):
     return d, dmin, f[:, :8], f[:, 8:]
 
 
-def test_roundtrip_q4_k():
+@pytest.mark.parametrize("t,qmax", [(Q4_K, 15), (Q5_K, 31)])
+def test_roundtrip_q4_k(t, qmax):
     x = _blocks_zoo(256)
-    q = orc.quantize(Q4_K, x)
-    xh = orc.dequantize(Q4_K, q, x.size).reshape(-1, 8, 32).astype(np.float64)
+    q = orc.quantize(t, x)
+    xh = orc.dequantize(t, q, x.size).reshape(-1, 8, 32).astype(np.float64)
     xb = x.reshape(-1, 8, 32).astype(np.float64)
     d, dmin, sc, m = _q4k_fields(q)
     step = d[:, None] * sc
@@ -297,12 +334,21 @@ def test_roundtrip_q4_k():
     scale = np.abs(xb).max(axis=(1, 2))
     bound = step / 2 * (1 + 1e-6) + 1e-6 * scale[:, None] + 1e-30
     assert np.all(err <= bound[:, :, None])
-    # the reconstruction is d*sc*q - dmin*m: recover q and check it is an integer in [0, 15]
+    # the reconstruction is d*sc*q - dmin*m: recover q and check it is an integer in [0, qmax]
     with np.errstate(invalid="ignore", divide="ignore"):
         qq = (xh + (dmin[:, None] * m)[:, :, None]) / step[:, :, None]
     ok = step > 0
     assert np.all(np.abs(qq[ok] - np.round(qq[ok])) < 1e-3)
-    assert np.all((np.round(qq[ok]) >= 0) & (np.round(qq[ok]) <= 15))
+    assert np.all((np.round(qq[ok]) >= 0) & (np.round(qq[ok]) <= qmax))
+    if t == Q5_K:
+        # the codes straight from the bytes (low nibbles and the fifth-bit
+        # plane as the format defines them) are the recovered codes
+        e = np.arange(256)
+        nib = np.where(e % 2 == 1, q[:, 16 + e // 2] >> 4, q[:, 16 + e // 2] & 15).astype(np.int64)
+        j, tt, i, p = e // 32, (e % 32) // 8, (e % 8) // 2, e % 2
+        hb = (q[:, 144 + 4 * j + i] >> (2 * tt + p)) & 1
+        codes = (nib | (hb.astype(np.int64) << 4)).reshape(-1, 8, 32)
+        np.testing.assert_array_equal(codes[ok], np.round(qq[ok]).astype(np.int64))
 
 
 def test_nonfinite_rejected():
@@ -316,7 +362,7 @@ def test_nonfinite_rejected():
 # The product: brute force in float64 on tiny inputs, and exact integer cases
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K, Q6_K])
+@pytest.mark.parametrize("wtype", [Q4_0, Q8_0, Q4_K, Q6_K, Q5_K])
 @pytest.mark.parametrize("rows,cols,batch", [(1, 256, 1), (5, 512, 3), (7, 1024, 2)])
 def test_matmul_ref_vs_bruteforce(wtype, rows, cols, batch):
     atype = orc.ACT_TYPE[wtype]
@@ -450,6 +496,51 @@ def test_integer_special_case_q6_k():
     np.testing.assert_array_equal(s, ref)
 
 
+def test_integer_special_case_q5_k():
+    """Q5_K with d = dmin = 1 and a Q8_K scale of 1: codes q in [0, 31], so
+    y = sum (sc*q - m)*a and the sums S1 = sum_j sc_j s_j, S2 = sum_j m_j t_j
+    are pure integers (numpy int64).  The blocks are packed here from the
+    format definition (low nibbles in the Q4_0 order; fifth bit of element
+    32j + 8t + 2i + p in bit 2t + p of byte 144 + 4j + i), independently of the
+    oracle's encoder."""
+    g = inputs.rng(10)
+    rows, cols, batch = 4, 512, 3
+    nsb = cols // 256
+    Q = g.integers(0, 32, size=(rows, cols))
+    SC = g.integers(0, 64, size=(rows, nsb, 8))
+    M = g.integers(0, 64, size=(rows, nsb, 8))
+    A = g.integers(-127, 128, size=(batch, cols))
+    Wq = np.zeros((rows, nsb, 176), np.uint8)
+    Wq[:, :, 1] = 0x3C
+    Wq[:, :, 3] = 0x3C
+    for r in range(rows):
+        for s in range(nsb):
+            v = 0
+            for k in range(8):
+                v |= int(SC[r, s, k]) << (6 * k)
+                v |= int(M[r, s, k]) << (6 * (k + 8))
+            Wq[r, s, 4:16] = np.frombuffer(v.to_bytes(12, "little"), np.uint8)
+            qb = Q[r, 256 * s:256 * (s + 1)]
+            Wq[r, s, 16:144] = ((qb[0::2] & 15) | ((qb[1::2] & 15) << 4)).astype(np.uint8)
+            for e in range(256):
+                if qb[e] >> 4:
+                    j, t, i, p = e // 32, (e % 32) // 8, (e % 8) // 2, e % 2
+                    Wq[r, s, 144 + 4 * j + i] |= 1 << (2 * t + p)
+    Xq = np.zeros((batch, nsb, 276), np.uint8)
+    Xq[:, :, 0:4] = np.frombuffer(np.float32(1.0).tobytes(), np.uint8)
+    Ab = A.reshape(batch, nsb, 256)
+    Xq[:, :, 4:260] = Ab.astype(np.int8).view(np.uint8)
+    Xq[:, :, 260:276] = Ab.reshape(batch, nsb, 8, 32).sum(-1).astype(np.int16).view(np.uint8)
+    Wint = (SC.repeat(32, axis=2).reshape(rows, cols) * Q - M.repeat(32, axis=2).reshape(rows, cols))
+    y, _ = orc.matmul_ref(Q5_K, Wq.reshape(rows, -1), Xq.reshape(batch, -1), rows, cols, batch)
+    np.testing.assert_array_equal(y, (A @ Wint.T).astype(np.float64))
+    s = orc.block_sums(Q5_K, Wq.reshape(rows, -1), Xq.reshape(batch, -1), rows, cols, batch)
+    S1 = np.einsum("rsk,brski->brs", SC, Q.reshape(1, rows, nsb, 8, 32) * Ab.reshape(batch, 1, nsb, 8, 32))
+    S2 = np.einsum("rsk,bsk->brs", M, Ab.reshape(batch, nsb, 8, 32).sum(-1))
+    np.testing.assert_array_equal(s[..., 0], S1)
+    np.testing.assert_array_equal(s[..., 1], S2)
+
+
 def test_tolerance_scale_is_sum_of_magnitudes():
     """T is at least |y| (triangle inequality) and equals |y| when every term
     has the same sign (all-positive weights and activations, Q8_0 x Q8_0)."""
@@ -463,7 +554,7 @@ def test_tolerance_scale_is_sum_of_magnitudes():
     assert np.all(T2 >= np.abs(y2))
 
 
-@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q4_K, Q8_K, Q6_K])
+@pytest.mark.parametrize("t", [Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K])
 def test_multithreaded_quantize_equals_blockwise(t):
     """The row-parallel quantizer used for timing is the pinned one, row by row."""
     be = orc.block_elems(t)
