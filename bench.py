@@ -14,14 +14,14 @@ when the kernel source matches the committed capture), the one-launch
 streaming point, the unfused step, the end-to-end figure with host buffers,
 the 7B-shape decode (tok/s), the batch sweep on 14336x4096 through both
 kernel families, the 512-column prefill GEMM, the quantized KV cache
-(scores and append), the Q6_K GEMV (dependent launches and one streaming
+(scores and append), the Q6_K and Q5_K GEMVs (dependent launches and one streaming
 launch), the 512x1024 Q4_0 GEMV (latency), the CPU oracle baseline (all
 cores and one core), the
 number of library kernel launches in the timed region, and the SM clocks
 sampled during it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
-                  [--only prefill|sweep|decode|stream|kv|q6k|q4_0] [--no-cpu]
+                  [--only prefill|sweep|decode|stream|kv|q6k|q5k|q4_0] [--no-cpu]
 """
 from __future__ import annotations
 
@@ -51,7 +51,8 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "q6k", "q4_0"], default=None,
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "q6k", "q5k", "q4_0"],
+                   default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
 
@@ -338,27 +339,28 @@ def run_cpu_configs(budget=0.25):
     return out
 
 
-def run_cpu_q6k(seconds=3.0):
-    """The oracle, as it stands, on all host cores for the Q6_K workload:
-    Q8_K act-quant + Q6_K GEMV of the 4096x4096 matrix, repeated for about
-    `seconds`."""
+def run_cpu_q6k(seconds=3.0, wtype=None):
+    """The oracle, as it stands, on all host cores for the Q6_K (or Q5_K)
+    workload: Q8_K act-quant + GEMV of the 4096x4096 matrix, repeated for
+    about `seconds`."""
     import oracle as orc
     from block_quantized_gb300 import inputs
+    wt = orc.Q6_K if wtype is None else wtype
     W, _ = inputs.gemv_q4_k(0)
-    Wq = orc.quantize(orc.Q6_K, W)
+    Wq = orc.quantize(wt, W)
     x = inputs.normal(inputs.rng(2), (GEMV_COLS,))
     nt = orc.max_threads()
     n = 0
     t0 = time.perf_counter()
     while True:
         xq = orc.quantize(orc.Q8_K, x)
-        orc.matmul_ref(orc.Q6_K, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, nt)
+        orc.matmul_ref(wt, Wq, xq, GEMV_ROWS, GEMV_COLS, 1, nt)
         n += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
             break
     return {"value": n * Wq.nbytes / dt / 1e9, "unit": "GB/s", "cores": nt, "kind": "oracle",
-            "sample": f"{n} x (Q8_K act-quant + Q6_K GEMV 4096x4096, batch 1) in {dt:.1f} s"}
+            "sample": f"{n} x (Q8_K act-quant + {orc.TYPE_NAMES[wt]} GEMV 4096x4096, batch 1) in {dt:.1f} s"}
 
 
 def run_cpu_q4_0(seconds=1.0):
@@ -475,6 +477,8 @@ def run_gpu(args, world, rank):
               "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak),
               "q6k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
                                        cpu=rank == 0 and world == 1 and not args.no_cpu),
+              "q5k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
+                                       cpu=rank == 0 and world == 1 and not args.no_cpu, wtype=gq.Q5_K),
               "q4_0": lambda: bench_q4_0(gq, inputs, torch, np, dev, capture, time_graph,
                                          cpu=rank == 0 and world == 1 and not args.no_cpu)}
         if rank == 0:
@@ -578,6 +582,8 @@ def run_gpu(args, world, rank):
         extras["prefill"] = leg(bench_prefill, gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
         extras["kv_cache"] = leg(bench_kv, gq, torch, dev, capture, time_graph, hbm_peak)
         extras["q6k"] = leg(bench_q6k, gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=cpu_leg)
+        extras["q5k"] = leg(bench_q6k, gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=cpu_leg,
+                            wtype=gq.Q5_K)
         extras["q4_0_512x1024"] = leg(bench_q4_0, gq, inputs, torch, np, dev, capture, time_graph, cpu=cpu_leg)
 
     cpu = cpu_configs = None
@@ -642,6 +648,8 @@ def summary_keys(line: dict) -> dict:
         mma_wins = [int(b) for b, v in sweep.items() if v.get("faster") == "mma"]
         out["sweep_crossover_batch"] = min(mma_wins) if mma_wins else None
     out["q6k_frac"] = r(get(line, "q6k", "frac"))
+    out["q5k_frac"] = r(get(line, "q5k", "frac"))
+    out["q5k_stream_frac"] = r(get(line, "q5k", "streaming", "frac"))
     out["kv_q8_0_frac"] = r(get(line, "kv_cache", "q8_0", "frac"))
     out["cpu_oracle_gbps_all_cores"] = r(get(line, "cpu_baseline", "value"))
     out["cpu_oracle_decode_tok_s"] = r(get(line, "cpu_baseline_configs", "decode_7b", "all_cores", "tok_s"), 4)
@@ -701,13 +709,15 @@ def bench_q4_0(gq, inputs, torch, np, dev, capture, time_graph, cpu=False):
             "weight_bytes": Wq.numel(), "cpu_baseline": run_cpu_q4_0() if cpu else None}
 
 
-def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=False):
-    """Q6_K x Q8_K GEMV on the 4096x4096 row-spread + outlier weights: 64
-    distinct copies (203 MB, larger than L2) as dependent back-to-back
-    launches on pre-quantized activations, and the same bytes as one tall
-    launch (262144 x 4096 rows)."""
+def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=False, wtype=None):
+    """Q6_K (or, with wtype, Q5_K) x Q8_K GEMV on the 4096x4096 row-spread +
+    outlier weights: 64 distinct copies (203 / 185 MB, larger than L2) as
+    dependent back-to-back launches on pre-quantized activations, and the same
+    bytes as one tall launch (262144 x 4096 rows)."""
+    wt = gq.Q6_K if wtype is None else wtype
+    name = "Q6_K" if wt == gq.Q6_K else "Q5_K"
     W, _ = inputs.gemv_q4_k(0)
-    Wq1 = gq.quantize(gq.Q6_K, torch.from_numpy(W).to(dev))
+    Wq1 = gq.quantize(wt, torch.from_numpy(W).to(dev))
     del W
     Wall = Wq1.reshape(1, -1).repeat(COPIES, 1)
     X = torch.from_numpy(inputs.normal(inputs.rng(2), (COPIES, GEMV_COLS))).to(dev)
@@ -718,27 +728,29 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
 
     def chain():
         for i in range(COPIES):
-            gq.gq_matmul(gq.Q6_K, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
+            gq.gq_matmul(wt, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
 
     def tall():
-        gq.gq_matmul(gq.Q6_K, Wall, XQ[0], Yt, GEMV_ROWS * COPIES, GEMV_COLS, 1)
+        gq.gq_matmul(wt, Wall, XQ[0], Yt, GEMV_ROWS * COPIES, GEMV_COLS, 1)
 
     k = 200
     t_c, _ = time_graph(capture(chain), k, 5)
     t_t, _ = time_graph(capture(tall), 50, 3)
     if not (torch.isfinite(Y).all() and torch.isfinite(Yt).all()):
-        raise RuntimeError("non-finite Q6_K GEMV output")
+        raise RuntimeError(f"non-finite {name} GEMV output")
     per = t_c / (k * COPIES)
     alg = w_bytes + GEMV_COLS // 256 * 276 + GEMV_ROWS * 4
     tall_s = t_t / 50
     del Wall, XQ
     torch.cuda.empty_cache()
-    return {"workload": "Q6_K x Q8_K GEMV 4096x4096 batch 1, 64 distinct matrices (203 MB)",
-            "cpu_baseline": run_cpu_q6k() if cpu else None,
-            "kernel": "gemv_q6k_kernel (whole-row bulk copies, per-warp ring)",
+    return {"workload": f"{name} x Q8_K GEMV 4096x4096 batch 1, 64 distinct matrices "
+                        f"({COPIES * w_bytes / 1e6:.0f} MB)",
+            "cpu_baseline": run_cpu_q6k(wtype=wt) if cpu else None,
+            "kernel": f"gemv_{name.lower().replace('_', '')}_kernel (whole-row bulk copies, per-warp ring)",
             "launch_us": per * 1e6, "alg_bytes_per_launch": alg, "weight_gbps": w_bytes / per / 1e9,
             "achieved": alg / per / 1e9, "frac": alg / per / 1e9 / hbm_peak,
-            "streaming": {"workload": "one launch over 262144 x 4096 Q6_K rows (814 MB)",
+            "streaming": {"workload": f"one launch over 262144 x 4096 {name} rows "
+                                      f"({COPIES * w_bytes / 1e6:.0f} MB)",
                           "us": tall_s * 1e6, "weight_gbps": COPIES * w_bytes / tall_s / 1e9,
                           "frac": COPIES * w_bytes / tall_s / 1e9 / hbm_peak}}
 

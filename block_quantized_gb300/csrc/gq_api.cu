@@ -61,12 +61,12 @@ gq_status make_ctx(gq_stream_t stream, LaunchCtx *ctx) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-bool valid_type(int t) { return t >= GQ_Q4_0 && t <= GQ_Q6_K; }
+bool valid_type(int t) { return t >= GQ_Q4_0 && t <= GQ_Q5_K; }
 
 int64_t block_elems(int t) {
     switch (t) {
     case GQ_Q4_0: case GQ_Q8_0: return 32;
-    case GQ_Q4_K: case GQ_Q8_K: case GQ_Q6_K: return 256;
+    case GQ_Q4_K: case GQ_Q8_K: case GQ_Q6_K: case GQ_Q5_K: return 256;
     }
     return -1;
 }
@@ -78,6 +78,7 @@ int64_t block_bytes(int t) {
     case GQ_Q4_K: return Q4_K_BYTES;
     case GQ_Q8_K: return Q8_K_BYTES;
     case GQ_Q6_K: return Q6_K_BYTES;
+    case GQ_Q5_K: return Q5_K_BYTES;
     }
     return -1;
 }
@@ -96,7 +97,7 @@ gq_status check_codec(gq_type type, const void *x, const void *q, int64_t n, boo
     if (n == 0) return GQ_OK;
     if (!x || !q) return GQ_ERR_NULL;
     if (!aligned(x, 4)) return GQ_ERR_ALIGN;
-    const uintptr_t qa = (type == GQ_Q4_K || type == GQ_Q8_K) ? 4 : 2;
+    const uintptr_t qa = (type == GQ_Q4_K || type == GQ_Q5_K || type == GQ_Q8_K) ? 4 : 2;
     if (!aligned(q, qa)) return GQ_ERR_ALIGN;
     (void)quant;
     return GQ_OK;
@@ -104,7 +105,8 @@ gq_status check_codec(gq_type type, const void *x, const void *q, int64_t n, boo
 
 gq_status check_matmul(gq_type wtype, const void *W, const void *xq, const void *out,
                        int64_t rows, int64_t cols, int64_t batch, uintptr_t out_align) {
-    if (wtype != GQ_Q4_0 && wtype != GQ_Q8_0 && wtype != GQ_Q4_K && wtype != GQ_Q6_K) return GQ_ERR_TYPE;
+    if (wtype != GQ_Q4_0 && wtype != GQ_Q8_0 && wtype != GQ_Q4_K && wtype != GQ_Q6_K && wtype != GQ_Q5_K)
+        return GQ_ERR_TYPE;
     if (rows < 0 || cols < 0 || batch < 0) return GQ_ERR_SHAPE;
     if (cols % block_elems(wtype) != 0) return GQ_ERR_SHAPE;
     if (rows > MAX_DIM || batch > MAX_DIM || cols > MAX_COLS) return GQ_ERR_SHAPE;
@@ -154,8 +156,9 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     gq_status st = sums ? check_matmul(wtype, W, act, sums, rows, cols, batch, 4)
                         : check_matmul(wtype, W, act, y, rows, cols, batch, 4);
     if (st != GQ_OK) return st;
+    const bool kstream = wtype == GQ_Q6_K || wtype == GQ_Q5_K;  // weight types with a GEMV of their own
     if (fused_f32) {
-        if (path == GQ_PATH_MMA || wtype == GQ_Q6_K) return GQ_ERR_TYPE;
+        if (path == GQ_PATH_MMA || kstream) return GQ_ERR_TYPE;
         if (cols % 256 != 0) return GQ_ERR_SHAPE;
     }
     if (path == GQ_PATH_MMA) {
@@ -172,12 +175,13 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         use_mma = !fused_f32 && wtype == GQ_Q4_K && tc_auto(rows, batch) &&
                   mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
-    if (!use_mma && wtype != GQ_Q6_K && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
+    if (!use_mma && !kstream && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
     cudaError_t e = use_mma            ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
                     : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, ctx)
+                    : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch, ctx)
                                        : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
                                                      (flags & GQ_FLAG_W_STATIC) != 0, ctx);
     if (e != cudaSuccess) return cuda_fail(e);

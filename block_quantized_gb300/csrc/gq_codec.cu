@@ -1,5 +1,5 @@
 // gq_codec.cu -- block codecs: quantize (fp32 -> blocks) and dequantize
-// (blocks -> fp32) for Q4_0, Q8_0, Q4_K and Q8_K.
+// (blocks -> fp32) for Q4_0, Q8_0, Q4_K, Q5_K and Q8_K.
 //
 // Every step is the IEEE fp32 operation the format definition names, written
 // with explicit round-to-nearest intrinsics (and this file is compiled with
@@ -10,8 +10,11 @@
 //   Q4_0 (b = 4, the §5.1 worked example) and the activation block Q8_K;
 //   §5.2 asymmetric quantization (scale and zero point from the min/max) and
 //   §5.5 (super-block scale d and min dmin over 6-bit per-sub-block factors)
-//   for Q4_K; §6.4 for the nibble order (element 2j in the low nibble of
-//   byte j).  Codes round half away from zero (roundf).
+//   for Q4_K and Q5_K (the 5-bit K-quant, one bit more than Q4_K: the
+//   discosf.com page "为什么说 llama.cpp 是'裸引擎'…", §4; the same fit with
+//   codes in [0, 31], their fifth bits in a bit plane of their own); §6.4
+//   for the nibble order (element 2j in the low nibble of byte j).  Codes
+//   round half away from zero (roundf).
 //
 // Work split: one warp per block.  Q8_0 / Q4_0: lane i owns element i.
 // Q4_K / Q8_K: lane l owns elements 8l..8l+7, so the four lanes 4j..4j+3 own
@@ -124,15 +127,21 @@ __global__ void __launch_bounds__(256) quantize_q8_k_kernel(const float *__restr
     }
 }
 
-// Q4_K: per 32-element sub-block j (lanes 4j..4j+3):
+// Q4_K (QMAX = 15) and Q5_K (QMAX = 31): per 32-element sub-block j (lanes
+// 4j..4j+3):
 //   lo_j = min(0, min x), hi_j = max x
 //   dmin = fp16_up(max_j(-lo_j) / 63), m_j = min(63, ceil(-lo_j / dmin))
 //   base_j = -(dmin * m_j), r_j = hi_j - base_j
-//   d = fp16_up(max_j r_j / 945), sc_j = min(63, ceil(r_j / (15 d)))
-//   q = clamp(round((x - base_j) / (d * sc_j)), 0, 15)
-__global__ void __launch_bounds__(256) quantize_q4_k_kernel(const float *__restrict__ x,
-                                                            uint8_t *__restrict__ dst,
-                                                            int64_t nblocks) {
+//   d = fp16_up(max_j r_j / (63 QMAX)), sc_j = min(63, ceil(r_j / (QMAX d)))
+//   q = clamp(round((x - base_j) / (d * sc_j)), 0, QMAX)
+// The low four bits of the codes fill bytes 16..143 (element 2l in the low
+// nibble of byte 16 + l); Q5_K puts the fifth bit of element
+// 32j + 8t + 2i + p into bit 2t + p of byte 144 + 4j + i.
+template <int QMAX>
+__global__ void __launch_bounds__(256) quantize_k_kernel(const float *__restrict__ x,
+                                                         uint8_t *__restrict__ dst,
+                                                         int64_t nblocks) {
+    constexpr int BYTES = QMAX == 15 ? Q4_K_BYTES : Q5_K_BYTES;
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     pdl_launch_dependents();  // dependents still wait for this grid's completion
@@ -171,22 +180,31 @@ __global__ void __launch_bounds__(256) quantize_q4_k_kernel(const float *__restr
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) rmax = fmaxf(rmax, __shfl_xor_sync(FULL, rmax, o));
         if (!(rmax > 0.0f)) rmax = 0.0f;
-        const __half dh = __float2half_ru(__fdiv_rn(rmax, 945.0f));
+        const __half dh = __float2half_ru(__fdiv_rn(rmax, (float)(63 * QMAX)));
         const float d = __half2float(dh);
-        float sc = (d == 0.0f) ? 0.0f : ceilf(__fdiv_rn(r, __fmul_rn(15.0f, d)));
+        float sc = (d == 0.0f) ? 0.0f : ceilf(__fdiv_rn(r, __fmul_rn((float)QMAX, d)));
         if (sc > 63.0f) sc = 63.0f;
         const float step = __fmul_rn(d, sc);
-        uint32_t packed = 0;
+        uint32_t packed = 0, fifth = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float q = (step == 0.0f)
                                 ? 0.0f
                                 : clampf(roundf(__fdiv_rn(__fsub_rn(v[i], base), step)), 0.0f,
-                                         15.0f);
-            packed |= (uint32_t)q << (4 * i);  // element 8l+i -> nibble i of the word
+                                         (float)QMAX);
+            const uint32_t qi = (uint32_t)q;
+            packed |= (qi & 15u) << (4 * i);  // element 8l+i -> nibble i of the word
+            // element 8l + i = 32j + 8t + 2(i/2) + (i&1), t = l % 4: fifth bit
+            // to bit 8(i/2) + 2t + (i&1) of the sub-block's fifth-bit word
+            fifth |= (qi >> 4) << (8 * (i >> 1) + 2 * (lane & 3) + (i & 1));
         }
-        uint8_t *blk = dst + b * Q4_K_BYTES;
+        uint8_t *blk = dst + b * BYTES;
         reinterpret_cast<uint32_t *>(blk + 16)[lane] = packed;
+        if (QMAX == 31) {
+            fifth |= __shfl_xor_sync(FULL, fifth, 1);
+            fifth |= __shfl_xor_sync(FULL, fifth, 2);
+            if ((lane & 3) == 0) reinterpret_cast<uint32_t *>(blk + 144)[lane >> 2] = fifth;
+        }
         // gather the eight (sc_j, m_j) pairs and pack sixteen 6-bit fields
         uint32_t w[3] = {0u, 0u, 0u};
 #pragma unroll
@@ -235,8 +253,8 @@ __global__ void dequantize_kernel(int type, const uint8_t *__restrict__ src,
             const uint8_t *blk = src + (e >> 5) * Q8_0_BYTES;
             const float d = half_bits_to_float(*reinterpret_cast<const uint16_t *>(blk));
             out = __fmul_rn(d, (float)(int8_t)blk[2 + (e & 31)]);
-        } else if (type == GQ_Q4_K) {
-            const uint8_t *blk = src + (e >> 8) * Q4_K_BYTES;
+        } else if (type == GQ_Q4_K || type == GQ_Q5_K) {
+            const uint8_t *blk = src + (e >> 8) * (type == GQ_Q4_K ? Q4_K_BYTES : Q5_K_BYTES);
             const int i = (int)(e & 255), j = i >> 5;
             const uint32_t *hdr = reinterpret_cast<const uint32_t *>(blk);
             const float d = half_bits_to_float(hdr[0]);
@@ -246,7 +264,12 @@ __global__ void dequantize_kernel(int type, const uint8_t *__restrict__ src,
             const float sc = (float)((lo64 >> (6 * j)) & 63);
             const float m = (float)((hi64 >> (6 * j + 16)) & 63);
             const int byte = blk[16 + (i >> 1)];
-            const float q = (float)((i & 1) ? (byte >> 4) : (byte & 15));
+            int qi = (i & 1) ? (byte >> 4) : (byte & 15);
+            if (type == GQ_Q5_K) {
+                const int r = i & 31;  // element 8t + 2i' + p of sub-block j
+                qi |= ((blk[144 + 4 * j + ((r & 7) >> 1)] >> (2 * (r >> 3) + (r & 1))) & 1) << 4;
+            }
+            const float q = (float)qi;
             out = __fsub_rn(__fmul_rn(__fmul_rn(d, sc), q), __fmul_rn(dmin, m));
         } else {
             const uint8_t *blk = src + (e >> 8) * Q8_K_BYTES;
@@ -269,7 +292,7 @@ int grid_for(int64_t work_items, int per_cta, int num_sms) {
 
 cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
                             const LaunchCtx &ctx) {
-    const int64_t nb = n / (t == GQ_Q4_K || t == GQ_Q8_K ? QK_K : 32);
+    const int64_t nb = n / (t == GQ_Q4_K || t == GQ_Q5_K || t == GQ_Q8_K ? QK_K : 32);
     const int grid = grid_for(nb, 8, ctx.num_sms);
     uint8_t *d8 = static_cast<uint8_t *>(dst);
     switch (t) {
@@ -280,7 +303,9 @@ cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
         return launch_pdl(quantize32_kernel<7>, grid, 256, 0, ctx.stream, src, d8, nb, std::max<int64_t>(nb, 1),
                           (int64_t)0);
     case GQ_Q4_K:
-        return launch_pdl(quantize_q4_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
+        return launch_pdl(quantize_k_kernel<15>, grid, 256, 0, ctx.stream, src, d8, nb);
+    case GQ_Q5_K:
+        return launch_pdl(quantize_k_kernel<31>, grid, 256, 0, ctx.stream, src, d8, nb);
     case GQ_Q8_K:
         return launch_pdl(quantize_q8_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
     }

@@ -13,7 +13,7 @@ namespace gq {
 // Format geometry (see include/gq.h for the layouts).
 constexpr int QK4_0 = 32, QK8_0 = 32, QK_K = 256;
 constexpr int Q4_0_BYTES = 18, Q8_0_BYTES = 34, Q4_K_BYTES = 144, Q8_K_BYTES = 276;
-constexpr int Q6_K_BYTES = 194;
+constexpr int Q6_K_BYTES = 194, Q5_K_BYTES = 176;
 
 // Bits of the device status word (one per kernel family that waits).
 constexpr uint32_t STATUS_GEMV_TMA_TIMEOUT = 1u << 0;

@@ -68,6 +68,12 @@ cudaError_t launch_dequantize_q6k(const void *src, float *dst, int64_t n, const 
 cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
                             int64_t batch, const LaunchCtx &ctx);
 
+// Q5_K x Q8_K GEMV (gq_q5k.cu; the Q5_K codecs are in gq_codec.cu): any
+// batch, one pass over W per activation vector; sums != nullptr selects the
+// int32 sums S1, S2 per 256-element block instead of y.
+cudaError_t launch_gemv_q5k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+                            int64_t batch, const LaunchCtx &ctx);
+
 // tcgen05 tensor-core family (Q4_K x Q8_K): a pack kernel writes the
 // activation operand into `workspace`, then the MMA kernel runs.
 cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,

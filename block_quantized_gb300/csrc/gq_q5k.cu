@@ -1,0 +1,358 @@
+// gq_q5k.cu -- the Q5_K x Q8_K GEMV.
+//
+// Q5_K is the 5-bit K-quant, one bit more than Q4_K (the discosf.com page
+// "为什么说 llama.cpp 是'裸引擎'——从模型加载的每一行代码说起", §4 量化不是"压缩"，
+// 而是"精度重分配"): the Q4_K super-block of "llama.cpp 推理引擎" §5.5 (fp16 d
+// and dmin, 6-bit scale sc_j and min m_j per 32-element sub-block) with codes
+// q in [0, 31], w = d * sc_j * q - dmin * m_j.  Block (176 B): bytes 0..143 as
+// Q4_K (d, dmin, the sixteen 6-bit fields, the low four bits of the codes in
+// the Q4_0 nibble order), then 32 bytes @144 with the fifth bits: bit 2t + p
+// of byte 144 + 4j + i is the fifth bit of element 32j + 8t + 2i + p.  That
+// places, for the nibble word t of sub-block j (elements 8t..8t+7), the fifth
+// bits of its even elements at bits 2t, 2t + 8, 2t + 16, 2t + 24 of the
+// sub-block's fifth-bit word -- one shift and one mask line them up with the
+// bytes of the word's low-nibble operand (likewise bit 2t + 1 for the odd
+// elements).  The codecs live with the other K-quant codecs (gq_codec.cu).
+//
+// The product, per super-block and activation vector ("llama.cpp 推理引擎"
+// §5.5 two-level scales, §6.4 block dot): s_j = sum_{i in j} q_i * a_i,
+// S1 = sum_j sc_j * s_j, S2 = sum_j m_j * t_j (t_j the Q8_K sub-block sums),
+// y += d_x * (d * S1 - dmin * S2).
+//
+// GEMV.  Decode is bound by the bytes of W streamed ("llama.cpp 推理引擎"
+// §7.3), so the kernel streams each row once:
+//   - a persistent grid of at most one CTA per SM, 16 warps (8 when sixteen
+//     two-stage rings do not fit); warp w of the grid owns rows w, w + warps,
+//     ...; each warp streams its rows through a private shared-memory ring of
+//     2-4 whole-row stages, one bulk copy (cp.async.bulk, evict-first L2
+//     policy) per row completing on an mbarrier; every wait is bounded.
+//     Blocks are 176 = 11 x 16 bytes, so every row and every block field is
+//     16-byte aligned and all shared loads are 128-bit;
+//   - the CTA stages its Q8_K vector once: codes in 128-byte half-super-block
+//     units, each 8-code group stored as (a0 a2 a4 a6 | a1 a3 a5 a7) so the
+//     even and odd elements of a nibble word meet their activations in one
+//     dp4a each, 16-byte pieces XOR-swizzled by the unit index (distinct
+//     banks for a quarter-warp); then the eight sub-block sums and the scale;
+//   - a lane takes half a super-block (four sub-blocks, 128 elements): one
+//     header load, four 16-byte nibble loads and one 16-byte fifth-bit load;
+//     per 8 elements two 5-bit code words built with shifts and masks and two
+//     dp4a; S1 and S2 of the half in int32; fp32 partial per lane and one
+//     warp-shuffle reduction per row.
+// Rows too long for a two-stage ring take a plain warp-per-row kernel that
+// reads W and the activations from global memory.
+#include <algorithm>
+
+#include "gq_common.cuh"
+#include "gq_internal.h"
+
+namespace gq {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr uint32_t NIB = 0x0F0F0F0Fu;
+constexpr uint32_t BIT4 = 0x10101010u;
+constexpr int MAX_NS = 4;  // ring stages per warp
+// the mbarriers, at the start of shared memory
+__host__ __device__ constexpr int bars_bytes(int nw) { return nw * MAX_NS * 8; }
+
+// Shared-memory footprint of one staged Q8_K vector of nblk blocks: codes,
+// then the eight int32 sub-block sums per block, then one fp32 scale per
+// block.
+__host__ __device__ constexpr size_t act_smem_bytes(int nblk) {
+    return (size_t)nblk * 256 + (size_t)nblk * 8 * 4 + (size_t)nblk * 4;
+}
+
+// Split-order words of 8 codes: (a0 a2 a4 a6) and (a1 a3 a5 a7).
+__device__ __forceinline__ uint2 split8(uint32_t w0, uint32_t w1) {
+    return make_uint2(__byte_perm(w0, w1, 0x6420), __byte_perm(w0, w1, 0x7531));
+}
+
+// Stage one Q8_K vector (nblk blocks at xq) into shared memory at `act`.
+// Unit u (16 codes: elements 128h + 16u .. +15) of half-block hb = 2k + h is
+// stored at hb * 128 + (u ^ (hb & 7)) * 16 as {split(g0).x, .y, split(g1).x, .y}.
+__device__ void stage_q8_k_vec(uint8_t *act, const uint8_t *__restrict__ xq, int nblk) {
+    int32_t *tsum = reinterpret_cast<int32_t *>(act + (size_t)nblk * 256);
+    float *dx = reinterpret_cast<float *>(tsum + 8 * nblk);
+    for (int idx = threadIdx.x; idx < nblk * 16; idx += blockDim.x) {
+        const int hb = idx >> 3, u = idx & 7;
+        const uint8_t *blk = xq + (size_t)(hb >> 1) * Q8_K_BYTES;  // 4-byte aligned
+        const uint32_t *c = reinterpret_cast<const uint32_t *>(blk + 4 + (hb & 1) * 128 + u * 16);
+        const uint2 g0 = split8(c[0], c[1]), g1 = split8(c[2], c[3]);
+        *reinterpret_cast<uint4 *>(act + (size_t)hb * 128 + ((u ^ (hb & 7)) << 4)) =
+            make_uint4(g0.x, g0.y, g1.x, g1.y);
+    }
+    for (int i = threadIdx.x; i < 8 * nblk; i += blockDim.x) {
+        const uint8_t *blk = xq + (size_t)(i >> 3) * Q8_K_BYTES;
+        tsum[i] = (int32_t) reinterpret_cast<const int16_t *>(blk + 260)[i & 7];
+        if ((i & 7) == 0) dx[i >> 3] = *reinterpret_cast<const float *>(blk);
+    }
+}
+
+// Integer sums of half h of the block at `blk` (shared memory, 16-byte
+// aligned) against the staged codes of half-block hb: S1 = sum_j sc_j s_j and
+// S2 = sum_j m_j t_j over the half's four sub-blocks j = 4h + k.
+__device__ __forceinline__ void half_sums(const uint8_t *blk, int h, const uint8_t *act, const int32_t *tsum,
+                                          int hb, int &S1, int &S2) {
+    const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 fb = *reinterpret_cast<const uint4 *>(blk + 144 + 16 * h);  // fifth bits of the half
+    uint4 q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * h + 16 * k);
+    // header bytes 4..15 = words y, z, w: this half's four sc (bits 24h..24h+23)
+    // and four m (bits 48+24h..71+24h) are three whole bytes each
+    const uint32_t sc24 = __byte_perm(hd.y, hd.z, h ? 0x0543u : 0x0210u);
+    const uint32_t m24 = __byte_perm(hd.z, hd.w, h ? 0x0765u : 0x0432u);
+    const int4 t = reinterpret_cast<const int4 *>(tsum)[hb];  // t_j of the half
+    const uint8_t *ah = act + (size_t)hb * 128;
+    const int sw = hb & 7;
+    const uint32_t F[4] = {fb.x, fb.y, fb.z, fb.w};
+    const int tj[4] = {t.x, t.y, t.z, t.w};
+    S1 = 0;
+    S2 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // sub-block 4h + k: units 2k, 2k + 1 of the half
+        const uint4 a0 = *reinterpret_cast<const uint4 *>(ah + (((2 * k) ^ sw) << 4));
+        const uint4 a1 = *reinterpret_cast<const uint4 *>(ah + (((2 * k + 1) ^ sw) << 4));
+        const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+        const uint32_t ae[4] = {a0.x, a0.z, a1.x, a1.z}, ao[4] = {a0.y, a0.w, a1.y, a1.w};
+        int s = 0;
+#pragma unroll
+        for (int tt = 0; tt < 4; ++tt) {  // nibble word tt: elements 8tt..8tt+7
+            // fifth bits of the even (odd) elements at bits 2tt (2tt + 1) of
+            // each byte of F[k], moved to bit 4 of each byte
+            const uint32_t fe = (2 * tt <= 4 ? F[k] << (4 - 2 * tt) : F[k] >> (2 * tt - 4)) & BIT4;
+            const uint32_t fo = (2 * tt + 1 <= 4 ? F[k] << (3 - 2 * tt) : F[k] >> (2 * tt - 3)) & BIT4;
+            s = dp4a_us((w[tt] & NIB) | fe, (int)ae[tt], s);
+            s = dp4a_us(((w[tt] >> 4) & NIB) | fo, (int)ao[tt], s);
+        }
+        S1 += (int)((sc24 >> (6 * k)) & 63u) * s;
+        S2 += (int)((m24 >> (6 * k)) & 63u) * tj[k];
+    }
+}
+
+// Streaming kernel: one activation vector per blockIdx.y.  SUMS: write the
+// int32 sums S1, S2 of every block instead of y.
+template <bool SUMS, int GW>
+__global__ void __launch_bounds__(GW * 32, 1) gemv_q5k_kernel(const uint8_t *__restrict__ W,
+                                                             const uint8_t *__restrict__ xq,
+                                                             float *__restrict__ y, int32_t *__restrict__ sums,
+                                                             int rows, int nblk, int ns, int stage_bytes,
+                                                             uint32_t *__restrict__ status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int warps_total = gridDim.x * GW;
+    const int wg = blockIdx.x * GW + warp;
+    const int total = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
+    const uint32_t row_bytes = (uint32_t)nblk * Q5_K_BYTES;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp * MAX_NS;
+    uint8_t *ring = smem + bars_bytes(GW) + (size_t)warp * ns * stage_bytes;
+    uint8_t *act = smem + bars_bytes(GW) + (size_t)GW * ns * stage_bytes;
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int i, int st) {
+        const size_t row = (size_t)wg + (size_t)i * warps_total;
+        mbar_arrive_expect_tx(bar + st, row_bytes);
+        bulk_g2s_hint(ring + (size_t)st * stage_bytes, W + row * row_bytes, row_bytes, bar + st, pol);
+    };
+
+    pdl_launch_dependents();
+    if (lane == 0 && total > 0) {
+        for (int s = 0; s < ns; ++s) mbar_init(bar + s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    pdl_wait();  // W and xq may come from the preceding kernel in the stream
+    if (lane == 0)
+        for (int i = 0; i < ns && i < total; ++i) issue(i, i);
+    stage_q8_k_vec(act, xq + (size_t)b * nblk * Q8_K_BYTES, nblk);
+    __syncthreads();
+
+    const int32_t *tsum = reinterpret_cast<const int32_t *>(act + (size_t)nblk * 256);
+    const float *dx = reinterpret_cast<const float *>(tsum + 8 * nblk);
+    const int iters = (2 * nblk + 31) / 32;
+    int st = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < total; ++i) {
+        if (!mbar_wait_bounded(bar + st, ph)) {
+            // A transfer never completed: flag it, let the other issued
+            // stages drain (bounded) and leave this warp's remaining rows.
+            if (lane == 0) atomicOr(status, STATUS_GEMV_TMA_TIMEOUT);
+            int s2 = st;
+            uint32_t p2 = ph;
+            for (int k = i + 1; k < total && k < i + ns; ++k) {
+                if (++s2 == ns) {
+                    s2 = 0;
+                    p2 ^= 1u;
+                }
+                mbar_wait_bounded(bar + s2, p2);
+            }
+            return;
+        }
+        const int row = wg + i * warps_total;
+        const uint8_t *stage = ring + (size_t)st * stage_bytes;
+        float acc = 0.0f;
+        for (int t = 0; t < iters; ++t) {
+            const int hb = lane + 32 * t;
+            int S1 = 0, S2 = 0;
+            if (hb < 2 * nblk) {
+                const int k = hb >> 1;
+                const uint8_t *blk = stage + (size_t)k * Q5_K_BYTES;
+                half_sums(blk, hb & 1, act, tsum, hb, S1, S2);
+                if (!SUMS) {
+                    const uint32_t dd = *reinterpret_cast<const uint32_t *>(blk);
+                    acc += dx[k] * (half_bits_to_float(dd) * (float)S1 - half_bits_to_float(dd >> 16) * (float)S2);
+                }
+            }
+            if (SUMS) {
+                const int s1 = S1 + __shfl_xor_sync(FULL, S1, 1);  // the two halves of block hb / 2
+                const int s2 = S2 + __shfl_xor_sync(FULL, S2, 1);
+                if (hb < 2 * nblk && (hb & 1) == 0) {
+                    int32_t *o = sums + (((size_t)b * rows + row) * nblk + (hb >> 1)) * 2;
+                    o[0] = s1;
+                    o[1] = s2;
+                }
+            }
+        }
+        if (!SUMS) {
+            acc = warp_sum(acc);
+            if (lane == 0) y[(size_t)b * rows + row] = acc;
+        }
+        __syncwarp();
+        if (lane == 0 && i + ns < total) issue(i + ns, st);
+        if (++st == ns) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+// Plain kernel for any cols (a multiple of 256): warp per (row, vector), lane
+// per half block, byte loads from global memory.
+constexpr int PW = 8;
+
+template <bool SUMS>
+__global__ void __launch_bounds__(PW * 32) gemv_q5k_plain_kernel(const uint8_t *__restrict__ W,
+                                                                 const uint8_t *__restrict__ xq,
+                                                                 float *__restrict__ y,
+                                                                 int32_t *__restrict__ sums, int rows, int nblk) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * PW + warp;
+    const int b = blockIdx.y;
+    pdl_launch_dependents();
+    pdl_wait();
+    if (row >= rows) return;
+    const int iters = (2 * nblk + 31) / 32;
+    float acc = 0.0f;
+    for (int t = 0; t < iters; ++t) {
+        const int hb = lane + 32 * t;
+        int S1 = 0, S2 = 0;
+        float d = 0.0f, dmin = 0.0f, dxv = 0.0f;
+        if (hb < 2 * nblk) {
+            const int k = hb >> 1, h = hb & 1;
+            const uint8_t *wb = W + ((size_t)row * nblk + k) * Q5_K_BYTES;
+            const uint8_t *ab = xq + ((size_t)b * nblk + k) * Q8_K_BYTES;
+            uint32_t f[16];  // the sixteen 6-bit fields, LSB-first in bytes 4..15
+            uint64_t lo = 0, hi = 0;
+            for (int i = 0; i < 8; ++i) lo |= (uint64_t)__ldg(wb + 4 + i) << (8 * i);
+            for (int i = 0; i < 4; ++i) hi |= (uint64_t)__ldg(wb + 12 + i) << (8 * i);
+            for (int i = 0; i < 10; ++i) f[i] = (uint32_t)((lo >> (6 * i)) & 63);
+            f[10] = (uint32_t)(((lo >> 60) | (hi << 4)) & 63);
+            for (int i = 11; i < 16; ++i) f[i] = (uint32_t)((hi >> (6 * i - 64)) & 63);
+            for (int j = 4 * h; j < 4 * h + 4; ++j) {
+                int s = 0;
+                for (int r = 0; r < 32; ++r) {
+                    const int e = 32 * j + r;
+                    const int nib = (__ldg(wb + 16 + (e >> 1)) >> (4 * (e & 1))) & 15;
+                    const int fifth = (__ldg(wb + 144 + 4 * j + ((r & 7) >> 1)) >> (2 * (r >> 3) + (r & 1))) & 1;
+                    s += (nib | (fifth << 4)) * (int)(int8_t)__ldg(ab + 4 + e);
+                }
+                S1 += (int)f[j] * s;
+                S2 += (int)f[8 + j] * (int)__ldg(reinterpret_cast<const int16_t *>(ab + 260) + j);
+            }
+            d = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(wb)));
+            dmin = half_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(wb) + 1));
+            dxv = __ldg(reinterpret_cast<const float *>(ab));
+        }
+        if (SUMS) {
+            const int s1 = S1 + __shfl_xor_sync(FULL, S1, 1);
+            const int s2 = S2 + __shfl_xor_sync(FULL, S2, 1);
+            if (hb < 2 * nblk && (hb & 1) == 0) {
+                int32_t *o = sums + (((size_t)b * rows + row) * nblk + (hb >> 1)) * 2;
+                o[0] = s1;
+                o[1] = s2;
+            }
+        } else {
+            acc += dxv * (d * (float)S1 - dmin * (float)S2);
+        }
+    }
+    if (!SUMS) {
+        acc = warp_sum(acc);
+        if (lane == 0) y[(size_t)b * rows + row] = acc;
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA on sm_103
+constexpr int64_t Y_MAX = 65535;    // vectors per launch (grid.y)
+
+size_t stream_smem(int nw, int ns, int nblk) {
+    return bars_bytes(nw) + (size_t)nw * ns * ((size_t)nblk * Q5_K_BYTES) + act_smem_bytes(nblk);
+}
+
+// Ring stages per warp for the streaming kernel with nw warps: as many as fit
+// (2..4) next to the staged vector; 0 when two stages do not fit.
+int pick_ns(int nw, int nblk) {
+    for (int ns = MAX_NS; ns >= 2; --ns)
+        if (stream_smem(nw, ns, nblk) <= (size_t)SMEM_LIMIT) return ns;
+    return 0;
+}
+
+template <bool SUMS, int NW>
+cudaError_t launch_stream(const uint8_t *W, const uint8_t *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
+                          int nb, int ns, const LaunchCtx &ctx) {
+    auto k = gemv_q5k_kernel<SUMS, NW>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+    if (e != cudaSuccess) return e;
+    const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
+    return launch_pdl(k, dim3((unsigned)gx, nb), dim3(NW * 32), stream_smem(NW, ns, nblk), ctx.stream, W, xb,
+                      yb, sb, (int)rows, nblk, ns, nblk * Q5_K_BYTES, ctx.status);
+}
+
+template <bool SUMS>
+cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+                     int64_t batch, const LaunchCtx &ctx) {
+    const int nblk = (int)(cols / QK_K);
+    int nw = 16, ns = pick_ns(nw, nblk);
+    if (!ns) ns = pick_ns(nw = 8, nblk);
+    for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
+        const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
+        const uint8_t *xb = xq + b0 * nblk * Q8_K_BYTES;
+        float *yb = SUMS ? nullptr : y + b0 * rows;
+        int32_t *sb = SUMS ? sums + b0 * rows * nblk * 2 : nullptr;
+        cudaError_t e;
+        if (ns && nw == 16) {
+            e = launch_stream<SUMS, 16>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+        } else if (ns) {
+            e = launch_stream<SUMS, 8>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+        } else {
+            const int64_t gx = (rows + PW - 1) / PW;
+            e = launch_pdl(gemv_q5k_plain_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(PW * 32), 0, ctx.stream, W,
+                           xb, yb, sb, (int)rows, nblk);
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_q5k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+                            int64_t batch, const LaunchCtx &ctx) {
+    const uint8_t *w8 = static_cast<const uint8_t *>(W);
+    const uint8_t *x8 = static_cast<const uint8_t *>(xq);
+    return sums ? run_gemv<true>(w8, x8, y, sums, rows, cols, batch, ctx)
+                : run_gemv<false>(w8, x8, y, sums, rows, cols, batch, ctx);
+}
+
+}  // namespace gq

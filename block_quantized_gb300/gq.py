@@ -18,12 +18,12 @@ import threading
 
 from . import build as _build
 
-Q4_0, Q8_0, Q4_K, Q8_K, Q6_K = 0, 1, 2, 3, 4
+Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K = 0, 1, 2, 3, 4, 5
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 FLAG_W_STATIC = 1
-ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K}
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q8_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q8_K: 276, Q6_K: 194}
+ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q5_K: Q8_K}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q8_K: 256, Q6_K: 256, Q5_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q8_K: 276, Q6_K: 194, Q5_K: 176}
 
 STATUS = {0: "GQ_OK", 1: "GQ_ERR_NULL", 2: "GQ_ERR_TYPE", 3: "GQ_ERR_SHAPE",
           4: "GQ_ERR_ALIGN", 5: "GQ_ERR_CUDA", 6: "GQ_ERR_TIMEOUT", 7: "GQ_ERR_ARCH"}
@@ -281,7 +281,7 @@ def matmul_f32(wtype: int, W, x, rows: int, cols: int, batch: int, flags: int = 
 def _sums_buffer(wtype, W, rows, cols, batch):
     import torch
     nb = cols // BLOCK_ELEMS[wtype]
-    shape = (batch, rows, nb, 2) if wtype == Q4_K else (batch, rows, nb)
+    shape = (batch, rows, nb, 2) if wtype in (Q4_K, Q5_K) else (batch, rows, nb)
     return torch.empty(shape, dtype=torch.int32, device=W.device)
 
 

@@ -37,6 +37,16 @@
  *                              sub-blocks, 6-bit main quantization; the
  *                              symmetric rule and this layout are this
  *                              library's reading.
+ *   Q5_K 176 B / 256 elements: bytes 0..143 as Q4_K (d, dmin, the sixteen
+ *                              6-bit fields, the low four bits of the codes
+ *                              q in [0, 31]), then 32 bytes @144 holding
+ *                              the fifth bits: bit 2t + p of byte
+ *                              144 + 4j + i is the fifth bit of element
+ *                              32j + 8t + 2i + p (t, i = 0..3, p = 0..1);
+ *                              w = d * sc_j * q - dmin * m_j.  The 5-bit
+ *                              K-quant of the same discosf.com page (one bit
+ *                              more than Q4_K); the layout is this
+ *                              library's reading.
  *   Q8_K 276 B / 256 elements: fp32 d @0, int8 q[256] @4, int16 bsums[8]
  *                              @260 (bsums[j] = sum of q over sub-block j);
  *                              w = d * q.
@@ -45,10 +55,11 @@
  * scales rounded to nearest-even; codes clamped to [-8, 7] and [-32, 31]
  * before the offsets 8 and 32); Q4_K fits each 32-element sub-block by its min/max with fp16
  * d and dmin rounded toward +infinity (so that the ceilinged 6-bit scale and
- * min always cover the sub-block) -- see the quantize entry point below.
+ * min always cover the sub-block) -- see the quantize entry point below;
+ * Q5_K is the same fit with 31 code steps instead of 15.
  *
  * Pairings for the product: Q4_0 and Q8_0 weights take Q8_0 activations;
- * Q4_K and Q6_K weights take Q8_K activations.
+ * Q4_K, Q5_K and Q6_K weights take Q8_K activations.
  *
  * General rules for every entry point:
  *   - All data pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA
@@ -90,7 +101,8 @@ typedef enum {
     GQ_Q8_0 = 1,
     GQ_Q4_K = 2,
     GQ_Q8_K = 3,
-    GQ_Q6_K = 4
+    GQ_Q6_K = 4,
+    GQ_Q5_K = 5
 } gq_type;
 
 typedef enum {
@@ -111,8 +123,8 @@ enum {
      * request their first weight chunks before waiting for the preceding
      * kernel in the stream to finish, overlapping the weight fetch with that
      * kernel's tail.  Without the flag every read of W happens after that
-     * wait.  Accepted with Q6_K weights, where it has no effect (that GEMV
-     * reads W only after the wait). */
+     * wait.  Accepted with Q5_K and Q6_K weights, where it has no effect
+     * (those GEMVs read W only after the wait). */
     GQ_FLAG_W_STATIC = 1u
 };
 
@@ -123,10 +135,10 @@ typedef enum {
     GQ_PATH_MMA = 2     /* tcgen05 tensor-core kernel (Q4_K weights only) */
 } gq_path;
 
-/* Elements per block: 32, 32, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K, Q6_K).
- * -1 for an unknown type. */
+/* Elements per block: 32, 32, 256, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K,
+ * Q6_K, Q5_K).  -1 for an unknown type. */
 int64_t gq_block_elems(gq_type type);
-/* Bytes per block: 18, 34, 144, 276, 194.  -1 for an unknown type. */
+/* Bytes per block: 18, 34, 144, 276, 194, 176.  -1 for an unknown type. */
 int64_t gq_block_bytes(gq_type type);
 /* Static text for a status code (never NULL). */
 const char *gq_status_string(gq_status status);
@@ -138,9 +150,9 @@ int gq_last_cuda_error(void);
  *   src : device, n floats, 4-byte aligned, finite values (non-finite input
  *         gives unspecified codes; magnitudes must keep the fp16 scales in
  *         range: |x| < 65504 * 127 for Q8_0, 65504 * 7 for Q4_0, 65504 * 945
- *         for Q4_K, 65504 * 31 for Q6_K).
+ *         for Q4_K, 65504 * 1953 for Q5_K, 65504 * 31 for Q6_K).
  *   dst : device, n / block_elems * block_bytes bytes; 4-byte aligned for
- *         Q8_K and Q4_K, 2-byte aligned for Q4_0 / Q8_0 / Q6_K (the product needs
+ *         Q8_K, Q4_K and Q5_K, 2-byte aligned for Q4_0 / Q8_0 / Q6_K (the product needs
  *         16-byte aligned weights, see gq_matmul).
  *   n   : element count, >= 0 and a multiple of block_elems(type).
  * Results are bit-identical to the reference definition of each format
@@ -174,18 +186,19 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *   Q8_0 x Q8_0 : d_w * d_x * sum_i w_i * a_i
  *   Q4_K x Q8_K : d_x * (d * sum_j sc_j * s_j - dmin * sum_j m_j * t_j),
  *                 s_j = sum_{i in j} q_i * a_i, t_j = bsums[j]
+ *   Q5_K x Q8_K : as Q4_K x Q8_K with the 5-bit codes
  *   Q6_K x Q8_K : d_w * d_x * sum_i (c_i - 32) * a_i   (per 256-element block)
- *   wtype : GQ_Q4_0, GQ_Q8_0, GQ_Q4_K or GQ_Q6_K.
+ *   wtype : GQ_Q4_0, GQ_Q8_0, GQ_Q4_K, GQ_Q5_K or GQ_Q6_K.
  *   W     : device, rows x (cols / block_elems) weight blocks, 16-byte aligned.
  *   xq    : device, batch x (cols / block_elems) activation blocks (Q8_0 for
- *           Q4_0 / Q8_0 weights, Q8_K for Q4_K / Q6_K), one vector after another;
+ *           Q4_0 / Q8_0 weights, Q8_K for Q4_K / Q5_K / Q6_K), one vector after another;
  *           16-byte aligned.
  *   y     : device, float[batch][rows], 4-byte aligned; fully overwritten.
  *   rows, cols, batch : > 0 (a zero size is a no-op returning GQ_OK);
- *           cols a multiple of 256 for Q4_K / Q6_K and of 32 for Q4_0 / Q8_0
+ *           cols a multiple of 256 for Q4_K / Q5_K / Q6_K and of 32 for Q4_0 / Q8_0
  *           (the fast kernels need cols % 256 == 0, and cols % 2048 == 0 up
  *           to 16384 for Q6_K; other shapes run a plain per-block kernel);
- *           Q6_K runs one pass over W per activation vector; cols at most
+ *           Q5_K and Q6_K run one pass over W per activation vector; cols at most
  *           131072 (and small
  *           enough for one activation vector to fit the kernels' shared
  *           memory: every cols up to that bound does).
@@ -257,7 +270,7 @@ gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y,
  * ("llama.cpp：一个人、一个周末…", 第一层：GGML 张量库: operators fused over
  * the computation graph).  GEMV kernels only (any batch); cols must be a
  * multiple of 256 (GQ_ERR_SHAPE otherwise).  Q4_0, Q8_0 and Q4_K weights
- * (GQ_ERR_TYPE for Q6_K).  Other arguments as gq_matmul.
+ * (GQ_ERR_TYPE for Q5_K and Q6_K).  Other arguments as gq_matmul.
  */
 gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
                         int64_t rows, int64_t cols, int64_t batch, unsigned flags,
@@ -268,7 +281,7 @@ gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
  * chosen kernel family, without the float scaling.
  *   sums : device, int32, 4-byte aligned, laid out [batch][rows][nblk][c] with
  *          nblk = cols / block_elems(wtype) and c = 1 (Q4_0, Q8_0: the block
- *          dot; Q6_K: sum_i (c_i - 32) * a_i) or c = 2 (Q4_K:
+ *          dot; Q6_K: sum_i (c_i - 32) * a_i) or c = 2 (Q4_K, Q5_K:
  *          S1 = sum_j sc_j * s_j, S2 = sum_j m_j * t_j).
  * Other arguments and errors as gq_matmul_path.
  */

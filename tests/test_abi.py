@@ -37,8 +37,8 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_block_geometry(lib):
-    assert [gq.gq_block_elems(t) for t in range(5)] == [32, 32, 256, 256, 256]
-    assert [gq.gq_block_bytes(t) for t in range(5)] == [18, 34, 144, 276, 194]
+    assert [gq.gq_block_elems(t) for t in range(6)] == [32, 32, 256, 256, 256, 256]
+    assert [gq.gq_block_bytes(t) for t in range(6)] == [18, 34, 144, 276, 194, 176]
     assert gq.gq_block_elems(9) == -1 and gq.gq_block_bytes(-1) == -1
 
 
@@ -80,12 +80,17 @@ def test_matmul_validation(lib):
     assert g(4, A16, A16, A16, 8, 256, 64, 2, None) == TYPE
     assert f(4, A16, A16, A16, 8, 32, 1, None) == SHAPE          # Q6_K needs 256-multiples
     assert f(4, 0, 0, 0, 8, 256, 0, None) == OK
+    assert g(5, A16, A16, A16, 8, 256, 64, 2, None) == TYPE      # no tensor-core Q5_K kernel
+    assert f(5, A16, A16, A16, 8, 32, 1, None) == SHAPE          # Q5_K needs 256-multiples
+    assert f(6, A16, A16, A16, 8, 256, 1, None) == TYPE
     assert lib.gq_block_sums(2, A16, A16, 0, 8, 256, 1, 1, None) == NULL
 
 
 def test_codec_validation(lib):
     q = lib.gq_quantize_rows
-    assert q(5, A16, A16, 32) == TYPE
+    assert q(6, A16, A16, 32) == TYPE
+    assert q(5, A16, A16, 32) == SHAPE                          # Q5_K needs 256-multiples
+    assert q(5, A16, A16 + 2, 256) == ALIGN                     # Q5_K dst 4-aligned
     assert q(0, A16, A16, 33) == SHAPE
     assert q(2, A16, A16, 32) == SHAPE                          # Q4_K needs 256-multiples
     assert q(1, A16, A16, -32) == SHAPE
@@ -123,6 +128,7 @@ def test_fused_and_flag_validation(lib):
     assert f(2, A16, A16, A16, 8, 256, 1, 2, None) == TYPE          # unknown flag bit
     assert f(3, A16, A16, A16, 8, 256, 1, 0, None) == TYPE
     assert f(4, A16, A16, A16, 8, 256, 1, 0, None) == TYPE          # no fused Q6_K kernel
+    assert f(5, A16, A16, A16, 8, 256, 1, 0, None) == TYPE          # nor a fused Q5_K one
     assert f(2, 0, 0, 0, 0, 256, 1, 0, None) == OK
     e = lib.gq_matmul_ex
     assert e(2, A16, A16, A16, 8, 256, 1, 1, 4, None) == TYPE

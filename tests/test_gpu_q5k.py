@@ -1,0 +1,172 @@
+"""GPU parity for Q5_K weights (the Q4_K super-block with 5-bit codes and a
+fifth-bit plane, paired with Q8_K activations): the codecs and the GEMV
+through the C ABI against the CPU oracle.
+
+Bar: quantized bytes and int32 block sums (S1, S2) bit-identical; y within
+1e-4 * sum|block terms| per output.  The shapes cover both GEMV kernels: the
+streaming kernel (whole rows through a per-warp shared-memory ring, 16 or 8
+warps, several rows per warp on the tall shapes) and the plain kernel (rows
+too long for a two-stage ring).
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle as orc  # noqa: E402
+from block_quantized_gb300 import gq, inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+Q8_K, Q5_K = 3, 5
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gq.load(build_if_missing=True)
+    yield
+    torch.cuda.synchronize()
+    assert gq.gq_device_status(reset=True) == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_close(y, y_ref, T):
+    err = np.abs(y.astype(np.float64) - y_ref)
+    bad = err > TOL * T
+    assert not bad.any(), (
+        f"{bad.sum()} outputs out of tolerance; worst ratio {np.max(err / np.maximum(T, 1e-300)):.3g}")
+
+
+def codec_inputs():
+    g = inputs.rng(6)
+    be = 256
+    parts = [
+        inputs.normal(g, (37 * be,), 0.02),
+        inputs.outlier_weights(g, 8, 4 * be, frac=0.01).reshape(-1),
+        inputs.normal(g, (16 * be,)),
+        np.abs(inputs.normal(g, (3 * be,))),
+        -np.abs(inputs.normal(g, (3 * be,))),
+        np.full(2 * be, 0.37, np.float32),
+        np.zeros(2 * be, np.float32),
+        inputs.normal(g, (3 * be,), 1e-6),     # subnormal fp16 scales, clipped codes
+        inputs.normal(g, (2 * be,), 1e-9),     # scale 0
+        inputs.normal(g, (2 * be,), 300.0),
+    ]
+    x = np.concatenate(parts).astype(np.float32)
+    # exact ties in the first super-block: sub-block 1 of range 1953/512
+    # (dmin = 2^-6, d = 2^-9) and sub-block 0 with min 0 and step 3/512, its
+    # elements at 0.5, 2.5 and 30.5 steps (codes 1, 3, 31)
+    r = np.arange(32)
+    x[0:32] = 0.0
+    x[1:4] = np.array([0.5, 2.5, 30.5], np.float32) * 3 / 512
+    x[32:64] = (63 * r - 504) / 512.0
+    return x
+
+
+def test_quantize_bit_exact():
+    x = codec_inputs()
+    assert host(gq.quantize(Q5_K, dev(x))).tobytes() == orc.quantize(Q5_K, x).tobytes()
+
+
+@pytest.mark.parametrize("nblocks", [1, 3, 9, 1000])
+def test_quantize_sizes(nblocks):
+    x = inputs.normal(inputs.rng(nblocks), (nblocks * 256,), 0.5)
+    assert host(gq.quantize(Q5_K, dev(x))).tobytes() == orc.quantize(Q5_K, x).tobytes()
+
+
+def test_dequantize_bit_exact():
+    x = codec_inputs()
+    q = orc.quantize(Q5_K, x)
+    ref = orc.dequantize(Q5_K, q, x.size)
+    got = host(gq.dequantize(Q5_K, dev(q.reshape(-1)), x.size))
+    assert got.view(np.uint32).tobytes() == ref.view(np.uint32).tobytes()
+
+
+SHAPES = [
+    # streaming kernel (every multiple of 256 whose rows fit a two-stage ring)
+    (1, 256, 1), (7, 2048, 1), (130, 4096, 1), (40, 4096, 2), (9, 16384, 3), (33, 768, 5),
+    (19, 2816, 3), (64, 11008, 1), (5, 18432, 2),
+    # plain kernel: rows too long for a two-stage ring of eight warps
+    (2, 131072, 1), (3, 65536, 2),
+]
+
+
+@pytest.mark.parametrize("rows,cols,batch", SHAPES)
+def test_gemv_block_sums_and_y(rows, cols, batch):
+    g = inputs.rng(rows * 7 + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = gq.quantize(Q5_K, dev(W)), gq.quantize(Q8_K, dev(X))
+    assert host(Wd).tobytes() == Wq.tobytes()
+    assert host(Xd).tobytes() == Xq.tobytes()
+    s = host(gq.block_sums(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    np.testing.assert_array_equal(s, orc.block_sums(Q5_K, Wq, Xq, rows, cols, batch))
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, Xq, rows, cols, batch)
+    assert_close(host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch)), y_ref, T)
+
+
+# More rows than the grid has warps: each warp streams several rows through
+# its ring (stage reuse, barrier phase flips), with a ragged last pass.
+TALL_SHAPES = [(4867, 4096, 1), (2435, 8192, 2), (1300, 16384, 1), (3000, 11008, 1)]
+
+
+@pytest.mark.parametrize("rows,cols,batch", TALL_SHAPES)
+def test_gemv_tall(rows, cols, batch):
+    g = inputs.rng(rows + cols)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, X)
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, Xq, rows, cols, batch, nthreads=orc.max_threads())
+    assert_close(host(gq.matmul(Q5_K, dev(Wq), dev(Xq), rows, cols, batch)), y_ref, T)
+    s = host(gq.block_sums(Q5_K, dev(Wq), dev(Xq), rows, cols, batch, gq.PATH_GEMV))
+    idx = np.array([0, 1, rows // 2, rows - 2, rows - 1])
+    np.testing.assert_array_equal(s[:, idx], orc.block_sums(Q5_K, Wq[idx], Xq, len(idx), cols, batch))
+
+
+def test_degenerate_blocks():
+    """Zero, constant, all-negative and tiny weight blocks, a block at the
+    extremes (every sc = 63 and code 31, which drives S1 to 63 * 31 * 127 *
+    256 = 63,499,968 with constant activations) and a zero activation vector."""
+    rows, cols = 8, 2048
+    W = inputs.normal(inputs.rng(3), (rows, cols), 0.02)
+    W[0] = 0.0
+    W[1] = 0.37
+    W[2, :256] = 1e-9
+    W[3, 256:512] = -2.5
+    W[4] = 1.0
+    W[4, 5] = 0.97
+    W[5] = -np.abs(W[5])
+    X = inputs.normal(inputs.rng(4), (2, cols))
+    X[1] = 0.0
+    X[0, :256] = 1.0
+    Wq, Xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, X)
+    assert host(gq.quantize(Q5_K, dev(W))).tobytes() == Wq.tobytes()
+    s = host(gq.block_sums(Q5_K, dev(Wq), dev(Xq), rows, cols, 2, gq.PATH_GEMV))
+    np.testing.assert_array_equal(s, orc.block_sums(Q5_K, Wq, Xq, rows, cols, 2))
+    y = host(gq.matmul(Q5_K, dev(Wq), dev(Xq), rows, cols, 2))
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, Xq, rows, cols, 2)
+    assert_close(y, y_ref, T)
+    assert np.all(y[1] == 0.0) and np.all(y[0, 0] == 0.0)
+
+
+def test_gemv_4096_outlier_weights():
+    """The 4096 x 4096 batch-1 GEMV on the row-spread + 0.1% outlier weights,
+    every row against the oracle."""
+    W, x = inputs.gemv_q4_k(0)
+    Wq, xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, x)
+    Wd = gq.quantize(Q5_K, dev(W))
+    assert host(Wd).tobytes() == Wq.tobytes()
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, xq, 4096, 4096, 1, nthreads=orc.max_threads())
+    assert_close(host(gq.matmul(Q5_K, Wd, dev(xq), 4096, 4096, 1)), y_ref, T)
