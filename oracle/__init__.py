@@ -68,6 +68,8 @@ def lib():
             L.or_block_bytes.restype = i64
             L.or_quantize.argtypes = [i32, vp, vp, i64]
             L.or_quantize.restype = i32
+            L.or_quantize_errmin.argtypes = [i32, vp, vp, i64]
+            L.or_quantize_errmin.restype = i32
             L.or_dequantize.argtypes = [i32, vp, vp, i64]
             L.or_dequantize.restype = i32
             L.or_dequantize_f64.argtypes = [i32, vp, vp, i64]
@@ -114,8 +116,11 @@ def f16_to_f32(h: int) -> float:
     return float(lib().or_f16_to_f32(h))
 
 
-def quantize(t: int, x: np.ndarray) -> np.ndarray:
+def quantize(t: int, x: np.ndarray, errmin: bool = False) -> np.ndarray:
     """Quantize a flat (or row-major 2-D) fp32 array to packed blocks.
+
+    errmin (Q4_K and Q5_K only): the error-minimizing refinement of the
+    sub-block scales and mins instead of the plain min/max fit.
 
     Returns a uint8 array of shape [n / block_elems, block_bytes] for flat
     input, or [rows, cols / block_elems * block_bytes] for 2-D input."""
@@ -125,7 +130,8 @@ def quantize(t: int, x: np.ndarray) -> np.ndarray:
     if n % be:
         raise ValueError("element count must be a multiple of the block size")
     out = np.empty(n // be * bb, dtype=np.uint8)
-    rc = lib().or_quantize(t, _ptr(x), _ptr(out), n)
+    fn = lib().or_quantize_errmin if errmin else lib().or_quantize
+    rc = fn(t, _ptr(x), _ptr(out), n)
     if rc != 0:
         raise ValueError(f"oracle quantize failed ({rc})")
     if x.ndim == 2:

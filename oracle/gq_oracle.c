@@ -400,6 +400,111 @@ static void quantize_q5_k_block(const float *x, uint8_t *blk)
     }
 }
 
+/* ------------------------------------------------------------------ */
+/* Error-minimizing K-quant fit                                          */
+/* ------------------------------------------------------------------ */
+
+/* [P2] §5.5 stores each sub-block's scale and min as small integers under
+ * the super-block's d and dmin, and §7.1 (with §3.3.3's llama-quantize
+ * --imatrix) recommends a quantizer that chooses them to minimize the
+ * weighted reconstruction error; the importance weights need calibration
+ * data, so the reading taken here is the uniform-weight case: per sub-block,
+ * the (sc, m) pair that minimizes the squared error of the 32 reconstructed
+ * values.  Search space (this library's): d and dmin as the min/max fit sets
+ * them, sc in [sc0 - 4, sc0 + 4] and m in [m0 - 4, m0 + 4] clipped to
+ * [0, 63] around the min/max fit's pair (sc0, m0), each candidate's codes
+ * the nearest in [0, qmax] (the fit's rounding rule).  The error of a
+ * candidate is computed in fp32 in a fixed order -- element by element
+ * within each eight-element group, then (g0 + g1) + (g2 + g3) -- so that any
+ * implementation following it makes the same choice.  The first candidate
+ * in (sc, m) ascending order whose error is strictly below the best so far
+ * wins, starting from the min/max pair, so the result is never worse than
+ * the min/max fit in this measure and stays in the same byte format. */
+#define EM_WINDOW 4
+
+static float em_sub_error(const float *x, float d, float dmin, int sc, int m, float qmax, uint8_t *q_out)
+{
+    float step = d * (float)sc;      /* exact */
+    float base = -(dmin * (float)m); /* exact */
+    float g[4];
+    for (int t = 0; t < 4; t++) {
+        float acc = 0.0f;
+        for (int k = 0; k < 8; k++) {
+            int i = 8 * t + k;
+            float qv = (step == 0.0f) ? 0.0f : clampf(rha((x[i] - base) / step), 0.0f, qmax);
+            float rec = step * qv + base;  /* the decoder's d*sc*q - dmin*m, rounded once */
+            float e = x[i] - rec;
+            acc = acc + e * e;
+            if (q_out) q_out[i] = (uint8_t)qv;
+        }
+        g[t] = acc;
+    }
+    return (g[0] + g[1]) + (g[2] + g[3]);
+}
+
+/* Re-chooses sc_j, m_j and the codes of every sub-block of a fitted
+ * super-block (fields and q as k_asym_fit wrote them) by the search above. */
+static void em_refine(const float *x, float qmax, uint16_t dh, uint16_t dminh, uint8_t fields[16],
+                      uint8_t q[256])
+{
+    float d = or_f16_to_f32(dh), dmin = or_f16_to_f32(dminh);
+    for (int j = 0; j < 8; j++) {
+        const float *xj = x + 32 * j;
+        int sc0 = fields[j], m0 = fields[8 + j];
+        int best_sc = sc0, best_m = m0;
+        float best = em_sub_error(xj, d, dmin, sc0, m0, qmax, NULL);
+        for (int sc = sc0 - EM_WINDOW; sc <= sc0 + EM_WINDOW; sc++) {
+            if (sc < 0 || sc > 63) continue;
+            for (int m = m0 - EM_WINDOW; m <= m0 + EM_WINDOW; m++) {
+                if (m < 0 || m > 63) continue;
+                float e = em_sub_error(xj, d, dmin, sc, m, qmax, NULL);
+                if (e < best) {
+                    best = e;
+                    best_sc = sc;
+                    best_m = m;
+                }
+            }
+        }
+        fields[j] = (uint8_t)best_sc;
+        fields[8 + j] = (uint8_t)best_m;
+        em_sub_error(xj, d, dmin, best_sc, best_m, qmax, q + 32 * j);
+    }
+}
+
+/* The error-minimizing Q4_K / Q5_K encoders: the min/max fit, refined. */
+static void quantize_k_errmin_block(int type, const float *x, uint8_t *blk)
+{
+    float qmax = (type == OR_Q4_K) ? 15.0f : 31.0f;
+    uint16_t dh, dminh;
+    uint8_t fields[16], q[256];
+    k_asym_fit(x, qmax, &dh, &dminh, fields, q);
+    em_refine(x, qmax, dh, dminh, fields, q);
+    put_u16(blk + 0, dh);
+    put_u16(blk + 2, dminh);
+    pack6(fields, blk + 4);
+    for (int l = 0; l < 128; l++)
+        blk[16 + l] = (uint8_t)((q[2 * l] & 15) | ((q[2 * l + 1] & 15) << 4));
+    if (type == OR_Q5_K) {
+        for (int k = 0; k < 32; k++) blk[144 + k] = 0;
+        for (int e = 0; e < 256; e++) {
+            int j = e / 32, t = (e % 32) / 8, i = (e % 8) / 2, p = e % 2;
+            if (q[e] >> 4) blk[144 + 4 * j + i] |= (uint8_t)(1u << (2 * t + p));
+        }
+    }
+}
+
+/* Error-minimizing quantization of n elements of Q4_K or Q5_K (-1 for other
+ * types or a bad n, -2 for non-finite input). */
+int or_quantize_errmin(int type, const float *x, uint8_t *dst, int64_t n)
+{
+    if (type != OR_Q4_K && type != OR_Q5_K) return -1;
+    int64_t bb = or_block_bytes(type);
+    if (n < 0 || n % 256) return -1;
+    if (!all_finite(x, n)) return -2;
+    for (int64_t b = 0; b < n / 256; b++) quantize_k_errmin_block(type, x + b * 256, dst + b * bb);
+    return 0;
+}
+
 /* The stored code of element e of a Q4_K (0..15) or Q5_K (0..31) block. */
 static int k_code(int type, const uint8_t *blk, int e)
 {

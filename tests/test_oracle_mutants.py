@@ -86,6 +86,18 @@ MUTANTS = [
      "q |= ((blk[144 + 4 * j + i] >> (2 * t + p)) & 1) << 4;",
      "q |= ((blk[144 + 4 * j + i] >> (2 * t + p)) & 1) << 3;",
      "integer_special_case_q5_k"),
+    ("error-minimizing search window of zero",
+     "#define EM_WINDOW 4",
+     "#define EM_WINDOW 0",
+     "errmin"),
+    ("error-minimizing search scores absolute instead of squared errors",
+     "acc = acc + e * e;",
+     "acc = acc + fabsf(e);",
+     "errmin_window_bruteforce"),
+    ("error-minimizing search keeps the last candidate tried",
+     "if (e < best) {",
+     "if (1) {",
+     "errmin"),
     ("q8_0 scale max/128 instead of max/127",
      "uint16_t dh = or_f16_rn(amax / 127.0f);",
      "uint16_t dh = or_f16_rn(amax / 128.0f);",

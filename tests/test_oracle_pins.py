@@ -351,6 +351,80 @@ def test_roundtrip_q4_k(t, qmax):
         np.testing.assert_array_equal(codes[ok], np.round(qq[ok]).astype(np.int64))
 
 
+def _k_fields(q):
+    """d, dmin and the 6-bit fields of Q4_K / Q5_K blocks, from the bytes."""
+    return _q4k_fields(q)
+
+
+def _sub_sse(x, xh):
+    """Squared reconstruction error per sub-block, float64: [blocks, 8]."""
+    return ((x.reshape(-1, 8, 32).astype(np.float64) - xh.reshape(-1, 8, 32)) ** 2).sum(axis=2)
+
+
+@pytest.mark.parametrize("t", [Q4_K, Q5_K])
+def test_errmin_never_worse_and_same_format(t):
+    """The error-minimizing encoder keeps the min/max fit's d and dmin (bytes
+    0..3) and never reconstructs a sub-block worse than the min/max fit
+    (float64 error, up to the fp32 rounding of the encoder's own measure)."""
+    x = np.concatenate([_blocks_zoo(256), inputs.outlier_weights(inputs.rng(5), 32, 2048, frac=0.01).reshape(-1)])
+    a, b = orc.quantize(t, x), orc.quantize(t, x, errmin=True)
+    assert a.shape == b.shape
+    np.testing.assert_array_equal(a[:, :4], b[:, :4])
+    ea = _sub_sse(x, orc.dequantize_f64(t, a, x.size))
+    eb = _sub_sse(x, orc.dequantize_f64(t, b, x.size))
+    assert np.all(eb <= ea * (1 + 1e-5) + 1e-30)
+    assert eb.sum() < 0.9 * ea.sum()  # and it does find better pairs on these inputs
+
+
+def _round_half_away(v):
+    return np.sign(v) * np.floor(np.abs(v) + 0.5)
+
+
+@pytest.mark.parametrize("t,qmax", [(Q4_K, 15), (Q5_K, 31)])
+def test_errmin_window_bruteforce(t, qmax):
+    """Brute force of the search's definition, in float64: for every
+    sub-block, every (sc, m) within 4 of the min/max fit's pair (clipped to
+    0..63) with its nearest codes; the encoder's choice lies in that window
+    and is its minimum up to fp32 rounding."""
+    x = inputs.outlier_weights(inputs.rng(6), 4, 512, frac=0.02).reshape(-1)
+    a, b = orc.quantize(t, x), orc.quantize(t, x, errmin=True)
+    d, dmin, sc0, m0 = _k_fields(a)
+    _, _, sc1, m1 = _k_fields(b)
+    eb = _sub_sse(x, orc.dequantize_f64(t, b, x.size))
+    xb = x.reshape(-1, 8, 32).astype(np.float64)
+    for blk in range(xb.shape[0]):
+        for j in range(8):
+            assert abs(sc1[blk, j] - sc0[blk, j]) <= 4 and abs(m1[blk, j] - m0[blk, j]) <= 4
+            best = np.inf
+            for sc in range(max(0, sc0[blk, j] - 4), min(63, sc0[blk, j] + 4) + 1):
+                for m in range(max(0, m0[blk, j] - 4), min(63, m0[blk, j] + 4) + 1):
+                    step, base = d[blk] * sc, -dmin[blk] * m
+                    qv = np.zeros(32) if step == 0 else np.clip(_round_half_away((xb[blk, j] - base) / step), 0, qmax)
+                    best = min(best, ((xb[blk, j] - (step * qv + base)) ** 2).sum())
+            assert eb[blk, j] <= best * (1 + 1e-5) + 1e-30
+
+
+def test_errmin_hand_case():
+    """A sub-block on the grid of step 2^-8 * 5 (codes 0..15, min 0) whose
+    largest element sits a hair above 15 steps: the min/max fit rounds the
+    scale up to sc = 6 (every other element then falls between codes), while
+    sc = 5 reconstructs all but that element exactly.  Sub-block 1 fixes
+    d = 2^-8 (range 945/256)."""
+    x = np.zeros(256, np.float32)
+    c = np.array([0, 15, 3, 8, 1, 12, 7, 4] * 4, np.float32)
+    x[0:32] = c * 5 / 256
+    x[1] = np.float32(75.01 / 256)
+    x[32:64] = np.arange(32, dtype=np.float32) * 945 / 256 / 31
+    a, b = orc.quantize(Q4_K, x), orc.quantize(Q4_K, x, errmin=True)
+    d, _, sc0, _ = _k_fields(a)
+    _, _, sc1, _ = _k_fields(b)
+    assert d[0] == 2.0 ** -8 and sc0[0, 0] == 6 and sc1[0, 0] == 5
+    xh = orc.dequantize_f64(Q4_K, b, 256)
+    others = np.r_[0, 2:32]
+    np.testing.assert_array_equal(xh[others], x[others].astype(np.float64))
+    assert _sub_sse(x, xh)[0, 0] < 1e-3 * _sub_sse(x, orc.dequantize_f64(Q4_K, a, 256))[0, 0]
+
+
 def test_nonfinite_rejected():
     x = np.zeros(32, np.float32)
     x[3] = np.nan
