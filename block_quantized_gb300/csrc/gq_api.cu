@@ -229,6 +229,20 @@ gq_status gq_quantize_rows(gq_type type, const float *src, void *dst, int64_t n)
     return gq_quantize_rows_async(type, src, dst, n, nullptr);
 }
 
+gq_status gq_quantize_rows_ex(gq_type type, const float *src, void *dst, int64_t n, unsigned flags,
+                              gq_stream_t stream) {
+    if (flags & ~(unsigned)GQ_QUANT_ERRMIN) return GQ_ERR_TYPE;
+    if (!(flags & GQ_QUANT_ERRMIN)) return gq_quantize_rows_async(type, src, dst, n, stream);
+    if (type != GQ_Q4_K && type != GQ_Q5_K) return GQ_ERR_TYPE;
+    gq_status st = check_codec(type, src, dst, n, true);
+    if (st != GQ_OK || n == 0) return st;
+    LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != GQ_OK) return st;
+    cudaError_t e = launch_quantize_k_errmin(type, src, dst, n, ctx);
+    return e == cudaSuccess ? GQ_OK : cuda_fail(e);
+}
+
 gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, int64_t n,
                                    gq_stream_t stream) {
     gq_status st = check_codec(type, dst, src, n, false);

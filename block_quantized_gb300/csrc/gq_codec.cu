@@ -137,7 +137,37 @@ __global__ void __launch_bounds__(256) quantize_q8_k_kernel(const float *__restr
 // The low four bits of the codes fill bytes 16..143 (element 2l in the low
 // nibble of byte 16 + l); Q5_K puts the fifth bit of element
 // 32j + 8t + 2i + p into bit 2t + p of byte 144 + 4j + i.
+//
+// ERRMIN: the error-minimizing refinement ("llama.cpp 推理引擎" §5.5 with
+// §7.1: sub-block scales chosen for the least reconstruction error, uniform
+// importance).  d and dmin stay the fit's; per sub-block every (sc, m) within
+// EM_WINDOW of the fit's pair (clipped to 0..63) is scored by the squared
+// error of its 32 reconstructed values (codes the nearest in [0, QMAX]),
+// computed in fp32 in a fixed order -- each lane's eight elements in turn,
+// then (g0 + g1) + (g2 + g3) over the sub-block's four lanes -- and the first
+// candidate in (sc, m) ascending order strictly below the best so far wins,
+// starting from the fit's pair.
+constexpr int EM_WINDOW = 4;
+
+// Squared reconstruction error of this lane's sub-block (all four lanes get
+// the same value) for the pair (sc, m).
 template <int QMAX>
+__device__ __forceinline__ float em_sub_error(const float (&v)[8], float d, float dmin, float sc, float m) {
+    const float step = __fmul_rn(d, sc);
+    const float base = -__fmul_rn(dmin, m);
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float q =
+            (step == 0.0f) ? 0.0f : clampf(roundf(__fdiv_rn(__fsub_rn(v[i], base), step)), 0.0f, (float)QMAX);
+        const float e = __fsub_rn(v[i], __fadd_rn(__fmul_rn(step, q), base));
+        acc = __fadd_rn(acc, __fmul_rn(e, e));
+    }
+    acc = __fadd_rn(acc, __shfl_xor_sync(FULL, acc, 1));
+    return __fadd_rn(acc, __shfl_xor_sync(FULL, acc, 2));
+}
+
+template <int QMAX, bool ERRMIN>
 __global__ void __launch_bounds__(256) quantize_k_kernel(const float *__restrict__ x,
                                                          uint8_t *__restrict__ dst,
                                                          int64_t nblocks) {
@@ -174,7 +204,7 @@ __global__ void __launch_bounds__(256) quantize_k_kernel(const float *__restrict
         const float dmin = __half2float(dminh);
         float m = (dmin == 0.0f) ? 0.0f : ceilf(__fdiv_rn(-lo, dmin));
         if (m > 63.0f) m = 63.0f;
-        const float base = -__fmul_rn(dmin, m);
+        float base = -__fmul_rn(dmin, m);
         const float r = __fsub_rn(hi, base);
         float rmax = r;
 #pragma unroll
@@ -184,6 +214,23 @@ __global__ void __launch_bounds__(256) quantize_k_kernel(const float *__restrict
         const float d = __half2float(dh);
         float sc = (d == 0.0f) ? 0.0f : ceilf(__fdiv_rn(r, __fmul_rn((float)QMAX, d)));
         if (sc > 63.0f) sc = 63.0f;
+        if (ERRMIN) {
+            const float sc0 = sc, m0 = m;
+            float best = em_sub_error<QMAX>(v, d, dmin, sc0, m0);
+            for (int a = -EM_WINDOW; a <= EM_WINDOW; ++a) {
+                for (int c = -EM_WINDOW; c <= EM_WINDOW; ++c) {
+                    const float cs = sc0 + (float)a, cm = m0 + (float)c;
+                    const bool ok = cs >= 0.0f && cs <= 63.0f && cm >= 0.0f && cm <= 63.0f;
+                    const float e = em_sub_error<QMAX>(v, d, dmin, ok ? cs : sc0, ok ? cm : m0);  // uniform shuffles
+                    if (ok && e < best) {
+                        best = e;
+                        sc = cs;
+                        m = cm;
+                    }
+                }
+            }
+            base = -__fmul_rn(dmin, m);
+        }
         const float step = __fmul_rn(d, sc);
         uint32_t packed = 0, fifth = 0;
 #pragma unroll
@@ -303,12 +350,21 @@ cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
         return launch_pdl(quantize32_kernel<7>, grid, 256, 0, ctx.stream, src, d8, nb, std::max<int64_t>(nb, 1),
                           (int64_t)0);
     case GQ_Q4_K:
-        return launch_pdl(quantize_k_kernel<15>, grid, 256, 0, ctx.stream, src, d8, nb);
+        return launch_pdl(quantize_k_kernel<15, false>, grid, 256, 0, ctx.stream, src, d8, nb);
     case GQ_Q5_K:
-        return launch_pdl(quantize_k_kernel<31>, grid, 256, 0, ctx.stream, src, d8, nb);
+        return launch_pdl(quantize_k_kernel<31, false>, grid, 256, 0, ctx.stream, src, d8, nb);
     case GQ_Q8_K:
         return launch_pdl(quantize_q8_k_kernel, grid, 256, 0, ctx.stream, src, d8, nb);
     }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_k_errmin(gq_type t, const float *src, void *dst, int64_t n, const LaunchCtx &ctx) {
+    const int64_t nb = n / QK_K;
+    const int grid = grid_for(nb, 8, ctx.num_sms);
+    uint8_t *d8 = static_cast<uint8_t *>(dst);
+    if (t == GQ_Q4_K) return launch_pdl(quantize_k_kernel<15, true>, grid, 256, 0, ctx.stream, src, d8, nb);
+    if (t == GQ_Q5_K) return launch_pdl(quantize_k_kernel<31, true>, grid, 256, 0, ctx.stream, src, d8, nb);
     return cudaErrorInvalidValue;
 }
 

@@ -37,6 +37,8 @@ cudaError_t launch_quantize(gq_type t, const float *src, void *dst, int64_t n,
                             const LaunchCtx &ctx);
 cudaError_t launch_dequantize(gq_type t, const void *src, float *dst, int64_t n,
                               const LaunchCtx &ctx);
+// The error-minimizing Q4_K / Q5_K encoder (GQ_QUANT_ERRMIN).
+cudaError_t launch_quantize_k_errmin(gq_type t, const float *src, void *dst, int64_t n, const LaunchCtx &ctx);
 // Q8_0 / Q4_0 quantize of `rows` rows of row_blocks blocks each, destination
 // rows dst_row_stride blocks apart (the KV-cache append).
 cudaError_t launch_quantize_rows_strided(gq_type t, const float *src, void *dst, int64_t rows,

@@ -21,6 +21,7 @@ from . import build as _build
 Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K = 0, 1, 2, 3, 4, 5
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 FLAG_W_STATIC = 1
+QUANT_ERRMIN = 1
 ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q5_K: Q8_K}
 BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q8_K: 256, Q6_K: 256, Q5_K: 256}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q8_K: 276, Q6_K: 194, Q5_K: 176}
@@ -37,6 +38,7 @@ SIGNATURES = {
     "gq_last_cuda_error": ([], _i32),
     "gq_quantize_rows": ([_i32, _vp, _vp, _i64], _i32),
     "gq_quantize_rows_async": ([_i32, _vp, _vp, _i64, _vp], _i32),
+    "gq_quantize_rows_ex": ([_i32, _vp, _vp, _i64, ctypes.c_uint, _vp], _i32),
     "gq_dequantize_rows": ([_i32, _vp, _vp, _i64], _i32),
     "gq_dequantize_rows_async": ([_i32, _vp, _vp, _i64, _vp], _i32),
     "gq_matmul": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _vp], _i32),
@@ -131,6 +133,11 @@ def gq_block_bytes(t: int) -> int:
 def gq_quantize_rows_async(t: int, src, dst, n: int, stream=None) -> None:
     _check("gq_quantize_rows_async",
            load().gq_quantize_rows_async(t, _p(src), _p(dst), n, _s(stream)))
+
+
+def gq_quantize_rows_ex(t: int, src, dst, n: int, flags: int = 0, stream=None) -> None:
+    _check("gq_quantize_rows_ex",
+           load().gq_quantize_rows_ex(t, _p(src), _p(dst), n, flags, _s(stream)))
 
 
 def gq_quantize_rows(t: int, src, dst, n: int) -> None:
@@ -242,15 +249,16 @@ def packed_bytes(t: int, n: int) -> int:
     return n // BLOCK_ELEMS[t] * BLOCK_BYTES[t]
 
 
-def quantize(t: int, x, stream=None):
+def quantize(t: int, x, stream=None, flags: int = 0):
     """Quantize a CUDA fp32 tensor [..., cols] into a uint8 tensor
-    [..., cols / block_elems * block_bytes]."""
+    [..., cols / block_elems * block_bytes] (flags: QUANT_ERRMIN for the
+    error-minimizing Q4_K / Q5_K encoder)."""
     import torch
     assert x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()
     cols = x.shape[-1]
     out = torch.empty(*x.shape[:-1], cols // BLOCK_ELEMS[t] * BLOCK_BYTES[t],
                       dtype=torch.uint8, device=x.device)
-    gq_quantize_rows_async(t, x, out, x.numel(), stream)
+    gq_quantize_rows_ex(t, x, out, x.numel(), flags, stream)
     return out
 
 

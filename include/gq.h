@@ -165,6 +165,31 @@ gq_status gq_quantize_rows(gq_type type, const float *src, void *dst, int64_t n)
 gq_status gq_quantize_rows_async(gq_type type, const float *src, void *dst, int64_t n,
                                  gq_stream_t stream);
 
+/* Flags for gq_quantize_rows_ex. */
+enum {
+    /* Error-minimizing K-quant encoder (Q4_K and Q5_K only): "llama.cpp 推理
+     * 引擎" §5.5 stores each sub-block's scale and min as 6-bit integers under
+     * the super-block's d and dmin, and §7.1 recommends choosing them for the
+     * least (importance-weighted) reconstruction error; with uniform weights
+     * (no calibration data is taken) this encoder keeps the min/max fit's d
+     * and dmin and, per 32-element sub-block, picks the (sc, m) within 4 of
+     * the fit's pair (clipped to 0..63) whose 32 reconstructed values, codes
+     * the nearest in range, have the least squared error.  The error is
+     * computed in fp32 in a fixed order (each group of eight consecutive
+     * elements in turn, then (g0 + g1) + (g2 + g3)); the first candidate in
+     * (sc, m) ascending order strictly below the best so far wins, starting
+     * from the fit's pair -- so no sub-block is reconstructed worse than by
+     * the min/max fit in that measure.  Same byte format: every decoder and
+     * product reads the result unchanged. */
+    GQ_QUANT_ERRMIN = 1u
+};
+
+/* gq_quantize_rows_async with flags (0 = the default encoder).  Errors as
+ * gq_quantize_rows, plus GQ_ERR_TYPE for an unknown flag bit or
+ * GQ_QUANT_ERRMIN with a type other than Q4_K / Q5_K. */
+gq_status gq_quantize_rows_ex(gq_type type, const float *src, void *dst, int64_t n, unsigned flags,
+                              gq_stream_t stream);
+
 /*
  * Reconstruct n fp32 values from packed blocks ("llama.cpp 推理引擎" §5.3
  * and §5.5 dequantization formulas, with the fp16 scale of Q8_0 and the

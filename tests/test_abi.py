@@ -102,6 +102,14 @@ def test_codec_validation(lib):
     assert q(4, A16, A16 + 1, 256) == ALIGN                     # Q6_K dst 2-aligned
     assert q(4, A16, A16, 32) == SHAPE
     assert q(1, 0, 0, 0) == OK
+    e = lib.gq_quantize_rows_ex
+    assert e(2, A16, A16, 256, 2, None) == TYPE                  # unknown flag bit
+    assert e(1, A16, A16, 32, 1, None) == TYPE                   # error-minimizing: K-quants only
+    assert e(4, A16, A16, 256, 1, None) == TYPE
+    assert e(2, A16, A16, 32, 1, None) == SHAPE
+    assert e(5, A16, A16 + 2, 256, 1, None) == ALIGN
+    assert e(2, 0, 0, 0, 1, None) == OK
+    assert e(0, A16, A16, 33, 0, None) == SHAPE                  # flags 0: the default encoder's rules
     d = lib.gq_dequantize_rows
     assert d(0, A16, A16, 31) == SHAPE
     assert d(2, A16 + 2, A16, 256) == ALIGN
