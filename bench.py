@@ -21,7 +21,7 @@ number of library kernel launches in the timed region, and the SM clocks
 sampled during it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
-                  [--only prefill|sweep|decode|stream|kv|q6k|q5k|q4_0] [--no-cpu]
+                  [--only prefill|sweep|decode|stream|kv|kv_q4_0|q6k|q5k|q4_0] [--no-cpu]
 """
 from __future__ import annotations
 
@@ -51,7 +51,7 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "q6k", "q5k", "q4_0"],
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "kv_q4_0", "q6k", "q5k", "q4_0"],
                    default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
@@ -475,6 +475,7 @@ def run_gpu(args, world, rank):
               "stream": lambda: bench_stream(gq, inputs, torch, np, dev, s, capture, time_graph, hbm_peak,
                                              args.steps),
               "kv": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak),
+              "kv_q4_0": lambda: bench_kv(gq, torch, dev, capture, time_graph, hbm_peak, types=("q4_0",)),
               "q6k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
                                        cpu=rank == 0 and world == 1 and not args.no_cpu),
               "q5k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
@@ -747,6 +748,7 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
                         f"({COPIES * w_bytes / 1e6:.0f} MB)",
             "cpu_baseline": run_cpu_q6k(wtype=wt) if cpu else None,
             "kernel": f"gemv_{name.lower().replace('_', '')}_kernel (whole-row bulk copies, per-warp ring)",
+            "traffic": kernel_traffic("gemv_" + name.lower().replace("_", "")),
             "launch_us": per * 1e6, "alg_bytes_per_launch": alg, "weight_gbps": w_bytes / per / 1e9,
             "achieved": alg / per / 1e9, "frac": alg / per / 1e9 / hbm_peak,
             "streaming": {"workload": f"one launch over 262144 x 4096 {name} rows "
@@ -755,7 +757,7 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
                           "frac": COPIES * w_bytes / tall_s / 1e9 / hbm_peak}}
 
 
-def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak):
+def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak, types=("q8_0", "q4_0")):
     """Quantized KV cache at 7B shape: 32 heads x 4096 positions x 128, keys
     as Q8_0 and as Q4_0.  Scores of one query against every cached key,
     rotated over 16 layer caches (larger than L2) and timed back to back; and
@@ -766,6 +768,8 @@ def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak):
     q = torch.randn(n_heads, head_dim, device=dev, generator=g)
     x = torch.randn(n_heads, head_dim, device=dev, generator=g)
     for name, t in (("q8_0", gq.Q8_0), ("q4_0", gq.Q4_0)):
+        if name not in types:
+            continue
         caches = [gq.kv_cache(t, n_heads, capacity, head_dim, dev) for _ in range(layers)]
         keys = torch.randn(capacity, n_heads, head_dim, device=dev, generator=g)
         for p in range(capacity):
@@ -790,7 +794,7 @@ def bench_kv(gq, torch, dev, capture, time_graph, hbm_peak):
         t_a, _ = time_graph(capture(app), 20, 3)
         out[name] = {"scores_us": per * 1e6, "key_bytes": kbytes, "key_gbps": kbytes / per / 1e9,
                      "frac": kbytes / per / 1e9 / hbm_peak, "append_us": t_a / (20 * layers) * 1e6,
-                     "traffic": kernel_traffic("kv_scores_q8_0") if t == gq.Q8_0 else None}
+                     "traffic": kernel_traffic("kv_scores_" + name)}
         del caches
         torch.cuda.empty_cache()
     return out
