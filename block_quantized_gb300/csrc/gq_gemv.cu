@@ -77,9 +77,6 @@ constexpr unsigned FULL = 0xffffffffu;
 #ifndef GQ_GEMV_PREFETCH
 #define GQ_GEMV_PREFETCH 1
 #endif
-#ifndef GQ_GEMV_BALANCE
-#define GQ_GEMV_BALANCE 0
-#endif
 
 constexpr int WARPS = GQ_GEMV_WARPS;      // warps per CTA
 
@@ -756,7 +753,7 @@ __host__ __device__ constexpr int bufs_off() {
 // dependency wait on the preceding kernel (the caller guarantees no kernel
 // still in flight writes W).
 template <int WT, int NB, bool SUMS, bool FUSED, int NW>
-__global__ void __launch_bounds__(NW * 32, NB == 1 ? GQ_GEMV_MIN_BLOCKS : 1) gemv_kernel(const uint8_t *__restrict__ W,
+__global__ void __launch_bounds__(NW * 32, GQ_GEMV_MIN_BLOCKS) gemv_kernel(const uint8_t *__restrict__ W,
                                                    const void *__restrict__ act_in,
                                                    float *__restrict__ y,
                                                    int32_t *__restrict__ sums, int rows,
@@ -769,7 +766,7 @@ __global__ void __launch_bounds__(NW * 32, NB == 1 ? GQ_GEMV_MIN_BLOCKS : 1) gem
     const int b0 = blockIdx.y * NB;
     const int nvec = min(NB, batch - b0);
     const int warps_total = gridDim.x * NW;
-    const int wg = GQ_GEMV_BALANCE ? warp * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * NW + warp;
+    const int wg = blockIdx.x * NW + warp;
     const int nchunk = (nblk + F::CH - 1) / F::CH;
     const int R = geo.R, ns = geo.ns;
     const int ipg = geo.whole ? 1 : nchunk;  // ring items per row group
@@ -1066,7 +1063,7 @@ cudaError_t launch_one(const void *W, const void *act, float *y, int32_t *sums, 
     if (e != cudaSuccess) return e;
     const int per_sm = std::max(1, std::min(CTAS_PER_SM, occ));
     const int groups = (rows + geo.R - 1) / geo.R;
-    int grid = GQ_GEMV_BALANCE ? groups : (groups + NW - 1) / NW;
+    int grid = (groups + NW - 1) / NW;
     grid = std::max(1, std::min(grid, ctx.num_sms * per_sm));
     dim3 g(grid, (batch + NB - 1) / NB);
     return launch_pdl(k, g, dim3(NW * 32), smem, ctx.stream, static_cast<const uint8_t *>(W), act,

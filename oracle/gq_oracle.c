@@ -383,11 +383,11 @@ static void quantize_q4_k_block(const float *x, uint8_t *blk)
  * bits of the codes in bytes 0..143 exactly as Q4_K, then 32 bytes @144 with
  * the fifth bits: byte 144 + 4j + i holds, in bit 2t + p, the fifth bit of
  * element 32j + 8t + 2i + p (sub-block j, t = 0..3, i = 0..3, p = 0..1). */
-static void quantize_q5_k_block(const float *x, uint8_t *blk)
+/* Writes a fitted Q5_K super-block: d, dmin, the fields, the low nibbles
+ * and the fifth-bit plane. */
+static void put_q5_k_block(uint16_t dh, uint16_t dminh, const uint8_t fields[16], const uint8_t q[256],
+                           uint8_t *blk)
 {
-    uint16_t dh, dminh;
-    uint8_t fields[16], q[256];
-    k_asym_fit(x, 31.0f, &dh, &dminh, fields, q);
     put_u16(blk + 0, dh);
     put_u16(blk + 2, dminh);
     pack6(fields, blk + 4);
@@ -398,6 +398,14 @@ static void quantize_q5_k_block(const float *x, uint8_t *blk)
         int j = e / 32, t = (e % 32) / 8, i = (e % 8) / 2, p = e % 2;
         if (q[e] >> 4) blk[144 + 4 * j + i] |= (uint8_t)(1u << (2 * t + p));
     }
+}
+
+static void quantize_q5_k_block(const float *x, uint8_t *blk)
+{
+    uint16_t dh, dminh;
+    uint8_t fields[16], q[256];
+    k_asym_fit(x, 31.0f, &dh, &dminh, fields, q);
+    put_q5_k_block(dh, dminh, fields, q, blk);
 }
 
 /* ------------------------------------------------------------------ */
@@ -479,18 +487,15 @@ static void quantize_k_errmin_block(int type, const float *x, uint8_t *blk)
     uint8_t fields[16], q[256];
     k_asym_fit(x, qmax, &dh, &dminh, fields, q);
     em_refine(x, qmax, dh, dminh, fields, q);
+    if (type == OR_Q5_K) {
+        put_q5_k_block(dh, dminh, fields, q, blk);
+        return;
+    }
     put_u16(blk + 0, dh);
     put_u16(blk + 2, dminh);
     pack6(fields, blk + 4);
     for (int l = 0; l < 128; l++)
         blk[16 + l] = (uint8_t)((q[2 * l] & 15) | ((q[2 * l + 1] & 15) << 4));
-    if (type == OR_Q5_K) {
-        for (int k = 0; k < 32; k++) blk[144 + k] = 0;
-        for (int e = 0; e < 256; e++) {
-            int j = e / 32, t = (e % 32) / 8, i = (e % 8) / 2, p = e % 2;
-            if (q[e] >> 4) blk[144 + 4 * j + i] |= (uint8_t)(1u << (2 * t + p));
-        }
-    }
 }
 
 /* Error-minimizing quantization of n elements of Q4_K or Q5_K (-1 for other
