@@ -639,6 +639,7 @@ def summary_keys(line: dict) -> dict:
            "stream_frac": r(get(line, "roofline_streaming", "frac")),
            "decode_tok_s": r(get(line, "decode", "tok_s"), 1),
            "decode_fused_weights_tok_s": r(get(line, "decode", "fused_weights", "tok_s"), 1),
+           "decode_head_us": r(get(line, "decode", "head_q8_0", "us_per_token"), 1),
            "prefill_ms": r(get(line, "prefill", "results", "mma", "ms"), 4),
            "prefill_tops": r(get(line, "prefill", "results", "mma", "tops"), 1),
            "prefill_frac": r(get(line, "prefill", "results", "mma", "roofline", "frac"))}
@@ -878,6 +879,16 @@ def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
         res[name] = {"tok_s": world / per_tok, "ms_per_token": per_tok * 1e3,
                      "weight_gbps": bytes_tok / per_tok / 1e9, "launches_per_token": launches}
     res["tok_s"] = max(res["unfused"]["tok_s"], res["fused"]["tok_s"], res["fused_weights"]["tok_s"])
+
+    # the Q8_0 output head alone (139 MB, larger than L2), fused act-quantize,
+    # as dependent launches: its share of a token
+    def head_chain():
+        for _ in range(8):
+            gq.gq_matmul_f32(gq.Q8_0, head, xin["head"], yh, hr, hc, 1, F)
+    t_h, _ = time_graph(capture(head_chain), 10, 2)
+    per_head = t_h / 80
+    res["head_q8_0"] = {"us_per_token": per_head * 1e6, "weight_gbps": head.numel() / per_head / 1e9,
+                        "share_of_token": per_head / res["fused_weights"]["ms_per_token"] * 1e3}
     del layers, head, fused_w
     torch.cuda.empty_cache()
     return res
