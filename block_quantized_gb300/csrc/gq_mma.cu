@@ -43,7 +43,8 @@
 //              (second half);
 //   warps 12-27 epilogue: four threads per row, 32 columns each (the warps
 //              whose columns lie past TN idle).
-// Per super-block a ready barrier (A and min-term rows built) and a done
+// Per super-block a ready barrier (A and min-term rows built, the S1 buffer
+// of its parity released by the epilogue) and a done
 // barrier (one commit after its MMAs, which frees its S1/S2 for the
 // epilogue and its activation slots and min-term rows for reuse), in a ring.
 // Tensor memory (512 columns): the S1 accumulator, double-buffered by
@@ -162,10 +163,10 @@ struct Cfg {
     static constexpr int OFF_RAW = OFF_MINA + NSM * MIN_A;        // NRAW x 18 KB
     static constexpr int OFF_META = OFF_RAW + NRAW * RAW_STAGE;   // NSM scale stages
     static constexpr int OFF_BAR = OFF_META + NSM * META_STAGE;
-    // per super-block ready (A and min-term rows built) and done (all its
-    // MMAs complete), A empty, B tx, raw full/empty, meta full/empty, S1
-    // empty, final.
-    static constexpr int NBARS = 2 * NF + NA + NBS + 2 * NRAW + 2 * NSM + 2 + 1;
+    // per super-block ready (A and min-term rows built, S1 buffer free) and
+    // done (all its MMAs complete), A empty, B tx, raw full/empty, meta
+    // full/empty, final.
+    static constexpr int NBARS = 2 * NF + NA + NBS + 2 * NRAW + 2 * NSM + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
@@ -373,7 +374,10 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
 // Barriers.  b_tx and raw_full complete when a copy has landed (their only
 // arrival is the producer's expect-tx).  Per super-block sb, in a ring of NF:
 //   sb_full[sb % NF]: its A operand (one arrival per builder warp) and its
-//                     min-term A rows (one per hh = 0 builder warp) are in place;
+//                     min-term A rows (one per hh = 0 builder warp) are in
+//                     place, and the S1 buffer of its parity is free (one
+//                     arrival per active epilogue warp after it read S1 of
+//                     sb - 2; made at initialization for sb = 0, 1);
 //   sb_done[sb % NF]: every MMA of sb has completed (one commit) -- its S1 and
 //                     S2 may be read, and its two B slots and min-term rows
 //                     reused.
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
 // waiter itself, a resource that x releases.
 struct Bars {
     uint64_t *sb_full, *sb_done, *a_empty, *b_tx, *raw_full, *raw_empty;
-    uint64_t *meta_full, *meta_empty, *acc_empty, *fin;
+    uint64_t *meta_full, *meta_empty, *fin;
 };
 
 template <class C>
@@ -397,8 +401,7 @@ __device__ __forceinline__ Bars bars_at(uint8_t *smem) {
     r.raw_empty = r.raw_full + C::NRAW;
     r.meta_full = r.raw_empty + C::NRAW;
     r.meta_empty = r.meta_full + NSM;
-    r.acc_empty = r.meta_empty + NSM;
-    r.fin = r.acc_empty + 2;
+    r.fin = r.meta_empty + NSM;
     return r;
 }
 
@@ -616,8 +619,9 @@ __device__ __forceinline__ void mma8_ta(uint32_t d, const uint32_t (&a)[8], cons
 
 
 // MMA issuer (warp 1, one thread).  Per super-block: once its A operand and
-// min-term rows are built (sb_full), the S1 buffer of its parity is drained
-// and the first B half has landed, eight K=16 steps of the S1 product (A from
+// min-term rows are built and the S1 buffer of its parity is drained (both
+// counted by sb_full) and the first B half has landed, eight K=16 steps of
+// the S1 product (A from
 // the super-block's tensor-memory buffer, B from the ring), then after the
 // second half has landed eight more, then one K=16 step of the min-term
 // product S2 written over the consumed A buffer; then a single commit
@@ -632,11 +636,9 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
     bool ok = true;
     for (int sb = 0; ok && sb < nsb; ++sb) {
         const int p = sb & 1;                                   // S1 buffer
-        const uint32_t ph = (uint32_t)(sb >> 1) & 1u;
         const int ai = sb % C::NA;                              // A buffer
         const int f = sb % NF;                                  // ready / done ring, min-term rows
         if (!(ok = wait_or_abort(B.sb_full + f, (uint32_t)(sb / NF) & 1u, abort))) break;
-        if (!(ok = wait_or_abort(B.acc_empty + p, ph ^ 1u, abort))) break;
         for (int h = 0; h < 2; ++h) {
             const int sl = b_slot<C>(sb, h);
             if (!(ok = wait_or_abort(B.b_tx + sl, b_phase<C>(sb), abort))) break;
@@ -706,7 +708,9 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(B.acc_empty + p);
+                    // S1 buffer p is next accumulated by super-block sb + 2: its
+                    // ready barrier counts this release
+                    if (sb + 2 < nsb) mbar_arrive(B.sb_full + (sb + 2) % NF);
                     mbar_arrive(B.a_empty + ai);
                 }
             }
@@ -765,12 +769,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NF; ++i) {
-            // one arrival per builder warp (A) and per hh = 0 builder warp (min-term rows)
-            mbar_init(B.sb_full + i, BLD_THREADS / 32 + 4);
+            // one arrival per builder warp (A), per hh = 0 builder warp (min-term
+            // rows) and per active epilogue warp (the S1 buffer of the
+            // super-block's parity released by super-block sb - 2)
+            mbar_init(B.sb_full + i, BLD_THREADS / 32 + 4 + C::EPI_ACTIVE);
             mbar_init(B.sb_done + i, 1);
         }
+        // super-blocks 0 and 1 find their S1 buffers free
+        for (int i = 0; i < 2; ++i)
+            for (int k = 0; k < C::EPI_ACTIVE; ++k) mbar_arrive(B.sb_full + i);
         for (int i = 0; i < C::NA; ++i) mbar_init(B.a_empty + i, C::EPI_ACTIVE);  // S2 over it read
-        for (int i = 0; i < 2; ++i) mbar_init(B.acc_empty + i, C::EPI_ACTIVE);
         for (int i = 0; i < C::NBS; ++i) mbar_init(B.b_tx + i, 1);
         for (int i = 0; i < C::NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
