@@ -21,7 +21,7 @@ number of library kernel launches in the timed region, and the SM clocks
 sampled during it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--quick]
-                  [--only prefill|sweep|decode|stream|kv|kv_q4_0|q6k|q5k|q4_0] [--no-cpu]
+                  [--only prefill|sweep|decode|stream|kv|kv_q4_0|q6k|q5k|q4_0|q0_gemm] [--no-cpu]
 """
 from __future__ import annotations
 
@@ -51,7 +51,8 @@ def parse_args():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--quick", action="store_true", help="headline only (no sweeps)")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "kv_q4_0", "q6k", "q5k", "q4_0"],
+    p.add_argument("--only", choices=["prefill", "sweep", "decode", "stream", "kv", "kv_q4_0", "q6k", "q5k", "q4_0",
+                                      "q0_gemm"],
                    default=None,
                    help="run one secondary workload alone and print its result (profiling)")
     return p.parse_args()
@@ -481,7 +482,8 @@ def run_gpu(args, world, rank):
               "q5k": lambda: bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak,
                                        cpu=rank == 0 and world == 1 and not args.no_cpu, wtype=gq.Q5_K),
               "q4_0": lambda: bench_q4_0(gq, inputs, torch, np, dev, capture, time_graph,
-                                         cpu=rank == 0 and world == 1 and not args.no_cpu)}
+                                         cpu=rank == 0 and world == 1 and not args.no_cpu),
+              "q0_gemm": lambda: bench_q0_gemm(gq, inputs, torch, np, dev, capture, time_graph, bf16_peak)}
         if rank == 0:
             print(json.dumps({"only": args.only, "result": fn[args.only]()}))
         else:
@@ -586,6 +588,7 @@ def run_gpu(args, world, rank):
         extras["q5k"] = leg(bench_q6k, gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=cpu_leg,
                             wtype=gq.Q5_K)
         extras["q4_0_512x1024"] = leg(bench_q4_0, gq, inputs, torch, np, dev, capture, time_graph, cpu=cpu_leg)
+        extras["q0_gemm"] = leg(bench_q0_gemm, gq, inputs, torch, np, dev, capture, time_graph, bf16_peak)
 
     cpu = cpu_configs = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -649,6 +652,9 @@ def summary_keys(line: dict) -> dict:
                                     for b, v in sweep.items()}
         mma_wins = [int(b) for b, v in sweep.items() if v.get("faster") == "mma"]
         out["sweep_crossover_batch"] = min(mma_wins) if mma_wins else None
+    for t in ("q4_0", "q8_0"):
+        out[f"prefill_{t}_tops"] = r(get(line, "q0_gemm", t, "prefill_28672x8192x512", "mma", "tops"), 1)
+        out[f"prefill_{t}_frac"] = r(get(line, "q0_gemm", t, "prefill_28672x8192x512", "mma", "roofline", "frac"))
     out["q6k_frac"] = r(get(line, "q6k", "frac"))
     out["q5k_frac"] = r(get(line, "q5k", "frac"))
     out["q5k_stream_frac"] = r(get(line, "q5k", "streaming", "frac"))
@@ -951,6 +957,54 @@ def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
     del Wq, Xq, Y, wsb
     torch.cuda.empty_cache()
     return {"rows": rows, "cols": cols, "batch": batch, "results": res}
+
+
+def bench_q0_gemm(gq, inputs, torch, np, dev, capture, time_graph, bf16_peak):
+    """Q4_0 / Q8_0 weights x Q8_0 columns on the tensor-core kernel that
+    needs no workspace (what gq_matmul runs from batch 16): the prefill shape
+    28672x8192 x 512 against the GEMV, and 14336x4096 at batch 8..64 (weights
+    rotated over copies larger than L2) against the GEMV."""
+    out = {}
+    big = inputs.gemm_q4_k(0, 28672, 8192, 512)
+    mid = inputs.gemm_q4_k(0, 14336, 4096, 64)
+    for name, wt in (("q4_0", gq.Q4_0), ("q8_0", gq.Q8_0)):
+        rows, cols, batch = 28672, 8192, 512
+        Wq = gq.quantize(wt, torch.from_numpy(big[0]).to(dev))
+        Xq = gq.quantize(gq.Q8_0, torch.from_numpy(big[1]).to(dev))
+        Y = torch.empty(batch, rows, dtype=torch.float32, device=dev)
+        res = {}
+        for pname, path, steps in (("mma", gq.PATH_MMA, 20), ("gemv", gq.PATH_GEMV, 3)):
+            def body():
+                gq.gq_matmul_path(wt, Wq, Xq, Y, rows, cols, batch, path)
+            t, _ = time_graph(capture(body), steps, 2)
+            per = t / steps
+            res[pname] = {"ms": per * 1e3, "tops": 2.0 * rows * cols * batch / per / 1e12}
+        res["mma"]["roofline"] = {"bound": "tensor", "achieved": res["mma"]["tops"], "peak": bf16_peak,
+                                  "unit": "TFLOP/s", "frac": res["mma"]["tops"] / bf16_peak,
+                                  "note": "int ops counted as 2 per multiply-add; fp16 tensor kind"}
+        del Wq, Xq, Y
+        rows, cols = 14336, 4096
+        Wq = gq.quantize(wt, torch.from_numpy(mid[0]).to(dev))
+        copies = max(2, int(np.ceil(300e6 / Wq.numel())))
+        Wc = Wq.reshape(1, -1).repeat(copies, 1)
+        Xq = gq.quantize(gq.Q8_0, torch.from_numpy(mid[1]).to(dev))
+        Y = torch.empty(64, rows, dtype=torch.float32, device=dev)
+        sweep = {}
+        for b in (8, 16, 32, 64):
+            r = {}
+            for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
+                def body():
+                    for i in range(copies):
+                        gq.gq_matmul_path(wt, Wc[i], Xq, Y, rows, cols, b, path)
+                t, _ = time_graph(capture(body), 10, 3)
+                per = t / (10 * copies)
+                r[pname] = {"us": per * 1e6, "weight_gbps": Wq.numel() / per / 1e9}
+            r["faster"] = min(("gemv", "mma"), key=lambda k: r[k]["us"])
+            sweep[str(b)] = r
+        del Wc, Wq, Xq, Y
+        torch.cuda.empty_cache()
+        out[name] = {"prefill_28672x8192x512": res, "sweep_14336x4096": sweep}
+    return out
 
 
 if __name__ == "__main__":

@@ -146,6 +146,13 @@ bool tc_auto(int64_t rows, int64_t batch) {
     return batch >= 16 || (batch >= 9 && rows >= 14336);
 }
 
+// The same choice for Q4_0 / Q8_0 weights (gq_mma_q0.cu).
+bool tc_auto_q0(int64_t rows, int64_t batch) {
+    (void)rows;
+    if (tc_min_batch_env()) return batch >= tc_min_batch_env();
+    return batch >= 16;
+}
+
 // One product call.  act is xq (quantized blocks) or, with fused_f32, fp32
 // activations; exactly one of y / sums is non-null.
 gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
@@ -161,25 +168,34 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         if (path == GQ_PATH_MMA || kstream) return GQ_ERR_TYPE;
         if (cols % 256 != 0) return GQ_ERR_SHAPE;
     }
+    // Q4_0 / Q8_0 weights have a tensor-core kernel of their own that needs
+    // no workspace (gq_mma_q0.cu); Q4_K's packs its activations into one.
+    const bool q0 = wtype == GQ_Q4_0 || wtype == GQ_Q8_0;
     if (path == GQ_PATH_MMA) {
-        if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+        if (!q0 && wtype != GQ_Q4_K) return GQ_ERR_TYPE;
         if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
-        if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
-        if (!ws) return GQ_ERR_NULL;
-        if (ws_bytes < mma_workspace_bytes(rows, cols, batch)) return GQ_ERR_SHAPE;
-        if (!aligned(ws, 16)) return GQ_ERR_ALIGN;
+        if (q0) {
+            if (!mma_q0_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+        } else {
+            if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+            if (!ws) return GQ_ERR_NULL;
+            if (ws_bytes < mma_workspace_bytes(rows, cols, batch)) return GQ_ERR_SHAPE;
+            if (!aligned(ws, 16)) return GQ_ERR_ALIGN;
+        }
     }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
     bool use_mma = path == GQ_PATH_MMA;
     if (path == GQ_PATH_AUTO)
-        use_mma = !fused_f32 && wtype == GQ_Q4_K && tc_auto(rows, batch) &&
-                  mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
-                  ws_bytes >= mma_workspace_bytes(rows, cols, batch);
+        use_mma = !fused_f32 &&
+                  (q0 ? tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch)
+                      : wtype == GQ_Q4_K && tc_auto(rows, batch) && mma_supported(rows, cols, batch) && ws &&
+                            aligned(ws, 16) && ws_bytes >= mma_workspace_bytes(rows, cols, batch));
     if (!use_mma && !kstream && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = use_mma            ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
+    cudaError_t e = use_mma && q0      ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
+                    : use_mma          ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
                     : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, ctx)
                     : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch, ctx)
                                        : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,

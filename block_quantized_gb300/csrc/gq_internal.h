@@ -82,6 +82,11 @@ cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sum
                            int64_t cols, int64_t batch, void *workspace, const LaunchCtx &ctx);
 bool mma_supported(int64_t rows, int64_t cols, int64_t batch);
 size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch);
+// tcgen05 tensor-core family for Q4_0 / Q8_0 weights x Q8_0 activations
+// (gq_mma_q0.cu): no workspace, cols a multiple of 256.
+cudaError_t launch_mma_q0(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
+                          int64_t cols, int64_t batch, const LaunchCtx &ctx);
+bool mma_q0_supported(int64_t rows, int64_t cols, int64_t batch);
 // The library's static scratch (no allocation): its size, and its device
 // address on `device` (looked up on the first call for that device, which
 // must be the current device).

@@ -68,9 +68,12 @@
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
+#include "gq_tc.cuh"
 
 namespace gq {
 namespace {
+
+using namespace tc;
 
 constexpr int TM = 128;   // weight rows per tile (MMA M)
 constexpr int KS = 64;    // K per B operand stage (one 128-byte swizzle atom)
@@ -97,25 +100,11 @@ constexpr uint32_t TMEM_COLS = 512;
 
 // ------------------------------------------------------------ tcgen05 helpers
 
-// Shared-memory matrix descriptor, K-major, 128-byte swizzle: 8-row groups
-// 1024 bytes apart; K advances inside the swizzle atom by moving the start
-// address (32 bytes per 16 fp16).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 // Shared-memory matrix descriptor, K-major, no swizzle: 8x16-byte core
 // matrices, `lbo` bytes apart along K and `sbo` bytes apart along M/N.
 __device__ __forceinline__ uint64_t desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, A/B fp16 (fmt 0) or
-// bf16 (fmt 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, uint32_t fmt) {
-    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Tile-width configuration.  A CTA computes TM weight rows x TN batch
@@ -188,16 +177,7 @@ struct Cfg {
 // Tile width for a batch: the narrowest tile that covers it, 128 beyond 64.
 inline int pick_tn(int64_t batch) { return batch <= 32 ? 32 : (batch <= 64 ? 64 : 128); }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The same with the A operand in tensor memory (lane = row, K along the
+// One MMA with the A operand in tensor memory (lane = row, K along the
 // columns, two fp16 per 32-bit column with the lower K in the low half).
 __device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
                                            uint32_t accumulate) {
@@ -206,25 +186,6 @@ __device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uin
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
         "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
@@ -257,47 +218,6 @@ __device__ __forceinline__ void tmem_ld8x2(uint32_t ta, uint32_t tb, float (&va)
     }
 }
 
-// Bounded wait that also gives up as soon as another role of the CTA set
-// the abort flag.  Returns false (and raises the flag) when it gives up.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort) return false;
-    }
-    *abort = 1u;
-    return false;
-}
-
-// The same for a whole warp: every lane polls, and the warp gives up together
-// if any lane did, so no lane leaves a warp-synchronous section alone.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
-    const bool ok = wait_or_abort(bar, parity, abort);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Super-block visited at step i of a CTA's K loop: every row tile starts at
-// its own super-block (rot), so the CTAs running at the same time read
-// different activation tiles instead of all hitting the same L2 lines.
-__device__ __forceinline__ int kslot(int i, int rot, int nsb) { return i + rot < nsb ? i + rot : i + rot - nsb; }
-
-// Ring position: stage index and the parity of its current use.
-struct RingPos {
-    int n, idx;
-    uint32_t phase;
-    __device__ explicit RingPos(int stages) : n(stages), idx(0), phase(0) {}
-    __device__ void next() {
-        if (++idx == n) {
-            idx = 0;
-            phase ^= 1u;
-        }
-    }
-};
-
-// Byte offset of the 16-byte chunk holding K group g (8 elements) of tile
-// row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t sw128_off(int r, int g) {
-    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((g ^ (r & 7)) << 4));
-}
 // Byte offset of K group g (0 or 1) of tile row r in the no-swizzle min-term
 // tile (core matrices 128 bytes apart along K, 8-row groups 256 bytes apart).
 __device__ __forceinline__ uint32_t plain_off(int r, int g) {
@@ -864,7 +784,7 @@ struct ScratchSlot {
 ScratchSlot g_scratch_slot[NOALLOC_MAX_DEVICES];
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link
-// dependency on the driver library).
+// dependency on the driver library); shared with gq_mma_q0.cu.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;

@@ -132,7 +132,7 @@ enum {
 typedef enum {
     GQ_PATH_AUTO = 0,   /* GEMV below the tensor-core crossover batch, MMA at or above */
     GQ_PATH_GEMV = 1,   /* dp4a GEMV kernels (any batch; batch is processed in chunks) */
-    GQ_PATH_MMA = 2     /* tcgen05 tensor-core kernel (Q4_K weights only) */
+    GQ_PATH_MMA = 2     /* tcgen05 tensor-core kernels (Q4_0, Q8_0, Q4_K weights) */
 } gq_path;
 
 /* Elements per block: 32, 32, 256, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K,
@@ -230,20 +230,28 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  * The integer block sums are exact (int32); y matches the double-precision
  * sum of the same terms within 1e-4 of the sum of their magnitudes.
  * Asynchronous on `stream`; allocates nothing.
- * Dispatch: this call has no workspace, so it always runs the GEMV kernels
- * (any batch; a batch is processed in chunks of up to eight vectors, one
- * pass over W per chunk).  The tensor-core kernel, which is faster from
- * about batch 9-16 on (see gq_matmul_ws), needs a workspace for its
- * repacked activations: call gq_matmul_ws, or gq_matmul_noalloc to use the
- * library's static scratch.
+ * Dispatch (GQ_PATH_AUTO):
+ *   Q4_0 / Q8_0 weights: the tcgen05 tensor-core kernel when cols % 256 == 0
+ *     and batch >= gq_tc_min_batch() (16 unless GQ_TC_MIN_BATCH is set; the
+ *     measured crossover on 14336 x 4096 lies between 8 and 16), the GEMV
+ *     kernels otherwise.  That kernel converts both operands in shared and
+ *     tensor memory and needs no workspace.
+ *   Q4_K weights: the GEMV kernels at every batch.  Q4_K's tensor-core
+ *     kernel, faster from about batch 9-16 on (see gq_matmul_ws), needs a
+ *     workspace for its repacked activations: call gq_matmul_ws, or
+ *     gq_matmul_noalloc to use the library's static scratch.
+ *   Q5_K / Q6_K weights: their GEMV kernels.
+ * The GEMV kernels take any batch, in chunks of up to eight vectors, one
+ * pass over W per chunk.
  */
 gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
                     int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
 
 /* gq_matmul with an explicit kernel family (crossover studies, tests).
- * Without a workspace GQ_PATH_AUTO runs the GEMV kernels, and GQ_PATH_MMA
- * returns GQ_ERR_NULL for Q4_K weights (the tensor-core kernel needs the
- * workspace of gq_matmul_ws) and GQ_ERR_TYPE for the other types. */
+ * GQ_PATH_AUTO dispatches as gq_matmul.  GQ_PATH_MMA runs the tensor-core
+ * kernel of Q4_0 / Q8_0 weights (GQ_ERR_SHAPE unless cols % 256 == 0); for
+ * Q4_K weights it returns GQ_ERR_NULL (that kernel needs the workspace of
+ * gq_matmul_ws), for Q5_K / Q6_K GQ_ERR_TYPE. */
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
                          int64_t rows, int64_t cols, int64_t batch, gq_path path,
                          gq_stream_t stream);
@@ -258,7 +266,8 @@ gq_status gq_matmul_ex(gq_type wtype, const void *W, const void *xq, float *y,
 
 /*
  * Bytes of workspace the tensor-core path needs for this product (0 when the
- * shape or type has no tensor-core path).  The workspace holds the activation
+ * shape or type has no tensor-core path, and for Q4_0 / Q8_0 weights, whose
+ * tensor-core kernel needs none).  The workspace holds the activation
  * operand repacked once per call as fp16 tiles (plus per-block scales, code
  * sums and the min-term operand), per column tile of tn = 32 (batch <= 32),
  * 64 (batch <= 64) or 128 columns and per super-block: ceil(batch / tn) *
@@ -273,7 +282,8 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * GQ_PATH_AUTO runs the tcgen05 tensor-core kernel for Q4_K when batch >=
  * gq_tc_min_batch(), or batch >= 9 on matrices of 14336 rows or more (the
  * measured crossovers), and the workspace suffices; the GEMV kernels
- * otherwise.  With GQ_TC_MIN_BATCH set, batch >= that value alone decides.
+ * otherwise.  Q4_0 / Q8_0 weights ignore the workspace and dispatch as in
+ * gq_matmul.  With GQ_TC_MIN_BATCH set, batch >= that value alone decides.
  * The tensor-core path computes the same y (within the tolerance above) and
  * the same exact integer super-block sums S1 and S2 as the GEMV kernels, for
  * every input (its fp32 accumulation only ever holds integers below 2^24).
@@ -314,7 +324,7 @@ gq_status gq_block_sums(gq_type wtype, const void *W, const void *xq, int32_t *s
                         int64_t rows, int64_t cols, int64_t batch, gq_path path,
                         gq_stream_t stream);
 
-/* gq_block_sums with a workspace (required for GQ_PATH_MMA). */
+/* gq_block_sums with a workspace (required for GQ_PATH_MMA with Q4_K weights). */
 gq_status gq_block_sums_ws(gq_type wtype, const void *W, const void *xq, int32_t *sums,
                            int64_t rows, int64_t cols, int64_t batch, gq_path path,
                            void *workspace, size_t workspace_bytes, gq_stream_t stream);
@@ -401,9 +411,10 @@ gq_status gq_kv_scores(gq_type type, const void *cache, const float *q, float *s
  * the call that timed out and the state of the context are suspect.) */
 gq_status gq_debug_kv_timeout(int on);
 
-/* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernel for
- * Q4_K at any row count (16, the measured crossover for the smaller
- * matrices; from batch 9 it does so on matrices of 14336 rows or more).  The
+/* Batch size at and above which GQ_PATH_AUTO uses the tensor-core kernels:
+ * for Q4_0 / Q8_0 weights, and for Q4_K at any row count (16, the measured
+ * crossover for the smaller matrices; Q4_K from batch 9 on matrices of
+ * 14336 rows or more).  The
  * environment variable GQ_TC_MIN_BATCH, read once, replaces both with a
  * plain threshold, which this then returns. */
 int64_t gq_tc_min_batch(void);

@@ -76,7 +76,12 @@ def test_matmul_validation(lib):
     # path and pairing rules
     g = lib.gq_matmul_path
     assert g(2, A16, A16, A16, 8, 256, 1, 9, None) == TYPE
-    assert g(0, A16, A16, A16, 8, 256, 64, 2, None) == TYPE      # MMA is Q4_K only
+    # tensor-core Q4_0 / Q8_0: cols a multiple of 256, no workspace (accepted,
+    # then no device here)
+    assert g(0, A16, A16, A16, 8, 288, 64, 2, None) == SHAPE
+    assert g(1, A16, A16, A16, 8, 96, 64, 2, None) == SHAPE
+    assert g(0, A16, A16, A16, 8, 256, 64, 2, None) == CUDA
+    assert g(1, A16, A16, A16, 8, 512, 64, 2, None) == CUDA
     assert g(4, A16, A16, A16, 8, 256, 64, 2, None) == TYPE
     assert f(4, A16, A16, A16, 8, 32, 1, None) == SHAPE          # Q6_K needs 256-multiples
     assert f(4, 0, 0, 0, 8, 256, 0, None) == OK
@@ -161,7 +166,8 @@ def test_workspace_rules_on_host(lib):
     assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, 0, need, None) == NULL
     assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, A16, need - 1, None) == SHAPE
     assert m(2, A16, A16, A16, 128, 256, 64, 2, 0, A16 + 8, need, None) == ALIGN
-    assert m(0, A16, A16, A16, 128, 256, 64, 2, 0, A16, need, None) == TYPE
+    assert m(4, A16, A16, A16, 128, 256, 64, 2, 0, A16, need, None) == TYPE  # no tensor-core Q6_K kernel
+    assert m(0, A16, A16, A16, 128, 256, 64, 2, 0, 0, 0, None) == CUDA      # Q4_0 needs no workspace
     assert lib.gq_matmul_path(2, A16, A16, A16, 128, 256, 64, 2, None) == NULL
 
 
