@@ -981,6 +981,7 @@ def bench_q0_gemm(gq, inputs, torch, np, dev, capture, time_graph, bf16_peak):
             res[pname] = {"ms": per * 1e3, "tops": 2.0 * rows * cols * batch / per / 1e12}
         res["mma"]["roofline"] = {"bound": "tensor", "achieved": res["mma"]["tops"], "peak": bf16_peak,
                                   "unit": "TFLOP/s", "frac": res["mma"]["tops"] / bf16_peak,
+                                  "traffic": kernel_traffic("mma_q0_" + name) if name == "q4_0" else None,
                                   "note": "int ops counted as 2 per multiply-add; fp16 tensor kind"}
         del Wq, Xq, Y
         rows, cols = 14336, 4096
