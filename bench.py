@@ -916,7 +916,7 @@ def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
     out = {}
     for b in (1, 2, 4, 8, 16, 32, 64):
         res = {}
-        for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
+        for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA), ("skinny", gq.PATH_SKINNY)):
             def body():
                 for i in range(copies):
                     gq.gq_matmul_ws(gq.Q4_K, Wc[i], Xq, Y, rows, cols, b, path, gq.FLAG_W_STATIC,
@@ -926,7 +926,7 @@ def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
             per = t / (steps * copies)
             res[pname] = {"us": per * 1e6, "weight_gbps": wbytes / per / 1e9,
                           "tops": 2.0 * rows * cols * b / per / 1e12}
-        res["faster"] = min(("gemv", "mma"), key=lambda k: res[k]["us"])
+        res["faster"] = min(("gemv", "mma", "skinny"), key=lambda k: res[k]["us"])
         out[str(b)] = res
     del Wc, Wq, Xq, Y, wsb
     torch.cuda.empty_cache()

@@ -146,6 +146,18 @@ bool tc_auto(int64_t rows, int64_t batch) {
     return batch >= 16 || (batch >= 9 && rows >= 14336);
 }
 
+// GQ_PATH_AUTO's choice of the warp-level tensor-core kernel for Q4_K
+// (gq_skinny.cu).  Measured on 14336 x 4096 (150 CTAs of 96 rows): 13 us at
+// batch 5..8 against the GEMV's 17..23, 13..17 us at 9..16 and 23 us at 32
+// against the tcgen05 kernel's 25.6..26.2, 40 us at 64 against its 30 and the
+// GEMV's 173.  So: batch 5..32 on matrices of 8192 rows or more (enough row
+// tiles to fill the GPU), and up to 64 when no workspace lets the tcgen05
+// kernel run.  Not taken when GQ_TC_MIN_BATCH sets a plain threshold.
+bool skinny_auto(int64_t rows, int64_t batch, bool tc_ready) {
+    if (tc_min_batch_env() || rows < 8192 || batch < 5) return false;
+    return batch <= 32 || (batch <= 64 && !tc_ready);
+}
+
 // The same choice for Q4_0 / Q8_0 weights (gq_mma_q0.cu).
 bool tc_auto_q0(int64_t rows, int64_t batch) {
     (void)rows;
@@ -158,14 +170,15 @@ bool tc_auto_q0(int64_t rows, int64_t batch) {
 gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
                      int64_t rows, int64_t cols, int64_t batch, gq_path path, unsigned flags,
                      bool fused_f32, void *ws, size_t ws_bytes, gq_stream_t stream) {
-    if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_MMA) return GQ_ERR_TYPE;
+    if (path != GQ_PATH_AUTO && path != GQ_PATH_GEMV && path != GQ_PATH_MMA && path != GQ_PATH_SKINNY)
+        return GQ_ERR_TYPE;
     if (flags & ~(unsigned)GQ_FLAG_W_STATIC) return GQ_ERR_TYPE;
     gq_status st = sums ? check_matmul(wtype, W, act, sums, rows, cols, batch, 4)
                         : check_matmul(wtype, W, act, y, rows, cols, batch, 4);
     if (st != GQ_OK) return st;
     const bool kstream = wtype == GQ_Q6_K || wtype == GQ_Q5_K;  // weight types with a GEMV of their own
     if (fused_f32) {
-        if (path == GQ_PATH_MMA || kstream) return GQ_ERR_TYPE;
+        if (path == GQ_PATH_MMA || path == GQ_PATH_SKINNY || kstream) return GQ_ERR_TYPE;
         if (cols % 256 != 0) return GQ_ERR_SHAPE;
     }
     // Q4_0 / Q8_0 weights have a tensor-core kernel of their own that needs
@@ -183,18 +196,30 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
             if (!aligned(ws, 16)) return GQ_ERR_ALIGN;
         }
     }
+    if (path == GQ_PATH_SKINNY) {
+        if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+        if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
+        if (!skinny_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+    }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
     bool use_mma = path == GQ_PATH_MMA;
-    if (path == GQ_PATH_AUTO)
-        use_mma = !fused_f32 &&
-                  (q0 ? tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch)
-                      : wtype == GQ_Q4_K && tc_auto(rows, batch) && mma_supported(rows, cols, batch) && ws &&
-                            aligned(ws, 16) && ws_bytes >= mma_workspace_bytes(rows, cols, batch));
-    if (!use_mma && !kstream && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
+    bool use_skinny = path == GQ_PATH_SKINNY;
+    if (path == GQ_PATH_AUTO && !fused_f32) {
+        if (q0) {
+            use_mma = tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch);
+        } else if (wtype == GQ_Q4_K) {
+            const bool tc_ready = mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
+                                  ws_bytes >= mma_workspace_bytes(rows, cols, batch);
+            use_skinny = skinny_supported(rows, cols, batch) && skinny_auto(rows, batch, tc_ready);
+            use_mma = !use_skinny && tc_ready && tc_auto(rows, batch);
+        }
+    }
+    if (!use_mma && !use_skinny && !kstream && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = use_mma && q0      ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
+    cudaError_t e = use_skinny         ? launch_skinny_q4k(W, act, y, sums, rows, cols, batch, ctx)
+                    : use_mma && q0    ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
                     : use_mma          ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
                     : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, ctx)
                     : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch, ctx)

@@ -19,7 +19,7 @@ import threading
 from . import build as _build
 
 Q4_0, Q8_0, Q4_K, Q8_K, Q6_K, Q5_K = 0, 1, 2, 3, 4, 5
-PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_SKINNY = 0, 1, 2, 3
 FLAG_W_STATIC = 1
 QUANT_ERRMIN = 1
 ACT_TYPE = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_K: Q8_K, Q6_K: Q8_K, Q5_K: Q8_K}

@@ -173,16 +173,24 @@ def test_mma_full_size(rows, cols, batch):
 
 
 @pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
-@pytest.mark.parametrize("rows,batch,want", [(14336, 9, "mma"), (4096, 9, "gemv"), (4096, 16, "mma"),
-                                             (14336, 8, "gemv")])
-def test_auto_dispatch_rule(rows, batch, want):
-    """GQ_PATH_AUTO: the tensor-core kernel from batch 9 on 14336 rows or
-    more, from batch 16 otherwise.  Both kernel families are deterministic, so
-    the AUTO result equals the chosen family's bit for bit."""
+@pytest.mark.parametrize("rows,batch,ws,want", [
+    (14336, 4, True, "gemv"), (14336, 5, True, "skinny"), (14336, 9, True, "skinny"), (14336, 32, True, "skinny"),
+    (14336, 33, True, "mma"), (14336, 33, False, "skinny"), (14336, 65, False, "gemv"), (14336, 65, True, "mma"),
+    (4096, 9, True, "gemv"), (4096, 16, True, "mma"), (4096, 16, False, "gemv")])
+def test_auto_dispatch_rule(rows, batch, ws, want):
+    """GQ_PATH_AUTO for Q4_K: the warp-level tensor-core kernel at batch 5..32
+    on matrices of 8192 rows or more (and up to 64 without a workspace); the
+    tcgen05 kernel, when a workspace is given, from batch 9 on 14336 rows and
+    16 otherwise; the GEMV below.  Every family is deterministic, so the AUTO
+    result equals the chosen family's bit for bit."""
     cols = 1024
     g = inputs.rng(rows + batch)
     Wd = gq.quantize(Q4_K, torch.from_numpy(inputs.normal(g, (rows, cols), 0.02)).cuda())
     Xd = gq.quantize(Q8_K, torch.from_numpy(inputs.normal(g, (batch, cols))).cuda())
-    y_auto = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_AUTO))
-    y_want = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA if want == "mma" else gq.PATH_GEMV))
+    if ws:
+        y_auto = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_AUTO))
+    else:
+        y_auto = host(gq.matmul(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_AUTO))
+    path = {"mma": gq.PATH_MMA, "gemv": gq.PATH_GEMV, "skinny": gq.PATH_SKINNY}[want]
+    y_want = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, path))
     assert y_auto.tobytes() == y_want.tobytes()
