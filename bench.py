@@ -648,10 +648,10 @@ def summary_keys(line: dict) -> dict:
            "prefill_frac": r(get(line, "prefill", "results", "mma", "roofline", "frac"))}
     sweep = get(line, "batch_sweep", "results")
     if isinstance(sweep, dict):
-        out["sweep_us_gemv_mma"] = {b: [r(get(v, "gemv", "us"), 1), r(get(v, "mma", "us"), 1)]
-                                    for b, v in sweep.items()}
-        mma_wins = [int(b) for b, v in sweep.items() if v.get("faster") == "mma"]
-        out["sweep_crossover_batch"] = min(mma_wins) if mma_wins else None
+        out["sweep_us_gemv_mma_skinny"] = {b: [r(get(v, "gemv", "us"), 1), r(get(v, "mma", "us"), 1),
+                                               r(get(v, "skinny", "us"), 1)] for b, v in sweep.items()}
+        tc_wins = [int(b) for b, v in sweep.items() if v.get("faster") in ("mma", "skinny")]
+        out["sweep_crossover_batch"] = min(tc_wins) if tc_wins else None
     for t in ("q4_0", "q8_0"):
         out[f"prefill_{t}_tops"] = r(get(line, "q0_gemm", t, "prefill_28672x8192x512", "mma", "tops"), 1)
         out[f"prefill_{t}_frac"] = r(get(line, "q0_gemm", t, "prefill_28672x8192x512", "mma", "roofline", "frac"))
@@ -901,9 +901,9 @@ def bench_decode(gq, inputs, torch, np, dev, s, capture, time_graph, world):
 
 
 def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
-    """Q4_K 14336x4096 at batch 1..64 through both kernel families (weights
-    rotated over 8 copies, 264 MB > L2); the tensor path includes its
-    activation pack kernel."""
+    """Q4_K 14336x4096 at batch 1..64 through the three kernel families: the
+    GEMV, the tcgen05 kernel (its activation pack kernel included) and the
+    warp-level tensor-core kernel (weights rotated over 8 copies, 264 MB > L2)."""
     rows, cols, copies = 14336, 4096, 8
     W, X = inputs.gemm_q4_k(0, rows, cols, 64)
     Wq = gq.quantize(gq.Q4_K, torch.from_numpy(W).to(dev))
@@ -926,6 +926,8 @@ def bench_batch_sweep(gq, inputs, torch, np, dev, s, capture, time_graph):
             per = t / (steps * copies)
             res[pname] = {"us": per * 1e6, "weight_gbps": wbytes / per / 1e9,
                           "tops": 2.0 * rows * cols * b / per / 1e12}
+            if pname == "skinny" and b == 16:
+                res[pname]["traffic"] = kernel_traffic("skinny_q4k_b16")
         res["faster"] = min(("gemv", "mma", "skinny"), key=lambda k: res[k]["us"])
         out[str(b)] = res
     del Wc, Wq, Xq, Y, wsb
