@@ -952,6 +952,11 @@ def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
         per = t / steps
         tops = 2.0 * rows * cols * batch / per / 1e12
         res[pname] = {"ms": per * 1e3, "tops": tops}
+    # gq_matmul itself (no workspace): the warp-level kernel over 64-column chunks
+    def body_nows():
+        gq.gq_matmul(gq.Q4_K, Wq, Xq, Y, rows, cols, batch)
+    t, _ = time_graph(capture(body_nows), 5, 2)
+    res["gq_matmul_no_workspace"] = {"ms": t / 5 * 1e3, "tops": 2.0 * rows * cols * batch / (t / 5) / 1e12}
     res["mma"]["roofline"] = {"bound": "tensor", "achieved": res["mma"]["tops"], "peak": bf16_peak,
                               "unit": "TFLOP/s", "frac": res["mma"]["tops"] / bf16_peak,
                               "traffic": kernel_traffic("mma_q4k"),

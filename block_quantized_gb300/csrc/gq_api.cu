@@ -2,6 +2,7 @@
 // per-device launch context, kernel-family dispatch and error reporting.
 // Nothing here allocates device memory ("llama.cpp：一个人、一个周末…",
 // 内存管理：推理时零分配: all buffers exist before the inference loop).
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -155,7 +156,7 @@ bool tc_auto(int64_t rows, int64_t batch) {
 // kernel run.  Not taken when GQ_TC_MIN_BATCH sets a plain threshold.
 bool skinny_auto(int64_t rows, int64_t batch, bool tc_ready) {
     if (tc_min_batch_env() || rows < 8192 || batch < 5) return false;
-    return batch <= 32 || (batch <= 64 && !tc_ready);
+    return batch <= 32 || !tc_ready;
 }
 
 // The same choice for Q4_0 / Q8_0 weights (gq_mma_q0.cu).
@@ -199,7 +200,7 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     if (path == GQ_PATH_SKINNY) {
         if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
         if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
-        if (!skinny_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
+        if (!skinny_supported(rows, cols, std::min<int64_t>(batch, 64))) return GQ_ERR_SHAPE;
     }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
     bool use_mma = path == GQ_PATH_MMA;
@@ -210,7 +211,9 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         } else if (wtype == GQ_Q4_K) {
             const bool tc_ready = mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
-            use_skinny = skinny_supported(rows, cols, batch) && skinny_auto(rows, batch, tc_ready);
+            // beyond batch 64 the warp-level kernel runs over 64-column chunks
+            use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) &&
+                         skinny_auto(rows, batch, tc_ready);
             use_mma = !use_skinny && tc_ready && tc_auto(rows, batch);
         }
     }
@@ -218,8 +221,20 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
-    cudaError_t e = use_skinny         ? launch_skinny_q4k(W, act, y, sums, rows, cols, batch, ctx)
-                    : use_mma && q0    ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
+    if (use_skinny) {
+        // chunks of up to 64 activation vectors, one launch each (y, sums and
+        // xq advance by whole vectors)
+        const int64_t nsb = cols / 256;
+        for (int64_t b0 = 0; b0 < batch; b0 += 64) {
+            const int64_t nb = std::min<int64_t>(64, batch - b0);
+            cudaError_t e = launch_skinny_q4k(W, static_cast<const uint8_t *>(act) + b0 * nsb * 276,
+                                              y ? y + b0 * rows : nullptr, sums ? sums + b0 * rows * nsb * 2 : nullptr,
+                                              rows, cols, nb, ctx);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        return GQ_OK;
+    }
+    cudaError_t e = use_mma && q0      ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
                     : use_mma          ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
                     : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, ctx)
                     : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch, ctx)

@@ -133,7 +133,7 @@ typedef enum {
     GQ_PATH_AUTO = 0,   /* GEMV below the tensor-core crossover batch, MMA at or above */
     GQ_PATH_GEMV = 1,   /* dp4a GEMV kernels (any batch; batch is processed in chunks) */
     GQ_PATH_MMA = 2,    /* tcgen05 tensor-core kernels (Q4_0, Q8_0, Q4_K weights) */
-    GQ_PATH_SKINNY = 3  /* warp-level tensor-core kernel (mma.sync) for Q4_K at batch <= 64 */
+    GQ_PATH_SKINNY = 3  /* warp-level tensor-core kernel (mma.sync) for Q4_K, 64 columns per launch */
 } gq_path;
 
 /* Elements per block: 32, 32, 256, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K,
@@ -238,8 +238,8 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *     kernels otherwise.  That kernel converts both operands in shared and
  *     tensor memory and needs no workspace.
  *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
- *     workspace) for batch 5..64 on matrices of 8192 rows or more, the GEMV
- *     kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
+ *     workspace; batches beyond 64 as 64-column chunks) from batch 5 on
+ *     matrices of 8192 rows or more, the GEMV kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
  *     such matrices and from batch 16 on smaller ones (see gq_matmul_ws),
  *     needs a workspace for its repacked activations: call gq_matmul_ws, or
  *     gq_matmul_noalloc to use the library's static scratch.
@@ -256,9 +256,9 @@ gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
  * Q4_K weights it returns GQ_ERR_NULL (that kernel needs the workspace of
  * gq_matmul_ws), for Q5_K / Q6_K GQ_ERR_TYPE.  GQ_PATH_SKINNY runs the
  * warp-level tensor-core kernel of Q4_K weights (mma.sync m16n8k16 on the
- * same exact integer operands as the tcgen05 kernel; batch <= 64 and cols %
- * 256 == 0, GQ_ERR_SHAPE otherwise; GQ_ERR_TYPE for the other weight types
- * and for fp32 activations). */
+ * same exact integer operands as the tcgen05 kernel; one launch per 64
+ * activation vectors; cols % 256 == 0, GQ_ERR_SHAPE otherwise; GQ_ERR_TYPE
+ * for the other weight types and for fp32 activations). */
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
                          int64_t rows, int64_t cols, int64_t batch, gq_path path,
                          gq_stream_t stream);
@@ -290,8 +290,8 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * 5..32 on matrices of 8192 rows or more; else the tcgen05 tensor-core
  * kernel when batch >= gq_tc_min_batch(), or batch >= 9 on matrices of
  * 14336 rows or more (the measured crossovers), and the workspace suffices;
- * else the warp-level kernel up to batch 64 on such matrices; else the GEMV
- * kernels.  Q4_0 / Q8_0 weights ignore the workspace and dispatch as in
+ * else the warp-level kernel (in 64-column chunks beyond batch 64) on such
+ * matrices; else the GEMV kernels.  Q4_0 / Q8_0 weights ignore the workspace and dispatch as in
  * gq_matmul.  With GQ_TC_MIN_BATCH set, batch >= that value alone decides.
  * The tensor-core path computes the same y (within the tolerance above) and
  * the same exact integer super-block sums S1 and S2 as the GEMV kernels, for

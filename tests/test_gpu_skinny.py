@@ -96,16 +96,28 @@ def test_skinny_sums_beyond_fp32_integers(batch):
     assert_close(y, y_ref, T)
 
 
+@pytest.mark.parametrize("batch", [65, 130, 200])
+def test_skinny_batches_beyond_one_tile(batch):
+    """Batches beyond 64 run as 64-column chunks (one launch each): sums and
+    y still match the oracle, the last chunk ragged."""
+    rows, cols = 200, 768
+    g = inputs.rng(31 + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q4_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = dev(Wq), dev(Xq)
+    np.testing.assert_array_equal(host(gq.block_sums(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY)),
+                                  orc.block_sums(Q4_K, Wq, Xq, rows, cols, batch))
+    y = host(gq.matmul(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY))
+    y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+
+
 def test_skinny_shape_rules():
-    """batch <= 64 and Q4_K weights only; AUTO and GEMV results agree with it
-    within the tolerance."""
+    """Q4_K weights and cols a multiple of 256 only."""
     rows, cols = 128, 512
     g = inputs.rng(31)
-    Wd = gq.quantize(Q4_K, dev(inputs.normal(g, (rows, cols), 0.02)))
-    Xd = gq.quantize(Q8_K, dev(inputs.normal(g, (65, cols))))
     y = torch.empty(65, rows, device="cuda")
-    with pytest.raises(gq.GQError):
-        gq.gq_matmul_path(Q4_K, Wd, Xd, y, rows, cols, 65, gq.PATH_SKINNY)
     Wq0 = gq.quantize(0, dev(inputs.normal(g, (rows, cols), 0.02)))
     Xq0 = gq.quantize(1, dev(inputs.normal(g, (8, cols))))
     with pytest.raises(gq.GQError):
@@ -117,10 +129,11 @@ def sampled_rows(rows, k, seed):
     return np.unique(np.concatenate([[0, rows - 1], g.choice(rows, size=min(k, rows), replace=False)]))
 
 
-@pytest.mark.parametrize("batch", [2, 8, 16, 32, 64])
-def test_skinny_full_size(batch):
-    """The 14336 x 4096 batch-sweep shape; the oracle recomputes sampled rows."""
-    rows, cols = 14336, 4096
+@pytest.mark.parametrize("rows,cols,batch", [(14336, 4096, 2), (14336, 4096, 8), (14336, 4096, 16),
+                                             (14336, 4096, 32), (14336, 4096, 64), (28672, 8192, 512)])
+def test_skinny_full_size(rows, cols, batch):
+    """The batch-sweep shape and the prefill shape (eight 64-column chunks);
+    the oracle recomputes sampled rows."""
     W, X = inputs.gemm_q4_k(0, rows, cols, batch)
     Wd = gq.quantize(Q4_K, dev(W))
     Xd = gq.quantize(Q8_K, dev(X))
