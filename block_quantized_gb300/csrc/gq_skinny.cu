@@ -1,14 +1,15 @@
-// gq_skinny.cu -- Q4_K x Q8_K for small batches (2..64 activation vectors):
-// the per-super-block product of "llama.cpp 推理引擎" §5.5 on warp-level
-// tensor-core MMAs (mma.sync m16n8k16, fp16 operands, fp32 accumulate).
+// gq_skinny.cu -- Q4_K x Q8_K for small batches (up to 64 activation vectors
+// per launch): the per-super-block product of "llama.cpp 推理引擎" §5.5 on
+// warp-level tensor-core MMAs (mma.sync m16n8k16, fp16 operands, fp32
+// accumulate).
 //
 // Between the GEMV (one pass over W per eight vectors, its dp4a work growing
 // with every vector) and the tcgen05 kernel (a CTA-wide pipeline whose
 // per-super-block handshakes cost more than the MMAs at these widths) lies a
 // band where the product is a skinny contraction bound by the weight stream.
-// Here every warp owns 16 weight rows and does its own work: it turns the
-// rows' nibbles into MMA A fragments in registers and issues the MMAs itself;
-// the only CTA-wide steps are one barrier per chunk of activations.
+// Here every compute warp owns 16 weight rows and does its own work: it turns
+// the rows' nibbles into MMA A fragments in registers and issues the MMAs
+// itself, with no hand-off to another role per super-block.
 //
 // Exactness (the integer sums of the tcgen05 kernel, same argument):
 //   A = sc_j * q - 512 in [-512, 433], B = a in [-128, 127] (fp16, exact);
@@ -24,12 +25,17 @@
 // nibble word unpacks with the 0x6400 trick -- so lane (g, t) of the
 // fragment takes elements 32 j + 8 t + 0..7 of its rows and columns.
 //
-// CTA: 6 compute warps (96 weight rows) + 1 producer warp.  The producer
-// streams one 2-D TMA tile per super-block (144 bytes x 96 rows; rows past
-// the matrix read as zeros) through a ring; the compute warps convert the
-// activations two super-blocks at a time into fp16 B fragments in shared
-// memory (double-buffered), then consume the ring.  Every mbarrier wait is
-// bounded and reports through the device status word.
+// CTA (96 weight rows, 8 NT activation columns):
+//   compute warps  KS groups of six (KS = 2 up to 32 columns, else 1); group
+//                  g takes the super-blocks sb = g (mod KS) of the 96 rows,
+//                  and the groups' partial y are added in group order at the
+//                  end (the int32 block sums are per super-block, exact);
+//   producer warp  one 2-D TMA tile per super-block (144 bytes x 96 rows;
+//                  rows past the matrix read as zeros) through a ring of NS;
+//   converter warps (four) turn the Q8_K activation blocks, KC super-blocks
+//                  at a time, into fp16 B fragments, min-term fragments and
+//                  column scales in shared memory (two chunk buffers).
+// Every mbarrier wait is bounded and reports through the device status word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
