@@ -236,8 +236,10 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     }
     cudaError_t e = use_mma && q0      ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
                     : use_mma          ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
-                    : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, ctx)
-                    : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch, ctx)
+                    : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch,
+                                                         (flags & GQ_FLAG_W_STATIC) != 0, ctx)
+                    : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch,
+                                                         (flags & GQ_FLAG_W_STATIC) != 0, ctx)
                                        : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
                                                      (flags & GQ_FLAG_W_STATIC) != 0, ctx);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__r
                                                              const uint8_t *__restrict__ xq,
                                                              float *__restrict__ y, int32_t *__restrict__ sums,
                                                              int rows, int nblk, int ns, int stage_bytes,
-                                                             uint32_t *__restrict__ status) {
+                                                             int w_static, uint32_t *__restrict__ status) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.y;
@@ -239,10 +239,14 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__r
     if (lane == 0 && total > 0) {
         for (int s = 0; s < ns; ++s) mbar_init(bar + s, 1);
         fence_mbar_init();
+        // weights no kernel in flight writes (GQ_FLAG_W_STATIC): the first
+        // ring stages are requested before the dependency wait
+        if (w_static)
+            for (int i = 0; i < ns && i < total; ++i) issue(i, i);
     }
     __syncwarp();
-    pdl_wait();  // W and xq may come from the preceding kernel in the stream
-    if (lane == 0)
+    pdl_wait();  // xq (and, unless static, W) may come from the preceding kernel in the stream
+    if (lane == 0 && !w_static)
         for (int i = 0; i < ns && i < total; ++i) issue(i, i);
     stage_q8_k_vec(act, xq + (size_t)b * nblk * Q8_K_BYTES, nblk);
     __syncthreads();
@@ -368,13 +372,13 @@ int pick_ns(int nw, int nblk) {
 
 template <bool SUMS, int NW>
 cudaError_t launch_stream(const uint8_t *W, const uint8_t *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
-                          int nb, int ns, const LaunchCtx &ctx) {
+                          int nb, int ns, int w_static, const LaunchCtx &ctx) {
     auto k = gemv_q6k_kernel<SUMS, NW>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
     return launch_pdl(k, dim3((unsigned)gx, nb), dim3(NW * 32), stream_smem(NW, ns, nblk), ctx.stream, W, xb,
-                      yb, sb, (int)rows, nblk, ns, nblk * Q6_K_BYTES + 16, ctx.status);
+                      yb, sb, (int)rows, nblk, ns, nblk * Q6_K_BYTES + 16, w_static, ctx.status);
 }
 
 int codec_grid(int64_t items, int per_cta, int num_sms) {
@@ -385,7 +389,7 @@ int codec_grid(int64_t items, int per_cta, int num_sms) {
 
 template <bool SUMS>
 cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                     int64_t batch, const LaunchCtx &ctx) {
+                     int64_t batch, int w_static, const LaunchCtx &ctx) {
     const int nblk = (int)(cols / QK_K);
     // the widest instantiation whose rings fit: GQ_Q6K_MAX_WARPS, 16 or 8 warps
     int nw = GQ_Q6K_MAX_WARPS, ns = pick_ns(nw, nblk);
@@ -398,11 +402,11 @@ cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sum
         int32_t *sb = SUMS ? sums + b0 * rows * nblk : nullptr;
         cudaError_t e;
         if (ns && nw == GQ_Q6K_MAX_WARPS) {
-            e = launch_stream<SUMS, GQ_Q6K_MAX_WARPS>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+            e = launch_stream<SUMS, GQ_Q6K_MAX_WARPS>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else if (ns && nw == 16) {
-            e = launch_stream<SUMS, 16>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+            e = launch_stream<SUMS, 16>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else if (ns) {
-            e = launch_stream<SUMS, 8>(W, xb, yb, sb, rows, nblk, nb, ns, ctx);
+            e = launch_stream<SUMS, 8>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else {
             const int64_t gx = (rows + PW - 1) / PW;
             e = launch_pdl(gemv_q6k_plain_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(PW * 32), 0, ctx.stream, W,
@@ -427,11 +431,11 @@ cudaError_t launch_dequantize_q6k(const void *src, float *dst, int64_t n, const 
 }
 
 cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                            int64_t batch, const LaunchCtx &ctx) {
+                            int64_t batch, bool w_static, const LaunchCtx &ctx) {
     const uint8_t *w8 = static_cast<const uint8_t *>(W);
     const uint8_t *x8 = static_cast<const uint8_t *>(xq);
-    return sums ? run_gemv<true>(w8, x8, y, sums, rows, cols, batch, ctx)
-                : run_gemv<false>(w8, x8, y, sums, rows, cols, batch, ctx);
+    return sums ? run_gemv<true>(w8, x8, y, sums, rows, cols, batch, w_static ? 1 : 0, ctx)
+                : run_gemv<false>(w8, x8, y, sums, rows, cols, batch, w_static ? 1 : 0, ctx);
 }
 
 }  // namespace gq

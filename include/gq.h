@@ -123,8 +123,8 @@ enum {
      * request their first weight chunks before waiting for the preceding
      * kernel in the stream to finish, overlapping the weight fetch with that
      * kernel's tail.  Without the flag every read of W happens after that
-     * wait.  Accepted with Q5_K and Q6_K weights, where it has no effect
-     * (those GEMVs read W only after the wait). */
+     * wait.  The Q4_0 / Q8_0 / Q4_K, Q5_K and Q6_K GEMV kernels act on it;
+     * the tensor-core kernels read W after the wait in any case. */
     GQ_FLAG_W_STATIC = 1u
 };
 

@@ -170,3 +170,21 @@ def test_gemv_4096_outlier_weights():
     assert host(Wd).tobytes() == Wq.tobytes()
     y_ref, T = orc.matmul_ref(Q5_K, Wq, xq, 4096, 4096, 1, nthreads=orc.max_threads())
     assert_close(host(gq.matmul(Q5_K, Wd, dev(xq), 4096, 4096, 1)), y_ref, T)
+
+
+def test_static_weights_flag_same_result():
+    """GQ_FLAG_W_STATIC only moves the first weight copies before the
+    dependency wait: a chain of products gives the same bytes with and
+    without it."""
+    rows, cols, n = 1000, 2048, 6
+    g = inputs.rng(77)
+    Ws = [gq.quantize(Q5_K, torch.from_numpy(inputs.normal(g, (rows, cols), 0.02)).cuda()) for _ in range(n)]
+    X = gq.quantize(Q8_K, torch.from_numpy(inputs.normal(g, (n, cols))).cuda())
+    ya = torch.empty(n, rows, device="cuda")
+    yb = torch.empty(n, rows, device="cuda")
+    for i in range(n):
+        gq.gq_matmul_ex(Q5_K, Ws[i], X[i], ya[i], rows, cols, 1, gq.PATH_AUTO, gq.FLAG_W_STATIC)
+    for i in range(n):
+        gq.gq_matmul(Q5_K, Ws[i], X[i], yb[i], rows, cols, 1)
+    torch.cuda.synchronize()
+    assert ya.cpu().numpy().tobytes() == yb.cpu().numpy().tobytes()
