@@ -149,13 +149,14 @@ bool tc_auto(int64_t rows, int64_t batch) {
 
 // GQ_PATH_AUTO's choice of the warp-level tensor-core kernel for Q4_K
 // (gq_skinny.cu).  Measured on 14336 x 4096 (150 CTAs of 96 rows): 13 us at
-// batch 5..8 against the GEMV's 17..23, 13..17 us at 9..16 and 23 us at 32
-// against the tcgen05 kernel's 25.6..26.2, 40 us at 64 against its 30 and the
-// GEMV's 173.  So: batch 5..32 on matrices of 8192 rows or more (enough row
-// tiles to fill the GPU), and up to 64 when no workspace lets the tcgen05
-// kernel run.  Not taken when GQ_TC_MIN_BATCH sets a plain threshold.
+// batch 4..8 against the GEMV's 14..23 (the GEMV wins below, 9.4 us at
+// batch 2), 13..17 us at 9..16 and 23 us at 32 against the tcgen05 kernel's
+// 25.3..26.2, 40 us at 64 against its 30 and the GEMV's 173.  So: batch 4..32
+// on matrices of 8192 rows or more (enough row tiles to fill the GPU), and
+// every batch from 4 when no workspace lets the tcgen05 kernel run.  Not taken
+// when GQ_TC_MIN_BATCH sets a plain threshold.
 bool skinny_auto(int64_t rows, int64_t batch, bool tc_ready) {
-    if (tc_min_batch_env() || rows < 8192 || batch < 5) return false;
+    if (tc_min_batch_env() || rows < 8192 || batch < 4) return false;
     return batch <= 32 || !tc_ready;
 }
 

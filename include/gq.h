@@ -238,7 +238,7 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *     kernels otherwise.  That kernel converts both operands in shared and
  *     tensor memory and needs no workspace.
  *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
- *     workspace; batches beyond 64 as 64-column chunks) from batch 5 on
+ *     workspace; batches beyond 64 as 64-column chunks) from batch 4 on
  *     matrices of 8192 rows or more, the GEMV kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
  *     such matrices and from batch 16 on smaller ones (see gq_matmul_ws),
  *     needs a workspace for its repacked activations: call gq_matmul_ws, or
@@ -287,7 +287,7 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * least gq_matmul_workspace_bytes bytes, owned by the caller, contents
  * overwritten; calls that share a workspace must not overlap on the GPU).
  * GQ_PATH_AUTO for Q4_K: the warp-level kernel (GQ_PATH_SKINNY) at batch
- * 5..32 on matrices of 8192 rows or more; else the tcgen05 tensor-core
+ * 4..32 on matrices of 8192 rows or more; else the tcgen05 tensor-core
  * kernel when batch >= gq_tc_min_batch(), or batch >= 9 on matrices of
  * 14336 rows or more (the measured crossovers), and the workspace suffices;
  * else the warp-level kernel (in 64-column chunks beyond batch 64) on such

@@ -174,12 +174,12 @@ def test_mma_full_size(rows, cols, batch):
 
 @pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
 @pytest.mark.parametrize("rows,batch,ws,want", [
-    (14336, 4, True, "gemv"), (14336, 5, True, "skinny"), (14336, 9, True, "skinny"), (14336, 32, True, "skinny"),
+    (14336, 3, True, "gemv"), (14336, 4, True, "skinny"), (14336, 9, True, "skinny"), (14336, 32, True, "skinny"),
     (14336, 33, True, "mma"), (14336, 33, False, "skinny"), (14336, 65, False, "skinny"), (14336, 65, True, "mma"),
     (4096, 9, True, "gemv"), (4096, 16, True, "mma"), (4096, 16, False, "gemv")])
 def test_auto_dispatch_rule(rows, batch, ws, want):
-    """GQ_PATH_AUTO for Q4_K: the warp-level tensor-core kernel at batch 5..32
-    on matrices of 8192 rows or more (at any batch from 5 without a
+    """GQ_PATH_AUTO for Q4_K: the warp-level tensor-core kernel at batch 4..32
+    on matrices of 8192 rows or more (at any batch from 4 without a
     workspace, in 64-column chunks); the
     tcgen05 kernel, when a workspace is given, from batch 9 on 14336 rows and
     16 otherwise; the GEMV below.  Every family is deterministic, so the AUTO
