@@ -721,8 +721,9 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
     """Q6_K (or, with wtype, Q5_K) x Q8_K GEMV on the 4096x4096 row-spread +
     outlier weights: 64 distinct copies (203 / 185 MB, larger than L2) as
     dependent back-to-back launches on pre-quantized activations (weights
-    marked static, as the headline's; also without the flag), and the same
-    bytes as one tall launch (262144 x 4096 rows)."""
+    marked static, as the headline's; also without the flag, and from fp32
+    activations quantized inside the kernel), and the same bytes as one tall
+    launch (262144 x 4096 rows)."""
     wt = gq.Q6_K if wtype is None else wtype
     name = "Q6_K" if wt == gq.Q6_K else "Q5_K"
     W, _ = inputs.gemv_q4_k(0)
@@ -744,12 +745,18 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
         for i in range(COPIES):
             gq.gq_matmul(wt, Wall[i], XQ[i], Y[i], GEMV_ROWS, GEMV_COLS, 1)
 
+    def chain_fused():
+        # fp32 activations quantized to Q8_K inside the GEMV (no separate pass)
+        for i in range(COPIES):
+            gq.gq_matmul_f32(wt, Wall[i], X[i], Y[i], GEMV_ROWS, GEMV_COLS, 1, gq.FLAG_W_STATIC)
+
     def tall():
         gq.gq_matmul(wt, Wall, XQ[0], Yt, GEMV_ROWS * COPIES, GEMV_COLS, 1)
 
     k = 200
     t_c, _ = time_graph(capture(chain), k, 5)
     t_p, _ = time_graph(capture(chain_plain), k, 5)
+    t_f, _ = time_graph(capture(chain_fused), k, 5)
     t_t, _ = time_graph(capture(tall), 50, 3)
     if not (torch.isfinite(Y).all() and torch.isfinite(Yt).all()):
         raise RuntimeError(f"non-finite {name} GEMV output")
@@ -766,6 +773,9 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
             "launch_us": per * 1e6, "alg_bytes_per_launch": alg, "weight_gbps": w_bytes / per / 1e9,
             "achieved": alg / per / 1e9, "frac": alg / per / 1e9 / hbm_peak,
             "launch_us_without_w_static": t_p / (k * COPIES) * 1e6,
+            "fused_f32": {"launch_us": t_f / (k * COPIES) * 1e6,
+                          "frac": (w_bytes + GEMV_COLS * 4 + GEMV_ROWS * 4) / (t_f / (k * COPIES)) / 1e9
+                          / hbm_peak},
             "streaming": {"workload": f"one launch over 262144 x 4096 {name} rows "
                                       f"({COPIES * w_bytes / 1e6:.0f} MB)",
                           "us": tall_s * 1e6, "weight_gbps": COPIES * w_bytes / tall_s / 1e9,

@@ -180,8 +180,12 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     if (st != GQ_OK) return st;
     const bool kstream = wtype == GQ_Q6_K || wtype == GQ_Q5_K;  // weight types with a GEMV of their own
     if (fused_f32) {
-        if (path == GQ_PATH_MMA || path == GQ_PATH_SKINNY || kstream) return GQ_ERR_TYPE;
+        if (path == GQ_PATH_MMA || path == GQ_PATH_SKINNY) return GQ_ERR_TYPE;
         if (cols % 256 != 0) return GQ_ERR_SHAPE;
+        // Q5_K / Q6_K quantize the activations into the streaming kernel's
+        // shared memory; there is no fused form of their long-vector kernel
+        if (wtype == GQ_Q6_K && !gemv_q6k_fused_fits(cols)) return GQ_ERR_SHAPE;
+        if (wtype == GQ_Q5_K && !gemv_q5k_fused_fits(cols)) return GQ_ERR_SHAPE;
     }
     // Q4_0 / Q8_0 weights have a tensor-core kernel of their own that needs
     // no workspace (gq_mma_q0.cu); Q4_K's packs its activations into one.
@@ -237,9 +241,9 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     }
     cudaError_t e = use_mma && q0      ? launch_mma_q0(wtype, W, act, y, sums, rows, cols, batch, ctx)
                     : use_mma          ? launch_mma_q4k(W, act, y, sums, rows, cols, batch, ws, ctx)
-                    : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch,
+                    : wtype == GQ_Q6_K ? launch_gemv_q6k(W, act, y, sums, rows, cols, batch, fused_f32,
                                                          (flags & GQ_FLAG_W_STATIC) != 0, ctx)
-                    : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch,
+                    : wtype == GQ_Q5_K ? launch_gemv_q5k(W, act, y, sums, rows, cols, batch, fused_f32,
                                                          (flags & GQ_FLAG_W_STATIC) != 0, ctx)
                                        : launch_gemv(wtype, W, act, y, sums, rows, cols, batch, fused_f32,
                                                      (flags & GQ_FLAG_W_STATIC) != 0, ctx);

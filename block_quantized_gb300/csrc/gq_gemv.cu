@@ -37,9 +37,12 @@
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
+#include "gq_quant8.cuh"
 
 namespace gq {
 namespace {
+
+using namespace q8;
 
 constexpr uint32_t NIB = 0x0F0F0F0Fu;
 constexpr unsigned FULL = 0xffffffffu;
@@ -235,73 +238,6 @@ __device__ void stage_q8_0(const Act &a, const uint8_t *__restrict__ xq, int nbl
 // the Q8_0 scale), so the codes equal theirs bit for bit.
 
 
-__device__ __forceinline__ float clamp127(float v) {
-    return v < -127.0f ? -127.0f : (v > 127.0f ? 127.0f : v);
-}
-
-// Code of x in a block with scale d != 0 and r = RN(1/d): roundf of the
-// IEEE quotient x / d, clamped to [-127, 127].  For |x / d| <= 128 the
-// product p = RN(x * r) lies within 2^-16 of x / d and RN(x / d) within
-// 2^-17, so the two round alike under roundf unless p is within 2^-15 of a
-// half-integer; p's distance is tested against 2^-14 and the near cases
-// (and a non-finite r, which makes the test fail through a NaN) take the
-// IEEE division.  Away from a half-integer, roundf(|p|) = floor(|p|) + (frac
-// > 1/2) exactly.
-__device__ __forceinline__ float q8_code(float x, float d, float r) {
-    const float p = __fmul_rn(x, r);
-    const float a = fabsf(p);
-    const float fl = floorf(a);
-    const float f = a - fl;
-    float q;
-    if (fabsf(f - 0.5f) > 0x1p-14f)
-        q = copysignf(fl + (f > 0.5f ? 1.0f : 0.0f), p);
-    else
-        q = roundf(__fdiv_rn(x, d));
-    return clamp127(q);
-}
-
-// Codes of eight elements of a block with scale d and r = RN(1/d), packed as
-// signed bytes (lowest element in the lowest byte), each equal to
-// q8_code(e[i], d, r), and zero when d == 0.  Away from a half-integer the
-// product p = RN(e * r) rounds the same to nearest-even (rintf) as half away
-// from zero, and |p - rintf(p)| is exact, so the fast path tests the same
-// 2^-14 window as q8_code and falls back to it for the whole group when any
-// element lies in the window (or r is not finite, which makes the test fail).
-// Every |e| <= 127 d up to the rounding of d (at most 2^-11 relative, for an
-// fp16 scale), so |p| < 127.5 and the fast codes need no clamp.
-__device__ __forceinline__ void q8_codes8(const float (&e)[8], float d, float r, uint32_t &w0,
-                                          uint32_t &w1) {
-    int q[8];
-    bool slow = false;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float p = __fmul_rn(e[i], r);
-        const float t = rintf(p);
-        slow |= !(fabsf(fabsf(p - t) - 0.5f) > 0x1p-14f);
-        q[i] = (int)t;
-    }
-    if (d == 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = 0;
-    } else if (slow) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = (int)q8_code(e[i], d, r);
-    }
-    w0 = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
-    w1 = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
-}
-
-__device__ __forceinline__ void unpack8(const float4 (&v)[2], float (&e)[8]) {
-    e[0] = v[0].x; e[1] = v[0].y; e[2] = v[0].z; e[3] = v[0].w;
-    e[4] = v[1].x; e[5] = v[1].y; e[6] = v[1].z; e[7] = v[1].w;
-}
-
-__device__ __forceinline__ float absmax8(const float (&e)[8]) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(e[i]));
-    return m;
-}
 
 // Q8_K: one warp per 256-element block, lane l owns elements 8l..8l+7
 // (= code group l of the layout).

@@ -64,18 +64,23 @@ bool gemv_fits(gq_type wtype, int64_t cols);
 
 // Q6_K weights (gq_q6k.cu): codecs, and the Q6_K x Q8_K GEMV (any batch,
 // one pass over W per activation vector; sums != nullptr selects the int32
-// block sums, one per 256-element block, instead of y; w_static as for
-// launch_gemv).
+// block sums, one per 256-element block, instead of y; fused_f32 and
+// w_static as for launch_gemv: with fused_f32 xq holds fp32 activations,
+// quantized to Q8_K in the CTA, and the activation vector must fit the
+// streaming kernel's shared memory, which gemv_q6k_fused_fits tells).
 cudaError_t launch_quantize_q6k(const float *src, void *dst, int64_t n, const LaunchCtx &ctx);
 cudaError_t launch_dequantize_q6k(const void *src, float *dst, int64_t n, const LaunchCtx &ctx);
 cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                            int64_t batch, bool w_static, const LaunchCtx &ctx);
+                            int64_t batch, bool fused_f32, bool w_static, const LaunchCtx &ctx);
+bool gemv_q6k_fused_fits(int64_t cols);
 
 // Q5_K x Q8_K GEMV (gq_q5k.cu; the Q5_K codecs are in gq_codec.cu): any
 // batch, one pass over W per activation vector; sums != nullptr selects the
-// int32 sums S1, S2 per 256-element block instead of y.
+// int32 sums S1, S2 per 256-element block instead of y; fused_f32 and
+// w_static as for launch_gemv_q6k.
 cudaError_t launch_gemv_q5k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                            int64_t batch, bool w_static, const LaunchCtx &ctx);
+                            int64_t batch, bool fused_f32, bool w_static, const LaunchCtx &ctx);
+bool gemv_q5k_fused_fits(int64_t cols);
 
 // tcgen05 tensor-core family (Q4_K x Q8_K): a pack kernel writes the
 // activation operand into `workspace`, then the MMA kernel runs.

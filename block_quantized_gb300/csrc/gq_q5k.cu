@@ -44,6 +44,7 @@
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
+#include "gq_quant8.cuh"
 
 namespace gq {
 namespace {
@@ -132,9 +133,9 @@ __device__ __forceinline__ void half_sums(const uint8_t *blk, int h, const uint8
 
 // Streaming kernel: one activation vector per blockIdx.y.  SUMS: write the
 // int32 sums S1, S2 of every block instead of y.
-template <bool SUMS, int GW>
+template <bool SUMS, int GW, bool FUSED>
 __global__ void __launch_bounds__(GW * 32, 1) gemv_q5k_kernel(const uint8_t *__restrict__ W,
-                                                             const uint8_t *__restrict__ xq,
+                                                             const void *__restrict__ act_in,
                                                              float *__restrict__ y, int32_t *__restrict__ sums,
                                                              int rows, int nblk, int ns, int stage_bytes,
                                                              int w_static, uint32_t *__restrict__ status) {
@@ -168,7 +169,10 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q5k_kernel(const uint8_t *__r
     pdl_wait();  // xq (and, unless static, W) may come from the preceding kernel in the stream
     if (lane == 0 && !w_static)
         for (int i = 0; i < ns && i < total; ++i) issue(i, i);
-    stage_q8_k_vec(act, xq + (size_t)b * nblk * Q8_K_BYTES, nblk);
+    if (FUSED)  // fp32 activations, quantized to Q8_K here exactly as by the codec
+        q8::stage_q8_k_from_f32<8>(act, static_cast<const float *>(act_in) + (size_t)b * nblk * QK_K, nblk);
+    else
+        stage_q8_k_vec(act, static_cast<const uint8_t *>(act_in) + (size_t)b * nblk * Q8_K_BYTES, nblk);
     __syncthreads();
 
     const int32_t *tsum = reinterpret_cast<const int32_t *>(act + (size_t)nblk * 256);
@@ -312,10 +316,10 @@ int pick_ns(int nw, int nblk) {
     return 0;
 }
 
-template <bool SUMS, int NW>
-cudaError_t launch_stream(const uint8_t *W, const uint8_t *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
+template <bool SUMS, int NW, bool FUSED>
+cudaError_t launch_stream(const uint8_t *W, const void *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
                           int nb, int ns, int w_static, const LaunchCtx &ctx) {
-    auto k = gemv_q5k_kernel<SUMS, NW>;
+    auto k = gemv_q5k_kernel<SUMS, NW, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
@@ -323,26 +327,28 @@ cudaError_t launch_stream(const uint8_t *W, const uint8_t *xb, float *yb, int32_
                       yb, sb, (int)rows, nblk, ns, nblk * Q5_K_BYTES, w_static, ctx.status);
 }
 
-template <bool SUMS>
-cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+template <bool SUMS, bool FUSED>
+cudaError_t run_gemv(const uint8_t *W, const void *act, float *y, int32_t *sums, int64_t rows, int64_t cols,
                      int64_t batch, int w_static, const LaunchCtx &ctx) {
     const int nblk = (int)(cols / QK_K);
     int nw = 16, ns = pick_ns(nw, nblk);
     if (!ns) ns = pick_ns(nw = 8, nblk);
     for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
         const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
-        const uint8_t *xb = xq + b0 * nblk * Q8_K_BYTES;
+        const void *xb = FUSED ? static_cast<const void *>(static_cast<const float *>(act) + b0 * cols)
+                               : static_cast<const void *>(static_cast<const uint8_t *>(act) + b0 * nblk * Q8_K_BYTES);
         float *yb = SUMS ? nullptr : y + b0 * rows;
         int32_t *sb = SUMS ? sums + b0 * rows * nblk * 2 : nullptr;
         cudaError_t e;
         if (ns && nw == 16) {
-            e = launch_stream<SUMS, 16>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+            e = launch_stream<SUMS, 16, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else if (ns) {
-            e = launch_stream<SUMS, 8>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+            e = launch_stream<SUMS, 8, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else {
+            if (FUSED) return cudaErrorInvalidValue;  // one vector does not fit the streaming kernel
             const int64_t gx = (rows + PW - 1) / PW;
             e = launch_pdl(gemv_q5k_plain_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(PW * 32), 0, ctx.stream, W,
-                           xb, yb, sb, (int)rows, nblk);
+                           static_cast<const uint8_t *>(xb), yb, sb, (int)rows, nblk);
         }
         if (e != cudaSuccess) return e;
     }
@@ -351,12 +357,23 @@ cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sum
 
 }  // namespace
 
+// The fused form has no plain-kernel fallback: the whole vector must fit the
+// streaming kernel next to a two-stage ring.
+bool gemv_q5k_fused_fits(int64_t cols) {
+    if (cols < 0 || cols % QK_K != 0 || cols > (int64_t)1 << 20) return false;
+    const int nblk = (int)(cols / QK_K);
+    return pick_ns(16, nblk) > 0 || pick_ns(8, nblk) > 0;
+}
+
 cudaError_t launch_gemv_q5k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                            int64_t batch, bool w_static, const LaunchCtx &ctx) {
+                            int64_t batch, bool fused, bool w_static, const LaunchCtx &ctx) {
     const uint8_t *w8 = static_cast<const uint8_t *>(W);
-    const uint8_t *x8 = static_cast<const uint8_t *>(xq);
-    return sums ? run_gemv<true>(w8, x8, y, sums, rows, cols, batch, w_static ? 1 : 0, ctx)
-                : run_gemv<false>(w8, x8, y, sums, rows, cols, batch, w_static ? 1 : 0, ctx);
+    const int ws = w_static ? 1 : 0;
+    if (fused)
+        return sums ? run_gemv<true, true>(w8, xq, y, sums, rows, cols, batch, ws, ctx)
+                    : run_gemv<false, true>(w8, xq, y, sums, rows, cols, batch, ws, ctx);
+    return sums ? run_gemv<true, false>(w8, xq, y, sums, rows, cols, batch, ws, ctx)
+                : run_gemv<false, false>(w8, xq, y, sums, rows, cols, batch, ws, ctx);
 }
 
 }  // namespace gq

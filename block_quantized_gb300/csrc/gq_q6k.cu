@@ -42,6 +42,7 @@
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
+#include "gq_quant8.cuh"
 
 namespace gq {
 namespace {
@@ -212,9 +213,9 @@ __device__ __forceinline__ int half_dot(const uint8_t *stage, uint32_t blk_off, 
 // Streaming kernel: cols a multiple of 2048 (rows are 16-byte multiples);
 // one activation vector per blockIdx.y.  SUMS: write the int32 block sums
 // instead of y.
-template <bool SUMS, int GW>
+template <bool SUMS, int GW, bool FUSED>
 __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__restrict__ W,
-                                                             const uint8_t *__restrict__ xq,
+                                                             const void *__restrict__ act_in,
                                                              float *__restrict__ y, int32_t *__restrict__ sums,
                                                              int rows, int nblk, int ns, int stage_bytes,
                                                              int w_static, uint32_t *__restrict__ status) {
@@ -248,7 +249,10 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__r
     pdl_wait();  // xq (and, unless static, W) may come from the preceding kernel in the stream
     if (lane == 0 && !w_static)
         for (int i = 0; i < ns && i < total; ++i) issue(i, i);
-    stage_q8_k_vec(act, xq + (size_t)b * nblk * Q8_K_BYTES, nblk);
+    if (FUSED)  // fp32 activations, quantized to Q8_K here exactly as by the codec
+        q8::stage_q8_k_from_f32<2>(act, static_cast<const float *>(act_in) + (size_t)b * nblk * QK_K, nblk);
+    else
+        stage_q8_k_vec(act, static_cast<const uint8_t *>(act_in) + (size_t)b * nblk * Q8_K_BYTES, nblk);
     __syncthreads();
 
     const int32_t *asum = reinterpret_cast<const int32_t *>(act + (size_t)nblk * 256);
@@ -370,10 +374,10 @@ int pick_ns(int nw, int nblk) {
     return 0;
 }
 
-template <bool SUMS, int NW>
-cudaError_t launch_stream(const uint8_t *W, const uint8_t *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
+template <bool SUMS, int NW, bool FUSED>
+cudaError_t launch_stream(const uint8_t *W, const void *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
                           int nb, int ns, int w_static, const LaunchCtx &ctx) {
-    auto k = gemv_q6k_kernel<SUMS, NW>;
+    auto k = gemv_q6k_kernel<SUMS, NW, FUSED>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
@@ -387,8 +391,8 @@ int codec_grid(int64_t items, int per_cta, int num_sms) {
     return (int)std::max<int64_t>(g, 1);
 }
 
-template <bool SUMS>
-cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
+template <bool SUMS, bool FUSED>
+cudaError_t run_gemv(const uint8_t *W, const void *act, float *y, int32_t *sums, int64_t rows, int64_t cols,
                      int64_t batch, int w_static, const LaunchCtx &ctx) {
     const int nblk = (int)(cols / QK_K);
     // the widest instantiation whose rings fit: GQ_Q6K_MAX_WARPS, 16 or 8 warps
@@ -397,20 +401,22 @@ cudaError_t run_gemv(const uint8_t *W, const uint8_t *xq, float *y, int32_t *sum
     if (!ns && nw > 8) ns = pick_ns(nw = 8, nblk);
     for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
         const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
-        const uint8_t *xb = xq + b0 * nblk * Q8_K_BYTES;
+        const void *xb = FUSED ? static_cast<const void *>(static_cast<const float *>(act) + b0 * cols)
+                               : static_cast<const void *>(static_cast<const uint8_t *>(act) + b0 * nblk * Q8_K_BYTES);
         float *yb = SUMS ? nullptr : y + b0 * rows;
         int32_t *sb = SUMS ? sums + b0 * rows * nblk : nullptr;
         cudaError_t e;
         if (ns && nw == GQ_Q6K_MAX_WARPS) {
-            e = launch_stream<SUMS, GQ_Q6K_MAX_WARPS>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+            e = launch_stream<SUMS, GQ_Q6K_MAX_WARPS, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else if (ns && nw == 16) {
-            e = launch_stream<SUMS, 16>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+            e = launch_stream<SUMS, 16, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else if (ns) {
-            e = launch_stream<SUMS, 8>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+            e = launch_stream<SUMS, 8, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
         } else {
+            if (FUSED) return cudaErrorInvalidValue;  // one vector does not fit the streaming kernel
             const int64_t gx = (rows + PW - 1) / PW;
             e = launch_pdl(gemv_q6k_plain_kernel<SUMS>, dim3((unsigned)gx, nb), dim3(PW * 32), 0, ctx.stream, W,
-                           xb, yb, sb, (int)rows, nblk);
+                           static_cast<const uint8_t *>(xb), yb, sb, (int)rows, nblk);
         }
         if (e != cudaSuccess) return e;
     }
@@ -430,12 +436,23 @@ cudaError_t launch_dequantize_q6k(const void *src, float *dst, int64_t n, const 
                       static_cast<const uint8_t *>(src), dst, n);
 }
 
+// The fused form has no plain-kernel fallback: the whole vector must fit the
+// streaming kernel next to a two-stage ring.
+bool gemv_q6k_fused_fits(int64_t cols) {
+    if (cols < 0 || cols % QK_K != 0 || cols > (int64_t)1 << 20) return false;
+    const int nblk = (int)(cols / QK_K);
+    return pick_ns(16, nblk) > 0 || pick_ns(8, nblk) > 0;
+}
+
 cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                            int64_t batch, bool w_static, const LaunchCtx &ctx) {
+                            int64_t batch, bool fused, bool w_static, const LaunchCtx &ctx) {
     const uint8_t *w8 = static_cast<const uint8_t *>(W);
-    const uint8_t *x8 = static_cast<const uint8_t *>(xq);
-    return sums ? run_gemv<true>(w8, x8, y, sums, rows, cols, batch, w_static ? 1 : 0, ctx)
-                : run_gemv<false>(w8, x8, y, sums, rows, cols, batch, w_static ? 1 : 0, ctx);
+    const int ws = w_static ? 1 : 0;
+    if (fused)
+        return sums ? run_gemv<true, true>(w8, xq, y, sums, rows, cols, batch, ws, ctx)
+                    : run_gemv<false, true>(w8, xq, y, sums, rows, cols, batch, ws, ctx);
+    return sums ? run_gemv<true, false>(w8, xq, y, sums, rows, cols, batch, ws, ctx)
+                : run_gemv<false, false>(w8, xq, y, sums, rows, cols, batch, ws, ctx);
 }
 
 }  // namespace gq

@@ -307,14 +307,17 @@ gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y,
 /*
  * Fused activation quantize + product: x holds fp32 activations
  * float[batch][cols] (device, 16-byte aligned); each CTA quantizes them to
- * Q8_K (Q4_K weights) or Q8_0 (Q4_0 / Q8_0 weights) in shared memory with
+ * Q8_K (Q4_K, Q5_K, Q6_K weights) or Q8_0 (Q4_0 / Q8_0 weights) in shared memory with
  * exactly the arithmetic of gq_quantize_rows, then runs the GEMV.  The result
  * equals gq_quantize_rows followed by gq_matmul_path(..., GQ_PATH_GEMV), bit
  * for bit, with one launch instead of two and no quantized activation buffer
  * ("llama.cpp：一个人、一个周末…", 第一层：GGML 张量库: operators fused over
  * the computation graph).  GEMV kernels only (any batch); cols must be a
- * multiple of 256 (GQ_ERR_SHAPE otherwise).  Q4_0, Q8_0 and Q4_K weights
- * (GQ_ERR_TYPE for Q5_K and Q6_K).  Other arguments as gq_matmul.
+ * multiple of 256 (GQ_ERR_SHAPE otherwise).  Q5_K and Q6_K weights: the
+ * quantized vector shares shared memory with the streaming kernel's weight
+ * ring, so cols is at most 18944 (Q5_K) or a multiple of 2048 up to 16384
+ * (Q6_K: whole rows of 16-byte multiples), GQ_ERR_SHAPE otherwise.  Other
+ * arguments as gq_matmul.
  */
 gq_status gq_matmul_f32(gq_type wtype, const void *W, const float *x, float *y,
                         int64_t rows, int64_t cols, int64_t batch, unsigned flags,

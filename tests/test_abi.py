@@ -145,8 +145,12 @@ def test_fused_and_flag_validation(lib):
     assert f(0, A16, A16, A16, 8, 96, 1, 0, None) == SHAPE          # fused needs cols % 256 == 0
     assert f(2, A16, A16, A16, 8, 256, 1, 2, None) == TYPE          # unknown flag bit
     assert f(3, A16, A16, A16, 8, 256, 1, 0, None) == TYPE
-    assert f(4, A16, A16, A16, 8, 256, 1, 0, None) == TYPE          # no fused Q6_K kernel
-    assert f(5, A16, A16, A16, 8, 256, 1, 0, None) == TYPE          # nor a fused Q5_K one
+    # Q5_K / Q6_K fuse only into the streaming kernel: the vector must fit its
+    # shared memory (Q6_K also wants whole 16-byte rows, cols % 2048 == 0)
+    assert f(5, A16, A16, A16, 8, 19200, 1, 0, None) == SHAPE
+    assert f(4, A16, A16, A16, 8, 18432, 1, 0, None) == SHAPE
+    assert f(4, A16, A16, A16, 8, 2304, 1, 0, None) == SHAPE
+    assert lib.gq_block_sums_f32(4, A16, A16, A16, 8, 768, 1, None) == SHAPE
     assert f(2, 0, 0, 0, 0, 256, 1, 0, None) == OK
     e = lib.gq_matmul_ex
     assert e(2, A16, A16, A16, 8, 256, 1, 1, 4, None) == TYPE

@@ -176,3 +176,81 @@ def test_static_weights_flag_same_result():
         gq.gq_matmul(Q6_K, Ws[i], X[i], yb[i], rows, cols, 1)
     torch.cuda.synchronize()
     assert ya.cpu().numpy().tobytes() == yb.cpu().numpy().tobytes()
+
+
+# ------------------------------------------- fused activation quantize path
+
+FUSED_SHAPES = [(1, 2048, 1), (7, 2048, 3), (130, 4096, 2), (33, 6144, 5), (4867, 4096, 1),
+                (9, 16384, 2)]
+
+
+@pytest.mark.parametrize("rows,cols,batch", FUSED_SHAPES)
+def test_fused_f32_matches_unfused_and_oracle(rows, cols, batch):
+    """gq_matmul_f32 quantizes the fp32 vector to Q8_K inside the streaming
+    kernel: its integer sums equal the oracle's, and y equals quantize +
+    gq_matmul bit for bit."""
+    g = inputs.rng(5 * rows + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q6_K, W), orc.quantize(Q8_K, X)
+    Wd, Xf = dev(Wq), dev(X)
+    s = host(gq.block_sums_f32(Q6_K, Wd, Xf, rows, cols, batch))
+    idx = np.unique(np.array([0, rows // 2, rows - 1]))
+    np.testing.assert_array_equal(s[:, idx], orc.block_sums(Q6_K, Wq[idx], Xq, len(idx), cols, batch))
+    y_f = host(gq.matmul_f32(Q6_K, Wd, Xf, rows, cols, batch))
+    y_u = host(gq.matmul(Q6_K, Wd, gq.quantize(Q8_K, Xf), rows, cols, batch))
+    assert y_f.view(np.uint32).tobytes() == y_u.view(np.uint32).tobytes()
+    y_ref, T = orc.matmul_ref(Q6_K, Wq[idx], Xq, len(idx), cols, batch)
+    assert_close(y_f[:, idx], y_ref, T)
+
+
+def test_fused_quantize_ties_match_oracle():
+    """Identity weights expose every activation code through the block sums
+    (one per block: the single nonzero weight code times the activation
+    code); activations on and next to rounding ties."""
+    cols = 2048
+    g = np.random.default_rng(43)
+    X = np.empty((2, cols), np.float32)
+    for r in range(2):
+        for b0 in range(0, cols, 256):
+            d = np.float32(2.0 ** int(g.integers(-12, 3))) if (b0 // 256 + r) % 2 == 0 else \
+                np.float32(g.uniform(0.01, 3.0) / 127.0)
+            v = ((g.integers(-126, 126, 256) + 0.5) * d).astype(np.float32)
+            nudge = g.integers(-1, 2, 256)
+            v = np.where(nudge > 0, np.nextafter(v, np.float32(np.inf)), v)
+            v = np.where(nudge < 0, np.nextafter(v, np.float32(-np.inf)), v)
+            v[0] = np.float32(127.0) * d
+            X[r, b0:b0 + 256] = v
+    Wq = orc.quantize(Q6_K, np.eye(cols, dtype=np.float32))
+    Xq = orc.quantize(Q8_K, X)
+    s = host(gq.block_sums_f32(Q6_K, dev(Wq), dev(X), cols, cols, 2))
+    np.testing.assert_array_equal(s, orc.block_sums(Q6_K, Wq, Xq, cols, cols, 2))
+
+
+def test_fused_f32_degenerate_vectors():
+    """A zero vector (scale 0: every code 0), a constant one and tiny values."""
+    rows, cols = 40, 2048
+    W = inputs.normal(inputs.rng(8), (rows, cols), 0.02)
+    X = inputs.normal(inputs.rng(9), (4, cols))
+    X[0] = 0.0
+    X[1] = 0.37
+    X[2, :512] = 1e-30
+    X[3, ::3] = -5.0
+    Wq, Xq = orc.quantize(Q6_K, W), orc.quantize(Q8_K, X)
+    s = host(gq.block_sums_f32(Q6_K, dev(Wq), dev(X), rows, cols, 4))
+    np.testing.assert_array_equal(s, orc.block_sums(Q6_K, Wq, Xq, rows, cols, 4))
+    y = host(gq.matmul_f32(Q6_K, dev(Wq), dev(X), rows, cols, 4))
+    y_ref, T = orc.matmul_ref(Q6_K, Wq, Xq, rows, cols, 4)
+    assert_close(y, y_ref, T)
+    assert np.all(y[0] == 0.0)
+
+
+@pytest.mark.parametrize("cols", [2304, 18432])
+def test_fused_f32_shape_limits(cols):
+    """Vectors the streaming kernel cannot take (rows not whole 16-byte
+    multiples, or too wide for its shared memory) are refused."""
+    Wd = torch.zeros(1, cols // 256 * 194, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1, cols, device="cuda")
+    y = torch.empty(1, 1, device="cuda")
+    with pytest.raises(gq.GQError):
+        gq.gq_matmul_f32(Q6_K, Wd, x, y, 1, cols, 1)
