@@ -26,7 +26,7 @@
 // fragment takes elements 32 j + 8 t + 0..7 of its rows and columns.
 //
 // CTA (96 weight rows, 8 NT activation columns):
-//   compute warps  KS groups of six (KS = 2 up to 32 columns, else 1); group
+//   compute warps  KS groups of six (KS = 4 for 8 columns, 2 up to 32, else 1); group
 //                  g takes the super-blocks sb = g (mod KS) of the 96 rows,
 //                  and the groups' partial y are added in group order at the
 //                  end (the int32 block sums are per super-block, exact);
@@ -57,9 +57,11 @@ struct SkCfg {
     static constexpr int BCOLS = 8 * NT_;
     // Tiles up to 32 columns split the super-blocks between KS groups of six
     // compute warps (group g takes the super-blocks sb = g mod KS of the same
-    // 96 rows), so twice as many independent warps cover the latency of each
-    // warp's conversion and MMA chain; their partial y meet at the end.
-    static constexpr int KS = NT_ <= 4 ? 2 : 1;
+    // 96 rows), so more independent warps cover the latency of each warp's
+    // conversion and MMA chain; their partial y meet at the end.  Four groups
+    // (64 registers a thread) pay off only for 8-column tiles: 12.8 vs 13.3 us
+    // at 14336 x 4096 x 8, but 17.1 vs 16.7 us at 16 columns.
+    static constexpr int KS = NT_ == 1 ? 4 : (NT_ <= 4 ? 2 : 1);
     static constexpr int NCW = SK_NW * KS;                 // compute warps
     static constexpr int CW = 4;                           // activation converter warps
     static constexpr int PRODUCER = NCW;                   // warp index of the weight producer
@@ -68,7 +70,7 @@ struct SkCfg {
     static constexpr int MINB = 1;
     static constexpr int LIMIT = SK_SM_SMEM - 1024;
     static constexpr int KC = NT_ <= 2 ? 4 / NT_ : 2;      // super-blocks per activation chunk
-    static constexpr int PART = KS > 1 ? SK_NW * 32 * NT_ * 16 : 0;  // group partial y (float4 per lane and tile)
+    static constexpr int PART = (KS - 1) * SK_NW * 32 * NT_ * 16;  // partial y of groups 1.. (float4 per lane and tile)
     // one activation chunk: B fragments [nt][sub-block of the chunk][lane]
     // (uint4: the two K = 16 steps of the sub-block), min-term B fragments
     // [nt][super-block of the chunk][lane] (uint2), column pairs (dx,
@@ -403,20 +405,22 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
                 // groups 1.. hand their partial y to group 0, which adds them
                 // in group order; every compute warp reaches both barriers
                 float4 *part = reinterpret_cast<float4 *>(smem + C::OFF_PART);
-                if (kg == 1)
+                if (kg > 0)
 #pragma unroll
                     for (int n = 0; n < NT; ++n)
-                        part[(rw * NT + n) * 32 + lane] = make_float4(yacc[n][0], yacc[n][1], yacc[n][2], yacc[n][3]);
+                        part[(((kg - 1) * SK_NW + rw) * NT + n) * 32 + lane] =
+                            make_float4(yacc[n][0], yacc[n][1], yacc[n][2], yacc[n][3]);
                 asm volatile("bar.sync 1, %0;" ::"r"(32 * C::NCW) : "memory");
                 if (kg == 0)
+                    for (int k = 1; k < C::KS; ++k)
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        const float4 v = part[(rw * NT + n) * 32 + lane];
-                        yacc[n][0] += v.x;
-                        yacc[n][1] += v.y;
-                        yacc[n][2] += v.z;
-                        yacc[n][3] += v.w;
-                    }
+                        for (int n = 0; n < NT; ++n) {
+                            const float4 v = part[(((k - 1) * SK_NW + rw) * NT + n) * 32 + lane];
+                            yacc[n][0] += v.x;
+                            yacc[n][1] += v.y;
+                            yacc[n][2] += v.z;
+                            yacc[n][3] += v.w;
+                        }
             }
             if (kg == 0 && !*abort) {
                 const int rg = row0 + 16 * rw + g;
