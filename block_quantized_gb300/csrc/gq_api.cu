@@ -234,7 +234,7 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
             const int64_t nb = std::min<int64_t>(64, batch - b0);
             cudaError_t e = launch_skinny_q4k(W, static_cast<const uint8_t *>(act) + b0 * nsb * 276,
                                               y ? y + b0 * rows : nullptr, sums ? sums + b0 * rows * nsb * 2 : nullptr,
-                                              rows, cols, nb, ctx);
+                                              rows, cols, nb, (flags & GQ_FLAG_W_STATIC) != 0, ctx);
             if (e != cudaSuccess) return cuda_fail(e);
         }
         return GQ_OK;

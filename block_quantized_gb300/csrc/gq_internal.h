@@ -94,9 +94,11 @@ cudaError_t launch_mma_q0(gq_type wtype, const void *W, const void *xq, float *y
                           int64_t cols, int64_t batch, const LaunchCtx &ctx);
 bool mma_q0_supported(int64_t rows, int64_t cols, int64_t batch);
 // Warp-level tensor-core kernel for Q4_K x Q8_K at small batches
-// (gq_skinny.cu): batch <= 64, cols a multiple of 256, no workspace.
+// (gq_skinny.cu): batch <= 64, cols a multiple of 256, no workspace;
+// w_static as for launch_gemv (the first weight tiles are requested before
+// the dependency wait).
 cudaError_t launch_skinny_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                              int64_t batch, const LaunchCtx &ctx);
+                              int64_t batch, bool w_static, const LaunchCtx &ctx);
 bool skinny_supported(int64_t rows, int64_t cols, int64_t batch);
 // The library's static scratch (no allocation): its size, and its device
 // address on `device` (looked up on the first call for that device, which

@@ -123,8 +123,10 @@ enum {
      * request their first weight chunks before waiting for the preceding
      * kernel in the stream to finish, overlapping the weight fetch with that
      * kernel's tail.  Without the flag every read of W happens after that
-     * wait.  The Q4_0 / Q8_0 / Q4_K, Q5_K and Q6_K GEMV kernels act on it;
-     * the tensor-core kernels read W after the wait in any case. */
+     * wait.  The Q4_0 / Q8_0 / Q4_K, Q5_K and Q6_K GEMV kernels and the
+     * warp-level tensor-core kernel (GQ_PATH_SKINNY, its first two weight
+     * tiles) act on it; the tcgen05 kernels read W after the wait in any
+     * case. */
     GQ_FLAG_W_STATIC = 1u
 };
 

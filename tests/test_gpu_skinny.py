@@ -113,6 +113,26 @@ def test_skinny_batches_beyond_one_tile(batch):
     assert_close(y, y_ref, T)
 
 
+@pytest.mark.parametrize("batch", [1, 16, 40])
+def test_skinny_static_weights_flag_same_result(batch):
+    """GQ_FLAG_W_STATIC only moves the first weight tiles before the
+    dependency wait: a chain of products over distinct matrices gives the
+    same bytes with and without it."""
+    rows, cols, n = 500, 1024, 5
+    g = inputs.rng(51 + batch)
+    Ws = [gq.quantize(Q4_K, dev(inputs.normal(g, (rows, cols), 0.02))) for _ in range(n)]
+    X = gq.quantize(Q8_K, dev(inputs.normal(g, (batch, cols))))
+    ya = torch.empty(n, batch, rows, device="cuda")
+    yb = torch.empty(n, batch, rows, device="cuda")
+    for i in range(n):
+        gq.gq_matmul_ex(Q4_K, Ws[i], X, ya[i], rows, cols, batch, gq.PATH_SKINNY, gq.FLAG_W_STATIC)
+    for i in range(n):
+        gq.gq_matmul_path(Q4_K, Ws[i], X, yb[i], rows, cols, batch, gq.PATH_SKINNY)
+    assert host(ya).tobytes() == host(yb).tobytes()
+    y_ref, T = orc.matmul_ref(Q4_K, host(Ws[-1]), host(X), rows, cols, batch)
+    assert_close(host(ya[-1]), y_ref, T)
+
+
 def test_skinny_shape_rules():
     """Q4_K weights and cols a multiple of 256 only."""
     rows, cols = 128, 512
