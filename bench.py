@@ -757,6 +757,16 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
     t_c, _ = time_graph(capture(chain), k, 5)
     t_p, _ = time_graph(capture(chain_plain), k, 5)
     t_f, _ = time_graph(capture(chain_fused), k, 5)
+    # small batches: up to eight vectors share one pass over each matrix
+    Yb = torch.empty(8, GEMV_ROWS, dtype=torch.float32, device=dev)
+    batch_us = {}
+    for nb in (2, 4, 8):
+        def chain_b():
+            for i in range(COPIES):
+                gq.gq_matmul_ex(wt, Wall[i], XQ[:nb], Yb, GEMV_ROWS, GEMV_COLS, nb, gq.PATH_AUTO,
+                                gq.FLAG_W_STATIC)
+        t_b, _ = time_graph(capture(chain_b), 50, 3)
+        batch_us[str(nb)] = t_b / (50 * COPIES) * 1e6
     t_t, _ = time_graph(capture(tall), 50, 3)
     if not (torch.isfinite(Y).all() and torch.isfinite(Yt).all()):
         raise RuntimeError(f"non-finite {name} GEMV output")
@@ -773,6 +783,7 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
             "launch_us": per * 1e6, "alg_bytes_per_launch": alg, "weight_gbps": w_bytes / per / 1e9,
             "achieved": alg / per / 1e9, "frac": alg / per / 1e9 / hbm_peak,
             "launch_us_without_w_static": t_p / (k * COPIES) * 1e6,
+            "batch_launch_us": batch_us,
             "fused_f32": {"launch_us": t_f / (k * COPIES) * 1e6,
                           "frac": (w_bytes + GEMV_COLS * 4 + GEMV_ROWS * 4) / (t_f / (k * COPIES)) / 1e9
                           / hbm_peak},

@@ -63,7 +63,7 @@ cudaError_t launch_gemv(gq_type wtype, const void *W, const void *act, float *y,
 bool gemv_fits(gq_type wtype, int64_t cols);
 
 // Q6_K weights (gq_q6k.cu): codecs, and the Q6_K x Q8_K GEMV (any batch,
-// one pass over W per activation vector; sums != nullptr selects the int32
+// one pass over W per group of up to eight activation vectors; sums != nullptr selects the int32
 // block sums, one per 256-element block, instead of y; fused_f32 and
 // w_static as for launch_gemv: with fused_f32 xq holds fp32 activations,
 // quantized to Q8_K in the CTA, and the activation vector must fit the
@@ -75,7 +75,7 @@ cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *su
 bool gemv_q6k_fused_fits(int64_t cols);
 
 // Q5_K x Q8_K GEMV (gq_q5k.cu; the Q5_K codecs are in gq_codec.cu): any
-// batch, one pass over W per activation vector; sums != nullptr selects the
+// batch, one pass over W per group of up to eight vectors; sums != nullptr selects the
 // int32 sums S1, S2 per 256-element block instead of y; fused_f32 and
 // w_static as for launch_gemv_q6k.
 cudaError_t launch_gemv_q5k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,

@@ -28,16 +28,21 @@
 //     policy) per row completing on an mbarrier; every wait is bounded.
 //     Blocks are 176 = 11 x 16 bytes, so every row and every block field is
 //     16-byte aligned and all shared loads are 128-bit;
-//   - the CTA stages its Q8_K vector once: codes in 128-byte half-super-block
-//     units, each 8-code group stored as (a0 a2 a4 a6 | a1 a3 a5 a7) so the
-//     even and odd elements of a nibble word meet their activations in one
-//     dp4a each, 16-byte pieces XOR-swizzled by the unit index (distinct
-//     banks for a quarter-warp); then the eight sub-block sums and the scale;
+//   - the CTA stages up to eight Q8_K vectors (the smallest group of 1, 2, 4
+//     or 8 that covers the batch, fewer when wide vectors leave no room for
+//     the rings), so W streams once per group; each vector: codes in 128-byte
+//     half-super-block units, each 8-code group stored as (a0 a2 a4 a6 |
+//     a1 a3 a5 a7) so the even and odd elements of a nibble word meet their
+//     activations in one dp4a each, 16-byte pieces XOR-swizzled by the unit
+//     index (distinct banks for a quarter-warp); then the eight sub-block
+//     sums and the scale;
 //   - a lane takes half a super-block (four sub-blocks, 128 elements): one
 //     header load, four 16-byte nibble loads and one 16-byte fifth-bit load;
-//     per 8 elements two 5-bit code words built with shifts and masks and two
-//     dp4a; S1 and S2 of the half in int32; fp32 partial per lane and one
-//     warp-shuffle reduction per row.
+//     per 8 elements two 5-bit code words built with shifts and masks, once,
+//     and two dp4a per staged vector; S1 and S2 of the half in int32; fp32
+//     partials per lane and vector, one warp-shuffle reduction per row and
+//     vector.  14336 x 4096 at batch 1 / 2 / 4 / 8: 9.4 / 11.5 / 16.2 / 25.6
+//     us (one vector per pass: 9.3 / 16.4 / 30.2 / 56.4).
 // Rows too long for a two-stage ring take a plain warp-per-row kernel that
 // reads W and the activations from global memory.
 #include <algorithm>
@@ -62,6 +67,8 @@ __host__ __device__ constexpr int bars_bytes(int nw) { return nw * MAX_NS * 8; }
 __host__ __device__ constexpr size_t act_smem_bytes(int nblk) {
     return (size_t)nblk * 256 + (size_t)nblk * 8 * 4 + (size_t)nblk * 4;
 }
+// Staged vectors follow one another at this stride (16-byte aligned).
+__host__ __device__ constexpr size_t act_stride(int nblk) { return (act_smem_bytes(nblk) + 15) / 16 * 16; }
 
 // Split-order words of 8 codes: (a0 a2 a4 a6) and (a1 a3 a5 a7).
 __device__ __forceinline__ uint2 split8(uint32_t w0, uint32_t w1) {
@@ -90,58 +97,77 @@ __device__ void stage_q8_k_vec(uint8_t *act, const uint8_t *__restrict__ xq, int
 }
 
 // Integer sums of half h of the block at `blk` (shared memory, 16-byte
-// aligned) against the staged codes of half-block hb: S1 = sum_j sc_j s_j and
-// S2 = sum_j m_j t_j over the half's four sub-blocks j = 4h + k.
-__device__ __forceinline__ void half_sums(const uint8_t *blk, int h, const uint8_t *act, const int32_t *tsum,
-                                          int hb, int &S1, int &S2) {
+// aligned) against the staged codes of half-block hb of NV vectors (vector v
+// at act + v * astride): S1[v] = sum_j sc_j s_j and S2[v] = sum_j m_j t_j over
+// the half's four sub-blocks j = 4h + k.  The 5-bit code words are built once
+// and serve every vector.
+template <int NV>
+__device__ __forceinline__ void half_sums(const uint8_t *blk, int h, const uint8_t *act, size_t astride, int nblk,
+                                          int hb, int (&S1)[NV], int (&S2)[NV]) {
     const uint4 hd = *reinterpret_cast<const uint4 *>(blk);
-    const uint4 fb = *reinterpret_cast<const uint4 *>(blk + 144 + 16 * h);  // fifth bits of the half
-    uint4 q[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) q[k] = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * h + 16 * k);
     // header bytes 4..15 = words y, z, w: this half's four sc (bits 24h..24h+23)
     // and four m (bits 48+24h..71+24h) are three whole bytes each
     const uint32_t sc24 = __byte_perm(hd.y, hd.z, h ? 0x0543u : 0x0210u);
     const uint32_t m24 = __byte_perm(hd.z, hd.w, h ? 0x0765u : 0x0432u);
-    const int4 t = reinterpret_cast<const int4 *>(tsum)[hb];  // t_j of the half
-    const uint8_t *ah = act + (size_t)hb * 128;
-    const int sw = hb & 7;
-    const uint32_t F[4] = {fb.x, fb.y, fb.z, fb.w};
-    const int tj[4] = {t.x, t.y, t.z, t.w};
-    S1 = 0;
-    S2 = 0;
+    uint32_t ce[4][4], co[4][4];  // [sub-block k][nibble word tt]: even / odd element codes
+    {
+        const uint4 fb = *reinterpret_cast<const uint4 *>(blk + 144 + 16 * h);  // fifth bits of the half
+        const uint32_t F[4] = {fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {  // sub-block 4h + k: units 2k, 2k + 1 of the half
-        const uint4 a0 = *reinterpret_cast<const uint4 *>(ah + (((2 * k) ^ sw) << 4));
-        const uint4 a1 = *reinterpret_cast<const uint4 *>(ah + (((2 * k + 1) ^ sw) << 4));
-        const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-        const uint32_t ae[4] = {a0.x, a0.z, a1.x, a1.z}, ao[4] = {a0.y, a0.w, a1.y, a1.w};
-        int s = 0;
+        for (int k = 0; k < 4; ++k) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(blk + 16 + 64 * h + 16 * k);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {  // nibble word tt: elements 8tt..8tt+7
-            // fifth bits of the even (odd) elements at bits 2tt (2tt + 1) of
-            // each byte of F[k], moved to bit 4 of each byte
-            const uint32_t fe = (2 * tt <= 4 ? F[k] << (4 - 2 * tt) : F[k] >> (2 * tt - 4)) & BIT4;
-            const uint32_t fo = (2 * tt + 1 <= 4 ? F[k] << (3 - 2 * tt) : F[k] >> (2 * tt - 3)) & BIT4;
-            s = dp4a_us((w[tt] & NIB) | fe, (int)ae[tt], s);
-            s = dp4a_us(((w[tt] >> 4) & NIB) | fo, (int)ao[tt], s);
+            for (int tt = 0; tt < 4; ++tt) {  // nibble word tt: elements 8tt..8tt+7
+                // fifth bits of the even (odd) elements at bits 2tt (2tt + 1)
+                // of each byte of F[k], moved to bit 4 of each byte
+                const uint32_t fe = (2 * tt <= 4 ? F[k] << (4 - 2 * tt) : F[k] >> (2 * tt - 4)) & BIT4;
+                const uint32_t fo = (2 * tt + 1 <= 4 ? F[k] << (3 - 2 * tt) : F[k] >> (2 * tt - 3)) & BIT4;
+                ce[k][tt] = (w[tt] & NIB) | fe;
+                co[k][tt] = ((w[tt] >> 4) & NIB) | fo;
+            }
         }
-        S1 += (int)((sc24 >> (6 * k)) & 63u) * s;
-        S2 += (int)((m24 >> (6 * k)) & 63u) * tj[k];
+    }
+    const int sw = hb & 7;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const uint8_t *av = act + (size_t)v * astride;
+        const uint8_t *ah = av + (size_t)hb * 128;
+        const int4 t = reinterpret_cast<const int4 *>(av + (size_t)nblk * 256)[hb];  // t_j of the half
+        const int tj[4] = {t.x, t.y, t.z, t.w};
+        int s1 = 0, s2 = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // sub-block 4h + k: units 2k, 2k + 1 of the half
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(ah + (((2 * k) ^ sw) << 4));
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(ah + (((2 * k + 1) ^ sw) << 4));
+            const uint32_t ae[4] = {a0.x, a0.z, a1.x, a1.z}, ao[4] = {a0.y, a0.w, a1.y, a1.w};
+            int sk = 0;
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                sk = dp4a_us(ce[k][tt], (int)ae[tt], sk);
+                sk = dp4a_us(co[k][tt], (int)ao[tt], sk);
+            }
+            s1 += (int)((sc24 >> (6 * k)) & 63u) * sk;
+            s2 += (int)((m24 >> (6 * k)) & 63u) * tj[k];
+        }
+        S1[v] = s1;
+        S2[v] = s2;
     }
 }
 
-// Streaming kernel: one activation vector per blockIdx.y.  SUMS: write the
-// int32 sums S1, S2 of every block instead of y.
-template <bool SUMS, int GW, bool FUSED>
+// Streaming kernel: NV activation vectors per blockIdx.y (vectors NV y ..
+// NV y + NV - 1 of the nvec in this launch), so W streams once per NV
+// vectors.  SUMS: write the int32 sums S1, S2 of every block instead of y.
+template <bool SUMS, int GW, bool FUSED, int NV>
 __global__ void __launch_bounds__(GW * 32, 1) gemv_q5k_kernel(const uint8_t *__restrict__ W,
                                                              const void *__restrict__ act_in,
                                                              float *__restrict__ y, int32_t *__restrict__ sums,
-                                                             int rows, int nblk, int ns, int stage_bytes,
+                                                             int rows, int nblk, int ns, int stage_bytes, int nvec,
                                                              int w_static, uint32_t *__restrict__ status) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.y;
+    const int b0 = blockIdx.y * NV, nv = min(NV, nvec - b0);
+    const size_t astride = act_stride(nblk);
     const int warps_total = gridDim.x * GW;
     const int wg = blockIdx.x * GW + warp;
     const int total = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
@@ -169,14 +195,17 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q5k_kernel(const uint8_t *__r
     pdl_wait();  // xq (and, unless static, W) may come from the preceding kernel in the stream
     if (lane == 0 && !w_static)
         for (int i = 0; i < ns && i < total; ++i) issue(i, i);
-    if (FUSED)  // fp32 activations, quantized to Q8_K here exactly as by the codec
-        q8::stage_q8_k_from_f32<8>(act, static_cast<const float *>(act_in) + (size_t)b * nblk * QK_K, nblk);
-    else
-        stage_q8_k_vec(act, static_cast<const uint8_t *>(act_in) + (size_t)b * nblk * Q8_K_BYTES, nblk);
+    for (int v = 0; v < nv; ++v) {
+        const size_t b = (size_t)(b0 + v);
+        if (FUSED)  // fp32 activations, quantized to Q8_K here exactly as by the codec
+            q8::stage_q8_k_from_f32<8>(act + v * astride, static_cast<const float *>(act_in) + b * nblk * QK_K,
+                                       nblk);
+        else
+            stage_q8_k_vec(act + v * astride, static_cast<const uint8_t *>(act_in) + b * nblk * Q8_K_BYTES, nblk);
+    }
     __syncthreads();
 
-    const int32_t *tsum = reinterpret_cast<const int32_t *>(act + (size_t)nblk * 256);
-    const float *dx = reinterpret_cast<const float *>(tsum + 8 * nblk);
+    const size_t dx_off = (size_t)nblk * 256 + (size_t)nblk * 8 * 4;  // the scales, within a staged vector
     const int iters = (2 * nblk + 31) / 32;
     int st = 0;
     uint32_t ph = 0;
@@ -198,32 +227,47 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q5k_kernel(const uint8_t *__r
         }
         const int row = wg + i * warps_total;
         const uint8_t *stage = ring + (size_t)st * stage_bytes;
-        float acc = 0.0f;
+        float acc[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[v] = 0.0f;
         for (int t = 0; t < iters; ++t) {
             const int hb = lane + 32 * t;
-            int S1 = 0, S2 = 0;
+            int S1[NV], S2[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) S1[v] = S2[v] = 0;
             if (hb < 2 * nblk) {
                 const int k = hb >> 1;
                 const uint8_t *blk = stage + (size_t)k * Q5_K_BYTES;
-                half_sums(blk, hb & 1, act, tsum, hb, S1, S2);
+                half_sums<NV>(blk, hb & 1, act, astride, nblk, hb, S1, S2);
                 if (!SUMS) {
                     const uint32_t dd = *reinterpret_cast<const uint32_t *>(blk);
-                    acc += dx[k] * (half_bits_to_float(dd) * (float)S1 - half_bits_to_float(dd >> 16) * (float)S2);
+                    const float d = half_bits_to_float(dd), dmin = half_bits_to_float(dd >> 16);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        const float dxv = reinterpret_cast<const float *>(act + v * astride + dx_off)[k];
+                        acc[v] += dxv * (d * (float)S1[v] - dmin * (float)S2[v]);
+                    }
                 }
             }
             if (SUMS) {
-                const int s1 = S1 + __shfl_xor_sync(FULL, S1, 1);  // the two halves of block hb / 2
-                const int s2 = S2 + __shfl_xor_sync(FULL, S2, 1);
-                if (hb < 2 * nblk && (hb & 1) == 0) {
-                    int32_t *o = sums + (((size_t)b * rows + row) * nblk + (hb >> 1)) * 2;
-                    o[0] = s1;
-                    o[1] = s2;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const int s1 = S1[v] + __shfl_xor_sync(FULL, S1[v], 1);  // the two halves of block hb / 2
+                    const int s2 = S2[v] + __shfl_xor_sync(FULL, S2[v], 1);
+                    if (v < nv && hb < 2 * nblk && (hb & 1) == 0) {
+                        int32_t *o = sums + (((size_t)(b0 + v) * rows + row) * nblk + (hb >> 1)) * 2;
+                        o[0] = s1;
+                        o[1] = s2;
+                    }
                 }
             }
         }
         if (!SUMS) {
-            acc = warp_sum(acc);
-            if (lane == 0) y[(size_t)b * rows + row] = acc;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const float a = warp_sum(acc[v]);
+                if (lane == 0 && v < nv) y[(size_t)(b0 + v) * rows + row] = a;
+            }
         }
         __syncwarp();
         if (lane == 0 && i + ns < total) issue(i + ns, st);
@@ -304,46 +348,80 @@ __global__ void __launch_bounds__(PW * 32) gemv_q5k_plain_kernel(const uint8_t *
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA on sm_103
 constexpr int64_t Y_MAX = 65535;    // vectors per launch (grid.y)
 
-size_t stream_smem(int nw, int ns, int nblk) {
-    return bars_bytes(nw) + (size_t)nw * ns * ((size_t)nblk * Q5_K_BYTES) + act_smem_bytes(nblk);
+size_t stream_smem(int nw, int ns, int nblk, int nv) {
+    return bars_bytes(nw) + (size_t)nw * ns * ((size_t)nblk * Q5_K_BYTES) + (size_t)nv * act_stride(nblk);
 }
 
 // Ring stages per warp for the streaming kernel with nw warps: as many as fit
-// (2..4) next to the staged vector; 0 when two stages do not fit.
-int pick_ns(int nw, int nblk) {
+// (2..4) next to nv staged vectors; 0 when two stages do not fit.
+int pick_ns(int nw, int nblk, int nv) {
     for (int ns = MAX_NS; ns >= 2; --ns)
-        if (stream_smem(nw, ns, nblk) <= (size_t)SMEM_LIMIT) return ns;
+        if (stream_smem(nw, ns, nblk, nv) <= (size_t)SMEM_LIMIT) return ns;
     return 0;
 }
 
-template <bool SUMS, int NW, bool FUSED>
+// Launch shape of the streaming kernel for a batch: nv vectors per CTA (the
+// smallest of 1, 2, 4, 8 that covers the batch, fewer when their staged
+// copies leave no room for a two-stage ring), 16 warps when sixteen rings fit
+// (eight vectors always take 8 warps: at 16 the kernel is capped at 128
+// registers and spills; 25.6 vs 29.8 us at 14336 x 4096), else 8, and the
+// ring depth.  ns == 0: not even one vector fits.
+struct Shape {
+    int nv, nw, ns;
+};
+Shape pick_shape(int nblk, int64_t batch) {
+    int nv = batch >= 8 ? 8 : batch >= 4 ? (batch > 4 ? 8 : 4) : batch >= 2 ? (batch > 2 ? 4 : 2) : 1;
+    for (; nv >= 1; nv >>= 1) {
+        if (nv < 8)
+            if (int ns = pick_ns(16, nblk, nv)) return {nv, 16, ns};
+        if (int ns = pick_ns(8, nblk, nv)) return {nv, 8, ns};
+    }
+    return {1, 8, 0};
+}
+
+template <bool SUMS, int NW, bool FUSED, int NV>
 cudaError_t launch_stream(const uint8_t *W, const void *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
                           int nb, int ns, int w_static, const LaunchCtx &ctx) {
-    auto k = gemv_q5k_kernel<SUMS, NW, FUSED>;
+    auto k = gemv_q5k_kernel<SUMS, NW, FUSED, NV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
-    return launch_pdl(k, dim3((unsigned)gx, nb), dim3(NW * 32), stream_smem(NW, ns, nblk), ctx.stream, W, xb,
-                      yb, sb, (int)rows, nblk, ns, nblk * Q5_K_BYTES, w_static, ctx.status);
+    return launch_pdl(k, dim3((unsigned)gx, (nb + NV - 1) / NV), dim3(NW * 32), stream_smem(NW, ns, nblk, NV),
+                      ctx.stream, W, xb, yb, sb, (int)rows, nblk, ns, nblk * Q5_K_BYTES, nb, w_static, ctx.status);
+}
+
+template <bool SUMS, bool FUSED, int NW>
+cudaError_t launch_nv(const Shape &sh, const uint8_t *W, const void *xb, float *yb, int32_t *sb, int64_t rows,
+                      int nblk, int nb, int w_static, const LaunchCtx &ctx) {
+    switch (sh.nv) {
+    case 8:
+        if constexpr (NW == 8)  // eight vectors always run on 8 warps (pick_shape)
+            return launch_stream<SUMS, NW, FUSED, 8>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+        else
+            return cudaErrorInvalidValue;
+    case 4: return launch_stream<SUMS, NW, FUSED, 4>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    case 2: return launch_stream<SUMS, NW, FUSED, 2>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    default: return launch_stream<SUMS, NW, FUSED, 1>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    }
 }
 
 template <bool SUMS, bool FUSED>
 cudaError_t run_gemv(const uint8_t *W, const void *act, float *y, int32_t *sums, int64_t rows, int64_t cols,
                      int64_t batch, int w_static, const LaunchCtx &ctx) {
     const int nblk = (int)(cols / QK_K);
-    int nw = 16, ns = pick_ns(nw, nblk);
-    if (!ns) ns = pick_ns(nw = 8, nblk);
-    for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
-        const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
+    const Shape sh = pick_shape(nblk, batch);
+    const int64_t per_launch = sh.ns ? Y_MAX * sh.nv : Y_MAX;
+    for (int64_t b0 = 0; b0 < batch; b0 += per_launch) {
+        const int nb = (int)std::min<int64_t>(per_launch, batch - b0);
         const void *xb = FUSED ? static_cast<const void *>(static_cast<const float *>(act) + b0 * cols)
                                : static_cast<const void *>(static_cast<const uint8_t *>(act) + b0 * nblk * Q8_K_BYTES);
         float *yb = SUMS ? nullptr : y + b0 * rows;
         int32_t *sb = SUMS ? sums + b0 * rows * nblk * 2 : nullptr;
         cudaError_t e;
-        if (ns && nw == 16) {
-            e = launch_stream<SUMS, 16, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
-        } else if (ns) {
-            e = launch_stream<SUMS, 8, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+        if (sh.ns && sh.nw == 16) {
+            e = launch_nv<SUMS, FUSED, 16>(sh, W, xb, yb, sb, rows, nblk, nb, w_static, ctx);
+        } else if (sh.ns) {
+            e = launch_nv<SUMS, FUSED, 8>(sh, W, xb, yb, sb, rows, nblk, nb, w_static, ctx);
         } else {
             if (FUSED) return cudaErrorInvalidValue;  // one vector does not fit the streaming kernel
             const int64_t gx = (rows + PW - 1) / PW;
@@ -361,8 +439,7 @@ cudaError_t run_gemv(const uint8_t *W, const void *act, float *y, int32_t *sums,
 // streaming kernel next to a two-stage ring.
 bool gemv_q5k_fused_fits(int64_t cols) {
     if (cols < 0 || cols % QK_K != 0 || cols > (int64_t)1 << 20) return false;
-    const int nblk = (int)(cols / QK_K);
-    return pick_ns(16, nblk) > 0 || pick_ns(8, nblk) > 0;
+    return pick_shape((int)(cols / QK_K), 1).ns > 0;
 }
 
 cudaError_t launch_gemv_q5k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,

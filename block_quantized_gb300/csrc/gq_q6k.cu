@@ -23,8 +23,10 @@
 //     ...  Each warp streams its rows through a private shared-memory ring of
 //     2-4 whole-row stages, one bulk copy (cp.async.bulk, evict-first L2
 //     policy) per row completing on an mbarrier; every wait is bounded;
-//   - the CTA stages its Q8_K activation vector once: codes in 128-byte
-//     half-super-block units, each 8-code group stored as (a0 a2 a4 a6 |
+//   - the CTA stages up to eight Q8_K activation vectors (the smallest group
+//     of 1, 2, 4 or 8 that covers the batch, fewer when wide vectors leave no
+//     room for the rings), so W streams once per group; each vector: codes in
+//     128-byte half-super-block units, each 8-code group stored as (a0 a2 a4 a6 |
 //     a1 a3 a5 a7) so that the masked low nibbles of a packed word line up
 //     with dp4a operands, and the 16-byte pieces of a unit XOR-swizzled by
 //     the unit index so that the lanes of a quarter-warp hit distinct banks;
@@ -32,9 +34,12 @@
 //   - a lane takes half a block (128 elements): 17 + 9 aligned 32-bit shared
 //     loads realigned with funnel shifts (blocks are 194 bytes, so half of
 //     them start 2 bytes off a word), the top bits spread into the code bytes
-//     with shifts and masks, 32 dp4a; the offset 32 is applied once per half
-//     through the code sum (s = sum c a - 32 sum a, exact in int32);
-//   - fp32 partial sums per lane, one warp-shuffle reduction per row.
+//     with shifts and masks once, 32 dp4a per staged vector; the offset 32 is
+//     applied once per half through the code sum (s = sum c a - 32 sum a,
+//     exact in int32);
+//   - fp32 partial sums per lane and vector, one warp-shuffle reduction per
+//     row and vector.  14336 x 4096 at batch 1 / 2 / 4 / 8: 12.1 / 13.5 /
+//     17.3 / 24.9 us (one vector per pass: 12.1 / 22.2 / 42.4 / 80.3).
 // Rows whose byte length is not a multiple of 16 (cols not a multiple of
 // 2048), or too long for a two-stage ring, take a plain warp-per-row kernel
 // with byte loads from global memory.
@@ -117,11 +122,6 @@ __global__ void dequantize_q6_k_kernel(const uint8_t *__restrict__ src, float *_
 
 // ------------------------------------------------------------------- GEMV
 
-// Warps per CTA of the streaming kernel: the widest of GQ_Q6K_MAX_WARPS, 16
-// and 8 whose rings (two stages or more) fit.
-#ifndef GQ_Q6K_MAX_WARPS
-#define GQ_Q6K_MAX_WARPS 16
-#endif
 // Independent dp4a accumulator chains per lane (1 or 2).
 #ifndef GQ_Q6K_CHAINS
 #define GQ_Q6K_CHAINS 1
@@ -135,6 +135,8 @@ __host__ __device__ constexpr int bars_bytes(int nw) { return nw * MAX_NS * 8; }
 __host__ __device__ constexpr size_t act_smem_bytes(int nblk) {
     return (size_t)nblk * 256 + (size_t)nblk * 2 * 4 + (size_t)nblk * 4;
 }
+// Staged vectors follow one another at this stride (16-byte aligned).
+__host__ __device__ constexpr size_t act_stride(int nblk) { return (act_smem_bytes(nblk) + 15) / 16 * 16; }
 
 // Split-order words of 8 codes: (a0 a2 a4 a6) and (a1 a3 a5 a7).
 __device__ __forceinline__ uint2 split8(uint32_t w0, uint32_t w1) {
@@ -171,11 +173,14 @@ __device__ __forceinline__ uint32_t spread_top(uint32_t t) {
     return x << 4;
 }
 
-// Integer sum of half block h of the block at `blk` (shared memory, 2-byte
+// Integer sums of half block h of the block at `blk` (shared memory, 2-byte
 // aligned, at least 4 readable bytes past its end) against the staged codes
-// of half-block hb: sum_i c_i a_i over the 128 elements (offset not applied).
-__device__ __forceinline__ int half_dot(const uint8_t *stage, uint32_t blk_off, int h, const uint8_t *act,
-                                        int hb) {
+// of half-block hb of NV vectors (vector v at act + v * astride):
+// sum_i c_i a_i over the 128 elements (offset not applied).  The 6-bit code
+// words are built once and serve every vector.
+template <int NV>
+__device__ __forceinline__ void half_dot(const uint8_t *stage, uint32_t blk_off, int h, const uint8_t *act,
+                                         size_t astride, int hb, int (&out)[NV]) {
     const uint32_t offa = blk_off + 2 + 64 * h;    // low-nibble bytes of the half
     const uint32_t offb = blk_off + 130 + 32 * h;  // top-bit bytes of the half
     const uint32_t *wa = reinterpret_cast<const uint32_t *>(stage + (offa & ~3u));
@@ -188,40 +193,53 @@ __device__ __forceinline__ int half_dot(const uint8_t *stage, uint32_t blk_off, 
     for (int i = 0; i < 9; ++i) vb[i] = wb[i];
     const uint8_t *ah = act + (size_t)hb * 128;
     const int sw = hb & 7;
-    int s = 0, s2 = 0;
+    int s[NV], s2[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) s[v] = s2[v] = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        const uint4 a = *reinterpret_cast<const uint4 *>(ah + ((u ^ sw) << 4));
         const uint32_t top = __funnelshift_rc(vb[u], vb[u + 1], shb);  // top bits of elements 16u..16u+15
+        uint32_t ca[2], cb[2];
 #pragma unroll
         for (int g2 = 0; g2 < 2; ++g2) {
             const int g = 2 * u + g2;
             const uint32_t w = __funnelshift_rc(va[g], va[g + 1], sha);  // low nibbles of elements 8g..8g+7
             const uint32_t t = g2 ? (top >> 16) : (top & 0xffffu);
-            const uint32_t ca = (w & NIB) | spread_top(t & 0x3333u);          // elements 0, 2, 4, 6
-            const uint32_t cb = ((w >> 4) & NIB) | spread_top((t >> 2) & 0x3333u);  // elements 1, 3, 5, 7
-            s = dp4a((int)ca, (int)(g2 ? a.z : a.x), s);
-            if (GQ_Q6K_CHAINS == 2)
-                s2 = dp4a((int)cb, (int)(g2 ? a.w : a.y), s2);
-            else
-                s = dp4a((int)cb, (int)(g2 ? a.w : a.y), s);
+            ca[g2] = (w & NIB) | spread_top(t & 0x3333u);                // elements 0, 2, 4, 6
+            cb[g2] = ((w >> 4) & NIB) | spread_top((t >> 2) & 0x3333u);  // elements 1, 3, 5, 7
+        }
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(ah + (size_t)v * astride + ((u ^ sw) << 4));
+            s[v] = dp4a((int)ca[0], (int)a.x, s[v]);
+            s[v] = dp4a((int)ca[1], (int)a.z, s[v]);
+            if (GQ_Q6K_CHAINS == 2) {
+                s2[v] = dp4a((int)cb[0], (int)a.y, s2[v]);
+                s2[v] = dp4a((int)cb[1], (int)a.w, s2[v]);
+            } else {
+                s[v] = dp4a((int)cb[0], (int)a.y, s[v]);
+                s[v] = dp4a((int)cb[1], (int)a.w, s[v]);
+            }
         }
     }
-    return s + s2;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) out[v] = s[v] + s2[v];
 }
 
 // Streaming kernel: cols a multiple of 2048 (rows are 16-byte multiples);
-// one activation vector per blockIdx.y.  SUMS: write the int32 block sums
-// instead of y.
-template <bool SUMS, int GW, bool FUSED>
+// NV activation vectors per blockIdx.y (vectors NV y .. NV y + NV - 1 of the
+// nvec in this launch), so W streams once per NV vectors.  SUMS: write the
+// int32 block sums instead of y.
+template <bool SUMS, int GW, bool FUSED, int NV>
 __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__restrict__ W,
                                                              const void *__restrict__ act_in,
                                                              float *__restrict__ y, int32_t *__restrict__ sums,
-                                                             int rows, int nblk, int ns, int stage_bytes,
+                                                             int rows, int nblk, int ns, int stage_bytes, int nvec,
                                                              int w_static, uint32_t *__restrict__ status) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.y;
+    const int b0 = blockIdx.y * NV, nv = min(NV, nvec - b0);
+    const size_t astride = act_stride(nblk);
     const int warps_total = gridDim.x * GW;
     const int wg = blockIdx.x * GW + warp;
     const int total = wg < rows ? (rows - 1 - wg) / warps_total + 1 : 0;
@@ -249,14 +267,18 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__r
     pdl_wait();  // xq (and, unless static, W) may come from the preceding kernel in the stream
     if (lane == 0 && !w_static)
         for (int i = 0; i < ns && i < total; ++i) issue(i, i);
-    if (FUSED)  // fp32 activations, quantized to Q8_K here exactly as by the codec
-        q8::stage_q8_k_from_f32<2>(act, static_cast<const float *>(act_in) + (size_t)b * nblk * QK_K, nblk);
-    else
-        stage_q8_k_vec(act, static_cast<const uint8_t *>(act_in) + (size_t)b * nblk * Q8_K_BYTES, nblk);
+    for (int v = 0; v < nv; ++v) {
+        const size_t b = (size_t)(b0 + v);
+        if (FUSED)  // fp32 activations, quantized to Q8_K here exactly as by the codec
+            q8::stage_q8_k_from_f32<2>(act + v * astride, static_cast<const float *>(act_in) + b * nblk * QK_K,
+                                       nblk);
+        else
+            stage_q8_k_vec(act + v * astride, static_cast<const uint8_t *>(act_in) + b * nblk * Q8_K_BYTES, nblk);
+    }
     __syncthreads();
 
-    const int32_t *asum = reinterpret_cast<const int32_t *>(act + (size_t)nblk * 256);
-    const float *dx = reinterpret_cast<const float *>(asum + 2 * nblk);
+    // within a staged vector: the half-block code sums, then the scales
+    const size_t asum_off = (size_t)nblk * 256, dx_off = asum_off + (size_t)nblk * 2 * 4;
     const int iters = (2 * nblk + 31) / 32;
     int st = 0;
     uint32_t ph = 0;
@@ -278,27 +300,40 @@ __global__ void __launch_bounds__(GW * 32, 1) gemv_q6k_kernel(const uint8_t *__r
         }
         const int row = wg + i * warps_total;
         const uint8_t *stage = ring + (size_t)st * stage_bytes;
-        float acc = 0.0f;
+        float acc[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[v] = 0.0f;
         for (int t = 0; t < iters; ++t) {
             const int hb = lane + 32 * t;
-            int s = 0;
+            int s[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) s[v] = 0;
             if (hb < 2 * nblk) {
                 const int k = hb >> 1;
-                s = half_dot(stage, (uint32_t)k * Q6_K_BYTES, hb & 1, act, hb) - 32 * asum[hb];
-                if (!SUMS) {
-                    const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t *>(stage + k * Q6_K_BYTES));
-                    acc += dw * dx[k] * (float)s;
+                half_dot<NV>(stage, (uint32_t)k * Q6_K_BYTES, hb & 1, act, astride, hb, s);
+                const float dw = half_bits_to_float(*reinterpret_cast<const uint16_t *>(stage + k * Q6_K_BYTES));
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const uint8_t *av = act + v * astride;
+                    s[v] -= 32 * reinterpret_cast<const int32_t *>(av + asum_off)[hb];
+                    if (!SUMS) acc[v] += dw * reinterpret_cast<const float *>(av + dx_off)[k] * (float)s[v];
                 }
             }
             if (SUMS) {
-                const int both = s + __shfl_xor_sync(FULL, s, 1);  // the two halves of block hb / 2
-                if (hb < 2 * nblk && (hb & 1) == 0)
-                    sums[((size_t)b * rows + row) * nblk + (hb >> 1)] = both;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const int both = s[v] + __shfl_xor_sync(FULL, s[v], 1);  // the two halves of block hb / 2
+                    if (v < nv && hb < 2 * nblk && (hb & 1) == 0)
+                        sums[((size_t)(b0 + v) * rows + row) * nblk + (hb >> 1)] = both;
+                }
             }
         }
         if (!SUMS) {
-            acc = warp_sum(acc);
-            if (lane == 0) y[(size_t)b * rows + row] = acc;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const float a = warp_sum(acc[v]);
+                if (lane == 0 && v < nv) y[(size_t)(b0 + v) * rows + row] = a;
+            }
         }
         __syncwarp();
         if (lane == 0 && i + ns < total) issue(i + ns, st);
@@ -360,29 +395,57 @@ __global__ void __launch_bounds__(PW * 32) gemv_q6k_plain_kernel(const uint8_t *
 constexpr int SMEM_LIMIT = 232448;  // opt-in shared memory per CTA on sm_103
 constexpr int64_t Y_MAX = 65535;    // vectors per launch (grid.y)
 
-size_t stream_smem(int nw, int ns, int nblk) {
-    return bars_bytes(nw) + (size_t)nw * ns * ((size_t)nblk * Q6_K_BYTES + 16) + act_smem_bytes(nblk);
+size_t stream_smem(int nw, int ns, int nblk, int nv) {
+    return bars_bytes(nw) + (size_t)nw * ns * ((size_t)nblk * Q6_K_BYTES + 16) + (size_t)nv * act_stride(nblk);
 }
 
 // Ring stages per warp for the streaming kernel with nw warps: as many as fit
-// (2..4) next to the staged vector; 0 when rows are not 16-byte multiples or
+// (2..4) next to nv staged vectors; 0 when rows are not 16-byte multiples or
 // two stages do not fit.
-int pick_ns(int nw, int nblk) {
+int pick_ns(int nw, int nblk, int nv) {
     if (nblk % 8 != 0) return 0;
     for (int ns = MAX_NS; ns >= 2; --ns)
-        if (stream_smem(nw, ns, nblk) <= (size_t)SMEM_LIMIT) return ns;
+        if (stream_smem(nw, ns, nblk, nv) <= (size_t)SMEM_LIMIT) return ns;
     return 0;
 }
 
-template <bool SUMS, int NW, bool FUSED>
+// Launch shape of the streaming kernel for a batch: nv vectors per CTA (the
+// smallest of 1, 2, 4, 8 that covers the batch, fewer when their staged
+// copies leave no room for a two-stage ring), 16 warps when sixteen rings fit,
+// else 8, and the ring depth.  ns == 0: the streaming kernel does not apply.
+struct Shape {
+    int nv, nw, ns;
+};
+Shape pick_shape(int nblk, int64_t batch) {
+    int nv = batch >= 8 ? 8 : batch >= 4 ? (batch > 4 ? 8 : 4) : batch >= 2 ? (batch > 2 ? 4 : 2) : 1;
+    for (; nv >= 1; nv >>= 1) {
+        if (int ns = pick_ns(16, nblk, nv)) return {nv, 16, ns};
+        if (int ns = pick_ns(8, nblk, nv)) return {nv, 8, ns};
+    }
+    return {1, 8, 0};
+}
+
+template <bool SUMS, int NW, bool FUSED, int NV>
 cudaError_t launch_stream(const uint8_t *W, const void *xb, float *yb, int32_t *sb, int64_t rows, int nblk,
                           int nb, int ns, int w_static, const LaunchCtx &ctx) {
-    auto k = gemv_q6k_kernel<SUMS, NW, FUSED>;
+    auto k = gemv_q6k_kernel<SUMS, NW, FUSED, NV>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
     if (e != cudaSuccess) return e;
     const int64_t gx = std::min<int64_t>(ctx.num_sms, (rows + NW - 1) / NW);
-    return launch_pdl(k, dim3((unsigned)gx, nb), dim3(NW * 32), stream_smem(NW, ns, nblk), ctx.stream, W, xb,
-                      yb, sb, (int)rows, nblk, ns, nblk * Q6_K_BYTES + 16, w_static, ctx.status);
+    return launch_pdl(k, dim3((unsigned)gx, (nb + NV - 1) / NV), dim3(NW * 32), stream_smem(NW, ns, nblk, NV),
+                      ctx.stream, W, xb, yb, sb, (int)rows, nblk, ns, nblk * Q6_K_BYTES + 16, nb, w_static,
+                      ctx.status);
+}
+
+template <bool SUMS, bool FUSED, int NW>
+cudaError_t launch_nv(const Shape &sh, const uint8_t *W, const void *xb, float *yb, int32_t *sb, int64_t rows,
+                      int nblk, int nb, int w_static, const LaunchCtx &ctx) {
+    switch (sh.nv) {
+    case 8: return launch_stream<SUMS, NW, FUSED, 8>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    case 4: return launch_stream<SUMS, NW, FUSED, 4>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    case 2: return launch_stream<SUMS, NW, FUSED, 2>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    default: return launch_stream<SUMS, NW, FUSED, 1>(W, xb, yb, sb, rows, nblk, nb, sh.ns, w_static, ctx);
+    }
 }
 
 int codec_grid(int64_t items, int per_cta, int num_sms) {
@@ -395,23 +458,19 @@ template <bool SUMS, bool FUSED>
 cudaError_t run_gemv(const uint8_t *W, const void *act, float *y, int32_t *sums, int64_t rows, int64_t cols,
                      int64_t batch, int w_static, const LaunchCtx &ctx) {
     const int nblk = (int)(cols / QK_K);
-    // the widest instantiation whose rings fit: GQ_Q6K_MAX_WARPS, 16 or 8 warps
-    int nw = GQ_Q6K_MAX_WARPS, ns = pick_ns(nw, nblk);
-    if (!ns && nw > 16) ns = pick_ns(nw = 16, nblk);
-    if (!ns && nw > 8) ns = pick_ns(nw = 8, nblk);
-    for (int64_t b0 = 0; b0 < batch; b0 += Y_MAX) {
-        const int nb = (int)std::min<int64_t>(Y_MAX, batch - b0);
+    const Shape sh = pick_shape(nblk, batch);
+    const int64_t per_launch = sh.ns ? Y_MAX * sh.nv : Y_MAX;
+    for (int64_t b0 = 0; b0 < batch; b0 += per_launch) {
+        const int nb = (int)std::min<int64_t>(per_launch, batch - b0);
         const void *xb = FUSED ? static_cast<const void *>(static_cast<const float *>(act) + b0 * cols)
                                : static_cast<const void *>(static_cast<const uint8_t *>(act) + b0 * nblk * Q8_K_BYTES);
         float *yb = SUMS ? nullptr : y + b0 * rows;
         int32_t *sb = SUMS ? sums + b0 * rows * nblk : nullptr;
         cudaError_t e;
-        if (ns && nw == GQ_Q6K_MAX_WARPS) {
-            e = launch_stream<SUMS, GQ_Q6K_MAX_WARPS, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
-        } else if (ns && nw == 16) {
-            e = launch_stream<SUMS, 16, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
-        } else if (ns) {
-            e = launch_stream<SUMS, 8, FUSED>(W, xb, yb, sb, rows, nblk, nb, ns, w_static, ctx);
+        if (sh.ns && sh.nw == 16) {
+            e = launch_nv<SUMS, FUSED, 16>(sh, W, xb, yb, sb, rows, nblk, nb, w_static, ctx);
+        } else if (sh.ns) {
+            e = launch_nv<SUMS, FUSED, 8>(sh, W, xb, yb, sb, rows, nblk, nb, w_static, ctx);
         } else {
             if (FUSED) return cudaErrorInvalidValue;  // one vector does not fit the streaming kernel
             const int64_t gx = (rows + PW - 1) / PW;
@@ -440,8 +499,7 @@ cudaError_t launch_dequantize_q6k(const void *src, float *dst, int64_t n, const 
 // streaming kernel next to a two-stage ring.
 bool gemv_q6k_fused_fits(int64_t cols) {
     if (cols < 0 || cols % QK_K != 0 || cols > (int64_t)1 << 20) return false;
-    const int nblk = (int)(cols / QK_K);
-    return pick_ns(16, nblk) > 0 || pick_ns(8, nblk) > 0;
+    return pick_shape((int)(cols / QK_K), 1).ns > 0;
 }
 
 cudaError_t launch_gemv_q6k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,

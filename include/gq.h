@@ -226,10 +226,11 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *           cols a multiple of 256 for Q4_K / Q5_K / Q6_K and of 32 for Q4_0 / Q8_0
  *           (the fast kernels need cols % 256 == 0, and cols % 2048 == 0 up
  *           to 16384 for Q6_K; other shapes run a plain per-block kernel);
- *           Q5_K and Q6_K run one pass over W per activation vector; cols at most
- *           131072 (and small
- *           enough for one activation vector to fit the kernels' shared
- *           memory: every cols up to that bound does).
+ *           Q5_K and Q6_K run one pass over W per group of up to eight
+ *           activation vectors (fewer when wide vectors fill the shared
+ *           memory); cols at most 131072 (and small enough for one
+ *           activation vector to fit the kernels' shared memory: every cols
+ *           up to that bound does).
  * The integer block sums are exact (int32); y matches the double-precision
  * sum of the same terms within 1e-4 of the sum of their magnitudes.
  * Asynchronous on `stream`; allocates nothing.

@@ -117,6 +117,28 @@ def test_gemv_block_sums_and_y(rows, cols, batch):
     assert_close(host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch)), y_ref, T)
 
 
+# Several vectors per CTA (W streamed once per group of up to eight): group
+# sizes 2, 4 and 8, ragged last groups, and more groups than one launch row.
+@pytest.mark.parametrize("rows,cols,batch", [(130, 4096, 2), (300, 2048, 3), (77, 4096, 8), (64, 1024, 9),
+                                             (200, 8192, 17), (33, 18432, 6)])
+def test_gemv_vector_groups(rows, cols, batch):
+    g = inputs.rng(rows * 11 + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = host(gq.block_sums(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    np.testing.assert_array_equal(s, orc.block_sums(Q5_K, Wq, Xq, rows, cols, batch))
+    y = host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch))
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+    # each vector's y equals its own single-vector product within the bar
+    for b in (0, batch - 1):
+        y1 = host(gq.matmul(Q5_K, Wd, Xd[b:b + 1], rows, cols, 1))
+        assert_close(y[b:b + 1], y_ref[b:b + 1], T[b:b + 1])
+        assert_close(y1, y_ref[b:b + 1], T[b:b + 1])
+
+
 # More rows than the grid has warps: each warp streams several rows through
 # its ring (stage reuse, barrier phase flips), with a ragged last pass.
 TALL_SHAPES = [(4867, 4096, 1), (2435, 8192, 2), (1300, 16384, 1), (3000, 11008, 1)]
@@ -193,7 +215,7 @@ def test_static_weights_flag_same_result():
 # ------------------------------------------- fused activation quantize path
 
 FUSED_SHAPES = [(1, 256, 1), (7, 2048, 1), (130, 4096, 2), (33, 768, 5), (19, 2816, 3),
-                (64, 11008, 1), (4867, 4096, 1), (5, 18944, 2)]
+                (64, 11008, 1), (4867, 4096, 1), (5, 18944, 2), (40, 4096, 8), (21, 2048, 11)]
 
 
 @pytest.mark.parametrize("rows,cols,batch", FUSED_SHAPES)

@@ -113,6 +113,27 @@ def test_gemv_block_sums_and_y(rows, cols, batch):
 
 # More rows than the grid has warps: each warp streams several rows through
 # its ring (stage reuse, barrier phase flips), with a ragged last pass.
+# Several vectors per CTA (W streamed once per group of up to eight): group
+# sizes 2, 4 and 8, ragged last groups, more groups than one launch row, and
+# a width where only one staged vector fits next to the ring.
+@pytest.mark.parametrize("rows,cols,batch", [(130, 4096, 2), (300, 2048, 3), (77, 4096, 8), (64, 2048, 9),
+                                             (200, 8192, 17), (33, 16384, 6)])
+def test_gemv_vector_groups(rows, cols, batch):
+    g = inputs.rng(rows * 11 + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q6_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = host(gq.block_sums(Q6_K, Wd, Xd, rows, cols, batch, gq.PATH_GEMV))
+    np.testing.assert_array_equal(s, orc.block_sums(Q6_K, Wq, Xq, rows, cols, batch))
+    y = host(gq.matmul(Q6_K, Wd, Xd, rows, cols, batch))
+    y_ref, T = orc.matmul_ref(Q6_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+    for b in (0, batch - 1):
+        y1 = host(gq.matmul(Q6_K, Wd, Xd[b:b + 1], rows, cols, 1))
+        assert_close(y1, y_ref[b:b + 1], T[b:b + 1])
+
+
 TALL_SHAPES = [(4867, 4096, 1), (2435, 8192, 2), (1300, 16384, 1)]
 
 
@@ -181,7 +202,7 @@ def test_static_weights_flag_same_result():
 # ------------------------------------------- fused activation quantize path
 
 FUSED_SHAPES = [(1, 2048, 1), (7, 2048, 3), (130, 4096, 2), (33, 6144, 5), (4867, 4096, 1),
-                (9, 16384, 2)]
+                (9, 16384, 2), (40, 4096, 8), (21, 2048, 11)]
 
 
 @pytest.mark.parametrize("rows,cols,batch", FUSED_SHAPES)
