@@ -655,6 +655,11 @@ def summary_keys(line: dict) -> dict:
     for t in ("q4_0", "q8_0"):
         out[f"prefill_{t}_tops"] = r(get(line, "q0_gemm", t, "prefill_28672x8192x512", "mma", "tops"), 1)
         out[f"prefill_{t}_frac"] = r(get(line, "q0_gemm", t, "prefill_28672x8192x512", "mma", "roofline", "frac"))
+        sw0 = get(line, "q0_gemm", t, "sweep_14336x4096")
+        if isinstance(sw0, dict):
+            out[f"sweep_{t}_us_gemv_mma_skinny"] = {
+                b: [r(get(v, "gemv", "us"), 1), r(get(v, "mma", "us"), 1), r(get(v, "skinny", "us"), 1)]
+                for b, v in sw0.items()}
     out["q6k_frac"] = r(get(line, "q6k", "frac"))
     out["q5k_frac"] = r(get(line, "q5k", "frac"))
     out["q5k_stream_frac"] = r(get(line, "q5k", "streaming", "frac"))
@@ -998,8 +1003,9 @@ def bench_prefill(gq, inputs, torch, np, dev, s, capture, time_graph, bf16_peak)
 def bench_q0_gemm(gq, inputs, torch, np, dev, capture, time_graph, bf16_peak):
     """Q4_0 / Q8_0 weights x Q8_0 columns on the tensor-core kernel that
     needs no workspace (what gq_matmul runs from batch 16): the prefill shape
-    28672x8192 x 512 against the GEMV, and 14336x4096 at batch 8..64 (weights
-    rotated over copies larger than L2) against the GEMV."""
+    28672x8192 x 512 against the GEMV, and 14336x4096 at batch 4..64 (weights
+    rotated over copies larger than L2) against the GEMV and the warp-level
+    kernel."""
     out = {}
     big = inputs.gemm_q4_k(0, 28672, 8192, 512)
     mid = inputs.gemm_q4_k(0, 14336, 4096, 64)
@@ -1027,16 +1033,18 @@ def bench_q0_gemm(gq, inputs, torch, np, dev, capture, time_graph, bf16_peak):
         Xq = gq.quantize(gq.Q8_0, torch.from_numpy(mid[1]).to(dev))
         Y = torch.empty(64, rows, dtype=torch.float32, device=dev)
         sweep = {}
-        for b in (8, 16, 32, 64):
+        for b in (4, 8, 16, 32, 64):
             r = {}
-            for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA)):
+            for pname, path in (("gemv", gq.PATH_GEMV), ("mma", gq.PATH_MMA), ("skinny", gq.PATH_SKINNY)):
                 def body():
                     for i in range(copies):
-                        gq.gq_matmul_path(wt, Wc[i], Xq, Y, rows, cols, b, path)
+                        gq.gq_matmul_ex(wt, Wc[i], Xq, Y, rows, cols, b, path, gq.FLAG_W_STATIC)
                 t, _ = time_graph(capture(body), 10, 3)
                 per = t / (10 * copies)
                 r[pname] = {"us": per * 1e6, "weight_gbps": Wq.numel() / per / 1e9}
-            r["faster"] = min(("gemv", "mma"), key=lambda k: r[k]["us"])
+                if pname == "skinny" and b == 16 and name == "q4_0":
+                    r[pname]["traffic"] = kernel_traffic("skinny_q0_q4_0_b16")
+            r["faster"] = min(("gemv", "mma", "skinny"), key=lambda k: r[k]["us"])
             sweep[str(b)] = r
         del Wc, Wq, Xq, Y
         torch.cuda.empty_cache()

@@ -23,9 +23,9 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE
           "--expt-relaxed-constexpr"]
 # The codecs must reproduce the reference bit for bit: no FMA contraction.
 PER_FILE = {"gq_codec.cu": ["-fmad=false"], "gq_q6k.cu": ["-fmad=false"]}
-SOURCES = ["gq_api.cu", "gq_codec.cu", "gq_gemv.cu", "gq_mma.cu", "gq_mma_q0.cu", "gq_skinny.cu", "gq_kv.cu",
-           "gq_q6k.cu", "gq_q5k.cu"]
-HEADERS = ["gq_common.cuh", "gq_internal.h", "gq_quant8.cuh", "gq_tc.cuh"]
+SOURCES = ["gq_api.cu", "gq_codec.cu", "gq_gemv.cu", "gq_mma.cu", "gq_mma_q0.cu", "gq_skinny.cu", "gq_skinny_q0.cu",
+           "gq_kv.cu", "gq_q6k.cu", "gq_q5k.cu"]
+HEADERS = ["gq_common.cuh", "gq_internal.h", "gq_mma_sync.cuh", "gq_quant8.cuh", "gq_tc.cuh"]
 
 
 def nvcc() -> str:

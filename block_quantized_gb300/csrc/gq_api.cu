@@ -160,6 +160,17 @@ bool skinny_auto(int64_t rows, int64_t batch, bool tc_ready) {
     return batch <= 32 || !tc_ready;
 }
 
+// The warp-level kernel for Q4_0 / Q8_0 weights (gq_skinny_q0.cu).
+// Measured on 14336 x 4096 (Q4_0 / Q8_0): 13.8 / 17.3 us at batch 4 against
+// the GEMV's 25.0 / 27.1, and 18.7 / 22.2, 30.8 / 34.6, 56.4 / 59.5 us at
+// batch 16, 32, 64 against the tcgen05 kernel's 53-61.  So: batch 4..64 on
+// matrices of 8192 rows or more; beyond 64 (two or more chunks) the tcgen05
+// kernel.  Not taken when GQ_TC_MIN_BATCH sets a plain threshold.
+bool skinny_auto_q0(int64_t rows, int64_t batch) {
+    if (tc_min_batch_env() || rows < 8192 || batch < 4) return false;
+    return batch <= 64;
+}
+
 // The same choice for Q4_0 / Q8_0 weights (gq_mma_q0.cu).
 bool tc_auto_q0(int64_t rows, int64_t batch) {
     (void)rows;
@@ -203,16 +214,19 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         }
     }
     if (path == GQ_PATH_SKINNY) {
-        if (wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+        if (!q0 && wtype != GQ_Q4_K) return GQ_ERR_TYPE;
         if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
-        if (!skinny_supported(rows, cols, std::min<int64_t>(batch, 64))) return GQ_ERR_SHAPE;
+        if (q0 ? !skinny_q0_supported(rows, cols, std::min<int64_t>(batch, 64))
+               : !skinny_supported(rows, cols, std::min<int64_t>(batch, 64)))
+            return GQ_ERR_SHAPE;
     }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
     bool use_mma = path == GQ_PATH_MMA;
     bool use_skinny = path == GQ_PATH_SKINNY;
     if (path == GQ_PATH_AUTO && !fused_f32) {
         if (q0) {
-            use_mma = tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch);
+            use_skinny = skinny_q0_supported(rows, cols, std::min<int64_t>(batch, 64)) && skinny_auto_q0(rows, batch);
+            use_mma = !use_skinny && tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch);
         } else if (wtype == GQ_Q4_K) {
             const bool tc_ready = mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
@@ -229,12 +243,17 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     if (use_skinny) {
         // chunks of up to 64 activation vectors, one launch each (y, sums and
         // xq advance by whole vectors)
-        const int64_t nsb = cols / 256;
+        const bool ws_static = (flags & GQ_FLAG_W_STATIC) != 0;
+        const int64_t nblk = cols / block_elems(wtype);          // weight blocks per row
+        const int64_t xbytes = q0 ? cols / 32 * Q8_0_BYTES : cols / 256 * Q8_K_BYTES;  // one activation vector
+        const int64_t per_row_sums = q0 ? nblk : nblk * 2;       // int32 sums per (vector, row)
         for (int64_t b0 = 0; b0 < batch; b0 += 64) {
             const int64_t nb = std::min<int64_t>(64, batch - b0);
-            cudaError_t e = launch_skinny_q4k(W, static_cast<const uint8_t *>(act) + b0 * nsb * 276,
-                                              y ? y + b0 * rows : nullptr, sums ? sums + b0 * rows * nsb * 2 : nullptr,
-                                              rows, cols, nb, (flags & GQ_FLAG_W_STATIC) != 0, ctx);
+            const uint8_t *xb = static_cast<const uint8_t *>(act) + b0 * xbytes;
+            float *yb = y ? y + b0 * rows : nullptr;
+            int32_t *sb = sums ? sums + b0 * rows * per_row_sums : nullptr;
+            cudaError_t e = q0 ? launch_skinny_q0(wtype, W, xb, yb, sb, rows, cols, nb, ws_static, ctx)
+                               : launch_skinny_q4k(W, xb, yb, sb, rows, cols, nb, ws_static, ctx);
             if (e != cudaSuccess) return cuda_fail(e);
         }
         return GQ_OK;

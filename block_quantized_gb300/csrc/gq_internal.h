@@ -100,6 +100,12 @@ bool mma_q0_supported(int64_t rows, int64_t cols, int64_t batch);
 cudaError_t launch_skinny_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
                               int64_t batch, bool w_static, const LaunchCtx &ctx);
 bool skinny_supported(int64_t rows, int64_t cols, int64_t batch);
+// The same for Q4_0 / Q8_0 weights x Q8_0 activations (gq_skinny_q0.cu):
+// batch <= 64, cols a multiple of 256, no workspace, int32 sums one per
+// 32-element block.
+cudaError_t launch_skinny_q0(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
+                             int64_t cols, int64_t batch, bool w_static, const LaunchCtx &ctx);
+bool skinny_q0_supported(int64_t rows, int64_t cols, int64_t batch);
 // The library's static scratch (no allocation): its size, and its device
 // address on `device` (looked up on the first call for that device, which
 // must be the current device).

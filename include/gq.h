@@ -135,7 +135,7 @@ typedef enum {
     GQ_PATH_AUTO = 0,   /* GEMV below the tensor-core crossover batch, MMA at or above */
     GQ_PATH_GEMV = 1,   /* dp4a GEMV kernels (any batch; batch is processed in chunks) */
     GQ_PATH_MMA = 2,    /* tcgen05 tensor-core kernels (Q4_0, Q8_0, Q4_K weights) */
-    GQ_PATH_SKINNY = 3  /* warp-level tensor-core kernel (mma.sync) for Q4_K, 64 columns per launch */
+    GQ_PATH_SKINNY = 3  /* warp-level tensor-core kernels (mma.sync) for Q4_K, Q4_0, Q8_0; 64 columns per launch */
 } gq_path;
 
 /* Elements per block: 32, 32, 256, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K,
@@ -235,11 +235,12 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  * sum of the same terms within 1e-4 of the sum of their magnitudes.
  * Asynchronous on `stream`; allocates nothing.
  * Dispatch (GQ_PATH_AUTO):
- *   Q4_0 / Q8_0 weights: the tcgen05 tensor-core kernel when cols % 256 == 0
- *     and batch >= gq_tc_min_batch() (16 unless GQ_TC_MIN_BATCH is set; the
- *     measured crossover on 14336 x 4096 lies between 8 and 16), the GEMV
- *     kernels otherwise.  That kernel converts both operands in shared and
- *     tensor memory and needs no workspace.
+ *   Q4_0 / Q8_0 weights (cols % 256 == 0): the warp-level tensor-core kernel
+ *     (GQ_PATH_SKINNY) at batch 4..64 on matrices of 8192 rows or more; the
+ *     tcgen05 tensor-core kernel at batch >= gq_tc_min_batch() otherwise (16
+ *     unless GQ_TC_MIN_BATCH is set, which also turns the warp-level choice
+ *     off); the GEMV kernels below.  Neither tensor-core kernel needs a
+ *     workspace.
  *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
  *     workspace; batches beyond 64 as 64-column chunks) from batch 4 on
  *     matrices of 8192 rows or more, the GEMV kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
@@ -258,10 +259,11 @@ gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
  * kernel of Q4_0 / Q8_0 weights (GQ_ERR_SHAPE unless cols % 256 == 0); for
  * Q4_K weights it returns GQ_ERR_NULL (that kernel needs the workspace of
  * gq_matmul_ws), for Q5_K / Q6_K GQ_ERR_TYPE.  GQ_PATH_SKINNY runs the
- * warp-level tensor-core kernel of Q4_K weights (mma.sync m16n8k16 on the
- * same exact integer operands as the tcgen05 kernel; one launch per 64
- * activation vectors; cols % 256 == 0, GQ_ERR_SHAPE otherwise; GQ_ERR_TYPE
- * for the other weight types and for fp32 activations). */
+ * warp-level tensor-core kernels of Q4_K, Q4_0 and Q8_0 weights (mma.sync
+ * m16n8k16 on exact integer operands, one fresh accumulator per 32-element
+ * block for Q4_0 / Q8_0; one launch per 64 activation vectors; cols % 256 ==
+ * 0, GQ_ERR_SHAPE otherwise; GQ_ERR_TYPE for Q5_K / Q6_K and for fp32
+ * activations). */
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
                          int64_t rows, int64_t cols, int64_t batch, gq_path path,
                          gq_stream_t stream);
