@@ -148,27 +148,35 @@ bool tc_auto(int64_t rows, int64_t batch) {
 }
 
 // GQ_PATH_AUTO's choice of the warp-level tensor-core kernel for Q4_K
-// (gq_skinny.cu).  Measured on 14336 x 4096 (150 CTAs of 96 rows): 13 us at
-// batch 4..8 against the GEMV's 14..23 (the GEMV wins below, 9.4 us at
-// batch 2), 13..17 us at 9..16 and 23 us at 32 against the tcgen05 kernel's
-// 25.3..26.2, 40 us at 64 against its 30 and the GEMV's 173.  So: batch 4..32
-// on matrices of 8192 rows or more (enough row tiles to fill the GPU), and
-// every batch from 4 when no workspace lets the tcgen05 kernel run.  Not taken
-// when GQ_TC_MIN_BATCH sets a plain threshold.
+// (gq_skinny.cu).  Measured on 14336 x 4096 (150 CTAs of 96 rows): 12.1 us
+// at batch 4 against the GEMV's 14.0 (the GEMV wins below: 11.7 us at batch
+// 3), 12.5..15.7 us at 8..16 and 22 us at 32 against the tcgen05 kernel's
+// 25.3..26.2, 39 us at 64 against its 30 and the GEMV's 173.  On 4096 x 4096
+// (43 CTAs): 14.2 / 20.7 us at batch 16 / 32 against the GEMV's 19.6 / 38.1
+// and the tcgen05 kernel's 24.4 / 24.9 (the GEMV wins at 8: 10.2 vs 11.3).
+// So: from batch 4 on matrices of 8192 rows or more, from 16 on 2048 or more,
+// up to 32 when a workspace lets the tcgen05 kernel take the larger batches,
+// at every such batch otherwise.  Not taken when GQ_TC_MIN_BATCH sets a plain
+// threshold.
 bool skinny_auto(int64_t rows, int64_t batch, bool tc_ready) {
-    if (tc_min_batch_env() || rows < 8192 || batch < 4) return false;
+    if (tc_min_batch_env() || rows < 2048) return false;
+    if (batch < (rows >= 8192 ? 4 : 16)) return false;
     return batch <= 32 || !tc_ready;
 }
 
 // The warp-level kernel for Q4_0 / Q8_0 weights (gq_skinny_q0.cu).
-// Measured on 14336 x 4096 (Q4_0 / Q8_0): 13.8 / 17.3 us at batch 4 against
-// the GEMV's 25.0 / 27.1, and 18.7 / 22.2, 30.8 / 34.6, 56.4 / 59.5 us at
-// batch 16, 32, 64 against the tcgen05 kernel's 53-61.  So: batch 4..64 on
-// matrices of 8192 rows or more; beyond 64 (two or more chunks) the tcgen05
-// kernel.  Not taken when GQ_TC_MIN_BATCH sets a plain threshold.
+// Measured on 14336 x 4096 (Q4_0 / Q8_0): 13.6 / 16.9 us at batch 2 against
+// the GEMV's 15.5 / 18.1 (the GEMV wins at batch 1: 11.0 / 14.0), 18.8 /
+// 22.1, 30.7 / 34.5, 56.4 / 59.5 us at batch 16, 32, 64 against the tcgen05
+// kernel's 53-61.  On 4096 x 4096: 12.7 / 14.2 us at batch 8 against the
+// GEMV's 25.8 / 17.0 (the GEMV wins at 4 for Q8_0: 10.4 vs 13.4), 55.4 /
+// 57.9 at 64 against the tcgen05 kernel's 59.1 / 59.7.  So: batch 2..64 on
+// matrices of 8192 rows or more, 8..64 on 2048 or more; beyond 64 (two or
+// more chunks) the tcgen05 kernel.  Not taken when GQ_TC_MIN_BATCH sets a
+// plain threshold.
 bool skinny_auto_q0(int64_t rows, int64_t batch) {
-    if (tc_min_batch_env() || rows < 8192 || batch < 4) return false;
-    return batch <= 64;
+    if (tc_min_batch_env() || rows < 2048) return false;
+    return batch >= (rows >= 8192 ? 2 : 8) && batch <= 64;
 }
 
 // The same choice for Q4_0 / Q8_0 weights (gq_mma_q0.cu).

@@ -236,14 +236,15 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  * Asynchronous on `stream`; allocates nothing.
  * Dispatch (GQ_PATH_AUTO):
  *   Q4_0 / Q8_0 weights (cols % 256 == 0): the warp-level tensor-core kernel
- *     (GQ_PATH_SKINNY) at batch 4..64 on matrices of 8192 rows or more; the
- *     tcgen05 tensor-core kernel at batch >= gq_tc_min_batch() otherwise (16
- *     unless GQ_TC_MIN_BATCH is set, which also turns the warp-level choice
- *     off); the GEMV kernels below.  Neither tensor-core kernel needs a
- *     workspace.
+ *     (GQ_PATH_SKINNY) at batch 2..64 on matrices of 8192 rows or more and
+ *     8..64 on 2048 or more; the tcgen05 tensor-core kernel at batch >=
+ *     gq_tc_min_batch() otherwise (16 unless GQ_TC_MIN_BATCH is set, which
+ *     also turns the warp-level choice off); the GEMV kernels below.  Neither
+ *     tensor-core kernel needs a workspace.
  *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
  *     workspace; batches beyond 64 as 64-column chunks) from batch 4 on
- *     matrices of 8192 rows or more, the GEMV kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
+ *     matrices of 8192 rows or more and from 16 on 2048 or more, the GEMV
+ *     kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
  *     such matrices and from batch 16 on smaller ones (see gq_matmul_ws),
  *     needs a workspace for its repacked activations: call gq_matmul_ws, or
  *     gq_matmul_noalloc to use the library's static scratch.
@@ -292,12 +293,13 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * least gq_matmul_workspace_bytes bytes, owned by the caller, contents
  * overwritten; calls that share a workspace must not overlap on the GPU).
  * GQ_PATH_AUTO for Q4_K: the warp-level kernel (GQ_PATH_SKINNY) at batch
- * 4..32 on matrices of 8192 rows or more; else the tcgen05 tensor-core
- * kernel when batch >= gq_tc_min_batch(), or batch >= 9 on matrices of
- * 14336 rows or more (the measured crossovers), and the workspace suffices;
- * else the warp-level kernel (in 64-column chunks beyond batch 64) on such
- * matrices; else the GEMV kernels.  Q4_0 / Q8_0 weights ignore the workspace and dispatch as in
- * gq_matmul.  With GQ_TC_MIN_BATCH set, batch >= that value alone decides.
+ * 4..32 on matrices of 8192 rows or more and 16..32 on 2048 or more; else
+ * the tcgen05 tensor-core kernel when batch >= gq_tc_min_batch(), or batch
+ * >= 9 on matrices of 14336 rows or more (the measured crossovers), and the
+ * workspace suffices; else the warp-level kernel (in 64-column chunks
+ * beyond batch 64) where it applies; else the GEMV kernels.  Q4_0 / Q8_0
+ * weights ignore the workspace and dispatch as in gq_matmul.  With
+ * GQ_TC_MIN_BATCH set, batch >= that value alone decides.
  * The tensor-core path computes the same y (within the tolerance above) and
  * the same exact integer super-block sums S1 and S2 as the GEMV kernels, for
  * every input (its fp32 accumulation only ever holds integers below 2^24).

@@ -169,9 +169,10 @@ def test_skinny_q0_static_weights_flag_same_result(wtype):
 
 @pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
 @pytest.mark.parametrize("wtype", [Q4_0, Q8_0])
-@pytest.mark.parametrize("rows,batch,want", [(8192, 3, "gemv"), (8192, 4, "skinny"), (14336, 33, "skinny"),
-                                             (14336, 64, "skinny"), (14336, 65, "mma"), (4096, 16, "mma"),
-                                             (4096, 8, "gemv")])
+@pytest.mark.parametrize("rows,batch,want", [(8192, 1, "gemv"), (8192, 2, "skinny"), (14336, 33, "skinny"),
+                                             (14336, 64, "skinny"), (14336, 65, "mma"), (4096, 7, "gemv"),
+                                             (4096, 8, "skinny"), (4096, 65, "mma"), (1024, 16, "mma"),
+                                             (1024, 8, "gemv")])
 def test_skinny_q0_auto_dispatch(wtype, rows, batch, want):
     """gq_matmul (no workspace) picks the family by rows and batch; every
     family is deterministic, so its result equals the chosen one's bit for
