@@ -179,6 +179,18 @@ bool skinny_auto_q0(int64_t rows, int64_t batch) {
     return batch >= (rows >= 8192 ? 2 : 8) && batch <= 64;
 }
 
+// The warp-level kernel for Q5_K weights (gq_skinny.cu; Q5_K has no
+// tcgen05 kernel).  Measured on 14336 x 4096: 15.4 us at batch 4 against the
+// multi-vector GEMV's 16.2 (the GEMV wins below: 11.7 us at batch 2), 18.5 /
+// 26.1 / 51.5 us at batch 16 / 32 / 64 against 49.3 / 96.8 / 190.9; on 4096
+// x 4096: 16.8 us at batch 16 against 19.6 (the GEMV wins at 8: 10.6 vs
+// 13.9).  So: from batch 4 on matrices of 8192 rows or more, from 16 on 2048
+// or more, in 32-column chunks at any larger batch.
+bool skinny_auto_q5k(int64_t rows, int64_t batch) {
+    if (tc_min_batch_env() || rows < 2048) return false;
+    return batch >= (rows >= 8192 ? 4 : 16);
+}
+
 // The same choice for Q4_0 / Q8_0 weights (gq_mma_q0.cu).
 bool tc_auto_q0(int64_t rows, int64_t batch) {
     (void)rows;
@@ -222,7 +234,7 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         }
     }
     if (path == GQ_PATH_SKINNY) {
-        if (!q0 && wtype != GQ_Q4_K) return GQ_ERR_TYPE;
+        if (!q0 && wtype != GQ_Q4_K && wtype != GQ_Q5_K) return GQ_ERR_TYPE;
         if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
         if (q0 ? !skinny_q0_supported(rows, cols, std::min<int64_t>(batch, 64))
                : !skinny_supported(rows, cols, std::min<int64_t>(batch, 64)))
@@ -242,6 +254,8 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
             use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) &&
                          skinny_auto(rows, batch, tc_ready);
             use_mma = !use_skinny && tc_ready && tc_auto(rows, batch);
+        } else if (wtype == GQ_Q5_K) {
+            use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 32)) && skinny_auto_q5k(rows, batch);
         }
     }
     if (!use_mma && !use_skinny && !kstream && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
@@ -249,19 +263,20 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
     st = make_ctx(stream, &ctx);
     if (st != GQ_OK) return st;
     if (use_skinny) {
-        // chunks of up to 64 activation vectors, one launch each (y, sums and
-        // xq advance by whole vectors)
+        // chunks of up to 64 activation vectors (32 for Q5_K), one launch each
+        // (y, sums and xq advance by whole vectors)
+        const int64_t chunk = q0 ? 64 : skinny_max_batch(wtype);
         const bool ws_static = (flags & GQ_FLAG_W_STATIC) != 0;
         const int64_t nblk = cols / block_elems(wtype);          // weight blocks per row
         const int64_t xbytes = q0 ? cols / 32 * Q8_0_BYTES : cols / 256 * Q8_K_BYTES;  // one activation vector
         const int64_t per_row_sums = q0 ? nblk : nblk * 2;       // int32 sums per (vector, row)
-        for (int64_t b0 = 0; b0 < batch; b0 += 64) {
-            const int64_t nb = std::min<int64_t>(64, batch - b0);
+        for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
+            const int64_t nb = std::min<int64_t>(chunk, batch - b0);
             const uint8_t *xb = static_cast<const uint8_t *>(act) + b0 * xbytes;
             float *yb = y ? y + b0 * rows : nullptr;
             int32_t *sb = sums ? sums + b0 * rows * per_row_sums : nullptr;
             cudaError_t e = q0 ? launch_skinny_q0(wtype, W, xb, yb, sb, rows, cols, nb, ws_static, ctx)
-                               : launch_skinny_q4k(W, xb, yb, sb, rows, cols, nb, ws_static, ctx);
+                               : launch_skinny_q4k(wtype, W, xb, yb, sb, rows, cols, nb, ws_static, ctx);
             if (e != cudaSuccess) return cuda_fail(e);
         }
         return GQ_OK;

@@ -93,12 +93,15 @@ size_t mma_workspace_bytes(int64_t rows, int64_t cols, int64_t batch);
 cudaError_t launch_mma_q0(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
                           int64_t cols, int64_t batch, const LaunchCtx &ctx);
 bool mma_q0_supported(int64_t rows, int64_t cols, int64_t batch);
-// Warp-level tensor-core kernel for Q4_K x Q8_K at small batches
+// Warp-level tensor-core kernel for Q4_K / Q5_K x Q8_K at small batches
 // (gq_skinny.cu): batch <= 64, cols a multiple of 256, no workspace;
 // w_static as for launch_gemv (the first weight tiles are requested before
 // the dependency wait).
-cudaError_t launch_skinny_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                              int64_t batch, bool w_static, const LaunchCtx &ctx);
+// Q4_K or Q5_K weights (wtype); at most skinny_max_batch(wtype) vectors per
+// launch (64, or 32 for Q5_K).
+cudaError_t launch_skinny_q4k(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
+                              int64_t cols, int64_t batch, bool w_static, const LaunchCtx &ctx);
+int skinny_max_batch(gq_type wtype);
 bool skinny_supported(int64_t rows, int64_t cols, int64_t batch);
 // The same for Q4_0 / Q8_0 weights x Q8_0 activations (gq_skinny_q0.cu):
 // batch <= 64, cols a multiple of 256, no workspace, int32 sums one per

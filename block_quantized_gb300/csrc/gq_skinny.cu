@@ -57,11 +57,23 @@ using namespace ms;
 constexpr int SK_PRE = 2;
 constexpr int SK_NW = 6;                   // row tiles of 16 per CTA
 constexpr int SK_ROWS = 16 * SK_NW;        // weight rows per CTA
-constexpr int SK_STAGE = SK_ROWS * Q4_K_BYTES;  // one ring stage: 13,824 bytes
 constexpr int SK_SM_SMEM = 233472;         // shared memory per SM (1 KB of it reserved per CTA)
 
-template <int NT_>
+// WT: Q4_K or Q5_K weights (the same super-block, 5-bit codes with a
+// fifth-bit plane for Q5_K).
+template <int WT, int NT_>
 struct SkCfg {
+    static constexpr bool Q5 = WT == GQ_Q5_K;
+    static constexpr int BB = Q5 ? Q5_K_BYTES : Q4_K_BYTES;  // super-block bytes
+    static constexpr int STAGE = SK_ROWS * BB;                // one ring stage: 13,824 / 16,896 bytes
+    // A = sc q - OFFSET keeps every operand an fp16 integer below 1024 in
+    // magnitude; S1 = S1' + OFFSET * asum
+    static constexpr int OFFSET = Q5 ? 1024 : 512;
+    // Q4_K: |S1'| <= 256 * 512 * 128 = 2^24 per super-block, one accumulator
+    // is exact (two for narrow tiles, for the latency).  Q5_K: 2^25, so the
+    // even and odd sub-blocks always accumulate apart (each <= 2^24, exact)
+    // and meet in int32.
+    static constexpr bool DUAL = Q5 || NT_ <= 2;
     static constexpr int NT = NT_;                       // 8-column N tiles
     static constexpr int BCOLS = 8 * NT_;
     // Tiles up to 32 columns split the super-blocks between KS groups of six
@@ -94,20 +106,41 @@ struct SkCfg {
     static constexpr int OFF_CHUNK = 0;                  // 2 x CHUNK
     static constexpr int OFF_SCT = 2 * CHUNK;            // 64 x uint4 scale constants
     static constexpr int OFF_PART = OFF_SCT + 64 * 16;   // partial y of groups 1.. (KS > 1)
-    static constexpr int OFF_RING = OFF_PART + PART;     // NS x SK_STAGE
+    static constexpr int OFF_RING = OFF_PART + PART;     // NS x STAGE
     static constexpr int FIXED = OFF_RING + 16 * 8 + 4 * 8 + 16 + 128;
-    static constexpr int NS = (LIMIT - FIXED) / SK_STAGE > 8 ? 8 : (LIMIT - FIXED) / SK_STAGE;
-    static constexpr int OFF_BAR = OFF_RING + NS * SK_STAGE;
+    static constexpr int NS = (LIMIT - FIXED) / STAGE > 8 ? 8 : (LIMIT - FIXED) / STAGE;
+    static constexpr int OFF_BAR = OFF_RING + NS * STAGE;
     static constexpr int OFF_MISC = OFF_BAR + (2 * NS + 4) * 8;  // ring full / empty, chunk full / empty
     static constexpr int SMEM_ALLOC = OFF_MISC + 16 + 128;  // slack for the 128-byte alignment
     static_assert(NS >= 2, "ring");
     static_assert(THREADS <= 1024, "threads per CTA");
     static_assert(SMEM_ALLOC <= LIMIT, "shared memory budget");
-    static_assert(OFF_RING % 128 == 0 && SK_STAGE % 128 == 0, "TMA destinations");
+    static_assert(OFF_RING % 128 == 0 && STAGE % 128 == 0, "TMA destinations");
+    static_assert(!Q5 || NT_ <= 4, "Q5_K tiles hold at most 32 columns (registers of the dual accumulators)");
     static_assert(CHUNK % 16 == 0, "fragment alignment");
 };
 
 inline int pick_nt(int64_t batch) { return batch <= 8 ? 1 : batch <= 16 ? 2 : batch <= 32 ? 4 : 8; }
+
+// One Q5_K nibble word w (byte i: element 2i low, 2i + 1 high) of lane t
+// with its sub-block's fifth-bit word F (bit 2t + p of byte i: the fifth bit
+// of element 2i + p of the lane's eight) to the fp16 pairs (v e0, v e4),
+// (v e1, v e5), (v e2, v e6), (v e3, v e7), v e = sc q - 1024.  Every 5-bit
+// code is placed in mantissa bits 4-8 of 0x6400 (fp16 1024 + 16 q) and one fma
+// with k = (sc / 16, -64 sc - 1024) maps it exactly (a 1024 + q form would
+// need the constant -1024 (sc + 1), below the fp16 range at sc = 63).
+__device__ __forceinline__ uint4 nib5x8_to_f16(uint32_t w, uint32_t F, int t, uint4 k) {
+    const uint32_t w8 = w >> 8, f = F >> (2 * t);
+    const __half2 s16 = h2_bits(k.x), c = h2_bits(k.y);
+    const uint32_t e04 = ((w << 4) & 0x00F000F0u) | ((f & 0x00010001u) << 8);
+    const uint32_t e15 = (w & 0x00F000F0u) | (((f >> 1) & 0x00010001u) << 8);
+    const uint32_t e26 = ((w8 << 4) & 0x00F000F0u) | (((f >> 8) & 0x00010001u) << 8);
+    const uint32_t e37 = (w8 & 0x00F000F0u) | (((f >> 9) & 0x00010001u) << 8);
+    return make_uint4(bits_h2(__hfma2(h2_bits(e04 | 0x64006400u), s16, c)),
+                      bits_h2(__hfma2(h2_bits(e15 | 0x64006400u), s16, c)),
+                      bits_h2(__hfma2(h2_bits(e26 | 0x64006400u), s16, c)),
+                      bits_h2(__hfma2(h2_bits(e37 | 0x64006400u), s16, c)));
+}
 
 // 6-bit field f (0..15) of a Q4_K header's twelve scale bytes (words y, z, w).
 __device__ __forceinline__ uint32_t field6(const uint4 &hd, int f) {
@@ -194,16 +227,18 @@ __device__ void convert_chunk(uint8_t *buf, const uint8_t *__restrict__ xq, int 
             int asum = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) asum += (int)(int16_t)(cw[u][1 + q] & 0xffffu) + (int)(int16_t)(cw[u][1 + q] >> 16);
-            cf[i] = make_float2(__uint_as_float(cw[u][0]), 512.0f * (float)asum);
+            // Q4_K: 512 asum as fp32 (below 2^24, exact); Q5_K: asum itself
+            // (the int32 bits), since 1024 asum can exceed 2^24
+            cf[i] = make_float2(__uint_as_float(cw[u][0]), C::Q5 ? __int_as_float(asum) : 512.0f * (float)asum);
         }
     }
 }
 
-template <int NT, bool SUMS>
-__global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4k_kernel(
+template <int WT, int NT, bool SUMS>
+__global__ void __launch_bounds__(SkCfg<WT, NT>::THREADS, SkCfg<WT, NT>::MINB) skinny_q4k_kernel(
     const __grid_constant__ CUtensorMap tmap_w, const uint8_t *__restrict__ xq, float *__restrict__ y,
     int32_t *__restrict__ sums, int rows, int nsb, int batch, int w_static, uint32_t *__restrict__ status) {
-    using C = SkCfg<NT>;
+    using C = SkCfg<WT, NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -227,21 +262,24 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
         *abort = 0u;
         fence_mbar_init();
     }
-    // per-scale fma constants of nib8_to_f16: (sc, -512 (2 sc + 1), sc / 16, -64 (sc + 8))
+    // per-scale fma constants: Q4_K (nib8_to_f16) (sc, -512 (2 sc + 1),
+    // sc / 16, -64 (sc + 8)); Q5_K (nib5x8_to_f16) (sc / 16, -64 sc - 1024)
     if (threadIdx.x < 64) {
         const float sc = (float)threadIdx.x;
         reinterpret_cast<uint4 *>(smem + C::OFF_SCT)[threadIdx.x] =
-            make_uint4(pack_h2(sc, sc), pack_h2(-512.0f * (2.0f * sc + 1.0f), -512.0f * (2.0f * sc + 1.0f)),
-                       pack_h2(sc * 0.0625f, sc * 0.0625f), pack_h2(-64.0f * (sc + 8.0f), -64.0f * (sc + 8.0f)));
+            C::Q5 ? make_uint4(pack_h2(sc * 0.0625f, sc * 0.0625f),
+                               pack_h2(-64.0f * sc - 1024.0f, -64.0f * sc - 1024.0f), 0u, 0u)
+                  : make_uint4(pack_h2(sc, sc), pack_h2(-512.0f * (2.0f * sc + 1.0f), -512.0f * (2.0f * sc + 1.0f)),
+                               pack_h2(sc * 0.0625f, sc * 0.0625f), pack_h2(-64.0f * (sc + 8.0f), -64.0f * (sc + 8.0f)));
     }
     __syncthreads();
     // one 2-D TMA tile (the super-block's 96 rows) into ring slot `slot`
     auto issue_tile = [&](int sb, int slot) {
-        mbar_arrive_expect_tx(full + slot, SK_STAGE);
+        mbar_arrive_expect_tx(full + slot, C::STAGE);
         asm volatile(
             "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + C::OFF_RING + slot * SK_STAGE)),
-            "l"(reinterpret_cast<uint64_t>(&tmap_w)), "r"(sb * Q4_K_BYTES), "r"(row0), "r"(smem_u32(full + slot))
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + C::OFF_RING + slot * C::STAGE)),
+            "l"(reinterpret_cast<uint64_t>(&tmap_w)), "r"(sb * C::BB), "r"(row0), "r"(smem_u32(full + slot))
             : "memory");
     };
     // Static weights (no kernel in flight writes W): the producer requests the
@@ -307,12 +345,12 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
                 if (sb % C::KS != kg) continue;
                 const int si = sb % C::NS;
                 if (!(ok = tc::wait_warp(full + si, (uint32_t)(sb / C::NS) & 1u, abort))) break;
-                const uint8_t *rg = smem + C::OFF_RING + si * SK_STAGE + (16 * rw + g) * Q4_K_BYTES;
-                const uint8_t *rh = rg + 8 * Q4_K_BYTES;
+                const uint8_t *rg = smem + C::OFF_RING + si * C::STAGE + (16 * rw + g) * C::BB;
+                const uint8_t *rh = rg + 8 * C::BB;
                 const uint4 hg = *reinterpret_cast<const uint4 *>(rg), hh = *reinterpret_cast<const uint4 *>(rh);
-                // narrow tiles: odd sub-blocks accumulate apart, so two MMA
-                // chains run side by side (both partial sums exact integers)
-                constexpr bool DUAL = NT <= 2;
+                // odd sub-blocks accumulate apart (C::DUAL): two MMA chains
+                // side by side, both partial sums exact integers
+                constexpr bool DUAL = C::DUAL;
                 float s1[NT][4], s1b[NT][4], s2[NT][4];
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
@@ -322,8 +360,16 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t wg = *reinterpret_cast<const uint32_t *>(rg + 16 + 16 * j + 4 * t);
                     const uint32_t wh = *reinterpret_cast<const uint32_t *>(rh + 16 + 16 * j + 4 * t);
-                    const uint4 ag = nib8_to_f16(wg, sct[field6(hg, j)]);
-                    const uint4 ah = nib8_to_f16(wh, sct[field6(hh, j)]);
+                    uint4 ag, ah;
+                    if constexpr (C::Q5) {
+                        const uint32_t fg = *reinterpret_cast<const uint32_t *>(rg + 144 + 4 * j);
+                        const uint32_t fh = *reinterpret_cast<const uint32_t *>(rh + 144 + 4 * j);
+                        ag = nib5x8_to_f16(wg, fg, t, sct[field6(hg, j)]);
+                        ah = nib5x8_to_f16(wh, fh, t, sct[field6(hh, j)]);
+                    } else {
+                        ag = nib8_to_f16(wg, sct[field6(hg, j)]);
+                        ah = nib8_to_f16(wh, sct[field6(hh, j)]);
+                    }
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         const uint4 b = bf[(n * C::KC * 8 + sbk * 8 + j) * 32 + lane];
@@ -332,7 +378,7 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
                         mma16816(acc, ag.z, ah.z, ag.w, ah.w, b.z, b.w);
                     }
                 }
-                if (DUAL) {
+                if (DUAL && !C::Q5) {
 #pragma unroll
                     for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -357,7 +403,31 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
                 for (int n = 0; n < NT; ++n) {
                     // columns 8 n + 2 t and + 1: (dx, 512 asum) of both
                     const float4 cv = cf[(sbk * C::BCOLS + 8 * n + 2 * t) / 2];
-                    if (SUMS) {
+                    if constexpr (C::Q5) {
+                        // S1 in int32: the two exact halves plus 1024 asum
+                        int S1[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            S1[e] = __float2int_rn(s1[n][e]) + __float2int_rn(s1b[n][e]) +
+                                    C::OFFSET * __float_as_int((e & 1) ? cv.w : cv.y);
+                        if (SUMS) {
+                            const int rr[2] = {row0 + 16 * rw + g, row0 + 16 * rw + g + 8};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int row = rr[e >> 1], b = 8 * n + 2 * t + (e & 1);
+                                if (row < rows && b < batch) {
+                                    int32_t *o = sums + (((size_t)b * rows + row) * nsb + sb) * 2;
+                                    o[0] = S1[e];
+                                    o[1] = (int32_t)s2[n][e];
+                                }
+                            }
+                        } else {
+                            yacc[n][0] = fmaf(cv.x, dg * (float)S1[0] - dming * s2[n][0], yacc[n][0]);
+                            yacc[n][1] = fmaf(cv.z, dg * (float)S1[1] - dming * s2[n][1], yacc[n][1]);
+                            yacc[n][2] = fmaf(cv.x, dh * (float)S1[2] - dminh * s2[n][2], yacc[n][2]);
+                            yacc[n][3] = fmaf(cv.z, dh * (float)S1[3] - dminh * s2[n][3], yacc[n][3]);
+                        }
+                    } else if (SUMS) {
                         const int rr[2] = {row0 + 16 * rw + g, row0 + 16 * rw + g + 8};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -419,11 +489,11 @@ __global__ void __launch_bounds__(SkCfg<NT>::THREADS, SkCfg<NT>::MINB) skinny_q4
     if (threadIdx.x == 0 && *abort) atomicOr(status, STATUS_MMA_TIMEOUT);
 }
 
-template <int NT>
+template <int WT, int NT>
 cudaError_t launch_nt(const CUtensorMap &tmap, const void *xq, float *y, int32_t *sums, int64_t rows, int nsb,
                       int64_t batch, bool w_static, const LaunchCtx &ctx) {
-    using C = SkCfg<NT>;
-    auto k = sums ? skinny_q4k_kernel<NT, true> : skinny_q4k_kernel<NT, false>;
+    using C = SkCfg<WT, NT>;
+    auto k = sums ? skinny_q4k_kernel<WT, NT, true> : skinny_q4k_kernel<WT, NT, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((rows + SK_ROWS - 1) / SK_ROWS));
@@ -434,31 +504,45 @@ cudaError_t launch_nt(const CUtensorMap &tmap, const void *xq, float *y, int32_t
 
 }  // namespace
 
+int skinny_max_batch(gq_type wtype) { return wtype == GQ_Q5_K ? 32 : 64; }
+
 bool skinny_supported(int64_t rows, int64_t cols, int64_t batch) {
     return rows >= 1 && batch >= 1 && batch <= 64 && cols >= QK_K && cols % QK_K == 0 &&
            (rows + SK_ROWS - 1) / SK_ROWS <= 0x7fffffff;
 }
 
-cudaError_t launch_skinny_q4k(const void *W, const void *xq, float *y, int32_t *sums, int64_t rows, int64_t cols,
-                              int64_t batch, bool w_static, const LaunchCtx &ctx) {
-    if (!skinny_supported(rows, cols, batch)) return cudaErrorInvalidValue;
+cudaError_t launch_skinny_q4k(gq_type wtype, const void *W, const void *xq, float *y, int32_t *sums, int64_t rows,
+                              int64_t cols, int64_t batch, bool w_static, const LaunchCtx &ctx) {
+    if (!skinny_supported(rows, cols, batch) || batch > skinny_max_batch(wtype) ||
+        (wtype != GQ_Q4_K && wtype != GQ_Q5_K))
+        return cudaErrorInvalidValue;
     const int nsb = (int)(cols / QK_K);
+    const int bb = wtype == GQ_Q5_K ? Q5_K_BYTES : Q4_K_BYTES;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {(cuuint64_t)nsb * Q4_K_BYTES, (cuuint64_t)rows};
-    const cuuint64_t gstride[1] = {(cuuint64_t)nsb * Q4_K_BYTES};
-    const cuuint32_t box[2] = {(cuuint32_t)Q4_K_BYTES, (cuuint32_t)SK_ROWS};
+    // W as a 2-D byte tensor: rows of nsb super-blocks; box = one super-block
+    // (144 or 176 bytes, both 16-byte multiples) of 96 rows
+    const cuuint64_t gdim[2] = {(cuuint64_t)nsb * bb, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)nsb * bb};
+    const cuuint32_t box[2] = {(cuuint32_t)bb, (cuuint32_t)SK_ROWS};
     const cuuint32_t estride[2] = {1, 1};
     if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), gdim, gstride, box, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    if (wtype == GQ_Q5_K) {
+        switch (pick_nt(batch)) {
+        case 1: return launch_nt<GQ_Q5_K, 1>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+        case 2: return launch_nt<GQ_Q5_K, 2>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+        default: return launch_nt<GQ_Q5_K, 4>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+        }
+    }
     switch (pick_nt(batch)) {
-    case 1: return launch_nt<1>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
-    case 2: return launch_nt<2>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
-    case 4: return launch_nt<4>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
-    default: return launch_nt<8>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+    case 1: return launch_nt<GQ_Q4_K, 1>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+    case 2: return launch_nt<GQ_Q4_K, 2>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+    case 4: return launch_nt<GQ_Q4_K, 4>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
+    default: return launch_nt<GQ_Q4_K, 8>(tmap, xq, y, sums, rows, nsb, batch, w_static, ctx);
     }
 }
 

@@ -135,7 +135,7 @@ typedef enum {
     GQ_PATH_AUTO = 0,   /* GEMV below the tensor-core crossover batch, MMA at or above */
     GQ_PATH_GEMV = 1,   /* dp4a GEMV kernels (any batch; batch is processed in chunks) */
     GQ_PATH_MMA = 2,    /* tcgen05 tensor-core kernels (Q4_0, Q8_0, Q4_K weights) */
-    GQ_PATH_SKINNY = 3  /* warp-level tensor-core kernels (mma.sync) for Q4_K, Q4_0, Q8_0; 64 columns per launch */
+    GQ_PATH_SKINNY = 3  /* warp-level tensor-core kernels (mma.sync): Q4_K, Q5_K, Q4_0, Q8_0; 64 (Q5_K: 32) columns a launch */
 } gq_path;
 
 /* Elements per block: 32, 32, 256, 256, 256, 256 (Q4_0, Q8_0, Q4_K, Q8_K,
@@ -248,7 +248,10 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *     such matrices and from batch 16 on smaller ones (see gq_matmul_ws),
  *     needs a workspace for its repacked activations: call gq_matmul_ws, or
  *     gq_matmul_noalloc to use the library's static scratch.
- *   Q5_K / Q6_K weights: their GEMV kernels.
+ *   Q5_K weights: the warp-level tensor-core kernel from batch 4 on matrices
+ *     of 8192 rows or more and from 16 on 2048 or more (32-column chunks
+ *     beyond 32), their GEMV kernels otherwise.
+ *   Q6_K weights: their GEMV kernels.
  * The GEMV kernels take any batch, in chunks of up to eight vectors, one
  * pass over W per chunk.
  */
@@ -260,11 +263,12 @@ gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
  * kernel of Q4_0 / Q8_0 weights (GQ_ERR_SHAPE unless cols % 256 == 0); for
  * Q4_K weights it returns GQ_ERR_NULL (that kernel needs the workspace of
  * gq_matmul_ws), for Q5_K / Q6_K GQ_ERR_TYPE.  GQ_PATH_SKINNY runs the
- * warp-level tensor-core kernels of Q4_K, Q4_0 and Q8_0 weights (mma.sync
- * m16n8k16 on exact integer operands, one fresh accumulator per 32-element
- * block for Q4_0 / Q8_0; one launch per 64 activation vectors; cols % 256 ==
- * 0, GQ_ERR_SHAPE otherwise; GQ_ERR_TYPE for Q5_K / Q6_K and for fp32
- * activations). */
+ * warp-level tensor-core kernels of Q4_K, Q5_K, Q4_0 and Q8_0 weights
+ * (mma.sync m16n8k16 on exact integer operands: sc q - 512 for Q4_K and
+ * sc q - 1024 for Q5_K, whose even and odd sub-blocks accumulate apart; one
+ * fresh accumulator per 32-element block for Q4_0 / Q8_0; one launch per 64
+ * activation vectors, 32 for Q5_K; cols % 256 == 0, GQ_ERR_SHAPE otherwise;
+ * GQ_ERR_TYPE for Q6_K and for fp32 activations). */
 gq_status gq_matmul_path(gq_type wtype, const void *W, const void *xq, float *y,
                          int64_t rows, int64_t cols, int64_t batch, gq_path path,
                          gq_stream_t stream);

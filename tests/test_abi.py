@@ -86,9 +86,10 @@ def test_matmul_validation(lib):
     assert f(4, A16, A16, A16, 8, 32, 1, None) == SHAPE          # Q6_K needs 256-multiples
     assert f(4, 0, 0, 0, 8, 256, 0, None) == OK
     assert g(5, A16, A16, A16, 8, 256, 64, 2, None) == TYPE      # no tensor-core Q5_K kernel
-    # the warp-level tensor-core path: Q4_K, Q4_0 and Q8_0, cols a multiple
-    # of 256 (batches beyond 64 run as 64-column chunks)
-    assert g(5, A16, A16, A16, 8, 256, 8, 3, None) == TYPE
+    # the warp-level tensor-core path: Q4_K, Q5_K, Q4_0 and Q8_0, cols a
+    # multiple of 256 (larger batches run as 64- or 32-column chunks)
+    assert g(4, A16, A16, A16, 8, 256, 8, 3, None) == TYPE
+    assert g(5, A16, A16, A16, 8, 256, 40, 3, None) == CUDA
     assert g(0, A16, A16, A16, 8, 288, 8, 3, None) == SHAPE
     assert g(1, A16, A16, A16, 8, 256, 8, 3, None) == CUDA
     assert g(2, A16, A16, A16, 8, 256, 65, 3, None) == CUDA

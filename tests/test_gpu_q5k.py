@@ -8,6 +8,8 @@ streaming kernel (whole rows through a per-warp shared-memory ring, 16 or 8
 warps, several rows per warp on the tall shapes) and the plain kernel (rows
 too long for a two-stage ring).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -285,3 +287,93 @@ def test_fused_f32_width_limit():
     y = torch.empty(1, 1, device="cuda")
     with pytest.raises(gq.GQError):
         gq.gq_matmul_f32(Q5_K, Wd, x, y, 1, 19200, 1)
+
+
+# ------------------------------------------- warp-level tensor-core path
+
+SKINNY_SHAPES = [(96, 256, 1), (100, 512, 2), (200, 768, 8), (300, 1280, 9), (77, 256, 16), (513, 2048, 17),
+                 (192, 1024, 32), (130, 2304, 33), (257, 4096, 64), (96, 3072, 5)]
+
+
+@pytest.mark.parametrize("rows,cols,batch", SKINNY_SHAPES)
+def test_skinny_sums_and_y(rows, cols, batch):
+    """GQ_PATH_SKINNY for Q5_K (mma.sync on A = sc q - 1024, the even and
+    odd sub-blocks in separate exact accumulators, 32 columns per launch):
+    S1, S2 bit-identical to the oracle, y within the bar."""
+    g = inputs.rng(rows * 13 + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = host(gq.block_sums(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY))
+    np.testing.assert_array_equal(s, orc.block_sums(Q5_K, Wq, Xq, rows, cols, batch))
+    y = host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY))
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+
+
+@pytest.mark.parametrize("batch", [3, 16, 40])
+def test_skinny_sums_beyond_fp32_integers(batch):
+    """Constant rows (sc = 63, codes 31) with single codes lowered, against
+    constant activations (codes +-127) and a column of raw -128 codes: S1
+    near 6.3e7, far above 2^24 and odd, still matches the oracle bit for
+    bit (each half's partial sums stay within 2^24)."""
+    rows, cols = 131, 512
+    W = inputs.outlier_weights(inputs.rng(9), rows, cols, frac=0.001)
+    W[0] = 1.0
+    W[0, 5] = 0.97
+    W[1] = 1.0
+    W[2] = 1.0
+    W[2, 1::2] = 0.97
+    W[130] = 1.0
+    W[130, 255] = 0.97
+    X = inputs.normal(inputs.rng(10), (batch, cols))
+    X[0] = 1.0
+    X[1] = -1.0
+    X[batch - 1] = 1.0
+    Wq, Xq = orc.quantize(Q5_K, W), orc.quantize(Q8_K, X)
+    blk = Xq.reshape(batch, cols // 256, 276)
+    blk[2, :, 4:260] = 0x80
+    blk[2, :, 260:276] = np.frombuffer(np.full(8, -128 * 32, np.int16).tobytes(), np.uint8)
+    s_ref = orc.block_sums(Q5_K, Wq, Xq, rows, cols, batch)
+    assert np.sum((np.abs(s_ref[..., 0]) > 2**25) & (s_ref[..., 0] % 2 != 0)) >= 2
+    Wd, Xd = dev(Wq), dev(Xq)
+    np.testing.assert_array_equal(host(gq.block_sums(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY)), s_ref)
+    y = host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY))
+    y_ref, T = orc.matmul_ref(Q5_K, Wq, Xq, rows, cols, batch)
+    assert_close(y, y_ref, T)
+
+
+@pytest.mark.parametrize("batch", [8, 32, 64])
+def test_skinny_full_size(batch):
+    """14336 x 4096 (the batch-sweep shape); the oracle recomputes sampled
+    rows from the same fp32 inputs."""
+    rows, cols = 14336, 4096
+    W, X = inputs.gemm_q4_k(0, rows, cols, batch)
+    Wd = gq.quantize(Q5_K, dev(W))
+    Xd = gq.quantize(Q8_K, dev(X))
+    y = host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch, gq.PATH_SKINNY))
+    g = np.random.Generator(np.random.PCG64(rows + batch))
+    idx = np.unique(np.concatenate([[0, rows - 1], g.choice(rows, size=32, replace=False)]))
+    Wq_s = orc.quantize(Q5_K, W[idx])
+    assert host(Wd)[idx].tobytes() == Wq_s.tobytes()
+    Xq = orc.quantize(Q8_K, X)
+    y_ref, T = orc.matmul_ref(Q5_K, Wq_s, Xq, len(idx), cols, batch, nthreads=orc.max_threads())
+    assert_close(y[:, idx], y_ref, T)
+
+
+@pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
+@pytest.mark.parametrize("rows,batch,want", [(14336, 3, "gemv"), (14336, 4, "skinny"), (8192, 70, "skinny"),
+                                             (4096, 15, "gemv"), (4096, 16, "skinny"), (1024, 64, "gemv")])
+def test_auto_dispatch(rows, batch, want):
+    """gq_matmul for Q5_K: the warp-level kernel from batch 4 on matrices of
+    8192 rows or more and from 16 on 2048 or more (32-column chunks beyond),
+    the multi-vector GEMV otherwise; both are deterministic, so the AUTO
+    result equals the chosen family's bit for bit."""
+    cols = 512
+    g = inputs.rng(rows + batch)
+    Wd = gq.quantize(Q5_K, dev(inputs.normal(g, (rows, cols), 0.02)))
+    Xd = gq.quantize(Q8_K, dev(inputs.normal(g, (batch, cols))))
+    y = host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch))
+    path = gq.PATH_SKINNY if want == "skinny" else gq.PATH_GEMV
+    assert y.tobytes() == host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch, path)).tobytes()

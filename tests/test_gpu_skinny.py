@@ -134,15 +134,15 @@ def test_skinny_static_weights_flag_same_result(batch):
 
 
 def test_skinny_shape_rules():
-    """Q4_K, Q4_0 and Q8_0 weights with cols a multiple of 256 only: Q5_K is
-    refused, and so is a Q4_0 row of 288 columns."""
-    rows, cols = 128, 512
+    """Q4_K, Q5_K, Q4_0 and Q8_0 weights with cols a multiple of 256 only:
+    Q6_K is refused, and so is a Q4_0 row of 288 columns."""
+    rows, cols = 128, 2048
     g = inputs.rng(31)
     y = torch.empty(65, rows, device="cuda")
-    W5 = gq.quantize(5, dev(inputs.normal(g, (rows, cols), 0.02)))
+    W6 = gq.quantize(4, dev(inputs.normal(g, (rows, cols), 0.02)))
     X8k = gq.quantize(Q8_K, dev(inputs.normal(g, (8, cols))))
     with pytest.raises(gq.GQError):
-        gq.gq_matmul_path(5, W5, X8k, y, rows, cols, 8, gq.PATH_SKINNY)
+        gq.gq_matmul_path(4, W6, X8k, y, rows, cols, 8, gq.PATH_SKINNY)
     W0 = gq.quantize(0, dev(inputs.normal(g, (rows, 288), 0.02)))
     X0 = gq.quantize(1, dev(inputs.normal(g, (8, 288))))
     with pytest.raises(gq.GQError):
