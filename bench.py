@@ -762,10 +762,12 @@ def bench_q6k(gq, inputs, torch, np, dev, capture, time_graph, hbm_peak, cpu=Fal
     t_c, _ = time_graph(capture(chain), k, 5)
     t_p, _ = time_graph(capture(chain_plain), k, 5)
     t_f, _ = time_graph(capture(chain_fused), k, 5)
-    # small batches: up to eight vectors share one pass over each matrix
-    Yb = torch.empty(8, GEMV_ROWS, dtype=torch.float32, device=dev)
+    # small batches through gq_matmul's own choice: up to eight vectors share
+    # one pass of the GEMV over each matrix; Q5_K takes the warp-level
+    # tensor-core kernel from batch 16 on these 4096 rows
+    Yb = torch.empty(32, GEMV_ROWS, dtype=torch.float32, device=dev)
     batch_us = {}
-    for nb in (2, 4, 8):
+    for nb in (2, 4, 8, 16, 32):
         def chain_b():
             for i in range(COPIES):
                 gq.gq_matmul_ex(wt, Wall[i], XQ[:nb], Yb, GEMV_ROWS, GEMV_COLS, nb, gq.PATH_AUTO,
