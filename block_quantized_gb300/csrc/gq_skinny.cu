@@ -1,7 +1,7 @@
-// gq_skinny.cu -- Q4_K x Q8_K for small batches (up to 64 activation vectors
-// per launch): the per-super-block product of "llama.cpp 推理引擎" §5.5 on
-// warp-level tensor-core MMAs (mma.sync m16n8k16, fp16 operands, fp32
-// accumulate).
+// gq_skinny.cu -- Q4_K (and Q5_K) x Q8_K for small batches (up to 64
+// activation vectors per launch, 32 for Q5_K): the per-super-block product of
+// "llama.cpp 推理引擎" §5.5 on warp-level tensor-core MMAs (mma.sync
+// m16n8k16, fp16 operands, fp32 accumulate).
 //
 // Between the GEMV (one pass over W per eight vectors, its dp4a work growing
 // with every vector) and the tcgen05 kernel (a CTA-wide pipeline whose
@@ -19,6 +19,10 @@
 //   S2 = sum_j m_j * t_j by one more K = 16 step, t_j split exactly as
 //   t_lo + 64 t_hi: A2 = [m | 64 m], B2 = [t_lo | t_hi] (|S2| < 2^21).
 //   y += d_x * (d * S1 - dmin * S2) per super-block, in fp32.
+// Q5_K (5-bit codes, the fifth bits in their own plane) uses A = sc_j * q -
+// 1024 in [-1024, 929]: |S1'| reaches 2^25, so the even and odd sub-blocks
+// accumulate apart (each within 2^24, exact) and S1 = S1'(even) + S1'(odd) +
+// 1024 * asum is formed in int32.
 //
 // Operand order: within each 8-element group of a 32-element sub-block both
 // operands use (e0, e4, e1, e5, e2, e6, e3, e7) -- the order in which a
@@ -30,7 +34,7 @@
 //                  g takes the super-blocks sb = g (mod KS) of the 96 rows,
 //                  and the groups' partial y are added in group order at the
 //                  end (the int32 block sums are per super-block, exact);
-//   producer warp  one 2-D TMA tile per super-block (144 bytes x 96 rows;
+//   producer warp  one 2-D TMA tile per super-block (144 or 176 bytes x 96 rows;
 //                  rows past the matrix read as zeros) through a ring of NS;
 //   converter warps (four) turn the Q8_K activation blocks, KC super-blocks
 //                  at a time, into fp16 B fragments, min-term fragments and
