@@ -179,6 +179,15 @@ bool skinny_auto_q0(int64_t rows, int64_t batch) {
     return batch >= (rows >= 8192 ? 2 : 8) && batch <= 64;
 }
 
+// Q4_K without a workspace: the tcgen05 kernel's variant that packs the
+// activations in the CTA (tiles of 64 columns) against the warp-level
+// kernel's 64-column chunks.  Measured on 14336 x 4096: 94.9 vs 78.2 us at
+// batch 128, 142.5 vs 156.7 at 256; the 28672 x 8192 x 512 prefill 1.10 vs
+// 1.29 ms.  So: from batch 192 on matrices of 8192 rows or more.
+bool tc_nows_auto(int64_t rows, int64_t batch) {
+    return !tc_min_batch_env() && rows >= 8192 && batch >= 192;
+}
+
 // The warp-level kernel for Q5_K weights (gq_skinny.cu; Q5_K has no
 // tcgen05 kernel).  Measured on 14336 x 4096: 15.4 us at batch 4 against the
 // multi-vector GEMV's 16.2 (the GEMV wins below: 11.7 us at batch 2), 18.5 /
@@ -228,9 +237,9 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
             if (!mma_q0_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
         } else {
             if (!mma_supported(rows, cols, batch)) return GQ_ERR_SHAPE;
-            if (!ws) return GQ_ERR_NULL;
-            if (ws_bytes < mma_workspace_bytes(rows, cols, batch)) return GQ_ERR_SHAPE;
-            if (!aligned(ws, 16)) return GQ_ERR_ALIGN;
+            // without a workspace the kernel packs the activations itself
+            if (ws && ws_bytes < mma_workspace_bytes(rows, cols, batch)) return GQ_ERR_SHAPE;
+            if (ws && !aligned(ws, 16)) return GQ_ERR_ALIGN;
         }
     }
     if (path == GQ_PATH_SKINNY) {
@@ -250,10 +259,13 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
         } else if (wtype == GQ_Q4_K) {
             const bool tc_ready = mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
-            // beyond batch 64 the warp-level kernel runs over 64-column chunks
-            use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) &&
+            // without a workspace, large batches take the tcgen05 kernel that
+            // packs its activations itself; otherwise beyond batch 64 the
+            // warp-level kernel runs over 64-column chunks
+            const bool tc_nows = !tc_ready && mma_supported(rows, cols, batch) && tc_nows_auto(rows, batch);
+            use_skinny = !tc_nows && skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) &&
                          skinny_auto(rows, batch, tc_ready);
-            use_mma = !use_skinny && tc_ready && tc_auto(rows, batch);
+            use_mma = tc_nows || (!use_skinny && tc_ready && tc_auto(rows, batch));
         } else if (wtype == GQ_Q5_K) {
             use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 32)) && skinny_auto_q5k(rows, batch);
         }

@@ -161,6 +161,10 @@ struct Cfg {
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
     // epilogue warps that own columns (four per 32 columns)
     static constexpr int EPI_ACTIVE = 4 * (TN / 32);
+    // epilogue warps with no columns: they pack the activations when there is
+    // no workspace (tiles of up to 64 columns)
+    static constexpr int NPACK = 16 - EPI_ACTIVE;
+    static constexpr int PACK_COLS = NPACK > 0 ? (TN + NPACK - 1) / NPACK : 1;  // columns per packing warp
     static_assert(COL_A0 + 128u * NA <= TMEM_COLS && 2 * TN <= (int)COL_A0, "tensor-memory columns");
     __host__ __device__ static constexpr uint32_t col_s1(int p) { return (uint32_t)(TN * p); }
     __host__ __device__ static constexpr uint32_t col_a(int i) { return COL_A0 + 128u * (uint32_t)i; }
@@ -240,6 +244,64 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // (K position 8 + j) of the min-term tile, and lane 0 the column scale dx
 // and the column's code sum (the sum of the eight t_j).  Columns past the
 // batch are zero.
+// What lane l of a warp reads of one column's Q8_K block: codes 8l..8l+7
+// and, lanes 0..7, the sub-block sum t_l (zeros for a column past the batch).
+struct PackIn {
+    uint32_t w0, w1;
+    int t;
+};
+
+__device__ __forceinline__ PackIn pack_load(const uint8_t *__restrict__ src, bool valid) {
+    const int lane = threadIdx.x & 31;
+    PackIn in{0u, 0u, 0};
+    if (valid) {
+        in.w0 = __ldg(reinterpret_cast<const uint32_t *>(src + 4 + 8 * lane));
+        in.w1 = __ldg(reinterpret_cast<const uint32_t *>(src + 8 + 8 * lane));
+        if (lane < 8) in.t = __ldg(reinterpret_cast<const int16_t *>(src + 260) + lane);
+    }
+    return in;
+}
+
+// Column c of one unit (a warp, lane l): the operand stages go to st01
+// (stages 0, 1) and st23 (stages 2, 3, then the min-term tile); returns the
+// column's code sum in every lane.
+template <class C>
+__device__ __forceinline__ int pack_store(const PackIn &in, int c, uint8_t *st01, uint8_t *st23) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t w0 = in.w0, w1 = in.w1;
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a[i] = (float)(int8_t)(w0 >> (8 * i));
+        a[4 + i] = (float)(int8_t)(w1 >> (8 * i));
+    }
+    const uint4 chunk = make_uint4(pack_h2(a[0], a[4]), pack_h2(a[1], a[5]), pack_h2(a[2], a[6]),
+                                   pack_h2(a[3], a[7]));
+    const int stage = lane >> 3;
+    uint8_t *st = stage < 2 ? st01 + stage * C::OP_B : st23 + (stage - 2) * C::OP_B;
+    *reinterpret_cast<uint4 *>(st + sw128_off(c, lane & 7)) = chunk;
+    const int t = in.t;
+    if (lane < 8) {
+        const int thi = t >> 6;          // floor(t / 64), in [-64, 63]
+        const int tlo = t - 64 * thi;    // in [0, 63]
+        uint8_t *mb = st23 + 2 * C::OP_B;
+        *reinterpret_cast<__half *>(mb + plain_off(c, 0) + 2 * lane) = __int2half_rn(tlo);
+        *reinterpret_cast<__half *>(mb + plain_off(c, 1) + 2 * lane) = __int2half_rn(thi);
+    }
+    // code sum of the column's super-block: lanes 0..7 hold t_0..t_7, the
+    // other lanes zero
+    int asum = t;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) asum += __shfl_xor_sync(0xffffffffu, asum, o);
+    return __shfl_sync(0xffffffffu, asum, 0);
+}
+
+template <class C>
+__device__ __forceinline__ int pack_column(const uint8_t *__restrict__ src, bool valid, int c, uint8_t *st01,
+                                           uint8_t *st23) {
+    return pack_store<C>(pack_load(src, valid), c, st01, st23);
+}
+
 template <int TN>
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ xq,
                                                    uint8_t *__restrict__ ws, int nsb, int batch) {
@@ -253,34 +315,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ x
         const int b = ct * TN + c;
         const bool valid = b < batch;
         const uint8_t *src = xq + ((size_t)(valid ? b : 0) * nsb + sb) * Q8_K_BYTES;
-        uint32_t w0 = 0, w1 = 0;
-        if (valid) {
-            w0 = __ldg(reinterpret_cast<const uint32_t *>(src + 4 + 8 * lane));
-            w1 = __ldg(reinterpret_cast<const uint32_t *>(src + 8 + 8 * lane));
-        }
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            a[i] = (float)(int8_t)(w0 >> (8 * i));
-            a[4 + i] = (float)(int8_t)(w1 >> (8 * i));
-        }
-        const uint4 chunk = make_uint4(pack_h2(a[0], a[4]), pack_h2(a[1], a[5]), pack_h2(a[2], a[6]),
-                                       pack_h2(a[3], a[7]));
-        *reinterpret_cast<uint4 *>(unit + (lane >> 3) * C::OP_B + sw128_off(c, lane & 7)) = chunk;
-        int t = 0;
-        if (valid && lane < 8) t = __ldg(reinterpret_cast<const int16_t *>(src + 260) + lane);
-        if (lane < 8) {
-            const int thi = t >> 6;          // floor(t / 64), in [-64, 63]
-            const int tlo = t - 64 * thi;    // in [0, 63]
-            uint8_t *mb = unit + C::WS_B;
-            *reinterpret_cast<__half *>(mb + plain_off(c, 0) + 2 * lane) = __int2half_rn(tlo);
-            *reinterpret_cast<__half *>(mb + plain_off(c, 1) + 2 * lane) = __int2half_rn(thi);
-        }
-        // code sum of the column's super-block: lanes 0..7 hold t_0..t_7,
-        // the other lanes zero
-        int asum = t;
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) asum += __shfl_xor_sync(0xffffffffu, asum, o);
+        const int asum = pack_column<C>(src, valid, c, unit, unit + 2 * C::OP_B);
         if (lane == 0) {
             float *cs = reinterpret_cast<float *>(unit + C::WS_B + C::WS_MIN);
             cs[c] = valid ? __ldg(reinterpret_cast<const float *>(src)) : 0.0f;
@@ -423,9 +458,10 @@ __device__ __forceinline__ uint4 nibbles_to_f16(uint32_t w, __half2 s1, __half2 
 // Then the hh = 0 threads write row t's min-term A row, the hh = 1 threads
 // row t's scales d, dmin and (t < TN) column t's scale dx and code sum (read
 // from the workspace, requested before the raw weights are waited for).
-template <class C>
+template <class C, bool WS>
 __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const uint8_t *__restrict__ ws,
-                             int ct, int rot, int nvalid, int nsb, volatile uint32_t *abort) {
+                             const uint8_t *__restrict__ xq, int batch, int ct, int rot, int nvalid, int nsb,
+                             volatile uint32_t *abort) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = 32 * (warp & 3) + lane, hh = (warp - BLD_WARP0) >> 2;
     const bool valid = t < nvalid;
@@ -436,10 +472,26 @@ __device__ void role_builder(uint8_t *smem, const Bars &B, uint32_t tmem, const 
         const uint32_t aph = (uint32_t)(sb / C::NA) & 1u;       // parity of its use
         float dx = 0.0f, as = 0.0f;
         if (hh == 1 && t < C::TN) {
-            const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * C::WS_UNIT;
-            const float *cs = reinterpret_cast<const float *>(unit + C::WS_B + C::WS_MIN);
-            dx = __ldg(cs + t);
-            as = __ldg(cs + C::TN + t);
+            if constexpr (WS) {
+                const uint8_t *unit = ws + ((size_t)ct * nsb + kslot(sb, rot, nsb)) * C::WS_UNIT;
+                const float *cs = reinterpret_cast<const float *>(unit + C::WS_B + C::WS_MIN);
+                dx = __ldg(cs + t);
+                as = __ldg(cs + C::TN + t);
+            } else if (ct * C::TN + t < batch) {
+                // no workspace: the column's scale and code sum straight from
+                // its Q8_K block (the eight sub-block sums added, exact)
+                const uint8_t *src = xq + ((size_t)(ct * C::TN + t) * nsb + kslot(sb, rot, nsb)) * Q8_K_BYTES;
+                dx = __ldg(reinterpret_cast<const float *>(src));
+                // Q8_K blocks are 276 bytes: only 4-byte alignment holds
+                const uint32_t *bs = reinterpret_cast<const uint32_t *>(src + 260);
+                int a = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t w = __ldg(bs + k);
+                    a += (int)(int16_t)(w & 0xffffu) + (int)(int16_t)(w >> 16);
+                }
+                as = (float)a;
+            }
         }
         if (!wait_warp(B.raw_full + rr.idx, rr.phase, abort)) return;
         const uint8_t *raw = smem + C::OFF_RAW + rr.idx * RAW_STAGE + t * Q4_K_BYTES;
@@ -583,6 +635,53 @@ __device__ void role_mma(uint8_t *smem, const Bars &B, uint32_t tmem, int nsb, v
     mma_commit(B.fin);
 }
 
+// Without a workspace (tiles of up to 64 columns): the epilogue warps whose
+// columns lie past TN pack the activation operand into the B ring themselves,
+// the work pack_kernel does into the workspace.  Per super-block they wait
+// until the MMAs of the super-block NBSB steps back have released the slot
+// pair, convert their columns (warp w of NP takes columns w, w + NP, ...),
+// make the stores visible to the tensor core and arrive on both halves'
+// barriers (NP arrivals complete each).
+template <class C>
+__device__ void role_pack(uint8_t *smem, const Bars &B, const uint8_t *__restrict__ xq, int batch, int ct,
+                          int rot, int nsb, int pw, volatile uint32_t *abort) {
+    constexpr int KMAX = C::PACK_COLS;
+    const int lane = threadIdx.x & 31;
+    // the reads of super-block sb + 1 are in flight while sb waits for its
+    // slots and is converted
+    PackIn cur[KMAX], nxt[KMAX];
+    auto load_sb = [&](int sb, PackIn (&in)[C::PACK_COLS]) {
+        const int ks = kslot(sb, rot, nsb);
+#pragma unroll
+        for (int k = 0; k < C::PACK_COLS; ++k) {
+            const int c = pw + k * C::NPACK, b = ct * C::TN + c;
+            const bool valid = c < C::TN && b < batch;
+            in[k] = pack_load(xq + ((size_t)(valid ? b : 0) * nsb + ks) * Q8_K_BYTES, valid);
+        }
+    };
+    load_sb(0, cur);
+    for (int sb = 0; sb < nsb; ++sb) {
+        if (sb + 1 < nsb) load_sb(sb + 1, nxt);
+        const int prev = sb - C::NBSB;  // the super-block that last used these slots
+        if (prev >= 0 && !wait_warp(B.sb_done + prev % NF, (uint32_t)(prev / NF) & 1u, abort)) return;
+        uint8_t *h0 = smem + C::OFF_B + b_slot<C>(sb, 0) * C::SLOT_B;
+        uint8_t *h1 = smem + C::OFF_B + b_slot<C>(sb, 1) * C::SLOT_B;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+            const int c = pw + k * C::NPACK;
+            if (c < C::TN) pack_store<C>(cur[k], c, h0, h1);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(B.b_tx + b_slot<C>(sb, 0));
+            mbar_arrive(B.b_tx + b_slot<C>(sb, 1));
+        }
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) cur[k] = nxt[k];
+    }
+}
+
 // Epilogue (warps 12-27): warp w reads tensor-memory lanes 32 (w % 4) .. + 31
 // (its 32 rows) and columns 32 h .. + 31, h = (w - 12) / 4, of S1 and of the
 // S2 written over the A buffer.  It frees both as soon as they are in
@@ -666,7 +765,10 @@ __device__ void role_epilogue(uint8_t *smem, const Bars &B, uint32_t tmem, int r
     }
 }
 
-template <int TN, bool SUMS>
+// WS: the activation operand comes packed in the workspace (bulk copies by
+// warps 0 and 3); otherwise the idle epilogue warps pack it from xq in the
+// CTA (TN <= 64).
+template <int TN, bool SUMS, bool WS>
 __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                                               const uint8_t *__restrict__ ws,
                                                               const uint8_t *__restrict__ xq,
@@ -675,6 +777,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
                                                               int nsb, int batch,
                                                               uint32_t *__restrict__ status) {
     using C = Cfg<TN>;
+    static_assert(WS || C::NPACK > 0, "packing in the CTA needs idle epilogue warps");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const Bars B = bars_at<C>(smem);
@@ -699,7 +802,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
         for (int i = 0; i < 2; ++i)
             for (int k = 0; k < C::EPI_ACTIVE; ++k) mbar_arrive(B.sb_full + i);
         for (int i = 0; i < C::NA; ++i) mbar_init(B.a_empty + i, C::EPI_ACTIVE);  // S2 over it read
-        for (int i = 0; i < C::NBS; ++i) mbar_init(B.b_tx + i, 1);
+        // a slot's operand half: one expect-tx arrival for its bulk copy, or
+        // one arrival per packing warp
+        for (int i = 0; i < C::NBS; ++i) mbar_init(B.b_tx + i, WS ? 1 : C::NPACK);
         for (int i = 0; i < C::NRAW; ++i) {
             mbar_init(B.raw_full + i, 1);
             mbar_init(B.raw_empty + i, BLD_THREADS);
@@ -725,16 +830,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) mma_q4k_kernel(const __grid_const
     pdl_wait();  // the packed activations come from the preceding kernel
 
     if (warp == 0 || warp == 3) {
-        role_producer_b<C>(smem, B, ws, nsb, ct, rot, warp == 3 ? 1 : 0, abort);
+        if (WS) role_producer_b<C>(smem, B, ws, nsb, ct, rot, warp == 3 ? 1 : 0, abort);
     } else if (warp == 2) {
         role_producer_w<C>(smem, B, &tmap_w, row0, nsb, rot, abort);
     } else if (warp == 1) {
         if (lane == 0) role_mma<C>(smem, B, tmem, nsb, abort);
         __syncwarp();
     } else if (warp >= BLD_WARP0 && warp < EPI_WARP0) {
-        role_builder<C>(smem, B, tmem, ws, ct, rot, nvalid, nsb, abort);
+        role_builder<C, WS>(smem, B, tmem, ws, xq, batch, ct, rot, nvalid, nsb, abort);
     } else if (warp >= EPI_WARP0) {
-        role_epilogue<C, SUMS>(smem, B, tmem, row0, rows, ct, nsb, rot, batch, y, sums, abort);
+        const int ew = warp - EPI_WARP0;  // epilogue warps with columns come first
+        if constexpr (!WS) {
+            if (ew >= C::EPI_ACTIVE)
+                role_pack<C>(smem, B, xq, batch, ct, rot, nsb, ew - C::EPI_ACTIVE, abort);
+            else
+                role_epilogue<C, SUMS>(smem, B, tmem, row0, rows, ct, nsb, rot, batch, y, sums, abort);
+        } else {
+            role_epilogue<C, SUMS>(smem, B, tmem, row0, rows, ct, nsb, rot, batch, y, sums, abort);
+        }
     }
     pdl_launch_dependents();
 
@@ -799,17 +912,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-template <int TN>
+template <int TN, bool WS>
 cudaError_t launch_tiles(const CUtensorMap &tmap, const void *xq, float *y, int32_t *sums, int64_t rows,
                          int nsb, int64_t batch, uint8_t *ws, const LaunchCtx &ctx) {
     using C = Cfg<TN>;
     const int ctiles = (int)((batch + TN - 1) / TN);
     const int rtiles = (int)((rows + TM - 1) / TM);
-    cudaError_t e = launch_pdl(pack_kernel<TN>, dim3(nsb, ctiles), dim3(256), 0, ctx.stream,
-                               static_cast<const uint8_t *>(xq), ws, nsb, (int)batch);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (WS) {
+        e = launch_pdl(pack_kernel<TN>, dim3(nsb, ctiles), dim3(256), 0, ctx.stream,
+                       static_cast<const uint8_t *>(xq), ws, nsb, (int)batch);
+        if (e != cudaSuccess) return e;
+    }
     const dim3 grid((unsigned)ctiles, (unsigned)rtiles);
-    auto k = sums ? mma_q4k_kernel<TN, true> : mma_q4k_kernel<TN, false>;
+    auto k = sums ? mma_q4k_kernel<TN, true, WS> : mma_q4k_kernel<TN, false, WS>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, grid, dim3(NTHREADS), C::SMEM_ALLOC, ctx.stream, tmap, (const uint8_t *)ws,
@@ -835,10 +951,15 @@ cudaError_t launch_mma_q4k(const void *W, const void *xq, float *y, int32_t *sum
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (!ws) {
+        // no workspace: tiles of at most 64 columns, packed in the CTA
+        if (batch <= 32) return launch_tiles<32, false>(tmap, xq, y, sums, rows, nsb, batch, nullptr, ctx);
+        return launch_tiles<64, false>(tmap, xq, y, sums, rows, nsb, batch, nullptr, ctx);
+    }
     switch (pick_tn(batch)) {
-    case 32: return launch_tiles<32>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
-    case 64: return launch_tiles<64>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
-    default: return launch_tiles<128>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
+    case 32: return launch_tiles<32, true>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
+    case 64: return launch_tiles<64, true>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
+    default: return launch_tiles<128, true>(tmap, xq, y, sums, rows, nsb, batch, ws, ctx);
     }
 }
 

@@ -243,11 +243,13 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *     tensor-core kernel needs a workspace.
  *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
  *     workspace; batches beyond 64 as 64-column chunks) from batch 4 on
- *     matrices of 8192 rows or more and from 16 on 2048 or more, the GEMV
- *     kernels otherwise.  Q4_K's tcgen05 kernel, faster beyond batch 32 on
- *     such matrices and from batch 16 on smaller ones (see gq_matmul_ws),
- *     needs a workspace for its repacked activations: call gq_matmul_ws, or
- *     gq_matmul_noalloc to use the library's static scratch.
+ *     matrices of 8192 rows or more and from 16 on 2048 or more, up to batch
+ *     191; from batch 192 on matrices of 8192 rows or more the tcgen05
+ *     kernel's variant that packs its activations in the CTA (64-column
+ *     tiles); the GEMV kernels otherwise.  The tcgen05 kernel with its
+ *     activations repacked once into a workspace is faster still (the
+ *     28672 x 8192 x 512 prefill: 0.32 ms against 1.10): call gq_matmul_ws,
+ *     or gq_matmul_noalloc to use the library's static scratch.
  *   Q5_K weights: the warp-level tensor-core kernel from batch 4 on matrices
  *     of 8192 rows or more and from 16 on 2048 or more (32-column chunks
  *     beyond 32), their GEMV kernels otherwise.
@@ -261,8 +263,9 @@ gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
 /* gq_matmul with an explicit kernel family (crossover studies, tests).
  * GQ_PATH_AUTO dispatches as gq_matmul.  GQ_PATH_MMA runs the tensor-core
  * kernel of Q4_0 / Q8_0 weights (GQ_ERR_SHAPE unless cols % 256 == 0); for
- * Q4_K weights it returns GQ_ERR_NULL (that kernel needs the workspace of
- * gq_matmul_ws), for Q5_K / Q6_K GQ_ERR_TYPE.  GQ_PATH_SKINNY runs the
+ * Q4_K weights the tcgen05 kernel's variant without a workspace (tiles of at
+ * most 64 columns whose idle epilogue warps pack the activation operand in
+ * the CTA; the same exact sums); for Q5_K / Q6_K GQ_ERR_TYPE.  GQ_PATH_SKINNY runs the
  * warp-level tensor-core kernels of Q4_K, Q5_K, Q4_0 and Q8_0 weights
  * (mma.sync m16n8k16 on exact integer operands: sc q - 512 for Q4_K and
  * sc q - 1024 for Q5_K, whose even and odd sub-blocks accumulate apart; one
@@ -307,8 +310,9 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * The tensor-core path computes the same y (within the tolerance above) and
  * the same exact integer super-block sums S1 and S2 as the GEMV kernels, for
  * every input (its fp32 accumulation only ever holds integers below 2^24).
- * Errors as gq_matmul_path, plus GQ_ERR_NULL (MMA path without workspace),
- * GQ_ERR_SHAPE (workspace too small), GQ_ERR_ALIGN.
+ * Errors as gq_matmul_path, plus GQ_ERR_SHAPE (workspace too small),
+ * GQ_ERR_ALIGN.  A NULL workspace with GQ_PATH_MMA runs the variant without
+ * one, as gq_matmul_path does.
  */
 gq_status gq_matmul_ws(gq_type wtype, const void *W, const void *xq, float *y,
                        int64_t rows, int64_t cols, int64_t batch, gq_path path,

@@ -76,8 +76,6 @@ def test_mma_auto_dispatch_and_workspace_rules():
     assert need == 1 * 2 * 35328  # one 64-column tile
     assert gq.gq_matmul_workspace_bytes(0, rows, cols, batch) == 0
     y = torch.empty(batch, rows, device="cuda")
-    with pytest.raises(gq.GQError):  # MMA without a workspace
-        gq.gq_matmul_path(Q4_K, dev(Wq), dev(Xq), y, rows, cols, batch, gq.PATH_MMA)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     with pytest.raises(gq.GQError):  # workspace too small
         gq.gq_matmul_ws(Q4_K, dev(Wq), dev(Xq), y, rows, cols, batch, gq.PATH_MMA, 0, ws, need - 16)
@@ -177,14 +175,16 @@ def test_mma_full_size(rows, cols, batch):
     (14336, 3, True, "gemv"), (14336, 4, True, "skinny"), (14336, 9, True, "skinny"), (14336, 32, True, "skinny"),
     (14336, 33, True, "mma"), (14336, 33, False, "skinny"), (14336, 65, False, "skinny"), (14336, 65, True, "mma"),
     (4096, 9, True, "gemv"), (4096, 15, False, "gemv"), (4096, 16, True, "skinny"), (4096, 16, False, "skinny"),
-    (4096, 33, True, "mma"), (4096, 40, False, "skinny"), (1024, 16, True, "mma"), (1024, 16, False, "gemv")])
+    (4096, 33, True, "mma"), (4096, 40, False, "skinny"), (1024, 16, True, "mma"), (1024, 16, False, "gemv"),
+    (8192, 191, False, "skinny"), (8192, 192, False, "mma")])
 def test_auto_dispatch_rule(rows, batch, ws, want):
     """GQ_PATH_AUTO for Q4_K: the warp-level tensor-core kernel from batch 4
     on matrices of 8192 rows or more and from 16 on 2048 or more, up to 32
-    when a workspace lets the tcgen05 kernel take larger batches (at any
-    such batch without one, in 64-column chunks); the tcgen05 kernel, when a
-    workspace is given, from batch 9 on 14336 rows and 16 otherwise; the GEMV
-    below.  Every family is deterministic, so the AUTO result equals the
+    when a workspace lets the tcgen05 kernel take larger batches (without
+    one, in 64-column chunks up to batch 191, then, on 8192 rows or more, the
+    tcgen05 variant that packs its activations in the CTA); the tcgen05
+    kernel, when a workspace is given, from batch 9 on 14336 rows and 16
+    otherwise; the GEMV below.  Every family is deterministic, so the AUTO result equals the
     chosen family's bit for bit."""
     cols = 1024
     g = inputs.rng(rows + batch)
@@ -197,3 +197,74 @@ def test_auto_dispatch_rule(rows, batch, ws, want):
     path = {"mma": gq.PATH_MMA, "gemv": gq.PATH_GEMV, "skinny": gq.PATH_SKINNY}[want]
     y_want = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, path))
     assert y_auto.tobytes() == y_want.tobytes()
+
+
+# ----------------------------------- the tcgen05 kernel without a workspace
+
+NOWS_SHAPES = [(128, 256, 1), (200, 768, 40), (77, 512, 32), (300, 1280, 33), (130, 2048, 64),
+               (257, 1024, 65), (384, 4096, 130), (96, 3072, 200)]
+
+
+@pytest.mark.parametrize("rows,cols,batch", NOWS_SHAPES)
+def test_mma_without_workspace(rows, cols, batch):
+    """GQ_PATH_MMA with no workspace: tiles of 32 / 64 columns whose idle
+    epilogue warps pack the activations in the CTA.  Sums equal the oracle's;
+    y equals the workspace variant's bit for bit (same per-output arithmetic
+    in the same super-block order, whatever the tile width) and the oracle's
+    within the bar."""
+    g = inputs.rng(rows * 3 + cols + batch)
+    W = inputs.outlier_weights(g, rows, cols, frac=0.001)
+    X = inputs.normal(g, (batch, cols))
+    Wq, Xq = orc.quantize(Q4_K, W), orc.quantize(Q8_K, X)
+    Wd, Xd = dev(Wq), dev(Xq)
+    s = torch.empty(batch, rows, cols // 256, 2, dtype=torch.int32, device="cuda")
+    gq.gq_block_sums(Q4_K, Wd, Xd, s, rows, cols, batch, gq.PATH_MMA)
+    np.testing.assert_array_equal(host(s), orc.block_sums(Q4_K, Wq, Xq, rows, cols, batch))
+    y = torch.empty(batch, rows, device="cuda")
+    gq.gq_matmul_path(Q4_K, Wd, Xd, y, rows, cols, batch, gq.PATH_MMA)
+    y_ws = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_MMA))
+    assert host(y).tobytes() == y_ws.tobytes()
+    y_ref, T = orc.matmul_ref(Q4_K, Wq, Xq, rows, cols, batch)
+    assert_close(host(y), y_ref, T)
+
+
+@pytest.mark.parametrize("batch", [5, 40, 100])
+def test_mma_without_workspace_beyond_fp32_integers(batch):
+    """The odd S1 above 2^24 case of the workspace variant, packed in the
+    CTA (raw -128 activation codes included)."""
+    rows, cols = 131, 512
+    W = inputs.outlier_weights(inputs.rng(7), rows, cols, frac=0.001)
+    W[0] = 1.0
+    W[0, 5] = 0.93
+    W[2] = 1.0
+    W[2, 1::2] = 0.93
+    X = inputs.normal(inputs.rng(8), (batch, cols))
+    X[0] = 1.0
+    X[batch - 1] = 1.0
+    Wq, Xq = orc.quantize(Q4_K, W), orc.quantize(Q8_K, X)
+    blk = Xq.reshape(batch, cols // 256, 276)
+    blk[1, :, 4:260] = 0x80
+    blk[1, :, 260:276] = np.frombuffer(np.full(8, -128 * 32, np.int16).tobytes(), np.uint8)
+    s_ref = orc.block_sums(Q4_K, Wq, Xq, rows, cols, batch)
+    assert np.sum((np.abs(s_ref[..., 0]) > 2**24) & (s_ref[..., 0] % 2 != 0)) >= 2
+    s = torch.empty(batch, rows, cols // 256, 2, dtype=torch.int32, device="cuda")
+    gq.gq_block_sums(Q4_K, dev(Wq), dev(Xq), s, rows, cols, batch, gq.PATH_MMA)
+    np.testing.assert_array_equal(host(s), s_ref)
+
+
+def test_mma_without_workspace_full_size():
+    """The prefill shape through gq_matmul_path(GQ_PATH_MMA) with no
+    workspace; the oracle recomputes sampled rows."""
+    rows, cols, batch = 28672, 8192, 512
+    W, X = inputs.gemm_q4_k(0, rows, cols, batch)
+    Wd = gq.quantize(Q4_K, dev(W))
+    Xd = gq.quantize(Q8_K, dev(X))
+    y = torch.empty(batch, rows, device="cuda")
+    gq.gq_matmul_path(Q4_K, Wd, Xd, y, rows, cols, batch, gq.PATH_MMA)
+    yh = host(y)
+    idx = sampled_rows(rows, 24, 99)
+    Wq_s = orc.quantize(Q4_K, W[idx])
+    Xq = orc.quantize(Q8_K, X)
+    y_ref, T = orc.matmul_ref(Q4_K, Wq_s, Xq, len(idx), cols, batch, nthreads=orc.max_threads())
+    assert_close(yh[:, idx], y_ref, T)
+
