@@ -154,14 +154,13 @@ bool tc_auto(int64_t rows, int64_t batch) {
 // 25.3..26.2, 39 us at 64 against its 30 and the GEMV's 173.  On 4096 x 4096
 // (43 CTAs): 14.2 / 20.7 us at batch 16 / 32 against the GEMV's 19.6 / 38.1
 // and the tcgen05 kernel's 24.4 / 24.9 (the GEMV wins at 8: 10.2 vs 11.3).
-// So: from batch 4 on matrices of 8192 rows or more, from 16 on 2048 or more,
-// up to 32 when a workspace lets the tcgen05 kernel take the larger batches,
-// at every such batch otherwise.  Not taken when GQ_TC_MIN_BATCH sets a plain
-// threshold.
-bool skinny_auto(int64_t rows, int64_t batch, bool tc_ready) {
+// So: from batch 4 on matrices of 8192 rows or more and from 16 on 2048 or
+// more, up to 32; larger batches take the tcgen05 kernel (with or without a
+// workspace, tc_auto / tc_nows_auto).  Not taken when GQ_TC_MIN_BATCH sets a
+// plain threshold.
+bool skinny_auto(int64_t rows, int64_t batch) {
     if (tc_min_batch_env() || rows < 2048) return false;
-    if (batch < (rows >= 8192 ? 4 : 16)) return false;
-    return batch <= 32 || !tc_ready;
+    return batch >= (rows >= 8192 ? 4 : 16) && batch <= 32;
 }
 
 // The warp-level kernel for Q4_0 / Q8_0 weights (gq_skinny_q0.cu).
@@ -181,11 +180,13 @@ bool skinny_auto_q0(int64_t rows, int64_t batch) {
 
 // Q4_K without a workspace: the tcgen05 kernel's variant that packs the
 // activations in the CTA (tiles of 64 columns) against the warp-level
-// kernel's 64-column chunks.  Measured on 14336 x 4096: 94.9 vs 78.2 us at
-// batch 128, 142.5 vs 156.7 at 256; the 28672 x 8192 x 512 prefill 1.10 vs
-// 1.29 ms.  So: from batch 192 on matrices of 8192 rows or more.
+// kernel.  Measured on 14336 x 4096: 33.5 vs 37.2 us at batch 48, 34.7 vs
+// 39.5 at 64, 66.5 vs 78.2 at 128 (two chunks), 100.3 vs 156.6 at 256; the
+// 28672 x 8192 x 512 prefill 0.76 vs 1.29 ms; at batch 32 (32-column
+// tiles) 26.1 vs 22.1.  So: beyond batch 32 on matrices of 2048 rows or
+// more, as with a workspace.
 bool tc_nows_auto(int64_t rows, int64_t batch) {
-    return !tc_min_batch_env() && rows >= 8192 && batch >= 192;
+    return !tc_min_batch_env() && rows >= 2048 && batch > 32;
 }
 
 // The warp-level kernel for Q5_K weights (gq_skinny.cu; Q5_K has no
@@ -260,11 +261,10 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
             const bool tc_ready = mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
                                   ws_bytes >= mma_workspace_bytes(rows, cols, batch);
             // without a workspace, large batches take the tcgen05 kernel that
-            // packs its activations itself; otherwise beyond batch 64 the
-            // warp-level kernel runs over 64-column chunks
+            // packs its activations itself
             const bool tc_nows = !tc_ready && mma_supported(rows, cols, batch) && tc_nows_auto(rows, batch);
             use_skinny = !tc_nows && skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) &&
-                         skinny_auto(rows, batch, tc_ready);
+                         skinny_auto(rows, batch);
             use_mma = tc_nows || (!use_skinny && tc_ready && tc_auto(rows, batch));
         } else if (wtype == GQ_Q5_K) {
             use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 32)) && skinny_auto_q5k(rows, batch);

@@ -68,6 +68,7 @@
 
 #include "gq_common.cuh"
 #include "gq_internal.h"
+#include "gq_mma_sync.cuh"
 #include "gq_tc.cuh"
 
 namespace gq {
@@ -263,20 +264,13 @@ __device__ __forceinline__ PackIn pack_load(const uint8_t *__restrict__ src, boo
 }
 
 // Column c of one unit (a warp, lane l): the operand stages go to st01
-// (stages 0, 1) and st23 (stages 2, 3, then the min-term tile); returns the
-// column's code sum in every lane.
-template <class C>
+// (stages 0, 1) and st23 (stages 2, 3, then the min-term tile); with SUM,
+// returns the column's code sum in every lane.
+template <class C, bool SUM = true>
 __device__ __forceinline__ int pack_store(const PackIn &in, int c, uint8_t *st01, uint8_t *st23) {
     const int lane = threadIdx.x & 31;
-    const uint32_t w0 = in.w0, w1 = in.w1;
-    float a[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        a[i] = (float)(int8_t)(w0 >> (8 * i));
-        a[4 + i] = (float)(int8_t)(w1 >> (8 * i));
-    }
-    const uint4 chunk = make_uint4(pack_h2(a[0], a[4]), pack_h2(a[1], a[5]), pack_h2(a[2], a[6]),
-                                   pack_h2(a[3], a[7]));
+    // the codes as exact fp16 pairs (a0, a4), (a1, a5), (a2, a6), (a3, a7)
+    const uint4 chunk = ms::i8x8_to_f16(in.w0, in.w1);
     const int stage = lane >> 3;
     uint8_t *st = stage < 2 ? st01 + stage * C::OP_B : st23 + (stage - 2) * C::OP_B;
     *reinterpret_cast<uint4 *>(st + sw128_off(c, lane & 7)) = chunk;
@@ -288,6 +282,7 @@ __device__ __forceinline__ int pack_store(const PackIn &in, int c, uint8_t *st01
         *reinterpret_cast<__half *>(mb + plain_off(c, 0) + 2 * lane) = __int2half_rn(tlo);
         *reinterpret_cast<__half *>(mb + plain_off(c, 1) + 2 * lane) = __int2half_rn(thi);
     }
+    if constexpr (!SUM) return 0;
     // code sum of the column's super-block: lanes 0..7 hold t_0..t_7, the
     // other lanes zero
     int asum = t;
@@ -669,7 +664,7 @@ __device__ void role_pack(uint8_t *smem, const Bars &B, const uint8_t *__restric
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) {
             const int c = pw + k * C::NPACK;
-            if (c < C::TN) pack_store<C>(cur[k], c, h0, h1);
+            if (c < C::TN) pack_store<C, false>(cur[k], c, h0, h1);  // the builders add the sums
         }
         fence_async_smem();
         __syncwarp();

@@ -244,12 +244,12 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
  *     workspace; batches beyond 64 as 64-column chunks) from batch 4 on
  *     matrices of 8192 rows or more and from 16 on 2048 or more, up to batch
- *     191; from batch 192 on matrices of 8192 rows or more the tcgen05
- *     kernel's variant that packs its activations in the CTA (64-column
- *     tiles); the GEMV kernels otherwise.  The tcgen05 kernel with its
- *     activations repacked once into a workspace is faster still (the
- *     28672 x 8192 x 512 prefill: 0.32 ms against 1.10): call gq_matmul_ws,
- *     or gq_matmul_noalloc to use the library's static scratch.
+ *     32; beyond 32 on such matrices the tcgen05 kernel's variant that packs
+ *     its activations in the CTA (64-column tiles); the GEMV kernels
+ *     otherwise.  The tcgen05 kernel with its activations repacked once into
+ *     a workspace is faster still (the 28672 x 8192 x 512 prefill: 0.32 ms
+ *     against 0.76): call gq_matmul_ws, or gq_matmul_noalloc to use the
+ *     library's static scratch.
  *   Q5_K weights: the warp-level tensor-core kernel from batch 4 on matrices
  *     of 8192 rows or more and from 16 on 2048 or more (32-column chunks
  *     beyond 32), their GEMV kernels otherwise.
@@ -303,8 +303,8 @@ size_t gq_matmul_workspace_bytes(gq_type wtype, int64_t rows, int64_t cols, int6
  * 4..32 on matrices of 8192 rows or more and 16..32 on 2048 or more; else
  * the tcgen05 tensor-core kernel when batch >= gq_tc_min_batch(), or batch
  * >= 9 on matrices of 14336 rows or more (the measured crossovers), and the
- * workspace suffices; else the warp-level kernel (in 64-column chunks
- * beyond batch 64) where it applies; else the GEMV kernels.  Q4_0 / Q8_0
+ * workspace suffices; else, beyond batch 32 on matrices of 2048 rows or
+ * more, the tcgen05 variant that needs no workspace; else the GEMV kernels.  Q4_0 / Q8_0
  * weights ignore the workspace and dispatch as in gq_matmul.  With
  * GQ_TC_MIN_BATCH set, batch >= that value alone decides.
  * The tensor-core path computes the same y (within the tolerance above) and

@@ -173,17 +173,16 @@ def test_mma_full_size(rows, cols, batch):
 @pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
 @pytest.mark.parametrize("rows,batch,ws,want", [
     (14336, 3, True, "gemv"), (14336, 4, True, "skinny"), (14336, 9, True, "skinny"), (14336, 32, True, "skinny"),
-    (14336, 33, True, "mma"), (14336, 33, False, "skinny"), (14336, 65, False, "skinny"), (14336, 65, True, "mma"),
+    (14336, 33, True, "mma"), (14336, 33, False, "mma"), (14336, 65, False, "mma"), (14336, 65, True, "mma"),
     (4096, 9, True, "gemv"), (4096, 15, False, "gemv"), (4096, 16, True, "skinny"), (4096, 16, False, "skinny"),
-    (4096, 33, True, "mma"), (4096, 40, False, "skinny"), (1024, 16, True, "mma"), (1024, 16, False, "gemv"),
-    (8192, 191, False, "skinny"), (8192, 192, False, "mma")])
+    (4096, 33, True, "mma"), (4096, 40, False, "mma"), (1024, 16, True, "mma"), (1024, 16, False, "gemv"),
+    (8192, 32, False, "skinny"), (8192, 33, False, "mma")])
 def test_auto_dispatch_rule(rows, batch, ws, want):
     """GQ_PATH_AUTO for Q4_K: the warp-level tensor-core kernel from batch 4
-    on matrices of 8192 rows or more and from 16 on 2048 or more, up to 32
-    when a workspace lets the tcgen05 kernel take larger batches (without
-    one, in 64-column chunks up to batch 191, then, on 8192 rows or more, the
-    tcgen05 variant that packs its activations in the CTA); the tcgen05
-    kernel, when a workspace is given, from batch 9 on 14336 rows and 16
+    on matrices of 8192 rows or more and from 16 on 2048 or more, up to 32;
+    beyond, the tcgen05 kernel (with a workspace, or the variant that packs
+    its activations in the CTA without one); with a workspace the tcgen05
+    kernel also below that band, from batch 9 on 14336 rows and 16
     otherwise; the GEMV below.  Every family is deterministic, so the AUTO result equals the
     chosen family's bit for bit."""
     cols = 1024
