@@ -208,6 +208,30 @@ bool tc_auto_q0(int64_t rows, int64_t batch) {
     return batch >= 16;
 }
 
+// The family GQ_PATH_AUTO takes for a product of valid, non-empty sizes with
+// quantized activations; tc_ready: a workspace large enough (and aligned)
+// for the Q4_K tcgen05 kernel is passed.  Host-only arithmetic on the sizes.
+gq_path auto_family(gq_type wtype, int64_t rows, int64_t cols, int64_t batch, bool tc_ready) {
+    const bool q0 = wtype == GQ_Q4_0 || wtype == GQ_Q8_0;
+    if (q0) {
+        if (skinny_q0_supported(rows, cols, std::min<int64_t>(batch, 64)) && skinny_auto_q0(rows, batch))
+            return GQ_PATH_SKINNY;
+        if (tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch)) return GQ_PATH_MMA;
+    } else if (wtype == GQ_Q4_K) {
+        // without a workspace, large batches take the tcgen05 kernel that
+        // packs its activations itself
+        const bool tc_nows = !tc_ready && mma_supported(rows, cols, batch) && tc_nows_auto(rows, batch);
+        if (tc_nows) return GQ_PATH_MMA;
+        if (skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) && skinny_auto(rows, batch))
+            return GQ_PATH_SKINNY;
+        if (tc_ready && tc_auto(rows, batch)) return GQ_PATH_MMA;
+    } else if (wtype == GQ_Q5_K) {
+        if (skinny_supported(rows, cols, std::min<int64_t>(batch, 32)) && skinny_auto_q5k(rows, batch))
+            return GQ_PATH_SKINNY;
+    }
+    return GQ_PATH_GEMV;
+}
+
 // One product call.  act is xq (quantized blocks) or, with fused_f32, fp32
 // activations; exactly one of y / sums is non-null.
 gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, int32_t *sums,
@@ -251,25 +275,14 @@ gq_status run_matmul(gq_type wtype, const void *W, const void *act, float *y, in
             return GQ_ERR_SHAPE;
     }
     if (rows == 0 || cols == 0 || batch == 0) return GQ_OK;
-    bool use_mma = path == GQ_PATH_MMA;
-    bool use_skinny = path == GQ_PATH_SKINNY;
     if (path == GQ_PATH_AUTO && !fused_f32) {
-        if (q0) {
-            use_skinny = skinny_q0_supported(rows, cols, std::min<int64_t>(batch, 64)) && skinny_auto_q0(rows, batch);
-            use_mma = !use_skinny && tc_auto_q0(rows, batch) && mma_q0_supported(rows, cols, batch);
-        } else if (wtype == GQ_Q4_K) {
-            const bool tc_ready = mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
-                                  ws_bytes >= mma_workspace_bytes(rows, cols, batch);
-            // without a workspace, large batches take the tcgen05 kernel that
-            // packs its activations itself
-            const bool tc_nows = !tc_ready && mma_supported(rows, cols, batch) && tc_nows_auto(rows, batch);
-            use_skinny = !tc_nows && skinny_supported(rows, cols, std::min<int64_t>(batch, 64)) &&
-                         skinny_auto(rows, batch);
-            use_mma = tc_nows || (!use_skinny && tc_ready && tc_auto(rows, batch));
-        } else if (wtype == GQ_Q5_K) {
-            use_skinny = skinny_supported(rows, cols, std::min<int64_t>(batch, 32)) && skinny_auto_q5k(rows, batch);
-        }
+        const bool tc_ready = wtype == GQ_Q4_K && mma_supported(rows, cols, batch) && ws && aligned(ws, 16) &&
+                              ws_bytes >= mma_workspace_bytes(rows, cols, batch);
+        path = auto_family(wtype, rows, cols, batch, tc_ready);
+        if (path == GQ_PATH_MMA && wtype == GQ_Q4_K && !tc_ready) ws = nullptr;  // the variant without one
     }
+    const bool use_mma = path == GQ_PATH_MMA;
+    const bool use_skinny = path == GQ_PATH_SKINNY;
     if (!use_mma && !use_skinny && !kstream && !gemv_fits(wtype, cols)) return GQ_ERR_SHAPE;
     LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
@@ -452,6 +465,21 @@ gq_status gq_matmul_noalloc(gq_type wtype, const void *W, const void *xq, float 
 }
 
 int64_t gq_tc_min_batch(void) { return tc_min_batch_value(); }
+
+gq_status gq_auto_path(gq_type wtype, int64_t rows, int64_t cols, int64_t batch, int with_workspace,
+                       gq_path *path) {
+    if (!path) return GQ_ERR_NULL;
+    if (wtype != GQ_Q4_0 && wtype != GQ_Q8_0 && wtype != GQ_Q4_K && wtype != GQ_Q5_K && wtype != GQ_Q6_K)
+        return GQ_ERR_TYPE;
+    if (rows < 0 || cols < 0 || batch < 0 || cols % block_elems(wtype) != 0) return GQ_ERR_SHAPE;
+    if (rows == 0 || cols == 0 || batch == 0) {
+        *path = GQ_PATH_GEMV;
+        return GQ_OK;
+    }
+    const bool tc_ready = with_workspace != 0 && wtype == GQ_Q4_K && mma_supported(rows, cols, batch);
+    *path = auto_family(wtype, rows, cols, batch, tc_ready);
+    return GQ_OK;
+}
 
 gq_status gq_debug_kv_timeout(int on) {
     LaunchCtx ctx;

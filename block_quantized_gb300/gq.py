@@ -57,6 +57,7 @@ SIGNATURES = {
     "gq_kv_scores": ([_i32, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp], _i32),
     "gq_debug_kv_timeout": ([_i32], _i32),
     "gq_tc_min_batch": ([], _i64),
+    "gq_auto_path": ([_i32, _i64, _i64, _i64, _i32, ctypes.POINTER(ctypes.c_int32)], _i32),
     "gq_device_status": ([_u32p, _i32], _i32),
 }
 
@@ -232,6 +233,15 @@ def gq_debug_kv_timeout(on: bool) -> None:
 
 def gq_tc_min_batch() -> int:
     return int(load().gq_tc_min_batch())
+
+
+def gq_auto_path(wtype: int, rows: int, cols: int, batch: int, with_workspace: bool = False) -> int:
+    """The family (PATH_GEMV, PATH_MMA or PATH_SKINNY) GQ_PATH_AUTO takes;
+    host only."""
+    out = ctypes.c_int32(-1)
+    _check("gq_auto_path", load().gq_auto_path(wtype, rows, cols, batch, 1 if with_workspace else 0,
+                                                ctypes.byref(out)))
+    return int(out.value)
 
 
 def gq_device_status(reset: bool = True) -> int:

@@ -447,6 +447,21 @@ gq_status gq_debug_kv_timeout(int on);
 int64_t gq_tc_min_batch(void);
 
 /*
+ * The kernel family GQ_PATH_AUTO takes for a product (GQ_PATH_GEMV,
+ * GQ_PATH_MMA or GQ_PATH_SKINNY) on quantized activations, as gq_matmul
+ * (with_workspace == 0) or gq_matmul_ws with a sufficient workspace
+ * (with_workspace != 0) would choose it: the rules of the Dispatch paragraph
+ * of gq_matmul and gq_matmul_ws, including GQ_TC_MIN_BATCH.  Host-only
+ * arithmetic on the sizes: no device call, no CUDA device needed.  Empty
+ * products report GQ_PATH_GEMV.
+ *   path : host, written on success.
+ * Errors: GQ_ERR_NULL (path), GQ_ERR_TYPE (not a weight type), GQ_ERR_SHAPE
+ * (negative size, cols not a block multiple).
+ */
+gq_status gq_auto_path(gq_type wtype, int64_t rows, int64_t cols, int64_t batch, int with_workspace,
+                       gq_path *path);
+
+/*
  * Reads (and with reset != 0 clears) the device status word of the current
  * device.  Synchronizes the device.  Returns GQ_OK when no bounded wait ran
  * out since the last reset, GQ_ERR_TIMEOUT otherwise (the raw word, a bit

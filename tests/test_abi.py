@@ -211,3 +211,48 @@ def test_kv_validation(lib):
     assert sc(0, A16 + 4, A16, A16, 4, 128, 64, 10, None) == ALIGN
     assert sc(0, A16, A16, A16 + 2, 4, 128, 64, 10, None) == ALIGN
     assert sc(0, A16, A16, A16, 4, 128, 64, 0, None) == OK       # no positions
+
+
+# The dispatch table of GQ_PATH_AUTO, pinned on the host (gq_auto_path does
+# no device call): weight type, rows, batch, workspace given -> family.  The
+# thresholds are the crossovers measured on 14336 x 4096 and 4096 x 4096;
+# the GPU tests check that gq_matmul's results equal the named family's.
+GEMV, MMA, SKINNY = 1, 2, 3
+AUTO_TABLE = [
+    # Q4_K: warp-level kernel 4..32 (>= 8192 rows) or 16..32 (>= 2048 rows),
+    # tcgen05 beyond (with or without a workspace), with a workspace also
+    # from 9 (>= 14336 rows) or 16 on smaller matrices, GEMV otherwise
+    (2, 14336, 3, False, GEMV), (2, 14336, 4, False, SKINNY), (2, 14336, 32, True, SKINNY),
+    (2, 14336, 33, False, MMA), (2, 14336, 33, True, MMA), (2, 14336, 512, False, MMA),
+    (2, 14336, 9, True, SKINNY), (2, 4096, 15, False, GEMV), (2, 4096, 16, False, SKINNY),
+    (2, 4096, 33, False, MMA), (2, 4096, 9, True, GEMV), (2, 1024, 16, True, MMA), (2, 1024, 16, False, GEMV),
+    (2, 1024, 64, False, GEMV),
+    # Q4_0 / Q8_0: warp-level kernel 2..64 (>= 8192 rows) or 8..64 (>= 2048),
+    # tcgen05 from 16 otherwise; the workspace changes nothing
+    (0, 8192, 1, False, GEMV), (0, 8192, 2, False, SKINNY), (1, 14336, 64, True, SKINNY),
+    (1, 14336, 65, False, MMA), (0, 4096, 7, False, GEMV), (0, 4096, 8, False, SKINNY),
+    (1, 1024, 15, False, GEMV), (1, 1024, 16, False, MMA),
+    # Q5_K: warp-level kernel from 4 (>= 8192 rows) or 16 (>= 2048), GEMV
+    # otherwise; Q6_K: always the GEMV
+    (5, 14336, 3, False, GEMV), (5, 14336, 4, False, SKINNY), (5, 8192, 200, True, SKINNY),
+    (5, 4096, 15, False, GEMV), (5, 4096, 16, False, SKINNY), (5, 1024, 64, False, GEMV),
+    (4, 14336, 64, True, GEMV),
+]
+
+
+@pytest.mark.skipif(bool(os.environ.get("GQ_TC_MIN_BATCH")), reason="threshold overridden")
+@pytest.mark.parametrize("wtype,rows,batch,ws,want", AUTO_TABLE)
+def test_auto_path_rules(lib, wtype, rows, batch, ws, want):
+    assert gq.gq_auto_path(wtype, rows, 4096, batch, ws) == want
+
+
+def test_auto_path_validation(lib):
+    out = ctypes.c_int32(-1)
+    f = lib.gq_auto_path
+    assert f(3, 8, 256, 1, 0, ctypes.byref(out)) == TYPE       # Q8_K is not a weight type
+    assert f(2, 8, 100, 1, 0, ctypes.byref(out)) == SHAPE      # not a block multiple
+    assert f(2, -1, 256, 1, 0, ctypes.byref(out)) == SHAPE
+    assert f(2, 8, 256, 1, 0, None) == NULL
+    assert f(2, 0, 256, 1, 0, ctypes.byref(out)) == OK and out.value == GEMV
+    # cols % 256 != 0 keeps Q4_0 on the GEMV at any batch
+    assert f(0, 14336, 288, 32, 0, ctypes.byref(out)) == OK and out.value == GEMV
