@@ -194,6 +194,7 @@ def test_auto_dispatch_rule(rows, batch, ws, want):
     else:
         y_auto = host(gq.matmul(Q4_K, Wd, Xd, rows, cols, batch, gq.PATH_AUTO))
     path = {"mma": gq.PATH_MMA, "gemv": gq.PATH_GEMV, "skinny": gq.PATH_SKINNY}[want]
+    assert gq.gq_auto_path(Q4_K, rows, cols, batch, ws) == path  # the host-side query agrees
     y_want = host(gq.matmul_ws(Q4_K, Wd, Xd, rows, cols, batch, path))
     assert y_auto.tobytes() == y_want.tobytes()
 

@@ -376,4 +376,5 @@ def test_auto_dispatch(rows, batch, want):
     Xd = gq.quantize(Q8_K, dev(inputs.normal(g, (batch, cols))))
     y = host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch))
     path = gq.PATH_SKINNY if want == "skinny" else gq.PATH_GEMV
+    assert gq.gq_auto_path(Q5_K, rows, cols, batch) == path  # the host-side query agrees
     assert y.tobytes() == host(gq.matmul(Q5_K, Wd, Xd, rows, cols, batch, path)).tobytes()

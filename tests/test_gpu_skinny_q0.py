@@ -184,6 +184,7 @@ def test_skinny_q0_auto_dispatch(wtype, rows, batch, want):
     y = torch.empty(batch, rows, device="cuda")
     gq.gq_matmul(wtype, Wd, Xd, y, rows, cols, batch)
     path = {"gemv": gq.PATH_GEMV, "skinny": gq.PATH_SKINNY, "mma": gq.PATH_MMA}[want]
+    assert gq.gq_auto_path(wtype, rows, cols, batch) == path  # the host-side query agrees
     assert host(y).tobytes() == host(gq.matmul(wtype, Wd, Xd, rows, cols, batch, path)).tobytes()
 
 
