@@ -241,10 +241,9 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *     gq_tc_min_batch() otherwise (16 unless GQ_TC_MIN_BATCH is set, which
  *     also turns the warp-level choice off); the GEMV kernels below.  Neither
  *     tensor-core kernel needs a workspace.
- *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY, no
- *     workspace; batches beyond 64 as 64-column chunks) from batch 4 on
- *     matrices of 8192 rows or more and from 16 on 2048 or more, up to batch
- *     32; beyond 32 on such matrices the tcgen05 kernel's variant that packs
+ *   Q4_K weights: the warp-level tensor-core kernel (GQ_PATH_SKINNY) from
+ *     batch 4 on matrices of 8192 rows or more and from 16 on 2048 or more,
+ *     up to batch 32; beyond 32 on such matrices the tcgen05 kernel's variant that packs
  *     its activations in the CTA (64-column tiles); the GEMV kernels
  *     otherwise.  The tcgen05 kernel with its activations repacked once into
  *     a workspace is faster still (the 28672 x 8192 x 512 prefill: 0.32 ms
@@ -255,7 +254,7 @@ gq_status gq_dequantize_rows_async(gq_type type, const void *src, float *dst, in
  *     beyond 32), their GEMV kernels otherwise.
  *   Q6_K weights: their GEMV kernels.
  * The GEMV kernels take any batch, in chunks of up to eight vectors, one
- * pass over W per chunk.
+ * pass over W per chunk.  gq_auto_path reports the family chosen for a shape.
  */
 gq_status gq_matmul(gq_type wtype, const void *W, const void *xq, float *y,
                     int64_t rows, int64_t cols, int64_t batch, gq_stream_t stream);
