@@ -256,3 +256,12 @@ def test_auto_path_validation(lib):
     assert f(2, 0, 256, 1, 0, ctypes.byref(out)) == OK and out.value == GEMV
     # cols % 256 != 0 keeps Q4_0 on the GEMV at any batch
     assert f(0, 14336, 288, 32, 0, ctypes.byref(out)) == OK and out.value == GEMV
+
+
+def test_build_lists_every_source():
+    """Every kernel source and header under csrc is compiled or tracked by the
+    build (a header missing from the list would leave a stale library after
+    an edit)."""
+    files = set(os.listdir(gqbuild.CSRC))
+    assert {f for f in files if f.endswith(".cu")} == set(gqbuild.SOURCES)
+    assert {f for f in files if f.endswith((".cuh", ".h"))} == set(gqbuild.HEADERS)
